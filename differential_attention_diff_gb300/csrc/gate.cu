@@ -1,0 +1,127 @@
+// gate.cu — V2 gate: gate[t, p] = sigmoid(sum_k x[t, k] * w_lambda[k, p]).
+//
+// "Differential Transformer V2" (pogovet.com), §1 and §4: the coefficient of
+// the second (odd) head is projected per token and per head from the input X
+// and passed through a sigmoid.  The projection is a skinny GEMM
+// [T, d_model] x [d_model, h] with h <= 64, so the kernel is bound by reading
+// X once from HBM: 64 tokens per CTA, X and W chunks of 64 features staged by
+// a 2-deep cp.async ring, the warp MMA for the products (each warp owns 16
+// tokens and all h outputs), and the sigmoid fused into the store.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace da {
+namespace {
+
+constexpr int kTok = 64;    // tokens per CTA
+constexpr int kChunk = 64;  // features per stage
+constexpr int kMaxH = 64;
+constexpr int kStages = 2;
+constexpr int kRow = 128;   // bytes per staged row (64 bf16)
+constexpr int kXBytes = kTok * kRow;
+constexpr int kWBytes = kChunk * kRow;
+constexpr int kStageBytes = kXBytes + kWBytes;
+
+__device__ __forceinline__ uint32_t off8(int r, int c) {
+  return static_cast<uint32_t>(r * kRow + ((c ^ (r & 7)) << 4));
+}
+
+__global__ void __launch_bounds__(128)
+gate_kernel(GateArgs a) {
+  __shared__ __align__(128) uint8_t smem[kStages * kStageBytes];
+  const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
+  const int t0 = blockIdx.x * kTok;
+  const int nchunks = a.d_model / kChunk;
+  const int hc = a.h / 8;  // 16-byte chunks per W row
+  const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.x);
+  const __nv_bfloat16* w = static_cast<const __nv_bfloat16*>(a.w);
+  const uint32_t sb = smem_u32(smem);
+
+  auto issue = [&](int ch) {
+    if (ch < nchunks) {
+      const uint32_t xs = sb + (ch % kStages) * kStageBytes;
+      const uint32_t ws = xs + kXBytes;
+      const int f0 = ch * kChunk;
+#pragma unroll
+      for (int i = 0; i < (kTok * 8) / 128; ++i) {
+        const int idx = i * 128 + tid;
+        const int r = idx >> 3, c = idx & 7;
+        const int t = t0 + r;
+        const bool ok = t < a.T;
+        cp_async_16(xs + off8(r, c), x + static_cast<int64_t>(ok ? t : 0) * a.x_stride + f0 + c * 8,
+                    ok ? 16 : 0);
+      }
+      for (int idx = tid; idx < kChunk * hc; idx += 128) {
+        const int r = idx / hc, c = idx % hc;
+        cp_async_16(ws + off8(r, c), w + static_cast<int64_t>(f0 + r) * a.h + c * 8, 16);
+      }
+    }
+    cp_async_commit();
+  };
+
+  float acc[kMaxH / 8][4];
+#pragma unroll
+  for (int i = 0; i < kMaxH / 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+
+  issue(0);
+  for (int ch = 0; ch < nchunks; ++ch) {
+    issue(ch + 1);
+    cp_async_wait<1>();
+    __syncthreads();
+    const uint32_t xs = sb + (ch % kStages) * kStageBytes;
+    const uint32_t ws = xs + kXBytes;
+#pragma unroll
+    for (int ks = 0; ks < kChunk / 16; ++ks) {
+      uint32_t af[4];
+      {
+        // A: tokens warp*16 .. +15, features ks*16 .. +15
+        const int r = warp * 16 + (lane & 15);
+        const int c = ks * 2 + (lane >> 4);
+        ldmatrix_x4(xs + off8(r, c), af[0], af[1], af[2], af[3]);
+      }
+#pragma unroll
+      for (int np = 0; np < kMaxH / 16; ++np) {
+        if (np * 2 < hc) {
+          // B = W[k][n]: matrices (k 0-7, n 0-7), (k 8-15, n 0-7), (k 0-7, n 8-15), (k 8-15, n 8-15)
+          const int r = ks * 16 + (lane & 7) + ((lane >> 3) & 1) * 8;
+          const int c = np * 2 + (lane >> 4);
+          uint32_t b0, b1, b2, b3;
+          ldmatrix_x4_trans(ws + off8(r, c), b0, b1, b2, b3);
+          mma_bf16_16816(acc[2 * np], af, b0, b1);
+          mma_bf16_16816(acc[2 * np + 1], af, b2, b3);
+        }
+      }
+    }
+    __syncthreads();
+  }
+
+  const int gr = lane >> 2, tq = lane & 3;
+#pragma unroll
+  for (int nt = 0; nt < kMaxH / 8; ++nt) {
+    if (nt < hc) {
+#pragma unroll
+      for (int half = 0; half < 2; ++half) {
+        const int t = t0 + warp * 16 + gr + half * 8;
+        if (t < a.T) {
+          const int col = nt * 8 + 2 * tq;
+          const float z0 = acc[nt][half * 2], z1 = acc[nt][half * 2 + 1];
+          float2 g;
+          g.x = 1.f / (1.f + expf(-z0));
+          g.y = 1.f / (1.f + expf(-z1));
+          *reinterpret_cast<float2*>(a.gate + static_cast<int64_t>(t) * a.h + col) = g;
+        }
+      }
+    }
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_gate(const GateArgs& a, cudaStream_t s) {
+  const int grid = (a.T + kTok - 1) / kTok;
+  if (grid == 0) return cudaSuccess;
+  gate_kernel<<<grid, 128, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace da

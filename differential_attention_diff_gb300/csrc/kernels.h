@@ -1,0 +1,92 @@
+// kernels.h — internal launch interface between api.cu (argument checks,
+// workspace carving, stream handling) and the kernel translation units.
+// Every launcher returns a cudaError_t from the launch itself.
+#pragma once
+
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "diffattn.h"
+
+namespace da {
+
+// ---- V2 gate: gate[t, p] = sigmoid(x[t, :] . w[:, p]) ---------------------
+struct GateArgs {
+  int T, d_model, h;
+  const void* x;
+  int64_t x_stride;
+  const void* w;
+  float* gate;
+};
+cudaError_t launch_gate(const GateArgs& a, cudaStream_t s);
+
+// ---- V2 decode: split-KV partials, then merge + even/odd gate ------------
+struct DecodeArgs {
+  int B, h, h_kv, d, L_max, num_splits;
+  float scale_log2;  // softmax scale * log2(e)
+  const void* q;
+  da_t4 k, v;
+  const int* seqlens;
+  const float* gate;  // [B, h]
+  void* out;          // bf16 [B, h, d]
+  float* part_o;      // [splits, B, 2h, d]
+  float* part_ml;     // [splits, B, 2h, 2]  (running max in log2 units, sum)
+  uint32_t* status;
+};
+cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+
+// ---- V1 forward, fp32 SIMT path ------------------------------------------
+struct V1F32Args {
+  int B, N, H, d_qk, d_v, causal;
+  float scale, lambda_init, rms_eps;
+  da_t4 q1, q2, k1, k2, v, out, o2;
+  const float *lq1, *lk1, *lq2, *lk2;
+  float *lse1, *lse2, *rstd, *lambda_out;
+};
+cudaError_t launch_v1_fwd_f32(const V1F32Args& a, cudaStream_t s);
+
+// ---- V2 forward, tcgen05 -------------------------------------------------
+struct V2FwdArgs {
+  int B, N, h, h_kv, d, causal;
+  float scale_log2;
+  da_t4 q, k, v, out;
+  const float* gate;  // [B, N, h]
+  float* lse;         // optional [B, 2h, N] (natural log)
+  uint32_t* status;
+  int num_sms;
+};
+cudaError_t launch_v2_fwd(const V2FwdArgs& a, cudaStream_t s);
+
+// ---- V1 forward, bf16, tcgen05 ---------------------------------------------
+struct V1FwdArgs {
+  int B, N, H, d_qk, d_v, causal;
+  float scale_log2, lambda_init, rms_eps;
+  da_t4 q1, q2, k1, k2, v, out, o2;
+  const float *lq1, *lk1, *lq2, *lk2;
+  float *lse1, *lse2, *rstd, *lambda_out;
+  uint32_t* status;
+  int num_sms;
+};
+cudaError_t launch_v1_fwd(const V1FwdArgs& a, cudaStream_t s);
+
+// ---- V1 backward, bf16 -----------------------------------------------------
+struct V1BwdArgs {
+  int B, N, H, d_qk, d_v, causal;
+  float scale, lambda_init, rms_eps;
+  da_t4 q1, q2, k1, k2, v, out, dout, o2;
+  const float *lq1, *lk1, *lq2, *lk2;
+  const float *lse1, *lse2, *rstd;
+  da_t4 dq1, dq2, dk1, dk2, dv;
+  float *dlq1, *dlk1, *dlq2, *dlk2;
+  void* workspace;
+  size_t workspace_bytes;
+  uint32_t* status;
+  int num_sms;
+};
+size_t v1_bwd_workspace_bytes(int B, int N, int H, int d_qk, int d_v);
+cudaError_t launch_v1_bwd(const V1BwdArgs& a, cudaStream_t s);
+
+// TMA descriptor encoding (driver entry point fetched through the runtime).
+bool tma_available();
+
+}  // namespace da

@@ -1,0 +1,241 @@
+/*
+ * diffattn.h — C ABI of libdiffattn.so, the differential-attention operator
+ * for NVIDIA GB300 (sm_103a).
+ *
+ * Sources for what the operator computes (web pages on the method; title and
+ * section as printed there):
+ *   [P1] "Differential Transformer | ICLR 2025 Oral" (dainus.ai blog)
+ *        - "Differential Attention: 빼기의 힘"  (the V1 formula)
+ *        - "λ의 역할과 학습"                    (the lambda_init schedule)
+ *        - "V2로의 진화"                         (V2 summary, memory-bound decode)
+ *   [P2] "Differential Transformer V2" (pogovet.com summary)
+ *        - §1 "DIFF V1에서 V2로 바뀐 핵심 구조" (V1 details; V2 structure)
+ *        - §2 "빠른 디코딩과 표준 커널 호환성"  (decode: KV heads not increased)
+ *        - §4 "RMS 정규화 제거와 차분 계수의 역할" (sigmoid gate, no RMSNorm)
+ *
+ * Conventions shared by every entry point
+ * ---------------------------------------
+ * - Pointers named in a *_params struct are DEVICE pointers unless stated.
+ *   The caller owns every buffer (inputs, outputs, optional saves and the
+ *   workspace); the library never allocates, frees or synchronises (except
+ *   diffattn_get_device_status, which synchronises the given stream).
+ * - 4-D tensors are passed as da_t4: a base pointer plus the element strides
+ *   of the batch (sb), sequence (sn) and head (sh) dimensions; the last
+ *   (feature) dimension is contiguous.  bf16 tensors need 16-byte aligned
+ *   base pointers and strides that are multiples of 8 elements.
+ * - Every call returns a da_status and never throws.  Arguments are checked
+ *   before anything is launched (null pointers, alignment, shapes the kernels
+ *   support).  A failed launch returns DA_ERR_CUDA.  Errors that a kernel
+ *   detects while running (a bounded wait that expired, an index check) are
+ *   recorded in a device status word read by diffattn_get_device_status.
+ * - Work is enqueued on the given CUDA stream (cudaStream_t passed as void*;
+ *   NULL = the legacy default stream) and runs asynchronously.
+ * - Causal masking means key j is visible to query i iff j <= i (queries and
+ *   keys share one position axis).
+ */
+#ifndef DIFFATTN_H
+#define DIFFATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  DA_OK = 0,
+  DA_ERR_INVALID_ARG = 1,  /* null pointer, bad size, misalignment          */
+  DA_ERR_UNSUPPORTED = 2,  /* valid but not implemented (head dim, dtype)    */
+  DA_ERR_CUDA = 3,         /* a CUDA runtime call or launch failed           */
+  DA_ERR_TIMEOUT = 4,      /* a kernel's bounded wait expired (device word)  */
+  DA_ERR_BOUNDS = 5,       /* a kernel's index check failed (device word)    */
+  DA_ERR_WORKSPACE = 6     /* workspace missing or smaller than required     */
+} da_status;
+
+typedef enum { DA_F32 = 0, DA_BF16 = 1 } da_dtype;
+
+/* A [B, N, H, D] tensor: element (b, n, h, x) lives at
+ * ptr + b*sb + n*sn + h*sh + x (in elements). */
+typedef struct {
+  void* ptr;
+  int64_t sb, sn, sh;
+} da_t4;
+
+/* ------------------------------------------------------------------------ */
+/* lambda_init(l) = 0.8 - 0.6 * exp(-0.3 * (l - 1)), l = 1-based layer index.
+ * [P1] "λ의 역할과 학습".  Host function; returns NaN for l < 1. */
+float diffattn_lambda_init(int layer);
+
+/* ------------------------------------------------------------------------ */
+/* V1 forward.  [P1] "Differential Attention: 빼기의 힘"; [P2] §1.
+ *   lambda = exp(lq1 . lk1) - exp(lq2 . lk2) + lambda_init   (one scalar,
+ *            computed on the device from the four vectors; never clamped)
+ *   O      = (softmax(s Q1 K1^T) - lambda softmax(s Q2 K2^T)) V
+ *   Y      = (1 - lambda_init) * O / sqrt(mean_k O_k^2 + rms_eps)
+ * per (b, n, h), the mean over the V head dim d_v (unit RMSNorm weight).
+ * q1, q2, k1, k2: [B, N, H, d_qk]; v, out: [B, N, H, d_v]; all of `dtype`.
+ * lq1, lk1, lq2, lk2: fp32 [d_qk].
+ * Supported: dtype DA_BF16 with d_qk = 128, d_v = 256, causal;
+ *            dtype DA_F32 with d_qk <= 128, d_v <= 256 (d_v % 32 == 0).
+ * Optional saves for the backward (NULL pointer = not written):
+ *   lse1, lse2 (log-sum-exp of the scaled scores per row), rstd
+ *   (1/sqrt(mean O^2 + eps)): fp32 [B, H, N] contiguous;
+ *   o2 = softmax(s Q2 K2^T) V: [B, N, H, d_v] of `dtype`;
+ *   lambda_out: fp32 [1].
+ * No workspace. */
+typedef struct {
+  int B, N, H, d_qk, d_v;
+  da_dtype dtype;
+  int causal;
+  float softmax_scale;   /* <= 0 selects 1/sqrt(d_qk) */
+  float lambda_init;
+  float rms_eps;
+  da_t4 q1, q2, k1, k2, v;
+  const float *lq1, *lk1, *lq2, *lk2;
+  da_t4 out;
+  float *lse1, *lse2, *rstd;
+  da_t4 o2;
+  float* lambda_out;
+} da_v1_fwd_params;
+
+da_status diffattn_v1_fwd(const da_v1_fwd_params* p, void* cuda_stream);
+
+/* ------------------------------------------------------------------------ */
+/* V1 backward: gradients of the V1 forward with respect to q1, q2, k1, k2,
+ * v and the four lambda vectors, given dY.  The pages state no backward; it
+ * is the chain rule applied to the forward above ([P1] formula, [P2] §1):
+ *   dO  = (c dY - Yhat mean(c dY * Yhat)) * rstd,   Yhat = Y / c, c = 1 - lambda_init
+ *   dP  = dO V^T;  D1 = <dO, A1 V>;  D2 = <dO, A2 V>
+ *   dS1 = A1 (dP - D1);  dS2 = -lambda A2 (dP - D2)
+ *   dQt = s dSt Kt;  dKt = s dSt^T Qt;  dV = (A1 - lambda A2)^T dO
+ *   dlambda = -sum <dO, A2 V>;  dlq1 = dlambda e^(lq1.lk1) lk1, ... .
+ * Inputs: the forward's inputs, its output `out` (Y), `dout` (dY), and the
+ * saves lse1, lse2, rstd, o2 written by diffattn_v1_fwd.  Outputs: dq1, dq2,
+ * dk1, dk2 [B,N,H,d_qk], dv [B,N,H,d_v] (dtype), dlq1, dlk1, dlq2, dlk2 fp32
+ * [d_qk] (overwritten).  Supported: DA_BF16, d_qk = 128, d_v = 256, causal.
+ * workspace: at least diffattn_v1_bwd_workspace_size(...) bytes, 256-byte
+ * aligned; its contents on entry do not matter. */
+typedef struct {
+  int B, N, H, d_qk, d_v;
+  da_dtype dtype;
+  int causal;
+  float softmax_scale;
+  float lambda_init;
+  float rms_eps;
+  da_t4 q1, q2, k1, k2, v;
+  const float *lq1, *lk1, *lq2, *lk2;
+  da_t4 out, dout;
+  const float *lse1, *lse2, *rstd;
+  da_t4 o2;
+  da_t4 dq1, dq2, dk1, dk2, dv;
+  float *dlq1, *dlk1, *dlq2, *dlk2;
+  void* workspace;
+  size_t workspace_bytes;
+} da_v1_bwd_params;
+
+size_t diffattn_v1_bwd_workspace_size(int B, int N, int H, int d_qk, int d_v);
+da_status diffattn_v1_bwd(const da_v1_bwd_params* p, void* cuda_stream);
+
+/* ------------------------------------------------------------------------ */
+/* V2 gate.  [P2] §1 and §4: a per-token, per-head coefficient projected from
+ * the input X and passed through a sigmoid (no bias):
+ *   gate[t, p] = sigmoid(sum_k x[t, k] * w_lambda[k, p])
+ * x: bf16 [T, d_model], row stride x_stride (elements, multiple of 8);
+ * w_lambda: bf16 [d_model, h] row-major contiguous; gate: fp32 [T, h]
+ * contiguous.  Supported: d_model % 64 == 0, h % 8 == 0, h <= 64. */
+typedef struct {
+  int T, d_model, h;
+  const void* x;
+  int64_t x_stride;
+  const void* w_lambda;
+  float* gate;
+} da_v2_gate_params;
+
+da_status diffattn_v2_gate(const da_v2_gate_params* p, void* cuda_stream);
+
+/* ------------------------------------------------------------------------ */
+/* V2 forward.  [P2] §1 and the one-line summary: one causal GQA attention
+ * over 2h query heads with h_kv K/V heads; q head j reads K/V head
+ * j / (2h / h_kv) (contiguous groups, so pair p = heads 2p and 2p+1 always
+ * shares one K/V head); then per token t and pair p
+ *   out[t, p] = O[t, 2p] - gate[t, p] * O[t, 2p + 1]
+ * which brings the width back to h * d.  No normalisation ([P2] §4).
+ * q: [B, N, 2h, d]; k, v: [B, N, h_kv, d]; out: [B, N, h, d]; all bf16.
+ * Gate source: either `gate` (fp32 [B, N, h] contiguous, already through the
+ * sigmoid) or, when gate == NULL, x (bf16 [B, N, d_model] contiguous) and
+ * w_lambda (bf16 [d_model, h]); the gate is then computed into the workspace
+ * (diffattn_v2_fwd_workspace_size bytes).  Optional lse: fp32 [B, 2h, N].
+ * Supported: d = 128, causal, (2h / h_kv) even. */
+typedef struct {
+  int B, N, h, h_kv, d, d_model;
+  int causal;
+  float softmax_scale;   /* <= 0 selects 1/sqrt(d) */
+  da_t4 q, k, v;
+  const float* gate;
+  const void* x;
+  const void* w_lambda;
+  da_t4 out;
+  float* lse;
+  void* workspace;
+  size_t workspace_bytes;
+} da_v2_fwd_params;
+
+size_t diffattn_v2_fwd_workspace_size(int B, int N, int h, int gate_given);
+da_status diffattn_v2_fwd(const da_v2_fwd_params* p, void* cuda_stream);
+
+/* ------------------------------------------------------------------------ */
+/* V2 decode.  [P1] "V2로의 진화" and [P2] §2: one new token per sequence
+ * attends over its KV cache; the KV heads and cache are those of a standard
+ * GQA model (only the query heads double), so the step is bound by reading
+ * the cache.  For sequence b the new token is already stored at position
+ * seqlens[b] - 1 and attends to positions 0 .. seqlens[b] - 1; then the
+ * even/odd combination with the gate as in diffattn_v2_fwd.
+ * q: bf16 [B, 2h, d] contiguous; k_cache, v_cache: bf16 [B, L_max, h_kv, d]
+ * (da_t4 strides; position stride sn); seqlens: int32 [B] device, each in
+ * [1, L_max] (NULL = all L_max); gate fp32 [B, h] or x bf16 [B, d_model] +
+ * w_lambda as in diffattn_v2_fwd; out: bf16 [B, h, d] contiguous.
+ * num_splits: key-range splits per (b, kv head); 0 = chosen by the library
+ * (diffattn_v2_decode_num_splits).  Workspace: split partials,
+ * diffattn_v2_decode_workspace_size bytes.  Supported: d = 128,
+ * 2 <= 2h / h_kv <= 16 and even.  A sequence length outside [1, L_max] is
+ * recorded as DA_ERR_BOUNDS in the device status word and its output row is
+ * written as zeros. */
+typedef struct {
+  int B, h, h_kv, d, L_max, d_model;
+  float softmax_scale;   /* <= 0 selects 1/sqrt(d) */
+  const void* q;
+  da_t4 k_cache, v_cache;
+  const int* seqlens;
+  const float* gate;
+  const void* x;
+  const void* w_lambda;
+  void* out;
+  int num_splits;
+  void* workspace;
+  size_t workspace_bytes;
+} da_v2_decode_params;
+
+int diffattn_v2_decode_num_splits(int B, int h_kv, int L_max);
+size_t diffattn_v2_decode_workspace_size(int B, int h, int h_kv, int d,
+                                         int L_max, int num_splits,
+                                         int gate_given);
+da_status diffattn_v2_decode(const da_v2_decode_params* p, void* cuda_stream);
+
+/* ------------------------------------------------------------------------ */
+/* Device status word.  Kernels record the first error they detect (a bounded
+ * wait that expired, a failed index check) in a per-device word instead of
+ * trapping.  diffattn_get_device_status synchronises `cuda_stream`, returns
+ * the recorded status (DA_OK if none) and clears the word.
+ * diffattn_get_device_status_detail additionally returns the raw word
+ * (status in the low byte, a kernel-specific site code above it). */
+da_status diffattn_get_device_status(void* cuda_stream);
+da_status diffattn_get_device_status_detail(void* cuda_stream, uint32_t* raw);
+
+const char* diffattn_status_string(da_status s);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* DIFFATTN_H */

@@ -1,0 +1,132 @@
+"""Host-side checks of the C ABI: the library loads without a GPU, exports
+every entry point that include/diffattn.h declares, and rejects bad
+arguments before launching anything."""
+
+import ctypes as C
+import math
+import os
+import re
+
+import pytest
+
+from differential_attention_diff_gb300 import binding as bd
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+def _declared():
+    src = open(os.path.join(ROOT, "include", "diffattn.h")).read()
+    return sorted(set(re.findall(r"\b(diffattn_\w+)\s*\(", src)))
+
+
+def test_header_matches_binding_list():
+    assert _declared() == sorted(bd.EXPORTS)
+
+
+def test_library_exports_every_declared_symbol(lib):
+    for name in _declared():
+        assert hasattr(lib, name), name
+
+
+def test_lambda_init_host_function(lib):
+    """lambda_init(l) = 0.8 - 0.6 exp(-0.3 (l - 1)) ("Differential Transformer",
+    section 'λ의 역할과 학습'); checked against the closed form in fp32."""
+    assert bd.diffattn_lambda_init(1) == pytest.approx(0.2, abs=1e-7)
+    for l in (2, 5, 14, 28):
+        assert bd.diffattn_lambda_init(l) == pytest.approx(0.8 - 0.6 * math.exp(-0.3 * (l - 1)), abs=1e-7)
+    assert math.isnan(bd.diffattn_lambda_init(0))
+
+
+def test_status_strings(lib):
+    for s in range(7):
+        assert lib.diffattn_status_string(s)
+    assert lib.diffattn_status_string(99) == b"unknown status"
+
+
+def test_null_params_rejected(lib):
+    for name in ("diffattn_v1_fwd", "diffattn_v1_bwd", "diffattn_v2_gate", "diffattn_v2_fwd",
+                 "diffattn_v2_decode"):
+        assert getattr(lib, name)(None, None) == bd.DA_ERR_INVALID_ARG, name
+
+
+def _v1p(**kw):
+    p = bd.da_v1_fwd_params()
+    p.B, p.N, p.H, p.d_qk, p.d_v = 1, 64, 2, 128, 256
+    p.dtype, p.causal, p.lambda_init, p.rms_eps = bd.DA_BF16, 1, 0.2, 1e-5
+    fake = 1 << 20  # never dereferenced: validation fails or stops first
+    for n in ("q1", "q2", "k1", "k2", "v", "out"):
+        setattr(p, n, bd.da_t4(fake, 64 * 2 * 256, 2 * 256, 256))
+    for n in ("lq1", "lk1", "lq2", "lk2"):
+        setattr(p, n, fake)
+    for k, v in kw.items():
+        setattr(p, k, v)
+    return p
+
+
+def test_v1_fwd_argument_checks(lib):
+    f = lib.diffattn_v1_fwd
+    assert f(C.byref(_v1p(B=-1)), None) == bd.DA_ERR_INVALID_ARG
+    assert f(C.byref(_v1p(dtype=7)), None) == bd.DA_ERR_INVALID_ARG
+    assert f(C.byref(_v1p(lq1=None)), None) == bd.DA_ERR_INVALID_ARG
+    assert f(C.byref(_v1p(q1=bd.da_t4(None, 0, 0, 0))), None) == bd.DA_ERR_INVALID_ARG
+    # misaligned bf16 base pointer and a stride that is not a multiple of 8
+    assert f(C.byref(_v1p(k1=bd.da_t4((1 << 20) + 2, 64, 64, 64))), None) == bd.DA_ERR_INVALID_ARG
+    assert f(C.byref(_v1p(v=bd.da_t4(1 << 20, 64, 60, 64))), None) == bd.DA_ERR_INVALID_ARG
+    assert f(C.byref(_v1p(rms_eps=-1.0)), None) == bd.DA_ERR_INVALID_ARG
+    # empty problems are a no-op
+    assert f(C.byref(_v1p(N=0)), None) == bd.DA_OK
+
+
+def test_decode_argument_checks(lib):
+    p = bd.da_v2_decode_params()
+    p.B, p.h, p.h_kv, p.d, p.L_max = 2, 32, 8, 128, 1024
+    fake = 1 << 20
+    p.q, p.out, p.gate = fake, fake, fake
+    p.k_cache = bd.da_t4(fake, 1024 * 8 * 128, 8 * 128, 128)
+    p.v_cache = bd.da_t4(fake, 1024 * 8 * 128, 8 * 128, 128)
+    f = lib.diffattn_v2_decode
+    bad = bd.da_v2_decode_params.from_buffer_copy(p)
+    bad.h_kv = 3  # 2h not divisible into groups
+    assert f(C.byref(bad), None) == bd.DA_ERR_INVALID_ARG
+    bad = bd.da_v2_decode_params.from_buffer_copy(p)
+    bad.h, bad.h_kv = 4, 8  # group of one query head: a pair would straddle groups
+    assert f(C.byref(bad), None) == bd.DA_ERR_INVALID_ARG
+    bad = bd.da_v2_decode_params.from_buffer_copy(p)
+    bad.d = 96
+    assert f(C.byref(bad), None) == bd.DA_ERR_UNSUPPORTED
+    # workspace missing
+    assert f(C.byref(p), None) == bd.DA_ERR_WORKSPACE
+    ws = lib.diffattn_v2_decode_workspace_size(2, 32, 8, 128, 1024, 4, 1)
+    assert ws >= 4 * 2 * 64 * 128 * 4
+    assert lib.diffattn_v2_decode_workspace_size(2, 32, 8, 128, 1024, 4, 0) > ws
+
+
+def test_v2_fwd_argument_checks(lib):
+    p = bd.da_v2_fwd_params()
+    p.B, p.N, p.h, p.h_kv, p.d, p.causal = 1, 128, 32, 8, 128, 1
+    fake = 1 << 20
+    for n in ("q", "k", "v", "out"):
+        setattr(p, n, bd.da_t4(fake, 1 << 16, 1 << 10, 128))
+    f = lib.diffattn_v2_fwd
+    # neither a gate nor x / w_lambda
+    assert f(C.byref(p), None) == bd.DA_ERR_INVALID_ARG
+    p.x, p.w_lambda, p.d_model = fake, fake, 4096
+    assert f(C.byref(p), None) == bd.DA_ERR_WORKSPACE
+    p.d = 64
+    assert f(C.byref(p), None) == bd.DA_ERR_UNSUPPORTED
+    assert lib.diffattn_v2_fwd_workspace_size(2, 8192, 32, 0) == 2 * 8192 * 32 * 4
+    assert lib.diffattn_v2_fwd_workspace_size(2, 8192, 32, 1) == 0
+
+
+def test_gate_argument_checks(lib):
+    p = bd.da_v2_gate_params(16, 100, 32, 1 << 20, 100, 1 << 20, 1 << 20)
+    assert lib.diffattn_v2_gate(C.byref(p), None) == bd.DA_ERR_INVALID_ARG  # stride % 8
+    p = bd.da_v2_gate_params(16, 96, 32, 1 << 20, 96, 1 << 20, 1 << 20)
+    assert lib.diffattn_v2_gate(C.byref(p), None) == bd.DA_ERR_UNSUPPORTED  # d_model % 64
+    p = bd.da_v2_gate_params(0, 64, 32, None, 64, None, None)
+    assert lib.diffattn_v2_gate(C.byref(p), None) == bd.DA_OK  # empty
+
+
+def test_bwd_workspace_size(lib):
+    assert lib.diffattn_v1_bwd_workspace_size(1, 8192, 16, 128, 256) > 0
+    assert lib.diffattn_v1_bwd_workspace_size(0, 8192, 16, 128, 256) == 0
