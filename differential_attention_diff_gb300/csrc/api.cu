@@ -115,10 +115,10 @@ da_status diffattn_v2_gate(const da_v2_gate_params* p, void* stream) {
   if (p->T < 0 || p->d_model <= 0 || p->h <= 0) return DA_ERR_INVALID_ARG;
   if (p->T == 0) return DA_OK;
   if (!p->x || !p->w_lambda || !p->gate) return DA_ERR_INVALID_ARG;
-  if (!aligned(p->x, 16) || !aligned(p->w_lambda, 16) || !aligned(p->gate, 8))
+  if (!aligned(p->x, 16) || !aligned(p->w_lambda, 16) || !aligned(p->gate, 4))
     return DA_ERR_INVALID_ARG;
   if (p->x_stride < p->d_model || (p->x_stride % 8)) return DA_ERR_INVALID_ARG;
-  if ((p->d_model % 64) || (p->h % 8) || p->h > 64) return DA_ERR_UNSUPPORTED;
+  if ((p->d_model % 64) || p->h > 64) return DA_ERR_UNSUPPORTED;
   da::GateArgs a{p->T, p->d_model, p->h, p->x, p->x_stride, p->w_lambda, p->gate};
   return cuda_status(da::launch_gate(a, static_cast<cudaStream_t>(stream)));
 }
@@ -162,7 +162,7 @@ da_status diffattn_v2_decode(const da_v2_decode_params* p, void* stream) {
     return DA_ERR_INVALID_ARG;
   if (p->gate == nullptr) {
     if (!p->x || !p->w_lambda || p->d_model <= 0) return DA_ERR_INVALID_ARG;
-    if ((p->d_model % 64) || (p->h % 8) || p->h > 64) return DA_ERR_UNSUPPORTED;
+    if ((p->d_model % 64) || p->h > 64) return DA_ERR_UNSUPPORTED;
   } else if (!aligned(p->gate, 4)) {
     return DA_ERR_INVALID_ARG;
   }
@@ -280,7 +280,7 @@ da_status diffattn_v2_fwd(const da_v2_fwd_params* p, void* stream) {
     if (check_t4(*t, DA_BF16) != DA_OK) return DA_ERR_INVALID_ARG;
   if (p->gate == nullptr) {
     if (!p->x || !p->w_lambda || p->d_model <= 0) return DA_ERR_INVALID_ARG;
-    if ((p->d_model % 64) || (p->h % 8) || p->h > 64) return DA_ERR_UNSUPPORTED;
+    if ((p->d_model % 64) || p->h > 64) return DA_ERR_UNSUPPORTED;
     const size_t need = diffattn_v2_fwd_workspace_size(p->B, p->N, p->h, 0);
     if (p->workspace == nullptr || p->workspace_bytes < need || !aligned(p->workspace, 256))
       return DA_ERR_WORKSPACE;

@@ -271,7 +271,7 @@ decode_merge_kernel(DecodeArgs a) {
     res[e] = lt > 0.f ? ot / lt : 0.f;
   }
   const float gte = a.gate[static_cast<int64_t>(b) * a.h + p];
-  const float y = res[0] - gte * res[1];
+  const float y = __fsub_rn(res[0], __fmul_rn(gte, res[1]));
   static_cast<__nv_bfloat16*>(a.out)[(static_cast<int64_t>(b) * a.h + p) * kD + col] =
       __float2bfloat16_rn(y);
 }

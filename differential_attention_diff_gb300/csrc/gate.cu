@@ -32,7 +32,7 @@ gate_kernel(GateArgs a) {
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t0 = blockIdx.x * kTok;
   const int nchunks = a.d_model / kChunk;
-  const int hc = a.h / 8;  // 16-byte chunks per W row
+  const int hc = (a.h + 7) / 8;  // 16-byte chunks per W row (padded)
   const __nv_bfloat16* x = static_cast<const __nv_bfloat16*>(a.x);
   const __nv_bfloat16* w = static_cast<const __nv_bfloat16*>(a.w);
   const uint32_t sb = smem_u32(smem);
@@ -51,9 +51,20 @@ gate_kernel(GateArgs a) {
         cp_async_16(xs + off8(r, c), x + static_cast<int64_t>(ok ? t : 0) * a.x_stride + f0 + c * 8,
                     ok ? 16 : 0);
       }
-      for (int idx = tid; idx < kChunk * hc; idx += 128) {
-        const int r = idx / hc, c = idx % hc;
-        cp_async_16(ws + off8(r, c), w + static_cast<int64_t>(f0 + r) * a.h + c * 8, 16);
+      if ((a.h & 7) == 0) {
+        for (int idx = tid; idx < kChunk * hc; idx += 128) {
+          const int r = idx / hc, c = idx % hc;
+          cp_async_16(ws + off8(r, c), w + static_cast<int64_t>(f0 + r) * a.h + c * 8, 16);
+        }
+      } else {
+        // h not a multiple of 8: element loads, zero padding up to the chunk edge
+        uint8_t* wsg = smem + (ch % kStages) * kStageBytes + kXBytes;
+        for (int idx = tid; idx < kChunk * hc * 8; idx += 128) {
+          const int r = idx / (hc * 8), col = idx % (hc * 8);
+          const __nv_bfloat16 v = col < a.h ? w[static_cast<int64_t>(f0 + r) * a.h + col]
+                                            : __float2bfloat16_rn(0.f);
+          *reinterpret_cast<__nv_bfloat16*>(wsg + off8(r, col >> 3) + (col & 7) * 2) = v;
+        }
       }
     }
     cp_async_commit();
@@ -104,11 +115,9 @@ gate_kernel(GateArgs a) {
         const int t = t0 + warp * 16 + gr + half * 8;
         if (t < a.T) {
           const int col = nt * 8 + 2 * tq;
-          const float z0 = acc[nt][half * 2], z1 = acc[nt][half * 2 + 1];
-          float2 g;
-          g.x = 1.f / (1.f + expf(-z0));
-          g.y = 1.f / (1.f + expf(-z1));
-          *reinterpret_cast<float2*>(a.gate + static_cast<int64_t>(t) * a.h + col) = g;
+          float* gp = a.gate + static_cast<int64_t>(t) * a.h + col;
+          if (col < a.h) gp[0] = 1.f / (1.f + expf(-acc[nt][half * 2]));
+          if (col + 1 < a.h) gp[1] = 1.f / (1.f + expf(-acc[nt][half * 2 + 1]));
         }
       }
     }

@@ -124,7 +124,7 @@ v1_fwd_f32_kernel(V1F32Args a) {
     o[c] = 0.f;
     if (c < nv) {
       o2[c] *= inv2;
-      o[c] = o1[c] * inv1 - lam * o2[c];
+      o[c] = __fsub_rn(__fmul_rn(o1[c], inv1), __fmul_rn(lam, o2[c]));
       ss += o[c] * o[c];
     }
   }

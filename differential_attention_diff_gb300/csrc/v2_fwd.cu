@@ -1,0 +1,429 @@
+// v2_fwd.cu — V2 differential attention forward on the 5th-generation tensor
+// cores (tcgen05 + TMEM + TMA), sm_103a.
+//
+// "Differential Transformer V2" (pogovet.com), §1 and the one-line summary:
+// one causal GQA attention over 2h query heads; heads 2p and 2p+1 share one
+// K/V head (same group) and are combined per token as
+//     out[t, p] = O[t, 2p] - gate[t, p] * O[t, 2p + 1].
+//
+// One CTA (persistent, one per SM) owns a work item = (batch, pair p, 128
+// query rows) at a time, heaviest causal rows first.  Both heads of the pair
+// are computed side by side against the same K/V tiles, each tile fetched
+// once by TMA for the two heads:
+//
+//   TMEM (512 columns x 128 lanes, lane = query row):
+//     [  0,128) S_even (fp32 scores) / P_even (bf16, first 64 columns)
+//     [128,256) S_odd / P_odd
+//     [256,384) O_even accumulator     [384,512) O_odd accumulator
+//   Shared memory: Q_even, Q_odd (2 x 32 KB), K and V rings of 2 stages
+//   (2 x 2 x 32 KB), all in 128-byte-swizzled 64-column boxes.
+//
+//   warp 8 (one lane): TMA producer — Q of the item, then K_j, V_j per tile.
+//   warp 9 (one lane): MMA issuer — S = Q K^T (SS form) and O += P V (P read
+//     from TMEM, V from shared memory), interleaving the two heads so that
+//     one head's softmax overlaps the other head's MMAs.
+//   warps 0-3 / 4-7: softmax of the even / odd head, one thread per query row
+//     (TMEM lane): row max, lazy rescale of O (only when the running max grows
+//     by more than 2^8), exp2, row sum, P written back to TMEM as bf16.
+//     The same threads run the epilogue: O_even / l_even - gate * O_odd /
+//     l_odd, bf16 store, optional log-sum-exp.
+//
+// Every mbarrier wait is bounded (about 2 s); on expiry the kernel records
+// DA_ERR_TIMEOUT in the status word, raises a shared abort flag so the other
+// roles leave too, drains its TMA loads and frees TMEM before returning.
+#include "kernels.h"
+#include "tma.cuh"
+
+namespace da {
+namespace {
+
+constexpr int kBM = 128;   // query rows per item
+constexpr int kBN = 128;   // keys per tile
+constexpr int kD = 128;    // head dim
+constexpr int kThreads = 320;
+constexpr int kBox = 128 * 128;            // bytes of one 64-column box of 128 rows
+constexpr int kOffQ = 0;                   // [head][box]
+constexpr int kOffK = 4 * kBox;            // [stage][box]
+constexpr int kOffV = 8 * kBox;            // [stage][box]
+constexpr int kOffBar = 12 * kBox;         // 196608
+constexpr int kSmemBytes = kOffBar + 4096 + 1024;  // + barriers/exchange + alignment slack
+
+// barrier indices (8 bytes each)
+enum {
+  B_QFULL = 0, B_QEMPTY = 1, B_KFULL = 2, B_VFULL = 4, B_KVEMPTY = 6, B_SFULL = 8,
+  B_PFULL = 10, B_ORDY = 12, B_EPI = 13, B_COUNT = 14
+};
+
+constexpr uint32_t kIdescS = idesc_bf16(128, 128, 0);   // Q (K-major) x K (K-major)
+constexpr uint32_t kIdescPV = idesc_bf16(128, 128, 1);  // P (TMEM) x V (MN-major)
+
+struct Shared {
+  uint32_t base;  // 1024-aligned shared address of the tile region
+  uint8_t* gen;   // same, generic pointer
+  __device__ uint32_t bar(int i) const { return base + kOffBar + 8 * i; }
+  __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(gen + kOffBar + 128); }
+  __device__ volatile int* abort_flag() const {
+    return reinterpret_cast<volatile int*>(gen + kOffBar + 192);
+  }
+  __device__ float* lx() const { return reinterpret_cast<float*>(gen + kOffBar + 256); }  // [2][128]
+  __device__ float* mx() const { return reinterpret_cast<float*>(gen + kOffBar + 1280); } // [2][128]
+};
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+// Bounded wait that also gives up when another role raised the abort flag.
+__device__ __forceinline__ bool wait_bar(const Shared& sh, uint32_t bar, uint32_t parity,
+                                         uint32_t* status, uint32_t site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*sh.abort_flag()) return false;
+    if (globaltimer() - t0 > 2000000000ull) {
+      record_status(status, DA_ERR_TIMEOUT, site);
+      *sh.abort_flag() = 1;
+      return false;
+    }
+  }
+}
+
+struct Item {
+  int b, p, mt, n_kv;
+};
+
+__device__ __forceinline__ Item item_of(int i, int units, int h, int n_mtiles) {
+  Item it;
+  it.mt = n_mtiles - 1 - i / units;
+  const int u = i % units;
+  it.b = u / h;
+  it.p = u % h;
+  it.n_kv = it.mt + 1;  // causal: tiles 0 .. mt
+  return it;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+v2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+              const __grid_constant__ CUtensorMap tm_v, V2FwdArgs a) {
+  extern __shared__ uint8_t smem_raw[];
+  Shared sh;
+  {
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t aligned = (raw + 1023u) & ~1023u;
+    sh.base = aligned;
+    sh.gen = smem_raw + (aligned - raw);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = (2 * a.h) / a.h_kv;
+  const int n_mtiles = (a.N + kBM - 1) / kBM;
+  const int units = a.B * a.h;
+  const int n_items = n_mtiles * units;
+
+  if (threadIdx.x == 0) {
+    mbar_init(sh.bar(B_QFULL), 1);
+    mbar_init(sh.bar(B_QEMPTY), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(sh.bar(B_KFULL + s), 1);
+      mbar_init(sh.bar(B_VFULL + s), 1);
+      mbar_init(sh.bar(B_KVEMPTY + s), 1);
+      mbar_init(sh.bar(B_SFULL + s), 1);
+      mbar_init(sh.bar(B_PFULL + s), 128);
+    }
+    mbar_init(sh.bar(B_ORDY), 1);
+    mbar_init(sh.bar(B_EPI), 256);
+    *sh.abort_flag() = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(sh.tmem_slot()), 512);
+    tmem_relinquish();
+  }
+  if (warp == 8 && lane == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *sh.tmem_slot();
+
+  if (warp == 8) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      int kv_it = 0, it = 0;
+      int last_kv = -1;  // last K/V tile issued (for the drain on error)
+      bool ok = true;
+      for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x, ++it) {
+        const Item w = item_of(i, units, a.h, n_mtiles);
+        const int g = (2 * w.p) / G;
+        if (it > 0 && !wait_bar(sh, sh.bar(B_QEMPTY), (it - 1) & 1, a.status, 0x2001)) {
+          ok = false;
+          break;
+        }
+        mbar_arrive_expect_tx(sh.bar(B_QFULL), 4 * kBox);
+        for (int hh = 0; hh < 2; ++hh)
+          for (int box = 0; box < 2; ++box)
+            tma_load_4d(sh.base + kOffQ + (hh * 2 + box) * kBox, &tm_q, sh.bar(B_QFULL), box * 64,
+                        2 * w.p + hh, w.mt * kBM, w.b);
+        for (int j = 0; j < w.n_kv; ++j, ++kv_it) {
+          const int st = kv_it & 1, use = kv_it >> 1;
+          if (use > 0 && !wait_bar(sh, sh.bar(B_KVEMPTY + st), (use - 1) & 1, a.status, 0x2002)) {
+            ok = false;
+            break;
+          }
+          mbar_arrive_expect_tx(sh.bar(B_KFULL + st), 2 * kBox);
+          for (int box = 0; box < 2; ++box)
+            tma_load_4d(sh.base + kOffK + (st * 2 + box) * kBox, &tm_k, sh.bar(B_KFULL + st),
+                        box * 64, g, j * kBN, w.b);
+          mbar_arrive_expect_tx(sh.bar(B_VFULL + st), 2 * kBox);
+          for (int box = 0; box < 2; ++box)
+            tma_load_4d(sh.base + kOffV + (st * 2 + box) * kBox, &tm_v, sh.bar(B_VFULL + st),
+                        box * 64, g, j * kBN, w.b);
+          last_kv = kv_it;
+        }
+      }
+      if (!ok && last_kv >= 0) {
+        // drain: give the loads already issued (bounded) time to land
+        for (int kv = last_kv; kv >= 0 && kv > last_kv - 2; --kv) {
+          const uint32_t par = (kv >> 1) & 1;
+          const uint64_t t0 = globaltimer();
+          while (globaltimer() - t0 < 200000000ull &&
+                 !(mbar_try_wait(sh.bar(B_KFULL + (kv & 1)), par) &&
+                   mbar_try_wait(sh.bar(B_VFULL + (kv & 1)), par))) {
+          }
+        }
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------- MMA issuer ---
+    if (lane == 0) {
+      int kv_it = 0, it = 0, pc = 0;
+      bool ok = true;
+      const uint32_t t_s[2] = {tmem + 0, tmem + 128};
+      const uint32_t t_o[2] = {tmem + 256, tmem + 384};
+      auto issue_s = [&](int hh, int st) {
+        const uint32_t qa = sh.base + kOffQ + hh * 2 * kBox;
+        const uint32_t kb = sh.base + kOffK + st * 2 * kBox;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+          tc_mma_ss(t_s[hh], sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                    kIdescS, kk > 0);
+        }
+      };
+      auto issue_pv = [&](int hh, int st, bool acc) {
+        const uint32_t vb = sh.base + kOffV + st * 2 * kBox;
+#pragma unroll
+        for (int kk = 0; kk < kBN / 16; ++kk) {
+          tc_mma_ts(t_o[hh], t_s[hh] + kk * 8, sdesc_sw128(vb + kk * 2048, kBox, 1024), kIdescPV,
+                    (acc || kk > 0) ? 1u : 0u);
+        }
+      };
+      for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x, ++it) {
+        const Item w = item_of(i, units, a.h, n_mtiles);
+        if (!wait_bar(sh, sh.bar(B_QFULL), it & 1, a.status, 0x2101)) { ok = false; break; }
+        tc_fence_after();
+        {
+          const int st = kv_it & 1;
+          if (!wait_bar(sh, sh.bar(B_KFULL + st), (kv_it >> 1) & 1, a.status, 0x2102)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(0, st);
+          tc_commit(sh.bar(B_SFULL + 0));
+          issue_s(1, st);
+          tc_commit(sh.bar(B_SFULL + 1));
+          if (w.n_kv == 1) tc_commit(sh.bar(B_QEMPTY));
+        }
+        for (int j = 0; j < w.n_kv; ++j) {
+          const int cur = kv_it + j, st = cur & 1;
+          const int nxt = cur + 1, st2 = nxt & 1;
+          const bool more = j + 1 < w.n_kv;
+          if (!wait_bar(sh, sh.bar(B_PFULL + 0), pc & 1, a.status, 0x2103)) { ok = false; break; }
+          if (!wait_bar(sh, sh.bar(B_VFULL + st), (cur >> 1) & 1, a.status, 0x2104)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(0, st, j > 0);
+          if (more) {
+            if (!wait_bar(sh, sh.bar(B_KFULL + st2), (nxt >> 1) & 1, a.status, 0x2105)) { ok = false; break; }
+            tc_fence_after();
+            issue_s(0, st2);
+            tc_commit(sh.bar(B_SFULL + 0));
+          }
+          if (!wait_bar(sh, sh.bar(B_PFULL + 1), pc & 1, a.status, 0x2106)) { ok = false; break; }
+          tc_fence_after();
+          issue_pv(1, st, j > 0);
+          tc_commit(sh.bar(B_KVEMPTY + st));
+          if (more) {
+            issue_s(1, st2);
+            tc_commit(sh.bar(B_SFULL + 1));
+            if (j + 2 == w.n_kv) tc_commit(sh.bar(B_QEMPTY));
+          }
+          ++pc;
+        }
+        if (!ok) break;
+        tc_commit(sh.bar(B_ORDY));
+        kv_it += w.n_kv;
+      }
+    }
+  } else {
+    // --------------------------------------------- softmax + epilogue -----
+    const int wg = warp >> 2;             // 0 = even head, 1 = odd head
+    const int q4 = warp & 3;
+    const int row = q4 * 32 + lane;       // query row within the item = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    const uint32_t t_s = tmem + lane_off + wg * 128;
+    const uint32_t t_o = tmem + lane_off + 256 + wg * 128;
+    const float sl2 = a.scale_log2;
+    int it = 0, sc = 0, ec = 0;
+    bool ok = true;
+    // bounded 256-thread sync of the two softmax warpgroups
+    auto epi_sync = [&](uint32_t site) -> bool {
+      mbar_arrive(sh.bar(B_EPI));
+      const bool r = wait_bar(sh, sh.bar(B_EPI), ec & 1, a.status, site);
+      ++ec;
+      return r;
+    };
+    for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x, ++it) {
+      const Item w = item_of(i, units, a.h, n_mtiles);
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = 0; j < w.n_kv; ++j, ++sc) {
+        if (!wait_bar(sh, sh.bar(B_SFULL + wg), sc & 1, a.status, 0x2201 + wg)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t s[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          tmem_ld32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
+        tmem_ld_wait();
+        const bool diag = (j == w.mt);
+        float mx = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 128; ++e) {
+          float v = __uint_as_float(s[e]);
+          if (diag && e > row) {
+            v = -INFINITY;
+            s[e] = __float_as_uint(v);
+          }
+          mx = fmaxf(mx, v);
+        }
+        const float m_tile = mx * sl2;
+        // lazy rescale: keep the stale max unless the new one exceeds it by > 8
+        const bool need = (j == 0) || (m_tile > m_run + 8.0f);
+        float alpha = 1.f;
+        if (need) {
+          const float m_new = fmaxf(m_run, m_tile);
+          alpha = (j == 0) ? 0.f : fast_exp2(m_run - m_new);
+          m_run = m_new;
+          l_run *= alpha;
+        }
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+          // O is stable here: the commit that signalled S(j) covers PV(j-1).
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t o[32];
+            tmem_ld32(t_o + c * 32, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(t_o + c * 32, o);
+          }
+        }
+        const float neg_m = -m_run;
+        float lsum = 0.f;
+        // P = exp2(s * scale - m), packed in place: chunk c (32 scores) becomes
+        // 16 bf16x2 words in s[c*32 .. c*32+15] = TMEM columns c*16 .. c*16+15
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = fast_exp2(fmaf(__uint_as_float(s[c * 32 + 2 * e]), sl2, neg_m));
+            const float p1 = fast_exp2(fmaf(__uint_as_float(s[c * 32 + 2 * e + 1]), sl2, neg_m));
+            lsum += p0 + p1;
+            s[c * 32 + e] = pack_bf16x2(p0, p1);
+          }
+        }
+        l_run += lsum;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          tmem_st16(t_s + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&s[c * 32]));
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(sh.bar(B_PFULL + wg));
+      }
+      if (!ok) break;
+      // ----------------------------------------------------- epilogue ----
+      if (!wait_bar(sh, sh.bar(B_ORDY), it & 1, a.status, 0x2203)) { ok = false; break; }
+      tc_fence_after();
+      sh.lx()[wg * 128 + row] = l_run;
+      sh.mx()[wg * 128 + row] = m_run;
+      if (!epi_sync(0x2204)) { ok = false; break; }
+      const int n = w.mt * kBM + row;
+      const float le = sh.lx()[row], lo = sh.lx()[128 + row];
+      uint32_t oe[2][32], oo[2][32];
+#pragma unroll
+      for (int c = 0; c < 2; ++c) {
+        tmem_ld32(tmem + lane_off + 256 + wg * 64 + c * 32, oe[c]);
+        tmem_ld32(tmem + lane_off + 384 + wg * 64 + c * 32, oo[c]);
+      }
+      tmem_ld_wait();
+      if (n < a.N) {
+        const float gte = a.gate[(static_cast<int64_t>(w.b) * a.N + n) * a.h + w.p];
+        const float ie = 1.f / le, io = gte / lo;
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out.ptr) + w.b * a.out.sb +
+                             static_cast<int64_t>(n) * a.out.sn + w.p * a.out.sh + wg * 64;
+        // both products rounded separately (no FMA contraction), so equal
+        // even and odd outputs with gate 1 cancel exactly
+        auto diff = [&](uint32_t xe, uint32_t xo) {
+          return __fsub_rn(__fmul_rn(__uint_as_float(xe), ie), __fmul_rn(__uint_as_float(xo), io));
+        };
+#pragma unroll
+        for (int c = 0; c < 2; ++c) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            uint4 v;
+            v.x = pack_bf16x2(diff(oe[c][e], oo[c][e]), diff(oe[c][e + 1], oo[c][e + 1]));
+            v.y = pack_bf16x2(diff(oe[c][e + 2], oo[c][e + 2]), diff(oe[c][e + 3], oo[c][e + 3]));
+            v.z = pack_bf16x2(diff(oe[c][e + 4], oo[c][e + 4]), diff(oe[c][e + 5], oo[c][e + 5]));
+            v.w = pack_bf16x2(diff(oe[c][e + 6], oo[c][e + 6]), diff(oe[c][e + 7], oo[c][e + 7]));
+            *reinterpret_cast<uint4*>(dst + c * 32 + e) = v;
+          }
+        }
+        if (a.lse) {
+          // natural-log LSE of head 2p + wg: (m + log2 l) * ln 2
+          a.lse[(static_cast<int64_t>(w.b) * 2 * a.h + 2 * w.p + wg) * a.N + n] =
+              (m_run + __log2f(l_run)) * 0.69314718055994531f;
+        }
+      }
+      tc_fence_before();
+      if (!epi_sync(0x2205)) { ok = false; break; }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 9) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+cudaError_t launch_v2_fwd(const V2FwdArgs& a, cudaStream_t s) {
+  CUtensorMap tq, tk, tv;
+  if (!encode_tmap_bf16_4d(&tq, a.q, a.B, a.N, 2 * a.h, kD, kBM)) return cudaErrorInvalidValue;
+  if (!encode_tmap_bf16_4d(&tk, a.k, a.B, a.N, a.h_kv, kD, kBN)) return cudaErrorInvalidValue;
+  if (!encode_tmap_bf16_4d(&tv, a.v, a.B, a.N, a.h_kv, kD, kBN)) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(v2_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int n_items = ((a.N + kBM - 1) / kBM) * a.B * a.h;
+  int grid = a.num_sms > 0 ? a.num_sms : 148;
+  if (grid > n_items) grid = n_items;
+  if (grid <= 0) return cudaSuccess;
+  v2_fwd_kernel<<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, a);
+  return cudaGetLastError();
+}
+
+}  // namespace da
