@@ -1,0 +1,578 @@
+"""Benchmark of the differential-attention hot path on GB300.
+
+    python bench.py [--gpus N] [--steps K] [--warmup W] [--workload NAME]
+                    [--impl ours|reference] [--no-rows] [--no-cpu-baseline]
+
+Prints ONE JSON line (rank 0).  `value` is the throughput of the selected
+workload (default: V1 forward bf16, B4 H12 N4096 d_qk 128 d_v 256, causal)
+with inputs resident in HBM; `rows` holds the same measurement for every
+other step of the path (V1 fp32, V2 gate + forward, V2 decode, V1
+forward + backward) on its own workload; `e2e` repeats the main workload
+through the public API with pinned host buffers and the copies inside the
+timed region; `roofline` relates the dominant kernel's live CUDA-event time
+to the measured (or fallback) peak; `cpu_baseline` times the fp64 oracle on a
+bounded sample of the same workload.
+
+`--impl reference` times the fp64 CPU oracle (the only reference there is)
+as the reference arm on the same workload and metric.
+
+Multi-GPU (torchrun): replicas only — every rank runs the full workload on
+its own GPU (no collective on the data path); the timed region is bracketed
+by barriers and the slowest rank's time is reported (weak scaling).
+"""
+
+from __future__ import annotations
+
+import argparse
+import json
+import math
+import os
+import statistics
+import subprocess
+import sys
+import threading
+import time
+
+ROOT = os.path.dirname(os.path.abspath(__file__))
+if ROOT not in sys.path:
+    sys.path.insert(0, ROOT)
+
+import numpy as np  # noqa: E402
+import torch  # noqa: E402
+
+L2_BYTES = 129 * 1024 * 1024
+FALLBACK_HBM_GBS = 6800.0
+FALLBACK_BF16_TFLOPS = 1900.0
+
+# --------------------------------------------------------------- workloads --
+# Algorithmic work per call (causal: half of the N^2 score matrix, the
+# flash-attention convention).
+
+
+def v1_fwd_flops(B, N, H, dqk, dv):
+    return B * H * 0.5 * (4.0 * N * N * dqk + 2.0 * N * N * dv)
+
+
+def v1_bwd_flops(B, N, H, dqk, dv):
+    return B * H * 0.5 * (12.0 * N * N * dqk + 4.0 * N * N * dv)
+
+
+def v2_fwd_flops(B, N, h, d):
+    return B * 2 * h * 0.5 * 4.0 * N * N * d
+
+
+def decode_bytes(B, L, hkv, d):
+    return 2.0 * B * L * hkv * d * 2
+
+
+class Workload:
+    """One step of the path on its configuration."""
+
+    name = ""
+    desc = ""
+    unit = "TFLOP/s"
+    bound = "tensor"
+    dtype = "bf16"
+    launches = 1
+
+    def work(self):  # flops or bytes per step
+        raise NotImplementedError
+
+    def setup(self, dev):
+        raise NotImplementedError
+
+    def run(self):  # device-resident step
+        raise NotImplementedError
+
+    def run_dominant(self):  # the dominant kernel alone (for the roofline)
+        self.run()
+
+    def dominant_work(self):
+        return self.work()
+
+    def scale(self, seconds):
+        w = self.work()
+        return w / seconds / (1e12 if self.unit == "TFLOP/s" else 1e9)
+
+
+class V1Fwd(Workload):
+    name = "v1_fwd"
+    desc = "V1 DiffAttn fwd bf16 B4 H12 N4096 d_qk128 d_v256 causal, layer 1"
+    B, N, H, dqk, dv, layer = 4, 4096, 12, 128, 256, 1
+
+    def work(self):
+        return v1_fwd_flops(self.B, self.N, self.H, self.dqk, self.dv)
+
+    def setup(self, dev):
+        from differential_attention_diff_gb300 import binding as bd, synth
+        self.bd = bd
+        self.t = synth.v1_inputs(self.B, self.N, self.H, self.dqk, self.dv, "bf16", seed=1002,
+                                 device=dev)
+        self.li = bd.diffattn_lambda_init(self.layer)
+        self.out = torch.empty((self.B, self.N, self.H, self.dv), dtype=torch.bfloat16, device=dev)
+
+    def args(self, t):
+        return [t[n] for n in ("q1", "q2", "k1", "k2", "v", "lq1", "lk1", "lq2", "lk2")]
+
+    def run(self):
+        self.bd.diffattn_v1_fwd(*self.args(self.t), self.li, out=self.out)
+
+    # end-to-end through the public API with host buffers
+    def e2e_setup(self):
+        self.host = {k: v.cpu().pin_memory() for k, v in self.t.items()}
+        self.host_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        self.h2d = sum(v.numel() * v.element_size() for v in self.host.values())
+        self.d2h = self.host_out.numel() * self.host_out.element_size()
+
+    def e2e_step(self):
+        dev = {k: v.to(self.out.device, non_blocking=True) for k, v in self.host.items()}
+        self.bd.diffattn_v1_fwd(*self.args(dev), self.li, out=self.out)
+        self.host_out.copy_(self.out, non_blocking=True)
+
+    def oracle_sample(self):
+        """fp64 oracle on a bounded sample: every head of batch 0, a seeded
+        set of query rows; returns (seconds, flops of the sampled rows)."""
+        from oracle import diffattn_oracle as orc
+        rows = np.sort(np.random.default_rng(0).choice(self.N, 96, replace=False))
+        ts = {k: v[:1].to("cpu", torch.float64).numpy() if v.dim() == 4 else
+              v.to("cpu", torch.float64).numpy() for k, v in self.t.items()}
+        t0 = time.perf_counter()
+        orc.v1_forward(*(ts[n] for n in ("q1", "q2", "k1", "k2", "v", "lq1", "lk1", "lq2", "lk2")),
+                       self.li, rows=rows)
+        dt = time.perf_counter() - t0
+        keys = float(np.sum(rows + 1))  # causal keys of the sampled rows
+        flops = self.H * keys * (4.0 * self.dqk + 2.0 * self.dv)
+        return dt, flops, f"batch 0, {self.H} heads, 96 seeded query rows of {self.N}"
+
+
+class V1FwdBwd(V1Fwd):
+    name = "v1_fwd_bwd"
+    desc = "V1 DiffAttn fwd+bwd bf16 B1 H16 N8192 d_qk128 d_v256 causal, layer 1"
+    B, N, H, dqk, dv, layer = 1, 8192, 16, 128, 256, 1
+
+    def work(self):
+        return v1_fwd_flops(self.B, self.N, self.H, self.dqk, self.dv) + \
+            v1_bwd_flops(self.B, self.N, self.H, self.dqk, self.dv)
+
+    def setup(self, dev):
+        from differential_attention_diff_gb300 import binding as bd, synth
+        self.bd = bd
+        self.t = synth.v1_inputs(self.B, self.N, self.H, self.dqk, self.dv, "bf16", seed=1005,
+                                 device=dev, with_dy=True)
+        self.li = bd.diffattn_lambda_init(self.layer)
+        self.out = torch.empty((self.B, self.N, self.H, self.dv), dtype=torch.bfloat16, device=dev)
+        _, self.saves = bd.diffattn_v1_fwd(*self.args(self.t), self.li, out=self.out, save=True)
+        self.grads = bd.diffattn_v1_bwd(*self.args(self.t), self.li, self.out, self.t["dy"],
+                                        self.saves)
+        need = bd.load().diffattn_v1_bwd_workspace_size(self.B, self.N, self.H, self.dqk, self.dv)
+        self.ws = torch.empty((max(need, 1),), dtype=torch.uint8, device=dev)
+        self.launches = None
+
+    def run(self):
+        self.bd.diffattn_v1_fwd(*self.args(self.t), self.li, out=self.out, save=True)
+        self.bd.diffattn_v1_bwd(*self.args(self.t), self.li, self.out, self.t["dy"], self.saves,
+                                grads=self.grads, workspace=self.ws)
+
+    def run_dominant(self):
+        self.bd.diffattn_v1_bwd(*self.args(self.t), self.li, self.out, self.t["dy"], self.saves,
+                                grads=self.grads, workspace=self.ws)
+
+    def dominant_work(self):
+        return v1_bwd_flops(self.B, self.N, self.H, self.dqk, self.dv)
+
+
+class V1FwdF32(V1Fwd):
+    name = "v1_fwd_f32"
+    desc = "V1 DiffAttn fwd fp32 B1 H2 N64 d_qk16 d_v32 causal, layer 1 (latency-bound)"
+    dtype = "f32"
+    bound = "alu"
+    B, N, H, dqk, dv, layer = 1, 64, 2, 16, 32, 1
+
+    def setup(self, dev):
+        from differential_attention_diff_gb300 import binding as bd, synth
+        self.bd = bd
+        self.t = synth.v1_inputs(self.B, self.N, self.H, self.dqk, self.dv, "f32", seed=1001,
+                                 device=dev)
+        self.li = bd.diffattn_lambda_init(self.layer)
+        self.out = torch.empty((self.B, self.N, self.H, self.dv), dtype=torch.float32, device=dev)
+
+
+class V2Fwd(Workload):
+    name = "v2_fwd"
+    desc = "V2 DiffAttn fwd bf16 B2 N8192 64q/8kv heads d128 causal, gate from X[2,8192,4096]"
+    launches = 2
+    B, N, h, hkv, d, dm = 2, 8192, 32, 8, 128, 4096
+
+    def work(self):
+        return v2_fwd_flops(self.B, self.N, self.h, self.d)
+
+    def setup(self, dev):
+        from differential_attention_diff_gb300 import binding as bd, synth
+        self.bd = bd
+        self.t = synth.v2_inputs(self.B, self.N, self.h, self.hkv, self.d, self.dm, seed=1003,
+                                 device=dev)
+        self.out = torch.empty((self.B, self.N, self.h, self.d), dtype=torch.bfloat16, device=dev)
+        need = bd.load().diffattn_v2_fwd_workspace_size(self.B, self.N, self.h, 0)
+        self.ws = torch.empty((need,), dtype=torch.uint8, device=dev)
+        self.gate = bd.diffattn_v2_gate(self.t["x"], self.t["w_lambda"])
+
+    def run(self):
+        t = self.t
+        self.bd.diffattn_v2_fwd(t["q"], t["k"], t["v"], x=t["x"], w_lambda=t["w_lambda"],
+                                out=self.out, workspace=self.ws)
+
+    def run_dominant(self):
+        t = self.t
+        self.bd.diffattn_v2_fwd(t["q"], t["k"], t["v"], gate=self.gate, out=self.out)
+
+    def e2e_setup(self):
+        self.host = {k: v.cpu().pin_memory() for k, v in self.t.items()}
+        self.host_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
+        self.h2d = sum(v.numel() * v.element_size() for v in self.host.values())
+        self.d2h = self.host_out.numel() * self.host_out.element_size()
+
+    def e2e_step(self):
+        d = {k: v.to(self.out.device, non_blocking=True) for k, v in self.host.items()}
+        self.bd.diffattn_v2_fwd(d["q"], d["k"], d["v"], x=d["x"], w_lambda=d["w_lambda"],
+                                out=self.out, workspace=self.ws)
+        self.host_out.copy_(self.out, non_blocking=True)
+
+    def oracle_sample(self):
+        from oracle import diffattn_oracle as orc
+        rows = np.sort(np.random.default_rng(0).choice(self.N, 48, replace=False))
+        G = 2 * self.h // self.hkv
+        t0 = time.perf_counter()
+        for p in range(4):  # four pairs of batch 0 (one per K/V group of the first four)
+            g = (2 * p) // G
+            sl = lambda x, a, b: x[0:1, :, a:b].to("cpu", torch.float64).numpy()  # noqa: E731
+            gate = orc.v2_gate(self.t["x"][0:1].to("cpu", torch.float64).numpy(),
+                               self.t["w_lambda"][:, p:p + 1].to("cpu", torch.float64).numpy())
+            orc.v2_forward(sl(self.t["q"], 2 * p, 2 * p + 2), sl(self.t["k"], g, g + 1),
+                           sl(self.t["v"], g, g + 1), gate, rows=rows)
+        dt = time.perf_counter() - t0
+        flops = 4 * 2 * float(np.sum(rows + 1)) * 4.0 * self.d
+        return dt, flops, "batch 0, 4 pairs, 48 seeded query rows of 8192 (gate included)"
+
+
+class V2Decode(Workload):
+    name = "v2_decode"
+    desc = "V2 decode bf16 B64 cache 32768 8 KV heads 64 query heads d128, gate from X[64,4096]"
+    unit = "GB/s"
+    bound = "hbm"
+    launches = 3
+    B, L, h, hkv, d, dm = 64, 32768, 32, 8, 128, 4096
+
+    def work(self):
+        return decode_bytes(self.B, self.L, self.hkv, self.d)
+
+    def setup(self, dev):
+        from differential_attention_diff_gb300 import binding as bd, synth
+        self.bd = bd
+        self.t = synth.decode_inputs(self.B, self.L, self.h, self.hkv, self.d, self.dm, seed=1004,
+                                     device=dev)
+        self.out = torch.empty((self.B, self.h, self.d), dtype=torch.bfloat16, device=dev)
+        need = bd.diffattn_v2_decode_workspace_size(self.B, self.h, self.hkv, self.d, self.L)
+        self.ws = torch.empty((need,), dtype=torch.uint8, device=dev)
+
+    def run(self):
+        t = self.t
+        self.bd.diffattn_v2_decode(t["q"], t["k_cache"], t["v_cache"], x=t["x"],
+                                   w_lambda=t["w_lambda"], out=self.out, workspace=self.ws)
+
+    def oracle_sample(self):
+        from oracle import diffattn_oracle as orc
+        t0 = time.perf_counter()
+        b = 0
+        gate = orc.v2_gate(self.t["x"][b:b + 1].to("cpu", torch.float64).numpy(),
+                           self.t["w_lambda"].to("cpu", torch.float64).numpy())
+        orc.v2_decode(self.t["q"][b:b + 1].to("cpu", torch.float64).numpy(),
+                      self.t["k_cache"][b:b + 1].to("cpu", torch.float64).numpy(),
+                      self.t["v_cache"][b:b + 1].to("cpu", torch.float64).numpy(), [self.L], gate)
+        dt = time.perf_counter() - t0
+        return dt, decode_bytes(1, self.L, self.hkv, self.d), "sequence 0 of 64 (full cache)"
+
+
+WORKLOADS = {w.name: w for w in (V1Fwd, V1FwdF32, V2Fwd, V2Decode, V1FwdBwd)}
+
+# ----------------------------------------------------------------- helpers --
+
+
+def measured_peaks():
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    if os.path.exists(path):
+        try:
+            d = json.load(open(path))
+            return d, "measured"
+        except Exception:  # noqa: BLE001
+            pass
+    return {}, "fallback"
+
+
+def peak_for(bound, long_step=False):
+    d, src = measured_peaks()
+    if bound == "hbm":
+        v = d.get("hbm_gbs")
+        return (float(v), "of measured") if v else (FALLBACK_HBM_GBS, "of fallback")
+    if bound == "tensor":
+        key = "bf16_tflops_sustained" if long_step else "bf16_tflops"
+        v = d.get(key) or d.get("bf16_tflops")
+        return (float(v), "of measured") if v else (FALLBACK_BF16_TFLOPS, "of fallback")
+    return None, None
+
+
+class ClockSampler:
+    """nvidia-smi clocks and throttle reasons sampled during the timed region."""
+
+    Q = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+         "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
+         "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
+
+    def __init__(self, index):
+        self.index = index
+        self.proc = None
+        self.lines = []
+
+    def start(self):
+        try:
+            self.proc = subprocess.Popen(
+                ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
+                 "-lms", "200", "-i", str(self.index)],
+                stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
+            self.thread = threading.Thread(target=self._read, daemon=True)
+            self.thread.start()
+        except Exception:  # noqa: BLE001
+            self.proc = None
+
+    def _read(self):
+        for line in self.proc.stdout:
+            self.lines.append(line.strip())
+
+    def stop(self):
+        if self.proc is None:
+            return None
+        self.proc.terminate()
+        try:
+            self.proc.wait(timeout=5)
+        except Exception:  # noqa: BLE001
+            self.proc.kill()
+        sm, smax, reasons = [], [], set()
+        names = ("hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap")
+        for ln in self.lines:
+            f = [x.strip() for x in ln.split(",")]
+            if len(f) < 9:
+                continue
+            try:
+                sm.append(float(f[1]))
+                smax.append(float(f[2]))
+            except ValueError:
+                continue
+            for n, v in zip(names, f[5:9]):
+                if v.lower() == "active":
+                    reasons.add(n)
+        if not sm:
+            return None
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
+                "reasons": sorted(reasons), "samples": len(sm)}
+
+
+def dist_env():
+    ws = int(os.environ.get("WORLD_SIZE", "1"))
+    rank = int(os.environ.get("RANK", "0"))
+    local = int(os.environ.get("LOCAL_RANK", "0"))
+    return ws, rank, local
+
+
+def time_steps(fn, steps, flush, stream):
+    """CUDA-event time of each of `steps` calls of fn (L2 flushed between
+    calls, outside the timed events).  Returns per-step milliseconds."""
+    times = []
+    for _ in range(steps):
+        if flush is not None:
+            flush.add_(1)  # write > L2 bytes
+        e0 = torch.cuda.Event(enable_timing=True)
+        e1 = torch.cuda.Event(enable_timing=True)
+        e0.record(stream)
+        fn()
+        e1.record(stream)
+        times.append((e0, e1))
+    torch.cuda.synchronize()
+    return [a.elapsed_time(b) for a, b in times]
+
+
+# ------------------------------------------------------------------- arms ---
+
+
+def run_ours(args, ws, rank, local):
+    dev = torch.device("cuda", local)
+    torch.cuda.set_device(dev)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.init_process_group("nccl", device_id=dev)
+    stream = torch.cuda.current_stream()
+    flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
+
+    main = WORKLOADS[args.workload]()
+    main.setup(dev)
+    for _ in range(args.warmup):
+        main.run()
+    torch.cuda.synchronize()
+
+    def barrier():
+        if ws > 1:
+            import torch.distributed as dist
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    sampler = ClockSampler(local)
+    barrier()
+    sampler.start()
+    per_step = time_steps(main.run, args.steps, flush, stream)
+    barrier()
+    clocks = sampler.stop()
+    total_ms = sum(per_step)
+    if ws > 1:
+        import torch.distributed as dist
+        tt = torch.tensor([total_ms], device=dev, dtype=torch.float64)
+        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
+        total_ms = float(tt.item())
+    ms = total_ms / args.steps
+    value = main.scale(ms / 1e3) * ws
+
+    # dominant kernel alone, live CUDA events on its launching stream
+    for _ in range(2):
+        main.run_dominant()
+    dom_ms = statistics.median(time_steps(main.run_dominant, max(3, args.steps), flush, stream))
+    peak, peak_src = peak_for(main.bound, long_step=False)
+    dom_work = main.dominant_work()
+    if main.unit == "TFLOP/s":
+        achieved = dom_work / (dom_ms / 1e3) / 1e12
+        r_unit = "TFLOP/s"
+    else:
+        achieved = dom_work / (dom_ms / 1e3) / 1e9
+        r_unit = "GB/s"
+    roofline = {"bound": main.bound, "achieved": round(achieved, 2),
+                "peak": peak, "unit": r_unit,
+                "frac": round(achieved / peak, 4) if peak else None,
+                "peak_source": peak_src, "traffic": None,
+                "kernel_ms": round(dom_ms, 4)}
+
+    # end-to-end through the public API with host buffers
+    e2e = None
+    if hasattr(main, "e2e_setup"):
+        main.e2e_setup()
+        for _ in range(2):
+            main.e2e_step()
+        torch.cuda.synchronize()
+        t0 = time.perf_counter()
+        for _ in range(args.steps):
+            main.e2e_step()
+        torch.cuda.synchronize()
+        e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
+        e2e = {"value": round(main.scale(e_ms / 1e3) * ws, 3), "unit": main.unit,
+               "ms_per_step": round(e_ms, 4), "h2d_bytes_per_step": main.h2d,
+               "d2h_bytes_per_step": main.d2h}
+
+    rows = {}
+    if not args.no_rows:
+        for name, cls in WORKLOADS.items():
+            if name == main.name:
+                continue
+            w = cls()
+            try:
+                w.setup(dev)
+                for _ in range(3):
+                    w.run()
+                t = statistics.median(time_steps(w.run, max(5, args.steps), flush, stream))
+                for _ in range(2):
+                    w.run_dominant()
+                td = statistics.median(time_steps(w.run_dominant, max(5, args.steps), flush, stream))
+                pk, src = peak_for(w.bound)
+                dw = w.dominant_work() / (td / 1e3) / (1e12 if w.unit == "TFLOP/s" else 1e9)
+                rows[name] = {"workload": w.desc, "ms_per_step": round(t, 4),
+                              "value": round(w.scale(t / 1e3), 3), "unit": w.unit,
+                              "dominant_kernel_ms": round(td, 4),
+                              "dominant_achieved": round(dw, 2),
+                              "dominant_frac": round(dw / pk, 4) if pk else None,
+                              "peak_source": src}
+            except Exception as exc:  # noqa: BLE001
+                rows[name] = {"workload": w.desc, "error": str(exc)[:200]}
+            del w
+            torch.cuda.empty_cache()
+
+    cpu = None
+    if rank == 0 and not args.no_cpu_baseline and hasattr(main, "oracle_sample"):
+        dt, work, sample = main.oracle_sample()
+        cpu = {"value": work / dt / (1e12 if main.unit == "TFLOP/s" else 1e9), "unit": main.unit,
+               "cores": torch.get_num_threads(), "kind": "oracle", "sample": sample,
+               "seconds": round(dt, 3)}
+
+    if rank == 0:
+        line = {
+            "metric": "diff-attn fwd TFLOP/s & % BF16 peak (prefill); decode HBM GB/s & % of 8 TB/s",
+            "value": round(value, 3), "unit": main.unit, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 4), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": main.dtype, "data": "synthetic",
+            "config": {"workload": main.desc, "l2": "flushed between timed steps (512 MB write)",
+                       "parallelism": f"replicas x{ws}"},
+            "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+            "gpu_launches": main.launches * args.steps if main.launches else None,
+            "rows": rows, "impl": "ours",
+        }
+        print(json.dumps(line), flush=True)
+    if ws > 1:
+        import torch.distributed as dist
+        dist.destroy_process_group()
+
+
+def run_reference(args, ws, rank):
+    """Reference arm: the fp64 CPU oracle on a bounded sample of the same
+    workload, on the host cores (rank 0 only)."""
+    if rank != 0:
+        return
+    main = WORKLOADS[args.workload]()
+    dev = "cuda" if torch.cuda.is_available() else "cpu"
+    main.setup(dev) if dev == "cuda" else None
+    if dev != "cuda":
+        print(json.dumps({"impl": "reference", "unavailable": "needs the GPU to draw inputs"}))
+        return
+    for _ in range(args.warmup):
+        main.oracle_sample()
+    secs, work, sample = 0.0, 0.0, ""
+    for _ in range(args.steps):
+        dt, w, sample = main.oracle_sample()
+        secs += dt
+        work += w
+    ms = secs * 1e3 / args.steps
+    value = work / secs / (1e12 if main.unit == "TFLOP/s" else 1e9)
+    line = {"metric": "diff-attn fwd TFLOP/s & % BF16 peak (prefill); decode HBM GB/s & % of 8 TB/s",
+            "value": value, "unit": main.unit, "n_gpus": ws, "steps": args.steps,
+            "warmup": args.warmup, "ms_per_step": round(ms, 3), "higher_is_better": True,
+            "scaling": "weak", "vs_baseline": None, "dtype": "f64", "data": "synthetic",
+            "config": {"workload": main.desc}, "impl": "reference",
+            "cpu_baseline": {"value": value, "unit": main.unit, "cores": torch.get_num_threads(),
+                             "kind": "oracle", "sample": sample},
+            "e2e": {"value": value, "unit": main.unit, "h2d_bytes_per_step": 0,
+                    "d2h_bytes_per_step": 0}}
+    print(json.dumps(line), flush=True)
+
+
+def main():
+    ap = argparse.ArgumentParser()
+    ap.add_argument("--gpus", type=int, default=1)
+    ap.add_argument("--steps", type=int, default=10)
+    ap.add_argument("--warmup", type=int, default=3)
+    ap.add_argument("--workload", default="v1_fwd", choices=sorted(WORKLOADS))
+    ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
+    ap.add_argument("--no-rows", action="store_true")
+    ap.add_argument("--no-cpu-baseline", action="store_true")
+    args = ap.parse_args()
+    args.warmup = max(3, args.warmup)
+    ws, rank, local = dist_env()
+    if args.impl == "reference":
+        run_reference(args, ws, rank)
+    else:
+        run_ours(args, ws, rank, local)
+
+
+if __name__ == "__main__":
+    main()
