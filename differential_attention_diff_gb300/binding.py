@@ -35,6 +35,7 @@ EXPORTS = (
     "diffattn_v2_fwd",
     "diffattn_v2_fwd_workspace_size",
     "diffattn_v2_decode",
+    "diffattn_v2_decode_noalloc",
     "diffattn_v2_decode_num_splits",
     "diffattn_v2_decode_workspace_size",
     "diffattn_get_device_status",
@@ -123,7 +124,8 @@ def load(path: str = LIB_PATH):
         lib.diffattn_status_string.argtypes = [C.c_int]
         for name, st in (("diffattn_v1_fwd", da_v1_fwd_params), ("diffattn_v1_bwd", da_v1_bwd_params),
                          ("diffattn_v2_gate", da_v2_gate_params), ("diffattn_v2_fwd", da_v2_fwd_params),
-                         ("diffattn_v2_decode", da_v2_decode_params)):
+                         ("diffattn_v2_decode", da_v2_decode_params),
+                         ("diffattn_v2_decode_noalloc", da_v2_decode_params)):
             f = getattr(lib, name)
             f.restype = C.c_int
             f.argtypes = [C.POINTER(st), vp]
@@ -302,6 +304,26 @@ def diffattn_v2_decode(q, k_cache, v_cache, *, seqlens=None, gate=None, x=None, 
         _t4(v_cache), _ptr(seqlens), _ptr(gate), _ptr(x), _ptr(w_lambda), out.data_ptr(),
         int(num_splits), workspace.data_ptr(), workspace.numel() * workspace.element_size())
     _check(lib.diffattn_v2_decode(C.byref(p), _stream(stream)), "diffattn_v2_decode")
+    return out
+
+
+def diffattn_v2_decode_noalloc(q, k_cache, v_cache, *, seqlens=None, gate=None, x=None,
+                               w_lambda=None, out=None, num_splits=0, softmax_scale=0.0,
+                               stream=None):
+    """V2 decode through the entry point that takes no workspace (its scratch
+    is a fixed array inside the library; see include/diffattn.h)."""
+    lib = load()
+    B, H2, d = q.shape
+    h = H2 // 2
+    L_max, hkv = k_cache.shape[1], k_cache.shape[2]
+    if out is None:
+        out = torch.empty((B, h, d), dtype=q.dtype, device=q.device)
+    d_model = 0 if x is None else x.shape[-1]
+    p = da_v2_decode_params(
+        B, h, hkv, d, L_max, d_model, float(softmax_scale), q.data_ptr(), _t4(k_cache),
+        _t4(v_cache), _ptr(seqlens), _ptr(gate), _ptr(x), _ptr(w_lambda), out.data_ptr(),
+        int(num_splits), None, 0)
+    _check(lib.diffattn_v2_decode_noalloc(C.byref(p), _stream(stream)), "diffattn_v2_decode_noalloc")
     return out
 
 

@@ -143,7 +143,7 @@ da_status diffattn_v1_bwd(const da_v1_bwd_params* p, void* cuda_stream);
  *   gate[t, p] = sigmoid(sum_k x[t, k] * w_lambda[k, p])
  * x: bf16 [T, d_model], row stride x_stride (elements, multiple of 8);
  * w_lambda: bf16 [d_model, h] row-major contiguous; gate: fp32 [T, h]
- * contiguous.  Supported: d_model % 64 == 0, h % 8 == 0, h <= 64. */
+ * contiguous.  Supported: d_model % 64 == 0, h <= 64. */
 typedef struct {
   int T, d_model, h;
   const void* x;
@@ -221,6 +221,33 @@ size_t diffattn_v2_decode_workspace_size(int B, int h, int h_kv, int d,
                                          int L_max, int num_splits,
                                          int gate_given);
 da_status diffattn_v2_decode(const da_v2_decode_params* p, void* cuda_stream);
+
+/* ------------------------------------------------------------------------ */
+/* V2 decode that allocates nothing and takes no workspace.  The method pages
+ * have no counterpart: this is a service for callers that cannot allocate
+ * device memory at all — an inference runtime that carves its memory once at
+ * start-up and forbids allocation inside the token loop, a program driving
+ * the GPU through a context it does not own, a plugin whose host framework
+ * hands it inputs and outputs but no scratch buffers.
+ *
+ * Same parameters and result as diffattn_v2_decode; `workspace` and
+ * `workspace_bytes` are ignored.  The split partials (and the gate, when it
+ * is computed from x) go to one fixed device array of
+ * DIFFATTN_NOALLOC_SCRATCH_BYTES inside the library, which every GPU that
+ * loads the library keeps until the process exits.  With num_splits = 0 the
+ * usual split count is lowered until the partials fit; a problem that needs
+ * more than the array even with one split (or an explicit num_splits that
+ * does not fit) returns DA_ERR_WORKSPACE without launching — use
+ * diffattn_v2_decode with a workspace for those.
+ *
+ * The first call on a device looks up the array's device address once (a
+ * CUDA runtime query with that device current); make that first call before
+ * any stream capture begins.  All calls share the array and each call
+ * overwrites what the previous one left there (nothing needs to start at
+ * zero), so calls that may overlap on the GPU — other streams, other host
+ * threads — race and must be serialised by the caller. */
+#define DIFFATTN_NOALLOC_SCRATCH_BYTES ((size_t)16 << 20)
+da_status diffattn_v2_decode_noalloc(const da_v2_decode_params* p, void* cuda_stream);
 
 /* ------------------------------------------------------------------------ */
 /* Device status word.  Kernels record the first error they detect (a bounded
