@@ -29,6 +29,7 @@ DA_F32, DA_BF16 = 0, 1
 EXPORTS = (
     "diffattn_lambda_init",
     "diffattn_v1_fwd",
+    "diffattn_v1_fwd_workspace_size",
     "diffattn_v1_bwd",
     "diffattn_v1_bwd_workspace_size",
     "diffattn_v2_gate",
@@ -64,7 +65,8 @@ class da_v1_fwd_params(C.Structure):
                 ("q1", da_t4), ("q2", da_t4), ("k1", da_t4), ("k2", da_t4), ("v", da_t4),
                 ("lq1", C.c_void_p), ("lk1", C.c_void_p), ("lq2", C.c_void_p), ("lk2", C.c_void_p),
                 ("out", da_t4), ("lse1", C.c_void_p), ("lse2", C.c_void_p), ("rstd", C.c_void_p),
-                ("o2", da_t4), ("lambda_out", C.c_void_p)]
+                ("o2", da_t4), ("lambda_out", C.c_void_p),
+                ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t)]
 
 
 class da_v1_bwd_params(C.Structure):
@@ -129,6 +131,8 @@ def load(path: str = LIB_PATH):
             f = getattr(lib, name)
             f.restype = C.c_int
             f.argtypes = [C.POINTER(st), vp]
+        lib.diffattn_v1_fwd_workspace_size.restype = C.c_size_t
+        lib.diffattn_v1_fwd_workspace_size.argtypes = [C.c_int] * 6
         lib.diffattn_v1_bwd_workspace_size.restype = C.c_size_t
         lib.diffattn_v1_bwd_workspace_size.argtypes = [C.c_int] * 5
         lib.diffattn_v2_fwd_workspace_size.restype = C.c_size_t
@@ -188,7 +192,8 @@ def diffattn_lambda_init(layer: int) -> float:
 
 
 def diffattn_v1_fwd(q1, q2, k1, k2, v, lq1, lk1, lq2, lk2, lambda_init, *, out=None,
-                    causal=True, softmax_scale=0.0, rms_eps=1e-5, save=False, stream=None):
+                    causal=True, softmax_scale=0.0, rms_eps=1e-5, save=False, saves=None,
+                    workspace=None, stream=None):
     """V1 forward.  Returns ``out`` or, with save=True, ``(out, saves)`` where
     saves = dict(lse1, lse2, rstd, o2, lam) are the tensors the backward reads."""
     lib = load()
@@ -196,20 +201,25 @@ def diffattn_v1_fwd(q1, q2, k1, k2, v, lq1, lk1, lq2, lk2, lambda_init, *, out=N
     dv = v.shape[-1]
     if out is None:
         out = torch.empty((B, N, H, dv), dtype=v.dtype, device=v.device)
-    saves = None
-    if save:
+    if save and saves is None:
         f32 = dict(dtype=torch.float32, device=v.device)
         saves = dict(lse1=torch.empty((B, H, N), **f32), lse2=torch.empty((B, H, N), **f32),
                      rstd=torch.empty((B, H, N), **f32),
                      o2=torch.empty((B, N, H, dv), dtype=v.dtype, device=v.device),
                      lam=torch.empty((1,), **f32))
+    if not save:
+        saves = None
+    need = lib.diffattn_v1_fwd_workspace_size(B, N, H, dqk, dv, _dtype_code(q1))
+    if workspace is None and need:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=v.device)
     p = da_v1_fwd_params(
         B, N, H, dqk, dv, _dtype_code(q1), int(causal), float(softmax_scale), float(lambda_init),
         float(rms_eps), _t4(q1), _t4(q2), _t4(k1), _t4(k2), _t4(v), _ptr(lq1), _ptr(lk1),
         _ptr(lq2), _ptr(lk2), _t4(out),
         _ptr(saves["lse1"]) if saves else None, _ptr(saves["lse2"]) if saves else None,
         _ptr(saves["rstd"]) if saves else None, _t4(saves["o2"] if saves else None),
-        _ptr(saves["lam"]) if saves else None)
+        _ptr(saves["lam"]) if saves else None, _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size())
     _check(lib.diffattn_v1_fwd(C.byref(p), _stream(stream)), "diffattn_v1_fwd")
     return (out, saves) if save else out
 

@@ -198,6 +198,12 @@ da_status diffattn_v2_decode(const da_v2_decode_params* p, void* stream) {
 }
 
 // ----------------------------------------------------------- V1 fwd --------
+size_t diffattn_v1_fwd_workspace_size(int B, int N, int H, int d_qk, int d_v, da_dtype dtype) {
+  if (dtype != DA_BF16 || B <= 0 || N <= 0 || H <= 0 || d_qk <= 0 || d_v <= 0) return 0;
+  DevInfo d = device_info();
+  return align256(da::v1_fwd_workspace_bytes(d.ok ? d.num_sms : 0));
+}
+
 da_status diffattn_v1_fwd(const da_v1_fwd_params* p, void* stream) {
   if (p == nullptr) return DA_ERR_INVALID_ARG;
   if (p->B < 0 || p->N < 0 || p->H < 0 || p->d_qk <= 0 || p->d_v <= 0) return DA_ERR_INVALID_ARG;
@@ -221,11 +227,15 @@ da_status diffattn_v1_fwd(const da_v1_fwd_params* p, void* stream) {
     return cuda_status(da::launch_v1_fwd_f32(a, s));
   }
   if (p->d_qk != 128 || p->d_v != 256 || !p->causal) return DA_ERR_UNSUPPORTED;
+  const size_t need = da::v1_fwd_workspace_bytes(d.num_sms);
+  if (p->workspace == nullptr || p->workspace_bytes < need || !aligned(p->workspace, 256))
+    return DA_ERR_WORKSPACE;
   if (!da::tma_available()) return DA_ERR_CUDA;
   da::V1FwdArgs a{p->B, p->N, p->H, p->d_qk, p->d_v, p->causal, scale * kLog2e,
                   p->lambda_init, p->rms_eps, p->q1, p->q2, p->k1, p->k2, p->v,
                   p->out, p->o2, p->lq1, p->lk1, p->lq2, p->lk2, p->lse1, p->lse2,
-                  p->rstd, p->lambda_out, d.status, d.num_sms};
+                  p->rstd, p->lambda_out, p->workspace, p->workspace_bytes, d.status,
+                  d.num_sms};
   return cuda_status(da::launch_v1_fwd(a, s));
 }
 

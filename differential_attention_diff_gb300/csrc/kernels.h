@@ -64,9 +64,12 @@ struct V1FwdArgs {
   da_t4 q1, q2, k1, k2, v, out, o2;
   const float *lq1, *lk1, *lq2, *lk2;
   float *lse1, *lse2, *rstd, *lambda_out;
+  void* workspace;  // exchange slots of the CTA pairs
+  size_t workspace_bytes;
   uint32_t* status;
   int num_sms;
 };
+size_t v1_fwd_workspace_bytes(int num_sms);
 cudaError_t launch_v1_fwd(const V1FwdArgs& a, cudaStream_t s);
 
 // ---- V1 backward, bf16 -----------------------------------------------------

@@ -1,6 +1,5 @@
 #include "kernels.h"
 namespace da {
-cudaError_t launch_v1_fwd(const V1FwdArgs&, cudaStream_t) { return cudaErrorNotSupported; }
 size_t v1_bwd_workspace_bytes(int, int, int, int, int) { return 256; }
 cudaError_t launch_v1_bwd(const V1BwdArgs&, cudaStream_t) { return cudaErrorNotSupported; }
 }

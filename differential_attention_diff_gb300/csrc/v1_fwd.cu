@@ -1,0 +1,531 @@
+// v1_fwd.cu — V1 differential attention forward (bf16) on tcgen05 + TMEM + TMA
+// with 2-CTA clusters, sm_103a.
+//
+// "Differential Transformer | ICLR 2025 Oral" (dainus.ai), "Differential
+// Attention: 빼기의 힘":
+//     O = (softmax(s Q1 K1^T) - lambda softmax(s Q2 K2^T)) V
+// "Differential Transformer V2" (pogovet.com), §1: lambda is one scalar per
+// layer from dot products of four learnable vectors plus the per-layer init;
+// the V head dim is twice the Q/K head dim; per-head RMS normalisation after
+// the subtraction, then the per-layer scale (read as 1 - lambda_init).
+//
+// One stream per CTA.  A stream needs 2 x 128 TMEM columns of scores (double
+// buffered, so the next tile's Q K^T runs while the softmax works) plus 256
+// columns for its O accumulator (d_v = 256): the whole 512-column TMEM of an
+// SM.  So a work item (batch, head, 128 query rows) runs on a cluster of two
+// CTAs: rank 0 computes stream 1, rank 1 stream 2, each from its own TMA
+// loads (V is read by both; the second read mostly hits L2).  In the
+// epilogue each CTA keeps half of the 256 output columns: it hands the other
+// half of its O/l to the partner through a 64 KB per-CTA slot of the
+// workspace (L2-resident), forms O = O1/l1 - lambda O2/l2 on its half, swaps
+// the per-row partial sums of squares with the partner through distributed
+// shared memory, and writes Y = (1 - lambda_init) O / sqrt(mean O^2 + eps).
+// Every hand-off is an mbarrier with a bounded wait (remote arrives at
+// cluster scope).
+//
+//   TMEM: [0,128) S / P buffer 0, [128,256) S / P buffer 1, [256,512) O.
+//   SMEM: Q (32 KB), K ring 2 x 32 KB, V ring 2 x 64 KB (128-byte swizzle).
+//   warps 0-3: softmax + epilogue (thread = query row = TMEM lane);
+//   warp 4: TMA producer; warp 5: MMA issuer (one lane).
+#include "kernels.h"
+#include "tma.cuh"
+
+namespace da {
+namespace {
+
+constexpr int kBM = 128, kBN = 128, kDqk = 128, kDv = 256;
+constexpr int kThreads = 192;
+constexpr int kBox = 128 * 128;  // one 64-column box of 128 rows (bf16)
+constexpr int kOffQ = 0;                      // 2 boxes
+constexpr int kOffK = 2 * kBox;               // [stage][2 boxes]
+constexpr int kOffV = 6 * kBox;               // [stage][4 boxes]
+constexpr int kOffBar = 14 * kBox;            // 229376
+constexpr int kSmemBytes = kOffBar + 1024 + 1024;
+constexpr size_t kSlotBytes = 128 * 128 * sizeof(float);  // per CTA exchange slot
+
+enum {
+  B_QFULL = 0, B_QEMPTY, B_KFULL, B_KFULL1, B_KEMPTY, B_KEMPTY1, B_VFULL, B_VFULL1,
+  B_VEMPTY, B_VEMPTY1, B_SFULL, B_SFULL1, B_PFULL, B_PFULL1, B_ORDY, B_ODONE, B_DATA, B_SSQ,
+  B_COUNT
+};
+
+constexpr uint32_t kIdescS = idesc_bf16(128, 128, 0);
+constexpr uint32_t kIdescPV = idesc_bf16(128, 256, 1);
+
+struct Shared {
+  uint32_t base;
+  uint8_t* gen;
+  __device__ uint32_t bar(int i) const { return base + kOffBar + 8 * i; }
+  __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(gen + kOffBar + 256); }
+  __device__ volatile int* abort_flag() const {
+    return reinterpret_cast<volatile int*>(gen + kOffBar + 264);
+  }
+  __device__ float* lam() const { return reinterpret_cast<float*>(gen + kOffBar + 268); }
+  __device__ uint32_t ssq_rx() const { return base + kOffBar + 512; }  // float[128]
+  __device__ float* ssq_rx_ptr() const { return reinterpret_cast<float*>(gen + kOffBar + 512); }
+};
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+__device__ __forceinline__ bool try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+template <bool kCluster = false>
+__device__ __forceinline__ bool wait_bar(const Shared& sh, uint32_t bar, uint32_t parity,
+                                         uint32_t* status, uint32_t site) {
+  auto poll = [&]() { return kCluster ? try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+  if (poll()) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (poll()) return true;
+    if (*sh.abort_flag()) return false;
+    if (globaltimer() - t0 > 2000000000ull) {
+      record_status(status, DA_ERR_TIMEOUT, site);
+      *sh.abort_flag() = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void remote_arrive(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+               : "memory");
+}
+__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
+  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+
+struct Item {
+  int b, h, mt, n_kv;
+};
+__device__ __forceinline__ Item item_of(int i, int units, int H, int n_mtiles) {
+  Item it;
+  it.mt = n_mtiles - 1 - i / units;
+  const int u = i % units;
+  it.b = u / H;
+  it.h = u % H;
+  it.n_kv = it.mt + 1;
+  return it;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__ CUtensorMap tm_q2,
+              const __grid_constant__ CUtensorMap tm_k1, const __grid_constant__ CUtensorMap tm_k2,
+              const __grid_constant__ CUtensorMap tm_v, V1FwdArgs a, float* __restrict__ xchg) {
+  extern __shared__ uint8_t smem_raw[];
+  Shared sh;
+  {
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t al = (raw + 1023u) & ~1023u;
+    sh.base = al;
+    sh.gen = smem_raw + (al - raw);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();         // 0: stream 1, 1: stream 2
+  const uint32_t partner = rank ^ 1u;
+  const int cluster_id = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
+  const int n_mtiles = (a.N + kBM - 1) / kBM;
+  const int units = a.B * a.H;
+  const int n_items = n_mtiles * units;
+  const CUtensorMap* tq = rank == 0 ? &tm_q1 : &tm_q2;
+  const CUtensorMap* tk = rank == 0 ? &tm_k1 : &tm_k2;
+
+  if (threadIdx.x == 0) {
+    mbar_init(sh.bar(B_QFULL), 1);
+    mbar_init(sh.bar(B_QEMPTY), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(sh.bar(B_KFULL + s), 1);
+      mbar_init(sh.bar(B_KEMPTY + s), 1);
+      mbar_init(sh.bar(B_VFULL + s), 1);
+      mbar_init(sh.bar(B_VEMPTY + s), 1);
+      mbar_init(sh.bar(B_SFULL + s), 1);
+      mbar_init(sh.bar(B_PFULL + s), 128);
+    }
+    mbar_init(sh.bar(B_ORDY), 1);
+    mbar_init(sh.bar(B_ODONE), 1);
+    mbar_init(sh.bar(B_DATA), 128);
+    mbar_init(sh.bar(B_SSQ), 128);
+    *sh.abort_flag() = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    // lambda = exp(lq1 . lk1) - exp(lq2 . lk2) + lambda_init
+    float d1 = 0.f, d2 = 0.f;
+    for (int x = lane; x < a.d_qk; x += 32) {
+      d1 = fmaf(a.lq1[x], a.lk1[x], d1);
+      d2 = fmaf(a.lq2[x], a.lk2[x], d2);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      d1 += __shfl_xor_sync(0xffffffffu, d1, o);
+      d2 += __shfl_xor_sync(0xffffffffu, d2, o);
+    }
+    if (lane == 0) {
+      const float lam = expf(d1) - expf(d2) + a.lambda_init;
+      *sh.lam() = lam;
+      if (a.lambda_out && blockIdx.x == 0) *a.lambda_out = lam;
+    }
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(sh.tmem_slot()), 512);
+    tmem_relinquish();
+  }
+  if (warp == 4 && lane == 0) {
+    prefetch_tmap(tq);
+    prefetch_tmap(tk);
+    prefetch_tmap(&tm_v);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // the partner's barriers are initialised before any remote arrive
+  tc_fence_after();
+  const uint32_t tmem = *sh.tmem_slot();
+
+  if (warp == 4) {
+    // ------------------------------------------------------ TMA producer --
+    if (lane == 0) {
+      int kv = 0, it = 0;
+      bool ok = true;
+      for (int i = cluster_id; i < n_items && ok; i += n_clusters, ++it) {
+        const Item w = item_of(i, units, a.H, n_mtiles);
+        if (it > 0 && !wait_bar(sh, sh.bar(B_QEMPTY), (it - 1) & 1, a.status, 0x3001)) { ok = false; break; }
+        mbar_arrive_expect_tx(sh.bar(B_QFULL), 2 * kBox);
+        for (int box = 0; box < 2; ++box)
+          tma_load_4d(sh.base + kOffQ + box * kBox, tq, sh.bar(B_QFULL), box * 64, w.h, w.mt * kBM, w.b);
+        for (int j = 0; j < w.n_kv; ++j, ++kv) {
+          const int st = kv & 1, use = kv >> 1;
+          if (use > 0 && !wait_bar(sh, sh.bar(B_KEMPTY + st), (use - 1) & 1, a.status, 0x3002)) { ok = false; break; }
+          mbar_arrive_expect_tx(sh.bar(B_KFULL + st), 2 * kBox);
+          for (int box = 0; box < 2; ++box)
+            tma_load_4d(sh.base + kOffK + (st * 2 + box) * kBox, tk, sh.bar(B_KFULL + st), box * 64,
+                        w.h, j * kBN, w.b);
+          if (use > 0 && !wait_bar(sh, sh.bar(B_VEMPTY + st), (use - 1) & 1, a.status, 0x3003)) { ok = false; break; }
+          mbar_arrive_expect_tx(sh.bar(B_VFULL + st), 4 * kBox);
+          for (int box = 0; box < 4; ++box)
+            tma_load_4d(sh.base + kOffV + (st * 4 + box) * kBox, &tm_v, sh.bar(B_VFULL + st),
+                        box * 64, w.h, j * kBN, w.b);
+        }
+      }
+      if (!ok) {
+        // bounded drain of the loads that may still be in flight
+        const uint64_t t0 = globaltimer();
+        while (globaltimer() - t0 < 200000000ull) {
+        }
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------- MMA issuer ---
+    if (lane == 0) {
+      int kv = 0, it = 0;
+      bool ok = true;
+      const uint32_t t_o = tmem + 256;
+      auto issue_s = [&](int g) {  // S of global tile g into buffer g & 1
+        const int st = g & 1;
+        const uint32_t kb = sh.base + kOffK + st * 2 * kBox;
+        const uint32_t qa = sh.base + kOffQ;
+#pragma unroll
+        for (int kk = 0; kk < kDqk / 16; ++kk) {
+          const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+          tc_mma_ss(tmem + (g & 1) * 128, sdesc_sw128(qa + off, 16, 1024),
+                    sdesc_sw128(kb + off, 16, 1024), kIdescS, kk > 0);
+        }
+      };
+      auto wait_k = [&](int g) {
+        return wait_bar(sh, sh.bar(B_KFULL + (g & 1)), (g >> 1) & 1, a.status, 0x3102);
+      };
+      for (int i = cluster_id; i < n_items && ok; i += n_clusters, ++it) {
+        const Item w = item_of(i, units, a.H, n_mtiles);
+        const int n = w.n_kv;
+        if (!wait_bar(sh, sh.bar(B_QFULL), it & 1, a.status, 0x3101)) { ok = false; break; }
+        tc_fence_after();
+        for (int j = 0; j < 2 && j < n; ++j) {
+          if (!wait_k(kv + j)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(kv + j);
+          tc_commit(sh.bar(B_KEMPTY + ((kv + j) & 1)));
+          tc_commit(sh.bar(B_SFULL + ((kv + j) & 1)));
+          if (j == n - 1) tc_commit(sh.bar(B_QEMPTY));
+        }
+        if (!ok) break;
+        for (int j = 0; j < n; ++j) {
+          const int g = kv + j, st = g & 1;
+          if (!wait_bar(sh, sh.bar(B_PFULL + st), (g >> 1) & 1, a.status, 0x3103)) { ok = false; break; }
+          if (!wait_bar(sh, sh.bar(B_VFULL + st), (g >> 1) & 1, a.status, 0x3104)) { ok = false; break; }
+          tc_fence_after();
+          const uint32_t vb = sh.base + kOffV + st * 4 * kBox;
+#pragma unroll
+          for (int kk = 0; kk < kBN / 16; ++kk)
+            tc_mma_ts(t_o, tmem + st * 128 + kk * 8, sdesc_sw128(vb + kk * 2048, kBox, 1024),
+                      kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+          tc_commit(sh.bar(B_VEMPTY + st));
+          tc_commit(sh.bar(B_ODONE));
+          if (j + 2 < n) {
+            if (!wait_k(g + 2)) { ok = false; break; }
+            tc_fence_after();
+            issue_s(g + 2);
+            tc_commit(sh.bar(B_KEMPTY + st));
+            tc_commit(sh.bar(B_SFULL + st));
+            if (j + 2 == n - 1) tc_commit(sh.bar(B_QEMPTY));
+          }
+        }
+        if (!ok) break;
+        tc_commit(sh.bar(B_ORDY));
+        kv += n;
+      }
+    }
+  } else {
+    // --------------------------------------------- softmax + epilogue -----
+    const int row = warp * 32 + lane;  // query row within the item = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
+    const uint32_t t_o = tmem + lane_off + 256;
+    const float sl2 = a.scale_log2;
+    const float lam = *sh.lam();
+    const float cscale = 1.f - a.lambda_init;
+    float* my_slot = xchg + (static_cast<size_t>(cluster_id) * 2 + rank) * (kSlotBytes / 4) + row * 128;
+    const float* other_slot =
+        xchg + (static_cast<size_t>(cluster_id) * 2 + partner) * (kSlotBytes / 4) + row * 128;
+    const uint32_t partner_data = map_to_rank(sh.bar(B_DATA), partner);
+    const uint32_t partner_ssq_bar = map_to_rank(sh.bar(B_SSQ), partner);
+    const uint32_t partner_ssq_slot = map_to_rank(sh.ssq_rx() + row * 4, partner);
+    int kv = 0, it = 0;
+    bool ok = true;
+    for (int i = cluster_id; i < n_items && ok; i += n_clusters, ++it) {
+      const Item w = item_of(i, units, a.H, n_mtiles);
+      float m_run = -INFINITY, l_run = 0.f;
+      for (int j = 0; j < w.n_kv; ++j) {
+        const int g = kv + j;
+        const uint32_t t_s = tmem + lane_off + (g & 1) * 128;
+        if (!wait_bar(sh, sh.bar(B_SFULL + (g & 1)), (g >> 1) & 1, a.status, 0x3201)) { ok = false; break; }
+        tc_fence_after();
+        uint32_t s[128];
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          tmem_ld32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
+        tmem_ld_wait();
+        const bool diag = (j == w.mt);
+        float mx = -INFINITY;
+#pragma unroll
+        for (int e = 0; e < 128; ++e) {
+          float v = __uint_as_float(s[e]);
+          if (diag && e > row) {
+            v = -INFINITY;
+            s[e] = __float_as_uint(v);
+          }
+          mx = fmaxf(mx, v);
+        }
+        const float m_tile = mx * sl2;
+        const bool need = (j == 0) || (m_tile > m_run + 8.0f);
+        float alpha = 1.f;
+        if (need) {
+          const float m_new = fmaxf(m_run, m_tile);
+          alpha = (j == 0) ? 0.f : fast_exp2(m_run - m_new);
+          m_run = m_new;
+          l_run *= alpha;
+        }
+        if (j > 0 && __any_sync(0xffffffffu, need)) {
+          // PV(g - 1) may still run: wait for it before rescaling O
+          if (!wait_bar(sh, sh.bar(B_ODONE), (g - 1) & 1, a.status, 0x3202)) { ok = false; break; }
+          tc_fence_after();
+#pragma unroll 1
+          for (int c = 0; c < 8; ++c) {
+            uint32_t o[32];
+            tmem_ld32(t_o + c * 32, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+            tmem_st32(t_o + c * 32, o);
+          }
+        }
+        const float neg_m = -m_run;
+        float lsum = 0.f;
+#pragma unroll
+        for (int c = 0; c < 4; ++c) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) {
+            const float p0 = fast_exp2(fmaf(__uint_as_float(s[c * 32 + 2 * e]), sl2, neg_m));
+            const float p1 = fast_exp2(fmaf(__uint_as_float(s[c * 32 + 2 * e + 1]), sl2, neg_m));
+            lsum += p0 + p1;
+            s[c * 32 + e] = pack_bf16x2(p0, p1);
+          }
+        }
+        l_run += lsum;
+#pragma unroll
+        for (int c = 0; c < 4; ++c)
+          tmem_st16(t_s + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&s[c * 32]));
+        tmem_st_wait();
+        tc_fence_before();
+        mbar_arrive(sh.bar(B_PFULL + (g & 1)));
+      }
+      if (!ok) break;
+      kv += w.n_kv;
+      // ----------------------------------------------------- epilogue ----
+      if (!wait_bar(sh, sh.bar(B_ORDY), it & 1, a.status, 0x3203)) { ok = false; break; }
+      tc_fence_after();
+      const float inv_l = 1.f / l_run;
+      // (1) the partner's half of my normalised O -> my exchange slot
+      const int give = (1 - static_cast<int>(rank)) * 128, keep = static_cast<int>(rank) * 128;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32(t_o + give + c * 32, o);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          float4 v = make_float4(__uint_as_float(o[e]) * inv_l, __uint_as_float(o[e + 1]) * inv_l,
+                                 __uint_as_float(o[e + 2]) * inv_l, __uint_as_float(o[e + 3]) * inv_l);
+          __stcg(reinterpret_cast<float4*>(my_slot + c * 32 + e), v);
+        }
+      }
+      remote_arrive(partner_data);
+      if (!wait_bar<true>(sh, sh.bar(B_DATA), it & 1, a.status, 0x3204)) { ok = false; break; }
+      // (2) O = O1/l1 - lambda O2/l2 on my half; partial sum of squares
+      float dvals[128];
+      float ssq = 0.f;
+      const int n = w.mt * kBM + row;
+      const bool live = n < a.N;
+      __nv_bfloat16* o2dst = (a.o2.ptr && live)
+          ? static_cast<__nv_bfloat16*>(a.o2.ptr) + w.b * a.o2.sb + static_cast<int64_t>(n) * a.o2.sn +
+                w.h * a.o2.sh + keep
+          : nullptr;
+#pragma unroll
+      for (int c = 0; c < 4; ++c) {
+        uint32_t o[32];
+        tmem_ld32(t_o + keep + c * 32, o);
+        tmem_ld_wait();
+        float o2v[32];
+#pragma unroll
+        for (int e = 0; e < 32; e += 4) {
+          const float4 oth = __ldcg(reinterpret_cast<const float4*>(other_slot + c * 32 + e));
+          const float othv[4] = {oth.x, oth.y, oth.z, oth.w};
+#pragma unroll
+          for (int u = 0; u < 4; ++u) {
+            const float own = __uint_as_float(o[e + u]) * inv_l;
+            const float a1 = rank == 0 ? own : othv[u];
+            const float a2 = rank == 0 ? othv[u] : own;
+            const float dd = __fsub_rn(a1, __fmul_rn(lam, a2));
+            dvals[c * 32 + e + u] = dd;
+            ssq = fmaf(dd, dd, ssq);
+            o2v[e + u] = a2;
+          }
+        }
+        if (o2dst) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            uint4 pk;
+            pk.x = pack_bf16x2(o2v[e], o2v[e + 1]);
+            pk.y = pack_bf16x2(o2v[e + 2], o2v[e + 3]);
+            pk.z = pack_bf16x2(o2v[e + 4], o2v[e + 5]);
+            pk.w = pack_bf16x2(o2v[e + 6], o2v[e + 7]);
+            *reinterpret_cast<uint4*>(o2dst + c * 32 + e) = pk;
+          }
+        }
+      }
+      st_cluster_f32(partner_ssq_slot, ssq);
+      remote_arrive(partner_ssq_bar);
+      if (!wait_bar<true>(sh, sh.bar(B_SSQ), it & 1, a.status, 0x3205)) { ok = false; break; }
+      const float other_ssq = sh.ssq_rx_ptr()[row];
+      const float tot = rank == 0 ? ssq + other_ssq : other_ssq + ssq;
+      const float rstd = 1.f / sqrtf(tot * (1.f / kDv) + a.rms_eps);
+      const float cs = cscale * rstd;
+      if (live) {
+        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out.ptr) + w.b * a.out.sb +
+                             static_cast<int64_t>(n) * a.out.sn + w.h * a.out.sh + keep;
+#pragma unroll
+        for (int e = 0; e < 128; e += 8) {
+          uint4 pk;
+          pk.x = pack_bf16x2(__fmul_rn(dvals[e], cs), __fmul_rn(dvals[e + 1], cs));
+          pk.y = pack_bf16x2(__fmul_rn(dvals[e + 2], cs), __fmul_rn(dvals[e + 3], cs));
+          pk.z = pack_bf16x2(__fmul_rn(dvals[e + 4], cs), __fmul_rn(dvals[e + 5], cs));
+          pk.w = pack_bf16x2(__fmul_rn(dvals[e + 6], cs), __fmul_rn(dvals[e + 7], cs));
+          *reinterpret_cast<uint4*>(dst + e) = pk;
+        }
+        const int64_t sidx = (static_cast<int64_t>(w.b) * a.H + w.h) * a.N + n;
+        float* lse = rank == 0 ? a.lse1 : a.lse2;
+        if (lse) lse[sidx] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
+        if (rank == 0 && a.rstd) a.rstd[sidx] = rstd;
+      }
+      tc_fence_before();
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();  // no CTA leaves while its partner may still address its shared memory
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tmem, 512);
+}
+
+}  // namespace
+
+size_t v1_fwd_workspace_bytes(int num_sms) {
+  const int clusters = (num_sms > 0 ? num_sms : 152) / 2;
+  return static_cast<size_t>(clusters) * 2 * kSlotBytes;
+}
+
+cudaError_t launch_v1_fwd(const V1FwdArgs& a, cudaStream_t s) {
+  CUtensorMap tq1, tq2, tk1, tk2, tv;
+  if (!encode_tmap_bf16_4d(&tq1, a.q1, a.B, a.N, a.H, kDqk, kBM) ||
+      !encode_tmap_bf16_4d(&tq2, a.q2, a.B, a.N, a.H, kDqk, kBM) ||
+      !encode_tmap_bf16_4d(&tk1, a.k1, a.B, a.N, a.H, kDqk, kBN) ||
+      !encode_tmap_bf16_4d(&tk2, a.k2, a.B, a.N, a.H, kDqk, kBN) ||
+      !encode_tmap_bf16_4d(&tv, a.v, a.B, a.N, a.H, kDv, kBN))
+    return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(v1_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int n_items = ((a.N + kBM - 1) / kBM) * a.B * a.H;
+  // clusters of two CTAs; as many as fit at once (one CTA per SM)
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  int max_clusters = 0;
+  cfg.gridDim = dim3(2 * ((a.num_sms > 0 ? a.num_sms : 152) / 2), 1, 1);
+  e = cudaOccupancyMaxActiveClusters(&max_clusters, v1_fwd_kernel, &cfg);
+  if (e != cudaSuccess || max_clusters <= 0) max_clusters = (a.num_sms > 0 ? a.num_sms : 152) / 2;
+  const int ws_clusters = static_cast<int>(a.workspace_bytes / (2 * kSlotBytes));
+  int clusters = max_clusters;
+  if (clusters > ws_clusters) clusters = ws_clusters;
+  if (clusters > n_items) clusters = n_items;
+  if (clusters <= 0) return cudaErrorInvalidValue;
+  cfg.gridDim = dim3(2 * clusters, 1, 1);
+  return cudaLaunchKernelEx(&cfg, v1_fwd_kernel, tq1, tq2, tk1, tk2, tv, a,
+                            static_cast<float*>(a.workspace));
+}
+
+}  // namespace da

@@ -83,7 +83,10 @@ float diffattn_lambda_init(int layer);
  *   (1/sqrt(mean O^2 + eps)): fp32 [B, H, N] contiguous;
  *   o2 = softmax(s Q2 K2^T) V: [B, N, H, d_v] of `dtype`;
  *   lambda_out: fp32 [1].
- * No workspace. */
+ * workspace: the bf16 path runs each (batch, head, 128-row) tile on a pair
+ * of CTAs (one per softmax stream) that exchange half of their outputs
+ * through it; at least diffattn_v1_fwd_workspace_size(...) bytes, 256-byte
+ * aligned, contents on entry irrelevant (0 bytes for DA_F32). */
 typedef struct {
   int B, N, H, d_qk, d_v;
   da_dtype dtype;
@@ -97,8 +100,12 @@ typedef struct {
   float *lse1, *lse2, *rstd;
   da_t4 o2;
   float* lambda_out;
+  void* workspace;
+  size_t workspace_bytes;
 } da_v1_fwd_params;
 
+/* Workspace bytes diffattn_v1_fwd needs on the current device. */
+size_t diffattn_v1_fwd_workspace_size(int B, int N, int H, int d_qk, int d_v, da_dtype dtype);
 da_status diffattn_v1_fwd(const da_v1_fwd_params* p, void* cuda_stream);
 
 /* ------------------------------------------------------------------------ */

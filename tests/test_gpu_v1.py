@@ -1,0 +1,131 @@
+"""GPU parity through the C ABI for the V1 bf16 forward (tcgen05, 2-CTA
+clusters) against the fp64 oracle: small shapes spanning several 128-row
+tiles and ragged tails, layers across the lambda_init schedule, the saves
+the backward reads, exact cancellation, strided views, and the full-size
+workloads on sampled rows.  Bar: max|diff| <= 2e-2 * RMS(V) on Y and O2;
+LSE within 1e-2 (natural log units); rstd within 2e-2 relative."""
+
+import math
+
+import numpy as np
+import pytest
+import torch
+
+from differential_attention_diff_gb300 import binding as bd
+from differential_attention_diff_gb300 import synth
+from oracle import diffattn_oracle as orc
+
+pytestmark = pytest.mark.gpu
+TOL = 2e-2
+NAMES = ("q1", "q2", "k1", "k2", "v", "lq1", "lk1", "lq2", "lk2")
+
+
+def f64(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def rms(a):
+    return float(np.sqrt(np.mean(np.square(a))))
+
+
+@pytest.fixture(autouse=True)
+def _status_clean():
+    yield
+    assert bd.diffattn_get_device_status() == bd.DA_OK
+
+
+def _check(t, li, y, sv, rows=None, heads=None, batches=None):
+    B, N, H, _ = t["q1"].shape
+    heads = range(H) if heads is None else heads
+    batches = range(B) if batches is None else batches
+    yv = f64(y)
+    worst = 0.0
+    for b in batches:
+        for h in heads:
+            sl = lambda n: f64(t[n][b:b + 1, :, h:h + 1])  # noqa: E731
+            ref = orc.v1_forward(sl("q1"), sl("q2"), sl("k1"), sl("k2"), sl("v"),
+                                 *(f64(t[n]) for n in NAMES[5:]), float(np.float32(li)), rows=rows)
+            r = ref["rows"]
+            tol = TOL * rms(f64(t["v"][b, :, h]))
+            worst = max(worst, float(np.max(np.abs(yv[b, r, h] - ref["y"][0, :, 0]))) / tol)
+            if sv is not None:
+                worst = max(worst, float(np.max(np.abs(f64(sv["o2"][b, r, h]) - ref["o2"][0, :, 0]))) / tol)
+                assert np.max(np.abs(f64(sv["lse1"][b, h, r]) - ref["lse1"][0, 0])) <= 1e-2
+                assert np.max(np.abs(f64(sv["lse2"][b, h, r]) - ref["lse2"][0, 0])) <= 1e-2
+                assert np.max(np.abs(f64(sv["rstd"][b, h, r]) / ref["rstd"][0, 0] - 1)) <= 2e-2
+    assert worst <= 1.0, worst
+
+
+@pytest.mark.parametrize("B,N,H,layer", [(1, 200, 2, 1), (2, 384, 3, 2), (1, 129, 2, 14),
+                                          (1, 1, 1, 28), (1, 1000, 4, 5), (3, 256, 1, 1)])
+def test_v1_fwd_parity_small(B, N, H, layer):
+    t = synth.v1_inputs(B, N, H, 128, 256, "bf16", seed=4000 + N + H, device="cuda")
+    li = bd.diffattn_lambda_init(layer)
+    y, sv = bd.diffattn_v1_fwd(*(t[n] for n in NAMES), li, save=True)
+    torch.cuda.synchronize()
+    ref_lam = orc.lambda_full(*(f64(t[n]) for n in NAMES[5:]), float(np.float32(li)))
+    assert abs(float(sv["lam"][0]) - ref_lam) <= 1e-5
+    _check(t, li, y, sv)
+
+
+def test_v1_fwd_without_saves_matches():
+    t = synth.v1_inputs(1, 300, 2, 128, 256, "bf16", seed=51, device="cuda")
+    li = bd.diffattn_lambda_init(3)
+    y1 = bd.diffattn_v1_fwd(*(t[n] for n in NAMES), li)
+    y2, _ = bd.diffattn_v1_fwd(*(t[n] for n in NAMES), li, save=True)
+    torch.cuda.synchronize()
+    assert torch.equal(y1, y2)
+
+
+def test_v1_fwd_exact_cancellation():
+    """Q1 = Q2, K1 = K2 and lambda = exp(ln 2) - exp(0) + 0 = 1: the two CTAs of
+    a pair run identical arithmetic, so O and Y are exactly zero."""
+    t = synth.v1_inputs(1, 333, 2, 128, 256, "bf16", seed=52, device="cuda")
+    lq1 = torch.zeros(128, device="cuda")
+    lq1[0] = 1.0
+    lk1 = torch.zeros(128, device="cuda")
+    lk1[0] = math.log(2.0)
+    z = torch.zeros(128, device="cuda")
+    y, sv = bd.diffattn_v1_fwd(t["q1"], t["q1"], t["k1"], t["k1"], t["v"], lq1, lk1, z, z, 0.0,
+                               save=True)
+    torch.cuda.synchronize()
+    assert float(sv["lam"][0]) == 1.0
+    assert torch.count_nonzero(y).item() == 0
+
+
+def test_v1_fwd_strided_packed_views():
+    """q1/q2 and k1/k2 as views into packed [B, N, H, 2, d_qk] buffers."""
+    B, N, H = 1, 260, 2
+    g = torch.Generator(device="cuda").manual_seed(53)
+    qp = torch.randn((B, N, H, 2, 128), generator=g, device="cuda").to(torch.bfloat16)
+    kp = torch.randn((B, N, H, 2, 128), generator=g, device="cuda").to(torch.bfloat16)
+    v = torch.randn((B, N, H, 256), generator=g, device="cuda").to(torch.bfloat16)
+    lam = [0.1 * torch.randn(128, generator=g, device="cuda") for _ in range(4)]
+    t = dict(q1=qp[:, :, :, 0], q2=qp[:, :, :, 1], k1=kp[:, :, :, 0], k2=kp[:, :, :, 1], v=v,
+             lq1=lam[0], lk1=lam[1], lq2=lam[2], lk2=lam[3])
+    li = bd.diffattn_lambda_init(2)
+    y = bd.diffattn_v1_fwd(*(t[n] for n in NAMES), li)
+    torch.cuda.synchronize()
+    _check(t, li, y, None)
+
+
+@pytest.mark.parametrize("layer", [1, 28])
+def test_v1_fwd_full_size_b4_h12_n4096(layer):
+    """B4 H12 N4096, d_qk 128 / d_v 256 (the V1 forward workload) on sampled
+    rows of sampled heads, including tile edges and the last row."""
+    t = synth.v1_inputs(4, 4096, 12, 128, 256, "bf16", seed=1002, device="cuda")
+    li = bd.diffattn_lambda_init(layer)
+    y, sv = bd.diffattn_v1_fwd(*(t[n] for n in NAMES), li, save=True)
+    torch.cuda.synchronize()
+    rows = np.array([0, 1, 127, 128, 2047, 2048, 4094, 4095, 1234, 3333])
+    _check(t, li, y, sv, rows=rows, heads=[0, 7, 11], batches=[0, 3])
+
+
+def test_v1_fwd_full_size_b1_h16_n8192():
+    """B1 H16 N8192 (the forward of the training-step workload), sampled rows."""
+    t = synth.v1_inputs(1, 8192, 16, 128, 256, "bf16", seed=1005, device="cuda")
+    li = bd.diffattn_lambda_init(1)
+    y, sv = bd.diffattn_v1_fwd(*(t[n] for n in NAMES), li, save=True)
+    torch.cuda.synchronize()
+    rows = np.array([0, 127, 128, 4096, 8191, 5000])
+    _check(t, li, y, sv, rows=rows, heads=[0, 15])
