@@ -25,9 +25,10 @@
 //
 //   TMEM: [0,128) S / P buffer 0, [128,256) S / P buffer 1, [256,512) O.
 //   SMEM: Q (32 KB), K ring 2 x 32 KB, V ring 2 x 64 KB (128-byte swizzle).
-//   warps 0-3: softmax + epilogue (thread = query row = TMEM lane);
+//   warps 0-3: softmax (softmax.cuh) + epilogue (thread = query row = TMEM lane);
 //   warp 4: TMA producer; warp 5: MMA issuer (one lane).
 #include "kernels.h"
+#include "softmax.cuh"
 #include "tma.cuh"
 
 namespace da {
@@ -126,10 +127,15 @@ __device__ __forceinline__ void cluster_sync() {
 struct Item {
   int b, h, mt, n_kv;
 };
-__device__ __forceinline__ Item item_of(int i, int units, int H, int n_mtiles) {
+// Items are taken in blocks of `ub` (batch, head) units whose K1, K2 and V
+// fit in L2 together; inside a block, heaviest causal rows first.
+__device__ __forceinline__ Item item_of(int i, int units, int H, int n_mtiles, int ub) {
+  const int per_blk = n_mtiles * ub;
+  const int blk = i / per_blk, r = i - blk * per_blk;
+  const int bsize = min(ub, units - blk * ub);
   Item it;
-  it.mt = n_mtiles - 1 - i / units;
-  const int u = i % units;
+  it.mt = n_mtiles - 1 - r / bsize;
+  const int u = blk * ub + r % bsize;
   it.b = u / H;
   it.h = u % H;
   it.n_kv = it.mt + 1;
@@ -155,6 +161,8 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
   const int n_mtiles = (a.N + kBM - 1) / kBM;
   const int units = a.B * a.H;
   const int n_items = n_mtiles * units;
+  // units per L2 block: K1 + K2 + V of one (batch, head) is N * 512 * 2 bytes
+  const int ub = max(1, min(units, static_cast<int>((48ll << 20) / (static_cast<long long>(a.N) * 1024))));
   const CUtensorMap* tq = rank == 0 ? &tm_q1 : &tm_q2;
   const CUtensorMap* tk = rank == 0 ? &tm_k1 : &tm_k2;
 
@@ -215,7 +223,7 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
       int kv = 0, it = 0;
       bool ok = true;
       for (int i = cluster_id; i < n_items && ok; i += n_clusters, ++it) {
-        const Item w = item_of(i, units, a.H, n_mtiles);
+        const Item w = item_of(i, units, a.H, n_mtiles, ub);
         if (it > 0 && !wait_bar(sh, sh.bar(B_QEMPTY), (it - 1) & 1, a.status, 0x3001)) { ok = false; break; }
         mbar_arrive_expect_tx(sh.bar(B_QFULL), 2 * kBox);
         for (int box = 0; box < 2; ++box)
@@ -262,7 +270,7 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
         return wait_bar(sh, sh.bar(B_KFULL + (g & 1)), (g >> 1) & 1, a.status, 0x3102);
       };
       for (int i = cluster_id; i < n_items && ok; i += n_clusters, ++it) {
-        const Item w = item_of(i, units, a.H, n_mtiles);
+        const Item w = item_of(i, units, a.H, n_mtiles, ub);
         const int n = w.n_kv;
         if (!wait_bar(sh, sh.bar(B_QFULL), it & 1, a.status, 0x3101)) { ok = false; break; }
         tc_fence_after();
@@ -318,39 +326,15 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
     int kv = 0, it = 0;
     bool ok = true;
     for (int i = cluster_id; i < n_items && ok; i += n_clusters, ++it) {
-      const Item w = item_of(i, units, a.H, n_mtiles);
+      const Item w = item_of(i, units, a.H, n_mtiles, ub);
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < w.n_kv; ++j) {
         const int g = kv + j;
         const uint32_t t_s = tmem + lane_off + (g & 1) * 128;
         if (!wait_bar(sh, sh.bar(B_SFULL + (g & 1)), (g >> 1) & 1, a.status, 0x3201)) { ok = false; break; }
         tc_fence_after();
-        uint32_t s[128];
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          tmem_ld32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
-        tmem_ld_wait();
-        const bool diag = (j == w.mt);
-        float mx = -INFINITY;
-#pragma unroll
-        for (int e = 0; e < 128; ++e) {
-          float v = __uint_as_float(s[e]);
-          if (diag && e > row) {
-            v = -INFINITY;
-            s[e] = __float_as_uint(v);
-          }
-          mx = fmaxf(mx, v);
-        }
-        const float m_tile = mx * sl2;
-        const bool need = (j == 0) || (m_tile > m_run + 8.0f);
-        float alpha = 1.f;
-        if (need) {
-          const float m_new = fmaxf(m_run, m_tile);
-          alpha = (j == 0) ? 0.f : fast_exp2(m_run - m_new);
-          m_run = m_new;
-          l_run *= alpha;
-        }
-        if (j > 0 && __any_sync(0xffffffffu, need)) {
+        const float alpha = softmax_tile(t_s, row, j == 0, j == w.mt, sl2, m_run, l_run);
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
           // PV(g - 1) may still run: wait for it before rescaling O
           if (!wait_bar(sh, sh.bar(B_ODONE), (g - 1) & 1, a.status, 0x3202)) { ok = false; break; }
           tc_fence_after();
@@ -364,22 +348,6 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
             tmem_st32(t_o + c * 32, o);
           }
         }
-        const float neg_m = -m_run;
-        float lsum = 0.f;
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float p0 = fast_exp2(fmaf(__uint_as_float(s[c * 32 + 2 * e]), sl2, neg_m));
-            const float p1 = fast_exp2(fmaf(__uint_as_float(s[c * 32 + 2 * e + 1]), sl2, neg_m));
-            lsum += p0 + p1;
-            s[c * 32 + e] = pack_bf16x2(p0, p1);
-          }
-        }
-        l_run += lsum;
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          tmem_st16(t_s + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&s[c * 32]));
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(sh.bar(B_PFULL + (g & 1)));

@@ -23,8 +23,9 @@
 //     from TMEM, V from shared memory), interleaving the two heads so that
 //     one head's softmax overlaps the other head's MMAs.
 //   warps 0-3 / 4-7: softmax of the even / odd head, one thread per query row
-//     (TMEM lane): row max, lazy rescale of O (only when the running max grows
-//     by more than 2^8), exp2, row sum, P written back to TMEM as bf16.
+//     (TMEM lane): online softmax per tile (softmax.cuh: the row max of the
+//     first tile, a guarded stale max afterwards), P written back to TMEM as
+//     bf16, O rescaled in TMEM on the rare tiles that raise the max.
 //     The same threads run the epilogue: O_even / l_even - gate * O_odd /
 //     l_odd, bf16 store, optional log-sum-exp.
 //
@@ -32,6 +33,7 @@
 // DA_ERR_TIMEOUT in the status word, raises a shared abort flag so the other
 // roles leave too, drains its TMA loads and frees TMEM before returning.
 #include "kernels.h"
+#include "softmax.cuh"
 #include "tma.cuh"
 
 namespace da {
@@ -293,33 +295,8 @@ v2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       for (int j = 0; j < w.n_kv; ++j, ++sc) {
         if (!wait_bar(sh, sh.bar(B_SFULL + wg), sc & 1, a.status, 0x2201 + wg)) { ok = false; break; }
         tc_fence_after();
-        uint32_t s[128];
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          tmem_ld32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
-        tmem_ld_wait();
-        const bool diag = (j == w.mt);
-        float mx = -INFINITY;
-#pragma unroll
-        for (int e = 0; e < 128; ++e) {
-          float v = __uint_as_float(s[e]);
-          if (diag && e > row) {
-            v = -INFINITY;
-            s[e] = __float_as_uint(v);
-          }
-          mx = fmaxf(mx, v);
-        }
-        const float m_tile = mx * sl2;
-        // lazy rescale: keep the stale max unless the new one exceeds it by > 8
-        const bool need = (j == 0) || (m_tile > m_run + 8.0f);
-        float alpha = 1.f;
-        if (need) {
-          const float m_new = fmaxf(m_run, m_tile);
-          alpha = (j == 0) ? 0.f : fast_exp2(m_run - m_new);
-          m_run = m_new;
-          l_run *= alpha;
-        }
-        if (j > 0 && __any_sync(0xffffffffu, need)) {
+        const float alpha = softmax_tile(t_s, row, j == 0, j == w.mt, sl2, m_run, l_run);
+        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
           // O is stable here: the commit that signalled S(j) covers PV(j-1).
 #pragma unroll 1
           for (int c = 0; c < 4; ++c) {
@@ -331,24 +308,6 @@ v2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             tmem_st32(t_o + c * 32, o);
           }
         }
-        const float neg_m = -m_run;
-        float lsum = 0.f;
-        // P = exp2(s * scale - m), packed in place: chunk c (32 scores) becomes
-        // 16 bf16x2 words in s[c*32 .. c*32+15] = TMEM columns c*16 .. c*16+15
-#pragma unroll
-        for (int c = 0; c < 4; ++c) {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) {
-            const float p0 = fast_exp2(fmaf(__uint_as_float(s[c * 32 + 2 * e]), sl2, neg_m));
-            const float p1 = fast_exp2(fmaf(__uint_as_float(s[c * 32 + 2 * e + 1]), sl2, neg_m));
-            lsum += p0 + p1;
-            s[c * 32 + e] = pack_bf16x2(p0, p1);
-          }
-        }
-        l_run += lsum;
-#pragma unroll
-        for (int c = 0; c < 4; ++c)
-          tmem_st16(t_s + c * 16, *reinterpret_cast<const uint32_t(*)[16]>(&s[c * 32]));
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(sh.bar(B_PFULL + wg));
