@@ -1,0 +1,750 @@
+// v1_bwd.cu — V1 differential attention backward (bf16) on tcgen05 + TMEM +
+// TMA with 2-CTA clusters, sm_103a.
+//
+// The method pages ("Differential Transformer | ICLR 2025 Oral", dainus.ai,
+// "Differential Attention: 빼기의 힘"; "Differential Transformer V2",
+// pogovet.com, §1) define the forward; this is its chain rule.  With
+// c = 1 - lambda_init, Yhat = Y / c = O * rstd, G = dY, s = softmax scale:
+//   dO  = c * rstd * (G - Yhat * mean(G * Yhat))        (RMSNorm backward)
+//   D1  = <dO, A1 V> = <dO, O + lambda O2>,   D2 = <dO, A2 V>
+//   dP  = dO V^T  (shared by both streams)
+//   dS1 = A1 (dP - D1),   dS2 = -lambda A2 (dP - D2)
+//   dQt = s dSt Kt,  dKt = s dSt^T Qt,  dV = (A1 - lambda A2)^T dO
+//   dlambda = -sum D2;  lambda = e^a - e^b + lambda_init with a = lq1.lk1,
+//   b = lq2.lk2:  dlq1 = dlambda e^a lk1, dlk1 = dlambda e^a lq1,
+//   dlq2 = -dlambda e^b lk2, dlk2 = -dlambda e^b lq2.
+//
+// Three launches:
+//  1. preprocess (one warp per row): dO (bf16, workspace), D1, D2, the LSEs in
+//     log2 units (padded to whole 64-row tiles), zeroed dQ accumulators, and
+//     per-block partial sums of -D2 for dlambda;
+//  2. main (tcgen05): a work item is (batch, head, 128-key tile); a cluster
+//     of two CTAs runs it, rank 0 for stream 1 and rank 1 for stream 2.  Each
+//     CTA keeps its K tile and the V tile in shared memory and walks the
+//     64-row query tiles at and after the diagonal:
+//        S^T  = K Q^T          (TMEM, 64 columns)
+//        dP^T = V dO^T         (TMEM, 64 columns)
+//        softmax warps (thread = key row): P = exp2(S^T s log2e - lse2),
+//          dS^T = sigma s P (dP^T - D), Psig^T = sigma P  (sigma = 1 or
+//          -lambda), both as bf16 rows into shared memory
+//        dQ^T = K^T dS^T       (TMEM, reusing the dP^T columns) -> fp32
+//                               reductions into the workspace
+//        dV  += Psig^T dO      (TMEM, 256 columns)
+//        dK  += dS^T Q         (TMEM, 128 columns)
+//     At the end each CTA writes its dK; the dV halves of the two streams are
+//     summed through distributed shared memory and written as bf16;
+//  3. finalize: dQ accumulators -> bf16, and the lambda-vector gradients.
+//
+// TMEM: [0,256) dV, [256,384) dK, [384,448) S^T, [448,512) dP^T / dQ^T.
+// SMEM: K 32 KB, V 64 KB, 2 stages of (Q 16 KB, dO 32 KB), Psig^T and dS^T
+//       16 KB each, lse2 and D of both stages (1 KB); every operand in 128-byte-swizzled
+//       64-column boxes (used K-major or MN-major by the MMAs as needed).
+#include "kernels.h"
+#include "tma.cuh"
+
+namespace da {
+namespace {
+
+constexpr int kKT = 128;   // keys per item
+constexpr int kQT = 64;    // queries per iteration
+constexpr int kDqk = 128, kDv = 256;
+constexpr int kThreads = 192;
+
+constexpr int kBoxK = 128 * 128;   // 64 columns x 128 rows of bf16
+constexpr int kBoxQ = 64 * 128;    // 64 columns x 64 rows
+constexpr int kOffK = 0;                           // 2 boxes  (32 KB)
+constexpr int kOffV = kOffK + 2 * kBoxK;           // 4 boxes  (64 KB)
+constexpr int kOffStage = kOffV + 4 * kBoxK;       // 96 KB
+constexpr int kStageQ = 0;                         // 2 boxes (16 KB)
+constexpr int kStageDO = 2 * kBoxQ;                // 4 boxes (32 KB)
+constexpr int kStageBytes = 6 * kBoxQ;             // 48 KB
+constexpr int kOffP = kOffStage + 2 * kStageBytes;
+constexpr int kOffDS = kOffP + kBoxK;              // 16 KB each
+constexpr int kOffLse = kOffDS + kBoxK;            // [stage] {lse2[64], D[64]}: 512 B each
+constexpr int kOffBar = kOffLse + 1024;
+constexpr int kSmemBytes = kOffBar + 512 + 1024;   // 231936 <= 232448
+
+enum {
+  B_KV = 0, B_QFULL, B_QFULL1, B_QEMPTY, B_QEMPTY1, B_SFULL, B_DPFULL, B_PFULL, B_DQFULL,
+  B_DQFREE, B_PBFREE, B_ACC, B_RTR, B_DATA, B_COUNT
+};
+
+__host__ __device__ constexpr uint32_t idesc2(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
+         (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+constexpr uint32_t kIdS = idesc2(128, 64, 0, 0);    // K (K-major) x Q (K-major)
+constexpr uint32_t kIdDP = idesc2(128, 64, 0, 0);   // V (K-major) x dO (K-major)
+constexpr uint32_t kIdDV = idesc2(128, 256, 0, 1);  // Psig^T (K-major) x dO (MN-major)
+constexpr uint32_t kIdDK = idesc2(128, 128, 0, 1);  // dS^T (K-major) x Q (MN-major)
+constexpr uint32_t kIdDQ = idesc2(128, 64, 1, 1);   // K^T (MN-major) x dS^T (MN-major)
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+struct Shared {
+  uint32_t base;
+  uint8_t* gen;
+  __device__ uint32_t bar(int i) const { return base + kOffBar + 8 * i; }
+  __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(gen + kOffBar + 256); }
+  __device__ volatile int* abort_flag() const {
+    return reinterpret_cast<volatile int*>(gen + kOffBar + 264);
+  }
+  __device__ float* lam() const { return reinterpret_cast<float*>(gen + kOffBar + 268); }
+};
+
+__device__ __forceinline__ bool try_wait_cluster(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.try_wait.parity.acquire.cluster.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+template <bool kCluster = false>
+__device__ __forceinline__ bool wait_bar(const Shared& sh, uint32_t bar, uint32_t parity,
+                                         uint32_t* status, uint32_t site) {
+  auto poll = [&]() { return kCluster ? try_wait_cluster(bar, parity) : mbar_try_wait(bar, parity); };
+  if (poll()) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (poll()) return true;
+    if (*sh.abort_flag()) return false;
+    if (globaltimer() - t0 > 2000000000ull) {
+      record_status(status, DA_ERR_TIMEOUT, site);
+      *sh.abort_flag() = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
+  uint32_t r;
+  asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
+  return r;
+}
+__device__ __forceinline__ void remote_arrive(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
+               : "memory");
+}
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x),
+               "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ uint32_t cluster_rank() {
+  uint32_t r;
+  asm volatile("mov.u32 %0, %%cluster_ctarank;" : "=r"(r));
+  return r;
+}
+__device__ __forceinline__ void cluster_sync() {
+  asm volatile("barrier.cluster.arrive.release.aligned;\nbarrier.cluster.wait.acquire.aligned;" ::
+                   : "memory");
+}
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+__device__ __forceinline__ void red_add(float* p, float v) {
+  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
+}
+
+// --------------------------------------------------------------------------
+// Workspace carve-up (all offsets 256-byte aligned).
+struct BwdWs {
+  __nv_bfloat16* dO;   // [B, N, H, 256]
+  float* lse2[2];      // [B, H, Npad]  (LSE * log2 e; +inf in padding rows)
+  float* D[2];         // [B, H, Npad]
+  float* dq[2];        // [B, N, H, 128] fp32 accumulators
+  float* dlam_part;    // [preprocess blocks]
+  int npad, pre_blocks;
+};
+
+size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
+
+constexpr int kPreWarps = 8;
+
+BwdWs carve(void* base, int B, int N, int H, size_t* total) {
+  BwdWs w;
+  w.npad = (N + kQT - 1) / kQT * kQT;
+  w.pre_blocks = static_cast<int>((static_cast<long long>(B) * H * w.npad + kPreWarps - 1) / kPreWarps);
+  uint8_t* p = static_cast<uint8_t*>(base);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    uint8_t* r = p ? p + off : nullptr;
+    off += a256(bytes);
+    return r;
+  };
+  const size_t rows = static_cast<size_t>(B) * N * H;
+  const size_t srow = static_cast<size_t>(B) * H * w.npad;
+  w.dO = reinterpret_cast<__nv_bfloat16*>(take(rows * kDv * 2));
+  for (int t = 0; t < 2; ++t) w.lse2[t] = reinterpret_cast<float*>(take(srow * 4));
+  for (int t = 0; t < 2; ++t) w.D[t] = reinterpret_cast<float*>(take(srow * 4));
+  for (int t = 0; t < 2; ++t) w.dq[t] = reinterpret_cast<float*>(take(rows * kDqk * 4));
+  w.dlam_part = reinterpret_cast<float*>(take(static_cast<size_t>(w.pre_blocks) * 4));
+  if (total) *total = off;
+  return w;
+}
+
+__device__ __forceinline__ float lambda_dev(const V1BwdArgs& a, int lane, float* ea, float* eb) {
+  float d1 = 0.f, d2 = 0.f;
+  for (int x = lane; x < a.d_qk; x += 32) {
+    d1 = fmaf(a.lq1[x], a.lk1[x], d1);
+    d2 = fmaf(a.lq2[x], a.lk2[x], d2);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    d1 += __shfl_xor_sync(0xffffffffu, d1, o);
+    d2 += __shfl_xor_sync(0xffffffffu, d2, o);
+  }
+  const float e1 = expf(d1), e2 = expf(d2);
+  if (ea) *ea = e1;
+  if (eb) *eb = e2;
+  return e1 - e2 + a.lambda_init;
+}
+
+// ------------------------------------------------------------ preprocess --
+__global__ void __launch_bounds__(kPreWarps * 32)
+v1_bwd_pre_kernel(V1BwdArgs a, BwdWs w) {
+  __shared__ float s_lam;
+  __shared__ float s_part[kPreWarps];
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (warp == 0) {
+    const float lam = lambda_dev(a, lane, nullptr, nullptr);
+    if (lane == 0) s_lam = lam;
+  }
+  __syncthreads();
+  const float lam = s_lam;
+  const float c = 1.f - a.lambda_init;
+  const long long row = static_cast<long long>(blockIdx.x) * kPreWarps + warp;  // over (b, h, n < npad)
+  const long long total = static_cast<long long>(a.B) * a.H * w.npad;
+  float part = 0.f;
+  if (row < total) {
+    const int n = static_cast<int>(row % w.npad);
+    const int bh = static_cast<int>(row / w.npad);
+    const int b = bh / a.H, h = bh % a.H;
+    if (n < a.N) {
+      const __nv_bfloat16* yp = static_cast<const __nv_bfloat16*>(a.out.ptr) + b * a.out.sb +
+                                static_cast<int64_t>(n) * a.out.sn + h * a.out.sh + lane * 8;
+      const __nv_bfloat16* gp = static_cast<const __nv_bfloat16*>(a.dout.ptr) + b * a.dout.sb +
+                                static_cast<int64_t>(n) * a.dout.sn + h * a.dout.sh + lane * 8;
+      const __nv_bfloat16* op = static_cast<const __nv_bfloat16*>(a.o2.ptr) + b * a.o2.sb +
+                                static_cast<int64_t>(n) * a.o2.sn + h * a.o2.sh + lane * 8;
+      const uint4 yv = *reinterpret_cast<const uint4*>(yp);
+      const uint4 gv = *reinterpret_cast<const uint4*>(gp);
+      const uint4 ov = *reinterpret_cast<const uint4*>(op);
+      const __nv_bfloat16* ye = reinterpret_cast<const __nv_bfloat16*>(&yv);
+      const __nv_bfloat16* ge = reinterpret_cast<const __nv_bfloat16*>(&gv);
+      const __nv_bfloat16* oe = reinterpret_cast<const __nv_bfloat16*>(&ov);
+      const int64_t sidx = (static_cast<int64_t>(b) * a.H + h) * a.N + n;
+      const float rstd = a.rstd[sidx];
+      const float inv_c = c != 0.f ? 1.f / c : 0.f;
+      float yh[8], g[8], o2[8], gy = 0.f;
+#pragma unroll
+      for (int e = 0; e < 8; ++e) {
+        yh[e] = __bfloat162float(ye[e]) * inv_c;
+        g[e] = __bfloat162float(ge[e]);
+        o2[e] = __bfloat162float(oe[e]);
+        gy = fmaf(g[e], yh[e], gy);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) gy += __shfl_xor_sync(0xffffffffu, gy, o);
+      const float mean_gy = gy * (1.f / kDv);
+      const float k = c * rstd;
+      const float inv_rstd = 1.f / rstd;
+      float d1 = 0.f, d2 = 0.f;
+      uint32_t pk[4];
+#pragma unroll
+      for (int e = 0; e < 8; e += 2) {
+        const float do0 = k * (g[e] - yh[e] * mean_gy);
+        const float do1 = k * (g[e + 1] - yh[e + 1] * mean_gy);
+        // round dO to bf16 once; D1 / D2 use the rounded values the MMAs see
+        pk[e / 2] = pack_bf16x2(do0, do1);
+        const __nv_bfloat162 r = *reinterpret_cast<const __nv_bfloat162*>(&pk[e / 2]);
+        const float r0 = __low2float(r), r1 = __high2float(r);
+        const float o_0 = yh[e] * inv_rstd, o_1 = yh[e + 1] * inv_rstd;
+        d1 = fmaf(r0, fmaf(lam, o2[e], o_0), d1);
+        d1 = fmaf(r1, fmaf(lam, o2[e + 1], o_1), d1);
+        d2 = fmaf(r0, o2[e], d2);
+        d2 = fmaf(r1, o2[e + 1], d2);
+      }
+#pragma unroll
+      for (int o = 16; o > 0; o >>= 1) {
+        d1 += __shfl_xor_sync(0xffffffffu, d1, o);
+        d2 += __shfl_xor_sync(0xffffffffu, d2, o);
+      }
+      const int64_t rrow = (static_cast<int64_t>(b) * a.N + n) * a.H + h;
+      *reinterpret_cast<uint4*>(w.dO + rrow * kDv + lane * 8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      *reinterpret_cast<float4*>(w.dq[0] + rrow * kDqk + lane * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+      *reinterpret_cast<float4*>(w.dq[1] + rrow * kDqk + lane * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (lane == 0) {
+        const int64_t pidx = static_cast<int64_t>(bh) * w.npad + n;
+        w.D[0][pidx] = d1;
+        w.D[1][pidx] = d2;
+        w.lse2[0][pidx] = a.lse1[sidx] * 1.4426950408889634f;
+        w.lse2[1][pidx] = a.lse2[sidx] * 1.4426950408889634f;
+        part = -d2;
+      }
+    } else if (lane == 0) {
+      const int64_t pidx = static_cast<int64_t>(bh) * w.npad + n;
+      w.D[0][pidx] = 0.f;
+      w.D[1][pidx] = 0.f;
+      w.lse2[0][pidx] = INFINITY;
+      w.lse2[1][pidx] = INFINITY;
+    }
+  }
+  if (lane == 0) s_part[warp] = part;
+  __syncthreads();
+  if (threadIdx.x == 0) {
+    float s = 0.f;
+    for (int i = 0; i < kPreWarps; ++i) s += s_part[i];
+    w.dlam_part[blockIdx.x] = s;
+  }
+}
+
+// -------------------------------------------------------------- main -------
+struct Item {
+  int b, h, kt, i0, n_it;
+};
+
+__global__ void __launch_bounds__(kThreads, 1)
+v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__ CUtensorMap tm_q2,
+                   const __grid_constant__ CUtensorMap tm_k1, const __grid_constant__ CUtensorMap tm_k2,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                   V1BwdArgs a, BwdWs w) {
+  extern __shared__ uint8_t smem_raw[];
+  Shared sh;
+  {
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t al = (raw + 1023u) & ~1023u;
+    sh.base = al;
+    sh.gen = smem_raw + (al - raw);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const uint32_t rank = cluster_rank();  // stream index
+  const uint32_t partner = rank ^ 1u;
+  // items: heaviest (first key tiles: most query tiles) first
+  const int n_kt = (a.N + kKT - 1) / kKT;
+  const int n_qt = w.npad / kQT;
+  Item it;
+  {
+    const int ci = blockIdx.x >> 1;
+    const int units = a.B * a.H;
+    it.kt = ci / units;
+    const int u = ci % units;
+    it.b = u / a.H;
+    it.h = u % a.H;
+    it.i0 = it.kt * (kKT / kQT);
+    it.n_it = n_qt - it.i0;
+  }
+  (void)n_kt;
+  const CUtensorMap* tq = rank == 0 ? &tm_q1 : &tm_q2;
+  const CUtensorMap* tk = rank == 0 ? &tm_k1 : &tm_k2;
+  const float* lse2 = w.lse2[rank];
+  const float* Dv = w.D[rank];
+  float* dq = w.dq[rank];
+
+  if (threadIdx.x == 0) {
+    mbar_init(sh.bar(B_KV), 1);
+    for (int s = 0; s < 2; ++s) {
+      mbar_init(sh.bar(B_QFULL + s), 1);
+      mbar_init(sh.bar(B_QEMPTY + s), 1);
+    }
+    mbar_init(sh.bar(B_SFULL), 1);
+    mbar_init(sh.bar(B_DPFULL), 1);
+    mbar_init(sh.bar(B_PFULL), 128);
+    mbar_init(sh.bar(B_DQFULL), 1);
+    mbar_init(sh.bar(B_DQFREE), 128);
+    mbar_init(sh.bar(B_PBFREE), 1);
+    mbar_init(sh.bar(B_ACC), 1);
+    mbar_init(sh.bar(B_RTR), 128);
+    mbar_init(sh.bar(B_DATA), 128);
+    *sh.abort_flag() = 0;
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    const float lam = lambda_dev(a, lane, nullptr, nullptr);
+    if (lane == 0) *sh.lam() = lam;
+  }
+  if (warp == 5) {
+    tmem_alloc(smem_u32(sh.tmem_slot()), 512);
+    tmem_relinquish();
+  }
+  if (warp == 4 && lane == 0) {
+    prefetch_tmap(tq);
+    prefetch_tmap(tk);
+    prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_do);
+  }
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  const uint32_t tmem = *sh.tmem_slot();
+  const uint32_t T_DV = tmem, T_DK = tmem + 256, T_S = tmem + 384, T_DP = tmem + 448;
+
+  if (warp == 4) {
+    // ---------------------------------------------------- TMA producer ----
+    if (lane == 0) {
+      mbar_arrive_expect_tx(sh.bar(B_KV), 6 * kBoxK);
+      for (int box = 0; box < 2; ++box)
+        tma_load_4d(sh.base + kOffK + box * kBoxK, tk, sh.bar(B_KV), box * 64, it.h, it.kt * kKT, it.b);
+      for (int box = 0; box < 4; ++box)
+        tma_load_4d(sh.base + kOffV + box * kBoxK, &tm_v, sh.bar(B_KV), box * 64, it.h, it.kt * kKT, it.b);
+      const size_t srow = (static_cast<size_t>(it.b) * a.H + it.h) * w.npad;
+      for (int k = 0; k < it.n_it; ++k) {
+        const int st = k & 1, use = k >> 1;
+        if (use > 0 && !wait_bar(sh, sh.bar(B_QEMPTY + st), (use - 1) & 1, a.status, 0x4001)) break;
+        const int q0 = (it.i0 + k) * kQT;
+        const uint32_t sb = sh.base + kOffStage + st * kStageBytes;
+        mbar_arrive_expect_tx(sh.bar(B_QFULL + st), 6 * kBoxQ + 512);
+        for (int box = 0; box < 2; ++box)
+          tma_load_4d(sb + kStageQ + box * kBoxQ, tq, sh.bar(B_QFULL + st), box * 64, it.h, q0, it.b);
+        for (int box = 0; box < 4; ++box)
+          tma_load_4d(sb + kStageDO + box * kBoxQ, &tm_do, sh.bar(B_QFULL + st), box * 64, it.h, q0, it.b);
+        const uint32_t lb = sh.base + kOffLse + st * 512;
+        bulk_load(lb, lse2 + srow + q0, 256, sh.bar(B_QFULL + st));
+        bulk_load(lb + 256, Dv + srow + q0, 256, sh.bar(B_QFULL + st));
+      }
+    }
+  } else if (warp == 5) {
+    // ------------------------------------------------------ MMA issuer ----
+    if (lane == 0) {
+      bool ok = wait_bar(sh, sh.bar(B_KV), 0, a.status, 0x4101);
+      tc_fence_after();
+      const uint32_t kA = sh.base + kOffK, vA = sh.base + kOffV;
+      auto stage = [&](int k) { return sh.base + kOffStage + (k & 1) * kStageBytes; };
+      auto issue_s = [&](int k) {  // S^T = K Q^T
+        const uint32_t qb = stage(k) + kStageQ;
+#pragma unroll
+        for (int kk = 0; kk < kDqk / 16; ++kk) {
+          const uint32_t offa = (kk >> 2) * kBoxK + (kk & 3) * 32;
+          const uint32_t offb = (kk >> 2) * kBoxQ + (kk & 3) * 32;
+          tc_mma_ss(T_S, sdesc_sw128(kA + offa, 16, 1024), sdesc_sw128(qb + offb, 16, 1024), kIdS, kk > 0);
+        }
+      };
+      auto issue_dp = [&](int k) {  // dP^T = V dO^T
+        const uint32_t db = stage(k) + kStageDO;
+#pragma unroll
+        for (int kk = 0; kk < kDv / 16; ++kk) {
+          const uint32_t offa = (kk >> 2) * kBoxK + (kk & 3) * 32;
+          const uint32_t offb = (kk >> 2) * kBoxQ + (kk & 3) * 32;
+          tc_mma_ss(T_DP, sdesc_sw128(vA + offa, 16, 1024), sdesc_sw128(db + offb, 16, 1024), kIdDP, kk > 0);
+        }
+      };
+      const uint32_t pA = sh.base + kOffP, dsA = sh.base + kOffDS;
+      for (int k = 0; k < it.n_it && ok; ++k) {
+        const int ph = k & 1;
+        if (k == 0) {
+          if (!wait_bar(sh, sh.bar(B_QFULL), 0, a.status, 0x4102)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(0);
+          tc_commit(sh.bar(B_SFULL));
+          issue_dp(0);
+          tc_commit(sh.bar(B_DPFULL));
+        }
+        if (!wait_bar(sh, sh.bar(B_PFULL), ph, a.status, 0x4103)) { ok = false; break; }
+        tc_fence_after();
+        // dQ^T = K^T dS^T  (into the dP^T columns, already consumed)
+#pragma unroll
+        for (int kk = 0; kk < kKT / 16; ++kk)
+          tc_mma_ss(T_DP, sdesc_sw128(kA + kk * 2048, kBoxK, 1024), sdesc_sw128(dsA + kk * 2048, kBoxQ, 1024),
+                    kIdDQ, kk > 0);
+        tc_commit(sh.bar(B_DQFULL));
+        const bool more = k + 1 < it.n_it;
+        if (more) {
+          if (!wait_bar(sh, sh.bar(B_QFULL + ((k + 1) & 1)), ((k + 1) >> 1) & 1, a.status, 0x4104)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(k + 1);
+          tc_commit(sh.bar(B_SFULL));
+        }
+        // dV += Psig^T dO ; dK += dS^T Q
+        const uint32_t db = stage(k) + kStageDO, qb = stage(k) + kStageQ;
+#pragma unroll
+        for (int kk = 0; kk < kQT / 16; ++kk)
+          tc_mma_ss(T_DV, sdesc_sw128(pA + kk * 32, 16, 1024), sdesc_sw128(db + kk * 2048, kBoxQ, 1024), kIdDV,
+                    (k > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < kQT / 16; ++kk)
+          tc_mma_ss(T_DK, sdesc_sw128(dsA + kk * 32, 16, 1024), sdesc_sw128(qb + kk * 2048, kBoxQ, 1024), kIdDK,
+                    (k > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(sh.bar(B_PBFREE));
+        tc_commit(sh.bar(B_QEMPTY + (k & 1)));
+        if (more) {
+          if (!wait_bar(sh, sh.bar(B_DQFREE), ph, a.status, 0x4105)) { ok = false; break; }
+          tc_fence_after();
+          issue_dp(k + 1);
+          tc_commit(sh.bar(B_DPFULL));
+        }
+      }
+      if (ok) tc_commit(sh.bar(B_ACC));
+    }
+  } else {
+    // ------------------------------- softmax / dS / dQ / epilogue ---------
+    const int r = warp * 32 + lane;  // key row within the tile = TMEM lane
+    const uint32_t loff = static_cast<uint32_t>(warp * 32) << 16;
+    const float lam = *sh.lam();
+    const float sigma = rank == 0 ? 1.f : -lam;
+    const float sds = sigma * a.scale;
+    const float sl2 = a.scale * 1.4426950408889634f;
+    const int key = it.kt * kKT + r;
+    bool ok = true;
+    uint8_t* pbuf = sh.gen + kOffP;
+    uint8_t* dsbuf = sh.gen + kOffDS;
+    for (int k = 0; k < it.n_it && ok; ++k) {
+      const int ph = k & 1;
+      const int q0 = (it.i0 + k) * kQT;
+      if (!wait_bar(sh, sh.bar(B_SFULL), ph, a.status, 0x4201)) { ok = false; break; }
+      if (!wait_bar(sh, sh.bar(B_DPFULL), ph, a.status, 0x4202)) { ok = false; break; }
+      if (k > 0 && !wait_bar(sh, sh.bar(B_PBFREE), (k - 1) & 1, a.status, 0x4203)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t sv[64], dp[64];
+      tmem_ld32(T_S + loff, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+      tmem_ld32(T_S + loff + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+      tmem_ld32(T_DP + loff, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
+      tmem_ld32(T_DP + loff + 32, *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
+      tmem_ld_wait();
+      const float* l2 = reinterpret_cast<const float*>(sh.gen + kOffLse + (k & 1) * 512);
+      const float* dd = l2 + 64;
+      const bool diag = q0 < it.kt * kKT + kKT;  // a query of this tile may precede a key
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {  // 8 queries per 16-byte chunk
+        uint32_t pw[4], dw[4];
+#pragma unroll
+        for (int e = 0; e < 8; e += 2) {
+          const int c = ch * 8 + e;
+          float p0 = fast_exp2(fmaf(__uint_as_float(sv[c]), sl2, -l2[c]));
+          float p1 = fast_exp2(fmaf(__uint_as_float(sv[c + 1]), sl2, -l2[c + 1]));
+          if (diag) {
+            if (key > q0 + c) p0 = 0.f;
+            if (key > q0 + c + 1) p1 = 0.f;
+          }
+          const float ds0 = p0 * (__uint_as_float(dp[c]) - dd[c]) * sds;
+          const float ds1 = p1 * (__uint_as_float(dp[c + 1]) - dd[c + 1]) * sds;
+          pw[e / 2] = pack_bf16x2(p0 * sigma, p1 * sigma);
+          dw[e / 2] = pack_bf16x2(ds0, ds1);
+        }
+        const int off = r * 128 + ((ch ^ (r & 7)) << 4);
+        *reinterpret_cast<uint4*>(pbuf + off) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
+        *reinterpret_cast<uint4*>(dsbuf + off) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
+      }
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(sh.bar(B_PFULL));
+      // dQ^T rows: lane = feature d of dQ; 64 queries
+      if (!wait_bar(sh, sh.bar(B_DQFULL), ph, a.status, 0x4204)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t qv[64];
+      tmem_ld32(T_DP + loff, *reinterpret_cast<uint32_t(*)[32]>(&qv[0]));
+      tmem_ld32(T_DP + loff + 32, *reinterpret_cast<uint32_t(*)[32]>(&qv[32]));
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(sh.bar(B_DQFREE));
+      const int nq = min(kQT, a.N - q0);
+      float* dqp = dq + ((static_cast<int64_t>(it.b) * a.N + q0) * a.H + it.h) * kDqk + r;
+      const int64_t qstride = static_cast<int64_t>(a.H) * kDqk;
+#pragma unroll
+      for (int c = 0; c < kQT; ++c)
+        if (c < nq) red_add(dqp + c * qstride, __uint_as_float(qv[c]));
+    }
+    // ----------------------------------------------------------- epilogue --
+    if (ok && wait_bar(sh, sh.bar(B_ACC), 0, a.status, 0x4205)) {
+      tc_fence_after();
+      const bool live = key < a.N;
+      // dK of this stream
+      __nv_bfloat16* dkp = static_cast<__nv_bfloat16*>(rank == 0 ? a.dk1.ptr : a.dk2.ptr);
+      const da_t4& dkt = rank == 0 ? a.dk1 : a.dk2;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(T_DK + loff + c * 32, v);
+        tmem_ld_wait();
+        if (live) {
+          __nv_bfloat16* dst = dkp + it.b * dkt.sb + static_cast<int64_t>(key) * dkt.sn + it.h * dkt.sh + c * 32;
+#pragma unroll
+          for (int e = 0; e < 32; e += 8) {
+            *reinterpret_cast<uint4*>(dst + e) = make_uint4(
+                pack_bf16x2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
+                pack_bf16x2(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])),
+                pack_bf16x2(__uint_as_float(v[e + 4]), __uint_as_float(v[e + 5])),
+                pack_bf16x2(__uint_as_float(v[e + 6]), __uint_as_float(v[e + 7])));
+          }
+        }
+      }
+      // dV: swap halves with the partner (the other stream) through DSMEM.
+      // Receive buffer = this CTA's V tile region (idle now): 128 rows x 512 B.
+      remote_arrive(map_to_rank(sh.bar(B_RTR), partner));
+      if (wait_bar<true>(sh, sh.bar(B_RTR), 0, a.status, 0x4206)) {
+        const int give = (1 - static_cast<int>(rank)) * 128, keep = static_cast<int>(rank) * 128;
+        const uint32_t rx = map_to_rank(sh.base + kOffV + r * 512, partner);
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          uint32_t v[32];
+          tmem_ld32(T_DV + loff + give + c * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            st_cluster_v4(rx + (c * 32 + e) * 4,
+                          make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
+                                      __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])));
+        }
+        remote_arrive(map_to_rank(sh.bar(B_DATA), partner));
+        if (wait_bar<true>(sh, sh.bar(B_DATA), 0, a.status, 0x4207)) {
+          const float* mine = reinterpret_cast<const float*>(sh.gen + kOffV + r * 512);
+          __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dv.ptr) + it.b * a.dv.sb +
+                               static_cast<int64_t>(key) * a.dv.sn + it.h * a.dv.sh + keep;
+#pragma unroll 1
+          for (int c = 0; c < 4; ++c) {
+            uint32_t v[32];
+            tmem_ld32(T_DV + loff + keep + c * 32, v);
+            tmem_ld_wait();
+            if (live) {
+#pragma unroll
+              for (int e = 0; e < 32; e += 8) {
+                float s8[8];
+#pragma unroll
+                for (int u = 0; u < 8; ++u) {
+                  const float other = mine[c * 32 + e + u];
+                  // stream 1 + stream 2 in a fixed order on both CTAs
+                  s8[u] = rank == 0 ? __uint_as_float(v[e + u]) + other : other + __uint_as_float(v[e + u]);
+                }
+                *reinterpret_cast<uint4*>(dst + c * 32 + e) =
+                    make_uint4(pack_bf16x2(s8[0], s8[1]), pack_bf16x2(s8[2], s8[3]),
+                               pack_bf16x2(s8[4], s8[5]), pack_bf16x2(s8[6], s8[7]));
+              }
+            }
+          }
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  cluster_sync();
+  tc_fence_after();
+  if (warp == 5) tmem_dealloc(tmem, 512);
+}
+
+// -------------------------------------------------------------- finalize --
+__global__ void __launch_bounds__(256)
+v1_bwd_finalize_kernel(V1BwdArgs a, BwdWs w) {
+  const long long rows = static_cast<long long>(a.B) * a.N * a.H;
+  const long long total = rows * (kDqk / 8);
+  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long row = idx / (kDqk / 8);
+    const int c8 = static_cast<int>(idx % (kDqk / 8)) * 8;
+    const int h = static_cast<int>(row % a.H);
+    const long long bn = row / a.H;
+    const int n = static_cast<int>(bn % a.N), b = static_cast<int>(bn / a.N);
+#pragma unroll
+    for (int t = 0; t < 2; ++t) {
+      const float* src = w.dq[t] + row * kDqk + c8;
+      const float4 x0 = *reinterpret_cast<const float4*>(src);
+      const float4 x1 = *reinterpret_cast<const float4*>(src + 4);
+      const da_t4& o = t == 0 ? a.dq1 : a.dq2;
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(o.ptr) + b * o.sb + static_cast<int64_t>(n) * o.sn +
+                           h * o.sh + c8;
+      *reinterpret_cast<uint4*>(dst) = make_uint4(pack_bf16x2(x0.x, x0.y), pack_bf16x2(x0.z, x0.w),
+                                                  pack_bf16x2(x1.x, x1.y), pack_bf16x2(x1.z, x1.w));
+    }
+  }
+  if (blockIdx.x == 0) {
+    __shared__ float red[256];
+    float s = 0.f;
+    for (int i = threadIdx.x; i < w.pre_blocks; i += 256) s += w.dlam_part[i];
+    red[threadIdx.x] = s;
+    __syncthreads();
+    for (int o = 128; o > 0; o >>= 1) {
+      if (threadIdx.x < o) red[threadIdx.x] += red[threadIdx.x + o];
+      __syncthreads();
+    }
+    const float dlam = red[0];
+    __shared__ float ea, eb;
+    if (threadIdx.x < 32) {
+      float e1, e2;
+      lambda_dev(a, threadIdx.x, &e1, &e2);
+      if (threadIdx.x == 0) {
+        ea = e1;
+        eb = e2;
+      }
+    }
+    __syncthreads();
+    for (int x = threadIdx.x; x < a.d_qk; x += 256) {
+      a.dlq1[x] = dlam * ea * a.lk1[x];
+      a.dlk1[x] = dlam * ea * a.lq1[x];
+      a.dlq2[x] = -dlam * eb * a.lk2[x];
+      a.dlk2[x] = -dlam * eb * a.lq2[x];
+    }
+  }
+}
+
+}  // namespace
+
+size_t v1_bwd_workspace_bytes(int B, int N, int H, int d_qk, int d_v) {
+  (void)d_qk;
+  (void)d_v;
+  size_t total = 0;
+  carve(nullptr, B, N, H, &total);
+  return total;
+}
+
+cudaError_t launch_v1_bwd(const V1BwdArgs& a, cudaStream_t s) {
+  size_t total = 0;
+  BwdWs w = carve(a.workspace, a.B, a.N, a.H, &total);
+  if (total > a.workspace_bytes) return cudaErrorInvalidValue;
+
+  v1_bwd_pre_kernel<<<w.pre_blocks, kPreWarps * 32, 0, s>>>(a, w);
+  cudaError_t e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  CUtensorMap tq1, tq2, tk1, tk2, tv, tdo;
+  da_t4 dot{w.dO, static_cast<int64_t>(a.N) * a.H * kDv, static_cast<int64_t>(a.H) * kDv, kDv};
+  if (!encode_tmap_bf16_4d(&tq1, a.q1, a.B, a.N, a.H, kDqk, kQT) ||
+      !encode_tmap_bf16_4d(&tq2, a.q2, a.B, a.N, a.H, kDqk, kQT) ||
+      !encode_tmap_bf16_4d(&tk1, a.k1, a.B, a.N, a.H, kDqk, kKT) ||
+      !encode_tmap_bf16_4d(&tk2, a.k2, a.B, a.N, a.H, kDqk, kKT) ||
+      !encode_tmap_bf16_4d(&tv, a.v, a.B, a.N, a.H, kDv, kKT) ||
+      !encode_tmap_bf16_4d(&tdo, dot, a.B, a.N, a.H, kDv, kQT))
+    return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(v1_bwd_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int n_kt = (a.N + kKT - 1) / kKT;
+  const int items = n_kt * a.B * a.H;
+  cudaLaunchConfig_t cfg = {};
+  cudaLaunchAttribute attr[1];
+  attr[0].id = cudaLaunchAttributeClusterDimension;
+  attr[0].val.clusterDim.x = 2;
+  attr[0].val.clusterDim.y = 1;
+  attr[0].val.clusterDim.z = 1;
+  cfg.gridDim = dim3(2 * items, 1, 1);
+  cfg.blockDim = dim3(kThreads, 1, 1);
+  cfg.dynamicSmemBytes = kSmemBytes;
+  cfg.stream = s;
+  cfg.attrs = attr;
+  cfg.numAttrs = 1;
+  e = cudaLaunchKernelEx(&cfg, v1_bwd_main_kernel, tq1, tq2, tk1, tk2, tv, tdo, a, w);
+  if (e != cudaSuccess) return e;
+
+  const long long work = static_cast<long long>(a.B) * a.N * a.H * (kDqk / 8);
+  int grid = static_cast<int>((work + 255) / 256);
+  if (grid > 4 * 152) grid = 4 * 152;
+  if (grid < 1) grid = 1;
+  v1_bwd_finalize_kernel<<<grid, 256, 0, s>>>(a, w);
+  return cudaGetLastError();
+}
+
+}  // namespace da

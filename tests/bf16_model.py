@@ -1,0 +1,49 @@
+"""bf16 rounding model of the V1 backward (test infrastructure).
+
+Runs the chain rule in exact fp64 EXCEPT at the five points where the
+library's backward must hold bf16 values: the forward outputs Y and O2, the
+upstream gradient after the RMSNorm backward (dO, an MMA operand), and the
+P and dS tiles fed to the tensor cores.  Its error against the fp64 oracle
+is the error any bf16 implementation with these storage points has; the GPU
+parity tests bound the library's error by a small multiple of it.
+"""
+
+import numpy as np
+import torch
+
+
+def bf16(x):
+    return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+
+
+def rounded_backward(f, fwd, li, heads=None):
+    """f: fp64 inputs (q1..v, dy) as [B, N, H, D]; fwd: the oracle forward on
+    them.  Returns the gradients dq1, dq2, dk1, dk2, dv (and dlam) computed
+    with the bf16 storage points; `heads` restricts to a list of heads."""
+    lam, c = fwd["lam"], 1.0 - li
+    B, N, H, dqk = f["q1"].shape
+    heads = range(H) if heads is None else heads
+    s = 1.0 / np.sqrt(dqk)
+    out = {n: np.zeros_like(f["q1"]) for n in ("dq1", "dq2", "dk1", "dk2")}
+    out["dv"] = np.zeros_like(f["v"])
+    dlam = 0.0
+    for b in range(B):
+        for h in heads:
+            Y, O2, rstd = bf16(fwd["y"][b, :, h]), bf16(fwd["o2"][b, :, h]), fwd["rstd"][b, h]
+            G = f["dy"][b, :, h]
+            yh = Y / c
+            gy = (G * yh).sum(1, keepdims=True)
+            dO = bf16(c * rstd[:, None] * (G - yh * gy / Y.shape[1]))
+            D2 = (dO * O2).sum(1)
+            D1 = (dO * (yh / rstd[:, None] + lam * O2)).sum(1)
+            dlam -= float(D2.sum())
+            dP = dO @ f["v"][b, :, h].T
+            for t, (sig, D, lse) in enumerate(((1.0, D1, fwd["lse1"]), (-lam, D2, fwd["lse2"])), 1):
+                Q, K = f[f"q{t}"][b, :, h], f[f"k{t}"][b, :, h]
+                P = np.tril(np.exp(s * Q @ K.T - lse[b, h][:, None]))
+                dS = bf16(sig * s * P * (dP - D[:, None]))
+                out[f"dq{t}"][b, :, h] = dS @ K
+                out[f"dk{t}"][b, :, h] = dS.T @ Q
+                out["dv"][b, :, h] += bf16(sig * P).T @ dO
+    out["dlam"] = dlam
+    return out

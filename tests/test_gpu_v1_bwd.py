@@ -1,0 +1,141 @@
+"""GPU parity through the C ABI for the V1 backward (preprocess, tcgen05 main
+kernel with 2-CTA clusters, finalize) against the fp64 oracle's chain rule.
+
+Bars (the pages state none for gradients).  The bf16 rounding model
+(tests/bf16_model.py: the exact chain rule with only the five bf16 storage
+points any bf16 backward has) gives, per input, the error that precision
+alone causes; a fixed max-abs bar cannot hold across inputs because that
+error grows with the cancellation between the streams (layer 14 at N 129
+reaches 11 % of RMS on dV).  So, per gradient tensor:
+* max|GPU - oracle| <= k * max|model - oracle| + 1e-3 * RMS(oracle) + floor,
+  k = 2 for the backward alone (fed the oracle's forward saves) and k = 3 for
+  the training step (GPU forward, then GPU backward on its saves: the
+  forward's own bf16 error enters too);
+* ||GPU - oracle|| / ||oracle|| <= 1.5e-2 (2e-2 for the step);
+* dlambda (the lambda-vector gradients are dlambda times fixed vectors)
+  within k * the model's error + 2e-3 relative.
+floor = 1e-3 * RMS(oracle dV) covers gradients that vanish analytically
+(N = 1: dQ, dK and dlambda are exactly zero).
+"""
+
+import numpy as np
+import pytest
+import torch
+
+from differential_attention_diff_gb300 import binding as bd
+from differential_attention_diff_gb300 import synth
+from bf16_model import rounded_backward
+from oracle import diffattn_oracle as orc
+
+pytestmark = pytest.mark.gpu
+BARS = {"bwd": (2.0, 1.5e-2), "step": (3.0, 2e-2)}  # (k, Frobenius)
+NAMES = ("q1", "q2", "k1", "k2", "v", "lq1", "lk1", "lq2", "lk2")
+GRADS = ("dq1", "dq2", "dk1", "dk2", "dv")
+
+
+def f64(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+@pytest.fixture(autouse=True)
+def _status_clean():
+    yield
+    assert bd.diffattn_get_device_status() == bd.DA_OK
+
+
+def _run(t, li):
+    """The training step: GPU forward with saves, then the GPU backward."""
+    y, sv = bd.diffattn_v1_fwd(*(t[n] for n in NAMES), li, save=True)
+    g = bd.diffattn_v1_bwd(*(t[n] for n in NAMES), li, y, t["dy"], sv)
+    torch.cuda.synchronize()
+    return g
+
+
+def _run_exact_saves(t, li):
+    """The GPU backward alone, given the oracle's forward outputs."""
+    fwd = orc.v1_forward(*(f64(t[n]) for n in NAMES), li)
+    dev = t["q1"].device
+    y = torch.from_numpy(fwd["y"]).to(dev, torch.bfloat16)
+    sv = dict(o2=torch.from_numpy(fwd["o2"]).to(dev, torch.bfloat16),
+              lse1=torch.from_numpy(fwd["lse1"]).to(dev, torch.float32),
+              lse2=torch.from_numpy(fwd["lse2"]).to(dev, torch.float32),
+              rstd=torch.from_numpy(fwd["rstd"]).to(dev, torch.float32))
+    g = bd.diffattn_v1_bwd(*(t[n] for n in NAMES), li, y, t["dy"], sv)
+    torch.cuda.synchronize()
+    return g
+
+
+def _compare(g, ref, model, heads=None, lam_vectors=True, bar="bwd"):
+    k, fro = BARS[bar]
+    floor = 1e-3 * float(np.sqrt(np.mean(ref["dv"] ** 2)))
+    worst = {}
+    for n in GRADS:
+        got, exp, mod = f64(g[n]), ref[n], model[n]
+        if heads is not None:  # the GPU ran all heads; oracle and model one
+            got = got[:, :, heads]
+        rms = float(np.sqrt(np.mean(exp ** 2)))
+        allowed = k * float(np.max(np.abs(mod - exp))) + 1e-3 * rms + floor
+        worst[n] = float(np.max(np.abs(got - exp))) / allowed
+        worst[n + "_fro"] = float(np.linalg.norm(got - exp)) / (
+            fro * float(np.linalg.norm(exp)) + floor * np.sqrt(exp.size))
+    if lam_vectors:
+        dlam_err = abs(model["dlam"] - ref["dlam"]) / max(abs(ref["dlam"]), 1e-30)
+        for n in ("dlq1", "dlk1", "dlq2", "dlk2"):
+            got, exp = f64(g[n]), ref[n]
+            scale = float(np.max(np.abs(exp)))
+            allowed = (k * dlam_err + 2e-3) * scale + 1e-3 * floor
+            worst[n] = float(np.max(np.abs(got - exp))) / allowed
+    assert max(worst.values()) <= 1.0, worst
+
+
+def _model(t, li, heads=None):
+    f = {n: f64(t[n]) for n in NAMES + ("dy",)}
+    fwd = orc.v1_forward(*(f[n] for n in NAMES), li)
+    return rounded_backward(f, fwd, li, heads=heads)
+
+
+@pytest.mark.parametrize("B,N,H,layer", [(1, 200, 2, 1), (2, 384, 1, 3), (1, 129, 2, 14),
+                                          (1, 1, 1, 1), (1, 700, 3, 28)])
+def test_v1_bwd_parity_small(B, N, H, layer):
+    t = synth.v1_inputs(B, N, H, 128, 256, "bf16", seed=5000 + N + H, device="cuda", with_dy=True)
+    li = float(np.float32(bd.diffattn_lambda_init(layer)))
+    ref = orc.v1_backward(*(f64(t[n]) for n in NAMES), li, f64(t["dy"]))
+    model = _model(t, li)
+    _compare(_run_exact_saves(t, li), ref, model, bar="bwd")
+    _compare(_run(t, li), ref, model, bar="step")
+
+
+def test_v1_bwd_deterministic_parts_repeat():
+    """dK and dV come from one CTA each (no atomics): bitwise equal on a rerun."""
+    t = synth.v1_inputs(1, 300, 2, 128, 256, "bf16", seed=61, device="cuda", with_dy=True)
+    li = bd.diffattn_lambda_init(2)
+    g1 = _run(t, li)
+    g2 = _run(t, li)
+    for n in ("dk1", "dk2", "dv"):
+        assert torch.equal(g1[n], g2[n]), n
+
+
+def test_v1_bwd_h16_n1024_all_heads():
+    """16 heads at N 1024: every gradient incl. the lambda vectors (dlambda
+    sums over all heads and rows)."""
+    t = synth.v1_inputs(1, 1024, 16, 128, 256, "bf16", seed=62, device="cuda", with_dy=True)
+    li = float(np.float32(bd.diffattn_lambda_init(1)))
+    ref = orc.v1_backward(*(f64(t[n]) for n in NAMES), li, f64(t["dy"]))
+    model = _model(t, li)
+    _compare(_run_exact_saves(t, li), ref, model, bar="bwd")
+    _compare(_run(t, li), ref, model, bar="step")
+
+
+def test_v1_bwd_full_size_b1_h16_n8192_one_head():
+    """B1 H16 N8192 (the training-step workload) through the library; the
+    oracle recomputes one head completely (its lambda-vector gradients are
+    partial, so only dQ, dK, dV are compared)."""
+    t = synth.v1_inputs(1, 8192, 16, 128, 256, "bf16", seed=1005, device="cuda", with_dy=True)
+    li = bd.diffattn_lambda_init(1)
+    g = _run(t, li)
+    h = 5
+    li = float(np.float32(li))
+    th = {n: (t[n][:, :, h:h + 1] if t[n].dim() == 4 else t[n]) for n in NAMES + ("dy",)}
+    ref = orc.v1_backward(*(f64(th[n]) for n in NAMES), li, f64(th["dy"]))
+    model = _model(th, li)
+    _compare(g, ref, model, heads=slice(h, h + 1), lam_vectors=False, bar="step")
