@@ -382,6 +382,19 @@ def dist_env():
     return ws, rank, local
 
 
+def aggregate(total_ms, steps, work_per_step, unit_scale, ws, device):
+    """Whole-job throughput of `ws` replicas: the slowest rank's time (max
+    over ranks of the local timed total), the work of every rank summed.
+    Returns (ms_per_step, value)."""
+    if ws > 1:
+        import torch.distributed as dist
+        t = torch.tensor([total_ms], device=device, dtype=torch.float64)
+        dist.all_reduce(t, op=dist.ReduceOp.MAX)
+        total_ms = float(t.item())
+    ms = total_ms / steps
+    return ms, work_per_step * ws / (ms / 1e3) / unit_scale
+
+
 def time_steps(fn, steps, flush, stream):
     """CUDA-event time of each of `steps` calls of fn (L2 flushed between
     calls, outside the timed events).  Returns per-step milliseconds."""
@@ -429,14 +442,8 @@ def run_ours(args, ws, rank, local):
     per_step = time_steps(main.run, args.steps, flush, stream)
     barrier()
     clocks = sampler.stop()
-    total_ms = sum(per_step)
-    if ws > 1:
-        import torch.distributed as dist
-        tt = torch.tensor([total_ms], device=dev, dtype=torch.float64)
-        dist.all_reduce(tt, op=dist.ReduceOp.MAX)
-        total_ms = float(tt.item())
-    ms = total_ms / args.steps
-    value = main.scale(ms / 1e3) * ws
+    ms, value = aggregate(sum(per_step), args.steps, main.work(),
+                          1e12 if main.unit == "TFLOP/s" else 1e9, ws, dev)
 
     # dominant kernel alone, live CUDA events on its launching stream
     for _ in range(2):
