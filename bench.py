@@ -110,12 +110,14 @@ class V1Fwd(Workload):
                                  device=dev)
         self.li = bd.diffattn_lambda_init(self.layer)
         self.out = torch.empty((self.B, self.N, self.H, self.dv), dtype=torch.bfloat16, device=dev)
+        need = bd.load().diffattn_v1_fwd_workspace_size(self.B, self.N, self.H, self.dqk, self.dv, 1)
+        self.fws = torch.empty((max(need, 1),), dtype=torch.uint8, device=dev)
 
     def args(self, t):
         return [t[n] for n in ("q1", "q2", "k1", "k2", "v", "lq1", "lk1", "lq2", "lk2")]
 
     def run(self):
-        self.bd.diffattn_v1_fwd(*self.args(self.t), self.li, out=self.out)
+        self.bd.diffattn_v1_fwd(*self.args(self.t), self.li, out=self.out, workspace=self.fws)
 
     # end-to-end through the public API with host buffers
     def e2e_setup(self):
@@ -126,7 +128,7 @@ class V1Fwd(Workload):
 
     def e2e_step(self):
         dev = {k: v.to(self.out.device, non_blocking=True) for k, v in self.host.items()}
-        self.bd.diffattn_v1_fwd(*self.args(dev), self.li, out=self.out)
+        self.bd.diffattn_v1_fwd(*self.args(dev), self.li, out=self.out, workspace=self.fws)
         self.host_out.copy_(self.out, non_blocking=True)
 
     def oracle_sample(self):
@@ -161,7 +163,10 @@ class V1FwdBwd(V1Fwd):
                                  device=dev, with_dy=True)
         self.li = bd.diffattn_lambda_init(self.layer)
         self.out = torch.empty((self.B, self.N, self.H, self.dv), dtype=torch.bfloat16, device=dev)
-        _, self.saves = bd.diffattn_v1_fwd(*self.args(self.t), self.li, out=self.out, save=True)
+        need = bd.load().diffattn_v1_fwd_workspace_size(self.B, self.N, self.H, self.dqk, self.dv, 1)
+        self.fws = torch.empty((max(need, 1),), dtype=torch.uint8, device=dev)
+        _, self.saves = bd.diffattn_v1_fwd(*self.args(self.t), self.li, out=self.out, save=True,
+                                           workspace=self.fws)
         self.grads = bd.diffattn_v1_bwd(*self.args(self.t), self.li, self.out, self.t["dy"],
                                         self.saves)
         need = bd.load().diffattn_v1_bwd_workspace_size(self.B, self.N, self.H, self.dqk, self.dv)
@@ -169,7 +174,8 @@ class V1FwdBwd(V1Fwd):
         self.launches = None
 
     def run(self):
-        self.bd.diffattn_v1_fwd(*self.args(self.t), self.li, out=self.out, save=True)
+        self.bd.diffattn_v1_fwd(*self.args(self.t), self.li, out=self.out, save=True,
+                                saves=self.saves, workspace=self.fws)
         self.bd.diffattn_v1_bwd(*self.args(self.t), self.li, self.out, self.t["dy"], self.saves,
                                 grads=self.grads, workspace=self.ws)
 
@@ -195,6 +201,7 @@ class V1FwdF32(V1Fwd):
                                  device=dev)
         self.li = bd.diffattn_lambda_init(self.layer)
         self.out = torch.empty((self.B, self.N, self.H, self.dv), dtype=torch.float32, device=dev)
+        self.fws = None
 
 
 class V2Fwd(Workload):

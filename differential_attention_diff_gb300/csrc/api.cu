@@ -201,7 +201,8 @@ da_status diffattn_v2_decode(const da_v2_decode_params* p, void* stream) {
 size_t diffattn_v1_fwd_workspace_size(int B, int N, int H, int d_qk, int d_v, da_dtype dtype) {
   if (dtype != DA_BF16 || B <= 0 || N <= 0 || H <= 0 || d_qk <= 0 || d_v <= 0) return 0;
   DevInfo d = device_info();
-  return align256(da::v1_fwd_workspace_bytes(d.ok ? d.num_sms : 0));
+  const size_t n = da::v1_fwd_workspace_bytes(d.ok ? d.num_sms : 0);
+  return n ? align256(n) : 0;
 }
 
 da_status diffattn_v1_fwd(const da_v1_fwd_params* p, void* stream) {
@@ -228,7 +229,7 @@ da_status diffattn_v1_fwd(const da_v1_fwd_params* p, void* stream) {
   }
   if (p->d_qk != 128 || p->d_v != 256 || !p->causal) return DA_ERR_UNSUPPORTED;
   const size_t need = da::v1_fwd_workspace_bytes(d.num_sms);
-  if (p->workspace == nullptr || p->workspace_bytes < need || !aligned(p->workspace, 256))
+  if (need && (p->workspace == nullptr || p->workspace_bytes < need || !aligned(p->workspace, 256)))
     return DA_ERR_WORKSPACE;
   if (!da::tma_available()) return DA_ERR_CUDA;
   da::V1FwdArgs a{p->B, p->N, p->H, p->d_qk, p->d_v, p->causal, scale * kLog2e,

@@ -15,12 +15,13 @@
 // SM.  So a work item (batch, head, 128 query rows) runs on a cluster of two
 // CTAs: rank 0 computes stream 1, rank 1 stream 2, each from its own TMA
 // loads (V is read by both; the second read mostly hits L2).  In the
-// epilogue each CTA keeps half of the 256 output columns: it hands the other
-// half of its O/l to the partner through a 64 KB per-CTA slot of the
-// workspace (L2-resident), forms O = O1/l1 - lambda O2/l2 on its half, swaps
-// the per-row partial sums of squares with the partner through distributed
-// shared memory, and writes Y = (1 - lambda_init) O / sqrt(mean O^2 + eps).
-// Every hand-off is an mbarrier with a bounded wait (remote arrives at
+// epilogue each CTA keeps half of the 256 output columns: it writes the other
+// half of its O/l straight into the partner's shared memory (distributed
+// shared memory, into the partner's K ring, which is idle then: each CTA's
+// producer loads the next item's K tiles only after its own epilogue), forms
+// O = O1/l1 - lambda O2/l2 on its half, swaps the per-row partial sums of
+// squares the same way, and writes Y = (1 - lambda_init) O / sqrt(mean O^2 +
+// eps).  Every hand-off is an mbarrier with a bounded wait (remote arrives at
 // cluster scope).
 //
 //   TMEM: [0,128) S / P buffer 0, [128,256) S / P buffer 1, [256,512) O.
@@ -42,12 +43,11 @@ constexpr int kOffK = 2 * kBox;               // [stage][2 boxes]
 constexpr int kOffV = 6 * kBox;               // [stage][4 boxes]
 constexpr int kOffBar = 14 * kBox;            // 229376
 constexpr int kSmemBytes = kOffBar + 1024 + 1024;
-constexpr size_t kSlotBytes = 128 * 128 * sizeof(float);  // per CTA exchange slot
 
 enum {
   B_QFULL = 0, B_QEMPTY, B_KFULL, B_KFULL1, B_KEMPTY, B_KEMPTY1, B_VFULL, B_VFULL1,
   B_VEMPTY, B_VEMPTY1, B_SFULL, B_SFULL1, B_PFULL, B_PFULL1, B_ORDY, B_ODONE, B_DATA, B_SSQ,
-  B_COUNT
+  B_RXRDY, B_EPI, B_STG, B_SCHF, B_SCHE = B_SCHF + 4, B_COUNT = B_SCHE + 4
 };
 
 constexpr uint32_t kIdescS = idesc_bf16(128, 128, 0);
@@ -62,6 +62,9 @@ struct Shared {
     return reinterpret_cast<volatile int*>(gen + kOffBar + 264);
   }
   __device__ float* lam() const { return reinterpret_cast<float*>(gen + kOffBar + 268); }
+  // ring of the next work items (4 slots), written by rank 0's producer
+  __device__ volatile int* ring() const { return reinterpret_cast<volatile int*>(gen + kOffBar + 272); }
+  __device__ uint32_t ring_s(int slot) const { return base + kOffBar + 272 + 4 * slot; }
   __device__ uint32_t ssq_rx() const { return base + kOffBar + 512; }  // float[128]
   __device__ float* ssq_rx_ptr() const { return reinterpret_cast<float*>(gen + kOffBar + 512); }
 };
@@ -111,6 +114,14 @@ __device__ __forceinline__ void remote_arrive(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
                : "memory");
 }
+__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float4 v) {
+  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x),
+               "f"(v.y), "f"(v.z), "f"(v.w)
+               : "memory");
+}
+__device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v) {
+  asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
+}
 __device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
   asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
 }
@@ -145,7 +156,8 @@ __device__ __forceinline__ Item item_of(int i, int units, int H, int n_mtiles, i
 __global__ void __launch_bounds__(kThreads, 1)
 v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__ CUtensorMap tm_q2,
               const __grid_constant__ CUtensorMap tm_k1, const __grid_constant__ CUtensorMap tm_k2,
-              const __grid_constant__ CUtensorMap tm_v, V1FwdArgs a, float* __restrict__ xchg) {
+              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_out,
+              const __grid_constant__ CUtensorMap tm_o2, V1FwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   Shared sh;
   {
@@ -157,7 +169,6 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();         // 0: stream 1, 1: stream 2
   const uint32_t partner = rank ^ 1u;
-  const int cluster_id = blockIdx.x >> 1, n_clusters = gridDim.x >> 1;
   const int n_mtiles = (a.N + kBM - 1) / kBM;
   const int units = a.B * a.H;
   const int n_items = n_mtiles * units;
@@ -181,6 +192,13 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
     mbar_init(sh.bar(B_ODONE), 1);
     mbar_init(sh.bar(B_DATA), 128);
     mbar_init(sh.bar(B_SSQ), 128);
+    mbar_init(sh.bar(B_RXRDY), 128);
+    mbar_init(sh.bar(B_EPI), 128);
+    mbar_init(sh.bar(B_STG), 128);
+    for (int q = 0; q < 4; ++q) {
+      mbar_init(sh.bar(B_SCHF + q), 1);
+      mbar_init(sh.bar(B_SCHE + q), 11);  // rank 0: MMA + 4 softmax warps; rank 1: + its producer
+    }
     *sh.abort_flag() = 0;
     fence_mbar_init();
   }
@@ -217,12 +235,46 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
   tc_fence_after();
   const uint32_t tmem = *sh.tmem_slot();
 
+  // ---- dynamic work distribution ------------------------------------------
+  // Rank 0's producer takes item indices from a global counter (zeroed by the
+  // host before the launch; heaviest items come first in index order) and
+  // publishes them to a 4-slot ring in both CTAs; every role of both CTAs
+  // reads the same sequence.  Index >= n_items ends the sequence.
+  int* counter = static_cast<int*>(a.workspace);
+  auto publish = [&](int k) -> int {  // rank 0 producer only
+    const int slot = k & 3;
+    if (k >= 4 && !wait_bar(sh, sh.bar(B_SCHE + slot), ((k >> 2) - 1) & 1, a.status, 0x3008)) return -1;
+    const int idx = atomicAdd(counter, 1);
+    sh.ring()[slot] = idx;
+    st_cluster_s32(map_to_rank(sh.ring_s(slot), partner), idx);
+    mbar_arrive(sh.bar(B_SCHF + slot));
+    remote_arrive(map_to_rank(sh.bar(B_SCHF + slot), partner));
+    return idx;
+  };
+  // consumers: returns the k-th item index (-1 on timeout); `releaser` arrives
+  // on rank 0's slot-free barrier once the index has been read
+  auto release = [&](int k) {
+    const int slot = k & 3;
+    if (rank == 0) mbar_arrive(sh.bar(B_SCHE + slot));
+    else remote_arrive(map_to_rank(sh.bar(B_SCHE + slot), 0));
+  };
+  auto consume = [&](int k, bool releaser) -> int {
+    const int slot = k & 3;
+    if (!wait_bar<true>(sh, sh.bar(B_SCHF + slot), (k >> 2) & 1, a.status, 0x3009)) return -1;
+    const int idx = sh.ring()[slot];
+    if (releaser) release(k);
+    return idx;
+  };
+
   if (warp == 4) {
     // ------------------------------------------------------ TMA producer --
     if (lane == 0) {
-      int kv = 0, it = 0;
+      int kv = 0;
       bool ok = true;
-      for (int i = cluster_id; i < n_items && ok; i += n_clusters, ++it) {
+      for (int it = 0; ok; ++it) {
+        const int i = rank == 0 ? publish(it) : consume(it, true);
+        if (i < 0) { ok = false; break; }
+        if (i >= n_items) break;
         const Item w = item_of(i, units, a.H, n_mtiles, ub);
         if (it > 0 && !wait_bar(sh, sh.bar(B_QEMPTY), (it - 1) & 1, a.status, 0x3001)) { ok = false; break; }
         mbar_arrive_expect_tx(sh.bar(B_QFULL), 2 * kBox);
@@ -230,16 +282,31 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
           tma_load_4d(sh.base + kOffQ + box * kBox, tq, sh.bar(B_QFULL), box * 64, w.h, w.mt * kBM, w.b);
         for (int j = 0; j < w.n_kv; ++j, ++kv) {
           const int st = kv & 1, use = kv >> 1;
-          if (use > 0 && !wait_bar(sh, sh.bar(B_KEMPTY + st), (use - 1) & 1, a.status, 0x3002)) { ok = false; break; }
-          mbar_arrive_expect_tx(sh.bar(B_KFULL + st), 2 * kBox);
-          for (int box = 0; box < 2; ++box)
-            tma_load_4d(sh.base + kOffK + (st * 2 + box) * kBox, tk, sh.bar(B_KFULL + st), box * 64,
-                        w.h, j * kBN, w.b);
-          if (use > 0 && !wait_bar(sh, sh.bar(B_VEMPTY + st), (use - 1) & 1, a.status, 0x3003)) { ok = false; break; }
-          mbar_arrive_expect_tx(sh.bar(B_VFULL + st), 4 * kBox);
-          for (int box = 0; box < 4; ++box)
-            tma_load_4d(sh.base + kOffV + (st * 4 + box) * kBox, &tm_v, sh.bar(B_VFULL + st),
-                        box * 64, w.h, j * kBN, w.b);
+          auto load_k = [&]() -> bool {
+            if (use > 0 && !wait_bar(sh, sh.bar(B_KEMPTY + st), (use - 1) & 1, a.status, 0x3002)) return false;
+            mbar_arrive_expect_tx(sh.bar(B_KFULL + st), 2 * kBox);
+            for (int box = 0; box < 2; ++box)
+              tma_load_4d(sh.base + kOffK + (st * 2 + box) * kBox, tk, sh.bar(B_KFULL + st), box * 64,
+                          w.h, j * kBN, w.b);
+            return true;
+          };
+          auto load_v = [&]() -> bool {
+            if (use > 0 && !wait_bar(sh, sh.bar(B_VEMPTY + st), (use - 1) & 1, a.status, 0x3003)) return false;
+            mbar_arrive_expect_tx(sh.bar(B_VFULL + st), 4 * kBox);
+            for (int box = 0; box < 4; ++box)
+              tma_load_4d(sh.base + kOffV + (st * 4 + box) * kBox, &tm_v, sh.bar(B_VFULL + st),
+                          box * 64, w.h, j * kBN, w.b);
+            return true;
+          };
+          if (j == 0) {
+            // the K ring receives the partner's half of O during the previous
+            // item's epilogue: load K only once that epilogue is over
+            if (!load_v()) { ok = false; break; }
+            if (it > 0 && !wait_bar(sh, sh.bar(B_EPI), (it - 1) & 1, a.status, 0x3004)) { ok = false; break; }
+            if (!load_k()) { ok = false; break; }
+          } else {
+            if (!load_k() || !load_v()) { ok = false; break; }
+          }
         }
       }
       if (!ok) {
@@ -269,7 +336,10 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
       auto wait_k = [&](int g) {
         return wait_bar(sh, sh.bar(B_KFULL + (g & 1)), (g >> 1) & 1, a.status, 0x3102);
       };
-      for (int i = cluster_id; i < n_items && ok; i += n_clusters, ++it) {
+      for (;; ++it) {
+        const int i = consume(it, true);
+        if (i < 0) { ok = false; break; }
+        if (i >= n_items) break;
         const Item w = item_of(i, units, a.H, n_mtiles, ub);
         const int n = w.n_kv;
         if (!wait_bar(sh, sh.bar(B_QFULL), it & 1, a.status, 0x3101)) { ok = false; break; }
@@ -317,15 +387,21 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
     const float sl2 = a.scale_log2;
     const float lam = *sh.lam();
     const float cscale = 1.f - a.lambda_init;
-    float* my_slot = xchg + (static_cast<size_t>(cluster_id) * 2 + rank) * (kSlotBytes / 4) + row * 128;
-    const float* other_slot =
-        xchg + (static_cast<size_t>(cluster_id) * 2 + partner) * (kSlotBytes / 4) + row * 128;
+    // receive buffer: this CTA's K ring, row r at r * 512 bytes
+    const uint8_t* my_rx = sh.gen + kOffK + row * 512;
+    const uint32_t partner_rx = map_to_rank(sh.base + kOffK + row * 512, partner);
+    const uint32_t partner_rxrdy = map_to_rank(sh.bar(B_RXRDY), partner);
     const uint32_t partner_data = map_to_rank(sh.bar(B_DATA), partner);
     const uint32_t partner_ssq_bar = map_to_rank(sh.bar(B_SSQ), partner);
     const uint32_t partner_ssq_slot = map_to_rank(sh.ssq_rx() + row * 4, partner);
     int kv = 0, it = 0;
     bool ok = true;
-    for (int i = cluster_id; i < n_items && ok; i += n_clusters, ++it) {
+    for (;; ++it) {
+      const int i = consume(it, false);
+      __syncwarp();
+      if (lane == 0 && i >= 0) release(it);  // the whole warp has read the slot
+      if (i < 0) { ok = false; break; }
+      if (i >= n_items) break;
       const Item w = item_of(i, units, a.H, n_mtiles, ub);
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < w.n_kv; ++j) {
@@ -358,18 +434,24 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
       if (!wait_bar(sh, sh.bar(B_ORDY), it & 1, a.status, 0x3203)) { ok = false; break; }
       tc_fence_after();
       const float inv_l = 1.f / l_run;
-      // (1) the partner's half of my normalised O -> my exchange slot
       const int give = (1 - static_cast<int>(rank)) * 128, keep = static_cast<int>(rank) * 128;
+      // (1) my MMAs are done, so my K ring may receive; wait until the
+      //     partner's is free too, then write the partner's half of my O/l
+      //     into it (row r: 512 bytes, 16-byte chunks XOR-swizzled by r & 7)
+      remote_arrive(partner_rxrdy);
+      if (!wait_bar<true>(sh, sh.bar(B_RXRDY), it & 1, a.status, 0x3206)) { ok = false; break; }
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
-        uint32_t o[32];
-        tmem_ld32(t_o + give + c * 32, o);
+      for (int c2 = 0; c2 < 2; ++c2) {
+        uint32_t o[64];
+        tmem_ld32(t_o + give + c2 * 64, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
+        tmem_ld32(t_o + give + c2 * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          float4 v = make_float4(__uint_as_float(o[e]) * inv_l, __uint_as_float(o[e + 1]) * inv_l,
-                                 __uint_as_float(o[e + 2]) * inv_l, __uint_as_float(o[e + 3]) * inv_l);
-          __stcg(reinterpret_cast<float4*>(my_slot + c * 32 + e), v);
+        for (int e = 0; e < 64; e += 4) {
+          const int u = (c2 * 64 + e) >> 2;
+          st_cluster_v4(partner_rx + ((u ^ (row & 7)) << 4),
+                        make_float4(__uint_as_float(o[e]) * inv_l, __uint_as_float(o[e + 1]) * inv_l,
+                                    __uint_as_float(o[e + 2]) * inv_l, __uint_as_float(o[e + 3]) * inv_l));
         }
       }
       remote_arrive(partner_data);
@@ -379,10 +461,13 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
       float ssq = 0.f;
       const int n = w.mt * kBM + row;
       const bool live = n < a.N;
-      __nv_bfloat16* o2dst = (a.o2.ptr && live)
-          ? static_cast<__nv_bfloat16*>(a.o2.ptr) + w.b * a.o2.sb + static_cast<int64_t>(n) * a.o2.sn +
-                w.h * a.o2.sh + keep
-          : nullptr;
+      // staging for the TMA stores: the V stage of this item's last tile,
+      // idle until the producer loads the next item's second V tile (after
+      // this epilogue): Y in boxes 0-1, O2 in boxes 2-3, 128-byte swizzle
+      const int stg_stage = (kv - 1) & 1;
+      uint8_t* stg = sh.gen + kOffV + stg_stage * 4 * kBox;
+      const uint32_t stg_s = sh.base + kOffV + stg_stage * 4 * kBox;
+      const bool want_o2 = a.o2.ptr != nullptr;
 #pragma unroll
       for (int c = 0; c < 4; ++c) {
         uint32_t o[32];
@@ -391,28 +476,31 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
         float o2v[32];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
-          const float4 oth = __ldcg(reinterpret_cast<const float4*>(other_slot + c * 32 + e));
+          const int u = (c * 32 + e) >> 2;
+          const float4 oth = *reinterpret_cast<const float4*>(my_rx + ((u ^ (row & 7)) << 4));
           const float othv[4] = {oth.x, oth.y, oth.z, oth.w};
 #pragma unroll
-          for (int u = 0; u < 4; ++u) {
-            const float own = __uint_as_float(o[e + u]) * inv_l;
-            const float a1 = rank == 0 ? own : othv[u];
-            const float a2 = rank == 0 ? othv[u] : own;
+          for (int q = 0; q < 4; ++q) {
+            const float own = __uint_as_float(o[e + q]) * inv_l;
+            const float a1 = rank == 0 ? own : othv[q];
+            const float a2 = rank == 0 ? othv[q] : own;
             const float dd = __fsub_rn(a1, __fmul_rn(lam, a2));
-            dvals[c * 32 + e + u] = dd;
+            dvals[c * 32 + e + q] = dd;
             ssq = fmaf(dd, dd, ssq);
-            o2v[e + u] = a2;
+            o2v[e + q] = a2;
           }
         }
-        if (o2dst) {
+        if (want_o2) {
 #pragma unroll
           for (int e = 0; e < 32; e += 8) {
+            const int col = c * 32 + e;  // 0..127 within this CTA's half
             uint4 pk;
             pk.x = pack_bf16x2(o2v[e], o2v[e + 1]);
             pk.y = pack_bf16x2(o2v[e + 2], o2v[e + 3]);
             pk.z = pack_bf16x2(o2v[e + 4], o2v[e + 5]);
             pk.w = pack_bf16x2(o2v[e + 6], o2v[e + 7]);
-            *reinterpret_cast<uint4*>(o2dst + c * 32 + e) = pk;
+            *reinterpret_cast<uint4*>(stg + (2 + (col >> 6)) * kBox + row * 128 +
+                                      ((((col & 63) >> 3) ^ (row & 7)) << 4)) = pk;
           }
         }
       }
@@ -423,23 +511,37 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
       const float tot = rank == 0 ? ssq + other_ssq : other_ssq + ssq;
       const float rstd = 1.f / sqrtf(tot * (1.f / kDv) + a.rms_eps);
       const float cs = cscale * rstd;
-      if (live) {
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out.ptr) + w.b * a.out.sb +
-                             static_cast<int64_t>(n) * a.out.sn + w.h * a.out.sh + keep;
 #pragma unroll
-        for (int e = 0; e < 128; e += 8) {
-          uint4 pk;
-          pk.x = pack_bf16x2(__fmul_rn(dvals[e], cs), __fmul_rn(dvals[e + 1], cs));
-          pk.y = pack_bf16x2(__fmul_rn(dvals[e + 2], cs), __fmul_rn(dvals[e + 3], cs));
-          pk.z = pack_bf16x2(__fmul_rn(dvals[e + 4], cs), __fmul_rn(dvals[e + 5], cs));
-          pk.w = pack_bf16x2(__fmul_rn(dvals[e + 6], cs), __fmul_rn(dvals[e + 7], cs));
-          *reinterpret_cast<uint4*>(dst + e) = pk;
-        }
+      for (int e = 0; e < 128; e += 8) {
+        uint4 pk;
+        pk.x = pack_bf16x2(__fmul_rn(dvals[e], cs), __fmul_rn(dvals[e + 1], cs));
+        pk.y = pack_bf16x2(__fmul_rn(dvals[e + 2], cs), __fmul_rn(dvals[e + 3], cs));
+        pk.z = pack_bf16x2(__fmul_rn(dvals[e + 4], cs), __fmul_rn(dvals[e + 5], cs));
+        pk.w = pack_bf16x2(__fmul_rn(dvals[e + 6], cs), __fmul_rn(dvals[e + 7], cs));
+        *reinterpret_cast<uint4*>(stg + (e >> 6) * kBox + row * 128 + ((((e & 63) >> 3) ^ (row & 7)) << 4)) = pk;
+      }
+      if (live) {
         const int64_t sidx = (static_cast<int64_t>(w.b) * a.H + w.h) * a.N + n;
         float* lse = rank == 0 ? a.lse1 : a.lse2;
         if (lse) lse[sidx] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
         if (rank == 0 && a.rstd) a.rstd[sidx] = rstd;
       }
+      // all rows staged -> one thread stores the tiles with TMA (rows past N
+      // are dropped), waits until the staging has been read, then the K ring
+      // and this V stage may take the next item's tiles
+      fence_proxy_async_smem();
+      mbar_arrive(sh.bar(B_STG));
+      if (!wait_bar(sh, sh.bar(B_STG), it & 1, a.status, 0x3207)) { ok = false; break; }
+      if (row == 0) {
+        for (int bx = 0; bx < 2; ++bx)
+          tma_store_4d(&tm_out, stg_s + bx * kBox, keep + bx * 64, w.h, w.mt * kBM, w.b);
+        if (want_o2)
+          for (int bx = 0; bx < 2; ++bx)
+            tma_store_4d(&tm_o2, stg_s + (2 + bx) * kBox, keep + bx * 64, w.h, w.mt * kBM, w.b);
+        bulk_commit();
+        bulk_wait_read();
+      }
+      mbar_arrive(sh.bar(B_EPI));
       tc_fence_before();
     }
   }
@@ -453,10 +555,8 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
 
 }  // namespace
 
-size_t v1_fwd_workspace_bytes(int num_sms) {
-  const int clusters = (num_sms > 0 ? num_sms : 152) / 2;
-  return static_cast<size_t>(clusters) * 2 * kSlotBytes;
-}
+// the work counter of the dynamic schedule
+size_t v1_fwd_workspace_bytes(int) { return 256; }
 
 cudaError_t launch_v1_fwd(const V1FwdArgs& a, cudaStream_t s) {
   CUtensorMap tq1, tq2, tk1, tk2, tv;
@@ -465,6 +565,10 @@ cudaError_t launch_v1_fwd(const V1FwdArgs& a, cudaStream_t s) {
       !encode_tmap_bf16_4d(&tk1, a.k1, a.B, a.N, a.H, kDqk, kBN) ||
       !encode_tmap_bf16_4d(&tk2, a.k2, a.B, a.N, a.H, kDqk, kBN) ||
       !encode_tmap_bf16_4d(&tv, a.v, a.B, a.N, a.H, kDv, kBN))
+    return cudaErrorInvalidValue;
+  CUtensorMap tout, to2;
+  if (!encode_tmap_bf16_4d(&tout, a.out, a.B, a.N, a.H, kDv, kBM) ||
+      !encode_tmap_bf16_4d(&to2, a.o2.ptr ? a.o2 : a.out, a.B, a.N, a.H, kDv, kBM))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(v1_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemBytes);
@@ -486,14 +590,13 @@ cudaError_t launch_v1_fwd(const V1FwdArgs& a, cudaStream_t s) {
   cfg.gridDim = dim3(2 * ((a.num_sms > 0 ? a.num_sms : 152) / 2), 1, 1);
   e = cudaOccupancyMaxActiveClusters(&max_clusters, v1_fwd_kernel, &cfg);
   if (e != cudaSuccess || max_clusters <= 0) max_clusters = (a.num_sms > 0 ? a.num_sms : 152) / 2;
-  const int ws_clusters = static_cast<int>(a.workspace_bytes / (2 * kSlotBytes));
   int clusters = max_clusters;
-  if (clusters > ws_clusters) clusters = ws_clusters;
   if (clusters > n_items) clusters = n_items;
   if (clusters <= 0) return cudaErrorInvalidValue;
   cfg.gridDim = dim3(2 * clusters, 1, 1);
-  return cudaLaunchKernelEx(&cfg, v1_fwd_kernel, tq1, tq2, tk1, tk2, tv, a,
-                            static_cast<float*>(a.workspace));
+  e = cudaMemsetAsync(a.workspace, 0, sizeof(int), s);
+  if (e != cudaSuccess) return e;
+  return cudaLaunchKernelEx(&cfg, v1_fwd_kernel, tq1, tq2, tk1, tk2, tv, tout, to2, a);
 }
 
 }  // namespace da

@@ -83,10 +83,9 @@ float diffattn_lambda_init(int layer);
  *   (1/sqrt(mean O^2 + eps)): fp32 [B, H, N] contiguous;
  *   o2 = softmax(s Q2 K2^T) V: [B, N, H, d_v] of `dtype`;
  *   lambda_out: fp32 [1].
- * workspace: the bf16 path runs each (batch, head, 128-row) tile on a pair
- * of CTAs (one per softmax stream) that exchange half of their outputs
- * through it; at least diffattn_v1_fwd_workspace_size(...) bytes, 256-byte
- * aligned, contents on entry irrelevant (0 bytes for DA_F32). */
+ * workspace: diffattn_v1_fwd_workspace_size(...) bytes (a work counter of
+ * the bf16 path's dynamic schedule; 0 for DA_F32), 256-byte aligned,
+ * contents on entry irrelevant (the call clears it on the stream). */
 typedef struct {
   int B, N, H, d_qk, d_v;
   da_dtype dtype;
