@@ -18,6 +18,9 @@ namespace da {
 // out-of-range rows read as zero.
 bool encode_tmap_bf16_4d(CUtensorMap* map, const da_t4& t, int B, int N, int H,
                          int D, int rows);
+// A 4-D fp32 tensor map over a contiguous [B, N, H, D] tensor, box = {D, 1,
+// rows, 1}, no swizzle (used for reduce-adds of fp32 tiles).
+bool encode_tmap_f32_4d(CUtensorMap* map, void* ptr, int B, int N, int H, int D, int rows);
 
 // ---------------------------------------------------------------- device ---
 // Every wait below is bounded: after kSpinLimit polls it records
@@ -85,6 +88,17 @@ __device__ __forceinline__ void tma_store_4d(const CUtensorMap* map, uint32_t sr
       "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
       : "memory");
 }
+// 4-D TMA reduce-add (fp32) of a shared-memory tile into global memory.
+__device__ __forceinline__ void tma_reduce_add_4d(const CUtensorMap* map, uint32_t src, int c0,
+                                                  int c1, int c2, int c3) {
+  asm volatile(
+      "cp.reduce.async.bulk.tensor.4d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3, %4, %5}], [%1];" ::"l"(
+          reinterpret_cast<uint64_t>(map)),
+      "r"(src), "r"(c0), "r"(c1), "r"(c2), "r"(c3)
+      : "memory");
+}
+// Wait until every bulk operation of this thread has completed.
+__device__ __forceinline__ void bulk_wait_all() { asm volatile("cp.async.bulk.wait_group 0;" ::: "memory"); }
 __device__ __forceinline__ void bulk_commit() { asm volatile("cp.async.bulk.commit_group;" ::: "memory"); }
 // Wait until every bulk store of this thread has finished reading shared memory.
 __device__ __forceinline__ void bulk_wait_read() {

@@ -27,8 +27,9 @@
 //        softmax warps (thread = key row): P = exp2(S^T s log2e - lse2),
 //          dS^T = sigma s P (dP^T - D), Psig^T = sigma P  (sigma = 1 or
 //          -lambda), both as bf16 rows into shared memory
-//        dQ^T = K^T dS^T       (TMEM, reusing the dP^T columns) -> fp32
-//                               reductions into the workspace
+//        dQ^T = K^T dS^T       (TMEM, reusing the dP^T columns) -> staged in
+//                               shared memory, TMA reduce-add into the fp32
+//                               accumulator in the workspace
 //        dV  += Psig^T dO      (TMEM, 256 columns)
 //        dK  += dS^T Q         (TMEM, 128 columns)
 //     At the end each CTA writes its dK; the dV halves of the two streams are
@@ -39,7 +40,10 @@
 // SMEM: K 32 KB, V 64 KB, 2 stages of (Q 16 KB, dO 32 KB), Psig^T and dS^T
 //       16 KB each, lse2 and D of both stages (1 KB); every operand in 128-byte-swizzled
 //       64-column boxes (used K-major or MN-major by the MMAs as needed).
+#include <type_traits>
+
 #include "kernels.h"
+#include "softmax.cuh"
 #include "tma.cuh"
 
 namespace da {
@@ -66,7 +70,7 @@ constexpr int kSmemBytes = kOffBar + 512 + 1024;   // 231936 <= 232448
 
 enum {
   B_KV = 0, B_QFULL, B_QFULL1, B_QEMPTY, B_QEMPTY1, B_SFULL, B_DPFULL, B_PFULL, B_DQFULL,
-  B_DQFREE, B_PBFREE, B_ACC, B_RTR, B_DATA, B_COUNT
+  B_DQFREE, B_PBFREE, B_ACC, B_RTR, B_DATA, B_STG, B_STGFREE, B_COUNT
 };
 
 __host__ __device__ constexpr uint32_t idesc2(int M, int N, int a_mn, int b_mn) {
@@ -156,9 +160,6 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
       "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
       "l"(src), "r"(bytes), "r"(bar)
       : "memory");
-}
-__device__ __forceinline__ void red_add(float* p, float v) {
-  asm volatile("red.global.add.f32 [%0], %1;" ::"l"(p), "f"(v) : "memory");
 }
 
 // --------------------------------------------------------------------------
@@ -323,6 +324,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__ CUtensorMap tm_q2,
                    const __grid_constant__ CUtensorMap tm_k1, const __grid_constant__ CUtensorMap tm_k2,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_do,
+                   const __grid_constant__ CUtensorMap tm_dq1, const __grid_constant__ CUtensorMap tm_dq2,
                    V1BwdArgs a, BwdWs w) {
   extern __shared__ uint8_t smem_raw[];
   Shared sh;
@@ -353,8 +355,8 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
   const CUtensorMap* tq = rank == 0 ? &tm_q1 : &tm_q2;
   const CUtensorMap* tk = rank == 0 ? &tm_k1 : &tm_k2;
   const float* lse2 = w.lse2[rank];
+  const CUtensorMap* tdq = rank == 0 ? &tm_dq1 : &tm_dq2;
   const float* Dv = w.D[rank];
-  float* dq = w.dq[rank];
 
   if (threadIdx.x == 0) {
     mbar_init(sh.bar(B_KV), 1);
@@ -371,6 +373,8 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
     mbar_init(sh.bar(B_ACC), 1);
     mbar_init(sh.bar(B_RTR), 128);
     mbar_init(sh.bar(B_DATA), 128);
+    mbar_init(sh.bar(B_STG), 128);
+    mbar_init(sh.bar(B_STGFREE), 1);
     *sh.abort_flag() = 0;
     fence_mbar_init();
   }
@@ -464,13 +468,7 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
                     kIdDQ, kk > 0);
         tc_commit(sh.bar(B_DQFULL));
         const bool more = k + 1 < it.n_it;
-        if (more) {
-          if (!wait_bar(sh, sh.bar(B_QFULL + ((k + 1) & 1)), ((k + 1) >> 1) & 1, a.status, 0x4104)) { ok = false; break; }
-          tc_fence_after();
-          issue_s(k + 1);
-          tc_commit(sh.bar(B_SFULL));
-        }
-        // dV += Psig^T dO ; dK += dS^T Q
+        // dV += Psig^T dO ; dK += dS^T Q  (so the P / dS buffers free early)
         const uint32_t db = stage(k) + kStageDO, qb = stage(k) + kStageQ;
 #pragma unroll
         for (int kk = 0; kk < kQT / 16; ++kk)
@@ -483,6 +481,10 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
         tc_commit(sh.bar(B_PBFREE));
         tc_commit(sh.bar(B_QEMPTY + (k & 1)));
         if (more) {
+          if (!wait_bar(sh, sh.bar(B_QFULL + ((k + 1) & 1)), ((k + 1) >> 1) & 1, a.status, 0x4104)) { ok = false; break; }
+          tc_fence_after();
+          issue_s(k + 1);
+          tc_commit(sh.bar(B_SFULL));
           if (!wait_bar(sh, sh.bar(B_DQFREE), ph, a.status, 0x4105)) { ok = false; break; }
           tc_fence_after();
           issue_dp(k + 1);
@@ -499,6 +501,7 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
     const float sigma = rank == 0 ? 1.f : -lam;
     const float sds = sigma * a.scale;
     const float sl2 = a.scale * 1.4426950408889634f;
+    const uint64_t sl2x2 = f2(sl2, sl2), sds2 = f2(sds, sds), sig2 = f2(sigma, sigma);
     const int key = it.kt * kKT + r;
     bool ok = true;
     uint8_t* pbuf = sh.gen + kOffP;
@@ -508,7 +511,6 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
       const int q0 = (it.i0 + k) * kQT;
       if (!wait_bar(sh, sh.bar(B_SFULL), ph, a.status, 0x4201)) { ok = false; break; }
       if (!wait_bar(sh, sh.bar(B_DPFULL), ph, a.status, 0x4202)) { ok = false; break; }
-      if (k > 0 && !wait_bar(sh, sh.bar(B_PBFREE), (k - 1) & 1, a.status, 0x4203)) { ok = false; break; }
       tc_fence_after();
       uint32_t sv[64], dp[64];
       tmem_ld32(T_S + loff, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
@@ -516,29 +518,52 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
       tmem_ld32(T_DP + loff, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
       tmem_ld32(T_DP + loff + 32, *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
       tmem_ld_wait();
-      const float* l2 = reinterpret_cast<const float*>(sh.gen + kOffLse + (k & 1) * 512);
-      const float* dd = l2 + 64;
+      const float4* l2v = reinterpret_cast<const float4*>(sh.gen + kOffLse + (k & 1) * 512);
+      const float4* ddv = l2v + 16;
       const bool diag = q0 < it.kt * kKT + kKT;  // a query of this tile may precede a key
+      uint32_t pw[32], dw[32];
+      auto tile = [&](auto masked) {
+        constexpr bool kMask = decltype(masked)::value;
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {  // 8 queries per 16-byte chunk
-        uint32_t pw[4], dw[4];
-#pragma unroll
-        for (int e = 0; e < 8; e += 2) {
-          const int c = ch * 8 + e;
-          float p0 = fast_exp2(fmaf(__uint_as_float(sv[c]), sl2, -l2[c]));
-          float p1 = fast_exp2(fmaf(__uint_as_float(sv[c + 1]), sl2, -l2[c + 1]));
-          if (diag) {
+        for (int q4 = 0; q4 < 16; ++q4) {  // 4 queries at a time
+          const float4 lq = l2v[q4];
+          const float4 dq4 = ddv[q4];
+          const int c = q4 * 4;
+          const uint64_t x01 = fma_f32x2(f2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2x2,
+                                         f2(-lq.x, -lq.y));
+          const uint64_t x23 = fma_f32x2(f2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), sl2x2,
+                                         f2(-lq.z, -lq.w));
+          float p0 = fast_exp2(f2_lo(x01)), p1 = fast_exp2(f2_hi(x01));
+          float p2 = fast_exp2(f2_lo(x23)), p3 = fast_exp2(f2_hi(x23));
+          if (kMask) {
             if (key > q0 + c) p0 = 0.f;
             if (key > q0 + c + 1) p1 = 0.f;
+            if (key > q0 + c + 2) p2 = 0.f;
+            if (key > q0 + c + 3) p3 = 0.f;
           }
-          const float ds0 = p0 * (__uint_as_float(dp[c]) - dd[c]) * sds;
-          const float ds1 = p1 * (__uint_as_float(dp[c + 1]) - dd[c + 1]) * sds;
-          pw[e / 2] = pack_bf16x2(p0 * sigma, p1 * sigma);
-          dw[e / 2] = pack_bf16x2(ds0, ds1);
+          const uint64_t t01 = add_f32x2(f2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), f2(-dq4.x, -dq4.y));
+          const uint64_t t23 = add_f32x2(f2(__uint_as_float(dp[c + 2]), __uint_as_float(dp[c + 3])), f2(-dq4.z, -dq4.w));
+          const uint64_t p01 = f2(p0, p1), p23 = f2(p2, p3);
+          const uint64_t d01 = mul_f32x2(mul_f32x2(t01, p01), sds2);
+          const uint64_t d23 = mul_f32x2(mul_f32x2(t23, p23), sds2);
+          const uint64_t s01 = mul_f32x2(p01, sig2), s23 = mul_f32x2(p23, sig2);
+          pw[q4 * 2] = pack_bf16x2(f2_lo(s01), f2_hi(s01));
+          pw[q4 * 2 + 1] = pack_bf16x2(f2_lo(s23), f2_hi(s23));
+          dw[q4 * 2] = pack_bf16x2(f2_lo(d01), f2_hi(d01));
+          dw[q4 * 2 + 1] = pack_bf16x2(f2_lo(d23), f2_hi(d23));
         }
+      };
+      if (diag) tile(std::true_type{});
+      else tile(std::false_type{});
+      // the P / dS buffers are free once dV(k-1) and dK(k-1) have read them
+      // and the TMA reduce has read the dQ tile staged there after them
+      if (k > 0 && !wait_bar(sh, sh.bar(B_PBFREE), (k - 1) & 1, a.status, 0x4203)) { ok = false; break; }
+      if (k > 0 && !wait_bar(sh, sh.bar(B_STGFREE), (k - 1) & 1, a.status, 0x4208)) { ok = false; break; }
+#pragma unroll
+      for (int ch = 0; ch < 8; ++ch) {
         const int off = r * 128 + ((ch ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(pbuf + off) = make_uint4(pw[0], pw[1], pw[2], pw[3]);
-        *reinterpret_cast<uint4*>(dsbuf + off) = make_uint4(dw[0], dw[1], dw[2], dw[3]);
+        *reinterpret_cast<uint4*>(pbuf + off) = make_uint4(pw[ch * 4], pw[ch * 4 + 1], pw[ch * 4 + 2], pw[ch * 4 + 3]);
+        *reinterpret_cast<uint4*>(dsbuf + off) = make_uint4(dw[ch * 4], dw[ch * 4 + 1], dw[ch * 4 + 2], dw[ch * 4 + 3]);
       }
       fence_proxy_async_smem();
       tc_fence_before();
@@ -552,13 +577,24 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(sh.bar(B_DQFREE));
-      const int nq = min(kQT, a.N - q0);
-      float* dqp = dq + ((static_cast<int64_t>(it.b) * a.N + q0) * a.H + it.h) * kDqk + r;
-      const int64_t qstride = static_cast<int64_t>(a.H) * kDqk;
+      // stage the dQ tile [64 queries][128 features] fp32 in the P / dS
+      // buffers once dV(k) / dK(k) have read them; one thread adds it to the
+      // fp32 accumulator with a TMA reduce (rows past N are dropped)
+      if (!wait_bar(sh, sh.bar(B_PBFREE), ph, a.status, 0x4209)) { ok = false; break; }
+      float* stage_dq = reinterpret_cast<float*>(pbuf);
 #pragma unroll
-      for (int c = 0; c < kQT; ++c)
-        if (c < nq) red_add(dqp + c * qstride, __uint_as_float(qv[c]));
+      for (int c = 0; c < kQT; ++c) stage_dq[c * kDqk + r] = __uint_as_float(qv[c]);
+      fence_proxy_async_smem();
+      mbar_arrive(sh.bar(B_STG));
+      if (r == 0) {
+        if (!wait_bar(sh, sh.bar(B_STG), ph, a.status, 0x420A)) { ok = false; break; }
+        tma_reduce_add_4d(tdq, sh.base + kOffP, 0, it.h, q0, it.b);
+        bulk_commit();
+        bulk_wait_read();
+        mbar_arrive(sh.bar(B_STGFREE));
+      }
     }
+    if (r == 0) bulk_wait_all();
     // ----------------------------------------------------------- epilogue --
     if (ok && wait_bar(sh, sh.bar(B_ACC), 0, a.status, 0x4205)) {
       tc_fence_after();
@@ -736,7 +772,11 @@ cudaError_t launch_v1_bwd(const V1BwdArgs& a, cudaStream_t s) {
   cfg.stream = s;
   cfg.attrs = attr;
   cfg.numAttrs = 1;
-  e = cudaLaunchKernelEx(&cfg, v1_bwd_main_kernel, tq1, tq2, tk1, tk2, tv, tdo, a, w);
+  CUtensorMap tdq1, tdq2;
+  if (!encode_tmap_f32_4d(&tdq1, w.dq[0], a.B, a.N, a.H, kDqk, kQT) ||
+      !encode_tmap_f32_4d(&tdq2, w.dq[1], a.B, a.N, a.H, kDqk, kQT))
+    return cudaErrorInvalidValue;
+  e = cudaLaunchKernelEx(&cfg, v1_bwd_main_kernel, tq1, tq2, tk1, tk2, tv, tdo, tdq1, tdq2, a, w);
   if (e != cudaSuccess) return e;
 
   const long long work = static_cast<long long>(a.B) * a.N * a.H * (kDqk / 8);
