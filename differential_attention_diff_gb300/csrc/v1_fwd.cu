@@ -15,10 +15,11 @@
 // SM.  So a work item (batch, head, 128 query rows) runs on a cluster of two
 // CTAs: rank 0 computes stream 1, rank 1 stream 2, each from its own TMA
 // loads (V is read by both; the second read mostly hits L2).  In the
-// epilogue each CTA keeps half of the 256 output columns: it writes the other
-// half of its O/l straight into the partner's shared memory (distributed
-// shared memory, into the partner's K ring, which is idle then: each CTA's
-// producer loads the next item's K tiles only after its own epilogue), forms
+// epilogue each CTA keeps half of the 256 output columns: it stages the other
+// half of its O/l in an idle V stage and one bulk copy moves it into the
+// partner's shared memory (distributed shared memory, into the partner's K
+// ring, which is idle then: each CTA's producer loads the next item's K tiles
+// only after its own epilogue has read the ring), forms
 // O = O1/l1 - lambda O2/l2 on its half, swaps the per-row partial sums of
 // squares the same way, and writes Y = (1 - lambda_init) O / sqrt(mean O^2 +
 // eps).  Every hand-off is an mbarrier with a bounded wait (remote arrives at
@@ -47,7 +48,7 @@ constexpr int kSmemBytes = kOffBar + 1024 + 1024;
 enum {
   B_QFULL = 0, B_QEMPTY, B_KFULL, B_KFULL1, B_KEMPTY, B_KEMPTY1, B_VFULL, B_VFULL1,
   B_VEMPTY, B_VEMPTY1, B_SFULL, B_SFULL1, B_PFULL, B_PFULL1, B_ORDY, B_ODONE, B_DATA, B_SSQ,
-  B_RXRDY, B_EPI, B_STG, B_SCHF, B_SCHE = B_SCHF + 4, B_COUNT = B_SCHE + 4
+  B_RXRDY, B_RXFREE, B_STG, B_STGFREE, B_GIVE, B_SCHF, B_SCHE = B_SCHF + 4, B_COUNT = B_SCHE + 4
 };
 
 constexpr uint32_t kIdescS = idesc_bf16(128, 128, 0);
@@ -114,10 +115,15 @@ __device__ __forceinline__ void remote_arrive(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
                : "memory");
 }
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float4 v) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x),
-               "f"(v.y), "f"(v.z), "f"(v.w)
-               : "memory");
+// shared::cta -> a cluster peer's shared memory, completion counted in bytes
+// on the peer's mbarrier
+__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
+                                                  uint32_t bar_cluster) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
+          dst_cluster),
+      "r"(src), "r"(bytes), "r"(bar_cluster)
+      : "memory");
 }
 __device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v) {
   asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
@@ -190,10 +196,12 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
     }
     mbar_init(sh.bar(B_ORDY), 1);
     mbar_init(sh.bar(B_ODONE), 1);
-    mbar_init(sh.bar(B_DATA), 128);
+    mbar_init(sh.bar(B_DATA), 1);  // + 64 KB of bulk-copy bytes from the partner
     mbar_init(sh.bar(B_SSQ), 128);
-    mbar_init(sh.bar(B_RXRDY), 128);
-    mbar_init(sh.bar(B_EPI), 128);
+    mbar_init(sh.bar(B_RXRDY), 1);
+    mbar_init(sh.bar(B_GIVE), 128);
+    mbar_init(sh.bar(B_RXFREE), 128);
+    mbar_init(sh.bar(B_STGFREE), 1);
     mbar_init(sh.bar(B_STG), 128);
     for (int q = 0; q < 4; ++q) {
       mbar_init(sh.bar(B_SCHF + q), 1);
@@ -271,7 +279,16 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
     if (lane == 0) {
       int kv = 0;
       bool ok = true;
+      // epilogues whose Y / O2 staging still occupies a V stage: the last tile
+      // of item `seq` used stage tile & 1; a V load into that stage for a
+      // later tile waits until the item's TMA stores have read the staging
+      int pend_tile[4], pend_seq[4], npend = 0;
       for (int it = 0; ok; ++it) {
+        if (it > 0 && npend < 4) {
+          pend_tile[npend] = kv - 1;
+          pend_seq[npend] = it - 1;
+          ++npend;
+        }
         const int i = rank == 0 ? publish(it) : consume(it, true);
         if (i < 0) { ok = false; break; }
         if (i >= n_items) break;
@@ -291,6 +308,16 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
             return true;
           };
           auto load_v = [&]() -> bool {
+            // release staging entries in order: the head when this load
+            // reuses its stage, or once the load is two tiles past it
+            while (npend > 0 && kv > pend_tile[0] + ((pend_tile[0] & 1) == st ? 0 : 1)) {
+              if (!wait_bar(sh, sh.bar(B_STGFREE), pend_seq[0] & 1, a.status, 0x3005)) return false;
+              for (int q = 1; q < npend; ++q) {
+                pend_tile[q - 1] = pend_tile[q];
+                pend_seq[q - 1] = pend_seq[q];
+              }
+              --npend;
+            }
             if (use > 0 && !wait_bar(sh, sh.bar(B_VEMPTY + st), (use - 1) & 1, a.status, 0x3003)) return false;
             mbar_arrive_expect_tx(sh.bar(B_VFULL + st), 4 * kBox);
             for (int box = 0; box < 4; ++box)
@@ -300,9 +327,9 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
           };
           if (j == 0) {
             // the K ring receives the partner's half of O during the previous
-            // item's epilogue: load K only once that epilogue is over
+            // item's epilogue: load K once every row has read it
             if (!load_v()) { ok = false; break; }
-            if (it > 0 && !wait_bar(sh, sh.bar(B_EPI), (it - 1) & 1, a.status, 0x3004)) { ok = false; break; }
+            if (it > 0 && !wait_bar(sh, sh.bar(B_RXFREE), (it - 1) & 1, a.status, 0x3004)) { ok = false; break; }
             if (!load_k()) { ok = false; break; }
           } else {
             if (!load_k() || !load_v()) { ok = false; break; }
@@ -389,7 +416,7 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
     const float cscale = 1.f - a.lambda_init;
     // receive buffer: this CTA's K ring, row r at r * 512 bytes
     const uint8_t* my_rx = sh.gen + kOffK + row * 512;
-    const uint32_t partner_rx = map_to_rank(sh.base + kOffK + row * 512, partner);
+    const uint32_t partner_rx0 = map_to_rank(sh.base + kOffK, partner);
     const uint32_t partner_rxrdy = map_to_rank(sh.bar(B_RXRDY), partner);
     const uint32_t partner_data = map_to_rank(sh.bar(B_DATA), partner);
     const uint32_t partner_ssq_bar = map_to_rank(sh.bar(B_SSQ), partner);
@@ -438,8 +465,12 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
       // (1) my MMAs are done, so my K ring may receive; wait until the
       //     partner's is free too, then write the partner's half of my O/l
       //     into it (row r: 512 bytes, 16-byte chunks XOR-swizzled by r & 7)
-      remote_arrive(partner_rxrdy);
-      if (!wait_bar<true>(sh, sh.bar(B_RXRDY), it & 1, a.status, 0x3206)) { ok = false; break; }
+      // stage the partner's half of my O/l in this item's last V stage (idle
+      // now; row r at r * 512 bytes, 16-byte chunks XOR-swizzled by r & 7),
+      // then one thread moves the 64 KB into the partner's K ring with a bulk
+      // copy whose bytes complete on the partner's DATA barrier
+      const int give_stage = (kv - 1) & 1;
+      uint8_t* gstg = sh.gen + kOffV + give_stage * 4 * kBox + row * 512;
 #pragma unroll 1
       for (int c2 = 0; c2 < 2; ++c2) {
         uint32_t o[64];
@@ -449,12 +480,24 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
 #pragma unroll
         for (int e = 0; e < 64; e += 4) {
           const int u = (c2 * 64 + e) >> 2;
-          st_cluster_v4(partner_rx + ((u ^ (row & 7)) << 4),
-                        make_float4(__uint_as_float(o[e]) * inv_l, __uint_as_float(o[e + 1]) * inv_l,
-                                    __uint_as_float(o[e + 2]) * inv_l, __uint_as_float(o[e + 3]) * inv_l));
+          *reinterpret_cast<float4*>(gstg + ((u ^ (row & 7)) << 4)) =
+              make_float4(__uint_as_float(o[e]) * inv_l, __uint_as_float(o[e + 1]) * inv_l,
+                          __uint_as_float(o[e + 2]) * inv_l, __uint_as_float(o[e + 3]) * inv_l);
         }
       }
-      remote_arrive(partner_data);
+      fence_proxy_async_smem();
+      mbar_arrive(sh.bar(B_GIVE));
+      if (row == 0) {
+        // my MMAs are done (ORDY), so my K ring may receive
+        remote_arrive(partner_rxrdy);
+        mbar_arrive_expect_tx(sh.bar(B_DATA), 128 * 512);
+        if (!wait_bar(sh, sh.bar(B_GIVE), it & 1, a.status, 0x3208) ||
+            !wait_bar<true>(sh, sh.bar(B_RXRDY), it & 1, a.status, 0x3206)) {
+          ok = false;
+          break;
+        }
+        bulk_copy_to_peer(partner_rx0, sh.base + kOffV + give_stage * 4 * kBox, 128 * 512, partner_data);
+      }
       if (!wait_bar<true>(sh, sh.bar(B_DATA), it & 1, a.status, 0x3204)) { ok = false; break; }
       // (2) O = O1/l1 - lambda O2/l2 on my half; partial sum of squares
       float dvals[128];
@@ -462,8 +505,11 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
       const int n = w.mt * kBM + row;
       const bool live = n < a.N;
       // staging for the TMA stores: the V stage of this item's last tile,
-      // idle until the producer loads the next item's second V tile (after
-      // this epilogue): Y in boxes 0-1, O2 in boxes 2-3, 128-byte swizzle
+      // which the producer refills only after these stores have read it (Y in
+      // boxes 0-1, O2 in boxes 2-3, 128-byte swizzle).  It held the outgoing
+      // half of O until the bulk copy read it: the partner sends its partial
+      // sums only after all those bytes arrived, so after the SSQ wait below
+      // it is free again.
       const int stg_stage = (kv - 1) & 1;
       uint8_t* stg = sh.gen + kOffV + stg_stage * 4 * kBox;
       const uint32_t stg_s = sh.base + kOffV + stg_stage * 4 * kBox;
@@ -473,7 +519,6 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
         uint32_t o[32];
         tmem_ld32(t_o + keep + c * 32, o);
         tmem_ld_wait();
-        float o2v[32];
 #pragma unroll
         for (int e = 0; e < 32; e += 4) {
           const int u = (c * 32 + e) >> 2;
@@ -487,10 +532,34 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
             const float dd = __fsub_rn(a1, __fmul_rn(lam, a2));
             dvals[c * 32 + e + q] = dd;
             ssq = fmaf(dd, dd, ssq);
-            o2v[e + q] = a2;
           }
         }
-        if (want_o2) {
+      }
+      st_cluster_f32(partner_ssq_slot, ssq);
+      remote_arrive(partner_ssq_bar);
+      if (!wait_bar<true>(sh, sh.bar(B_SSQ), it & 1, a.status, 0x3205)) { ok = false; break; }
+      if (want_o2) {
+        // O2 / l2 of my columns: received (rank 0) or my own (rank 1)
+#pragma unroll 1
+        for (int c = 0; c < 4; ++c) {
+          float o2v[32];
+          if (rank == 0) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 4) {
+              const int u = (c * 32 + e) >> 2;
+              const float4 v4 = *reinterpret_cast<const float4*>(my_rx + ((u ^ (row & 7)) << 4));
+              o2v[e] = v4.x;
+              o2v[e + 1] = v4.y;
+              o2v[e + 2] = v4.z;
+              o2v[e + 3] = v4.w;
+            }
+          } else {
+            uint32_t o[32];
+            tmem_ld32(t_o + keep + c * 32, o);
+            tmem_ld_wait();
+#pragma unroll
+            for (int e = 0; e < 32; ++e) o2v[e] = __uint_as_float(o[e]) * inv_l;
+          }
 #pragma unroll
           for (int e = 0; e < 32; e += 8) {
             const int col = c * 32 + e;  // 0..127 within this CTA's half
@@ -504,9 +573,7 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
           }
         }
       }
-      st_cluster_f32(partner_ssq_slot, ssq);
-      remote_arrive(partner_ssq_bar);
-      if (!wait_bar<true>(sh, sh.bar(B_SSQ), it & 1, a.status, 0x3205)) { ok = false; break; }
+      mbar_arrive(sh.bar(B_RXFREE));  // this row's part of the K ring has been read
       const float other_ssq = sh.ssq_rx_ptr()[row];
       const float tot = rank == 0 ? ssq + other_ssq : other_ssq + ssq;
       const float rstd = 1.f / sqrtf(tot * (1.f / kDv) + a.rms_eps);
@@ -527,8 +594,8 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
         if (rank == 0 && a.rstd) a.rstd[sidx] = rstd;
       }
       // all rows staged -> one thread stores the tiles with TMA (rows past N
-      // are dropped), waits until the staging has been read, then the K ring
-      // and this V stage may take the next item's tiles
+      // are dropped) and, once the staging has been read, releases this V
+      // stage to the producer
       fence_proxy_async_smem();
       mbar_arrive(sh.bar(B_STG));
       if (!wait_bar(sh, sh.bar(B_STG), it & 1, a.status, 0x3207)) { ok = false; break; }
@@ -540,8 +607,8 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
             tma_store_4d(&tm_o2, stg_s + (2 + bx) * kBox, keep + bx * 64, w.h, w.mt * kBM, w.b);
         bulk_commit();
         bulk_wait_read();
+        mbar_arrive(sh.bar(B_STGFREE));
       }
-      mbar_arrive(sh.bar(B_EPI));
       tc_fence_before();
     }
   }
