@@ -131,20 +131,23 @@ class V1Fwd(Workload):
         self.bd.diffattn_v1_fwd(*self.args(dev), self.li, out=self.out, workspace=self.fws)
         self.host_out.copy_(self.out, non_blocking=True)
 
-    def oracle_sample(self):
-        """fp64 oracle on a bounded sample: every head of batch 0, a seeded
-        set of query rows; returns (seconds, flops of the sampled rows)."""
+    def oracle_sample(self, big=True):
+        """fp64 oracle on a bounded sample (every head of the first batches, a
+        seeded set of query rows); returns (seconds, flops of the sampled
+        rows, description)."""
         from oracle import diffattn_oracle as orc
-        rows = np.sort(np.random.default_rng(0).choice(self.N, 96, replace=False))
-        ts = {k: v[:1].to("cpu", torch.float64).numpy() if v.dim() == 4 else
+        nb, nrows = (min(self.B, 4), min(self.N, 1024)) if big else (1, min(self.N, 128))
+        rows = np.sort(np.random.default_rng(0).choice(self.N, nrows, replace=False))
+        ts = {k: v[:nb].to("cpu", torch.float64).numpy() if v.dim() == 4 else
               v.to("cpu", torch.float64).numpy() for k, v in self.t.items()}
         t0 = time.perf_counter()
         orc.v1_forward(*(ts[n] for n in ("q1", "q2", "k1", "k2", "v", "lq1", "lk1", "lq2", "lk2")),
                        self.li, rows=rows)
         dt = time.perf_counter() - t0
         keys = float(np.sum(rows + 1))  # causal keys of the sampled rows
-        flops = self.H * keys * (4.0 * self.dqk + 2.0 * self.dv)
-        return dt, flops, f"batch 0, {self.H} heads, 96 seeded query rows of {self.N}"
+        flops = nb * self.H * keys * (4.0 * self.dqk + 2.0 * self.dv)
+        return dt, flops, (f"batches 0-{nb - 1}, {self.H} heads, {nrows} seeded query rows of "
+                           f"{self.N} (fp64 numpy oracle)")
 
 
 class V1FwdBwd(V1Fwd):
@@ -244,9 +247,9 @@ class V2Fwd(Workload):
                                 out=self.out, workspace=self.ws)
         self.host_out.copy_(self.out, non_blocking=True)
 
-    def oracle_sample(self):
+    def oracle_sample(self, big=True):
         from oracle import diffattn_oracle as orc
-        rows = np.sort(np.random.default_rng(0).choice(self.N, 48, replace=False))
+        rows = np.sort(np.random.default_rng(0).choice(self.N, 256 if big else 48, replace=False))
         G = 2 * self.h // self.hkv
         t0 = time.perf_counter()
         for p in range(4):  # four pairs of batch 0 (one per K/V group of the first four)
@@ -258,7 +261,7 @@ class V2Fwd(Workload):
                            sl(self.t["v"], g, g + 1), gate, rows=rows)
         dt = time.perf_counter() - t0
         flops = 4 * 2 * float(np.sum(rows + 1)) * 4.0 * self.d
-        return dt, flops, "batch 0, 4 pairs, 48 seeded query rows of 8192 (gate included)"
+        return dt, flops, f"batch 0, 4 pairs, {len(rows)} seeded query rows of 8192 (gate included)"
 
 
 class V2Decode(Workload):
@@ -286,7 +289,7 @@ class V2Decode(Workload):
         self.bd.diffattn_v2_decode(t["q"], t["k_cache"], t["v_cache"], x=t["x"],
                                    w_lambda=t["w_lambda"], out=self.out, workspace=self.ws)
 
-    def oracle_sample(self):
+    def oracle_sample(self, big=True):
         from oracle import diffattn_oracle as orc
         t0 = time.perf_counter()
         b = 0
@@ -299,9 +302,49 @@ class V2Decode(Workload):
         return dt, decode_bytes(1, self.L, self.hkv, self.d), "sequence 0 of 64 (full cache)"
 
 
+class V2DecodeSmall(V2Decode):
+    """The decode kernel on a 1 GB cache (B8): big enough that DRAM figures
+    mean something, small enough for a multi-pass ncu capture."""
+    name = "v2_decode_small"
+    desc = "V2 decode bf16 B8 cache 32768 8 KV heads 64 query heads d128 (profiling size)"
+    B = 8
+
+
 WORKLOADS = {w.name: w for w in (V1Fwd, V1FwdF32, V2Fwd, V2Decode, V1FwdBwd)}
+PROFILE_ONLY = {V2DecodeSmall.name: V2DecodeSmall}
 
 # ----------------------------------------------------------------- helpers --
+
+
+KERNEL_SOURCES = {
+    "v1_fwd": ("v1_fwd.cu", "softmax.cuh", "tma.cuh", "common.cuh"),
+    "v1_fwd_bwd": ("v1_bwd.cu", "softmax.cuh", "tma.cuh", "common.cuh"),
+    "v2_fwd": ("v2_fwd.cu", "softmax.cuh", "tma.cuh", "common.cuh"),
+    "v2_decode": ("decode.cu", "common.cuh"),
+}
+
+
+def source_hash(workload):
+    import hashlib
+    h = hashlib.sha256()
+    for f in KERNEL_SOURCES.get(workload, ()):
+        with open(os.path.join(ROOT, "differential_attention_diff_gb300", "csrc", f), "rb") as fh:
+            h.update(fh.read())
+    return h.hexdigest()[:16]
+
+
+def recorded_traffic(workload):
+    """DRAM bytes per launch of the dominant kernel from the committed ncu
+    record (profiles/traffic.json), or None when the kernel's sources changed
+    since the counters were taken."""
+    path = os.path.join(ROOT, "profiles", "traffic.json")
+    try:
+        rec = json.load(open(path)).get(workload)
+    except Exception:  # noqa: BLE001
+        return None
+    if not rec or rec.get("source_hash") != source_hash(workload):
+        return None
+    return rec.get("dram_bytes_per_launch")
 
 
 def measured_peaks():
@@ -431,7 +474,7 @@ def run_ours(args, ws, rank, local):
     stream = torch.cuda.current_stream()
     flush = torch.empty(2 * L2_BYTES // 4, dtype=torch.float32, device=dev)
 
-    main = WORKLOADS[args.workload]()
+    main = {**WORKLOADS, **PROFILE_ONLY}[args.workload]()
     main.setup(dev)
     for _ in range(args.warmup):
         main.run()
@@ -467,7 +510,7 @@ def run_ours(args, ws, rank, local):
     roofline = {"bound": main.bound, "achieved": round(achieved, 2),
                 "peak": peak, "unit": r_unit,
                 "frac": round(achieved / peak, 4) if peak else None,
-                "peak_source": peak_src, "traffic": None,
+                "peak_source": peak_src, "traffic": recorded_traffic(main.name),
                 "kernel_ms": round(dom_ms, 4)}
 
     # end-to-end through the public API with host buffers
@@ -507,7 +550,7 @@ def run_ours(args, ws, rank, local):
                               "dominant_kernel_ms": round(td, 4),
                               "dominant_achieved": round(dw, 2),
                               "dominant_frac": round(dw / pk, 4) if pk else None,
-                              "peak_source": src}
+                              "peak_source": src, "traffic": recorded_traffic(name)}
             except Exception as exc:  # noqa: BLE001
                 rows[name] = {"workload": w.desc, "error": str(exc)[:200]}
             del w
@@ -543,17 +586,17 @@ def run_reference(args, ws, rank):
     workload, on the host cores (rank 0 only)."""
     if rank != 0:
         return
-    main = WORKLOADS[args.workload]()
+    main = {**WORKLOADS, **PROFILE_ONLY}[args.workload]()
     dev = "cuda" if torch.cuda.is_available() else "cpu"
     main.setup(dev) if dev == "cuda" else None
     if dev != "cuda":
         print(json.dumps({"impl": "reference", "unavailable": "needs the GPU to draw inputs"}))
         return
     for _ in range(args.warmup):
-        main.oracle_sample()
+        main.oracle_sample(big=False)
     secs, work, sample = 0.0, 0.0, ""
     for _ in range(args.steps):
-        dt, w, sample = main.oracle_sample()
+        dt, w, sample = main.oracle_sample(big=False)
         secs += dt
         work += w
     ms = secs * 1e3 / args.steps
@@ -575,7 +618,7 @@ def main():
     ap.add_argument("--gpus", type=int, default=1)
     ap.add_argument("--steps", type=int, default=10)
     ap.add_argument("--warmup", type=int, default=3)
-    ap.add_argument("--workload", default="v1_fwd", choices=sorted(WORKLOADS))
+    ap.add_argument("--workload", default="v1_fwd", choices=sorted(WORKLOADS) + sorted(PROFILE_ONLY))
     ap.add_argument("--impl", default="ours", choices=("ours", "reference"))
     ap.add_argument("--no-rows", action="store_true")
     ap.add_argument("--no-cpu-baseline", action="store_true")
