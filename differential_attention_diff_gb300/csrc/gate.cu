@@ -5,8 +5,9 @@
 // and passed through a sigmoid.  The projection is a skinny GEMM
 // [T, d_model] x [d_model, h] with h <= 64, so the kernel is bound by reading
 // X once from HBM: 64 tokens per CTA, X and W chunks of 64 features staged by
-// a 2-deep cp.async ring, the warp MMA for the products (each warp owns 16
-// tokens and all h outputs), and the sigmoid fused into the store.
+// a 4-deep cp.async ring (three chunks in flight while one is consumed), the
+// warp MMA for the products (each warp owns 16 tokens and all h outputs), and
+// the sigmoid fused into the store.
 #include "common.cuh"
 #include "kernels.h"
 
@@ -16,7 +17,7 @@ namespace {
 constexpr int kTok = 64;    // tokens per CTA
 constexpr int kChunk = 64;  // features per stage
 constexpr int kMaxH = 64;
-constexpr int kStages = 2;
+constexpr int kStages = 4;
 constexpr int kRow = 128;   // bytes per staged row (64 bf16)
 constexpr int kXBytes = kTok * kRow;
 constexpr int kWBytes = kChunk * kRow;
@@ -28,7 +29,7 @@ __device__ __forceinline__ uint32_t off8(int r, int c) {
 
 __global__ void __launch_bounds__(128)
 gate_kernel(GateArgs a) {
-  __shared__ __align__(128) uint8_t smem[kStages * kStageBytes];
+  extern __shared__ __align__(128) uint8_t smem[];
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int t0 = blockIdx.x * kTok;
   const int nchunks = a.d_model / kChunk;
@@ -74,10 +75,11 @@ gate_kernel(GateArgs a) {
 #pragma unroll
   for (int i = 0; i < kMaxH / 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
 
-  issue(0);
+#pragma unroll
+  for (int ch = 0; ch < kStages - 1; ++ch) issue(ch);
   for (int ch = 0; ch < nchunks; ++ch) {
-    issue(ch + 1);
-    cp_async_wait<1>();
+    issue(ch + kStages - 1);
+    cp_async_wait<kStages - 1>();
     __syncthreads();
     const uint32_t xs = sb + (ch % kStages) * kStageBytes;
     const uint32_t ws = xs + kXBytes;
@@ -129,7 +131,14 @@ gate_kernel(GateArgs a) {
 cudaError_t launch_gate(const GateArgs& a, cudaStream_t s) {
   const int grid = (a.T + kTok - 1) / kTok;
   if (grid == 0) return cudaSuccess;
-  gate_kernel<<<grid, 128, 0, s>>>(a);
+  static bool attr_done = false;
+  if (!attr_done) {
+    cudaError_t e = cudaFuncSetAttribute(gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                         kStages * kStageBytes);
+    if (e != cudaSuccess) return e;
+    attr_done = true;
+  }
+  gate_kernel<<<grid, 128, kStages * kStageBytes, s>>>(a);
   return cudaGetLastError();
 }
 
