@@ -55,6 +55,7 @@ __all__ = [
     "v2_gate",
     "v2_forward",
     "v2_decode",
+    "v2_backward",
 ]
 
 
@@ -260,6 +261,52 @@ def v2_forward(q, k, v, gate, *, scale: float | None = None,
             lse[b, j] = l
     out = o[:, :, 0::2] - gate[:, rows, :, None] * o[:, :, 1::2]
     return dict(out=out, o=o, lse=lse, rows=rows)
+
+
+def v2_backward(q, k, v, x, w, dout, *, scale: float | None = None, causal: bool = True):
+    """Gradients of the V2 forward (``v2_gate`` then ``v2_forward``) with
+    respect to q, k, v, x and w, given dOut.  The pages state no backward; this
+    is the chain rule of the forward above, step by step.  With g = sigmoid(z),
+    z = X W, Out_p = O_2p - g_p O_2p+1, G = dOut:
+      dO_2p = G,  dO_2p+1 = -g G,  dg_p = -<G_p, O_2p+1>,  dz = dg g (1 - g)
+      dW = X^T dz,  dX = dz W^T
+      per query head j (kv head c = j // group):  A = softmax(s Q_j K_c^T),
+      dP = dO_j V_c^T,  dS = A * (dP - <dO_j, O_j>),
+      dQ_j = s dS K_c,  dK_c += s dS^T Q_j,  dV_c += A^T dO_j.
+    Pinned against central finite differences of the forward."""
+    q, k, v, x, w, dout = (_f64(t) for t in (q, k, v, x, w, dout))
+    B, N, H2, d = q.shape
+    hkv = k.shape[2]
+    group = H2 // hkv
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    z = x @ w
+    g = _sigmoid(z)
+    fwd = v2_forward(q, k, v, g, scale=scale, causal=causal)
+    o = fwd["o"]
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    do = np.zeros_like(o)
+    do[:, :, 0::2] = dout
+    do[:, :, 1::2] = -g[..., None] * dout
+    dg = -np.sum(dout * o[:, :, 1::2], axis=-1)
+    dz = dg * g * (1.0 - g)
+    dw = np.einsum("btk,btp->kp", x, dz)
+    dx = dz @ w.T
+    for b in range(B):
+        for j in range(H2):
+            c = j // group
+            Q, K, V = q[b, :, j], k[b, :, c], v[b, :, c]
+            a, _ = attention_maps(Q, K, scale, causal)
+            dO = do[b, :, j]
+            dP = dO @ V.T
+            D = np.sum(dO * o[b, :, j], axis=1, keepdims=True)
+            dS = a * (dP - D)
+            dq[b, :, j] = scale * dS @ K
+            dk[b, :, c] += scale * dS.T @ Q
+            dv[b, :, c] += a.T @ dO
+    return dict(dq=dq, dk=dk, dv=dv, dx=dx, dw=dw, dz=dz, gate=g)
 
 
 def v2_decode(q, k_cache, v_cache, seqlens, gate, *, scale: float | None = None):

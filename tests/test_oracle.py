@@ -398,3 +398,55 @@ def test_v1_backward_finite_differences():
             num[idx] = (loss(tp) - loss(tm)) / (2 * eps)
         err = np.max(np.abs(num - g)) / max(np.max(np.abs(num)), 1e-12)
         assert err < 1e-6, (name, err)
+
+
+def test_v2_backward_finite_differences():
+    """Every V2 gradient (q, k, v, x, w_lambda) against central differences of
+    gate + forward (fp64), on a GQA case with two pairs per K/V group."""
+    r = _rng(40)
+    B, N, h, hkv, d, dm = 1, 5, 2, 1, 3, 4
+    t = dict(q=r.standard_normal((B, N, 2 * h, d)), k=r.standard_normal((B, N, hkv, d)),
+             v=r.standard_normal((B, N, hkv, d)), x=r.standard_normal((B, N, dm)),
+             w=0.5 * r.standard_normal((dm, h)))
+    dout = r.standard_normal((B, N, h, d))
+    grads = orc.v2_backward(t["q"], t["k"], t["v"], t["x"], t["w"], dout)
+
+    def loss(tt):
+        gate = orc.v2_gate(tt["x"], tt["w"])
+        return float(np.sum(orc.v2_forward(tt["q"], tt["k"], tt["v"], gate)["out"] * dout))
+
+    eps = 1e-6
+    for name in ("q", "k", "v", "x", "w"):
+        g = grads["d" + name]
+        num = np.zeros_like(t[name])
+        it = np.nditer(t[name], flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            tp = {kk: vv.copy() for kk, vv in t.items()}
+            tm = {kk: vv.copy() for kk, vv in t.items()}
+            tp[name][idx] += eps
+            tm[name][idx] -= eps
+            num[idx] = (loss(tp) - loss(tm)) / (2 * eps)
+        err = np.max(np.abs(num - g)) / max(np.max(np.abs(num)), 1e-12)
+        assert err < 1e-6, (name, err)
+
+
+def test_v2_backward_gate_zero_reduces_to_even_heads():
+    """With W = 0 the gate is 1/2 everywhere; with the odd queries zero the odd
+    heads are uniform maps whose V-gradient is the closed form -1/2 * causal
+    column means of dOut (each key j receives sum_{i >= j} dOut_i / (i + 1))."""
+    r = _rng(41)
+    B, N, h, hkv, d, dm = 1, 6, 1, 1, 4, 3
+    q = r.standard_normal((B, N, 2, d))
+    q[:, :, 1] = 0.0
+    k, v = r.standard_normal((B, N, hkv, d)), r.standard_normal((B, N, hkv, d))
+    x, w = r.standard_normal((B, N, dm)), np.zeros((dm, h))
+    dout = r.standard_normal((B, N, h, d))
+    full = orc.v2_backward(q, k, v, x, w, dout)
+    s = 1 / np.sqrt(d)
+    a, _ = orc.attention_maps(q[0, :, 0], k[0, :, 0], s, True)
+    dv_even = a.T @ dout[0, :, 0]
+    n = np.arange(1, N + 1)[:, None]
+    dv_odd = -0.5 * np.cumsum((dout[0, :, 0] / n)[::-1], axis=0)[::-1]
+    np.testing.assert_allclose(full["dv"][0, :, 0], dv_even + dv_odd, atol=1e-12)
+    np.testing.assert_allclose(full["gate"], 0.5, atol=0)
