@@ -52,10 +52,31 @@ struct V2FwdArgs {
   da_t4 q, k, v, out;
   const float* gate;  // [B, N, h]
   float* lse;         // optional [B, 2h, N] (natural log)
+  da_t4 o_heads;      // optional [B, N, 2h, d] per-head outputs
   uint32_t* status;
   int num_sms;
 };
 cudaError_t launch_v2_fwd(const V2FwdArgs& a, cudaStream_t s);
+
+// ---- V2 backward, bf16, tcgen05 --------------------------------------------
+struct V2BwdArgs {
+  int B, N, h, h_kv, d, d_model, causal;
+  float scale;
+  da_t4 q, k, v, o_heads, dout, dq, dk, dv;
+  const float* gate;   // [B, N, h], or NULL: computed from x, w into the workspace
+  const float* lse;    // [B, 2h, N] natural log
+  const void* x;       // bf16 [B, N, d_model] (optional)
+  const void* w;       // bf16 [d_model, h] (optional)
+  float* dz;           // optional [B, N, h] output (else kept in the workspace)
+  void* dx;            // optional bf16 [B, N, d_model]
+  float* dw;           // optional fp32 [d_model, h]
+  void* workspace;
+  size_t workspace_bytes;
+  uint32_t* status;
+  int num_sms;
+};
+size_t v2_bwd_workspace_bytes(int B, int N, int h, int d_model);
+cudaError_t launch_v2_bwd(const V2BwdArgs& a, cudaStream_t s);
 
 // ---- V1 forward, bf16, tcgen05 ---------------------------------------------
 struct V1FwdArgs {

@@ -1,0 +1,840 @@
+// v2_bwd.cu — V2 differential attention backward (bf16) on tcgen05 + TMEM +
+// TMA, sm_103a, plus the gradients of the gate projection.
+//
+// "Differential Transformer V2" (pogovet.com), §1 and §4 define the forward:
+// one causal GQA attention over 2h query heads, then per token t and pair p
+//   out[t, p] = O[t, 2p] - g[t, p] O[t, 2p + 1],   g = sigmoid(x[t] . W[:, p]).
+// This file is its chain rule.  With G = dOut[t, p] and s the softmax scale:
+//   dO_2p = G,  dO_2p+1 = -g G,  dz = -<G, O_2p+1> g (1 - g)
+//   dW = X^T dz,  dX = dz W^T
+//   per query head j of K/V group c:  P = exp(s Q_j K_c^T - lse_j) (causal),
+//   dP = dO_j V_c^T,  dS = s P (dP - D_j),  D_j = <dO_j, O_j>
+//   dQ_j = dS K_c,  dK_c += dS^T Q_j,  dV_c += P^T dO_j.
+//
+// Launches:
+//  1. (gate from x and W when the caller passes none: the gate kernel)
+//  2. preprocess (one warp per (token, pair)): dO of the odd head as bf16,
+//     D of both heads, the LSEs in log2 units padded to whole 64-row tiles,
+//     dz, and zeroed fp32 dQ accumulators;
+//  3. main (tcgen05): a work item is (batch, K/V group, 128-key tile); one
+//     CTA keeps the K and V tiles in shared memory and walks every query head
+//     of the group and its 64-row query tiles at and after the diagonal,
+//     accumulating dK and dV of the group in TMEM across the heads:
+//        S^T  = K Q^T,  dP^T = V dO^T  (TMEM, double-buffered, issued while
+//                                       the softmax warps work on the tile
+//                                       before)
+//        softmax warps (thread = key row): P^T and dS^T as bf16 rows in
+//                                       shared memory
+//        dQ^T = K^T dS^T   (TMEM, in the dP^T buffer just consumed) -> the
+//                          dQ warps stage it in shared memory and one thread
+//                          adds it to the fp32 accumulator by TMA reduce-add
+//        dV  += P^T dO,  dK += dS^T Q   (TMEM, 128 columns each)
+//     then the softmax warps write dK and the dQ warps dV, as bf16;
+//  4. finalize: dQ accumulators -> bf16;
+//  5. (when asked) dX = dz W^T, and dW = X^T dz as per-chunk partial sums
+//     reduced in a fixed order.
+//
+// Warp roles (320 threads): 0-3 softmax / dK epilogue, 4-7 dQ readback and
+// reduce / dV epilogue, 8 TMA producer, 9 MMA issuer.
+// TMEM: [0,128) dV, [128,256) dK, [256,384) S^T x 2, [384,512) dP^T / dQ^T x 2.
+// SMEM: K 32 KB, V 32 KB, 3 stages of (Q 16 KB, dO 16 KB), P^T 16 KB,
+//       dS^T 16 KB, dQ staging 32 KB, per-stage lse2 / D (1.5 KB); every bf16
+//       operand in 128-byte-swizzled 64-column boxes.
+// Every mbarrier wait is bounded (about 2 s); on expiry the kernel records
+// DA_ERR_TIMEOUT, raises an abort flag that the other roles see, and leaves.
+#include <type_traits>
+
+#include "kernels.h"
+#include "softmax.cuh"
+#include "tma.cuh"
+
+namespace da {
+namespace {
+
+constexpr int kKT = 128;  // keys per item
+constexpr int kQT = 64;   // queries per iteration
+constexpr int kD = 128;
+constexpr int kThreads = 320;
+constexpr int kStages = 3;
+
+constexpr int kBoxK = 128 * 128;  // 64 columns x 128 rows of bf16
+constexpr int kBoxQ = 64 * 128;   // 64 columns x 64 rows
+constexpr int kOffK = 0;
+constexpr int kOffV = kOffK + 2 * kBoxK;
+constexpr int kOffStage = kOffV + 2 * kBoxK;  // 65536
+constexpr int kStageQ = 0;
+constexpr int kStageDO = 2 * kBoxQ;
+constexpr int kStageBytes = 4 * kBoxQ;                  // 32 KB
+constexpr int kOffP = kOffStage + kStages * kStageBytes;  // 163840
+constexpr int kOffDS = kOffP + kBoxK;
+constexpr int kOffDQ = kOffDS + kBoxK;                  // fp32 [64][128]
+constexpr int kOffLse = kOffDQ + kQT * kD * 4;          // [stage] {lse2[64], D[64]}
+constexpr int kOffBar = kOffLse + kStages * 512;
+constexpr int kSmemBytes = kOffBar + 512 + 1024;        // 232448: the per-block limit
+
+enum {
+  B_KV = 0, B_QFULL, B_QEMPTY = B_QFULL + kStages, B_SFULL = B_QEMPTY + kStages, B_PFULL = B_SFULL + 2,
+  B_DQFULL, B_DQFREE = B_DQFULL + 2, B_PBFREE = B_DQFREE + 2, B_STG, B_STGFREE, B_ACC, B_COUNT
+};
+static_assert(B_COUNT * 8 <= 256, "barrier area");
+
+__host__ __device__ constexpr uint32_t idesc2(int M, int N, int a_mn, int b_mn) {
+  return (1u << 4) | (1u << 7) | (1u << 10) | (static_cast<uint32_t>(a_mn) << 15) |
+         (static_cast<uint32_t>(b_mn) << 16) | (static_cast<uint32_t>(N >> 3) << 17) |
+         (static_cast<uint32_t>(M >> 4) << 24);
+}
+constexpr uint32_t kIdS = idesc2(128, 64, 0, 0);    // K (K-major) x Q (K-major); V x dO
+constexpr uint32_t kIdAcc = idesc2(128, 128, 0, 1); // P^T / dS^T (K-major) x dO / Q (MN-major)
+constexpr uint32_t kIdDQ = idesc2(128, 64, 1, 1);   // K^T (MN-major) x dS^T (MN-major)
+
+__device__ __forceinline__ uint64_t globaltimer() {
+  uint64_t t;
+  asm volatile("mov.u64 %0, %globaltimer;" : "=l"(t));
+  return t;
+}
+
+struct Shared {
+  uint32_t base;
+  uint8_t* gen;
+  __device__ uint32_t bar(int i) const { return base + kOffBar + 8 * i; }
+  __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(gen + kOffBar + 256); }
+  __device__ volatile int* abort_flag() const {
+    return reinterpret_cast<volatile int*>(gen + kOffBar + 264);
+  }
+};
+
+__device__ __forceinline__ bool wait_bar(const Shared& sh, uint32_t bar, uint32_t parity,
+                                         uint32_t* status, uint32_t site) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const uint64_t t0 = globaltimer();
+  while (true) {
+#pragma unroll 1
+    for (int i = 0; i < 64; ++i)
+      if (mbar_try_wait(bar, parity)) return true;
+    if (*sh.abort_flag()) return false;
+    if (globaltimer() - t0 > 2000000000ull) {
+      record_status(status, DA_ERR_TIMEOUT, site);
+      *sh.abort_flag() = 1;
+      return false;
+    }
+  }
+}
+
+__device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_t bytes,
+                                          uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.shared::cluster.global.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(dst),
+      "l"(src), "r"(bytes), "r"(bar)
+      : "memory");
+}
+
+// --------------------------------------------------------------------------
+// Workspace carve-up (all offsets 256-byte aligned).  Every region is always
+// reserved so that the size depends only on (B, N, h, d_model).
+constexpr int kDwChunk = 1024;  // tokens per dW partial sum
+
+struct BwdWs {
+  __nv_bfloat16* dodd;  // [B, N, h, 128]  dO of the odd heads = -g G
+  float* lse2;          // [B, 2h, Npad]   LSE * log2 e; +inf in padding rows
+  float* D;             // [B, 2h, Npad]
+  float* dq;            // [B, N, 2h, 128] fp32 accumulators
+  float* gate;          // [B, N, h]  when computed here
+  float* dz;            // [B, N, h]  when the caller keeps none
+  float* dw_part;       // [chunks, d_model, h]
+  int npad, chunks;
+};
+
+size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
+
+BwdWs carve(void* base, int B, int N, int h, int d_model, size_t* total) {
+  BwdWs w;
+  w.npad = (N + kQT - 1) / kQT * kQT;
+  const long long T = static_cast<long long>(B) * N;
+  w.chunks = static_cast<int>((T + kDwChunk - 1) / kDwChunk);
+  uint8_t* p = static_cast<uint8_t*>(base);
+  size_t off = 0;
+  auto take = [&](size_t bytes) {
+    uint8_t* r = p ? p + off : nullptr;
+    off += a256(bytes);
+    return r;
+  };
+  const size_t tok = static_cast<size_t>(T);
+  const size_t srow = static_cast<size_t>(B) * 2 * h * w.npad;
+  w.dodd = reinterpret_cast<__nv_bfloat16*>(take(tok * h * kD * 2));
+  w.lse2 = reinterpret_cast<float*>(take(srow * 4));
+  w.D = reinterpret_cast<float*>(take(srow * 4));
+  w.dq = reinterpret_cast<float*>(take(tok * 2 * h * kD * 4));
+  w.gate = reinterpret_cast<float*>(take(tok * h * 4));
+  w.dz = reinterpret_cast<float*>(take(tok * h * 4));
+  w.dw_part = reinterpret_cast<float*>(
+      take(d_model > 0 ? static_cast<size_t>(w.chunks) * d_model * h * 4 : 0));
+  if (total) *total = off;
+  return w;
+}
+
+// ------------------------------------------------------------ preprocess --
+constexpr int kPreWarps = 8;
+
+__global__ void __launch_bounds__(kPreWarps * 32)
+v2_bwd_pre_kernel(V2BwdArgs a, BwdWs w, const float* __restrict__ gate, float* __restrict__ dz) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const long long row = static_cast<long long>(blockIdx.x) * kPreWarps + warp;  // (b, p, n < npad)
+  const long long total = static_cast<long long>(a.B) * a.h * w.npad;
+  if (row >= total) return;
+  const int n = static_cast<int>(row % w.npad);
+  const int bp = static_cast<int>(row / w.npad);
+  const int b = bp / a.h, p = bp % a.h;
+  const int he = 2 * p;
+  const int64_t se = (static_cast<int64_t>(b) * 2 * a.h + he) * w.npad + n;  // padded rows
+  const int64_t so = se + w.npad;
+  if (n >= a.N) {
+    if (lane == 0) {
+      w.lse2[se] = INFINITY;
+      w.lse2[so] = INFINITY;
+      w.D[se] = 0.f;
+      w.D[so] = 0.f;
+    }
+    return;
+  }
+  const __nv_bfloat16* gp = static_cast<const __nv_bfloat16*>(a.dout.ptr) + b * a.dout.sb +
+                            static_cast<int64_t>(n) * a.dout.sn + p * a.dout.sh + lane * 4;
+  const __nv_bfloat16* op = static_cast<const __nv_bfloat16*>(a.o_heads.ptr) + b * a.o_heads.sb +
+                            static_cast<int64_t>(n) * a.o_heads.sn + he * a.o_heads.sh + lane * 4;
+  const uint2 gv = *reinterpret_cast<const uint2*>(gp);
+  const uint2 ev = *reinterpret_cast<const uint2*>(op);
+  const uint2 ov = *reinterpret_cast<const uint2*>(op + a.o_heads.sh);
+  const __nv_bfloat16* ge = reinterpret_cast<const __nv_bfloat16*>(&gv);
+  const __nv_bfloat16* ee = reinterpret_cast<const __nv_bfloat16*>(&ev);
+  const __nv_bfloat16* oe = reinterpret_cast<const __nv_bfloat16*>(&ov);
+  const int64_t tp = (static_cast<int64_t>(b) * a.N + n) * a.h + p;
+  const float g = gate[tp];
+  float de = 0.f, dd = 0.f, go = 0.f;
+  uint32_t pk[2];
+#pragma unroll
+  for (int e = 0; e < 4; e += 2) {
+    const float g0 = __bfloat162float(ge[e]), g1 = __bfloat162float(ge[e + 1]);
+    // the odd head's dO is an MMA operand: round it once, and take D from
+    // the rounded values the MMAs see
+    pk[e / 2] = pack_bf16x2(-g * g0, -g * g1);
+    const __nv_bfloat162 r = *reinterpret_cast<const __nv_bfloat162*>(&pk[e / 2]);
+    const float o0 = __bfloat162float(oe[e]), o1 = __bfloat162float(oe[e + 1]);
+    de = fmaf(g0, __bfloat162float(ee[e]), de);
+    de = fmaf(g1, __bfloat162float(ee[e + 1]), de);
+    dd = fmaf(__low2float(r), o0, dd);
+    dd = fmaf(__high2float(r), o1, dd);
+    go = fmaf(g0, o0, go);
+    go = fmaf(g1, o1, go);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) {
+    de += __shfl_xor_sync(0xffffffffu, de, o);
+    dd += __shfl_xor_sync(0xffffffffu, dd, o);
+    go += __shfl_xor_sync(0xffffffffu, go, o);
+  }
+  *reinterpret_cast<uint2*>(w.dodd + tp * kD + lane * 4) = make_uint2(pk[0], pk[1]);
+  const int64_t qrow = (static_cast<int64_t>(b) * a.N + n) * 2 * a.h + he;
+  *reinterpret_cast<float4*>(w.dq + qrow * kD + lane * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+  *reinterpret_cast<float4*>(w.dq + (qrow + 1) * kD + lane * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+  if (lane == 0) {
+    const int64_t le = (static_cast<int64_t>(b) * 2 * a.h + he) * a.N + n;
+    w.lse2[se] = a.lse[le] * 1.4426950408889634f;
+    w.lse2[so] = a.lse[le + a.N] * 1.4426950408889634f;
+    w.D[se] = de;
+    w.D[so] = dd;
+    dz[tp] = -go * g * (1.f - g);
+  }
+}
+
+// -------------------------------------------------------------- main -------
+struct Item {
+  int b, g, kt, i0, n_ith, n_it;
+};
+
+// Items: (batch, K/V group, key tile).  Groups of `per` (batch, K/V group)
+// units are taken one block at a time (their dQ accumulators stay in L2),
+// the heaviest key tiles (most query tiles) first within each block.
+__device__ __forceinline__ Item item_of(int i, int n_kt, int n_qt, int units, int h_kv, int per,
+                                        int G) {
+  const int blk = i / (per * n_kt);
+  const int base = blk * per;
+  const int pb = min(per, units - base);
+  const int wi = i - blk * per * n_kt;
+  Item it;
+  it.kt = wi / pb;
+  const int u = base + wi % pb;
+  it.b = u / h_kv;
+  it.g = u % h_kv;
+  it.i0 = it.kt * (kKT / kQT);
+  it.n_ith = n_qt - it.i0;
+  it.n_it = it.n_ith * G;
+  return it;
+}
+
+__global__ void __launch_bounds__(kThreads, 1)
+v2_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
+                   const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
+                   const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_dq,
+                   V2BwdArgs a, BwdWs w, int per) {
+  extern __shared__ uint8_t smem_raw[];
+  Shared sh;
+  {
+    const uint32_t raw = smem_u32(smem_raw);
+    const uint32_t al = (raw + 1023u) & ~1023u;
+    sh.base = al;
+    sh.gen = smem_raw + (al - raw);
+  }
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int G = (2 * a.h) / a.h_kv;
+  const int n_kt = (a.N + kKT - 1) / kKT;
+  const int n_qt = w.npad / kQT;
+  const Item it = item_of(blockIdx.x, n_kt, n_qt, a.B * a.h_kv, a.h_kv, per, G);
+
+  if (threadIdx.x == 0) {
+    mbar_init(sh.bar(B_KV), 1);
+    for (int s = 0; s < kStages; ++s) {
+      mbar_init(sh.bar(B_QFULL + s), 1);
+      mbar_init(sh.bar(B_QEMPTY + s), 1);
+    }
+    for (int b = 0; b < 2; ++b) {
+      mbar_init(sh.bar(B_SFULL + b), 1);
+      mbar_init(sh.bar(B_DQFULL + b), 1);
+      mbar_init(sh.bar(B_DQFREE + b), 128);
+    }
+    mbar_init(sh.bar(B_PFULL), 128);
+    mbar_init(sh.bar(B_PBFREE), 1);
+    mbar_init(sh.bar(B_STG), 128);
+    mbar_init(sh.bar(B_STGFREE), 1);
+    mbar_init(sh.bar(B_ACC), 1);
+    *sh.abort_flag() = 0;
+    fence_mbar_init();
+  }
+  if (warp == 9) {
+    tmem_alloc(smem_u32(sh.tmem_slot()), 512);
+    tmem_relinquish();
+  }
+  if (warp == 8 && lane == 0) {
+    prefetch_tmap(&tm_q);
+    prefetch_tmap(&tm_k);
+    prefetch_tmap(&tm_v);
+    prefetch_tmap(&tm_g);
+    prefetch_tmap(&tm_do);
+    prefetch_tmap(&tm_dq);
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *sh.tmem_slot();
+  const uint32_t T_DV = tmem, T_DK = tmem + 128;
+  auto t_s = [&](int b) { return tmem + 256 + b * 64; };
+  auto t_d = [&](int b) { return tmem + 384 + b * 64; };
+  // iteration k -> (query head within the group, first query row)
+  auto head_of = [&](int k) { return k / it.n_ith; };
+  auto q0_of = [&](int k) { return (it.i0 + k % it.n_ith) * kQT; };
+
+  if (warp == 8) {
+    // ---------------------------------------------------- TMA producer ----
+    if (lane == 0) {
+      mbar_arrive_expect_tx(sh.bar(B_KV), 4 * kBoxK);
+      for (int box = 0; box < 2; ++box)
+        tma_load_4d(sh.base + kOffK + box * kBoxK, &tm_k, sh.bar(B_KV), box * 64, it.g, it.kt * kKT, it.b);
+      for (int box = 0; box < 2; ++box)
+        tma_load_4d(sh.base + kOffV + box * kBoxK, &tm_v, sh.bar(B_KV), box * 64, it.g, it.kt * kKT, it.b);
+      int last = -1;
+      bool ok = true;
+      for (int k = 0; k < it.n_it; ++k) {
+        const int st = k % kStages, use = k / kStages;
+        if (use > 0 && !wait_bar(sh, sh.bar(B_QEMPTY + st), (use - 1) & 1, a.status, 0x6001)) {
+          ok = false;
+          break;
+        }
+        const int qh = it.g * G + head_of(k);
+        const int q0 = q0_of(k);
+        const uint32_t sb = sh.base + kOffStage + st * kStageBytes;
+        const uint32_t bar = sh.bar(B_QFULL + st);
+        mbar_arrive_expect_tx(bar, 4 * kBoxQ + 512);
+        for (int box = 0; box < 2; ++box)
+          tma_load_4d(sb + kStageQ + box * kBoxQ, &tm_q, bar, box * 64, qh, q0, it.b);
+        // dO of an even head is dOut itself; of an odd head, -g dOut (workspace)
+        const CUtensorMap* tdo = (qh & 1) ? &tm_do : &tm_g;
+        for (int box = 0; box < 2; ++box)
+          tma_load_4d(sb + kStageDO + box * kBoxQ, tdo, bar, box * 64, qh >> 1, q0, it.b);
+        const size_t srow = (static_cast<size_t>(it.b) * 2 * a.h + qh) * w.npad + q0;
+        const uint32_t lb = sh.base + kOffLse + st * 512;
+        bulk_load(lb, w.lse2 + srow, 256, bar);
+        bulk_load(lb + 256, w.D + srow, 256, bar);
+        last = k;
+      }
+      if (!ok) {
+        // give the loads already issued (bounded) time to land before exit
+        const uint64_t t0 = globaltimer();
+        if (!mbar_try_wait(sh.bar(B_KV), 0))
+          while (globaltimer() - t0 < 200000000ull && !mbar_try_wait(sh.bar(B_KV), 0)) {
+          }
+        for (int k = last; k >= 0 && k > last - kStages; --k) {
+          const uint32_t bar = sh.bar(B_QFULL + k % kStages);
+          const uint32_t par = (k / kStages) & 1;
+          while (globaltimer() - t0 < 400000000ull && !mbar_try_wait(bar, par)) {
+          }
+        }
+      }
+    }
+  } else if (warp == 9) {
+    // ------------------------------------------------------ MMA issuer ----
+    if (lane == 0) {
+      bool ok = wait_bar(sh, sh.bar(B_KV), 0, a.status, 0x6101);
+      tc_fence_after();
+      const uint32_t kA = sh.base + kOffK, vA = sh.base + kOffV;
+      const uint32_t pA = sh.base + kOffP, dsA = sh.base + kOffDS;
+      auto stage = [&](int k) { return sh.base + kOffStage + (k % kStages) * kStageBytes; };
+      auto issue_sdp = [&](int k) {  // S^T = K Q^T and dP^T = V dO^T into buffers k & 1
+        const uint32_t qb = stage(k) + kStageQ, db = stage(k) + kStageDO;
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t offa = (kk >> 2) * kBoxK + (kk & 3) * 32;
+          const uint32_t offb = (kk >> 2) * kBoxQ + (kk & 3) * 32;
+          tc_mma_ss(t_s(k & 1), sdesc_sw128(kA + offa, 16, 1024), sdesc_sw128(qb + offb, 16, 1024), kIdS,
+                    kk > 0);
+        }
+#pragma unroll
+        for (int kk = 0; kk < kD / 16; ++kk) {
+          const uint32_t offa = (kk >> 2) * kBoxK + (kk & 3) * 32;
+          const uint32_t offb = (kk >> 2) * kBoxQ + (kk & 3) * 32;
+          tc_mma_ss(t_d(k & 1), sdesc_sw128(vA + offa, 16, 1024), sdesc_sw128(db + offb, 16, 1024), kIdS,
+                    kk > 0);
+        }
+        tc_commit(sh.bar(B_SFULL + (k & 1)));
+      };
+      if (ok && it.n_it > 0) {
+        if (wait_bar(sh, sh.bar(B_QFULL), 0, a.status, 0x6102)) {
+          tc_fence_after();
+          issue_sdp(0);
+        } else {
+          ok = false;
+        }
+      }
+      for (int k = 0; k < it.n_it && ok; ++k) {
+        const int b = k & 1;
+        if (k + 1 < it.n_it) {
+          // S / dP of the next tile run while the softmax warps work on this one
+          const int k1 = k + 1;
+          if (!wait_bar(sh, sh.bar(B_QFULL + k1 % kStages), (k1 / kStages) & 1, a.status, 0x6103)) {
+            ok = false;
+            break;
+          }
+          // its dP^T buffer held dQ^T(k - 1): wait until the dQ warps read it
+          if (k >= 1 && !wait_bar(sh, sh.bar(B_DQFREE + (k1 & 1)), ((k - 1) >> 1) & 1, a.status, 0x6104)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
+          issue_sdp(k1);
+        }
+        if (!wait_bar(sh, sh.bar(B_PFULL), k & 1, a.status, 0x6105)) {
+          ok = false;
+          break;
+        }
+        tc_fence_after();
+        // dQ^T = K^T dS^T  (into the dP^T buffer of this tile, already read)
+#pragma unroll
+        for (int kk = 0; kk < kKT / 16; ++kk)
+          tc_mma_ss(t_d(b), sdesc_sw128(kA + kk * 2048, kBoxK, 1024), sdesc_sw128(dsA + kk * 2048, kBoxQ, 1024),
+                    kIdDQ, kk > 0);
+        tc_commit(sh.bar(B_DQFULL + b));
+        // dV += P^T dO ; dK += dS^T Q
+        const uint32_t db = stage(k) + kStageDO, qb = stage(k) + kStageQ;
+#pragma unroll
+        for (int kk = 0; kk < kQT / 16; ++kk)
+          tc_mma_ss(T_DV, sdesc_sw128(pA + kk * 32, 16, 1024), sdesc_sw128(db + kk * 2048, kBoxQ, 1024), kIdAcc,
+                    (k > 0 || kk > 0) ? 1u : 0u);
+#pragma unroll
+        for (int kk = 0; kk < kQT / 16; ++kk)
+          tc_mma_ss(T_DK, sdesc_sw128(dsA + kk * 32, 16, 1024), sdesc_sw128(qb + kk * 2048, kBoxQ, 1024), kIdAcc,
+                    (k > 0 || kk > 0) ? 1u : 0u);
+        tc_commit(sh.bar(B_PBFREE));
+        tc_commit(sh.bar(B_QEMPTY + k % kStages));
+      }
+      if (ok) tc_commit(sh.bar(B_ACC));
+    }
+  } else if (warp < 4) {
+    // ------------------------------------------ softmax / dS, dK epilogue --
+    const int r = warp * 32 + lane;  // key row within the tile = TMEM lane
+    const uint32_t loff = static_cast<uint32_t>(warp * 32) << 16;
+    const float sl2 = a.scale * 1.4426950408889634f;
+    const uint64_t sl2x2 = f2(sl2, sl2), sc2 = f2(a.scale, a.scale);
+    const int key = it.kt * kKT + r;
+    bool ok = true;
+    uint8_t* pbuf = sh.gen + kOffP;
+    uint8_t* dsbuf = sh.gen + kOffDS;
+    for (int k = 0; k < it.n_it && ok; ++k) {
+      const int b = k & 1;
+      const int q0 = q0_of(k);
+      if (!wait_bar(sh, sh.bar(B_SFULL + b), (k >> 1) & 1, a.status, 0x6201)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      const float4* l2v = reinterpret_cast<const float4*>(sh.gen + kOffLse + (k % kStages) * 512);
+      const float4* ddv = l2v + 16;
+      const bool diag = q0 < it.kt * kKT + kKT;  // a query of this tile may precede a key
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t sv[32], dp[32];
+        tmem_ld32(t_s(b) + loff + hf * 32, sv);
+        tmem_ld32(t_d(b) + loff + hf * 32, dp);
+        tmem_ld_wait();
+        uint32_t pw[16], dw[16];
+        auto half = [&](auto masked) {
+          constexpr bool kMask = decltype(masked)::value;
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {  // 4 queries at a time
+            const float4 lq = l2v[hf * 8 + q4];
+            const float4 dq4 = ddv[hf * 8 + q4];
+            const int c = q4 * 4;
+            const int qa = q0 + hf * 32 + c;
+            const uint64_t x01 = fma_f32x2(f2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2x2,
+                                           f2(-lq.x, -lq.y));
+            const uint64_t x23 = fma_f32x2(f2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), sl2x2,
+                                           f2(-lq.z, -lq.w));
+            float p0 = fast_exp2(f2_lo(x01)), p1 = fast_exp2(f2_hi(x01));
+            float p2 = fast_exp2(f2_lo(x23)), p3 = fast_exp2(f2_hi(x23));
+            if (kMask) {
+              if (key > qa) p0 = 0.f;
+              if (key > qa + 1) p1 = 0.f;
+              if (key > qa + 2) p2 = 0.f;
+              if (key > qa + 3) p3 = 0.f;
+            }
+            const uint64_t t01 = add_f32x2(f2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), f2(-dq4.x, -dq4.y));
+            const uint64_t t23 =
+                add_f32x2(f2(__uint_as_float(dp[c + 2]), __uint_as_float(dp[c + 3])), f2(-dq4.z, -dq4.w));
+            const uint64_t d01 = mul_f32x2(mul_f32x2(t01, f2(p0, p1)), sc2);
+            const uint64_t d23 = mul_f32x2(mul_f32x2(t23, f2(p2, p3)), sc2);
+            pw[q4 * 2] = pack_bf16x2(p0, p1);
+            pw[q4 * 2 + 1] = pack_bf16x2(p2, p3);
+            dw[q4 * 2] = pack_bf16x2(f2_lo(d01), f2_hi(d01));
+            dw[q4 * 2 + 1] = pack_bf16x2(f2_lo(d23), f2_hi(d23));
+          }
+        };
+        if (diag) half(std::true_type{});
+        else half(std::false_type{});
+        // the P / dS buffers are free once dQ, dV and dK of the previous
+        // tile have read them
+        if (hf == 0 && k > 0 && !wait_bar(sh, sh.bar(B_PBFREE), (k - 1) & 1, a.status, 0x6202)) {
+          ok = false;
+          break;
+        }
+#pragma unroll
+        for (int cc = 0; cc < 4; ++cc) {
+          const int ch = hf * 4 + cc;
+          const int off = r * 128 + ((ch ^ (r & 7)) << 4);
+          *reinterpret_cast<uint4*>(pbuf + off) = make_uint4(pw[cc * 4], pw[cc * 4 + 1], pw[cc * 4 + 2], pw[cc * 4 + 3]);
+          *reinterpret_cast<uint4*>(dsbuf + off) = make_uint4(dw[cc * 4], dw[cc * 4 + 1], dw[cc * 4 + 2], dw[cc * 4 + 3]);
+        }
+      }
+      if (!ok) break;
+      fence_proxy_async_smem();
+      tc_fence_before();
+      mbar_arrive(sh.bar(B_PFULL));
+    }
+    // ------------------------------------------------------- dK epilogue --
+    if (ok && wait_bar(sh, sh.bar(B_ACC), 0, a.status, 0x6203)) {
+      tc_fence_after();
+      // the TMEM loads are warp-collective: every lane loads, live rows store
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dk.ptr) + it.b * a.dk.sb +
+                           static_cast<int64_t>(key) * a.dk.sn + it.g * a.dk.sh;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(T_DK + loff + c * 32, v);
+        tmem_ld_wait();
+        if (key < a.N) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 8)
+            *reinterpret_cast<uint4*>(dst + c * 32 + e) = make_uint4(
+                pack_bf16x2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
+                pack_bf16x2(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])),
+                pack_bf16x2(__uint_as_float(v[e + 4]), __uint_as_float(v[e + 5])),
+                pack_bf16x2(__uint_as_float(v[e + 6]), __uint_as_float(v[e + 7])));
+        }
+      }
+    }
+  } else {
+    // ------------------------------------- dQ readback + reduce, dV epilogue
+    const int q4w = warp & 3;
+    const int r = q4w * 32 + lane;  // feature of dQ^T = TMEM lane; key row in the epilogue
+    const uint32_t loff = static_cast<uint32_t>(q4w * 32) << 16;
+    float* stage_dq = reinterpret_cast<float*>(sh.gen + kOffDQ);
+    bool ok = true;
+    for (int k = 0; k < it.n_it && ok; ++k) {
+      const int b = k & 1;
+      if (!wait_bar(sh, sh.bar(B_DQFULL + b), (k >> 1) & 1, a.status, 0x6301)) {
+        ok = false;
+        break;
+      }
+      tc_fence_after();
+      uint32_t qv[64];
+      tmem_ld32(t_d(b) + loff, *reinterpret_cast<uint32_t(*)[32]>(&qv[0]));
+      tmem_ld32(t_d(b) + loff + 32, *reinterpret_cast<uint32_t(*)[32]>(&qv[32]));
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(sh.bar(B_DQFREE + b));
+      // the staging buffer is free once the previous reduce has read it
+      if (k > 0 && !wait_bar(sh, sh.bar(B_STGFREE), (k - 1) & 1, a.status, 0x6302)) {
+        ok = false;
+        break;
+      }
+#pragma unroll
+      for (int c = 0; c < kQT; ++c) stage_dq[c * kD + r] = __uint_as_float(qv[c]);
+      fence_proxy_async_smem();
+      mbar_arrive(sh.bar(B_STG));
+      bool stg_ok = true;
+      if (r == 0) {
+        stg_ok = wait_bar(sh, sh.bar(B_STG), k & 1, a.status, 0x6303);
+        if (stg_ok) {
+          // add the [64 queries][128] tile to the fp32 accumulator (rows
+          // past N are dropped by the unit)
+          tma_reduce_add_4d(&tm_dq, sh.base + kOffDQ, 0, it.g * G + head_of(k), q0_of(k), it.b);
+          bulk_commit();
+          bulk_wait_read();
+          mbar_arrive(sh.bar(B_STGFREE));
+        }
+      }
+      // keep warp 4 uniform for the warp-collective TMEM loads
+      if (q4w == 0) stg_ok = __shfl_sync(0xffffffffu, stg_ok, 0);
+      if (!stg_ok) ok = false;
+    }
+    if (r == 0) bulk_wait_all();
+    // ------------------------------------------------------- dV epilogue --
+    if (ok && wait_bar(sh, sh.bar(B_ACC), 0, a.status, 0x6304)) {
+      tc_fence_after();
+      const int key = it.kt * kKT + r;
+      // the TMEM loads are warp-collective: every lane loads, live rows store
+      __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dv.ptr) + it.b * a.dv.sb +
+                           static_cast<int64_t>(key) * a.dv.sn + it.g * a.dv.sh;
+#pragma unroll 1
+      for (int c = 0; c < 4; ++c) {
+        uint32_t v[32];
+        tmem_ld32(T_DV + loff + c * 32, v);
+        tmem_ld_wait();
+        if (key < a.N) {
+#pragma unroll
+          for (int e = 0; e < 32; e += 8)
+            *reinterpret_cast<uint4*>(dst + c * 32 + e) = make_uint4(
+                pack_bf16x2(__uint_as_float(v[e]), __uint_as_float(v[e + 1])),
+                pack_bf16x2(__uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])),
+                pack_bf16x2(__uint_as_float(v[e + 4]), __uint_as_float(v[e + 5])),
+                pack_bf16x2(__uint_as_float(v[e + 6]), __uint_as_float(v[e + 7])));
+        }
+      }
+    }
+  }
+
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  if (warp == 9) tmem_dealloc(tmem, 512);
+}
+
+// -------------------------------------------------------------- finalize --
+__global__ void __launch_bounds__(256)
+v2_bwd_finalize_kernel(V2BwdArgs a, BwdWs w) {
+  const int H2 = 2 * a.h;
+  const long long rows = static_cast<long long>(a.B) * a.N * H2;
+  const long long total = rows * (kD / 8);
+  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const long long row = idx / (kD / 8);
+    const int c8 = static_cast<int>(idx % (kD / 8)) * 8;
+    const int hq = static_cast<int>(row % H2);
+    const long long bn = row / H2;
+    const int n = static_cast<int>(bn % a.N), b = static_cast<int>(bn / a.N);
+    const float* src = w.dq + row * kD + c8;
+    const float4 x0 = *reinterpret_cast<const float4*>(src);
+    const float4 x1 = *reinterpret_cast<const float4*>(src + 4);
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dq.ptr) + b * a.dq.sb +
+                         static_cast<int64_t>(n) * a.dq.sn + hq * a.dq.sh + c8;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(pack_bf16x2(x0.x, x0.y), pack_bf16x2(x0.z, x0.w),
+                                                pack_bf16x2(x1.x, x1.y), pack_bf16x2(x1.z, x1.w));
+  }
+}
+
+// ------------------------------------------------- gate-projection grads --
+// dX[t, c] = sum_p dz[t, p] W[c, p]: a thread owns two columns (W rows in
+// registers), a block 64 tokens x 256 columns; dz rows staged in shared
+// memory and read as broadcasts.
+constexpr int kDxTok = 64;
+
+template <int HC>
+__global__ void __launch_bounds__(128)
+v2_bwd_dx_kernel(int T, int d_model, int h, const float* __restrict__ dz,
+                 const __nv_bfloat16* __restrict__ W, __nv_bfloat16* __restrict__ dx) {
+  __shared__ float s_dz[kDxTok][HC];
+  const int t0 = blockIdx.x * kDxTok;
+  const int c = blockIdx.y * 256 + threadIdx.x * 2;
+  for (int i = threadIdx.x; i < kDxTok * HC; i += 128) {
+    const int t = i / HC, p = i % HC;
+    s_dz[t][p] = (t0 + t < T && p < h) ? dz[static_cast<int64_t>(t0 + t) * h + p] : 0.f;
+  }
+  float w0[HC], w1[HC];
+#pragma unroll
+  for (int p = 0; p < HC; ++p) {
+    const bool in = c < d_model && p < h;
+    w0[p] = in ? __bfloat162float(W[static_cast<int64_t>(c) * h + p]) : 0.f;
+    w1[p] = in ? __bfloat162float(W[static_cast<int64_t>(c + 1) * h + p]) : 0.f;
+  }
+  __syncthreads();
+  if (c >= d_model) return;
+  const int tn = min(kDxTok, T - t0);
+#pragma unroll 1
+  for (int t = 0; t < tn; ++t) {
+    float a0 = 0.f, a1 = 0.f;
+#pragma unroll
+    for (int p = 0; p < HC; ++p) {
+      a0 = fmaf(s_dz[t][p], w0[p], a0);
+      a1 = fmaf(s_dz[t][p], w1[p], a1);
+    }
+    *reinterpret_cast<uint32_t*>(dx + static_cast<int64_t>(t0 + t) * d_model + c) = pack_bf16x2(a0, a1);
+  }
+}
+
+// dW partials: block = (64 columns, one chunk of kDwChunk tokens); thread =
+// (column, 16 gate heads); dz staged 128 tokens at a time.
+constexpr int kDwSub = 128;
+
+__global__ void __launch_bounds__(256)
+v2_bwd_dw_partial_kernel(int T, int d_model, int h, const float* __restrict__ dz,
+                         const __nv_bfloat16* __restrict__ X, float* __restrict__ part) {
+  __shared__ float s_dz[kDwSub][64];
+  const int cl = threadIdx.x & 63, pg = threadIdx.x >> 6;
+  const int c = blockIdx.x * 64 + cl;
+  const int chunk = blockIdx.y;
+  float acc[16];
+#pragma unroll
+  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
+  const int tbeg = chunk * kDwChunk, tend = min(T, tbeg + kDwChunk);
+  for (int ts = tbeg; ts < tend; ts += kDwSub) {
+    const int tn = min(kDwSub, tend - ts);
+    __syncthreads();
+    for (int i = threadIdx.x; i < kDwSub * 64; i += 256) {
+      const int t = i >> 6, p = i & 63;
+      s_dz[t][p] = (t < tn && p < h) ? dz[static_cast<int64_t>(ts + t) * h + p] : 0.f;
+    }
+    __syncthreads();
+    if (c < d_model && pg * 16 < h) {
+#pragma unroll 4
+      for (int t = 0; t < tn; ++t) {
+        const float xv = __bfloat162float(X[static_cast<int64_t>(ts + t) * d_model + c]);
+#pragma unroll
+        for (int i = 0; i < 16; ++i) acc[i] = fmaf(xv, s_dz[t][pg * 16 + i], acc[i]);
+      }
+    }
+  }
+  if (c < d_model) {
+#pragma unroll
+    for (int i = 0; i < 16; ++i) {
+      const int p = pg * 16 + i;
+      if (p < h) part[(static_cast<int64_t>(chunk) * d_model + c) * h + p] = acc[i];
+    }
+  }
+}
+
+__global__ void __launch_bounds__(256)
+v2_bwd_dw_reduce_kernel(int d_model, int h, int chunks, const float* __restrict__ part,
+                        float* __restrict__ dw) {
+  const int64_t n = static_cast<int64_t>(d_model) * h;
+  for (int64_t i = static_cast<int64_t>(blockIdx.x) * blockDim.x + threadIdx.x; i < n;
+       i += static_cast<int64_t>(gridDim.x) * blockDim.x) {
+    float s = 0.f;
+    for (int c = 0; c < chunks; ++c) s += part[c * n + i];
+    dw[i] = s;
+  }
+}
+
+cudaError_t launch_dx(int T, int d_model, int h, const float* dz, const void* W, void* dx,
+                      cudaStream_t s) {
+  const dim3 grid((T + kDxTok - 1) / kDxTok, (d_model + 255) / 256);
+  const auto* w = static_cast<const __nv_bfloat16*>(W);
+  auto* o = static_cast<__nv_bfloat16*>(dx);
+  if (h <= 16) v2_bwd_dx_kernel<16><<<grid, 128, 0, s>>>(T, d_model, h, dz, w, o);
+  else if (h <= 32) v2_bwd_dx_kernel<32><<<grid, 128, 0, s>>>(T, d_model, h, dz, w, o);
+  else v2_bwd_dx_kernel<64><<<grid, 128, 0, s>>>(T, d_model, h, dz, w, o);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t v2_bwd_workspace_bytes(int B, int N, int h, int d_model) {
+  size_t total = 0;
+  carve(nullptr, B, N, h, d_model, &total);
+  return total;
+}
+
+cudaError_t launch_v2_bwd(const V2BwdArgs& a_in, cudaStream_t s) {
+  V2BwdArgs a = a_in;
+  size_t total = 0;
+  const BwdWs w = carve(a.workspace, a.B, a.N, a.h, a.dw ? a.d_model : 0, &total);
+  if (total > a.workspace_bytes) return cudaErrorInvalidValue;
+  const long long T = static_cast<long long>(a.B) * a.N;
+  cudaError_t e;
+  if (a.gate == nullptr) {
+    GateArgs ga{static_cast<int>(T), a.d_model, a.h, a.x, a.d_model, a.w, w.gate};
+    e = launch_gate(ga, s);
+    if (e != cudaSuccess) return e;
+    a.gate = w.gate;
+  }
+  float* dz = a.dz ? a.dz : w.dz;
+
+  const long long pre_rows = static_cast<long long>(a.B) * a.h * w.npad;
+  v2_bwd_pre_kernel<<<static_cast<unsigned>((pre_rows + kPreWarps - 1) / kPreWarps), kPreWarps * 32, 0, s>>>(
+      a, w, a.gate, dz);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  CUtensorMap tq, tk, tv, tg, tdo, tdq;
+  const da_t4 dot{w.dodd, static_cast<int64_t>(a.N) * a.h * kD, static_cast<int64_t>(a.h) * kD, kD};
+  if (!encode_tmap_bf16_4d(&tq, a.q, a.B, a.N, 2 * a.h, kD, kQT) ||
+      !encode_tmap_bf16_4d(&tk, a.k, a.B, a.N, a.h_kv, kD, kKT) ||
+      !encode_tmap_bf16_4d(&tv, a.v, a.B, a.N, a.h_kv, kD, kKT) ||
+      !encode_tmap_bf16_4d(&tg, a.dout, a.B, a.N, a.h, kD, kQT) ||
+      !encode_tmap_bf16_4d(&tdo, dot, a.B, a.N, a.h, kD, kQT) ||
+      !encode_tmap_f32_4d(&tdq, w.dq, a.B, a.N, 2 * a.h, kD, kQT))
+    return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(v2_bwd_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int n_kt = (a.N + kKT - 1) / kKT;
+  const int units = a.B * a.h_kv;
+  const int sms = a.num_sms > 0 ? a.num_sms : 148;
+  // (batch, group) units per scheduling block: about two waves of items
+  int per = (2 * sms + n_kt - 1) / n_kt;
+  if (per < 1) per = 1;
+  if (per > units) per = units;
+  v2_bwd_main_kernel<<<n_kt * units, kThreads, kSmemBytes, s>>>(tq, tk, tv, tg, tdo, tdq, a, w, per);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  const long long work = T * 2 * a.h * (kD / 8);
+  int grid = static_cast<int>((work + 255) / 256);
+  if (grid > 8 * sms) grid = 8 * sms;
+  if (grid < 1) grid = 1;
+  v2_bwd_finalize_kernel<<<grid, 256, 0, s>>>(a, w);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  if (a.dx) {
+    e = launch_dx(static_cast<int>(T), a.d_model, a.h, dz, a.w, a.dx, s);
+    if (e != cudaSuccess) return e;
+  }
+  if (a.dw) {
+    v2_bwd_dw_partial_kernel<<<dim3((a.d_model + 63) / 64, w.chunks), 256, 0, s>>>(
+        static_cast<int>(T), a.d_model, a.h, dz, static_cast<const __nv_bfloat16*>(a.x), w.dw_part);
+    e = cudaGetLastError();
+    if (e != cudaSuccess) return e;
+    const long long n = static_cast<long long>(a.d_model) * a.h;
+    int g2 = static_cast<int>((n + 255) / 256);
+    if (g2 > 4 * sms) g2 = 4 * sms;
+    v2_bwd_dw_reduce_kernel<<<g2, 256, 0, s>>>(a.d_model, a.h, w.chunks, w.dw_part, a.dw);
+    e = cudaGetLastError();
+  }
+  return e;
+}
+
+}  // namespace da

@@ -27,7 +27,8 @@
 //     first tile, a guarded stale max afterwards), P written back to TMEM as
 //     bf16, O rescaled in TMEM on the rare tiles that raise the max.
 //     The same threads run the epilogue: O_even / l_even - gate * O_odd /
-//     l_odd, bf16 store, optional log-sum-exp.
+//     l_odd, bf16 store, optional log-sum-exp and per-head outputs (the
+//     backward's saves).
 //
 // Every mbarrier wait is bounded (about 2 s); on expiry the kernel records
 // DA_ERR_TIMEOUT in the status word, raises a shared abort flag so the other
@@ -348,6 +349,30 @@ v2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
             v.z = pack_bf16x2(diff(oe[c][e + 4], oo[c][e + 4]), diff(oe[c][e + 5], oo[c][e + 5]));
             v.w = pack_bf16x2(diff(oe[c][e + 6], oo[c][e + 6]), diff(oe[c][e + 7], oo[c][e + 7]));
             *reinterpret_cast<uint4*>(dst + c * 32 + e) = v;
+          }
+        }
+        if (a.o_heads.ptr) {
+          // the saves for the backward: each head's normalised output
+          const float inv_o = 1.f / lo;
+          __nv_bfloat16* he = static_cast<__nv_bfloat16*>(a.o_heads.ptr) + w.b * a.o_heads.sb +
+                              static_cast<int64_t>(n) * a.o_heads.sn + 2 * w.p * a.o_heads.sh + wg * 64;
+          __nv_bfloat16* ho = he + a.o_heads.sh;
+#pragma unroll
+          for (int c = 0; c < 2; ++c) {
+#pragma unroll
+            for (int e = 0; e < 32; e += 8) {
+              uint4 ve, vo;
+              ve.x = pack_bf16x2(__uint_as_float(oe[c][e]) * ie, __uint_as_float(oe[c][e + 1]) * ie);
+              ve.y = pack_bf16x2(__uint_as_float(oe[c][e + 2]) * ie, __uint_as_float(oe[c][e + 3]) * ie);
+              ve.z = pack_bf16x2(__uint_as_float(oe[c][e + 4]) * ie, __uint_as_float(oe[c][e + 5]) * ie);
+              ve.w = pack_bf16x2(__uint_as_float(oe[c][e + 6]) * ie, __uint_as_float(oe[c][e + 7]) * ie);
+              vo.x = pack_bf16x2(__uint_as_float(oo[c][e]) * inv_o, __uint_as_float(oo[c][e + 1]) * inv_o);
+              vo.y = pack_bf16x2(__uint_as_float(oo[c][e + 2]) * inv_o, __uint_as_float(oo[c][e + 3]) * inv_o);
+              vo.z = pack_bf16x2(__uint_as_float(oo[c][e + 4]) * inv_o, __uint_as_float(oo[c][e + 5]) * inv_o);
+              vo.w = pack_bf16x2(__uint_as_float(oo[c][e + 6]) * inv_o, __uint_as_float(oo[c][e + 7]) * inv_o);
+              *reinterpret_cast<uint4*>(he + c * 32 + e) = ve;
+              *reinterpret_cast<uint4*>(ho + c * 32 + e) = vo;
+            }
           }
         }
         if (a.lse) {

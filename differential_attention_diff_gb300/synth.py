@@ -45,18 +45,22 @@ def v1_inputs(B, N, H, dqk, dv, dtype="bf16", seed=0, device="cpu",
     return out
 
 
-def v2_inputs(B, N, h, hkv, d, d_model, seed=0, device="cpu"):
+def v2_inputs(B, N, h, hkv, d, d_model, seed=0, device="cpu", with_dout=False):
     """V2 operands: q [B,N,2h,d]; k, v [B,N,hkv,d]; x [B,N,d_model];
-    w_lambda [d_model,h] (all bf16)."""
+    w_lambda [d_model,h] (all bf16); optionally the upstream gradient dout
+    [B,N,h,d] ~ N(0, 1)."""
     dt = torch.bfloat16
     g = _gen(seed, device)
-    return {
+    out = {
         "q": _randn((B, N, 2 * h, d), 1.0, dt, g, device),
         "k": _randn((B, N, hkv, d), 1.0, dt, g, device),
         "v": _randn((B, N, hkv, d), 1.0, dt, g, device),
         "x": _randn((B, N, d_model), 1.0, dt, g, device),
         "w_lambda": _randn((d_model, h), 0.02, dt, g, device),
     }
+    if with_dout:
+        out["dout"] = _randn((B, N, h, d), 1.0, dt, g, device)
+    return out
 
 
 def decode_inputs(B, L_max, h, hkv, d, d_model, seed=0, device="cpu",

@@ -171,7 +171,11 @@ da_status diffattn_v2_gate(const da_v2_gate_params* p, void* cuda_stream);
  * Gate source: either `gate` (fp32 [B, N, h] contiguous, already through the
  * sigmoid) or, when gate == NULL, x (bf16 [B, N, d_model] contiguous) and
  * w_lambda (bf16 [d_model, h]); the gate is then computed into the workspace
- * (diffattn_v2_fwd_workspace_size bytes).  Optional lse: fp32 [B, 2h, N].
+ * (diffattn_v2_fwd_workspace_size bytes).
+ * Optional saves for diffattn_v2_bwd (NULL pointer = not written): lse, fp32
+ * [B, 2h, N] contiguous (natural-log log-sum-exp of each head's scaled scores
+ * per query); o_heads, bf16 [B, N, 2h, d] (each head's normalised output
+ * O[t, j] before the even/odd combination).
  * Supported: d = 128, causal, (2h / h_kv) even. */
 typedef struct {
   int B, N, h, h_kv, d, d_model;
@@ -183,12 +187,58 @@ typedef struct {
   const void* w_lambda;
   da_t4 out;
   float* lse;
+  da_t4 o_heads;
   void* workspace;
   size_t workspace_bytes;
 } da_v2_fwd_params;
 
 size_t diffattn_v2_fwd_workspace_size(int B, int N, int h, int gate_given);
 da_status diffattn_v2_fwd(const da_v2_fwd_params* p, void* cuda_stream);
+
+/* ------------------------------------------------------------------------ */
+/* V2 backward: gradients of diffattn_v2_fwd (and of the gate projection)
+ * given dOut.  The pages state no backward; it is the chain rule of the V2
+ * forward ([P2] §1, §4).  With g = sigmoid(z), z[t, p] = x[t] . w_lambda[:, p],
+ * G = dOut[t, p] and O_j the normalised output of query head j:
+ *   dO_2p = G,  dO_2p+1 = -g G,  dz = -<G, O_2p+1> g (1 - g)
+ *   dW_lambda = X^T dz,  dX (the part through the gate) = dz W_lambda^T
+ *   per query head j reading K/V head c:  A = softmax(s Q_j K_c^T) (causal),
+ *   dP = dO_j V_c^T,  dS = A (dP - <dO_j, O_j>),
+ *   dQ_j = s dS K_c,  dK_c += s dS^T Q_j,  dV_c += A^T dO_j
+ * (dK and dV sum over every query head of the K/V group).
+ * Inputs: the forward's q, k, v (as in diffattn_v2_fwd), the gate source
+ * (`gate`, or x and w_lambda when gate == NULL), the forward's saves
+ * `o_heads` and `lse`, and dout: bf16 [B, N, h, d].
+ * Outputs (overwritten): dq [B, N, 2h, d], dk, dv [B, N, h_kv, d], bf16.
+ * Optional outputs (NULL = not computed): dgate_logit fp32 [B, N, h]
+ * contiguous (dz); dx bf16 [B, N, d_model] contiguous and dw_lambda fp32
+ * [d_model, h] row-major, both of which need x and w_lambda.
+ * Supported: d = 128, causal, (2h / h_kv) even; d_model % 64 == 0 and
+ * h <= 64 where x / w_lambda are used.
+ * workspace: diffattn_v2_bwd_workspace_size(B, N, h, d_model) bytes (with
+ * d_model = 0 it covers calls that do not request dw_lambda), 256-byte
+ * aligned, contents on entry irrelevant. */
+typedef struct {
+  int B, N, h, h_kv, d, d_model;
+  int causal;
+  float softmax_scale;   /* <= 0 selects 1/sqrt(d) */
+  da_t4 q, k, v;
+  const float* gate;
+  const void* x;
+  const void* w_lambda;
+  da_t4 o_heads;
+  const float* lse;
+  da_t4 dout;
+  da_t4 dq, dk, dv;
+  float* dgate_logit;
+  void* dx;
+  float* dw_lambda;
+  void* workspace;
+  size_t workspace_bytes;
+} da_v2_bwd_params;
+
+size_t diffattn_v2_bwd_workspace_size(int B, int N, int h, int d_model);
+da_status diffattn_v2_bwd(const da_v2_bwd_params* p, void* cuda_stream);
 
 /* ------------------------------------------------------------------------ */
 /* V2 decode.  [P1] "V2로의 진화" and [P2] §2: one new token per sequence

@@ -306,7 +306,7 @@ def v2_backward(q, k, v, x, w, dout, *, scale: float | None = None, causal: bool
             dq[b, :, j] = scale * dS @ K
             dk[b, :, c] += scale * dS.T @ Q
             dv[b, :, c] += a.T @ dO
-    return dict(dq=dq, dk=dk, dv=dv, dx=dx, dw=dw, dz=dz, gate=g)
+    return dict(dq=dq, dk=dk, dv=dv, dx=dx, dw=dw, dz=dz, gate=g, o=o, lse=fwd["lse"])
 
 
 def v2_decode(q, k_cache, v_cache, seqlens, gate, *, scale: float | None = None):

@@ -1,11 +1,13 @@
-"""bf16 rounding model of the V1 backward (test infrastructure).
+"""bf16 rounding models of the V1 and V2 backwards (test infrastructure).
 
-Runs the chain rule in exact fp64 EXCEPT at the five points where the
-library's backward must hold bf16 values: the forward outputs Y and O2, the
-upstream gradient after the RMSNorm backward (dO, an MMA operand), and the
-P and dS tiles fed to the tensor cores.  Its error against the fp64 oracle
-is the error any bf16 implementation with these storage points has; the GPU
-parity tests bound the library's error by a small multiple of it.
+Each runs the chain rule in exact fp64 EXCEPT at the points where the
+library's backward must hold bf16 values.  V1: the forward outputs Y and O2,
+the upstream gradient after the RMSNorm backward (dO, an MMA operand), and the
+P and dS tiles fed to the tensor cores.  V2: the saved per-head outputs O_j,
+the odd heads' dO = -g dOut (an MMA operand), the P and dS tiles, and the
+bf16 gradient outputs.  A model's error against the fp64 oracle is the error
+any bf16 implementation with these storage points has; the GPU parity tests
+bound the library's error by a small multiple of it.
 """
 
 import numpy as np
@@ -46,4 +48,35 @@ def rounded_backward(f, fwd, li, heads=None):
                 out[f"dk{t}"][b, :, h] = dS.T @ Q
                 out["dv"][b, :, h] += bf16(sig * P).T @ dO
     out["dlam"] = dlam
+    return out
+
+
+def rounded_backward_v2(f, fwd, gate, scale=None, rnd=bf16):
+    """f: fp64 V2 inputs (q, k, v, x, w_lambda, dout); fwd: the oracle's V2
+    forward on them; gate: fp64 [B, N, h].  Returns dq, dk, dv, dz, dx, dw
+    with the V2 backward's bf16 storage points (``rnd`` = the rounding; the
+    identity gives the exact chain rule)."""
+    q, k, v, dout = f["q"], f["k"], f["v"], f["dout"]
+    B, N, H2, d = q.shape
+    group = H2 // k.shape[2]
+    s = 1.0 / np.sqrt(d) if scale is None else scale
+    o = rnd(fwd["o"])
+    dodd = rnd(-gate[..., None] * dout)
+    out = dict(dq=np.zeros_like(q), dk=np.zeros_like(k), dv=np.zeros_like(v))
+    for b in range(B):
+        for j in range(H2):
+            c = j // group
+            dO = dout[b, :, j // 2] if j % 2 == 0 else dodd[b, :, j // 2]
+            D = (dO * o[b, :, j]).sum(1)
+            P = np.tril(np.exp(s * q[b, :, j] @ k[b, :, c].T - fwd["lse"][b, j][:, None]))
+            dS = rnd(s * P * (dO @ v[b, :, c].T - D[:, None]))
+            out["dq"][b, :, j] = dS @ k[b, :, c]
+            out["dk"][b, :, c] += dS.T @ q[b, :, j]
+            out["dv"][b, :, c] += rnd(P).T @ dO
+    dz = -(dout * o[:, :, 1::2]).sum(-1) * gate * (1.0 - gate)
+    out["dz"] = dz
+    out["dx"] = rnd(dz @ f["w_lambda"].T)
+    out["dw"] = np.einsum("btk,btp->kp", f["x"], dz)
+    for n in ("dq", "dk", "dv"):
+        out[n] = rnd(out[n])
     return out

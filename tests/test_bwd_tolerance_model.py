@@ -19,7 +19,7 @@ import numpy as np
 import torch
 
 from differential_attention_diff_gb300 import synth
-from bf16_model import rounded_backward
+from bf16_model import rounded_backward, rounded_backward_v2
 from oracle import diffattn_oracle as orc
 
 
@@ -38,3 +38,20 @@ def test_bf16_rounding_model_sets_the_gradient_tolerance():
         fro[n] = float(np.linalg.norm(got[n] - e) / np.linalg.norm(e))
     assert max(maxrel.values()) > 2e-2, maxrel     # a fixed 2e-2 bar is unreachable
     assert max(fro.values()) < 0.5 * 1.5e-2, fro   # the Frobenius bar leaves margin
+
+
+def test_v2_rounding_model_is_the_chain_rule_and_sets_the_tolerance():
+    """The V2 model without rounding reproduces the oracle's gradients (so it
+    rounds the right quantities of the right formula); with bf16 rounding its
+    Frobenius error stays well under the GPU bars."""
+    t = synth.v2_inputs(1, 150, 2, 1, 128, 64, seed=5203, device="cpu", with_dout=True)
+    f = {k: v.to(torch.float64).numpy() for k, v in t.items()}
+    ref = orc.v2_backward(f["q"], f["k"], f["v"], f["x"], f["w_lambda"], f["dout"])
+    fwd = orc.v2_forward(f["q"], f["k"], f["v"], ref["gate"])
+    exact = rounded_backward_v2(f, fwd, ref["gate"], rnd=lambda a: a)
+    for n in ("dq", "dk", "dv", "dz", "dx", "dw"):
+        np.testing.assert_allclose(exact[n], ref[n], rtol=1e-10, atol=1e-12 * np.abs(ref[n]).max())
+    got = rounded_backward_v2(f, fwd, ref["gate"])
+    for n in ("dq", "dk", "dv", "dz", "dx", "dw"):
+        fro = float(np.linalg.norm(got[n] - ref[n]) / np.linalg.norm(ref[n]))
+        assert fro < 0.5 * 1.5e-2, (n, fro)
