@@ -61,6 +61,10 @@ def v2_fwd_flops(B, N, h, d):
     return B * 2 * h * 0.5 * 4.0 * N * N * d
 
 
+def v2_bwd_flops(B, N, h, d):
+    return B * 2 * h * 0.5 * 10.0 * N * N * d
+
+
 def decode_bytes(B, L, hkv, d):
     return 2.0 * B * L * hkv * d * 2
 
@@ -190,6 +194,23 @@ class V1FwdBwd(V1Fwd):
         return v1_bwd_flops(self.B, self.N, self.H, self.dqk, self.dv)
 
 
+    def e2e_setup(self):
+        names = ("q1", "q2", "k1", "k2", "v", "lq1", "lk1", "lq2", "lk2", "dy")
+        self.host = {k: self.t[k].cpu().pin_memory() for k in names}
+        self.host_g = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in self.grads.items()}
+        self.h2d = sum(v.numel() * v.element_size() for v in self.host.values())
+        self.d2h = sum(v.numel() * v.element_size() for v in self.host_g.values())
+
+    def e2e_step(self):
+        d = {k: v.to(self.out.device, non_blocking=True) for k, v in self.host.items()}
+        self.bd.diffattn_v1_fwd(*self.args(d), self.li, out=self.out, save=True, saves=self.saves,
+                                workspace=self.fws)
+        self.bd.diffattn_v1_bwd(*self.args(d), self.li, self.out, d["dy"], self.saves,
+                                grads=self.grads, workspace=self.ws)
+        for k, v in self.grads.items():
+            self.host_g[k].copy_(v, non_blocking=True)
+
+
 class V1FwdF32(V1Fwd):
     name = "v1_fwd_f32"
     desc = "V1 DiffAttn fwd fp32 B1 H2 N64 d_qk16 d_v32 causal, layer 1 (latency-bound)"
@@ -264,6 +285,76 @@ class V2Fwd(Workload):
         return dt, flops, f"batch 0, 4 pairs, {len(rows)} seeded query rows of 8192 (gate included)"
 
 
+class V2FwdBwd(V2Fwd):
+    name = "v2_fwd_bwd"
+    desc = ("V2 DiffAttn fwd+bwd bf16 B2 N8192 64q/8kv heads d128 causal, gate from X[2,8192,4096]; "
+            "grads of q, k, v, X, W_lambda")
+    launches = None
+
+    def work(self):
+        return v2_fwd_flops(self.B, self.N, self.h, self.d) + v2_bwd_flops(self.B, self.N, self.h, self.d)
+
+    def setup(self, dev):
+        from differential_attention_diff_gb300 import binding as bd, synth
+        self.bd = bd
+        self.t = synth.v2_inputs(self.B, self.N, self.h, self.hkv, self.d, self.dm, seed=1003,
+                                 device=dev, with_dout=True)
+        self.out = torch.empty((self.B, self.N, self.h, self.d), dtype=torch.bfloat16, device=dev)
+        need = bd.load().diffattn_v2_fwd_workspace_size(self.B, self.N, self.h, 0)
+        self.ws = torch.empty((need,), dtype=torch.uint8, device=dev)
+        t = self.t
+        _, self.saves = bd.diffattn_v2_fwd(t["q"], t["k"], t["v"], x=t["x"], w_lambda=t["w_lambda"],
+                                           out=self.out, save=True, workspace=self.ws)
+        need = bd.diffattn_v2_bwd_workspace_size(self.B, self.N, self.h, self.dm)
+        self.bws = torch.empty((need,), dtype=torch.uint8, device=dev)
+        self.grads = bd.diffattn_v2_bwd(t["q"], t["k"], t["v"], t["dout"], self.saves, x=t["x"],
+                                        w_lambda=t["w_lambda"], workspace=self.bws)
+
+    def _step(self, t):
+        self.bd.diffattn_v2_fwd(t["q"], t["k"], t["v"], x=t["x"], w_lambda=t["w_lambda"], out=self.out,
+                                save=True, saves=self.saves, workspace=self.ws)
+        self.bd.diffattn_v2_bwd(t["q"], t["k"], t["v"], t["dout"], self.saves, x=t["x"],
+                                w_lambda=t["w_lambda"], grads=self.grads, workspace=self.bws)
+
+    def run(self):
+        self._step(self.t)
+
+    def run_dominant(self):
+        t = self.t
+        self.bd.diffattn_v2_bwd(t["q"], t["k"], t["v"], t["dout"], self.saves, x=t["x"],
+                                w_lambda=t["w_lambda"], grads=self.grads, workspace=self.bws)
+
+    def dominant_work(self):
+        return v2_bwd_flops(self.B, self.N, self.h, self.d)
+
+    def e2e_setup(self):
+        self.host = {k: v.cpu().pin_memory() for k, v in self.t.items()}
+        self.host_g = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in self.grads.items()}
+        self.h2d = sum(v.numel() * v.element_size() for v in self.host.values())
+        self.d2h = sum(v.numel() * v.element_size() for v in self.host_g.values())
+
+    def e2e_step(self):
+        self._step({k: v.to(self.out.device, non_blocking=True) for k, v in self.host.items()})
+        for k, v in self.grads.items():
+            self.host_g[k].copy_(v, non_blocking=True)
+
+    def oracle_sample(self, big=True):
+        """fp64 oracle backward on a bounded sample: one (batch, K/V group) of
+        the workload cut to its first n tokens (causal, so a prefix is a
+        self-contained problem)."""
+        from oracle import diffattn_oracle as orc
+        n = 1024 if big else 256
+        G = 2 * self.h // self.hkv
+        sl = lambda x: x.to("cpu", torch.float64).numpy()  # noqa: E731
+        t = self.t
+        t0 = time.perf_counter()
+        orc.v2_backward(sl(t["q"][0:1, :n, 0:G]), sl(t["k"][0:1, :n, 0:1]), sl(t["v"][0:1, :n, 0:1]),
+                        sl(t["x"][0:1, :n]), sl(t["w_lambda"][:, 0:G // 2]), sl(t["dout"][0:1, :n, 0:G // 2]))
+        dt = time.perf_counter() - t0
+        flops = v2_fwd_flops(1, n, G // 2, self.d) + v2_bwd_flops(1, n, G // 2, self.d)
+        return dt, flops, f"batch 0, K/V group 0 ({G} query heads), first {n} tokens (fp64 oracle fwd+bwd)"
+
+
 class V2Decode(Workload):
     name = "v2_decode"
     desc = "V2 decode bf16 B64 cache 32768 8 KV heads 64 query heads d128, gate from X[64,4096]"
@@ -310,8 +401,16 @@ class V2DecodeSmall(V2Decode):
     B = 8
 
 
-WORKLOADS = {w.name: w for w in (V1Fwd, V1FwdF32, V2Fwd, V2Decode, V1FwdBwd)}
-PROFILE_ONLY = {V2DecodeSmall.name: V2DecodeSmall}
+class V2FwdBwdSmall(V2FwdBwd):
+    """The V2 training step at B1 N4096 (134 MB of dQ accumulators, above L2):
+    a size for multi-pass ncu captures of the backward's kernels."""
+    name = "v2_fwd_bwd_small"
+    desc = "V2 DiffAttn fwd+bwd bf16 B1 N4096 64q/8kv heads d128 causal (profiling size)"
+    B, N = 1, 4096
+
+
+WORKLOADS = {w.name: w for w in (V1Fwd, V1FwdF32, V2Fwd, V2Decode, V1FwdBwd, V2FwdBwd)}
+PROFILE_ONLY = {V2DecodeSmall.name: V2DecodeSmall, V2FwdBwdSmall.name: V2FwdBwdSmall}
 
 # ----------------------------------------------------------------- helpers --
 
@@ -321,6 +420,7 @@ KERNEL_SOURCES = {
     "v1_fwd_bwd": ("v1_bwd.cu", "softmax.cuh", "tma.cuh", "common.cuh"),
     "v2_fwd": ("v2_fwd.cu", "softmax.cuh", "tma.cuh", "common.cuh"),
     "v2_decode": ("decode.cu", "common.cuh"),
+    "v2_fwd_bwd": ("v2_bwd.cu", "softmax.cuh", "tma.cuh", "common.cuh"),
 }
 
 
