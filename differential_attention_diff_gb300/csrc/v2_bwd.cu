@@ -23,12 +23,14 @@
 //        S^T  = K Q^T,  dP^T = V dO^T  (TMEM, double-buffered, issued while
 //                                       the softmax warps work on the tile
 //                                       before)
-//        softmax warps (thread = key row): P^T and dS^T as bf16 rows in
-//                                       shared memory
+//        softmax warps (thread = key row): P^T and dS^T as bf16 into the
+//                                       S^T columns just read (TMEM), dS^T
+//                                       also into shared memory
 //        dQ^T = K^T dS^T   (TMEM, in the dP^T buffer just consumed) -> the
 //                          dQ warps stage it in shared memory and one thread
 //                          adds it to the fp32 accumulator by TMA reduce-add
-//        dV  += P^T dO,  dK += dS^T Q   (TMEM, 128 columns each)
+//        dV  += P^T dO,  dK += dS^T Q   (A operands from TMEM; 128 columns
+//                                        of TMEM each)
 //     then the softmax warps write dK and the dQ warps dV, as bf16;
 //  4. finalize: dQ accumulators -> bf16;
 //  5. (when asked) dX = dz W^T, and dW = X^T dz as per-chunk partial sums
@@ -37,9 +39,11 @@
 // Warp roles (320 threads): 0-3 softmax / dK epilogue, 4-7 dQ readback and
 // reduce / dV epilogue, 8 TMA producer, 9 MMA issuer.
 // TMEM: [0,128) dV, [128,256) dK, [256,384) S^T x 2, [384,512) dP^T / dQ^T x 2.
-// SMEM: K 32 KB, V 32 KB, 3 stages of (Q 16 KB, dO 16 KB), P^T 16 KB,
-//       dS^T 16 KB, dQ staging 32 KB, per-stage lse2 / D (1.5 KB); every bf16
-//       operand in 128-byte-swizzled 64-column boxes.
+// SMEM: K 32 KB, V 32 KB, 3 stages of (Q 16 KB, dO 16 KB), dS^T x 2
+//       (16 KB each), dQ staging 32 KB, per-stage lse2 / D (1.5 KB); every
+//       bf16 operand in 128-byte-swizzled 64-column boxes.  The MMAs are
+//       bound by shared-memory reads, which is why P^T and dS^T reach dV and
+//       dK through TMEM.
 // Every mbarrier wait is bounded (about 2 s); on expiry the kernel records
 // DA_ERR_TIMEOUT, raises an abort flag that the other roles see, and leaves.
 #include <type_traits>
@@ -65,16 +69,16 @@ constexpr int kOffStage = kOffV + 2 * kBoxK;  // 65536
 constexpr int kStageQ = 0;
 constexpr int kStageDO = 2 * kBoxQ;
 constexpr int kStageBytes = 4 * kBoxQ;                  // 32 KB
-constexpr int kOffP = kOffStage + kStages * kStageBytes;  // 163840
-constexpr int kOffDS = kOffP + kBoxK;
-constexpr int kOffDQ = kOffDS + kBoxK;                  // fp32 [64][128]
+constexpr int kOffDS = kOffStage + kStages * kStageBytes;  // 163840: [2][128 keys][64 queries]
+constexpr int kOffDQ = kOffDS + 2 * kBoxK;                // fp32 [64][128]
 constexpr int kOffLse = kOffDQ + kQT * kD * 4;          // [stage] {lse2[64], D[64]}
 constexpr int kOffBar = kOffLse + kStages * 512;
 constexpr int kSmemBytes = kOffBar + 512 + 1024;        // 232448: the per-block limit
 
 enum {
   B_KV = 0, B_QFULL, B_QEMPTY = B_QFULL + kStages, B_SFULL = B_QEMPTY + kStages, B_PFULL = B_SFULL + 2,
-  B_DQFULL, B_DQFREE = B_DQFULL + 2, B_PBFREE = B_DQFREE + 2, B_STG, B_STGFREE, B_ACC, B_COUNT
+  B_DQFULL = B_PFULL + 2, B_DQFREE = B_DQFULL + 2, B_DSFREE = B_DQFREE + 2, B_STG = B_DSFREE + 2, B_STGFREE, B_ACC,
+  B_COUNT
 };
 static_assert(B_COUNT * 8 <= 256, "barrier area");
 
@@ -84,7 +88,7 @@ __host__ __device__ constexpr uint32_t idesc2(int M, int N, int a_mn, int b_mn) 
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 constexpr uint32_t kIdS = idesc2(128, 64, 0, 0);    // K (K-major) x Q (K-major); V x dO
-constexpr uint32_t kIdAcc = idesc2(128, 128, 0, 1); // P^T / dS^T (K-major) x dO / Q (MN-major)
+constexpr uint32_t kIdAcc = idesc2(128, 128, 0, 1); // P^T / dS^T (TMEM) x dO / Q (MN-major)
 constexpr uint32_t kIdDQ = idesc2(128, 64, 1, 1);   // K^T (MN-major) x dS^T (MN-major)
 
 __device__ __forceinline__ uint64_t globaltimer() {
@@ -299,9 +303,9 @@ v2_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       mbar_init(sh.bar(B_SFULL + b), 1);
       mbar_init(sh.bar(B_DQFULL + b), 1);
       mbar_init(sh.bar(B_DQFREE + b), 128);
+      mbar_init(sh.bar(B_DSFREE + b), 1);
+      mbar_init(sh.bar(B_PFULL + b), 128);
     }
-    mbar_init(sh.bar(B_PFULL), 128);
-    mbar_init(sh.bar(B_PBFREE), 1);
     mbar_init(sh.bar(B_STG), 128);
     mbar_init(sh.bar(B_STGFREE), 1);
     mbar_init(sh.bar(B_ACC), 1);
@@ -384,7 +388,7 @@ v2_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       bool ok = wait_bar(sh, sh.bar(B_KV), 0, a.status, 0x6101);
       tc_fence_after();
       const uint32_t kA = sh.base + kOffK, vA = sh.base + kOffV;
-      const uint32_t pA = sh.base + kOffP, dsA = sh.base + kOffDS;
+      auto dsA = [&](int b) { return sh.base + kOffDS + b * kBoxK; };
       auto stage = [&](int k) { return sh.base + kOffStage + (k % kStages) * kStageBytes; };
       auto issue_sdp = [&](int k) {  // S^T = K Q^T and dP^T = V dO^T into buffers k & 1
         const uint32_t qb = stage(k) + kStageQ, db = stage(k) + kStageDO;
@@ -429,7 +433,7 @@ v2_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
           tc_fence_after();
           issue_sdp(k1);
         }
-        if (!wait_bar(sh, sh.bar(B_PFULL), k & 1, a.status, 0x6105)) {
+        if (!wait_bar(sh, sh.bar(B_PFULL + b), (k >> 1) & 1, a.status, 0x6105)) {
           ok = false;
           break;
         }
@@ -437,20 +441,21 @@ v2_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         // dQ^T = K^T dS^T  (into the dP^T buffer of this tile, already read)
 #pragma unroll
         for (int kk = 0; kk < kKT / 16; ++kk)
-          tc_mma_ss(t_d(b), sdesc_sw128(kA + kk * 2048, kBoxK, 1024), sdesc_sw128(dsA + kk * 2048, kBoxQ, 1024),
+          tc_mma_ss(t_d(b), sdesc_sw128(kA + kk * 2048, kBoxK, 1024), sdesc_sw128(dsA(b) + kk * 2048, kBoxQ, 1024),
                     kIdDQ, kk > 0);
         tc_commit(sh.bar(B_DQFULL + b));
-        // dV += P^T dO ; dK += dS^T Q
+        tc_commit(sh.bar(B_DSFREE + b));
+        // dV += P^T dO ; dK += dS^T Q  (P^T in columns 0-31 of the S^T
+        // buffer, dS^T in columns 32-63)
         const uint32_t db = stage(k) + kStageDO, qb = stage(k) + kStageQ;
 #pragma unroll
         for (int kk = 0; kk < kQT / 16; ++kk)
-          tc_mma_ss(T_DV, sdesc_sw128(pA + kk * 32, 16, 1024), sdesc_sw128(db + kk * 2048, kBoxQ, 1024), kIdAcc,
+          tc_mma_ts(T_DV, t_s(b) + kk * 8, sdesc_sw128(db + kk * 2048, kBoxQ, 1024), kIdAcc,
                     (k > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < kQT / 16; ++kk)
-          tc_mma_ss(T_DK, sdesc_sw128(dsA + kk * 32, 16, 1024), sdesc_sw128(qb + kk * 2048, kBoxQ, 1024), kIdAcc,
+          tc_mma_ts(T_DK, t_s(b) + 32 + kk * 8, sdesc_sw128(qb + kk * 2048, kBoxQ, 1024), kIdAcc,
                     (k > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(sh.bar(B_PBFREE));
         tc_commit(sh.bar(B_QEMPTY + k % kStages));
       }
       if (ok) tc_commit(sh.bar(B_ACC));
@@ -463,8 +468,6 @@ v2_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     const uint64_t sl2x2 = f2(sl2, sl2), sc2 = f2(a.scale, a.scale);
     const int key = it.kt * kKT + r;
     bool ok = true;
-    uint8_t* pbuf = sh.gen + kOffP;
-    uint8_t* dsbuf = sh.gen + kOffDS;
     for (int k = 0; k < it.n_it && ok; ++k) {
       const int b = k & 1;
       const int q0 = q0_of(k);
@@ -476,6 +479,8 @@ v2_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       const float4* l2v = reinterpret_cast<const float4*>(sh.gen + kOffLse + (k % kStages) * 512);
       const float4* ddv = l2v + 16;
       const bool diag = q0 < it.kt * kKT + kKT;  // a query of this tile may precede a key
+      uint8_t* dsbuf = sh.gen + kOffDS + b * kBoxK;
+      uint32_t dkeep[16];  // dS^T of the first half, stored to TMEM once the second half's S^T is read
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
         uint32_t sv[32], dp[32];
@@ -516,9 +521,10 @@ v2_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         };
         if (diag) half(std::true_type{});
         else half(std::false_type{});
-        // the P / dS buffers are free once dQ, dV and dK of the previous
-        // tile have read them
-        if (hf == 0 && k > 0 && !wait_bar(sh, sh.bar(B_PBFREE), (k - 1) & 1, a.status, 0x6202)) {
+        // P^T over S^T columns this thread has already read
+        tmem_st16(t_s(b) + loff + hf * 16, pw);
+        // the dS^T buffer is free once dQ of the tile two back has read it
+        if (hf == 0 && k > 1 && !wait_bar(sh, sh.bar(B_DSFREE + b), ((k >> 1) - 1) & 1, a.status, 0x6202)) {
           ok = false;
           break;
         }
@@ -526,14 +532,23 @@ v2_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         for (int cc = 0; cc < 4; ++cc) {
           const int ch = hf * 4 + cc;
           const int off = r * 128 + ((ch ^ (r & 7)) << 4);
-          *reinterpret_cast<uint4*>(pbuf + off) = make_uint4(pw[cc * 4], pw[cc * 4 + 1], pw[cc * 4 + 2], pw[cc * 4 + 3]);
           *reinterpret_cast<uint4*>(dsbuf + off) = make_uint4(dw[cc * 4], dw[cc * 4 + 1], dw[cc * 4 + 2], dw[cc * 4 + 3]);
+        }
+        if (hf == 0) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) dkeep[e] = dw[e];
+        } else {
+          tmem_st16(t_s(b) + loff + 32, dkeep);
+          tmem_st16(t_s(b) + loff + 48, dw);
         }
       }
       if (!ok) break;
+      tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
-      mbar_arrive(sh.bar(B_PFULL));
+      // one barrier per S^T buffer: this warpgroup can run two tiles ahead
+      // of the MMA issuer's wait, never two uses of one buffer
+      mbar_arrive(sh.bar(B_PFULL + b));
     }
     // ------------------------------------------------------- dK epilogue --
     if (ok && wait_bar(sh, sh.bar(B_ACC), 0, a.status, 0x6203)) {
