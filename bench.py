@@ -158,6 +158,7 @@ class V1FwdBwd(V1Fwd):
     name = "v1_fwd_bwd"
     desc = "V1 DiffAttn fwd+bwd bf16 B1 H16 N8192 d_qk128 d_v256 causal, layer 1"
     B, N, H, dqk, dv, layer = 1, 8192, 16, 128, 256, 1
+    deterministic = False
 
     def work(self):
         return v1_fwd_flops(self.B, self.N, self.H, self.dqk, self.dv) + \
@@ -175,8 +176,9 @@ class V1FwdBwd(V1Fwd):
         _, self.saves = bd.diffattn_v1_fwd(*self.args(self.t), self.li, out=self.out, save=True,
                                            workspace=self.fws)
         self.grads = bd.diffattn_v1_bwd(*self.args(self.t), self.li, self.out, self.t["dy"],
-                                        self.saves)
-        need = bd.load().diffattn_v1_bwd_workspace_size(self.B, self.N, self.H, self.dqk, self.dv)
+                                        self.saves, deterministic=self.deterministic)
+        need = bd.load().diffattn_v1_bwd_workspace_size(self.B, self.N, self.H, self.dqk, self.dv,
+                                                        int(self.deterministic))
         self.ws = torch.empty((max(need, 1),), dtype=torch.uint8, device=dev)
         self.launches = None
 
@@ -184,11 +186,13 @@ class V1FwdBwd(V1Fwd):
         self.bd.diffattn_v1_fwd(*self.args(self.t), self.li, out=self.out, save=True,
                                 saves=self.saves, workspace=self.fws)
         self.bd.diffattn_v1_bwd(*self.args(self.t), self.li, self.out, self.t["dy"], self.saves,
-                                grads=self.grads, workspace=self.ws)
+                                grads=self.grads, workspace=self.ws,
+                                deterministic=self.deterministic)
 
     def run_dominant(self):
         self.bd.diffattn_v1_bwd(*self.args(self.t), self.li, self.out, self.t["dy"], self.saves,
-                                grads=self.grads, workspace=self.ws)
+                                grads=self.grads, workspace=self.ws,
+                                deterministic=self.deterministic)
 
     def dominant_work(self):
         return v1_bwd_flops(self.B, self.N, self.H, self.dqk, self.dv)
@@ -206,9 +210,17 @@ class V1FwdBwd(V1Fwd):
         self.bd.diffattn_v1_fwd(*self.args(d), self.li, out=self.out, save=True, saves=self.saves,
                                 workspace=self.fws)
         self.bd.diffattn_v1_bwd(*self.args(d), self.li, self.out, d["dy"], self.saves,
-                                grads=self.grads, workspace=self.ws)
+                                grads=self.grads, workspace=self.ws,
+                                deterministic=self.deterministic)
         for k, v in self.grads.items():
             self.host_g[k].copy_(v, non_blocking=True)
+
+
+class V1FwdBwdDet(V1FwdBwd):
+    name = "v1_fwd_bwd_det"
+    desc = ("V1 DiffAttn fwd+bwd bf16 B1 H16 N8192 d_qk128 d_v256 causal, layer 1, "
+            "deterministic dQ (bitwise reproducible)")
+    deterministic = True
 
 
 class V1FwdF32(V1Fwd):
@@ -409,7 +421,7 @@ class V2FwdBwdSmall(V2FwdBwd):
     B, N = 1, 4096
 
 
-WORKLOADS = {w.name: w for w in (V1Fwd, V1FwdF32, V2Fwd, V2Decode, V1FwdBwd, V2FwdBwd)}
+WORKLOADS = {w.name: w for w in (V1Fwd, V1FwdF32, V2Fwd, V2Decode, V1FwdBwd, V1FwdBwdDet, V2FwdBwd)}
 PROFILE_ONLY = {V2DecodeSmall.name: V2DecodeSmall, V2FwdBwdSmall.name: V2FwdBwdSmall}
 
 # ----------------------------------------------------------------- helpers --
@@ -418,6 +430,7 @@ PROFILE_ONLY = {V2DecodeSmall.name: V2DecodeSmall, V2FwdBwdSmall.name: V2FwdBwdS
 KERNEL_SOURCES = {
     "v1_fwd": ("v1_fwd.cu", "softmax.cuh", "tma.cuh", "common.cuh"),
     "v1_fwd_bwd": ("v1_bwd.cu", "softmax.cuh", "tma.cuh", "common.cuh"),
+    "v1_fwd_bwd_det": ("v1_bwd.cu", "softmax.cuh", "tma.cuh", "common.cuh"),
     "v2_fwd": ("v2_fwd.cu", "softmax.cuh", "tma.cuh", "common.cuh"),
     "v2_decode": ("decode.cu", "common.cuh"),
     "v2_fwd_bwd": ("v2_bwd.cu", "softmax.cuh", "tma.cuh", "common.cuh"),

@@ -81,7 +81,7 @@ class da_v1_bwd_params(C.Structure):
                 ("lse1", C.c_void_p), ("lse2", C.c_void_p), ("rstd", C.c_void_p), ("o2", da_t4),
                 ("dq1", da_t4), ("dq2", da_t4), ("dk1", da_t4), ("dk2", da_t4), ("dv", da_t4),
                 ("dlq1", C.c_void_p), ("dlk1", C.c_void_p), ("dlq2", C.c_void_p), ("dlk2", C.c_void_p),
-                ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t)]
+                ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t), ("deterministic", C.c_int)]
 
 
 class da_v2_gate_params(C.Structure):
@@ -147,7 +147,7 @@ def load(path: str = LIB_PATH):
         lib.diffattn_v1_fwd_workspace_size.restype = C.c_size_t
         lib.diffattn_v1_fwd_workspace_size.argtypes = [C.c_int] * 6
         lib.diffattn_v1_bwd_workspace_size.restype = C.c_size_t
-        lib.diffattn_v1_bwd_workspace_size.argtypes = [C.c_int] * 5
+        lib.diffattn_v1_bwd_workspace_size.argtypes = [C.c_int] * 6
         lib.diffattn_v2_fwd_workspace_size.restype = C.c_size_t
         lib.diffattn_v2_fwd_workspace_size.argtypes = [C.c_int] * 4
         lib.diffattn_v2_bwd_workspace_size.restype = C.c_size_t
@@ -241,8 +241,9 @@ def diffattn_v1_fwd(q1, q2, k1, k2, v, lq1, lk1, lq2, lk2, lambda_init, *, out=N
 
 def diffattn_v1_bwd(q1, q2, k1, k2, v, lq1, lk1, lq2, lk2, lambda_init, out, dout, saves, *,
                     causal=True, softmax_scale=0.0, rms_eps=1e-5, grads=None, workspace=None,
-                    stream=None):
-    """V1 backward.  Returns dict(dq1, dq2, dk1, dk2, dv, dlq1, dlk1, dlq2, dlk2)."""
+                    deterministic=False, stream=None):
+    """V1 backward.  Returns dict(dq1, dq2, dk1, dk2, dv, dlq1, dlk1, dlq2, dlk2).
+    deterministic=True makes dQ (and so every output) bitwise reproducible."""
     lib = load()
     B, N, H, dqk = q1.shape
     dv = v.shape[-1]
@@ -250,7 +251,7 @@ def diffattn_v1_bwd(q1, q2, k1, k2, v, lq1, lk1, lq2, lk2, lambda_init, out, dou
         grads = {n: torch.empty_like(t) for n, t in
                  (("dq1", q1), ("dq2", q2), ("dk1", k1), ("dk2", k2), ("dv", v),
                   ("dlq1", lq1), ("dlk1", lk1), ("dlq2", lq2), ("dlk2", lk2))}
-    need = lib.diffattn_v1_bwd_workspace_size(B, N, H, dqk, dv)
+    need = lib.diffattn_v1_bwd_workspace_size(B, N, H, dqk, dv, int(bool(deterministic)))
     if workspace is None:
         workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=v.device)
     p = da_v1_bwd_params(
@@ -260,7 +261,7 @@ def diffattn_v1_bwd(q1, q2, k1, k2, v, lq1, lk1, lq2, lk2, lambda_init, out, dou
         _ptr(saves["rstd"]), _t4(saves["o2"]), _t4(grads["dq1"]), _t4(grads["dq2"]),
         _t4(grads["dk1"]), _t4(grads["dk2"]), _t4(grads["dv"]), _ptr(grads["dlq1"]),
         _ptr(grads["dlk1"]), _ptr(grads["dlq2"]), _ptr(grads["dlk2"]), workspace.data_ptr(),
-        workspace.numel() * workspace.element_size())
+        workspace.numel() * workspace.element_size(), int(bool(deterministic)))
     _check(lib.diffattn_v1_bwd(C.byref(p), _stream(stream)), "diffattn_v1_bwd")
     return grads
 

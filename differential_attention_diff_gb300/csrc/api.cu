@@ -241,9 +241,9 @@ da_status diffattn_v1_fwd(const da_v1_fwd_params* p, void* stream) {
 }
 
 // ----------------------------------------------------------- V1 bwd --------
-size_t diffattn_v1_bwd_workspace_size(int B, int N, int H, int d_qk, int d_v) {
+size_t diffattn_v1_bwd_workspace_size(int B, int N, int H, int d_qk, int d_v, int deterministic) {
   if (B <= 0 || N <= 0 || H <= 0) return 0;
-  return da::v1_bwd_workspace_bytes(B, N, H, d_qk, d_v);
+  return da::v1_bwd_workspace_bytes(B, N, H, d_qk, d_v, deterministic != 0);
 }
 
 da_status diffattn_v1_bwd(const da_v1_bwd_params* p, void* stream) {
@@ -259,7 +259,7 @@ da_status diffattn_v1_bwd(const da_v1_bwd_params* p, void* stream) {
                          &p->dq1, &p->dq2, &p->dk1, &p->dk2, &p->dv})
     if (check_t4(*t, p->dtype) != DA_OK) return DA_ERR_INVALID_ARG;
   if (!p->lse1 || !p->lse2 || !p->rstd) return DA_ERR_INVALID_ARG;
-  const size_t need = da::v1_bwd_workspace_bytes(p->B, p->N, p->H, p->d_qk, p->d_v);
+  const size_t need = da::v1_bwd_workspace_bytes(p->B, p->N, p->H, p->d_qk, p->d_v, p->deterministic != 0);
   if (p->workspace == nullptr || p->workspace_bytes < need || !aligned(p->workspace, 256))
     return DA_ERR_WORKSPACE;
   DevInfo d = device_info();
@@ -270,7 +270,7 @@ da_status diffattn_v1_bwd(const da_v1_bwd_params* p, void* stream) {
                   p->rms_eps, p->q1, p->q2, p->k1, p->k2, p->v, p->out, p->dout, p->o2,
                   p->lq1, p->lk1, p->lq2, p->lk2, p->lse1, p->lse2, p->rstd,
                   p->dq1, p->dq2, p->dk1, p->dk2, p->dv, p->dlq1, p->dlk1, p->dlq2, p->dlk2,
-                  p->workspace, p->workspace_bytes, d.status, d.num_sms};
+                  p->workspace, p->workspace_bytes, d.status, d.num_sms, p->deterministic != 0};
   return cuda_status(da::launch_v1_bwd(a, static_cast<cudaStream_t>(stream)));
 }
 

@@ -106,8 +106,9 @@ struct V1BwdArgs {
   size_t workspace_bytes;
   uint32_t* status;
   int num_sms;
+  int deterministic;  // dQ through per-key-tile slots summed in a fixed order
 };
-size_t v1_bwd_workspace_bytes(int B, int N, int H, int d_qk, int d_v);
+size_t v1_bwd_workspace_bytes(int B, int N, int H, int d_qk, int d_v, int deterministic);
 cudaError_t launch_v1_bwd(const V1BwdArgs& a, cudaStream_t s);
 
 // TMA descriptor encoding (driver entry point fetched through the runtime).

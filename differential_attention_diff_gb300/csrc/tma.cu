@@ -63,4 +63,18 @@ bool encode_tmap_f32_4d(CUtensorMap* map, void* ptr, int B, int N, int H, int D,
   return r == CUDA_SUCCESS;
 }
 
+bool encode_tmap_f32_slots(CUtensorMap* map, void* ptr, int units, int slots, int rows, int D) {
+  if (!tma_available()) return false;
+  cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows),
+                        static_cast<cuuint64_t>(slots), static_cast<cuuint64_t>(units)};
+  cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 4, static_cast<cuuint64_t>(rows) * D * 4,
+                           static_cast<cuuint64_t>(slots) * rows * D * 4};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(D), static_cast<cuuint32_t>(rows), 1, 1};
+  cuuint32_t estr[4] = {1, 1, 1, 1};
+  CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ptr, dims, strides, box, estr,
+                        CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
+                        CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 }  // namespace da

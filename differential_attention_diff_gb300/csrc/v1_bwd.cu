@@ -35,6 +35,11 @@
 //     At the end each CTA writes its dK; the dV halves of the two streams are
 //     summed through distributed shared memory and written as bf16;
 //  3. finalize: dQ accumulators -> bf16, and the lambda-vector gradients.
+// Deterministic mode: the main kernel stores each dQ tile (TMA store) into a
+// slot of its own, (key tile, query tile) compacted to the causal tiles, and
+// the finalize sums a row's slots in ascending key-tile order instead of
+// reading an accumulator, so no result depends on the order in which CTAs
+// finish.
 //
 // TMEM: [0,256) dV, [256,384) dK, [384,448) S^T, [448,512) dP^T / dQ^T.
 // SMEM: K 32 KB, V 64 KB, 2 stages of (Q 16 KB, dO 32 KB), Psig^T and dS^T
@@ -168,18 +173,30 @@ struct BwdWs {
   __nv_bfloat16* dO;   // [B, N, H, 256]
   float* lse2[2];      // [B, H, Npad]  (LSE * log2 e; +inf in padding rows)
   float* D[2];         // [B, H, Npad]
-  float* dq[2];        // [B, N, H, 128] fp32 accumulators
+  float* dq[2];        // [B, N, H, 128] fp32 accumulators, or (deterministic)
+                       // [B*H, n_slots, 64, 128] per-tile slots
   float* dlam_part;    // [preprocess blocks]
   int npad, pre_blocks;
+  int det, n_kt, n_qt, n_slots;
 };
+
+// Slot of the dQ tile of (key tile kt, query tile qt), qt >= 2 kt: the causal
+// tiles of key tiles 0 .. kt-1 come first.
+__host__ __device__ __forceinline__ int dq_slot(int kt, int qt, int n_qt) {
+  return kt * n_qt - kt * (kt - 1) + (qt - 2 * kt);
+}
 
 size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
 
 constexpr int kPreWarps = 8;
 
-BwdWs carve(void* base, int B, int N, int H, size_t* total) {
+BwdWs carve(void* base, int B, int N, int H, bool det, size_t* total) {
   BwdWs w;
   w.npad = (N + kQT - 1) / kQT * kQT;
+  w.det = det ? 1 : 0;
+  w.n_kt = (N + kKT - 1) / kKT;
+  w.n_qt = w.npad / kQT;
+  w.n_slots = w.n_kt * w.n_qt - w.n_kt * (w.n_kt - 1);
   w.pre_blocks = static_cast<int>((static_cast<long long>(B) * H * w.npad + kPreWarps - 1) / kPreWarps);
   uint8_t* p = static_cast<uint8_t*>(base);
   size_t off = 0;
@@ -193,7 +210,8 @@ BwdWs carve(void* base, int B, int N, int H, size_t* total) {
   w.dO = reinterpret_cast<__nv_bfloat16*>(take(rows * kDv * 2));
   for (int t = 0; t < 2; ++t) w.lse2[t] = reinterpret_cast<float*>(take(srow * 4));
   for (int t = 0; t < 2; ++t) w.D[t] = reinterpret_cast<float*>(take(srow * 4));
-  for (int t = 0; t < 2; ++t) w.dq[t] = reinterpret_cast<float*>(take(rows * kDqk * 4));
+  const size_t dq_elems = det ? static_cast<size_t>(B) * H * w.n_slots * kQT * kDqk : rows * kDqk;
+  for (int t = 0; t < 2; ++t) w.dq[t] = reinterpret_cast<float*>(take(dq_elems * 4));
   w.dlam_part = reinterpret_cast<float*>(take(static_cast<size_t>(w.pre_blocks) * 4));
   if (total) *total = off;
   return w;
@@ -288,8 +306,10 @@ v1_bwd_pre_kernel(V1BwdArgs a, BwdWs w) {
       }
       const int64_t rrow = (static_cast<int64_t>(b) * a.N + n) * a.H + h;
       *reinterpret_cast<uint4*>(w.dO + rrow * kDv + lane * 8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
-      *reinterpret_cast<float4*>(w.dq[0] + rrow * kDqk + lane * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
-      *reinterpret_cast<float4*>(w.dq[1] + rrow * kDqk + lane * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+      if (!w.det) {
+        *reinterpret_cast<float4*>(w.dq[0] + rrow * kDqk + lane * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+        *reinterpret_cast<float4*>(w.dq[1] + rrow * kDqk + lane * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+      }
       if (lane == 0) {
         const int64_t pidx = static_cast<int64_t>(bh) * w.npad + n;
         w.D[0][pidx] = d1;
@@ -588,7 +608,10 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
       mbar_arrive(sh.bar(B_STG));
       if (r == 0) {
         if (!wait_bar(sh, sh.bar(B_STG), ph, a.status, 0x420A)) { ok = false; break; }
-        tma_reduce_add_4d(tdq, sh.base + kOffP, 0, it.h, q0, it.b);
+        if (w.det)
+          tma_store_4d(tdq, sh.base + kOffP, 0, 0, dq_slot(it.kt, it.i0 + k, w.n_qt), it.b * a.H + it.h);
+        else
+          tma_reduce_add_4d(tdq, sh.base + kOffP, 0, it.h, q0, it.b);
         bulk_commit();
         bulk_wait_read();
         mbar_arrive(sh.bar(B_STGFREE));
@@ -688,9 +711,26 @@ v1_bwd_finalize_kernel(V1BwdArgs a, BwdWs w) {
     const int n = static_cast<int>(bn % a.N), b = static_cast<int>(bn / a.N);
 #pragma unroll
     for (int t = 0; t < 2; ++t) {
-      const float* src = w.dq[t] + row * kDqk + c8;
-      const float4 x0 = *reinterpret_cast<const float4*>(src);
-      const float4 x1 = *reinterpret_cast<const float4*>(src + 4);
+      float4 x0, x1;
+      if (w.det) {
+        // the key tiles 0 .. qt / 2 that reach this query row, in that order
+        const int qt = n / kQT;
+        const float* base = w.dq[t] + (static_cast<int64_t>(b) * a.H + h) * w.n_slots * (kQT * kDqk) +
+                            (n % kQT) * kDqk + c8;
+        x0 = make_float4(0.f, 0.f, 0.f, 0.f);
+        x1 = x0;
+        for (int kt = 0; kt <= qt / 2; ++kt) {
+          const float* src = base + static_cast<int64_t>(dq_slot(kt, qt, w.n_qt)) * (kQT * kDqk);
+          const float4 y0 = *reinterpret_cast<const float4*>(src);
+          const float4 y1 = *reinterpret_cast<const float4*>(src + 4);
+          x0.x += y0.x; x0.y += y0.y; x0.z += y0.z; x0.w += y0.w;
+          x1.x += y1.x; x1.y += y1.y; x1.z += y1.z; x1.w += y1.w;
+        }
+      } else {
+        const float* src = w.dq[t] + row * kDqk + c8;
+        x0 = *reinterpret_cast<const float4*>(src);
+        x1 = *reinterpret_cast<const float4*>(src + 4);
+      }
       const da_t4& o = t == 0 ? a.dq1 : a.dq2;
       __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(o.ptr) + b * o.sb + static_cast<int64_t>(n) * o.sn +
                            h * o.sh + c8;
@@ -730,17 +770,17 @@ v1_bwd_finalize_kernel(V1BwdArgs a, BwdWs w) {
 
 }  // namespace
 
-size_t v1_bwd_workspace_bytes(int B, int N, int H, int d_qk, int d_v) {
+size_t v1_bwd_workspace_bytes(int B, int N, int H, int d_qk, int d_v, int deterministic) {
   (void)d_qk;
   (void)d_v;
   size_t total = 0;
-  carve(nullptr, B, N, H, &total);
+  carve(nullptr, B, N, H, deterministic != 0, &total);
   return total;
 }
 
 cudaError_t launch_v1_bwd(const V1BwdArgs& a, cudaStream_t s) {
   size_t total = 0;
-  BwdWs w = carve(a.workspace, a.B, a.N, a.H, &total);
+  BwdWs w = carve(a.workspace, a.B, a.N, a.H, a.deterministic != 0, &total);
   if (total > a.workspace_bytes) return cudaErrorInvalidValue;
 
   v1_bwd_pre_kernel<<<w.pre_blocks, kPreWarps * 32, 0, s>>>(a, w);
@@ -773,9 +813,14 @@ cudaError_t launch_v1_bwd(const V1BwdArgs& a, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   CUtensorMap tdq1, tdq2;
-  if (!encode_tmap_f32_4d(&tdq1, w.dq[0], a.B, a.N, a.H, kDqk, kQT) ||
-      !encode_tmap_f32_4d(&tdq2, w.dq[1], a.B, a.N, a.H, kDqk, kQT))
+  if (w.det) {
+    if (!encode_tmap_f32_slots(&tdq1, w.dq[0], a.B * a.H, w.n_slots, kQT, kDqk) ||
+        !encode_tmap_f32_slots(&tdq2, w.dq[1], a.B * a.H, w.n_slots, kQT, kDqk))
+      return cudaErrorInvalidValue;
+  } else if (!encode_tmap_f32_4d(&tdq1, w.dq[0], a.B, a.N, a.H, kDqk, kQT) ||
+             !encode_tmap_f32_4d(&tdq2, w.dq[1], a.B, a.N, a.H, kDqk, kQT)) {
     return cudaErrorInvalidValue;
+  }
   e = cudaLaunchKernelEx(&cfg, v1_bwd_main_kernel, tq1, tq2, tk1, tk2, tv, tdo, tdq1, tdq2, a, w);
   if (e != cudaSuccess) return e;
 

@@ -120,8 +120,15 @@ da_status diffattn_v1_fwd(const da_v1_fwd_params* p, void* cuda_stream);
  * saves lse1, lse2, rstd, o2 written by diffattn_v1_fwd.  Outputs: dq1, dq2,
  * dk1, dk2 [B,N,H,d_qk], dv [B,N,H,d_v] (dtype), dlq1, dlk1, dlq2, dlk2 fp32
  * [d_qk] (overwritten).  Supported: DA_BF16, d_qk = 128, d_v = 256, causal.
- * workspace: at least diffattn_v1_bwd_workspace_size(...) bytes, 256-byte
- * aligned; its contents on entry do not matter. */
+ * workspace: at least diffattn_v1_bwd_workspace_size(..., deterministic)
+ * bytes, 256-byte aligned; its contents on entry do not matter.
+ * deterministic = 0: each key tile adds its dQ tile into an fp32 accumulator
+ * (TMA reduce-add), so dQ1 / dQ2 may differ in the last bits between runs;
+ * every other output is reproducible.  deterministic != 0: each key tile
+ * stores its dQ tile into its own slot of the workspace and the finalize sums
+ * the slots in ascending key-tile order, so every output is bitwise
+ * reproducible; the workspace grows by about B*H*N^2/64 * 4 bytes per stream
+ * (causal tiles only) and the call takes longer. */
 typedef struct {
   int B, N, H, d_qk, d_v;
   da_dtype dtype;
@@ -138,9 +145,10 @@ typedef struct {
   float *dlq1, *dlk1, *dlq2, *dlk2;
   void* workspace;
   size_t workspace_bytes;
+  int deterministic;
 } da_v1_bwd_params;
 
-size_t diffattn_v1_bwd_workspace_size(int B, int N, int H, int d_qk, int d_v);
+size_t diffattn_v1_bwd_workspace_size(int B, int N, int H, int d_qk, int d_v, int deterministic);
 da_status diffattn_v1_bwd(const da_v1_bwd_params* p, void* cuda_stream);
 
 /* ------------------------------------------------------------------------ */

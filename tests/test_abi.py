@@ -128,5 +128,12 @@ def test_gate_argument_checks(lib):
 
 
 def test_bwd_workspace_size(lib):
-    assert lib.diffattn_v1_bwd_workspace_size(1, 8192, 16, 128, 256) > 0
-    assert lib.diffattn_v1_bwd_workspace_size(0, 8192, 16, 128, 256) == 0
+    base = lib.diffattn_v1_bwd_workspace_size(1, 8192, 16, 128, 256, 0)
+    det = lib.diffattn_v1_bwd_workspace_size(1, 8192, 16, 128, 256, 1)
+    assert base > 0 and lib.diffattn_v1_bwd_workspace_size(0, 8192, 16, 128, 256, 0) == 0
+    # deterministic mode: one fp32 [64, 128] slot per causal (key tile, query
+    # tile) pair and stream replaces the [N, 128] accumulators
+    n_kt, n_qt = 8192 // 128, 8192 // 64
+    slots = n_kt * n_qt - n_kt * (n_kt - 1)
+    assert det - base == 2 * 16 * (slots * 64 - 8192) * 128 * 4
+    assert lib.diffattn_v2_bwd_workspace_size(2, 8192, 32, 4096) > lib.diffattn_v2_bwd_workspace_size(2, 8192, 32, 0)

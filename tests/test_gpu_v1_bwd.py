@@ -11,7 +11,9 @@ reaches 11 % of RMS on dV).  So, per gradient tensor:
   k = 2 for the backward alone (fed the oracle's forward saves) and k = 3 for
   the training step (GPU forward, then GPU backward on its saves: the
   forward's own bf16 error enters too);
-* ||GPU - oracle|| / ||oracle|| <= 1.5e-2 (2e-2 for the step);
+* ||GPU - oracle|| <= max(1.5e-2 ||oracle||, k ||model - oracle||) (2e-2 for
+  the step): the second term only matters where a gradient vanishes
+  analytically and rounding noise is all that is left;
 * dlambda (the lambda-vector gradients are dlambda times fixed vectors)
   within k * the model's error + 2e-3 relative.
 floor = 1e-3 * RMS(oracle dV) covers gradients that vanish analytically
@@ -76,8 +78,12 @@ def _compare(g, ref, model, heads=None, lam_vectors=True, bar="bwd"):
         rms = float(np.sqrt(np.mean(exp ** 2)))
         allowed = k * float(np.max(np.abs(mod - exp))) + 1e-3 * rms + floor
         worst[n] = float(np.max(np.abs(got - exp))) / allowed
+        # relative Frobenius bar, or k times the rounding model's own error
+        # where the gradient vanishes analytically (N = 1) and only rounding
+        # noise is left
         worst[n + "_fro"] = float(np.linalg.norm(got - exp)) / (
-            fro * float(np.linalg.norm(exp)) + floor * np.sqrt(exp.size))
+            max(fro * float(np.linalg.norm(exp)), k * float(np.linalg.norm(mod - exp)))
+            + floor * np.sqrt(exp.size))
     if lam_vectors:
         dlam_err = abs(model["dlam"] - ref["dlam"]) / max(abs(ref["dlam"]), 1e-30)
         for n in ("dlq1", "dlk1", "dlq2", "dlk2"):
@@ -139,3 +145,40 @@ def test_v1_bwd_full_size_b1_h16_n8192_one_head():
     ref = orc.v1_backward(*(f64(th[n]) for n in NAMES), li, f64(th["dy"]))
     model = _model(th, li)
     _compare(g, ref, model, heads=slice(h, h + 1), lam_vectors=False, bar="step")
+
+
+@pytest.mark.parametrize("B,N,H,layer", [(1, 300, 2, 2), (2, 129, 1, 14), (1, 1, 1, 1)])
+def test_v1_bwd_deterministic_mode(B, N, H, layer):
+    """deterministic=True: dQ from per-key-tile slots summed in a fixed order.
+    Same bars as the default mode, and bitwise equal results on a rerun."""
+    t = synth.v1_inputs(B, N, H, 128, 256, "bf16", seed=5100 + N + H, device="cuda", with_dy=True)
+    li = float(np.float32(bd.diffattn_lambda_init(layer)))
+    ref = orc.v1_backward(*(f64(t[n]) for n in NAMES), li, f64(t["dy"]))
+    model = _model(t, li)
+    y, sv = bd.diffattn_v1_fwd(*(t[n] for n in NAMES), li, save=True)
+    g1 = bd.diffattn_v1_bwd(*(t[n] for n in NAMES), li, y, t["dy"], sv, deterministic=True)
+    g2 = bd.diffattn_v1_bwd(*(t[n] for n in NAMES), li, y, t["dy"], sv, deterministic=True)
+    torch.cuda.synchronize()
+    for n in g1:
+        assert torch.equal(g1[n], g2[n]), n
+    _compare(g1, ref, model, bar="step")
+
+
+def test_v1_bwd_deterministic_full_size_repeat():
+    """B1 H16 N8192: two deterministic backward runs agree bit for bit, and
+    agree with the default (reduce-add) mode to within bf16 rounding."""
+    t = synth.v1_inputs(1, 8192, 16, 128, 256, "bf16", seed=1005, device="cuda", with_dy=True)
+    li = bd.diffattn_lambda_init(1)
+    y, sv = bd.diffattn_v1_fwd(*(t[n] for n in NAMES), li, save=True)
+    g1 = bd.diffattn_v1_bwd(*(t[n] for n in NAMES), li, y, t["dy"], sv, deterministic=True)
+    g2 = bd.diffattn_v1_bwd(*(t[n] for n in NAMES), li, y, t["dy"], sv, deterministic=True)
+    g3 = bd.diffattn_v1_bwd(*(t[n] for n in NAMES), li, y, t["dy"], sv)
+    torch.cuda.synchronize()
+    for n in g1:
+        assert torch.equal(g1[n], g2[n]), n
+    for n in ("dq1", "dq2"):
+        a, b = g1[n].float(), g3[n].float()
+        rms = float(a.pow(2).mean().sqrt())
+        assert float((a - b).abs().max()) <= 2e-2 * rms, n
+    for n in ("dk1", "dk2", "dv"):
+        assert torch.equal(g1[n], g3[n]), n

@@ -9,7 +9,9 @@ precision alone causes on the same inputs.  Per gradient tensor:
 * max|GPU - oracle| <= k * max|model - oracle| + 1e-3 * RMS(oracle) + floor,
   k = 2 for the backward alone (fed the oracle's forward saves), 3 for the
   training step (GPU forward with saves, then the GPU backward);
-* ||GPU - oracle|| / ||oracle|| <= 1.5e-2 (2e-2 for the step);
+* ||GPU - oracle|| <= max(1.5e-2 ||oracle||, k ||model - oracle||) (2e-2 for
+  the step): the second term only matters where a gradient vanishes
+  analytically and rounding noise is all that is left;
 floor = 1e-3 * RMS(oracle dV) for dQ / dK / dV and 1e-3 * RMS of the tensor
 itself for the gate gradients (dQ and dK vanish analytically at N = 1).
 """
@@ -79,8 +81,12 @@ def _compare(g, ref, model, names=ATTN + GATE, bar="bwd", sl=None):
         floor = floor_attn if n in ATTN else 1e-3 * rms
         allowed = k * float(np.max(np.abs(mod - exp))) + 1e-3 * rms + floor
         worst[n] = float(np.max(np.abs(got - exp))) / allowed
+        # relative Frobenius bar, or k times the rounding model's own error
+        # where the gradient vanishes analytically (N = 1) and only rounding
+        # noise is left
         worst[n + "_fro"] = float(np.linalg.norm(got - exp)) / (
-            fro * float(np.linalg.norm(exp)) + floor * np.sqrt(exp.size))
+            max(fro * float(np.linalg.norm(exp)), k * float(np.linalg.norm(mod - exp)))
+            + floor * np.sqrt(exp.size))
     assert max(worst.values()) <= 1.0, worst
 
 
