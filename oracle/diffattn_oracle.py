@@ -36,7 +36,8 @@ even head 2p minus gate times odd head 2p+1, contiguous GQA groups
 
 Parity pins: every function here is pinned by ``tests/test_oracle.py``
 (closed forms, library SDPA special cases, Hadamard-exact RMS bounds, finite
-differences for the backward, decode == last causal row).  None is unpinned.
+differences for the backward, decode == last causal row for V1 and V2).  None
+is unpinned.
 
 Layouts: Q/K/V are ``[B, N, H, D]`` float64 arrays (the exact bf16 / fp32
 values the GPU reads, widened); per-row statistics are ``[B, H, N]``.
@@ -56,6 +57,7 @@ __all__ = [
     "v2_forward",
     "v2_decode",
     "v2_backward",
+    "v1_decode",
 ]
 
 
@@ -336,3 +338,43 @@ def v2_decode(q, k_cache, v_cache, seqlens, gate, *, scale: float | None = None)
             lse[b, j] = l[0]
     out = o[:, 0::2] - gate[:, :, None] * o[:, 1::2]
     return dict(out=out, o=o, lse=lse)
+
+
+def v1_decode(q1, q2, k1_cache, k2_cache, v_cache, seqlens, lq1, lk1, lq2, lk2,
+              lam_init: float, *, scale: float | None = None, eps: float = 1e-5):
+    """V1 decode: one new token per sequence, the V1 operator of [P1]
+    "Differential Attention: 빼기의 힘" (two maps over two K caches, one shared
+    V cache) followed by the per-head RMSNorm and (1 - lambda_init) scale of
+    [P2] §1, for the query of the token at position seqlens[b] - 1 (its own
+    K1/K2/V rows are already in the caches).  [P1] "V2로의 진화" names LLM
+    decoding as the memory-bound case.
+
+    q1, q2: [B, H, d_qk]; k1_cache, k2_cache: [B, L_max, H, d_qk];
+    v_cache: [B, L_max, H, d_v]; seqlens: [B] ints.
+    Returns dict: y [B, H, d_v], o (pre-norm) [B, H, d_v], lse1, lse2 [B, H],
+    lam.
+    """
+    q1, q2, k1_cache, k2_cache, v_cache = (_f64(t) for t in (q1, q2, k1_cache, k2_cache, v_cache))
+    B, H, dqk = q1.shape
+    dv = v_cache.shape[-1]
+    if scale is None:
+        scale = 1.0 / np.sqrt(dqk)
+    lam = lambda_full(lq1, lk1, lq2, lk2, lam_init)
+    c = 1.0 - lam_init
+    y = np.zeros((B, H, dv))
+    o = np.zeros((B, H, dv))
+    lse1 = np.zeros((B, H))
+    lse2 = np.zeros((B, H))
+    for b in range(B):
+        L = int(seqlens[b])
+        for h in range(H):
+            a1, l1 = attention_maps(q1[b, h][None, :], k1_cache[b, :L, h], scale, causal=False)
+            a2, l2 = attention_maps(q2[b, h][None, :], k2_cache[b, :L, h], scale, causal=False)
+            o_bh = ((a1 - lam * a2) @ v_cache[b, :L, h])[0]
+            r = np.sqrt(np.mean(o_bh * o_bh) + eps)
+            y[b, h] = c * o_bh / r
+            o[b, h] = o_bh
+            lse1[b, h] = l1[0]
+            lse2[b, h] = l2[0]
+    return dict(y=y, o=o, lse1=lse1, lse2=lse2, lam=lam)
+

@@ -369,6 +369,24 @@ def test_decode_equals_last_causal_row():
     np.testing.assert_allclose(dec["lse"][0], full["lse"][0, :, 12], atol=1e-12)
 
 
+def test_v1_decode_equals_last_causal_row():
+    """V1 decode at position L-1 is the last row of the causal V1 forward
+    (both maps, the difference, the RMSNorm and the scale) on the same
+    tensors; ragged lengths truncate both K caches and the V cache."""
+    t = _v1_rand(B=2, N=11, H=2, dqk=4, dv=8, seed=25, lam_std=0.4)
+    li = 0.45
+    full = _v1(t, li)
+    seqlens = np.array([11, 4])
+    q1 = np.stack([t["q1"][0, 10], t["q1"][1, 3]])
+    q2 = np.stack([t["q2"][0, 10], t["q2"][1, 3]])
+    dec = orc.v1_decode(q1, q2, t["k1"], t["k2"], t["v"], seqlens, t["lq1"], t["lk1"], t["lq2"],
+                        t["lk2"], li)
+    np.testing.assert_allclose(dec["y"][0], full["y"][0, 10], atol=1e-12)
+    np.testing.assert_allclose(dec["y"][1], full["y"][1, 3], atol=1e-12)
+    np.testing.assert_allclose(dec["lse2"][1], full["lse2"][1, :, 3], atol=1e-12)
+    assert dec["lam"] == full["lam"]
+
+
 # -------------------------------------------------------------- backward ----
 
 def test_v1_backward_finite_differences():
