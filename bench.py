@@ -69,6 +69,10 @@ def decode_bytes(B, L, hkv, d):
     return 2.0 * B * L * hkv * d * 2
 
 
+def v1_decode_bytes(B, L, H, dqk, dv):
+    return B * L * H * (2.0 * dqk + dv) * 2
+
+
 class Workload:
     """One step of the path on its configuration."""
 
@@ -405,6 +409,44 @@ class V2Decode(Workload):
         return dt, decode_bytes(1, self.L, self.hkv, self.d), "sequence 0 of 64 (full cache)"
 
 
+class V1Decode(Workload):
+    name = "v1_decode"
+    desc = "V1 decode bf16 B64 cache 32768 16 heads d_qk128 d_v256 (K1, K2 and V caches), layer 1"
+    unit = "GB/s"
+    bound = "hbm"
+    launches = 2
+    B, L, H, dqk, dv, layer = 64, 32768, 16, 128, 256, 1
+
+    def work(self):
+        return v1_decode_bytes(self.B, self.L, self.H, self.dqk, self.dv)
+
+    def setup(self, dev):
+        from differential_attention_diff_gb300 import binding as bd, synth
+        self.bd = bd
+        self.t = synth.v1_decode_inputs(self.B, self.L, self.H, self.dqk, self.dv, seed=1006, device=dev)
+        self.li = bd.diffattn_lambda_init(self.layer)
+        self.out = torch.empty((self.B, self.H, self.dv), dtype=torch.bfloat16, device=dev)
+        need = bd.diffattn_v1_decode_workspace_size(self.B, self.H, self.dv, self.L)
+        self.ws = torch.empty((need,), dtype=torch.uint8, device=dev)
+
+    def run(self):
+        t = self.t
+        self.bd.diffattn_v1_decode(t["q1"], t["q2"], t["k1_cache"], t["k2_cache"], t["v_cache"],
+                                   t["lq1"], t["lk1"], t["lq2"], t["lk2"], self.li, out=self.out,
+                                   workspace=self.ws)
+
+    def oracle_sample(self, big=True):
+        from oracle import diffattn_oracle as orc
+        t = self.t
+        sl = lambda x: x[0:1].to("cpu", torch.float64).numpy()  # noqa: E731
+        lam = [t[n].to("cpu", torch.float64).numpy() for n in ("lq1", "lk1", "lq2", "lk2")]
+        t0 = time.perf_counter()
+        orc.v1_decode(sl(t["q1"]), sl(t["q2"]), sl(t["k1_cache"]), sl(t["k2_cache"]), sl(t["v_cache"]),
+                      [self.L], *lam, self.li)
+        dt = time.perf_counter() - t0
+        return dt, v1_decode_bytes(1, self.L, self.H, self.dqk, self.dv), "sequence 0 of 64 (full cache)"
+
+
 class V2DecodeSmall(V2Decode):
     """The decode kernel on a 1 GB cache (B8): big enough that DRAM figures
     mean something, small enough for a multi-pass ncu capture."""
@@ -421,7 +463,8 @@ class V2FwdBwdSmall(V2FwdBwd):
     B, N = 1, 4096
 
 
-WORKLOADS = {w.name: w for w in (V1Fwd, V1FwdF32, V2Fwd, V2Decode, V1FwdBwd, V1FwdBwdDet, V2FwdBwd)}
+WORKLOADS = {w.name: w for w in (V1Fwd, V1FwdF32, V2Fwd, V2Decode, V1FwdBwd, V1FwdBwdDet, V2FwdBwd,
+                                 V1Decode)}
 PROFILE_ONLY = {V2DecodeSmall.name: V2DecodeSmall, V2FwdBwdSmall.name: V2FwdBwdSmall}
 
 # ----------------------------------------------------------------- helpers --
@@ -434,6 +477,7 @@ KERNEL_SOURCES = {
     "v2_fwd": ("v2_fwd.cu", "softmax.cuh", "tma.cuh", "common.cuh"),
     "v2_decode": ("decode.cu", "common.cuh"),
     "v2_fwd_bwd": ("v2_bwd.cu", "softmax.cuh", "tma.cuh", "common.cuh"),
+    "v1_decode": ("v1_decode.cu", "common.cuh"),
 }
 
 

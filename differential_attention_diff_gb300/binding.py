@@ -32,6 +32,9 @@ EXPORTS = (
     "diffattn_v1_fwd_workspace_size",
     "diffattn_v1_bwd",
     "diffattn_v1_bwd_workspace_size",
+    "diffattn_v1_decode",
+    "diffattn_v1_decode_num_splits",
+    "diffattn_v1_decode_workspace_size",
     "diffattn_v2_bwd",
     "diffattn_v2_bwd_workspace_size",
     "diffattn_v2_gate",
@@ -82,6 +85,15 @@ class da_v1_bwd_params(C.Structure):
                 ("dq1", da_t4), ("dq2", da_t4), ("dk1", da_t4), ("dk2", da_t4), ("dv", da_t4),
                 ("dlq1", C.c_void_p), ("dlk1", C.c_void_p), ("dlq2", C.c_void_p), ("dlk2", C.c_void_p),
                 ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t), ("deterministic", C.c_int)]
+
+
+class da_v1_decode_params(C.Structure):
+    _fields_ = [("B", C.c_int), ("H", C.c_int), ("d_qk", C.c_int), ("d_v", C.c_int), ("L_max", C.c_int),
+                ("softmax_scale", C.c_float), ("lambda_init", C.c_float), ("rms_eps", C.c_float),
+                ("q1", C.c_void_p), ("q2", C.c_void_p), ("k1_cache", da_t4), ("k2_cache", da_t4),
+                ("v_cache", da_t4), ("seqlens", C.c_void_p), ("lq1", C.c_void_p), ("lk1", C.c_void_p),
+                ("lq2", C.c_void_p), ("lk2", C.c_void_p), ("out", C.c_void_p), ("num_splits", C.c_int),
+                ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t)]
 
 
 class da_v2_gate_params(C.Structure):
@@ -138,7 +150,7 @@ def load(path: str = LIB_PATH):
         lib.diffattn_status_string.argtypes = [C.c_int]
         for name, st in (("diffattn_v1_fwd", da_v1_fwd_params), ("diffattn_v1_bwd", da_v1_bwd_params),
                          ("diffattn_v2_gate", da_v2_gate_params), ("diffattn_v2_fwd", da_v2_fwd_params),
-                         ("diffattn_v2_bwd", da_v2_bwd_params),
+                         ("diffattn_v2_bwd", da_v2_bwd_params), ("diffattn_v1_decode", da_v1_decode_params),
                          ("diffattn_v2_decode", da_v2_decode_params),
                          ("diffattn_v2_decode_noalloc", da_v2_decode_params)):
             f = getattr(lib, name)
@@ -150,6 +162,10 @@ def load(path: str = LIB_PATH):
         lib.diffattn_v1_bwd_workspace_size.argtypes = [C.c_int] * 6
         lib.diffattn_v2_fwd_workspace_size.restype = C.c_size_t
         lib.diffattn_v2_fwd_workspace_size.argtypes = [C.c_int] * 4
+        lib.diffattn_v1_decode_num_splits.restype = C.c_int
+        lib.diffattn_v1_decode_num_splits.argtypes = [C.c_int] * 3
+        lib.diffattn_v1_decode_workspace_size.restype = C.c_size_t
+        lib.diffattn_v1_decode_workspace_size.argtypes = [C.c_int] * 5
         lib.diffattn_v2_bwd_workspace_size.restype = C.c_size_t
         lib.diffattn_v2_bwd_workspace_size.argtypes = [C.c_int] * 4
         lib.diffattn_v2_decode_num_splits.restype = C.c_int
@@ -264,6 +280,35 @@ def diffattn_v1_bwd(q1, q2, k1, k2, v, lq1, lk1, lq2, lk2, lambda_init, out, dou
         workspace.numel() * workspace.element_size(), int(bool(deterministic)))
     _check(lib.diffattn_v1_bwd(C.byref(p), _stream(stream)), "diffattn_v1_bwd")
     return grads
+
+
+def diffattn_v1_decode_num_splits(B, H, L_max) -> int:
+    return int(load().diffattn_v1_decode_num_splits(B, H, L_max))
+
+
+def diffattn_v1_decode_workspace_size(B, H, d_v, L_max, num_splits=0) -> int:
+    return int(load().diffattn_v1_decode_workspace_size(B, H, d_v, L_max, num_splits))
+
+
+def diffattn_v1_decode(q1, q2, k1_cache, k2_cache, v_cache, lq1, lk1, lq2, lk2, lambda_init, *,
+                       seqlens=None, out=None, num_splits=0, softmax_scale=0.0, rms_eps=1e-5,
+                       workspace=None, stream=None):
+    """V1 decode: out [B, H, d_v] for one new token per sequence."""
+    lib = load()
+    B, H, dqk = q1.shape
+    L_max, dv = v_cache.shape[1], v_cache.shape[3]
+    if out is None:
+        out = torch.empty((B, H, dv), dtype=q1.dtype, device=q1.device)
+    need = lib.diffattn_v1_decode_workspace_size(B, H, dv, L_max, num_splits)
+    if workspace is None:
+        workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=q1.device)
+    p = da_v1_decode_params(
+        B, H, dqk, dv, L_max, float(softmax_scale), float(lambda_init), float(rms_eps), q1.data_ptr(),
+        q2.data_ptr(), _t4(k1_cache), _t4(k2_cache), _t4(v_cache), _ptr(seqlens), _ptr(lq1), _ptr(lk1),
+        _ptr(lq2), _ptr(lk2), out.data_ptr(), int(num_splits), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size())
+    _check(lib.diffattn_v1_decode(C.byref(p), _stream(stream)), "diffattn_v1_decode")
+    return out
 
 
 def diffattn_v2_gate(x, w_lambda, *, gate=None, stream=None):

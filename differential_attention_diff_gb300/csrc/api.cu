@@ -359,4 +359,55 @@ da_status diffattn_v2_bwd(const da_v2_bwd_params* p, void* stream) {
   return cuda_status(da::launch_v2_bwd(a, static_cast<cudaStream_t>(stream)));
 }
 
+// ------------------------------------------------------------ V1 decode ----
+int diffattn_v1_decode_num_splits(int B, int H, int L_max) {
+  if (B <= 0 || H <= 0 || L_max <= 0) return 1;
+  // one 192 KB CTA per SM: about 8 waves, no split shorter than 1024 keys
+  int sms = 152;
+  DevInfo d = device_info();
+  if (d.ok) sms = d.num_sms;
+  const long units = static_cast<long>(B) * H;
+  long s = (8L * sms + units - 1) / units;
+  const long max_s = (L_max + 1023) / 1024;
+  if (s > max_s) s = max_s;
+  if (s < 1) s = 1;
+  return static_cast<int>(s);
+}
+
+size_t diffattn_v1_decode_workspace_size(int B, int H, int d_v, int L_max, int num_splits) {
+  if (B <= 0 || H <= 0 || d_v <= 0) return 0;
+  if (num_splits <= 0) num_splits = diffattn_v1_decode_num_splits(B, H, L_max);
+  const size_t po = static_cast<size_t>(num_splits) * B * H * 2 * d_v * sizeof(float);
+  const size_t pml = static_cast<size_t>(num_splits) * B * H * 2 * 2 * sizeof(float);
+  return align256(po) + align256(pml);
+}
+
+da_status diffattn_v1_decode(const da_v1_decode_params* p, void* stream) {
+  if (p == nullptr) return DA_ERR_INVALID_ARG;
+  if (p->B <= 0 || p->H <= 0 || p->d_qk <= 0 || p->d_v <= 0 || p->L_max <= 0) return DA_ERR_INVALID_ARG;
+  if (!(p->rms_eps >= 0.f)) return DA_ERR_INVALID_ARG;
+  if (p->d_qk != 128 || p->d_v != 256) return DA_ERR_UNSUPPORTED;
+  if (!p->q1 || !p->q2 || !p->out || !aligned(p->q1, 16) || !aligned(p->q2, 16) || !aligned(p->out, 16))
+    return DA_ERR_INVALID_ARG;
+  if (!p->lq1 || !p->lk1 || !p->lq2 || !p->lk2) return DA_ERR_INVALID_ARG;
+  for (const da_t4* t : {&p->k1_cache, &p->k2_cache, &p->v_cache})
+    if (check_t4(*t, DA_BF16) != DA_OK) return DA_ERR_INVALID_ARG;
+  const int splits = p->num_splits > 0 ? p->num_splits : diffattn_v1_decode_num_splits(p->B, p->H, p->L_max);
+  if (splits > 65535) return DA_ERR_INVALID_ARG;
+  const size_t need = diffattn_v1_decode_workspace_size(p->B, p->H, p->d_v, p->L_max, splits);
+  if (p->workspace == nullptr || p->workspace_bytes < need || !aligned(p->workspace, 256))
+    return DA_ERR_WORKSPACE;
+  DevInfo d = device_info();
+  if (!d.ok) return DA_ERR_CUDA;
+  uint8_t* ws = static_cast<uint8_t*>(p->workspace);
+  const size_t po = static_cast<size_t>(splits) * p->B * p->H * 2 * p->d_v * sizeof(float);
+  const float scale = p->softmax_scale > 0.f ? p->softmax_scale
+                                             : 1.f / std::sqrt(static_cast<float>(p->d_qk));
+  da::V1DecodeArgs a{p->B, p->H, p->L_max, splits, scale * kLog2e, p->lambda_init, p->rms_eps,
+                     p->q1, p->q2, p->k1_cache, p->k2_cache, p->v_cache, p->seqlens,
+                     p->lq1, p->lk1, p->lq2, p->lk2, p->out,
+                     reinterpret_cast<float*>(ws), reinterpret_cast<float*>(ws + align256(po)), d.status};
+  return cuda_status(da::launch_v1_decode(a, static_cast<cudaStream_t>(stream)));
+}
+
 }  // extern "C"

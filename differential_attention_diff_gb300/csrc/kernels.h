@@ -35,6 +35,22 @@ struct DecodeArgs {
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 
+// ---- V1 decode: split-KV partials of both streams, then merge + RMSNorm ----
+struct V1DecodeArgs {
+  int B, H, L_max, num_splits;
+  float scale_log2, lambda_init, rms_eps;
+  const void* q1;  // bf16 [B, H, 128]
+  const void* q2;
+  da_t4 k1, k2, v;  // [B, L_max, H, 128 | 128 | 256]
+  const int* seqlens;
+  const float *lq1, *lk1, *lq2, *lk2;
+  void* out;       // bf16 [B, H, 256]
+  float* part_o;   // [splits, B, H, 2, 256]
+  float* part_ml;  // [splits, B, H, 2, 2]  (running max in log2 units, sum)
+  uint32_t* status;
+};
+cudaError_t launch_v1_decode(const V1DecodeArgs& a, cudaStream_t s);
+
 // ---- V1 forward, fp32 SIMT path ------------------------------------------
 struct V1F32Args {
   int B, N, H, d_qk, d_v, causal;

@@ -63,6 +63,27 @@ def v2_inputs(B, N, h, hkv, d, d_model, seed=0, device="cpu", with_dout=False):
     return out
 
 
+def v1_decode_inputs(B, L_max, H, dqk, dv, seed=0, device="cpu", seqlens=None):
+    """V1 decode operands: q1, q2 [B,H,dqk]; k1_cache, k2_cache [B,L_max,H,dqk];
+    v_cache [B,L_max,H,dv] (bf16); four fp32 lambda vectors [dqk] ~ N(0, 0.1);
+    seqlens int32 [B] (default: every sequence full)."""
+    dt = torch.bfloat16
+    g = _gen(seed, device)
+    out = {
+        "q1": _randn((B, H, dqk), 1.0, dt, g, device),
+        "q2": _randn((B, H, dqk), 1.0, dt, g, device),
+        "k1_cache": _randn((B, L_max, H, dqk), 1.0, dt, g, device),
+        "k2_cache": _randn((B, L_max, H, dqk), 1.0, dt, g, device),
+        "v_cache": _randn((B, L_max, H, dv), 1.0, dt, g, device),
+    }
+    for name in ("lq1", "lk1", "lq2", "lk2"):
+        out[name] = _randn((dqk,), 0.1, torch.float32, g, device)
+    if seqlens is None:
+        seqlens = [L_max] * B
+    out["seqlens"] = torch.tensor(list(seqlens), dtype=torch.int32, device=device)
+    return out
+
+
 def decode_inputs(B, L_max, h, hkv, d, d_model, seed=0, device="cpu",
                   seqlens=None):
     """V2 decode operands: q [B,2h,d]; k_cache, v_cache [B,L_max,hkv,d];

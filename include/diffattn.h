@@ -152,6 +152,46 @@ size_t diffattn_v1_bwd_workspace_size(int B, int N, int H, int d_qk, int d_v, in
 da_status diffattn_v1_bwd(const da_v1_bwd_params* p, void* cuda_stream);
 
 /* ------------------------------------------------------------------------ */
+/* V1 decode.  [P1] "Differential Attention: 빼기의 힘" (the V1 formula) and
+ * "V2로의 진화" (LLM decoding, memory-bound); [P2] §1 (per-head RMSNorm and
+ * the (1 - lambda_init) scale).  One new token per sequence: for sequence b
+ * the new token's K1, K2 and V rows are already stored at position
+ * seqlens[b] - 1, and its queries q1, q2 attend to positions
+ * 0 .. seqlens[b] - 1 of the two K caches and the shared V cache:
+ *   O = (softmax(s q1 K1^T) - lambda softmax(s q2 K2^T)) V
+ *   Y = (1 - lambda_init) O / sqrt(mean_k O_k^2 + rms_eps)
+ * with lambda from the four vectors as in diffattn_v1_fwd.
+ * q1, q2: bf16 [B, H, d_qk] contiguous; k1_cache, k2_cache: bf16
+ * [B, L_max, H, d_qk], v_cache: bf16 [B, L_max, H, d_v] (da_t4 strides);
+ * seqlens: int32 [B] device, each in [1, L_max] (NULL = all L_max);
+ * lq1, lk1, lq2, lk2: fp32 [d_qk]; out: bf16 [B, H, d_v] contiguous.
+ * num_splits: key-range splits per (b, head); 0 = chosen by the library
+ * (diffattn_v1_decode_num_splits).  Workspace: split partials,
+ * diffattn_v1_decode_workspace_size bytes, 256-byte aligned.
+ * Supported: d_qk = 128, d_v = 256.  A sequence length outside [1, L_max] is
+ * recorded as DA_ERR_BOUNDS in the device status word and that row of out is
+ * written as zeros. */
+typedef struct {
+  int B, H, d_qk, d_v, L_max;
+  float softmax_scale;   /* <= 0 selects 1/sqrt(d_qk) */
+  float lambda_init;
+  float rms_eps;
+  const void* q1;
+  const void* q2;
+  da_t4 k1_cache, k2_cache, v_cache;
+  const int* seqlens;
+  const float *lq1, *lk1, *lq2, *lk2;
+  void* out;
+  int num_splits;
+  void* workspace;
+  size_t workspace_bytes;
+} da_v1_decode_params;
+
+int diffattn_v1_decode_num_splits(int B, int H, int L_max);
+size_t diffattn_v1_decode_workspace_size(int B, int H, int d_v, int L_max, int num_splits);
+da_status diffattn_v1_decode(const da_v1_decode_params* p, void* cuda_stream);
+
+/* ------------------------------------------------------------------------ */
 /* V2 gate.  [P2] §1 and §4: a per-token, per-head coefficient projected from
  * the input X and passed through a sigmoid (no bias):
  *   gate[t, p] = sigmoid(sum_k x[t, k] * w_lambda[k, p])
