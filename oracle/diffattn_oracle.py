@@ -58,6 +58,7 @@ __all__ = [
     "v2_decode",
     "v2_backward",
     "v1_decode",
+    "grouped_forward",
 ]
 
 
@@ -377,4 +378,47 @@ def v1_decode(q1, q2, k1_cache, k2_cache, v_cache, seqlens, lq1, lk1, lq2, lk2,
             lse1[b, h] = l1[0]
             lse2[b, h] = l2[0]
     return dict(y=y, o=o, lse1=lse1, lse2=lse2, lam=lam)
+
+
+def grouped_forward(q, k, v, gate, ratio: int, *, scale: float | None = None,
+                    causal: bool = True):
+    """Grouped differential attention, forward.  [P1] "같은 문제, 다른 접근"
+    names it as a follow-up that gives signal heads and noise heads an uneven
+    share, 3:1 or 4:1; the pages give nothing more.  Plainest reading, in the
+    V2 form ([P2] §1: one GQA attention, the subtracted heads share K and V,
+    a per-token per-head sigmoid gate): the query heads come in groups of
+    ``ratio`` signal heads followed by one noise head, and every signal head
+    subtracts the gated output of its group's noise head:
+        Out[b, t, g r + i] = O[b, t, g (r+1) + i]
+                             - gate[b, t, g r + i] * O[b, t, g (r+1) + r]
+    for i < r.  With ratio 1 this is the V2 forward exactly.
+
+    q: [B, N, h (r+1) / r, d]; k, v: [B, N, h_kv, d] (contiguous GQA groups,
+    each holding whole signal/noise groups); gate: [B, N, h].
+    Returns dict: out [B, N, h, d], o (per query head) [B, N, Hq, d],
+    lse [B, Hq, N].
+    """
+    q, k, v, gate = (_f64(t) for t in (q, k, v, gate))
+    B, N, Hq, d = q.shape
+    hkv = k.shape[2]
+    group = Hq // hkv
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    o = np.zeros((B, N, Hq, d))
+    lse = np.zeros((B, Hq, N))
+    for b in range(B):
+        for j in range(Hq):
+            c = j // group
+            a, l = attention_maps(q[b, :, j], k[b, :, c], scale, causal)
+            o[b, :, j] = a @ v[b, :, c]
+            lse[b, j] = l
+    n_groups = Hq // (ratio + 1)
+    h = n_groups * ratio
+    out = np.zeros((B, N, h, d))
+    for g in range(n_groups):
+        noise = o[:, :, g * (ratio + 1) + ratio]
+        for i in range(ratio):
+            p = g * ratio + i
+            out[:, :, p] = o[:, :, g * (ratio + 1) + i] - gate[:, :, p, None] * noise
+    return dict(out=out, o=o, lse=lse)
 

@@ -387,6 +387,55 @@ def test_v1_decode_equals_last_causal_row():
     assert dec["lam"] == full["lam"]
 
 
+def test_grouped_ratio_one_is_v2():
+    """Grouped differential attention with one signal head per noise head is
+    the V2 forward (pins the head order of a group and the gate index)."""
+    t = _v2_rand(seed=26, N=10)
+    gate = orc.v2_gate(t["x"], t["w"])
+    v2 = orc.v2_forward(t["q"], t["k"], t["v"], gate)
+    gr = orc.grouped_forward(t["q"], t["k"], t["v"], gate, 1)
+    np.testing.assert_allclose(gr["out"], v2["out"], atol=1e-13)
+
+
+def test_grouped_gate_zero_and_shared_noise():
+    """Gate 0: each output head is torch SDPA of its signal head over the
+    repeated K/V (a library routine); gate 1 with every signal query equal to
+    its group's noise query: exact zero; a noise head with zero query gives
+    signal - gate * cumulative mean of V, the same for every signal head of
+    the group."""
+    r = _rng(27)
+    B, N, ratio, hkv, d = 2, 9, 3, 2, 5
+    Hq = 2 * (ratio + 1) * hkv  # two groups per K/V head
+    q = r.standard_normal((B, N, Hq, d))
+    k = r.standard_normal((B, N, hkv, d))
+    v = r.standard_normal((B, N, hkv, d))
+    h = Hq // (ratio + 1) * ratio
+    out0 = orc.grouped_forward(q, k, v, np.zeros((B, N, h)), ratio)["out"]
+    G = Hq // hkv
+    kr = torch.from_numpy(np.repeat(k, G, axis=2)).permute(0, 2, 1, 3)
+    vr = torch.from_numpy(np.repeat(v, G, axis=2)).permute(0, 2, 1, 3)
+    sdpa = torch.nn.functional.scaled_dot_product_attention(
+        torch.from_numpy(q).permute(0, 2, 1, 3), kr, vr, is_causal=True).permute(0, 2, 1, 3).numpy()
+    sig = [g * (ratio + 1) + i for g in range(Hq // (ratio + 1)) for i in range(ratio)]
+    np.testing.assert_allclose(out0, sdpa[:, :, sig], atol=1e-12)
+    qs = q.copy()
+    for g in range(Hq // (ratio + 1)):
+        for i in range(ratio):
+            qs[:, :, g * (ratio + 1) + i] = q[:, :, g * (ratio + 1) + ratio]
+    assert np.all(orc.grouped_forward(qs, k, v, np.ones((B, N, h)), ratio)["out"] == 0.0)
+    qz = q.copy()
+    qz[:, :, ratio::ratio + 1] = 0.0
+    gate = r.uniform(0, 1, (B, N, h))
+    got = orc.grouped_forward(qz, k, v, gate, ratio)
+    cm = np.cumsum(v, axis=1) / np.arange(1, N + 1)[None, :, None, None]
+    for g in range(Hq // (ratio + 1)):
+        c = (g * (ratio + 1)) // G
+        for i in range(ratio):
+            p = g * ratio + i
+            want = sdpa[:, :, g * (ratio + 1) + i] - gate[:, :, p, None] * cm[:, :, c]
+            np.testing.assert_allclose(got["out"][:, :, p], want, atol=1e-12)
+
+
 # -------------------------------------------------------------- backward ----
 
 def test_v1_backward_finite_differences():
