@@ -371,6 +371,45 @@ class V2FwdBwd(V2Fwd):
         return dt, flops, f"batch 0, K/V group 0 ({G} query heads), first {n} tokens (fp64 oracle fwd+bwd)"
 
 
+class GroupedFwd(Workload):
+    name = "grouped_fwd"
+    desc = ("Grouped DiffAttn 3:1 fwd bf16 B2 N8192, 64 query heads = 16 x (3 signal + 1 noise), 8 kv heads, "
+            "d128 causal, gate from X[2,8192,4096]")
+    launches = 3
+    B, N, h, ratio, hkv, d, dm = 2, 8192, 48, 3, 8, 128, 4096
+
+    def work(self):
+        Hq = self.h // self.ratio * (self.ratio + 1)
+        return v2_fwd_flops(self.B, self.N, Hq // 2, self.d)
+
+    def setup(self, dev):
+        from differential_attention_diff_gb300 import binding as bd, synth
+        self.bd = bd
+        self.t = synth.grouped_inputs(self.B, self.N, self.h, self.ratio, self.hkv, self.d, self.dm, seed=1007,
+                                      device=dev)
+        self.out = torch.empty((self.B, self.N, self.h, self.d), dtype=torch.bfloat16, device=dev)
+        need = bd.load().diffattn_grouped_fwd_workspace_size(self.B, self.N, self.h, self.ratio, self.d, 0, 0)
+        self.ws = torch.empty((need,), dtype=torch.uint8, device=dev)
+
+    def run(self):
+        t = self.t
+        self.bd.diffattn_grouped_fwd(t["q"], t["k"], t["v"], self.ratio, x=t["x"], w_lambda=t["w_lambda"],
+                                     out=self.out, workspace=self.ws)
+
+    def oracle_sample(self, big=True):
+        from oracle import diffattn_oracle as orc
+        rows = np.sort(np.random.default_rng(0).choice(self.N, 256 if big else 48, replace=False))
+        sl = lambda x: x.to("cpu", torch.float64).numpy()  # noqa: E731
+        t = self.t
+        t0 = time.perf_counter()
+        gate = orc.v2_gate(sl(t["x"][0:1]), sl(t["w_lambda"][:, 0:self.ratio]))
+        orc.grouped_forward(sl(t["q"][0:1, :, 0:self.ratio + 1]), sl(t["k"][0:1, :, 0:1]), sl(t["v"][0:1, :, 0:1]),
+                            gate, self.ratio, rows=rows)
+        dt = time.perf_counter() - t0
+        flops = (self.ratio + 1) * float(np.sum(rows + 1)) * 4.0 * self.d
+        return dt, flops, f"batch 0, group 0 ({self.ratio + 1} query heads), {len(rows)} seeded rows (gate included)"
+
+
 class V2Decode(Workload):
     name = "v2_decode"
     desc = "V2 decode bf16 B64 cache 32768 8 KV heads 64 query heads d128, gate from X[64,4096]"
@@ -464,7 +503,7 @@ class V2FwdBwdSmall(V2FwdBwd):
 
 
 WORKLOADS = {w.name: w for w in (V1Fwd, V1FwdF32, V2Fwd, V2Decode, V1FwdBwd, V1FwdBwdDet, V2FwdBwd,
-                                 V1Decode)}
+                                 V1Decode, GroupedFwd)}
 PROFILE_ONLY = {V2DecodeSmall.name: V2DecodeSmall, V2FwdBwdSmall.name: V2FwdBwdSmall}
 
 # ----------------------------------------------------------------- helpers --
@@ -478,6 +517,7 @@ KERNEL_SOURCES = {
     "v2_decode": ("decode.cu", "common.cuh"),
     "v2_fwd_bwd": ("v2_bwd.cu", "softmax.cuh", "tma.cuh", "common.cuh"),
     "v1_decode": ("v1_decode.cu", "common.cuh"),
+    "grouped_fwd": ("v2_fwd.cu", "grouped.cu", "softmax.cuh", "tma.cuh", "common.cuh"),
 }
 
 

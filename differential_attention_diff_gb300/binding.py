@@ -37,6 +37,8 @@ EXPORTS = (
     "diffattn_v1_decode_workspace_size",
     "diffattn_v2_bwd",
     "diffattn_v2_bwd_workspace_size",
+    "diffattn_grouped_fwd",
+    "diffattn_grouped_fwd_workspace_size",
     "diffattn_v2_gate",
     "diffattn_v2_fwd",
     "diffattn_v2_fwd_workspace_size",
@@ -109,6 +111,14 @@ class da_v2_fwd_params(C.Structure):
                 ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t)]
 
 
+class da_grouped_fwd_params(C.Structure):
+    _fields_ = [("B", C.c_int), ("N", C.c_int), ("h", C.c_int), ("ratio", C.c_int), ("h_kv", C.c_int),
+                ("d", C.c_int), ("d_model", C.c_int), ("causal", C.c_int), ("softmax_scale", C.c_float),
+                ("q", da_t4), ("k", da_t4), ("v", da_t4), ("gate", C.c_void_p), ("x", C.c_void_p),
+                ("w_lambda", C.c_void_p), ("out", da_t4), ("lse", C.c_void_p), ("o_heads", da_t4),
+                ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t)]
+
+
 class da_v2_bwd_params(C.Structure):
     _fields_ = [("B", C.c_int), ("N", C.c_int), ("h", C.c_int), ("h_kv", C.c_int), ("d", C.c_int),
                 ("d_model", C.c_int), ("causal", C.c_int), ("softmax_scale", C.c_float),
@@ -151,6 +161,7 @@ def load(path: str = LIB_PATH):
         for name, st in (("diffattn_v1_fwd", da_v1_fwd_params), ("diffattn_v1_bwd", da_v1_bwd_params),
                          ("diffattn_v2_gate", da_v2_gate_params), ("diffattn_v2_fwd", da_v2_fwd_params),
                          ("diffattn_v2_bwd", da_v2_bwd_params), ("diffattn_v1_decode", da_v1_decode_params),
+                         ("diffattn_grouped_fwd", da_grouped_fwd_params),
                          ("diffattn_v2_decode", da_v2_decode_params),
                          ("diffattn_v2_decode_noalloc", da_v2_decode_params)):
             f = getattr(lib, name)
@@ -166,6 +177,8 @@ def load(path: str = LIB_PATH):
         lib.diffattn_v1_decode_num_splits.argtypes = [C.c_int] * 3
         lib.diffattn_v1_decode_workspace_size.restype = C.c_size_t
         lib.diffattn_v1_decode_workspace_size.argtypes = [C.c_int] * 5
+        lib.diffattn_grouped_fwd_workspace_size.restype = C.c_size_t
+        lib.diffattn_grouped_fwd_workspace_size.argtypes = [C.c_int] * 7
         lib.diffattn_v2_bwd_workspace_size.restype = C.c_size_t
         lib.diffattn_v2_bwd_workspace_size.argtypes = [C.c_int] * 4
         lib.diffattn_v2_decode_num_splits.restype = C.c_int
@@ -353,6 +366,29 @@ def diffattn_v2_fwd(q, k, v, *, gate=None, x=None, w_lambda=None, out=None, lse=
         _ptr(workspace), 0 if workspace is None else workspace.numel() * workspace.element_size())
     _check(lib.diffattn_v2_fwd(C.byref(p), _stream(stream)), "diffattn_v2_fwd")
     return (out, saves) if save else out
+
+
+def diffattn_grouped_fwd(q, k, v, ratio, *, gate=None, x=None, w_lambda=None, out=None, lse=None,
+                         o_heads=None, causal=True, softmax_scale=0.0, workspace=None, stream=None):
+    """Grouped differential attention: q [B, N, h (ratio+1)/ratio, d] in groups
+    of `ratio` signal heads then one noise head; out [B, N, h, d]."""
+    lib = load()
+    B, N, Hq, d = q.shape
+    h = Hq // (ratio + 1) * ratio
+    hkv = k.shape[2]
+    if out is None:
+        out = torch.empty((B, N, h, d), dtype=q.dtype, device=q.device)
+    d_model = 0 if x is None else x.shape[-1]
+    need = lib.diffattn_grouped_fwd_workspace_size(B, N, h, ratio, d, int(gate is not None),
+                                                   int(o_heads is not None))
+    if workspace is None and need:
+        workspace = torch.empty((need,), dtype=torch.uint8, device=q.device)
+    p = da_grouped_fwd_params(
+        B, N, h, int(ratio), hkv, d, d_model, int(causal), float(softmax_scale), _t4(q), _t4(k), _t4(v),
+        _ptr(gate), _ptr(x), _ptr(w_lambda), _t4(out), _ptr(lse), _t4(o_heads), _ptr(workspace),
+        0 if workspace is None else workspace.numel() * workspace.element_size())
+    _check(lib.diffattn_grouped_fwd(C.byref(p), _stream(stream)), "diffattn_grouped_fwd")
+    return out
 
 
 def diffattn_v2_bwd_workspace_size(B, N, h, d_model=0) -> int:

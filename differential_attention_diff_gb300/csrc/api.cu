@@ -410,4 +410,68 @@ da_status diffattn_v1_decode(const da_v1_decode_params* p, void* stream) {
   return cuda_status(da::launch_v1_decode(a, static_cast<cudaStream_t>(stream)));
 }
 
+// --------------------------------------------------------- grouped fwd -----
+size_t diffattn_grouped_fwd_workspace_size(int B, int N, int h, int ratio, int d, int gate_given,
+                                           int heads_given) {
+  if (B <= 0 || N <= 0 || h <= 0 || ratio <= 0 || d <= 0 || h % ratio) return 0;
+  const size_t Hq = static_cast<size_t>(h) / ratio * (ratio + 1);
+  const size_t g = gate_given ? 0 : static_cast<size_t>(B) * N * h * sizeof(float);
+  const size_t o = heads_given ? 0 : static_cast<size_t>(B) * N * Hq * d * 2;
+  return align256(g) + align256(o);
+}
+
+da_status diffattn_grouped_fwd(const da_grouped_fwd_params* p, void* stream) {
+  if (p == nullptr) return DA_ERR_INVALID_ARG;
+  if (p->B < 0 || p->N < 0 || p->h <= 0 || p->ratio <= 0 || p->h_kv <= 0 || p->d <= 0)
+    return DA_ERR_INVALID_ARG;
+  if (p->h % p->ratio) return DA_ERR_INVALID_ARG;
+  const int Hq = p->h / p->ratio * (p->ratio + 1);
+  if (Hq % p->h_kv) return DA_ERR_INVALID_ARG;
+  const int G = Hq / p->h_kv;
+  if (G % (p->ratio + 1)) return DA_ERR_INVALID_ARG;  // a group must sit in one K/V group
+  if (p->B == 0 || p->N == 0) return DA_OK;
+  if (p->d != 128 || !p->causal || (G % 2)) return DA_ERR_UNSUPPORTED;
+  for (const da_t4* t : {&p->q, &p->k, &p->v, &p->out})
+    if (check_t4(*t, DA_BF16) != DA_OK) return DA_ERR_INVALID_ARG;
+  if (p->o_heads.ptr && check_t4(p->o_heads, DA_BF16) != DA_OK) return DA_ERR_INVALID_ARG;
+  if (p->lse && !aligned(p->lse, 4)) return DA_ERR_INVALID_ARG;
+  if (p->gate == nullptr) {
+    if (!p->x || !p->w_lambda || p->d_model <= 0) return DA_ERR_INVALID_ARG;
+    if ((p->d_model % 64) || p->h > 64) return DA_ERR_UNSUPPORTED;
+  } else if (!aligned(p->gate, 4)) {
+    return DA_ERR_INVALID_ARG;
+  }
+  const size_t need = diffattn_grouped_fwd_workspace_size(p->B, p->N, p->h, p->ratio, p->d, p->gate != nullptr,
+                                                          p->o_heads.ptr != nullptr);
+  if (need && (p->workspace == nullptr || p->workspace_bytes < need || !aligned(p->workspace, 256)))
+    return DA_ERR_WORKSPACE;
+  if (!da::tma_available()) return DA_ERR_CUDA;
+  DevInfo d = device_info();
+  if (!d.ok) return DA_ERR_CUDA;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  uint8_t* ws = static_cast<uint8_t*>(p->workspace);
+  const float* gate = p->gate;
+  size_t off = 0;
+  if (gate == nullptr) {
+    float* g = reinterpret_cast<float*>(ws);
+    da::GateArgs ga{p->B * p->N, p->d_model, p->h, p->x, p->d_model, p->w_lambda, g};
+    if (da::launch_gate(ga, s) != cudaSuccess) return DA_ERR_CUDA;
+    gate = g;
+    off = align256(static_cast<size_t>(p->B) * p->N * p->h * sizeof(float));
+  }
+  da_t4 heads = p->o_heads;
+  if (heads.ptr == nullptr) {
+    const int64_t sn = static_cast<int64_t>(Hq) * p->d;
+    heads = da_t4{ws + off, static_cast<int64_t>(p->N) * sn, sn, p->d};
+  }
+  const float scale = p->softmax_scale > 0.f ? p->softmax_scale
+                                             : 1.f / std::sqrt(static_cast<float>(p->d));
+  // the attention over all Hq heads (taken two at a time), per-head outputs only
+  da::V2FwdArgs fa{p->B, p->N, Hq / 2, p->h_kv, p->d, p->causal, scale * kLog2e,
+                   p->q, p->k, p->v, da_t4{nullptr, 0, 0, 0}, nullptr, p->lse, heads, d.status, d.num_sms};
+  if (da::launch_v2_fwd(fa, s) != cudaSuccess) return DA_ERR_CUDA;
+  da::GroupedArgs ca{p->B, p->N, p->h, p->ratio, heads, gate, p->out};
+  return cuda_status(da::launch_grouped_combine(ca, s));
+}
+
 }  // extern "C"

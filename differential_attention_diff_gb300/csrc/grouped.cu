@@ -1,0 +1,67 @@
+// grouped.cu — the combination step of grouped differential attention.
+//
+// "Differential Transformer | ICLR 2025 Oral" (dainus.ai), "같은 문제, 다른
+// 접근": a follow-up gives signal-extracting heads and noise-controlling heads
+// an uneven share, 3:1 or 4:1.  Read in the V2 form ("Differential Transformer
+// V2", pogovet.com, §1): query heads come in groups of `ratio` signal heads
+// followed by one noise head (all in one K/V group), and
+//   out[t, g r + i] = O[t, g (r+1) + i] - gate[t, g r + i] * O[t, g (r+1) + r].
+// The per-head outputs O come from the V2 attention kernel run without its
+// pair combination (a group spans more heads than a pair, and one SM's TMEM
+// holds two heads' scores and accumulators); this HBM-bound kernel then reads
+// each signal row and its group's noise row once per output and writes out.
+#include "common.cuh"
+#include "kernels.h"
+
+namespace da {
+namespace {
+
+constexpr int kD = 128;
+
+// One thread per 8 features of one (b, n, output head).
+__global__ void __launch_bounds__(256)
+grouped_combine_kernel(GroupedArgs a) {
+  const long long total = static_cast<long long>(a.B) * a.N * a.h * (kD / 8);
+  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
+       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
+    const int c8 = static_cast<int>(idx % (kD / 8)) * 8;
+    const long long row = idx / (kD / 8);  // (b, n, p)
+    const int p = static_cast<int>(row % a.h);
+    const long long bn = row / a.h;
+    const int n = static_cast<int>(bn % a.N), b = static_cast<int>(bn / a.N);
+    const int g = p / a.ratio, i = p % a.ratio;
+    const __nv_bfloat16* base = static_cast<const __nv_bfloat16*>(a.o_heads.ptr) + b * a.o_heads.sb +
+                                static_cast<int64_t>(n) * a.o_heads.sn + c8;
+    const uint4 sv = *reinterpret_cast<const uint4*>(base + static_cast<int64_t>(g * (a.ratio + 1) + i) * a.o_heads.sh);
+    const uint4 nv =
+        *reinterpret_cast<const uint4*>(base + static_cast<int64_t>(g * (a.ratio + 1) + a.ratio) * a.o_heads.sh);
+    const float gt = a.gate[row];
+    const __nv_bfloat162* s2 = reinterpret_cast<const __nv_bfloat162*>(&sv);
+    const __nv_bfloat162* n2 = reinterpret_cast<const __nv_bfloat162*>(&nv);
+    uint32_t r[4];
+#pragma unroll
+    for (int e = 0; e < 4; ++e) {
+      // both terms rounded on their own: equal signal and noise rows with
+      // gate 1 give exactly zero
+      const float lo = __fsub_rn(__low2float(s2[e]), __fmul_rn(gt, __low2float(n2[e])));
+      const float hi = __fsub_rn(__high2float(s2[e]), __fmul_rn(gt, __high2float(n2[e])));
+      r[e] = pack_bf16x2(lo, hi);
+    }
+    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out.ptr) + b * a.out.sb + static_cast<int64_t>(n) * a.out.sn +
+                         p * a.out.sh + c8;
+    *reinterpret_cast<uint4*>(dst) = make_uint4(r[0], r[1], r[2], r[3]);
+  }
+}
+
+}  // namespace
+
+cudaError_t launch_grouped_combine(const GroupedArgs& a, cudaStream_t s) {
+  const long long total = static_cast<long long>(a.B) * a.N * a.h * (kD / 8);
+  long long grid = (total + 255) / 256;
+  if (grid > 16 * 152) grid = 16 * 152;
+  if (grid < 1) grid = 1;
+  grouped_combine_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(a);
+  return cudaGetLastError();
+}
+
+}  // namespace da

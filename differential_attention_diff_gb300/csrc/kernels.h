@@ -74,6 +74,15 @@ struct V2FwdArgs {
 };
 cudaError_t launch_v2_fwd(const V2FwdArgs& a, cudaStream_t s);
 
+// ---- grouped differential attention: combine per-head outputs -------------
+struct GroupedArgs {
+  int B, N, h, ratio;   // h output (signal) heads, ratio signal heads per noise head
+  da_t4 o_heads;        // [B, N, h (ratio + 1) / ratio, d] bf16
+  const float* gate;    // [B, N, h]
+  da_t4 out;            // [B, N, h, d] bf16
+};
+cudaError_t launch_grouped_combine(const GroupedArgs& a, cudaStream_t s);
+
 // ---- V2 backward, bf16, tcgen05 --------------------------------------------
 struct V2BwdArgs {
   int B, N, h, h_kv, d, d_model, causal;

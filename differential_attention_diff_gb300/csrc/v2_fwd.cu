@@ -28,7 +28,9 @@
 //     bf16, O rescaled in TMEM on the rare tiles that raise the max.
 //     The same threads run the epilogue: O_even / l_even - gate * O_odd /
 //     l_odd, bf16 store, optional log-sum-exp and per-head outputs (the
-//     backward's saves).
+//     backward's saves).  With no output tensor the kernel writes only the
+//     per-head outputs (the attention part of grouped differential
+//     attention, whose groups span more than a pair).
 //
 // Every mbarrier wait is bounded (about 2 s); on expiry the kernel records
 // DA_ERR_TIMEOUT in the status word, raises a shared abort flag so the other
@@ -330,25 +332,28 @@ v2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       }
       tmem_ld_wait();
       if (n < a.N) {
-        const float gte = a.gate[(static_cast<int64_t>(w.b) * a.N + n) * a.h + w.p];
-        const float ie = 1.f / le, io = gte / lo;
-        __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out.ptr) + w.b * a.out.sb +
-                             static_cast<int64_t>(n) * a.out.sn + w.p * a.out.sh + wg * 64;
-        // both products rounded separately (no FMA contraction), so equal
-        // even and odd outputs with gate 1 cancel exactly
-        auto diff = [&](uint32_t xe, uint32_t xo) {
-          return __fsub_rn(__fmul_rn(__uint_as_float(xe), ie), __fmul_rn(__uint_as_float(xo), io));
-        };
+        const float ie = 1.f / le;
+        if (a.out.ptr) {
+          const float gte = a.gate[(static_cast<int64_t>(w.b) * a.N + n) * a.h + w.p];
+          const float io = gte / lo;
+          __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out.ptr) + w.b * a.out.sb +
+                               static_cast<int64_t>(n) * a.out.sn + w.p * a.out.sh + wg * 64;
+          // both products rounded separately (no FMA contraction), so equal
+          // even and odd outputs with gate 1 cancel exactly
+          auto diff = [&](uint32_t xe, uint32_t xo) {
+            return __fsub_rn(__fmul_rn(__uint_as_float(xe), ie), __fmul_rn(__uint_as_float(xo), io));
+          };
 #pragma unroll
-        for (int c = 0; c < 2; ++c) {
+          for (int c = 0; c < 2; ++c) {
 #pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            uint4 v;
-            v.x = pack_bf16x2(diff(oe[c][e], oo[c][e]), diff(oe[c][e + 1], oo[c][e + 1]));
-            v.y = pack_bf16x2(diff(oe[c][e + 2], oo[c][e + 2]), diff(oe[c][e + 3], oo[c][e + 3]));
-            v.z = pack_bf16x2(diff(oe[c][e + 4], oo[c][e + 4]), diff(oe[c][e + 5], oo[c][e + 5]));
-            v.w = pack_bf16x2(diff(oe[c][e + 6], oo[c][e + 6]), diff(oe[c][e + 7], oo[c][e + 7]));
-            *reinterpret_cast<uint4*>(dst + c * 32 + e) = v;
+            for (int e = 0; e < 32; e += 8) {
+              uint4 v;
+              v.x = pack_bf16x2(diff(oe[c][e], oo[c][e]), diff(oe[c][e + 1], oo[c][e + 1]));
+              v.y = pack_bf16x2(diff(oe[c][e + 2], oo[c][e + 2]), diff(oe[c][e + 3], oo[c][e + 3]));
+              v.z = pack_bf16x2(diff(oe[c][e + 4], oo[c][e + 4]), diff(oe[c][e + 5], oo[c][e + 5]));
+              v.w = pack_bf16x2(diff(oe[c][e + 6], oo[c][e + 6]), diff(oe[c][e + 7], oo[c][e + 7]));
+              *reinterpret_cast<uint4*>(dst + c * 32 + e) = v;
+            }
           }
         }
         if (a.o_heads.ptr) {

@@ -63,6 +63,21 @@ def v2_inputs(B, N, h, hkv, d, d_model, seed=0, device="cpu", with_dout=False):
     return out
 
 
+def grouped_inputs(B, N, h, ratio, hkv, d, d_model, seed=0, device="cpu"):
+    """Grouped differential attention operands: q [B,N,h(ratio+1)/ratio,d];
+    k, v [B,N,hkv,d]; x [B,N,d_model]; w_lambda [d_model,h] (all bf16)."""
+    dt = torch.bfloat16
+    g = _gen(seed, device)
+    Hq = h // ratio * (ratio + 1)
+    return {
+        "q": _randn((B, N, Hq, d), 1.0, dt, g, device),
+        "k": _randn((B, N, hkv, d), 1.0, dt, g, device),
+        "v": _randn((B, N, hkv, d), 1.0, dt, g, device),
+        "x": _randn((B, N, d_model), 1.0, dt, g, device),
+        "w_lambda": _randn((d_model, h), 0.02, dt, g, device),
+    }
+
+
 def v1_decode_inputs(B, L_max, H, dqk, dv, seed=0, device="cpu", seqlens=None):
     """V1 decode operands: q1, q2 [B,H,dqk]; k1_cache, k2_cache [B,L_max,H,dqk];
     v_cache [B,L_max,H,dv] (bf16); four fp32 lambda vectors [dqk] ~ N(0, 0.1);

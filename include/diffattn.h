@@ -244,6 +244,42 @@ size_t diffattn_v2_fwd_workspace_size(int B, int N, int h, int gate_given);
 da_status diffattn_v2_fwd(const da_v2_fwd_params* p, void* cuda_stream);
 
 /* ------------------------------------------------------------------------ */
+/* Grouped differential attention, forward.  [P1] "같은 문제, 다른 접근" names
+ * the follow-up that gives signal heads and noise heads an uneven share (3:1
+ * or 4:1) and says nothing more; the reading implemented here is the V2 form
+ * ([P2] §1): one causal GQA attention over Hq = h (ratio + 1) / ratio query
+ * heads that come in groups of `ratio` signal heads followed by one noise
+ * head, every group inside one K/V group, and per token t and output head p
+ * of group g = p / ratio, i = p mod ratio:
+ *   out[t, p] = O[t, g (ratio+1) + i] - gate[t, p] * O[t, g (ratio+1) + ratio]
+ * With ratio 1 this is diffattn_v2_fwd's result.
+ * q: [B, N, Hq, d]; k, v: [B, N, h_kv, d]; out: [B, N, h, d]; all bf16.
+ * Gate source as in diffattn_v2_fwd (fp32 [B, N, h], or x + w_lambda with
+ * w_lambda [d_model, h]).  Optional saves: lse fp32 [B, Hq, N]; o_heads bf16
+ * [B, N, Hq, d] (each head's normalised output; when NULL the per-head
+ * outputs go to the workspace).  Supported: d = 128, causal, h divisible by
+ * ratio, Hq / h_kv a multiple of ratio + 1 and even.
+ * workspace: diffattn_grouped_fwd_workspace_size bytes, 256-byte aligned. */
+typedef struct {
+  int B, N, h, ratio, h_kv, d, d_model;
+  int causal;
+  float softmax_scale;   /* <= 0 selects 1/sqrt(d) */
+  da_t4 q, k, v;
+  const float* gate;
+  const void* x;
+  const void* w_lambda;
+  da_t4 out;
+  float* lse;
+  da_t4 o_heads;
+  void* workspace;
+  size_t workspace_bytes;
+} da_grouped_fwd_params;
+
+size_t diffattn_grouped_fwd_workspace_size(int B, int N, int h, int ratio, int d, int gate_given,
+                                           int heads_given);
+da_status diffattn_grouped_fwd(const da_grouped_fwd_params* p, void* cuda_stream);
+
+/* ------------------------------------------------------------------------ */
 /* V2 backward: gradients of diffattn_v2_fwd (and of the gate projection)
  * given dOut.  The pages state no backward; it is the chain rule of the V2
  * forward ([P2] §1, §4).  With g = sigmoid(z), z[t, p] = x[t] . w_lambda[:, p],

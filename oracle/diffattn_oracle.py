@@ -381,7 +381,7 @@ def v1_decode(q1, q2, k1_cache, k2_cache, v_cache, seqlens, lq1, lk1, lq2, lk2,
 
 
 def grouped_forward(q, k, v, gate, ratio: int, *, scale: float | None = None,
-                    causal: bool = True):
+                    causal: bool = True, rows=None):
     """Grouped differential attention, forward.  [P1] "같은 문제, 다른 접근"
     names it as a follow-up that gives signal heads and noise heads an uneven
     share, 3:1 or 4:1; the pages give nothing more.  Plainest reading, in the
@@ -395,8 +395,9 @@ def grouped_forward(q, k, v, gate, ratio: int, *, scale: float | None = None,
 
     q: [B, N, h (r+1) / r, d]; k, v: [B, N, h_kv, d] (contiguous GQA groups,
     each holding whole signal/noise groups); gate: [B, N, h].
-    Returns dict: out [B, N, h, d], o (per query head) [B, N, Hq, d],
-    lse [B, Hq, N].
+    ``rows`` restricts the query rows computed (every key is still used).
+    Returns dict: out [B, R, h, d], o (per query head) [B, R, Hq, d],
+    lse [B, Hq, R], rows.
     """
     q, k, v, gate = (_f64(t) for t in (q, k, v, gate))
     B, N, Hq, d = q.shape
@@ -404,21 +405,23 @@ def grouped_forward(q, k, v, gate, ratio: int, *, scale: float | None = None,
     group = Hq // hkv
     if scale is None:
         scale = 1.0 / np.sqrt(d)
-    o = np.zeros((B, N, Hq, d))
-    lse = np.zeros((B, Hq, N))
+    rows = np.arange(N) if rows is None else np.asarray(rows)
+    R = rows.shape[0]
+    o = np.zeros((B, R, Hq, d))
+    lse = np.zeros((B, Hq, R))
     for b in range(B):
         for j in range(Hq):
             c = j // group
-            a, l = attention_maps(q[b, :, j], k[b, :, c], scale, causal)
+            a, l = attention_maps(q[b, :, j], k[b, :, c], scale, causal, rows)
             o[b, :, j] = a @ v[b, :, c]
             lse[b, j] = l
     n_groups = Hq // (ratio + 1)
     h = n_groups * ratio
-    out = np.zeros((B, N, h, d))
+    out = np.zeros((B, R, h, d))
     for g in range(n_groups):
         noise = o[:, :, g * (ratio + 1) + ratio]
         for i in range(ratio):
             p = g * ratio + i
-            out[:, :, p] = o[:, :, g * (ratio + 1) + i] - gate[:, :, p, None] * noise
-    return dict(out=out, o=o, lse=lse)
+            out[:, :, p] = o[:, :, g * (ratio + 1) + i] - gate[:, rows, p, None] * noise
+    return dict(out=out, o=o, lse=lse, rows=rows)
 

@@ -137,3 +137,15 @@ def test_bwd_workspace_size(lib):
     slots = n_kt * n_qt - n_kt * (n_kt - 1)
     assert det - base == 2 * 16 * (slots * 64 - 8192) * 128 * 4
     assert lib.diffattn_v2_bwd_workspace_size(2, 8192, 32, 4096) > lib.diffattn_v2_bwd_workspace_size(2, 8192, 32, 0)
+
+
+def test_grouped_shape_checks(lib):
+    """Grouped differential attention rejects, before any launch, groups that
+    do not divide the heads or straddle K/V groups, and an odd number of query
+    heads per K/V head (the attention kernel takes heads two at a time)."""
+    def p(h, ratio, hkv):
+        return bd.da_grouped_fwd_params(B=1, N=64, h=h, ratio=ratio, h_kv=hkv, d=128, d_model=0, causal=1)
+    assert lib.diffattn_grouped_fwd(C.byref(p(7, 3, 1)), None) == bd.DA_ERR_INVALID_ARG   # h % ratio
+    assert lib.diffattn_grouped_fwd(C.byref(p(6, 3, 4)), None) == bd.DA_ERR_INVALID_ARG   # 8 heads / 4 kv: groups of 4 straddle
+    assert lib.diffattn_grouped_fwd(C.byref(p(8, 4, 2)), None) == bd.DA_ERR_UNSUPPORTED   # 5 heads per kv head
+    assert lib.diffattn_grouped_fwd_workspace_size(2, 8192, 48, 3, 128, 0, 0) == 2 * 8192 * 48 * 4 + 2 * 8192 * 64 * 128 * 2
