@@ -7,9 +7,12 @@ Prints ONE JSON line (rank 0).  `value` is the throughput of the selected
 workload (default: V1 forward bf16, B4 H12 N4096 d_qk 128 d_v 256, causal)
 with inputs resident in HBM; `rows` holds the same measurement for every
 other step of the path (V1 fp32, V2 gate + forward, V2 decode, V1
-forward + backward) on its own workload; `e2e` repeats the main workload
-through the public API with pinned host buffers and the copies inside the
-timed region; `roofline` relates the dominant kernel's live CUDA-event time
+forward + backward, deterministic V1 backward, V2 forward + backward, V1
+decode, grouped attention) on its own workload; `e2e` repeats the main
+workload through the public API with every step's inputs uploaded from pinned
+host memory and its results read back inside the timed region (uploads,
+kernels and read-backs of consecutive steps overlap on three streams; decode
+keeps its KV cache resident as model state); `roofline` relates the dominant kernel's live CUDA-event time
 to the measured (or fallback) peak; `cpu_baseline` times the fp64 oracle on a
 bounded sample of the same workload.
 
@@ -128,16 +131,16 @@ class V1Fwd(Workload):
         self.bd.diffattn_v1_fwd(*self.args(self.t), self.li, out=self.out, workspace=self.fws)
 
     # end-to-end through the public API with host buffers
-    def e2e_setup(self):
-        self.host = {k: v.cpu().pin_memory() for k, v in self.t.items()}
-        self.host_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
-        self.h2d = sum(v.numel() * v.element_size() for v in self.host.values())
-        self.d2h = self.host_out.numel() * self.host_out.element_size()
+    # end-to-end through the public API: inputs uploaded from pinned host
+    # memory, the result read back, every step (see run_e2e)
+    def e2e_inputs(self):
+        return dict(self.t)
 
-    def e2e_step(self):
-        dev = {k: v.to(self.out.device, non_blocking=True) for k, v in self.host.items()}
-        self.bd.diffattn_v1_fwd(*self.args(dev), self.li, out=self.out, workspace=self.fws)
-        self.host_out.copy_(self.out, non_blocking=True)
+    def e2e_outputs(self):
+        return [self.out]
+
+    def e2e_compute(self, d, outs):
+        self.bd.diffattn_v1_fwd(*self.args(d), self.li, out=outs[0], workspace=self.fws)
 
     def oracle_sample(self, big=True):
         """fp64 oracle on a bounded sample (every head of the first batches, a
@@ -202,22 +205,20 @@ class V1FwdBwd(V1Fwd):
         return v1_bwd_flops(self.B, self.N, self.H, self.dqk, self.dv)
 
 
-    def e2e_setup(self):
-        names = ("q1", "q2", "k1", "k2", "v", "lq1", "lk1", "lq2", "lk2", "dy")
-        self.host = {k: self.t[k].cpu().pin_memory() for k in names}
-        self.host_g = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in self.grads.items()}
-        self.h2d = sum(v.numel() * v.element_size() for v in self.host.values())
-        self.d2h = sum(v.numel() * v.element_size() for v in self.host_g.values())
+    GRADS = ("dq1", "dq2", "dk1", "dk2", "dv", "dlq1", "dlk1", "dlq2", "dlk2")
 
-    def e2e_step(self):
-        d = {k: v.to(self.out.device, non_blocking=True) for k, v in self.host.items()}
+    def e2e_inputs(self):
+        return dict(self.t)
+
+    def e2e_outputs(self):
+        return [self.grads[n] for n in self.GRADS]
+
+    def e2e_compute(self, d, outs):
         self.bd.diffattn_v1_fwd(*self.args(d), self.li, out=self.out, save=True, saves=self.saves,
                                 workspace=self.fws)
         self.bd.diffattn_v1_bwd(*self.args(d), self.li, self.out, d["dy"], self.saves,
-                                grads=self.grads, workspace=self.ws,
+                                grads=dict(zip(self.GRADS, outs)), workspace=self.ws,
                                 deterministic=self.deterministic)
-        for k, v in self.grads.items():
-            self.host_g[k].copy_(v, non_blocking=True)
 
 
 class V1FwdBwdDet(V1FwdBwd):
@@ -272,17 +273,15 @@ class V2Fwd(Workload):
         t = self.t
         self.bd.diffattn_v2_fwd(t["q"], t["k"], t["v"], gate=self.gate, out=self.out)
 
-    def e2e_setup(self):
-        self.host = {k: v.cpu().pin_memory() for k, v in self.t.items()}
-        self.host_out = torch.empty(self.out.shape, dtype=self.out.dtype).pin_memory()
-        self.h2d = sum(v.numel() * v.element_size() for v in self.host.values())
-        self.d2h = self.host_out.numel() * self.host_out.element_size()
+    def e2e_inputs(self):
+        return dict(self.t)
 
-    def e2e_step(self):
-        d = {k: v.to(self.out.device, non_blocking=True) for k, v in self.host.items()}
+    def e2e_outputs(self):
+        return [self.out]
+
+    def e2e_compute(self, d, outs):
         self.bd.diffattn_v2_fwd(d["q"], d["k"], d["v"], x=d["x"], w_lambda=d["w_lambda"],
-                                out=self.out, workspace=self.ws)
-        self.host_out.copy_(self.out, non_blocking=True)
+                                out=outs[0], workspace=self.ws)
 
     def oracle_sample(self, big=True):
         from oracle import diffattn_oracle as orc
@@ -343,16 +342,19 @@ class V2FwdBwd(V2Fwd):
     def dominant_work(self):
         return v2_bwd_flops(self.B, self.N, self.h, self.d)
 
-    def e2e_setup(self):
-        self.host = {k: v.cpu().pin_memory() for k, v in self.t.items()}
-        self.host_g = {k: torch.empty(v.shape, dtype=v.dtype).pin_memory() for k, v in self.grads.items()}
-        self.h2d = sum(v.numel() * v.element_size() for v in self.host.values())
-        self.d2h = sum(v.numel() * v.element_size() for v in self.host_g.values())
+    def e2e_inputs(self):
+        return dict(self.t)
 
-    def e2e_step(self):
-        self._step({k: v.to(self.out.device, non_blocking=True) for k, v in self.host.items()})
-        for k, v in self.grads.items():
-            self.host_g[k].copy_(v, non_blocking=True)
+    def e2e_outputs(self):
+        return [self.grads[n] for n in sorted(self.grads)]
+
+    def e2e_compute(self, d, outs):
+        t = d
+        self.bd.diffattn_v2_fwd(t["q"], t["k"], t["v"], x=t["x"], w_lambda=t["w_lambda"], out=self.out,
+                                save=True, saves=self.saves, workspace=self.ws)
+        self.bd.diffattn_v2_bwd(t["q"], t["k"], t["v"], t["dout"], self.saves, x=t["x"],
+                                w_lambda=t["w_lambda"], grads=dict(zip(sorted(self.grads), outs)),
+                                workspace=self.bws)
 
     def oracle_sample(self, big=True):
         """fp64 oracle backward on a bounded sample: one (batch, K/V group) of
@@ -396,6 +398,16 @@ class GroupedFwd(Workload):
         self.bd.diffattn_grouped_fwd(t["q"], t["k"], t["v"], self.ratio, x=t["x"], w_lambda=t["w_lambda"],
                                      out=self.out, workspace=self.ws)
 
+    def e2e_inputs(self):
+        return dict(self.t)
+
+    def e2e_outputs(self):
+        return [self.out]
+
+    def e2e_compute(self, d, outs):
+        self.bd.diffattn_grouped_fwd(d["q"], d["k"], d["v"], self.ratio, x=d["x"], w_lambda=d["w_lambda"],
+                                     out=outs[0], workspace=self.ws)
+
     def oracle_sample(self, big=True):
         from oracle import diffattn_oracle as orc
         rows = np.sort(np.random.default_rng(0).choice(self.N, 256 if big else 48, replace=False))
@@ -435,6 +447,21 @@ class V2Decode(Workload):
         self.bd.diffattn_v2_decode(t["q"], t["k_cache"], t["v_cache"], x=t["x"],
                                    w_lambda=t["w_lambda"], out=self.out, workspace=self.ws)
 
+    # end to end: the KV cache is the model's resident state; each step
+    # uploads the new tokens' queries and gate inputs and reads the output
+    RESIDENT = ("k_cache", "v_cache", "seqlens")
+
+    def e2e_inputs(self):
+        return {k: v for k, v in self.t.items() if k not in self.RESIDENT}
+
+    def e2e_outputs(self):
+        return [self.out]
+
+    def e2e_compute(self, d, outs):
+        t = self.t
+        self.bd.diffattn_v2_decode(d["q"], t["k_cache"], t["v_cache"], x=d["x"], w_lambda=d["w_lambda"],
+                                   out=outs[0], workspace=self.ws)
+
     def oracle_sample(self, big=True):
         from oracle import diffattn_oracle as orc
         t0 = time.perf_counter()
@@ -473,6 +500,19 @@ class V1Decode(Workload):
         self.bd.diffattn_v1_decode(t["q1"], t["q2"], t["k1_cache"], t["k2_cache"], t["v_cache"],
                                    t["lq1"], t["lk1"], t["lq2"], t["lk2"], self.li, out=self.out,
                                    workspace=self.ws)
+
+    RESIDENT = ("k1_cache", "k2_cache", "v_cache", "seqlens")
+
+    def e2e_inputs(self):
+        return {k: v for k, v in self.t.items() if k not in self.RESIDENT}
+
+    def e2e_outputs(self):
+        return [self.out]
+
+    def e2e_compute(self, d, outs):
+        t = self.t
+        self.bd.diffattn_v1_decode(d["q1"], d["q2"], t["k1_cache"], t["k2_cache"], t["v_cache"], d["lq1"],
+                                   d["lk1"], d["lq2"], d["lk2"], self.li, out=outs[0], workspace=self.ws)
 
     def oracle_sample(self, big=True):
         from oracle import diffattn_oracle as orc
@@ -642,6 +682,77 @@ def aggregate(total_ms, steps, work_per_step, unit_scale, ws, device):
     return ms, work_per_step * ws / (ms / 1e3) / unit_scale
 
 
+def run_e2e(main, steps, warm=2, n_up=1):
+    """End-to-end steps through the public API.  Every step uploads its
+    inputs from pinned host memory, runs the call and reads its outputs back
+    into pinned host memory.  Two device buffer sets and three streams
+    (upload, compute, download) let step i+1's upload and step i-1's download
+    run under step i's kernels, as a serving loop would; every step still
+    moves all of its bytes inside the timed region.  Returns (ms per step,
+    h2d bytes per step, d2h bytes per step)."""
+    src = main.e2e_inputs()
+    tmpl = main.e2e_outputs()
+    host_in = {k: v.cpu().pin_memory() for k, v in src.items()}
+    dev_in = [{k: torch.empty_like(v) for k, v in src.items()} for _ in range(2)]
+    dev_out = [[torch.empty_like(t) for t in tmpl] for _ in range(2)]
+    host_out = [[torch.empty(t.shape, dtype=t.dtype).pin_memory() for t in tmpl] for _ in range(2)]
+    comp = torch.cuda.current_stream()
+    ups = [torch.cuda.Stream() for _ in range(n_up)]
+    down = torch.cuda.Stream()
+    ev_in = [[torch.cuda.Event() for _ in range(n_up)] for _ in range(2)]  # slot's inputs uploaded
+    ev_done = [torch.cuda.Event() for _ in range(2)]  # slot's step computed
+    ev_out = [torch.cuda.Event() for _ in range(2)]   # slot's outputs downloaded
+    # uploads in chunks of about 32 MB, spread over n_up streams (more than
+    # one stream measured no faster: the host link runs at about 180 GB/s)
+    chunks = []
+    for k, v in host_in.items():
+        flat = v.view(-1)
+        step_el = max(1, (32 << 20) // v.element_size())
+        for a in range(0, flat.numel(), step_el):
+            chunks.append((k, a, min(flat.numel(), a + step_el)))
+
+    def upload(i):
+        s = i % 2
+        for u, st in enumerate(ups):
+            with torch.cuda.stream(st):
+                if i >= 2:
+                    st.wait_event(ev_done[s])  # step i-2 has read this slot's inputs
+                for c, (k, a, b) in enumerate(chunks):
+                    if c % n_up == u:
+                        dev_in[s][k].view(-1)[a:b].copy_(host_in[k].view(-1)[a:b], non_blocking=True)
+                ev_in[s][u].record(st)
+
+    def step(i):
+        s = i % 2
+        for e in ev_in[s]:
+            comp.wait_event(e)
+        if i >= 2:
+            comp.wait_event(ev_out[s])  # step i-2's outputs have been read back
+        main.e2e_compute(dev_in[s], dev_out[s])
+        ev_done[s].record(comp)
+        with torch.cuda.stream(down):
+            down.wait_event(ev_done[s])
+            for o, h in zip(dev_out[s], host_out[s]):
+                h.copy_(o, non_blocking=True)
+            ev_out[s].record(down)
+
+    def run(n):
+        upload(0)
+        for i in range(n):
+            if i + 1 < n:
+                upload(i + 1)
+            step(i)
+        torch.cuda.synchronize()
+
+    run(warm)
+    t0 = time.perf_counter()
+    run(steps)
+    ms = (time.perf_counter() - t0) * 1e3 / steps
+    h2d = sum(v.numel() * v.element_size() for v in host_in.values())
+    d2h = sum(t.numel() * t.element_size() for t in tmpl)
+    return ms, h2d, d2h
+
+
 def time_steps(fn, steps, flush, stream):
     """CUDA-event time of each of `steps` calls of fn (L2 flushed between
     calls, outside the timed events).  Returns per-step milliseconds."""
@@ -712,19 +823,14 @@ def run_ours(args, ws, rank, local):
 
     # end-to-end through the public API with host buffers
     e2e = None
-    if hasattr(main, "e2e_setup"):
-        main.e2e_setup()
-        for _ in range(2):
-            main.e2e_step()
-        torch.cuda.synchronize()
-        t0 = time.perf_counter()
-        for _ in range(args.steps):
-            main.e2e_step()
-        torch.cuda.synchronize()
-        e_ms = (time.perf_counter() - t0) * 1e3 / args.steps
+    if hasattr(main, "e2e_compute"):
+        e_ms, h2d, d2h = run_e2e(main, args.steps)
         e2e = {"value": round(main.scale(e_ms / 1e3) * ws, 3), "unit": main.unit,
-               "ms_per_step": round(e_ms, 4), "h2d_bytes_per_step": main.h2d,
-               "d2h_bytes_per_step": main.d2h}
+               "ms_per_step": round(e_ms, 4), "h2d_bytes_per_step": h2d,
+               "d2h_bytes_per_step": d2h,
+               "pipeline": "2 buffer sets; upload, compute and download streams overlap across steps"}
+        if hasattr(main, "RESIDENT"):
+            e2e["resident_state"] = list(main.RESIDENT)
 
     rows = {}
     if not args.no_rows:
