@@ -49,13 +49,13 @@ bool encode_tmap_bf16_4d(CUtensorMap* map, const da_t4& t, int B, int N, int H, 
   return r == CUDA_SUCCESS;
 }
 
-bool encode_tmap_f32_4d(CUtensorMap* map, void* ptr, int B, int N, int H, int D, int rows) {
+bool encode_tmap_f32_4d(CUtensorMap* map, void* ptr, int B, int N, int H, int D, int rows, int box_d) {
   if (!tma_available()) return false;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(H),
                         static_cast<cuuint64_t>(N), static_cast<cuuint64_t>(B)};
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 4, static_cast<cuuint64_t>(H) * D * 4,
                            static_cast<cuuint64_t>(N) * H * D * 4};
-  cuuint32_t box[4] = {static_cast<cuuint32_t>(D), 1, static_cast<cuuint32_t>(rows), 1};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(box_d > 0 ? box_d : D), 1, static_cast<cuuint32_t>(rows), 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ptr, dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,
@@ -63,13 +63,13 @@ bool encode_tmap_f32_4d(CUtensorMap* map, void* ptr, int B, int N, int H, int D,
   return r == CUDA_SUCCESS;
 }
 
-bool encode_tmap_f32_slots(CUtensorMap* map, void* ptr, int units, int slots, int rows, int D) {
+bool encode_tmap_f32_slots(CUtensorMap* map, void* ptr, int units, int slots, int rows, int D, int box_d) {
   if (!tma_available()) return false;
   cuuint64_t dims[4] = {static_cast<cuuint64_t>(D), static_cast<cuuint64_t>(rows),
                         static_cast<cuuint64_t>(slots), static_cast<cuuint64_t>(units)};
   cuuint64_t strides[3] = {static_cast<cuuint64_t>(D) * 4, static_cast<cuuint64_t>(rows) * D * 4,
                            static_cast<cuuint64_t>(slots) * rows * D * 4};
-  cuuint32_t box[4] = {static_cast<cuuint32_t>(D), static_cast<cuuint32_t>(rows), 1, 1};
+  cuuint32_t box[4] = {static_cast<cuuint32_t>(box_d > 0 ? box_d : D), static_cast<cuuint32_t>(rows), 1, 1};
   cuuint32_t estr[4] = {1, 1, 1, 1};
   CUresult r = g_encode(map, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 4, ptr, dims, strides, box, estr,
                         CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_NONE,

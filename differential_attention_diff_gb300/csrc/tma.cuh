@@ -18,12 +18,12 @@ namespace da {
 // out-of-range rows read as zero.
 bool encode_tmap_bf16_4d(CUtensorMap* map, const da_t4& t, int B, int N, int H,
                          int D, int rows);
-// A 4-D fp32 tensor map over a contiguous [B, N, H, D] tensor, box = {D, 1,
-// rows, 1}, no swizzle (used for reduce-adds of fp32 tiles).
-bool encode_tmap_f32_4d(CUtensorMap* map, void* ptr, int B, int N, int H, int D, int rows);
+// A 4-D fp32 tensor map over a contiguous [B, N, H, D] tensor, box = {box_d
+// (0: D), 1, rows, 1}, no swizzle (used for reduce-adds of fp32 tiles).
+bool encode_tmap_f32_4d(CUtensorMap* map, void* ptr, int B, int N, int H, int D, int rows, int box_d = 0);
 // A 4-D fp32 tensor map over contiguous [units, slots, rows, D] tiles, box =
-// one whole [rows, D] tile, no swizzle (per-tile slots stored by TMA).
-bool encode_tmap_f32_slots(CUtensorMap* map, void* ptr, int units, int slots, int rows, int D);
+// {box_d (0: D), rows, 1, 1}, no swizzle (per-tile slots stored by TMA).
+bool encode_tmap_f32_slots(CUtensorMap* map, void* ptr, int units, int slots, int rows, int D, int box_d = 0);
 
 // ---------------------------------------------------------------- device ---
 // Every wait below is bounded: after kSpinLimit polls it records

@@ -26,12 +26,14 @@
 //        dP^T = V dO^T         (TMEM, 64 columns)
 //        softmax warps (thread = key row): P = exp2(S^T s log2e - lse2),
 //          dS^T = sigma s P (dP^T - D), Psig^T = sigma P  (sigma = 1 or
-//          -lambda), both as bf16 rows into shared memory
-//        dQ^T = K^T dS^T       (TMEM, reusing the dP^T columns) -> staged in
-//                               shared memory, TMA reduce-add into the fp32
-//                               accumulator in the workspace
-//        dV  += Psig^T dO      (TMEM, 256 columns)
-//        dK  += dS^T Q         (TMEM, 128 columns)
+//          -lambda), both as bf16 over the S^T columns just read (TMEM),
+//          dS^T also into shared memory
+//        dQ^T = K^T dS^T       (TMEM, reusing the dP^T columns) -> read by the
+//                               dQ warps, staged in shared memory in two
+//                               halves and added to the fp32 accumulator
+//                               with TMA reduce-adds
+//        dV  += Psig^T dO      (TMEM, 256 columns; A operand from TMEM)
+//        dK  += dS^T Q         (TMEM, 128 columns; A operand from TMEM)
 //     At the end each CTA writes its dK; the dV halves of the two streams are
 //     summed through distributed shared memory and written as bf16;
 //  3. finalize: dQ accumulators -> bf16, and the lambda-vector gradients.
@@ -41,10 +43,14 @@
 // reading an accumulator, so no result depends on the order in which CTAs
 // finish.
 //
-// TMEM: [0,256) dV, [256,384) dK, [384,448) S^T, [448,512) dP^T / dQ^T.
-// SMEM: K 32 KB, V 64 KB, 2 stages of (Q 16 KB, dO 32 KB), Psig^T and dS^T
-//       16 KB each, lse2 and D of both stages (1 KB); every operand in 128-byte-swizzled
-//       64-column boxes (used K-major or MN-major by the MMAs as needed).
+// Warp roles (320 threads): 0-3 softmax / dS and the epilogue, 4-7 dQ readback
+// and reduce, 8 TMA producer, 9 MMA issuer.  TMEM: [0,256) dV, [256,384) dK,
+// [384,448) S^T (then Psig^T and dS^T), [448,512) dP^T / dQ^T.  TMEM is full,
+// so S^T and dP^T are single-buffered; taking the dQ readback off the softmax
+// warps keeps it out of the per-tile chain.
+// SMEM: K 32 KB, V 64 KB, 2 stages of (Q 16 KB, dO 32 KB), dQ staging of one
+//       64-feature half (16 KB), dS^T 16 KB, lse2 and D of both stages (1 KB);
+//       every bf16 operand in 128-byte-swizzled 64-column boxes.
 #include <type_traits>
 
 #include "kernels.h"
@@ -57,7 +63,7 @@ namespace {
 constexpr int kKT = 128;   // keys per item
 constexpr int kQT = 64;    // queries per iteration
 constexpr int kDqk = 128, kDv = 256;
-constexpr int kThreads = 192;
+constexpr int kThreads = 320;
 
 constexpr int kBoxK = 128 * 128;   // 64 columns x 128 rows of bf16
 constexpr int kBoxQ = 64 * 128;    // 64 columns x 64 rows
@@ -67,15 +73,15 @@ constexpr int kOffStage = kOffV + 4 * kBoxK;       // 96 KB
 constexpr int kStageQ = 0;                         // 2 boxes (16 KB)
 constexpr int kStageDO = 2 * kBoxQ;                // 4 boxes (32 KB)
 constexpr int kStageBytes = 6 * kBoxQ;             // 48 KB
-constexpr int kOffP = kOffStage + 2 * kStageBytes;
-constexpr int kOffDS = kOffP + kBoxK;              // 16 KB each
+constexpr int kOffStg = kOffStage + 2 * kStageBytes;  // dQ staging: fp32 [64 queries][64 features]
+constexpr int kOffDS = kOffStg + kBoxK;            // 16 KB each
 constexpr int kOffLse = kOffDS + kBoxK;            // [stage] {lse2[64], D[64]}: 512 B each
 constexpr int kOffBar = kOffLse + 1024;
 constexpr int kSmemBytes = kOffBar + 512 + 1024;   // 231936 <= 232448
 
 enum {
   B_KV = 0, B_QFULL, B_QFULL1, B_QEMPTY, B_QEMPTY1, B_SFULL, B_DPFULL, B_PFULL, B_DQFULL,
-  B_DQFREE, B_PBFREE, B_ACC, B_RTR, B_DATA, B_STG, B_STGFREE, B_COUNT
+  B_DQFREE, B_ACC, B_RTR, B_DATA, B_STG0, B_STG1, B_FREE0, B_FREE1, B_COUNT
 };
 
 __host__ __device__ constexpr uint32_t idesc2(int M, int N, int a_mn, int b_mn) {
@@ -85,8 +91,8 @@ __host__ __device__ constexpr uint32_t idesc2(int M, int N, int a_mn, int b_mn) 
 }
 constexpr uint32_t kIdS = idesc2(128, 64, 0, 0);    // K (K-major) x Q (K-major)
 constexpr uint32_t kIdDP = idesc2(128, 64, 0, 0);   // V (K-major) x dO (K-major)
-constexpr uint32_t kIdDV = idesc2(128, 256, 0, 1);  // Psig^T (K-major) x dO (MN-major)
-constexpr uint32_t kIdDK = idesc2(128, 128, 0, 1);  // dS^T (K-major) x Q (MN-major)
+constexpr uint32_t kIdDV = idesc2(128, 256, 0, 1);  // Psig^T (TMEM) x dO (MN-major)
+constexpr uint32_t kIdDK = idesc2(128, 128, 0, 1);  // dS^T (TMEM) x Q (MN-major)
 constexpr uint32_t kIdDQ = idesc2(128, 64, 1, 1);   // K^T (MN-major) x dS^T (MN-major)
 
 __device__ __forceinline__ uint64_t globaltimer() {
@@ -358,7 +364,6 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
   const uint32_t rank = cluster_rank();  // stream index
   const uint32_t partner = rank ^ 1u;
   // items: heaviest (first key tiles: most query tiles) first
-  const int n_kt = (a.N + kKT - 1) / kKT;
   const int n_qt = w.npad / kQT;
   Item it;
   {
@@ -371,7 +376,6 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
     it.i0 = it.kt * (kKT / kQT);
     it.n_it = n_qt - it.i0;
   }
-  (void)n_kt;
   const CUtensorMap* tq = rank == 0 ? &tm_q1 : &tm_q2;
   const CUtensorMap* tk = rank == 0 ? &tm_k1 : &tm_k2;
   const float* lse2 = w.lse2[rank];
@@ -389,12 +393,13 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
     mbar_init(sh.bar(B_PFULL), 128);
     mbar_init(sh.bar(B_DQFULL), 1);
     mbar_init(sh.bar(B_DQFREE), 128);
-    mbar_init(sh.bar(B_PBFREE), 1);
     mbar_init(sh.bar(B_ACC), 1);
     mbar_init(sh.bar(B_RTR), 128);
     mbar_init(sh.bar(B_DATA), 128);
-    mbar_init(sh.bar(B_STG), 128);
-    mbar_init(sh.bar(B_STGFREE), 1);
+    for (int h = 0; h < 2; ++h) {
+      mbar_init(sh.bar(B_STG0 + h), 64);
+      mbar_init(sh.bar(B_FREE0 + h), 1);
+    }
     *sh.abort_flag() = 0;
     fence_mbar_init();
   }
@@ -402,15 +407,16 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
     const float lam = lambda_dev(a, lane, nullptr, nullptr);
     if (lane == 0) *sh.lam() = lam;
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(sh.tmem_slot()), 512);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     prefetch_tmap(tq);
     prefetch_tmap(tk);
     prefetch_tmap(&tm_v);
     prefetch_tmap(&tm_do);
+    prefetch_tmap(tdq);
   }
   tc_fence_before();
   __syncthreads();
@@ -419,7 +425,7 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
   const uint32_t tmem = *sh.tmem_slot();
   const uint32_t T_DV = tmem, T_DK = tmem + 256, T_S = tmem + 384, T_DP = tmem + 448;
 
-  if (warp == 4) {
+  if (warp == 8) {
     // ---------------------------------------------------- TMA producer ----
     if (lane == 0) {
       mbar_arrive_expect_tx(sh.bar(B_KV), 6 * kBoxK);
@@ -428,9 +434,14 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
       for (int box = 0; box < 4; ++box)
         tma_load_4d(sh.base + kOffV + box * kBoxK, &tm_v, sh.bar(B_KV), box * 64, it.h, it.kt * kKT, it.b);
       const size_t srow = (static_cast<size_t>(it.b) * a.H + it.h) * w.npad;
+      int last = -1;
+      bool ok = true;
       for (int k = 0; k < it.n_it; ++k) {
         const int st = k & 1, use = k >> 1;
-        if (use > 0 && !wait_bar(sh, sh.bar(B_QEMPTY + st), (use - 1) & 1, a.status, 0x4001)) break;
+        if (use > 0 && !wait_bar(sh, sh.bar(B_QEMPTY + st), (use - 1) & 1, a.status, 0x4001)) {
+          ok = false;
+          break;
+        }
         const int q0 = (it.i0 + k) * kQT;
         const uint32_t sb = sh.base + kOffStage + st * kStageBytes;
         mbar_arrive_expect_tx(sh.bar(B_QFULL + st), 6 * kBoxQ + 512);
@@ -441,9 +452,19 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
         const uint32_t lb = sh.base + kOffLse + st * 512;
         bulk_load(lb, lse2 + srow + q0, 256, sh.bar(B_QFULL + st));
         bulk_load(lb + 256, Dv + srow + q0, 256, sh.bar(B_QFULL + st));
+        last = k;
+      }
+      if (!ok) {
+        // give the loads already issued (bounded) time to land before exit
+        const uint64_t t0 = globaltimer();
+        while (globaltimer() - t0 < 200000000ull && !mbar_try_wait(sh.bar(B_KV), 0)) {
+        }
+        for (int k = last; k >= 0 && k > last - 2; --k)
+          while (globaltimer() - t0 < 400000000ull && !mbar_try_wait(sh.bar(B_QFULL + (k & 1)), (k >> 1) & 1)) {
+          }
       }
     }
-  } else if (warp == 5) {
+  } else if (warp == 9) {
     // ------------------------------------------------------ MMA issuer ----
     if (lane == 0) {
       bool ok = wait_bar(sh, sh.bar(B_KV), 0, a.status, 0x4101);
@@ -458,6 +479,7 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
           const uint32_t offb = (kk >> 2) * kBoxQ + (kk & 3) * 32;
           tc_mma_ss(T_S, sdesc_sw128(kA + offa, 16, 1024), sdesc_sw128(qb + offb, 16, 1024), kIdS, kk > 0);
         }
+        tc_commit(sh.bar(B_SFULL));
       };
       auto issue_dp = [&](int k) {  // dP^T = V dO^T
         const uint32_t db = stage(k) + kStageDO;
@@ -467,54 +489,112 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
           const uint32_t offb = (kk >> 2) * kBoxQ + (kk & 3) * 32;
           tc_mma_ss(T_DP, sdesc_sw128(vA + offa, 16, 1024), sdesc_sw128(db + offb, 16, 1024), kIdDP, kk > 0);
         }
+        tc_commit(sh.bar(B_DPFULL));
       };
-      const uint32_t pA = sh.base + kOffP, dsA = sh.base + kOffDS;
-      for (int k = 0; k < it.n_it && ok; ++k) {
-        const int ph = k & 1;
-        if (k == 0) {
-          if (!wait_bar(sh, sh.bar(B_QFULL), 0, a.status, 0x4102)) { ok = false; break; }
+      const uint32_t dsA = sh.base + kOffDS;
+      if (ok && it.n_it > 0) {
+        if (wait_bar(sh, sh.bar(B_QFULL), 0, a.status, 0x4102)) {
           tc_fence_after();
           issue_s(0);
-          tc_commit(sh.bar(B_SFULL));
           issue_dp(0);
-          tc_commit(sh.bar(B_DPFULL));
+        } else {
+          ok = false;
         }
+      }
+      for (int k = 0; k < it.n_it && ok; ++k) {
+        const int ph = k & 1;
         if (!wait_bar(sh, sh.bar(B_PFULL), ph, a.status, 0x4103)) { ok = false; break; }
         tc_fence_after();
-        // dQ^T = K^T dS^T  (into the dP^T columns, already consumed)
+        // dQ^T = K^T dS^T  (into the dP^T columns, already read)
 #pragma unroll
         for (int kk = 0; kk < kKT / 16; ++kk)
           tc_mma_ss(T_DP, sdesc_sw128(kA + kk * 2048, kBoxK, 1024), sdesc_sw128(dsA + kk * 2048, kBoxQ, 1024),
                     kIdDQ, kk > 0);
         tc_commit(sh.bar(B_DQFULL));
-        const bool more = k + 1 < it.n_it;
-        // dV += Psig^T dO ; dK += dS^T Q  (so the P / dS buffers free early)
+        // dV += Psig^T dO ; dK += dS^T Q  (Psig^T in S^T columns 0-31, dS^T
+        // in 32-63)
         const uint32_t db = stage(k) + kStageDO, qb = stage(k) + kStageQ;
 #pragma unroll
         for (int kk = 0; kk < kQT / 16; ++kk)
-          tc_mma_ss(T_DV, sdesc_sw128(pA + kk * 32, 16, 1024), sdesc_sw128(db + kk * 2048, kBoxQ, 1024), kIdDV,
-                    (k > 0 || kk > 0) ? 1u : 0u);
+          tc_mma_ts(T_DV, T_S + kk * 8, sdesc_sw128(db + kk * 2048, kBoxQ, 1024), kIdDV, (k > 0 || kk > 0) ? 1u : 0u);
 #pragma unroll
         for (int kk = 0; kk < kQT / 16; ++kk)
-          tc_mma_ss(T_DK, sdesc_sw128(dsA + kk * 32, 16, 1024), sdesc_sw128(qb + kk * 2048, kBoxQ, 1024), kIdDK,
+          tc_mma_ts(T_DK, T_S + 32 + kk * 8, sdesc_sw128(qb + kk * 2048, kBoxQ, 1024), kIdDK,
                     (k > 0 || kk > 0) ? 1u : 0u);
-        tc_commit(sh.bar(B_PBFREE));
         tc_commit(sh.bar(B_QEMPTY + (k & 1)));
-        if (more) {
+        if (k + 1 < it.n_it) {
           if (!wait_bar(sh, sh.bar(B_QFULL + ((k + 1) & 1)), ((k + 1) >> 1) & 1, a.status, 0x4104)) { ok = false; break; }
           tc_fence_after();
+          // S^T(k+1) overwrites Psig^T / dS^T only after dV(k) / dK(k) have
+          // read them (MMAs of one thread run in order)
           issue_s(k + 1);
-          tc_commit(sh.bar(B_SFULL));
+          // dP^T(k+1) overwrites dQ^T(k) once the dQ warps have read it
           if (!wait_bar(sh, sh.bar(B_DQFREE), ph, a.status, 0x4105)) { ok = false; break; }
           tc_fence_after();
           issue_dp(k + 1);
-          tc_commit(sh.bar(B_DPFULL));
         }
       }
       if (ok) tc_commit(sh.bar(B_ACC));
     }
+  } else if (warp >= 4) {
+    // ------------------------------------------------- dQ readback + reduce --
+    // thread = feature of dQ^T (TMEM lane); warps 4-5 stage features 0-63,
+    // warps 6-7 features 64-127, one half at a time through one 16 KB buffer
+    const int r = (warp - 4) * 32 + lane;
+    const uint32_t loff = static_cast<uint32_t>((warp - 4) * 32) << 16;
+    const int half = (warp - 4) >> 1;
+    const int col = r - half * 64;
+    float* stg = reinterpret_cast<float*>(sh.gen + kOffStg);
+    bool ok = true;
+    for (int k = 0; k < it.n_it && ok; ++k) {
+      if (!wait_bar(sh, sh.bar(B_DQFULL), k & 1, a.status, 0x4301)) { ok = false; break; }
+      tc_fence_after();
+      uint32_t qv[64];
+      tmem_ld32(T_DP + loff, *reinterpret_cast<uint32_t(*)[32]>(&qv[0]));
+      tmem_ld32(T_DP + loff + 32, *reinterpret_cast<uint32_t(*)[32]>(&qv[32]));
+      tmem_ld_wait();
+      tc_fence_before();
+      mbar_arrive(sh.bar(B_DQFREE));
+      // the staging buffer alternates between the halves: half 0 of tile k
+      // waits until half 1 of tile k-1 has been read (FREE0), half 1 until
+      // half 0 of tile k has (FREE1).  One barrier per direction completes
+      // once per tile, so no waiter can be two phases away from it even when
+      // the warps that do not issue the copy run a tile ahead of the one that
+      // does (a single barrier shared by both halves would let such a warp
+      // match an older phase of the same parity and overwrite the buffer
+      // while it is still being read).
+      if (half == 0 ? (k > 0 && !wait_bar(sh, sh.bar(B_FREE0), (k - 1) & 1, a.status, 0x4302))
+                    : !wait_bar(sh, sh.bar(B_FREE1), k & 1, a.status, 0x4302)) {
+        ok = false;
+        break;
+      }
+#pragma unroll
+      for (int c = 0; c < kQT; ++c) stg[c * 64 + col] = __uint_as_float(qv[c]);
+      fence_proxy_async_smem();
+      mbar_arrive(sh.bar(B_STG0 + half));
+      bool stg_ok = true;
+      if (col == 0) {
+        stg_ok = wait_bar(sh, sh.bar(B_STG0 + half), k & 1, a.status, 0x4303);
+        if (stg_ok) {
+          // add the [64 queries][64 features] tile into the fp32 accumulator
+          // (rows past N are dropped by the unit), or store it into its slot
+          if (w.det)
+            tma_store_4d(tdq, sh.base + kOffStg, half * 64, 0, dq_slot(it.kt, it.i0 + k, w.n_qt),
+                         it.b * a.H + it.h);
+          else
+            tma_reduce_add_4d(tdq, sh.base + kOffStg, half * 64, it.h, (it.i0 + k) * kQT, it.b);
+          bulk_commit();
+          bulk_wait_read();
+          mbar_arrive(sh.bar(half == 0 ? B_FREE1 : B_FREE0));
+        }
+      }
+      // keep the issuing warp uniform for the warp-collective TMEM loads
+      if ((warp & 1) == 0) stg_ok = __shfl_sync(0xffffffffu, stg_ok, 0);
+      if (!stg_ok) ok = false;
+    }
+    if (col == 0) bulk_wait_all();
   } else {
-    // ------------------------------- softmax / dS / dQ / epilogue ---------
+    // --------------------------------------------- softmax / dS, epilogue --
     const int r = warp * 32 + lane;  // key row within the tile = TMEM lane
     const uint32_t loff = static_cast<uint32_t>(warp * 32) << 16;
     const float lam = *sh.lam();
@@ -524,7 +604,6 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
     const uint64_t sl2x2 = f2(sl2, sl2), sds2 = f2(sds, sds), sig2 = f2(sigma, sigma);
     const int key = it.kt * kKT + r;
     bool ok = true;
-    uint8_t* pbuf = sh.gen + kOffP;
     uint8_t* dsbuf = sh.gen + kOffDS;
     for (int k = 0; k < it.n_it && ok; ++k) {
       const int ph = k & 1;
@@ -532,92 +611,75 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
       if (!wait_bar(sh, sh.bar(B_SFULL), ph, a.status, 0x4201)) { ok = false; break; }
       if (!wait_bar(sh, sh.bar(B_DPFULL), ph, a.status, 0x4202)) { ok = false; break; }
       tc_fence_after();
-      uint32_t sv[64], dp[64];
-      tmem_ld32(T_S + loff, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-      tmem_ld32(T_S + loff + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
-      tmem_ld32(T_DP + loff, *reinterpret_cast<uint32_t(*)[32]>(&dp[0]));
-      tmem_ld32(T_DP + loff + 32, *reinterpret_cast<uint32_t(*)[32]>(&dp[32]));
-      tmem_ld_wait();
       const float4* l2v = reinterpret_cast<const float4*>(sh.gen + kOffLse + (k & 1) * 512);
       const float4* ddv = l2v + 16;
       const bool diag = q0 < it.kt * kKT + kKT;  // a query of this tile may precede a key
-      uint32_t pw[32], dw[32];
-      auto tile = [&](auto masked) {
-        constexpr bool kMask = decltype(masked)::value;
+      uint32_t dkeep[16];  // dS^T of the first half, stored once the second half's S^T is read
 #pragma unroll
-        for (int q4 = 0; q4 < 16; ++q4) {  // 4 queries at a time
-          const float4 lq = l2v[q4];
-          const float4 dq4 = ddv[q4];
-          const int c = q4 * 4;
-          const uint64_t x01 = fma_f32x2(f2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2x2,
-                                         f2(-lq.x, -lq.y));
-          const uint64_t x23 = fma_f32x2(f2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), sl2x2,
-                                         f2(-lq.z, -lq.w));
-          float p0 = fast_exp2(f2_lo(x01)), p1 = fast_exp2(f2_hi(x01));
-          float p2 = fast_exp2(f2_lo(x23)), p3 = fast_exp2(f2_hi(x23));
-          if (kMask) {
-            if (key > q0 + c) p0 = 0.f;
-            if (key > q0 + c + 1) p1 = 0.f;
-            if (key > q0 + c + 2) p2 = 0.f;
-            if (key > q0 + c + 3) p3 = 0.f;
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t sv[32], dp[32];
+        tmem_ld32(T_S + loff + hf * 32, sv);
+        tmem_ld32(T_DP + loff + hf * 32, dp);
+        tmem_ld_wait();
+        uint32_t pw[16], dw[16];
+        auto tile = [&](auto masked) {
+          constexpr bool kMask = decltype(masked)::value;
+#pragma unroll
+          for (int q4 = 0; q4 < 8; ++q4) {  // 4 queries at a time
+            const float4 lq = l2v[hf * 8 + q4];
+            const float4 dq4 = ddv[hf * 8 + q4];
+            const int c = q4 * 4;
+            const int qa = q0 + hf * 32 + c;
+            const uint64_t x01 = fma_f32x2(f2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2x2,
+                                           f2(-lq.x, -lq.y));
+            const uint64_t x23 = fma_f32x2(f2(__uint_as_float(sv[c + 2]), __uint_as_float(sv[c + 3])), sl2x2,
+                                           f2(-lq.z, -lq.w));
+            float p0 = fast_exp2(f2_lo(x01)), p1 = fast_exp2(f2_hi(x01));
+            float p2 = fast_exp2(f2_lo(x23)), p3 = fast_exp2(f2_hi(x23));
+            if (kMask) {
+              if (key > qa) p0 = 0.f;
+              if (key > qa + 1) p1 = 0.f;
+              if (key > qa + 2) p2 = 0.f;
+              if (key > qa + 3) p3 = 0.f;
+            }
+            const uint64_t t01 = add_f32x2(f2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), f2(-dq4.x, -dq4.y));
+            const uint64_t t23 =
+                add_f32x2(f2(__uint_as_float(dp[c + 2]), __uint_as_float(dp[c + 3])), f2(-dq4.z, -dq4.w));
+            const uint64_t p01 = f2(p0, p1), p23 = f2(p2, p3);
+            const uint64_t d01 = mul_f32x2(mul_f32x2(t01, p01), sds2);
+            const uint64_t d23 = mul_f32x2(mul_f32x2(t23, p23), sds2);
+            const uint64_t s01 = mul_f32x2(p01, sig2), s23 = mul_f32x2(p23, sig2);
+            pw[q4 * 2] = pack_bf16x2(f2_lo(s01), f2_hi(s01));
+            pw[q4 * 2 + 1] = pack_bf16x2(f2_lo(s23), f2_hi(s23));
+            dw[q4 * 2] = pack_bf16x2(f2_lo(d01), f2_hi(d01));
+            dw[q4 * 2 + 1] = pack_bf16x2(f2_lo(d23), f2_hi(d23));
           }
-          const uint64_t t01 = add_f32x2(f2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), f2(-dq4.x, -dq4.y));
-          const uint64_t t23 = add_f32x2(f2(__uint_as_float(dp[c + 2]), __uint_as_float(dp[c + 3])), f2(-dq4.z, -dq4.w));
-          const uint64_t p01 = f2(p0, p1), p23 = f2(p2, p3);
-          const uint64_t d01 = mul_f32x2(mul_f32x2(t01, p01), sds2);
-          const uint64_t d23 = mul_f32x2(mul_f32x2(t23, p23), sds2);
-          const uint64_t s01 = mul_f32x2(p01, sig2), s23 = mul_f32x2(p23, sig2);
-          pw[q4 * 2] = pack_bf16x2(f2_lo(s01), f2_hi(s01));
-          pw[q4 * 2 + 1] = pack_bf16x2(f2_lo(s23), f2_hi(s23));
-          dw[q4 * 2] = pack_bf16x2(f2_lo(d01), f2_hi(d01));
-          dw[q4 * 2 + 1] = pack_bf16x2(f2_lo(d23), f2_hi(d23));
-        }
-      };
-      if (diag) tile(std::true_type{});
-      else tile(std::false_type{});
-      // the P / dS buffers are free once dV(k-1) and dK(k-1) have read them
-      // and the TMA reduce has read the dQ tile staged there after them
-      if (k > 0 && !wait_bar(sh, sh.bar(B_PBFREE), (k - 1) & 1, a.status, 0x4203)) { ok = false; break; }
-      if (k > 0 && !wait_bar(sh, sh.bar(B_STGFREE), (k - 1) & 1, a.status, 0x4208)) { ok = false; break; }
+        };
+        if (diag) tile(std::true_type{});
+        else tile(std::false_type{});
+        // Psig^T over S^T columns this thread has already read
+        tmem_st16(T_S + loff + hf * 16, pw);
+        // dS^T for the dQ^T MMA (its previous reader, dQ^T of the tile
+        // before, completed before S^T of this tile was signalled)
 #pragma unroll
-      for (int ch = 0; ch < 8; ++ch) {
-        const int off = r * 128 + ((ch ^ (r & 7)) << 4);
-        *reinterpret_cast<uint4*>(pbuf + off) = make_uint4(pw[ch * 4], pw[ch * 4 + 1], pw[ch * 4 + 2], pw[ch * 4 + 3]);
-        *reinterpret_cast<uint4*>(dsbuf + off) = make_uint4(dw[ch * 4], dw[ch * 4 + 1], dw[ch * 4 + 2], dw[ch * 4 + 3]);
+        for (int cc = 0; cc < 4; ++cc) {
+          const int ch = hf * 4 + cc;
+          const int off = r * 128 + ((ch ^ (r & 7)) << 4);
+          *reinterpret_cast<uint4*>(dsbuf + off) = make_uint4(dw[cc * 4], dw[cc * 4 + 1], dw[cc * 4 + 2], dw[cc * 4 + 3]);
+        }
+        if (hf == 0) {
+#pragma unroll
+          for (int e = 0; e < 16; ++e) dkeep[e] = dw[e];
+        } else {
+          tmem_st16(T_S + loff + 32, dkeep);
+          tmem_st16(T_S + loff + 48, dw);
+        }
       }
+      tmem_st_wait();
       fence_proxy_async_smem();
       tc_fence_before();
       mbar_arrive(sh.bar(B_PFULL));
-      // dQ^T rows: lane = feature d of dQ; 64 queries
-      if (!wait_bar(sh, sh.bar(B_DQFULL), ph, a.status, 0x4204)) { ok = false; break; }
-      tc_fence_after();
-      uint32_t qv[64];
-      tmem_ld32(T_DP + loff, *reinterpret_cast<uint32_t(*)[32]>(&qv[0]));
-      tmem_ld32(T_DP + loff + 32, *reinterpret_cast<uint32_t(*)[32]>(&qv[32]));
-      tmem_ld_wait();
-      tc_fence_before();
-      mbar_arrive(sh.bar(B_DQFREE));
-      // stage the dQ tile [64 queries][128 features] fp32 in the P / dS
-      // buffers once dV(k) / dK(k) have read them; one thread adds it to the
-      // fp32 accumulator with a TMA reduce (rows past N are dropped)
-      if (!wait_bar(sh, sh.bar(B_PBFREE), ph, a.status, 0x4209)) { ok = false; break; }
-      float* stage_dq = reinterpret_cast<float*>(pbuf);
-#pragma unroll
-      for (int c = 0; c < kQT; ++c) stage_dq[c * kDqk + r] = __uint_as_float(qv[c]);
-      fence_proxy_async_smem();
-      mbar_arrive(sh.bar(B_STG));
-      if (r == 0) {
-        if (!wait_bar(sh, sh.bar(B_STG), ph, a.status, 0x420A)) { ok = false; break; }
-        if (w.det)
-          tma_store_4d(tdq, sh.base + kOffP, 0, 0, dq_slot(it.kt, it.i0 + k, w.n_qt), it.b * a.H + it.h);
-        else
-          tma_reduce_add_4d(tdq, sh.base + kOffP, 0, it.h, q0, it.b);
-        bulk_commit();
-        bulk_wait_read();
-        mbar_arrive(sh.bar(B_STGFREE));
-      }
     }
-    if (r == 0) bulk_wait_all();
     // ----------------------------------------------------------- epilogue --
     if (ok && wait_bar(sh, sh.bar(B_ACC), 0, a.status, 0x4205)) {
       tc_fence_after();
@@ -694,7 +756,7 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
   __syncthreads();
   cluster_sync();
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, 512);
+  if (warp == 9) tmem_dealloc(tmem, 512);
 }
 
 // -------------------------------------------------------------- finalize --
@@ -813,12 +875,13 @@ cudaError_t launch_v1_bwd(const V1BwdArgs& a, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   CUtensorMap tdq1, tdq2;
+  // dQ tiles leave in two 64-feature halves
   if (w.det) {
-    if (!encode_tmap_f32_slots(&tdq1, w.dq[0], a.B * a.H, w.n_slots, kQT, kDqk) ||
-        !encode_tmap_f32_slots(&tdq2, w.dq[1], a.B * a.H, w.n_slots, kQT, kDqk))
+    if (!encode_tmap_f32_slots(&tdq1, w.dq[0], a.B * a.H, w.n_slots, kQT, kDqk, 64) ||
+        !encode_tmap_f32_slots(&tdq2, w.dq[1], a.B * a.H, w.n_slots, kQT, kDqk, 64))
       return cudaErrorInvalidValue;
-  } else if (!encode_tmap_f32_4d(&tdq1, w.dq[0], a.B, a.N, a.H, kDqk, kQT) ||
-             !encode_tmap_f32_4d(&tdq2, w.dq[1], a.B, a.N, a.H, kDqk, kQT)) {
+  } else if (!encode_tmap_f32_4d(&tdq1, w.dq[0], a.B, a.N, a.H, kDqk, kQT, 64) ||
+             !encode_tmap_f32_4d(&tdq2, w.dq[1], a.B, a.N, a.H, kDqk, kQT, 64)) {
     return cudaErrorInvalidValue;
   }
   e = cudaLaunchKernelEx(&cfg, v1_bwd_main_kernel, tq1, tq2, tk1, tk2, tv, tdo, tdq1, tdq2, a, w);
