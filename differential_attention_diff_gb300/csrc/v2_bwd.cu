@@ -673,81 +673,117 @@ v2_bwd_finalize_kernel(V2BwdArgs a, BwdWs w) {
 }
 
 // ------------------------------------------------- gate-projection grads --
-// dX[t, c] = sum_p dz[t, p] W[c, p]: a thread owns two columns (W rows in
-// registers), a block 64 tokens x 256 columns; dz rows staged in shared
-// memory and read as broadcasts.
-constexpr int kDxTok = 64;
+// Both are 2 T d_model h FLOP on the FMA pipes with register tiles fed from
+// shared memory (fp32 throughout, as exact as the gate itself):
+//   dX[t, c] = sum_p dz[t, p] W[c, p]
+//   dW[c, p] = sum_t X[t, c] dz[t, p]   (per-chunk partial sums, then a
+//                                        fixed-order reduction)
+constexpr int kGT = 64;    // tokens per staged tile
+constexpr int kGC = 128;   // d_model columns per block
+constexpr int kGP = 32;    // gate heads per block (dW) / per pass (dX)
 
-template <int HC>
-__global__ void __launch_bounds__(128)
+// dX: block = 64 tokens x 128 columns, 256 threads; thread = 8 tokens x 4
+// consecutive columns (32 accumulators).  W^T slice [p][128 columns] and the
+// dz tile [64 tokens][p] in shared memory; p in passes of 32.
+__global__ void __launch_bounds__(256)
 v2_bwd_dx_kernel(int T, int d_model, int h, const float* __restrict__ dz,
                  const __nv_bfloat16* __restrict__ W, __nv_bfloat16* __restrict__ dx) {
-  __shared__ float s_dz[kDxTok][HC];
-  const int t0 = blockIdx.x * kDxTok;
-  const int c = blockIdx.y * 256 + threadIdx.x * 2;
-  for (int i = threadIdx.x; i < kDxTok * HC; i += 128) {
-    const int t = i / HC, p = i % HC;
-    s_dz[t][p] = (t0 + t < T && p < h) ? dz[static_cast<int64_t>(t0 + t) * h + p] : 0.f;
-  }
-  float w0[HC], w1[HC];
+  __shared__ float s_w[kGP][kGC];
+  __shared__ float s_z[kGT][kGP + 1];
+  const int tid = threadIdx.x, tx = tid & 31, ty = tid >> 5;
+  const int t0 = blockIdx.x * kGT, c0 = blockIdx.y * kGC;
+  float acc[8][4];
 #pragma unroll
-  for (int p = 0; p < HC; ++p) {
-    const bool in = c < d_model && p < h;
-    w0[p] = in ? __bfloat162float(W[static_cast<int64_t>(c) * h + p]) : 0.f;
-    w1[p] = in ? __bfloat162float(W[static_cast<int64_t>(c + 1) * h + p]) : 0.f;
-  }
-  __syncthreads();
-  if (c >= d_model) return;
-  const int tn = min(kDxTok, T - t0);
-#pragma unroll 1
-  for (int t = 0; t < tn; ++t) {
-    float a0 = 0.f, a1 = 0.f;
-#pragma unroll
-    for (int p = 0; p < HC; ++p) {
-      a0 = fmaf(s_dz[t][p], w0[p], a0);
-      a1 = fmaf(s_dz[t][p], w1[p], a1);
-    }
-    *reinterpret_cast<uint32_t*>(dx + static_cast<int64_t>(t0 + t) * d_model + c) = pack_bf16x2(a0, a1);
-  }
-}
-
-// dW partials: block = (64 columns, one chunk of kDwChunk tokens); thread =
-// (column, 16 gate heads); dz staged 128 tokens at a time.
-constexpr int kDwSub = 128;
-
-__global__ void __launch_bounds__(256)
-v2_bwd_dw_partial_kernel(int T, int d_model, int h, const float* __restrict__ dz,
-                         const __nv_bfloat16* __restrict__ X, float* __restrict__ part) {
-  __shared__ float s_dz[kDwSub][64];
-  const int cl = threadIdx.x & 63, pg = threadIdx.x >> 6;
-  const int c = blockIdx.x * 64 + cl;
-  const int chunk = blockIdx.y;
-  float acc[16];
-#pragma unroll
-  for (int i = 0; i < 16; ++i) acc[i] = 0.f;
-  const int tbeg = chunk * kDwChunk, tend = min(T, tbeg + kDwChunk);
-  for (int ts = tbeg; ts < tend; ts += kDwSub) {
-    const int tn = min(kDwSub, tend - ts);
+  for (int i = 0; i < 8; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+  for (int p0 = 0; p0 < h; p0 += kGP) {
     __syncthreads();
-    for (int i = threadIdx.x; i < kDwSub * 64; i += 256) {
-      const int t = i >> 6, p = i & 63;
-      s_dz[t][p] = (t < tn && p < h) ? dz[static_cast<int64_t>(ts + t) * h + p] : 0.f;
+    for (int i = tid; i < kGP * kGC; i += 256) {
+      // consecutive threads take consecutive columns: conflict-free stores of
+      // the transposed slice (the 8 KB of W rows they read stay in L1)
+      const int p = i / kGC, c = i % kGC;
+      s_w[p][c] = (c0 + c < d_model && p0 + p < h) ? __bfloat162float(W[static_cast<int64_t>(c0 + c) * h + p0 + p])
+                                                   : 0.f;
+    }
+    for (int i = tid; i < kGT * kGP; i += 256) {
+      const int t = i / kGP, p = i % kGP;
+      s_z[t][p] = (t0 + t < T && p0 + p < h) ? dz[static_cast<int64_t>(t0 + t) * h + p0 + p] : 0.f;
     }
     __syncthreads();
-    if (c < d_model && pg * 16 < h) {
 #pragma unroll 4
-      for (int t = 0; t < tn; ++t) {
-        const float xv = __bfloat162float(X[static_cast<int64_t>(ts + t) * d_model + c]);
+    for (int p = 0; p < kGP; ++p) {
+      const float4 w4 = *reinterpret_cast<const float4*>(&s_w[p][tx * 4]);
 #pragma unroll
-        for (int i = 0; i < 16; ++i) acc[i] = fmaf(xv, s_dz[t][pg * 16 + i], acc[i]);
+      for (int i = 0; i < 8; ++i) {
+        const float z = s_z[ty * 8 + i][p];
+        acc[i][0] = fmaf(z, w4.x, acc[i][0]);
+        acc[i][1] = fmaf(z, w4.y, acc[i][1]);
+        acc[i][2] = fmaf(z, w4.z, acc[i][2]);
+        acc[i][3] = fmaf(z, w4.w, acc[i][3]);
       }
     }
   }
-  if (c < d_model) {
+  const int c = c0 + tx * 4;
+  if (c >= d_model) return;  // d_model is a multiple of 64: all four columns or none
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
-      const int p = pg * 16 + i;
-      if (p < h) part[(static_cast<int64_t>(chunk) * d_model + c) * h + p] = acc[i];
+  for (int i = 0; i < 8; ++i) {
+    const int t = t0 + ty * 8 + i;
+    if (t < T)
+      *reinterpret_cast<uint2*>(dx + static_cast<int64_t>(t) * d_model + c) =
+          make_uint2(pack_bf16x2(acc[i][0], acc[i][1]), pack_bf16x2(acc[i][2], acc[i][3]));
+  }
+}
+
+// dW partials: block = 128 columns x 32 gate heads over one chunk of
+// kDwChunk tokens, 256 threads; thread = 4 consecutive columns x 4 heads.
+// X and dz staged 64 tokens at a time.
+__global__ void __launch_bounds__(256)
+v2_bwd_dw_partial_kernel(int T, int d_model, int h, const float* __restrict__ dz,
+                         const __nv_bfloat16* __restrict__ X, float* __restrict__ part) {
+  __shared__ __align__(16) __nv_bfloat16 s_x[kGT][kGC];
+  __shared__ __align__(16) float s_z[kGT][kGP];
+  const int tid = threadIdx.x, tx = tid & 31, ty = tid >> 5;
+  const int c0 = blockIdx.x * kGC, chunk = blockIdx.y, p0 = blockIdx.z * kGP;
+  float acc[4][4];
+#pragma unroll
+  for (int i = 0; i < 4; ++i) acc[i][0] = acc[i][1] = acc[i][2] = acc[i][3] = 0.f;
+  const int tbeg = chunk * kDwChunk, tend = min(T, tbeg + kDwChunk);
+  for (int ts = tbeg; ts < tend; ts += kGT) {
+    __syncthreads();
+    // X tile: 64 tokens x 128 columns, 16-byte loads (d_model % 64 == 0)
+    for (int i = tid; i < kGT * (kGC / 8); i += 256) {
+      const int t = i / (kGC / 8), c8 = (i % (kGC / 8)) * 8;
+      uint4 v = make_uint4(0u, 0u, 0u, 0u);
+      if (ts + t < tend && c0 + c8 < d_model)
+        v = *reinterpret_cast<const uint4*>(X + static_cast<int64_t>(ts + t) * d_model + c0 + c8);
+      *reinterpret_cast<uint4*>(&s_x[t][c8]) = v;
+    }
+    for (int i = tid; i < kGT * kGP; i += 256) {
+      const int t = i / kGP, p = i % kGP;
+      s_z[t][p] = (ts + t < tend && p0 + p < h) ? dz[static_cast<int64_t>(ts + t) * h + p0 + p] : 0.f;
+    }
+    __syncthreads();
+#pragma unroll 4
+    for (int t = 0; t < kGT; ++t) {
+      const uint2 xr = *reinterpret_cast<const uint2*>(&s_x[t][tx * 4]);
+      const float4 z4 = *reinterpret_cast<const float4*>(&s_z[t][ty * 4]);
+      const __nv_bfloat162 x01 = *reinterpret_cast<const __nv_bfloat162*>(&xr.x);
+      const __nv_bfloat162 x23 = *reinterpret_cast<const __nv_bfloat162*>(&xr.y);
+      const float xv[4] = {__low2float(x01), __high2float(x01), __low2float(x23), __high2float(x23)};
+      const float zv[4] = {z4.x, z4.y, z4.z, z4.w};
+#pragma unroll
+      for (int i = 0; i < 4; ++i)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) acc[i][j] = fmaf(xv[i], zv[j], acc[i][j]);
+    }
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int c = c0 + tx * 4 + i;
+    if (c >= d_model) continue;
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const int p = p0 + ty * 4 + j;
+      if (p < h) part[(static_cast<int64_t>(chunk) * d_model + c) * h + p] = acc[i][j];
     }
   }
 }
@@ -766,12 +802,9 @@ v2_bwd_dw_reduce_kernel(int d_model, int h, int chunks, const float* __restrict_
 
 cudaError_t launch_dx(int T, int d_model, int h, const float* dz, const void* W, void* dx,
                       cudaStream_t s) {
-  const dim3 grid((T + kDxTok - 1) / kDxTok, (d_model + 255) / 256);
-  const auto* w = static_cast<const __nv_bfloat16*>(W);
-  auto* o = static_cast<__nv_bfloat16*>(dx);
-  if (h <= 16) v2_bwd_dx_kernel<16><<<grid, 128, 0, s>>>(T, d_model, h, dz, w, o);
-  else if (h <= 32) v2_bwd_dx_kernel<32><<<grid, 128, 0, s>>>(T, d_model, h, dz, w, o);
-  else v2_bwd_dx_kernel<64><<<grid, 128, 0, s>>>(T, d_model, h, dz, w, o);
+  const dim3 grid((T + kGT - 1) / kGT, (d_model + kGC - 1) / kGC);
+  v2_bwd_dx_kernel<<<grid, 256, 0, s>>>(T, d_model, h, dz, static_cast<const __nv_bfloat16*>(W),
+                                        static_cast<__nv_bfloat16*>(dx));
   return cudaGetLastError();
 }
 
@@ -839,7 +872,7 @@ cudaError_t launch_v2_bwd(const V2BwdArgs& a_in, cudaStream_t s) {
     if (e != cudaSuccess) return e;
   }
   if (a.dw) {
-    v2_bwd_dw_partial_kernel<<<dim3((a.d_model + 63) / 64, w.chunks), 256, 0, s>>>(
+    v2_bwd_dw_partial_kernel<<<dim3((a.d_model + kGC - 1) / kGC, w.chunks, (a.h + kGP - 1) / kGP), 256, 0, s>>>(
         static_cast<int>(T), a.d_model, a.h, dz, static_cast<const __nv_bfloat16*>(a.x), w.dw_part);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
