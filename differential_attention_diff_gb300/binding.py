@@ -47,6 +47,7 @@ EXPORTS = (
     "diffattn_v2_decode_num_splits",
     "diffattn_v2_decode_workspace_size",
     "diffattn_get_device_status",
+    "diffattn_debug_inject_fault",
     "diffattn_get_device_status_detail",
     "diffattn_status_string",
 )
@@ -185,6 +186,8 @@ def load(path: str = LIB_PATH):
         lib.diffattn_v2_decode_num_splits.argtypes = [C.c_int] * 3
         lib.diffattn_v2_decode_workspace_size.restype = C.c_size_t
         lib.diffattn_v2_decode_workspace_size.argtypes = [C.c_int] * 7
+        lib.diffattn_debug_inject_fault.restype = C.c_int
+        lib.diffattn_debug_inject_fault.argtypes = [C.c_int]
         lib.diffattn_get_device_status.restype = C.c_int
         lib.diffattn_get_device_status.argtypes = [vp]
         lib.diffattn_get_device_status_detail.restype = C.c_int
@@ -478,6 +481,14 @@ def diffattn_v2_decode_noalloc(q, k_cache, v_cache, *, seqlens=None, gate=None, 
         int(num_splits), None, 0)
     _check(lib.diffattn_v2_decode_noalloc(C.byref(p), _stream(stream)), "diffattn_v2_decode_noalloc")
     return out
+
+
+DA_FAULT_NONE, DA_FAULT_V2_FWD_SKIP_LOAD = 0, 1
+
+
+def diffattn_debug_inject_fault(fault: int):
+    """Test hook: arm a one-shot fault for the next call it applies to."""
+    _check(load().diffattn_debug_inject_fault(int(fault)), "diffattn_debug_inject_fault")
 
 
 def diffattn_get_device_status(stream=None, detail=False):

@@ -5,6 +5,7 @@
 #include <cuda_runtime.h>
 
 #include <cmath>
+#include <atomic>
 #include <mutex>
 
 #include "diffattn.h"
@@ -65,6 +66,10 @@ da_status check_t4(const da_t4& t, da_dtype dt) {
 
 da_status cuda_status(cudaError_t e) { return e == cudaSuccess ? DA_OK : DA_ERR_CUDA; }
 
+// One-shot test hook (diffattn_debug_inject_fault): consumed by the next call
+// it applies to.
+std::atomic<int> g_fault{0};
+
 constexpr float kLog2e = 1.4426950408889634f;
 
 size_t align256(size_t x) { return (x + 255) & ~size_t(255); }
@@ -103,6 +108,12 @@ da_status diffattn_get_device_status_detail(void* stream, uint32_t* raw) {
   if (cudaStreamSynchronize(s) != cudaSuccess) return DA_ERR_CUDA;
   if (raw) *raw = word;
   return static_cast<da_status>(word & 0xffu);
+}
+
+da_status diffattn_debug_inject_fault(int fault) {
+  if (fault != DA_FAULT_NONE && fault != DA_FAULT_V2_FWD_SKIP_LOAD) return DA_ERR_INVALID_ARG;
+  g_fault.store(fault);
+  return DA_OK;
 }
 
 da_status diffattn_get_device_status(void* stream) {
@@ -313,8 +324,9 @@ da_status diffattn_v2_fwd(const da_v2_fwd_params* p, void* stream) {
   }
   const float scale = p->softmax_scale > 0.f ? p->softmax_scale
                                              : 1.f / std::sqrt(static_cast<float>(p->d));
+  const int fault = g_fault.exchange(0) == DA_FAULT_V2_FWD_SKIP_LOAD ? 1 : 0;
   da::V2FwdArgs a{p->B, p->N, p->h, p->h_kv, p->d, p->causal, scale * kLog2e,
-                  p->q, p->k, p->v, p->out, gate, p->lse, p->o_heads, d.status, d.num_sms};
+                  p->q, p->k, p->v, p->out, gate, p->lse, p->o_heads, d.status, d.num_sms, fault};
   return cuda_status(da::launch_v2_fwd(a, s));
 }
 
@@ -468,7 +480,7 @@ da_status diffattn_grouped_fwd(const da_grouped_fwd_params* p, void* stream) {
                                              : 1.f / std::sqrt(static_cast<float>(p->d));
   // the attention over all Hq heads (taken two at a time), per-head outputs only
   da::V2FwdArgs fa{p->B, p->N, Hq / 2, p->h_kv, p->d, p->causal, scale * kLog2e,
-                   p->q, p->k, p->v, da_t4{nullptr, 0, 0, 0}, nullptr, p->lse, heads, d.status, d.num_sms};
+                   p->q, p->k, p->v, da_t4{nullptr, 0, 0, 0}, nullptr, p->lse, heads, d.status, d.num_sms, 0};
   if (da::launch_v2_fwd(fa, s) != cudaSuccess) return DA_ERR_CUDA;
   da::GroupedArgs ca{p->B, p->N, p->h, p->ratio, heads, gate, p->out};
   return cuda_status(da::launch_grouped_combine(ca, s));

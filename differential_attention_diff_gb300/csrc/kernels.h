@@ -71,6 +71,7 @@ struct V2FwdArgs {
   da_t4 o_heads;      // optional [B, N, 2h, d] per-head outputs
   uint32_t* status;
   int num_sms;
+  int fault;          // test hook: CTA 0 skips its first K tile load
 };
 cudaError_t launch_v2_fwd(const V2FwdArgs& a, cudaStream_t s);
 

@@ -401,6 +401,21 @@ da_status diffattn_get_device_status_detail(void* cuda_stream, uint32_t* raw);
 
 const char* diffattn_status_string(da_status s);
 
+/* ------------------------------------------------------------------------ */
+/* Test hook for the failure path of the bounded waits.  Every mbarrier wait
+ * in the tcgen05 kernels gives up after about 2 s, records DA_ERR_TIMEOUT
+ * (with a site code) in the device status word, raises a per-CTA abort flag
+ * so that the CTA's other roles leave their loops, lets its own in-flight
+ * copies land and frees its TMEM before returning; the context stays usable.
+ * DA_FAULT_V2_FWD_SKIP_LOAD makes the NEXT diffattn_v2_fwd call (only that
+ * one) leave the first K tile of its first CTA unloaded, so the wait for it
+ * expires: that call's outputs are incomplete, diffattn_get_device_status
+ * then returns DA_ERR_TIMEOUT, and later calls run normally.
+ * DA_FAULT_NONE cancels a pending injection.  Returns DA_ERR_INVALID_ARG for
+ * any other value.  Host-side state of the library (not per device). */
+typedef enum { DA_FAULT_NONE = 0, DA_FAULT_V2_FWD_SKIP_LOAD = 1 } da_fault;
+da_status diffattn_debug_inject_fault(int fault);
+
 #ifdef __cplusplus
 }
 #endif

@@ -149,3 +149,11 @@ def test_grouped_shape_checks(lib):
     assert lib.diffattn_grouped_fwd(C.byref(p(6, 3, 4)), None) == bd.DA_ERR_INVALID_ARG   # 8 heads / 4 kv: groups of 4 straddle
     assert lib.diffattn_grouped_fwd(C.byref(p(8, 4, 2)), None) == bd.DA_ERR_UNSUPPORTED   # 5 heads per kv head
     assert lib.diffattn_grouped_fwd_workspace_size(2, 8192, 48, 3, 128, 0, 0) == 2 * 8192 * 48 * 4 + 2 * 8192 * 64 * 128 * 2
+
+
+def test_fault_hook_arguments(lib):
+    """The test hook accepts only the faults it knows, and NONE disarms it
+    (host-side state: no kernel is launched)."""
+    assert lib.diffattn_debug_inject_fault(7) == bd.DA_ERR_INVALID_ARG
+    assert lib.diffattn_debug_inject_fault(bd.DA_FAULT_V2_FWD_SKIP_LOAD) == bd.DA_OK
+    assert lib.diffattn_debug_inject_fault(bd.DA_FAULT_NONE) == bd.DA_OK
