@@ -542,9 +542,18 @@ class V2FwdBwdSmall(V2FwdBwd):
     B, N = 1, 4096
 
 
+class V1DecodeSmall(V1Decode):
+    """The V1 decode kernels on a 2.1 GB cache (B4): above L2, small enough
+    for a multi-pass ncu capture."""
+    name = "v1_decode_small"
+    desc = "V1 decode bf16 B4 cache 32768 16 heads d_qk128 d_v256 (profiling size)"
+    B = 4
+
+
 WORKLOADS = {w.name: w for w in (V1Fwd, V1FwdF32, V2Fwd, V2Decode, V1FwdBwd, V1FwdBwdDet, V2FwdBwd,
                                  V1Decode, GroupedFwd)}
-PROFILE_ONLY = {V2DecodeSmall.name: V2DecodeSmall, V2FwdBwdSmall.name: V2FwdBwdSmall}
+PROFILE_ONLY = {V2DecodeSmall.name: V2DecodeSmall, V2FwdBwdSmall.name: V2FwdBwdSmall,
+                V1DecodeSmall.name: V1DecodeSmall}
 
 # ----------------------------------------------------------------- helpers --
 
