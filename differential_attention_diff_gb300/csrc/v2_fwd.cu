@@ -7,7 +7,7 @@
 //     out[t, p] = O[t, 2p] - gate[t, p] * O[t, 2p + 1].
 //
 // One CTA (persistent, one per SM) owns a work item = (batch, pair p, 128
-// query rows) at a time, heaviest causal rows first.  Both heads of the pair
+// query rows) at a time, heaviest causal rows first, dealt in a snake order.  Both heads of the pair
 // are computed side by side against the same K/V tiles, each tile fetched
 // once by TMA for the two heads:
 //
@@ -112,6 +112,16 @@ __device__ __forceinline__ Item item_of(int i, int units, int h, int n_mtiles) {
   return it;
 }
 
+// The k-th item of this CTA: rounds of gridDim.x items taken heaviest first,
+// every other round in reverse CTA order (a snake), so that no CTA draws the
+// largest item of every round (1.03-1.09x -> 1.00x the ideal makespan for
+// causal item sizes).  Increasing in k, so a CTA stops at its first index
+// past the end.
+__device__ __forceinline__ int sched(int k) {
+  return k * static_cast<int>(gridDim.x) +
+         ((k & 1) ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x));
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
 v2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, V2FwdArgs a) {
@@ -164,7 +174,7 @@ v2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       int kv_it = 0, it = 0;
       int last_kv = -1;  // last K/V tile issued (for the drain on error)
       bool ok = true;
-      for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x, ++it) {
+      for (int i = sched(0); i < n_items && ok; ++it, i = sched(it)) {
         const Item w = item_of(i, units, a.h, n_mtiles);
         const int g = (2 * w.p) / G;
         if (it > 0 && !wait_bar(sh, sh.bar(B_QEMPTY), (it - 1) & 1, a.status, 0x2001)) {
@@ -234,7 +244,7 @@ v2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
                     (acc || kk > 0) ? 1u : 0u);
         }
       };
-      for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x, ++it) {
+      for (int i = sched(0); i < n_items && ok; ++it, i = sched(it)) {
         const Item w = item_of(i, units, a.h, n_mtiles);
         if (!wait_bar(sh, sh.bar(B_QFULL), it & 1, a.status, 0x2101)) { ok = false; break; }
         tc_fence_after();
@@ -296,7 +306,7 @@ v2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       ++ec;
       return r;
     };
-    for (int i = blockIdx.x; i < n_items && ok; i += gridDim.x, ++it) {
+    for (int i = sched(0); i < n_items && ok; ++it, i = sched(it)) {
       const Item w = item_of(i, units, a.h, n_mtiles);
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < w.n_kv; ++j, ++sc) {
