@@ -45,7 +45,8 @@ def test_status_strings(lib):
 
 def test_null_params_rejected(lib):
     for name in ("diffattn_v1_fwd", "diffattn_v1_bwd", "diffattn_v2_gate", "diffattn_v2_fwd",
-                 "diffattn_v2_decode"):
+                 "diffattn_v2_decode", "diffattn_v2_decode_noalloc", "diffattn_v2_bwd", "diffattn_v1_decode",
+                 "diffattn_grouped_fwd"):
         assert getattr(lib, name)(None, None) == bd.DA_ERR_INVALID_ARG, name
 
 
@@ -157,3 +158,62 @@ def test_fault_hook_arguments(lib):
     assert lib.diffattn_debug_inject_fault(7) == bd.DA_ERR_INVALID_ARG
     assert lib.diffattn_debug_inject_fault(bd.DA_FAULT_V2_FWD_SKIP_LOAD) == bd.DA_OK
     assert lib.diffattn_debug_inject_fault(bd.DA_FAULT_NONE) == bd.DA_OK
+
+
+def test_v1_decode_argument_checks(lib):
+    p = bd.da_v1_decode_params()
+    p.B, p.H, p.d_qk, p.d_v, p.L_max = 2, 4, 128, 256, 1024
+    p.lambda_init, p.rms_eps = 0.2, 1e-5
+    fake = 1 << 20
+    p.q1, p.q2, p.out = fake, fake, fake
+    p.lq1 = p.lk1 = p.lq2 = p.lk2 = fake
+    p.k1_cache = bd.da_t4(fake, 1024 * 4 * 128, 4 * 128, 128)
+    p.k2_cache = bd.da_t4(fake, 1024 * 4 * 128, 4 * 128, 128)
+    p.v_cache = bd.da_t4(fake, 1024 * 4 * 256, 4 * 256, 256)
+    f = lib.diffattn_v1_decode
+
+    def with_(**kw):
+        q = bd.da_v1_decode_params.from_buffer_copy(p)
+        for k, v in kw.items():
+            setattr(q, k, v)
+        return C.byref(q)
+    assert f(with_(d_qk=64), None) == bd.DA_ERR_UNSUPPORTED
+    assert f(with_(q1=fake + 2), None) == bd.DA_ERR_INVALID_ARG          # misaligned query
+    assert f(with_(lk2=None), None) == bd.DA_ERR_INVALID_ARG
+    assert f(with_(rms_eps=-1.0), None) == bd.DA_ERR_INVALID_ARG
+    assert f(with_(v_cache=bd.da_t4(fake, 1024, 12, 256)), None) == bd.DA_ERR_INVALID_ARG  # stride % 8
+    assert f(with_(num_splits=70000), None) == bd.DA_ERR_INVALID_ARG
+    assert f(with_(), None) == bd.DA_ERR_WORKSPACE                       # no workspace
+    # split partials: [splits, B, H, 2 streams, d_v] fp32 + (max, sum) per stream
+    a256 = lambda x: (x + 255) // 256 * 256  # noqa: E731
+    assert lib.diffattn_v1_decode_workspace_size(2, 4, 256, 1024, 3) == \
+        a256(3 * 2 * 4 * 2 * 256 * 4) + a256(3 * 2 * 4 * 2 * 2 * 4)
+    assert lib.diffattn_v1_decode_num_splits(64, 16, 32768) >= 1
+    assert lib.diffattn_v1_decode_num_splits(1, 1, 1000) == 1            # no split under 1024 keys
+
+
+def test_v2_bwd_argument_checks(lib):
+    p = bd.da_v2_bwd_params()
+    p.B, p.N, p.h, p.h_kv, p.d, p.causal = 1, 256, 4, 2, 128, 1
+    fake = 1 << 20
+    for n in ("q", "o_heads", "dq"):
+        setattr(p, n, bd.da_t4(fake, 1 << 18, 1 << 10, 128))
+    for n in ("k", "v", "dk", "dv"):
+        setattr(p, n, bd.da_t4(fake, 1 << 16, 1 << 8, 128))
+    p.dout = bd.da_t4(fake, 1 << 17, 1 << 9, 128)
+    p.lse, p.gate = fake, fake
+    f = lib.diffattn_v2_bwd
+
+    def with_(**kw):
+        q = bd.da_v2_bwd_params.from_buffer_copy(p)
+        for k, v in kw.items():
+            setattr(q, k, v)
+        return C.byref(q)
+    assert f(with_(h_kv=3), None) == bd.DA_ERR_INVALID_ARG       # 2h not divisible into groups
+    assert f(with_(h=1, h_kv=2), None) == bd.DA_ERR_INVALID_ARG  # a pair would straddle groups
+    assert f(with_(d=64), None) == bd.DA_ERR_UNSUPPORTED
+    assert f(with_(lse=None), None) == bd.DA_ERR_INVALID_ARG     # the forward's saves are needed
+    assert f(with_(gate=None), None) == bd.DA_ERR_INVALID_ARG    # no gate and no x / w_lambda
+    assert f(with_(dx=fake), None) == bd.DA_ERR_INVALID_ARG      # dX needs x and w_lambda
+    assert f(with_(), None) == bd.DA_ERR_WORKSPACE
+    assert f(with_(N=0), None) == bd.DA_OK                       # empty problem
