@@ -279,16 +279,12 @@ decode_merge_kernel(DecodeArgs a) {
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(
-        decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  // set on every launch: the attribute is per device, and the call is cheap
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
   dim3 g1(a.num_splits, a.h_kv, a.B);
   decode_split_kernel<<<g1, kWarps * 32, kSmemBytes, s>>>(a);
-  cudaError_t e = cudaGetLastError();
+  e = cudaGetLastError();
   if (e != cudaSuccess) return e;
   dim3 g2(a.h, a.B);
   decode_merge_kernel<<<g2, 128, 0, s>>>(a);

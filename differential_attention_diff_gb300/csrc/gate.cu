@@ -131,13 +131,9 @@ gate_kernel(GateArgs a) {
 cudaError_t launch_gate(const GateArgs& a, cudaStream_t s) {
   const int grid = (a.T + kTok - 1) / kTok;
   if (grid == 0) return cudaSuccess;
-  static bool attr_done = false;
-  if (!attr_done) {
-    cudaError_t e = cudaFuncSetAttribute(gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                         kStages * kStageBytes);
-    if (e != cudaSuccess) return e;
-    attr_done = true;
-  }
+  // set on every launch: the attribute is per device, and the call is cheap
+  cudaError_t e = cudaFuncSetAttribute(gate_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kStages * kStageBytes);
+  if (e != cudaSuccess) return e;
   gate_kernel<<<grid, 128, kStages * kStageBytes, s>>>(a);
   return cudaGetLastError();
 }
