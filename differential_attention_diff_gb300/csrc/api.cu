@@ -167,7 +167,7 @@ da_status diffattn_v2_decode(const da_v2_decode_params* p, void* stream) {
   if ((2 * p->h) % p->h_kv) return DA_ERR_INVALID_ARG;
   const int G = 2 * p->h / p->h_kv;
   if (G % 2) return DA_ERR_INVALID_ARG;  // a pair must sit in one K/V group
-  if (p->d != 128 || G > 16) return DA_ERR_UNSUPPORTED;
+  if ((p->d != 64 && p->d != 128) || G > 16) return DA_ERR_UNSUPPORTED;
   if (!p->q || !p->out || !aligned(p->q, 16) || !aligned(p->out, 16)) return DA_ERR_INVALID_ARG;
   if (check_t4(p->k_cache, DA_BF16) != DA_OK || check_t4(p->v_cache, DA_BF16) != DA_OK)
     return DA_ERR_INVALID_ARG;
@@ -238,7 +238,8 @@ da_status diffattn_v1_fwd(const da_v1_fwd_params* p, void* stream) {
                     p->lq1, p->lk1, p->lq2, p->lk2, p->lse1, p->lse2, p->rstd, p->lambda_out};
     return cuda_status(da::launch_v1_fwd_f32(a, s));
   }
-  if (p->d_qk != 128 || p->d_v != 256 || !p->causal) return DA_ERR_UNSUPPORTED;
+  if (!((p->d_qk == 128 && p->d_v == 256) || (p->d_qk == 64 && p->d_v == 128)) || !p->causal)
+    return DA_ERR_UNSUPPORTED;
   const size_t need = da::v1_fwd_workspace_bytes(d.num_sms);
   if (need && (p->workspace == nullptr || p->workspace_bytes < need || !aligned(p->workspace, 256)))
     return DA_ERR_WORKSPACE;
@@ -297,7 +298,7 @@ da_status diffattn_v2_fwd(const da_v2_fwd_params* p, void* stream) {
   if ((2 * p->h) % p->h_kv) return DA_ERR_INVALID_ARG;
   if ((2 * p->h / p->h_kv) % 2) return DA_ERR_INVALID_ARG;
   if (p->B == 0 || p->N == 0) return DA_OK;
-  if (p->d != 128 || !p->causal) return DA_ERR_UNSUPPORTED;
+  if ((p->d != 64 && p->d != 128) || !p->causal) return DA_ERR_UNSUPPORTED;
   for (const da_t4* t : {&p->q, &p->k, &p->v, &p->out})
     if (check_t4(*t, DA_BF16) != DA_OK) return DA_ERR_INVALID_ARG;
   if (p->o_heads.ptr && check_t4(p->o_heads, DA_BF16) != DA_OK) return DA_ERR_INVALID_ARG;
@@ -398,7 +399,7 @@ da_status diffattn_v1_decode(const da_v1_decode_params* p, void* stream) {
   if (p == nullptr) return DA_ERR_INVALID_ARG;
   if (p->B <= 0 || p->H <= 0 || p->d_qk <= 0 || p->d_v <= 0 || p->L_max <= 0) return DA_ERR_INVALID_ARG;
   if (!(p->rms_eps >= 0.f)) return DA_ERR_INVALID_ARG;
-  if (p->d_qk != 128 || p->d_v != 256) return DA_ERR_UNSUPPORTED;
+  if (!((p->d_qk == 128 && p->d_v == 256) || (p->d_qk == 64 && p->d_v == 128))) return DA_ERR_UNSUPPORTED;
   if (!p->q1 || !p->q2 || !p->out || !aligned(p->q1, 16) || !aligned(p->q2, 16) || !aligned(p->out, 16))
     return DA_ERR_INVALID_ARG;
   if (!p->lq1 || !p->lk1 || !p->lq2 || !p->lk2) return DA_ERR_INVALID_ARG;
@@ -415,7 +416,7 @@ da_status diffattn_v1_decode(const da_v1_decode_params* p, void* stream) {
   const size_t po = static_cast<size_t>(splits) * p->B * p->H * 2 * p->d_v * sizeof(float);
   const float scale = p->softmax_scale > 0.f ? p->softmax_scale
                                              : 1.f / std::sqrt(static_cast<float>(p->d_qk));
-  da::V1DecodeArgs a{p->B, p->H, p->L_max, splits, scale * kLog2e, p->lambda_init, p->rms_eps,
+  da::V1DecodeArgs a{p->B, p->H, p->d_qk, p->d_v, p->L_max, splits, scale * kLog2e, p->lambda_init, p->rms_eps,
                      p->q1, p->q2, p->k1_cache, p->k2_cache, p->v_cache, p->seqlens,
                      p->lq1, p->lk1, p->lq2, p->lk2, p->out,
                      reinterpret_cast<float*>(ws), reinterpret_cast<float*>(ws + align256(po)), d.status};
@@ -442,7 +443,7 @@ da_status diffattn_grouped_fwd(const da_grouped_fwd_params* p, void* stream) {
   const int G = Hq / p->h_kv;
   if (G % (p->ratio + 1)) return DA_ERR_INVALID_ARG;  // a group must sit in one K/V group
   if (p->B == 0 || p->N == 0) return DA_OK;
-  if (p->d != 128 || !p->causal || (G % 2)) return DA_ERR_UNSUPPORTED;
+  if ((p->d != 64 && p->d != 128) || !p->causal || (G % 2)) return DA_ERR_UNSUPPORTED;
   for (const da_t4* t : {&p->q, &p->k, &p->v, &p->out})
     if (check_t4(*t, DA_BF16) != DA_OK) return DA_ERR_INVALID_ARG;
   if (p->o_heads.ptr && check_t4(p->o_heads, DA_BF16) != DA_OK) return DA_ERR_INVALID_ARG;
@@ -482,7 +483,7 @@ da_status diffattn_grouped_fwd(const da_grouped_fwd_params* p, void* stream) {
   da::V2FwdArgs fa{p->B, p->N, Hq / 2, p->h_kv, p->d, p->causal, scale * kLog2e,
                    p->q, p->k, p->v, da_t4{nullptr, 0, 0, 0}, nullptr, p->lse, heads, d.status, d.num_sms, 0};
   if (da::launch_v2_fwd(fa, s) != cudaSuccess) return DA_ERR_CUDA;
-  da::GroupedArgs ca{p->B, p->N, p->h, p->ratio, heads, gate, p->out};
+  da::GroupedArgs ca{p->B, p->N, p->h, p->ratio, p->d, heads, gate, p->out};
   return cuda_status(da::launch_grouped_combine(ca, s));
 }
 

@@ -21,24 +21,35 @@
 namespace da {
 namespace {
 
-constexpr int kD = 128;          // head dim
 constexpr int kTileKeys = 64;    // keys per pipeline stage
 constexpr int kStages = 3;
 constexpr int kWarps = 4;
-constexpr int kRowBytes = kD * 2;                        // 256 B per key row
-constexpr int kTileBytes = kTileKeys * kRowBytes;        // 16 KB
-constexpr int kStageBytes = 2 * kTileBytes;              // K + V
-constexpr int kSmemBytes = kStages * kStageBytes;        // 96 KB
+// Per head dim D (64 or 128): key rows of D * 2 bytes (D / 8 16-byte chunks),
+// K + V tiles of 64 keys per stage.
+template <int D>
+struct Cfg {
+  static constexpr int kChunks = D / 8;
+  static constexpr int kRowBytes = D * 2;
+  static constexpr int kTileBytes = kTileKeys * kRowBytes;
+  static constexpr int kStageBytes = 2 * kTileBytes;  // K + V
+};
+constexpr int kSmemBytes = kStages * Cfg<128>::kStageBytes;  // 96 KB (the D = 128 ring)
 
-// Byte offset of 16-byte chunk c of key row r inside a tile (rows of 16
+// Byte offset of 16-byte chunk c of key row r inside a tile (rows of D / 8
 // chunks; the low 3 chunk bits are XORed with the row so that 8 consecutive
 // rows at one logical chunk hit 8 different bank groups).
+template <int D>
 __device__ __forceinline__ uint32_t tile_off(int r, int c) {
-  return static_cast<uint32_t>(r * kRowBytes + ((c ^ (r & 7)) << 4));
+  return static_cast<uint32_t>(r * Cfg<D>::kRowBytes + ((c ^ (r & 7)) << 4));
 }
 
+template <int D>
 __global__ void __launch_bounds__(kWarps * 32, 2)
 decode_split_kernel(DecodeArgs a) {
+  constexpr int kD = D;
+  constexpr int kChunks = Cfg<D>::kChunks;
+  constexpr int kTileBytes = Cfg<D>::kTileBytes;
+  constexpr int kStageBytes = Cfg<D>::kStageBytes;
   extern __shared__ __align__(1024) uint8_t smem[];
   const int split = blockIdx.x, g = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -71,14 +82,14 @@ decode_split_kernel(DecodeArgs a) {
       const uint32_t ks = sbase + stage * kStageBytes;
       const uint32_t vs = ks + kTileBytes;
 #pragma unroll
-      for (int i = 0; i < (kTileKeys * 16) / (kWarps * 32); ++i) {
+      for (int i = 0; i < (kTileKeys * kChunks) / (kWarps * 32); ++i) {
         const int idx = i * kWarps * 32 + tid;
-        const int r = idx >> 4, c = idx & 15;
+        const int r = idx / kChunks, c = idx % kChunks;
         const int key = key0 + r;
         const bool ok = key < k_end;
         const int kk = ok ? key : k_begin;  // any in-range row when masked
-        cp_async_16(ks + tile_off(r, c), kbase + kk * a.k.sn + c * 8, ok ? 16 : 0);
-        cp_async_16(vs + tile_off(r, c), vbase + kk * a.v.sn + c * 8, ok ? 16 : 0);
+        cp_async_16(ks + tile_off<D>(r, c), kbase + kk * a.k.sn + c * 8, ok ? 16 : 0);
+        cp_async_16(vs + tile_off<D>(r, c), vbase + kk * a.v.sn + c * 8, ok ? 16 : 0);
       }
     }
     cp_async_commit();
@@ -86,12 +97,12 @@ decode_split_kernel(DecodeArgs a) {
 
   // query rows as MMA A fragments: row = head (G <= 16), k = feature
   const int gr = lane >> 2, tq = lane & 3;
-  uint32_t qa[8][4];
+  uint32_t qa[kD / 16][4];
   {
     const __nv_bfloat16* qb = static_cast<const __nv_bfloat16*>(a.q) +
                               (static_cast<int64_t>(b) * 2 * a.h + qh0) * kD;
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
+    for (int ks = 0; ks < kD / 16; ++ks) {
       const int c0 = ks * 16 + 2 * tq;
       auto ld = [&](int row, int col) -> uint32_t {
         if (row >= G) return 0u;
@@ -104,9 +115,9 @@ decode_split_kernel(DecodeArgs a) {
     }
   }
 
-  float o[16][4];
+  float o[kD / 8][4];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  for (int i = 0; i < kD / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
   float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
 
 #pragma unroll
@@ -129,12 +140,12 @@ decode_split_kernel(DecodeArgs a) {
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
-      for (int kp = 0; kp < 4; ++kp) {  // pairs of k-steps (32 features)
+      for (int kp = 0; kp < kD / 32; ++kp) {  // pairs of k-steps (32 features)
         // matrix m (0..3) = keys nt*8..+7, features kp*32 + m*8 .. +7
         const int r = wkey0 + nt * 8 + (lane & 7);
         const int c = kp * 4 + (lane >> 3);
         uint32_t b0, b1, b2, b3;
-        ldmatrix_x4(ks + tile_off(r, c), b0, b1, b2, b3);
+        ldmatrix_x4(ks + tile_off<D>(r, c), b0, b1, b2, b3);
         mma_bf16_16816(s[nt], qa[2 * kp], b0, b1);
         mma_bf16_16816(s[nt], qa[2 * kp + 1], b2, b3);
       }
@@ -174,7 +185,7 @@ decode_split_kernel(DecodeArgs a) {
     l_lo = l_lo * al_lo + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
     l_hi = l_hi * al_hi + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < kD / 8; ++i) {
       o[i][0] *= al_lo;
       o[i][1] *= al_lo;
       o[i][2] *= al_hi;
@@ -185,14 +196,14 @@ decode_split_kernel(DecodeArgs a) {
     pa[1] = pack_bf16x2(p[0][2], p[0][3]);
     pa[2] = pack_bf16x2(p[1][0], p[1][1]);
     pa[3] = pack_bf16x2(p[1][2], p[1][3]);
-    // O[16 x 128] += P[16 x 16 keys] . V[16 keys x 128]
+    // O[16 x D] += P[16 x 16 keys] . V[16 keys x D]
 #pragma unroll
-    for (int np = 0; np < 8; ++np) {  // pairs of 8-wide feature tiles
+    for (int np = 0; np < kD / 16; ++np) {  // pairs of 8-wide feature tiles
       // matrices: (keys 0-7, f 0-7), (keys 8-15, f 0-7), (keys 0-7, f 8-15), (keys 8-15, f 8-15)
       const int r = wkey0 + (lane & 7) + ((lane >> 3) & 1) * 8;
       const int c = np * 2 + (lane >> 4);
       uint32_t b0, b1, b2, b3;
-      ldmatrix_x4_trans(vs + tile_off(r, c), b0, b1, b2, b3);
+      ldmatrix_x4_trans(vs + tile_off<D>(r, c), b0, b1, b2, b3);
       mma_bf16_16816(o[2 * np], pa, b0, b1);
       mma_bf16_16816(o[2 * np + 1], pa, b2, b3);
     }
@@ -207,10 +218,10 @@ decode_split_kernel(DecodeArgs a) {
   l_hi += __shfl_xor_sync(0xffffffffu, l_hi, 2);
 
   // merge the 4 warps through shared memory (reuses the ring)
-  float* so = reinterpret_cast<float*>(smem);            // [warps][16][128]
+  float* so = reinterpret_cast<float*>(smem);            // [warps][16][D]
   float* sml = so + kWarps * 16 * kD;                    // [warps][16][2]
 #pragma unroll
-  for (int nt = 0; nt < 16; ++nt) {
+  for (int nt = 0; nt < kD / 8; ++nt) {
     const int col = nt * 8 + 2 * tq;
     so[(warp * 16 + gr) * kD + col] = o[nt][0];
     so[(warp * 16 + gr) * kD + col + 1] = o[nt][1];
@@ -247,7 +258,7 @@ decode_split_kernel(DecodeArgs a) {
   }
 }
 
-// Merge the splits of one pair and apply the gate.  Block = 128 threads, one
+// Merge the splits of one pair and apply the gate.  Block = d threads, one
 // feature each; grid (h, B).
 __global__ void __launch_bounds__(128)
 decode_merge_kernel(DecodeArgs a) {
@@ -266,28 +277,35 @@ decode_merge_kernel(DecodeArgs a) {
       const int64_t pidx = (static_cast<int64_t>(s) * a.B + b) * H2 + j;
       const float f = exp2f(a.part_ml[pidx * 2] - base);
       lt += a.part_ml[pidx * 2 + 1] * f;
-      ot += a.part_o[pidx * kD + col] * f;
+      ot += a.part_o[pidx * a.d + col] * f;
     }
     res[e] = lt > 0.f ? ot / lt : 0.f;
   }
   const float gte = a.gate[static_cast<int64_t>(b) * a.h + p];
   const float y = __fsub_rn(res[0], __fmul_rn(gte, res[1]));
-  static_cast<__nv_bfloat16*>(a.out)[(static_cast<int64_t>(b) * a.h + p) * kD + col] =
+  static_cast<__nv_bfloat16*>(a.out)[(static_cast<int64_t>(b) * a.h + p) * a.d + col] =
       __float2bfloat16_rn(y);
+}
+
+template <int D>
+cudaError_t launch_split(const DecodeArgs& a, cudaStream_t s) {
+  // set on every launch: the attribute is per device, and the call is cheap
+  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       kSmemBytes);
+  if (e != cudaSuccess) return e;
+  dim3 g1(a.num_splits, a.h_kv, a.B);
+  decode_split_kernel<D><<<g1, kWarps * 32, kSmemBytes, s>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s) {
-  // set on every launch: the attribute is per device, and the call is cheap
-  cudaError_t e = cudaFuncSetAttribute(decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e != cudaSuccess) return e;
-  dim3 g1(a.num_splits, a.h_kv, a.B);
-  decode_split_kernel<<<g1, kWarps * 32, kSmemBytes, s>>>(a);
-  e = cudaGetLastError();
+  cudaError_t e = a.d == 128 ? launch_split<128>(a, s) : a.d == 64 ? launch_split<64>(a, s)
+                                                                    : cudaErrorInvalidValue;
   if (e != cudaSuccess) return e;
   dim3 g2(a.h, a.B);
-  decode_merge_kernel<<<g2, 128, 0, s>>>(a);
+  decode_merge_kernel<<<g2, a.d, 0, s>>>(a);
   return cudaGetLastError();
 }
 

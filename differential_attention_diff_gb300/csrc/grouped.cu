@@ -16,16 +16,15 @@
 namespace da {
 namespace {
 
-constexpr int kD = 128;
-
 // One thread per 8 features of one (b, n, output head).
 __global__ void __launch_bounds__(256)
 grouped_combine_kernel(GroupedArgs a) {
-  const long long total = static_cast<long long>(a.B) * a.N * a.h * (kD / 8);
+  const int nc = a.d / 8;
+  const long long total = static_cast<long long>(a.B) * a.N * a.h * nc;
   for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
        idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int c8 = static_cast<int>(idx % (kD / 8)) * 8;
-    const long long row = idx / (kD / 8);  // (b, n, p)
+    const int c8 = static_cast<int>(idx % nc) * 8;
+    const long long row = idx / nc;  // (b, n, p)
     const int p = static_cast<int>(row % a.h);
     const long long bn = row / a.h;
     const int n = static_cast<int>(bn % a.N), b = static_cast<int>(bn / a.N);
@@ -56,7 +55,7 @@ grouped_combine_kernel(GroupedArgs a) {
 }  // namespace
 
 cudaError_t launch_grouped_combine(const GroupedArgs& a, cudaStream_t s) {
-  const long long total = static_cast<long long>(a.B) * a.N * a.h * (kD / 8);
+  const long long total = static_cast<long long>(a.B) * a.N * a.h * (a.d / 8);
   long long grid = (total + 255) / 256;
   if (grid > 16 * 152) grid = 16 * 152;
   if (grid < 1) grid = 1;

@@ -37,15 +37,15 @@ cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
 
 // ---- V1 decode: split-KV partials of both streams, then merge + RMSNorm ----
 struct V1DecodeArgs {
-  int B, H, L_max, num_splits;
+  int B, H, d_qk, d_v, L_max, num_splits;  // (d_qk, d_v) = (128, 256) or (64, 128)
   float scale_log2, lambda_init, rms_eps;
-  const void* q1;  // bf16 [B, H, 128]
+  const void* q1;  // bf16 [B, H, d_qk]
   const void* q2;
-  da_t4 k1, k2, v;  // [B, L_max, H, 128 | 128 | 256]
+  da_t4 k1, k2, v;  // [B, L_max, H, d_qk | d_qk | d_v]
   const int* seqlens;
   const float *lq1, *lk1, *lq2, *lk2;
-  void* out;       // bf16 [B, H, 256]
-  float* part_o;   // [splits, B, H, 2, 256]
+  void* out;       // bf16 [B, H, d_v]
+  float* part_o;   // [splits, B, H, 2, d_v]
   float* part_ml;  // [splits, B, H, 2, 2]  (running max in log2 units, sum)
   uint32_t* status;
 };
@@ -78,6 +78,7 @@ cudaError_t launch_v2_fwd(const V2FwdArgs& a, cudaStream_t s);
 // ---- grouped differential attention: combine per-head outputs -------------
 struct GroupedArgs {
   int B, N, h, ratio;   // h output (signal) heads, ratio signal heads per noise head
+  int d;                // head dim (a multiple of 8)
   da_t4 o_heads;        // [B, N, h (ratio + 1) / ratio, d] bf16
   const float* gate;    // [B, N, h]
   da_t4 out;            // [B, N, h, d] bf16

@@ -20,7 +20,7 @@
 // unnormalised partial O of each stream and its (max in log2 units, sum).
 // Stage 2 (merge): grid (H, B), one thread per V feature: the log-sum-exp
 // merge of each stream, O = O1 - lambda O2 (each product rounded on its own,
-// so equal streams with lambda 1 cancel exactly), the RMS over the 256
+// so equal streams with lambda 1 cancel exactly), the RMS over the d_v
 // features, and Y = (1 - lambda_init) O / sqrt(mean O^2 + eps) in bf16.
 #include "common.cuh"
 #include "kernels.h"
@@ -28,17 +28,22 @@
 namespace da {
 namespace {
 
-constexpr int kDqk = 128, kDv = 256;
 constexpr int kTileKeys = 64;
 constexpr int kStages = 3;
 constexpr int kWarps = 8;
 constexpr int kThreads = kWarps * 32;
-constexpr int kKRow = kDqk * 2;                        // 256 B
-constexpr int kVRow = kDv * 2;                         // 512 B
-constexpr int kKTile = kTileKeys * kKRow;              // 16 KB
-constexpr int kVTile = kTileKeys * kVRow;              // 32 KB
-constexpr int kStageBytes = 2 * kKTile + kVTile;       // 64 KB
-constexpr int kSmemBytes = kStages * kStageBytes;      // 192 KB
+// Head dims (DQK, DV = 2 DQK) = (128, 256) or (64, 128): K rows of DQK * 2
+// bytes, V rows of DV * 2 bytes, K1 + K2 + V tiles of 64 keys per stage
+// (64 KB for (128, 256)).
+template <int DQK, int DV>
+struct Cfg {
+  static constexpr int kKRow = DQK * 2;
+  static constexpr int kVRow = DV * 2;
+  static constexpr int kKTile = kTileKeys * kKRow;
+  static constexpr int kVTile = kTileKeys * kVRow;
+  static constexpr int kStageBytes = 2 * kKTile + kVTile;
+  static constexpr int kSmemBytes = kStages * kStageBytes;
+};
 
 // 16-byte chunk c of row r: the low 3 chunk bits XORed with the row, so that
 // 8 consecutive rows at one logical chunk land in 8 different bank groups.
@@ -46,8 +51,13 @@ __device__ __forceinline__ uint32_t row_off(int r, int c, int row_bytes) {
   return static_cast<uint32_t>(r * row_bytes + ((c ^ (r & 7)) << 4));
 }
 
+template <int DQK, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
 v1_decode_split_kernel(V1DecodeArgs a) {
+  using C = Cfg<DQK, DV>;
+  constexpr int kDqk = DQK, kDv = DV, kHalf = DV / 2;
+  constexpr int kKRow = C::kKRow, kVRow = C::kVRow, kKTile = C::kKTile, kStageBytes = C::kStageBytes;
+  constexpr int kKC = DQK / 8, kVC = DV / 8;  // 16-byte chunks per K / V row
   extern __shared__ __align__(1024) uint8_t smem[];
   const int split = blockIdx.x, h = blockIdx.y, b = blockIdx.z;
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
@@ -75,9 +85,9 @@ v1_decode_split_kernel(V1DecodeArgs a) {
       const uint32_t ks2 = ks1 + kKTile;
       const uint32_t vs = ks2 + kKTile;
 #pragma unroll
-      for (int i = 0; i < (kTileKeys * 16) / kThreads; ++i) {
+      for (int i = 0; i < (kTileKeys * kKC) / kThreads; ++i) {
         const int idx = i * kThreads + tid;
-        const int r = idx >> 4, c = idx & 15;
+        const int r = idx / kKC, c = idx % kKC;
         const int key = key0 + r;
         const bool ok = key < k_end;
         const int kk = ok ? key : k_begin;  // any in-range row when masked
@@ -85,9 +95,9 @@ v1_decode_split_kernel(V1DecodeArgs a) {
         cp_async_16(ks2 + row_off(r, c, kKRow), k2base + static_cast<int64_t>(kk) * a.k2.sn + c * 8, ok ? 16 : 0);
       }
 #pragma unroll
-      for (int i = 0; i < (kTileKeys * 32) / kThreads; ++i) {
+      for (int i = 0; i < (kTileKeys * kVC) / kThreads; ++i) {
         const int idx = i * kThreads + tid;
-        const int r = idx >> 5, c = idx & 31;
+        const int r = idx / kVC, c = idx % kVC;
         const int key = key0 + r;
         const bool ok = key < k_end;
         const int kk = ok ? key : k_begin;
@@ -101,13 +111,13 @@ v1_decode_split_kernel(V1DecodeArgs a) {
   // 1); the other 14 rows are zero.  Only the (row gr, k) halves of the
   // fragment can be non-zero, so two registers per k-step and stream.
   const int gr = lane >> 2, tq = lane & 3;
-  uint32_t q1a[8][2], q2a[8][2];
+  uint32_t q1a[kDqk / 16][2], q2a[kDqk / 16][2];
   {
     const int64_t qoff = (static_cast<int64_t>(b) * a.H + h) * kDqk;
     const __nv_bfloat16* q1p = static_cast<const __nv_bfloat16*>(a.q1) + qoff;
     const __nv_bfloat16* q2p = static_cast<const __nv_bfloat16*>(a.q2) + qoff;
 #pragma unroll
-    for (int ks = 0; ks < 8; ++ks) {
+    for (int ks = 0; ks < kDqk / 16; ++ks) {
       const int c0 = ks * 16 + 2 * tq;
       q1a[ks][0] = gr == 0 ? *reinterpret_cast<const uint32_t*>(q1p + c0) : 0u;
       q1a[ks][1] = gr == 0 ? *reinterpret_cast<const uint32_t*>(q1p + c0 + 8) : 0u;
@@ -116,9 +126,9 @@ v1_decode_split_kernel(V1DecodeArgs a) {
     }
   }
 
-  float o[16][4];
+  float o[kHalf / 8][4];
 #pragma unroll
-  for (int i = 0; i < 16; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
+  for (int i = 0; i < kHalf / 8; ++i) o[i][0] = o[i][1] = o[i][2] = o[i][3] = 0.f;
   float m_lo = -INFINITY, m_hi = -INFINITY, l_lo = 0.f, l_hi = 0.f;
   const int wk0 = (warp & 3) * 16;  // this warp's keys within a tile
   const int fh = warp >> 2;         // this warp's half of the V features
@@ -144,7 +154,7 @@ v1_decode_split_kernel(V1DecodeArgs a) {
 #pragma unroll
     for (int nt = 0; nt < 2; ++nt) {
 #pragma unroll
-      for (int kp = 0; kp < 4; ++kp) {
+      for (int kp = 0; kp < kDqk / 32; ++kp) {
         const int r = wk0 + nt * 8 + (lane & 7);
         const int c = kp * 4 + (lane >> 3);
         uint32_t b0, b1, b2, b3;
@@ -201,7 +211,7 @@ v1_decode_split_kernel(V1DecodeArgs a) {
     l_lo = l_lo * al_lo + (p[0][0] + p[0][1] + p[1][0] + p[1][1]);
     l_hi = l_hi * al_hi + (p[0][2] + p[0][3] + p[1][2] + p[1][3]);
 #pragma unroll
-    for (int i = 0; i < 16; ++i) {
+    for (int i = 0; i < kHalf / 8; ++i) {
       o[i][0] *= al_lo;
       o[i][1] *= al_lo;
       o[i][2] *= al_hi;
@@ -212,11 +222,11 @@ v1_decode_split_kernel(V1DecodeArgs a) {
     pa[1] = pack_bf16x2(p[0][2], p[0][3]);
     pa[2] = pack_bf16x2(p[1][0], p[1][1]);
     pa[3] = pack_bf16x2(p[1][2], p[1][3]);
-    // O[16 x 128 (this half)] += P[16 x 16 keys] . V[16 keys x 128]
+    // O[16 x DV/2 (this half)] += P[16 x 16 keys] . V[16 keys x DV/2]
 #pragma unroll
-    for (int np = 0; np < 8; ++np) {
+    for (int np = 0; np < kHalf / 16; ++np) {
       const int r = wk0 + (lane & 7) + ((lane >> 3) & 1) * 8;
-      const int c = fh * 16 + np * 2 + (lane >> 4);
+      const int c = fh * (kHalf / 8) + np * 2 + (lane >> 4);
       uint32_t b0, b1, b2, b3;
       ldmatrix_x4_trans(vs + row_off(r, c, kVRow), b0, b1, b2, b3);
       mma_bf16_16816(o[2 * np], pa, b0, b1);
@@ -231,14 +241,14 @@ v1_decode_split_kernel(V1DecodeArgs a) {
 
   // merge the 4 key-warps of each feature half (rows 0 and 1 only) through
   // shared memory, reusing the ring
-  float* so = reinterpret_cast<float*>(smem);  // [warp][row 0..1][128]
-  float* sml = so + kWarps * 2 * 128;          // [warp][row 0..1][max, sum]
+  float* so = reinterpret_cast<float*>(smem);  // [warp][row 0..1][DV/2]
+  float* sml = so + kWarps * 2 * kHalf;        // [warp][row 0..1][max, sum]
   if (gr < 2) {
 #pragma unroll
-    for (int nt = 0; nt < 16; ++nt) {
+    for (int nt = 0; nt < kHalf / 8; ++nt) {
       const int col = nt * 8 + 2 * tq;
-      so[(warp * 2 + gr) * 128 + col] = o[nt][0];
-      so[(warp * 2 + gr) * 128 + col + 1] = o[nt][1];
+      so[(warp * 2 + gr) * kHalf + col] = o[nt][0];
+      so[(warp * 2 + gr) * kHalf + col + 1] = o[nt][1];
     }
     if (tq == 0) {
       sml[(warp * 2 + gr) * 2] = m_lo;
@@ -248,7 +258,7 @@ v1_decode_split_kernel(V1DecodeArgs a) {
   __syncthreads();
   for (int idx = tid; idx < 2 * kDv; idx += kThreads) {
     const int row = idx / kDv, f = idx % kDv;
-    const int half = f / 128, col = f % 128;
+    const int half = f / kHalf, col = f % kHalf;
     float mt = -INFINITY;
 #pragma unroll
     for (int j = 0; j < 4; ++j) mt = fmaxf(mt, sml[((half * 4 + j) * 2 + row) * 2]);
@@ -259,7 +269,7 @@ v1_decode_split_kernel(V1DecodeArgs a) {
       const int w = half * 4 + j;
       const float fct = fast_exp2(sml[(w * 2 + row) * 2] - base);
       lt += sml[(w * 2 + row) * 2 + 1] * fct;
-      ot += so[(w * 2 + row) * 128 + col] * fct;
+      ot += so[(w * 2 + row) * kHalf + col] * fct;
     }
     const int64_t pidx = ((static_cast<int64_t>(split) * a.B + b) * a.H + h) * 2 + row;
     a.part_o[pidx * kDv + f] = ot;
@@ -271,16 +281,17 @@ v1_decode_split_kernel(V1DecodeArgs a) {
 }
 
 // Merge the splits of both streams, the difference, the RMSNorm and the
-// scale.  Block = 256 threads, one V feature each; grid (H, B).
-__global__ void __launch_bounds__(kDv)
+// scale.  Block = d_v threads (<= 256), one V feature each; grid (H, B).
+__global__ void __launch_bounds__(256)
 v1_decode_merge_kernel(V1DecodeArgs a) {
+  const int dqk = a.d_qk, dv = a.d_v;
   __shared__ float s_lam;
-  __shared__ float s_red[kDv / 32];
+  __shared__ float s_red[8];
   const int h = blockIdx.x, b = blockIdx.y, f = threadIdx.x;
   const int warp = f >> 5, lane = f & 31;
   if (warp == 0) {
     float d1 = 0.f, d2 = 0.f;
-    for (int x = lane; x < kDqk; x += 32) {
+    for (int x = lane; x < dqk; x += 32) {
       d1 = fmaf(a.lq1[x], a.lk1[x], d1);
       d2 = fmaf(a.lq2[x], a.lk2[x], d2);
     }
@@ -303,7 +314,7 @@ v1_decode_merge_kernel(V1DecodeArgs a) {
       const int64_t pidx = ((static_cast<int64_t>(s) * a.B + b) * a.H + h) * 2 + e;
       const float fct = exp2f(a.part_ml[pidx * 2] - base);
       lt += a.part_ml[pidx * 2 + 1] * fct;
-      ot += a.part_o[pidx * kDv + f] * fct;
+      ot += a.part_o[pidx * dv + f] * fct;
     }
     res[e] = lt > 0.f ? ot / lt : 0.f;
   }
@@ -316,22 +327,31 @@ v1_decode_merge_kernel(V1DecodeArgs a) {
   __syncthreads();
   float tot = 0.f;
 #pragma unroll
-  for (int w = 0; w < kDv / 32; ++w) tot += s_red[w];
-  const float rstd = 1.f / sqrtf(tot * (1.f / kDv) + a.rms_eps);
-  static_cast<__nv_bfloat16*>(a.out)[(static_cast<int64_t>(b) * a.H + h) * kDv + f] =
+  for (int w = 0; w < 8; ++w)
+    if (w < dv / 32) tot += s_red[w];
+  const float rstd = 1.f / sqrtf(tot * (1.f / dv) + a.rms_eps);
+  static_cast<__nv_bfloat16*>(a.out)[(static_cast<int64_t>(b) * a.H + h) * dv + f] =
       __float2bfloat16_rn((1.f - a.lambda_init) * o * rstd);
+}
+
+template <int DQK, int DV>
+cudaError_t launch_split(const V1DecodeArgs& a, cudaStream_t s) {
+  constexpr int kSmem = Cfg<DQK, DV>::kSmemBytes;
+  cudaError_t e = cudaFuncSetAttribute(v1_decode_split_kernel<DQK, DV>,
+                                       cudaFuncAttributeMaxDynamicSharedMemorySize, kSmem);
+  if (e != cudaSuccess) return e;
+  v1_decode_split_kernel<DQK, DV><<<dim3(a.num_splits, a.H, a.B), kThreads, kSmem, s>>>(a);
+  return cudaGetLastError();
 }
 
 }  // namespace
 
 cudaError_t launch_v1_decode(const V1DecodeArgs& a, cudaStream_t s) {
-  cudaError_t e = cudaFuncSetAttribute(v1_decode_split_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       kSmemBytes);
+  cudaError_t e = (a.d_qk == 128 && a.d_v == 256) ? launch_split<128, 256>(a, s)
+                  : (a.d_qk == 64 && a.d_v == 128) ? launch_split<64, 128>(a, s)
+                                                   : cudaErrorInvalidValue;
   if (e != cudaSuccess) return e;
-  v1_decode_split_kernel<<<dim3(a.num_splits, a.H, a.B), kThreads, kSmemBytes, s>>>(a);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-  v1_decode_merge_kernel<<<dim3(a.H, a.B), kDv, 0, s>>>(a);
+  v1_decode_merge_kernel<<<dim3(a.H, a.B), a.d_v, 0, s>>>(a);
   return cudaGetLastError();
 }
 

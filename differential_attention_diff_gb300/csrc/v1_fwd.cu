@@ -25,8 +25,9 @@
 // eps).  Every hand-off is an mbarrier with a bounded wait (remote arrives at
 // cluster scope).
 //
-//   TMEM: [0,128) S / P buffer 0, [128,256) S / P buffer 1, [256,512) O.
-//   SMEM: Q (32 KB), K ring 2 x 32 KB, V ring 2 x 64 KB (128-byte swizzle).
+//   TMEM: [0,128) S / P buffer 0, [128,256) S / P buffer 1, [256,256+DV) O.
+//   SMEM: Q (32 KB), K ring 2 x 32 KB, V ring 2 x 64 KB (128-byte swizzle),
+//   for head dims (128, 256); half of each for (64, 128).
 //   warps 0-3: softmax (softmax.cuh) + epilogue (thread = query row = TMEM lane);
 //   warp 4: TMA producer; warp 5: MMA issuer (one lane).
 #include "kernels.h"
@@ -36,12 +37,12 @@
 namespace da {
 namespace {
 
-constexpr int kBM = 128, kBN = 128, kDqk = 128, kDv = 256;
+constexpr int kBM = 128, kBN = 128;
 constexpr int kThreads = 192;
 constexpr int kBox = 128 * 128;  // one 64-column box of 128 rows (bf16)
-constexpr int kOffQ = 0;                      // 2 boxes
-constexpr int kOffK = 2 * kBox;               // [stage][2 boxes]
-constexpr int kOffV = 6 * kBox;               // [stage][4 boxes]
+// Tiles for head dims (DQK, DV = 2 DQK) = (128, 256) or (64, 128), in boxes:
+//   Q at 0 (DQK/64), K ring [stage][DQK/64] after it, V ring [stage][DV/64]
+//   after that.  The barrier block sits after the largest layout.
 constexpr int kOffBar = 14 * kBox;            // 229376
 constexpr int kSmemBytes = kOffBar + 1024 + 1024;
 
@@ -52,7 +53,6 @@ enum {
 };
 
 constexpr uint32_t kIdescS = idesc_bf16(128, 128, 0);
-constexpr uint32_t kIdescPV = idesc_bf16(128, 256, 1);
 
 struct Shared {
   uint32_t base;
@@ -159,6 +159,7 @@ __device__ __forceinline__ Item item_of(int i, int units, int H, int n_mtiles, i
   return it;
 }
 
+template <int DQK, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
 v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__ CUtensorMap tm_q2,
               const __grid_constant__ CUtensorMap tm_k1, const __grid_constant__ CUtensorMap tm_k2,
@@ -172,14 +173,21 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
     sh.base = al;
     sh.gen = smem_raw + (al - raw);
   }
+  constexpr int kDqk = DQK, kDv = DV;
+  constexpr int kNQ = DQK / 64, kNV = DV / 64;  // 64-column boxes per tile row
+  constexpr int kOffQ = 0, kOffK = kNQ * kBox, kOffV = 3 * kNQ * kBox;
+  constexpr int kHalf = DV / 2;                 // output columns each CTA finishes
+  constexpr int kRowX = kHalf * 4;              // bytes per row of exchanged fp32 O/l
+  constexpr uint32_t kIdescPV = idesc_bf16(128, DV, 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();         // 0: stream 1, 1: stream 2
   const uint32_t partner = rank ^ 1u;
   const int n_mtiles = (a.N + kBM - 1) / kBM;
   const int units = a.B * a.H;
   const int n_items = n_mtiles * units;
-  // units per L2 block: K1 + K2 + V of one (batch, head) is N * 512 * 2 bytes
-  const int ub = max(1, min(units, static_cast<int>((48ll << 20) / (static_cast<long long>(a.N) * 1024))));
+  // units per L2 block: K1 + K2 + V of one (batch, head) is N (2 DQK + DV) * 2 bytes
+  const int ub = max(1, min(units, static_cast<int>((48ll << 20) /
+                                                    (static_cast<long long>(a.N) * (2 * DQK + DV) * 2))));
   const CUtensorMap* tq = rank == 0 ? &tm_q1 : &tm_q2;
   const CUtensorMap* tk = rank == 0 ? &tm_k1 : &tm_k2;
 
@@ -294,16 +302,16 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
         if (i >= n_items) break;
         const Item w = item_of(i, units, a.H, n_mtiles, ub);
         if (it > 0 && !wait_bar(sh, sh.bar(B_QEMPTY), (it - 1) & 1, a.status, 0x3001)) { ok = false; break; }
-        mbar_arrive_expect_tx(sh.bar(B_QFULL), 2 * kBox);
-        for (int box = 0; box < 2; ++box)
+        mbar_arrive_expect_tx(sh.bar(B_QFULL), kNQ * kBox);
+        for (int box = 0; box < kNQ; ++box)
           tma_load_4d(sh.base + kOffQ + box * kBox, tq, sh.bar(B_QFULL), box * 64, w.h, w.mt * kBM, w.b);
         for (int j = 0; j < w.n_kv; ++j, ++kv) {
           const int st = kv & 1, use = kv >> 1;
           auto load_k = [&]() -> bool {
             if (use > 0 && !wait_bar(sh, sh.bar(B_KEMPTY + st), (use - 1) & 1, a.status, 0x3002)) return false;
-            mbar_arrive_expect_tx(sh.bar(B_KFULL + st), 2 * kBox);
-            for (int box = 0; box < 2; ++box)
-              tma_load_4d(sh.base + kOffK + (st * 2 + box) * kBox, tk, sh.bar(B_KFULL + st), box * 64,
+            mbar_arrive_expect_tx(sh.bar(B_KFULL + st), kNQ * kBox);
+            for (int box = 0; box < kNQ; ++box)
+              tma_load_4d(sh.base + kOffK + (st * kNQ + box) * kBox, tk, sh.bar(B_KFULL + st), box * 64,
                           w.h, j * kBN, w.b);
             return true;
           };
@@ -319,9 +327,9 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
               --npend;
             }
             if (use > 0 && !wait_bar(sh, sh.bar(B_VEMPTY + st), (use - 1) & 1, a.status, 0x3003)) return false;
-            mbar_arrive_expect_tx(sh.bar(B_VFULL + st), 4 * kBox);
-            for (int box = 0; box < 4; ++box)
-              tma_load_4d(sh.base + kOffV + (st * 4 + box) * kBox, &tm_v, sh.bar(B_VFULL + st),
+            mbar_arrive_expect_tx(sh.bar(B_VFULL + st), kNV * kBox);
+            for (int box = 0; box < kNV; ++box)
+              tma_load_4d(sh.base + kOffV + (st * kNV + box) * kBox, &tm_v, sh.bar(B_VFULL + st),
                           box * 64, w.h, j * kBN, w.b);
             return true;
           };
@@ -351,7 +359,7 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
       const uint32_t t_o = tmem + 256;
       auto issue_s = [&](int g) {  // S of global tile g into buffer g & 1
         const int st = g & 1;
-        const uint32_t kb = sh.base + kOffK + st * 2 * kBox;
+        const uint32_t kb = sh.base + kOffK + st * kNQ * kBox;
         const uint32_t qa = sh.base + kOffQ;
 #pragma unroll
         for (int kk = 0; kk < kDqk / 16; ++kk) {
@@ -385,7 +393,7 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
           if (!wait_bar(sh, sh.bar(B_PFULL + st), (g >> 1) & 1, a.status, 0x3103)) { ok = false; break; }
           if (!wait_bar(sh, sh.bar(B_VFULL + st), (g >> 1) & 1, a.status, 0x3104)) { ok = false; break; }
           tc_fence_after();
-          const uint32_t vb = sh.base + kOffV + st * 4 * kBox;
+          const uint32_t vb = sh.base + kOffV + st * kNV * kBox;
 #pragma unroll
           for (int kk = 0; kk < kBN / 16; ++kk)
             tc_mma_ts(t_o, tmem + st * 128 + kk * 8, sdesc_sw128(vb + kk * 2048, kBox, 1024),
@@ -415,7 +423,7 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
     const float lam = *sh.lam();
     const float cscale = 1.f - a.lambda_init;
     // receive buffer: this CTA's K ring, row r at r * 512 bytes
-    const uint8_t* my_rx = sh.gen + kOffK + row * 512;
+    const uint8_t* my_rx = sh.gen + kOffK + row * kRowX;
     const uint32_t partner_rx0 = map_to_rank(sh.base + kOffK, partner);
     const uint32_t partner_rxrdy = map_to_rank(sh.bar(B_RXRDY), partner);
     const uint32_t partner_data = map_to_rank(sh.bar(B_DATA), partner);
@@ -442,7 +450,7 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
           if (!wait_bar(sh, sh.bar(B_ODONE), (g - 1) & 1, a.status, 0x3202)) { ok = false; break; }
           tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < 8; ++c) {
+          for (int c = 0; c < kDv / 32; ++c) {
             uint32_t o[32];
             tmem_ld32(t_o + c * 32, o);
             tmem_ld_wait();
@@ -461,7 +469,7 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
       if (!wait_bar(sh, sh.bar(B_ORDY), it & 1, a.status, 0x3203)) { ok = false; break; }
       tc_fence_after();
       const float inv_l = 1.f / l_run;
-      const int give = (1 - static_cast<int>(rank)) * 128, keep = static_cast<int>(rank) * 128;
+      const int give = (1 - static_cast<int>(rank)) * kHalf, keep = static_cast<int>(rank) * kHalf;
       // (1) my MMAs are done, so my K ring may receive; wait until the
       //     partner's is free too, then write the partner's half of my O/l
       //     into it (row r: 512 bytes, 16-byte chunks XOR-swizzled by r & 7)
@@ -470,9 +478,9 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
       // then one thread moves the 64 KB into the partner's K ring with a bulk
       // copy whose bytes complete on the partner's DATA barrier
       const int give_stage = (kv - 1) & 1;
-      uint8_t* gstg = sh.gen + kOffV + give_stage * 4 * kBox + row * 512;
+      uint8_t* gstg = sh.gen + kOffV + give_stage * kNV * kBox + row * kRowX;
 #pragma unroll 1
-      for (int c2 = 0; c2 < 2; ++c2) {
+      for (int c2 = 0; c2 < kHalf / 64; ++c2) {
         uint32_t o[64];
         tmem_ld32(t_o + give + c2 * 64, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
         tmem_ld32(t_o + give + c2 * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
@@ -490,32 +498,32 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
       if (row == 0) {
         // my MMAs are done (ORDY), so my K ring may receive
         remote_arrive(partner_rxrdy);
-        mbar_arrive_expect_tx(sh.bar(B_DATA), 128 * 512);
+        mbar_arrive_expect_tx(sh.bar(B_DATA), 128 * kRowX);
         if (!wait_bar(sh, sh.bar(B_GIVE), it & 1, a.status, 0x3208) ||
             !wait_bar<true>(sh, sh.bar(B_RXRDY), it & 1, a.status, 0x3206)) {
           ok = false;
           break;
         }
-        bulk_copy_to_peer(partner_rx0, sh.base + kOffV + give_stage * 4 * kBox, 128 * 512, partner_data);
+        bulk_copy_to_peer(partner_rx0, sh.base + kOffV + give_stage * kNV * kBox, 128 * kRowX, partner_data);
       }
       if (!wait_bar<true>(sh, sh.bar(B_DATA), it & 1, a.status, 0x3204)) { ok = false; break; }
       // (2) O = O1/l1 - lambda O2/l2 on my half; partial sum of squares
-      float dvals[128];
+      float dvals[kHalf];
       float ssq = 0.f;
       const int n = w.mt * kBM + row;
       const bool live = n < a.N;
       // staging for the TMA stores: the V stage of this item's last tile,
       // which the producer refills only after these stores have read it (Y in
-      // boxes 0-1, O2 in boxes 2-3, 128-byte swizzle).  It held the outgoing
+      // the first DV/128 boxes, O2 in the next DV/128, 128-byte swizzle).  It held the outgoing
       // half of O until the bulk copy read it: the partner sends its partial
       // sums only after all those bytes arrived, so after the SSQ wait below
       // it is free again.
       const int stg_stage = (kv - 1) & 1;
-      uint8_t* stg = sh.gen + kOffV + stg_stage * 4 * kBox;
-      const uint32_t stg_s = sh.base + kOffV + stg_stage * 4 * kBox;
+      uint8_t* stg = sh.gen + kOffV + stg_stage * kNV * kBox;
+      const uint32_t stg_s = sh.base + kOffV + stg_stage * kNV * kBox;
       const bool want_o2 = a.o2.ptr != nullptr;
 #pragma unroll
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < kHalf / 32; ++c) {
         uint32_t o[32];
         tmem_ld32(t_o + keep + c * 32, o);
         tmem_ld_wait();
@@ -541,7 +549,7 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
       if (want_o2) {
         // O2 / l2 of my columns: received (rank 0) or my own (rank 1)
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < kHalf / 32; ++c) {
           float o2v[32];
           if (rank == 0) {
 #pragma unroll
@@ -562,13 +570,13 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
           }
 #pragma unroll
           for (int e = 0; e < 32; e += 8) {
-            const int col = c * 32 + e;  // 0..127 within this CTA's half
+            const int col = c * 32 + e;  // column within this CTA's half
             uint4 pk;
             pk.x = pack_bf16x2(o2v[e], o2v[e + 1]);
             pk.y = pack_bf16x2(o2v[e + 2], o2v[e + 3]);
             pk.z = pack_bf16x2(o2v[e + 4], o2v[e + 5]);
             pk.w = pack_bf16x2(o2v[e + 6], o2v[e + 7]);
-            *reinterpret_cast<uint4*>(stg + (2 + (col >> 6)) * kBox + row * 128 +
+            *reinterpret_cast<uint4*>(stg + (kHalf / 64 + (col >> 6)) * kBox + row * 128 +
                                       ((((col & 63) >> 3) ^ (row & 7)) << 4)) = pk;
           }
         }
@@ -579,7 +587,7 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
       const float rstd = 1.f / sqrtf(tot * (1.f / kDv) + a.rms_eps);
       const float cs = cscale * rstd;
 #pragma unroll
-      for (int e = 0; e < 128; e += 8) {
+      for (int e = 0; e < kHalf; e += 8) {
         uint4 pk;
         pk.x = pack_bf16x2(__fmul_rn(dvals[e], cs), __fmul_rn(dvals[e + 1], cs));
         pk.y = pack_bf16x2(__fmul_rn(dvals[e + 2], cs), __fmul_rn(dvals[e + 3], cs));
@@ -600,11 +608,11 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
       mbar_arrive(sh.bar(B_STG));
       if (!wait_bar(sh, sh.bar(B_STG), it & 1, a.status, 0x3207)) { ok = false; break; }
       if (row == 0) {
-        for (int bx = 0; bx < 2; ++bx)
+        for (int bx = 0; bx < kHalf / 64; ++bx)
           tma_store_4d(&tm_out, stg_s + bx * kBox, keep + bx * 64, w.h, w.mt * kBM, w.b);
         if (want_o2)
-          for (int bx = 0; bx < 2; ++bx)
-            tma_store_4d(&tm_o2, stg_s + (2 + bx) * kBox, keep + bx * 64, w.h, w.mt * kBM, w.b);
+          for (int bx = 0; bx < kHalf / 64; ++bx)
+            tma_store_4d(&tm_o2, stg_s + (kHalf / 64 + bx) * kBox, keep + bx * 64, w.h, w.mt * kBM, w.b);
         bulk_commit();
         bulk_wait_read();
         mbar_arrive(sh.bar(B_STGFREE));
@@ -625,7 +633,11 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
 // the work counter of the dynamic schedule
 size_t v1_fwd_workspace_bytes(int) { return 256; }
 
-cudaError_t launch_v1_fwd(const V1FwdArgs& a, cudaStream_t s) {
+namespace {
+
+template <int DQK, int DV>
+cudaError_t launch_dims(const V1FwdArgs& a, cudaStream_t s) {
+  constexpr int kDqk = DQK, kDv = DV;
   CUtensorMap tq1, tq2, tk1, tk2, tv;
   if (!encode_tmap_bf16_4d(&tq1, a.q1, a.B, a.N, a.H, kDqk, kBM) ||
       !encode_tmap_bf16_4d(&tq2, a.q2, a.B, a.N, a.H, kDqk, kBM) ||
@@ -637,7 +649,7 @@ cudaError_t launch_v1_fwd(const V1FwdArgs& a, cudaStream_t s) {
   if (!encode_tmap_bf16_4d(&tout, a.out, a.B, a.N, a.H, kDv, kBM) ||
       !encode_tmap_bf16_4d(&to2, a.o2.ptr ? a.o2 : a.out, a.B, a.N, a.H, kDv, kBM))
     return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(v1_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  cudaError_t e = cudaFuncSetAttribute(v1_fwd_kernel<DQK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemBytes);
   if (e != cudaSuccess) return e;
   const int n_items = ((a.N + kBM - 1) / kBM) * a.B * a.H;
@@ -655,7 +667,7 @@ cudaError_t launch_v1_fwd(const V1FwdArgs& a, cudaStream_t s) {
   cfg.numAttrs = 1;
   int max_clusters = 0;
   cfg.gridDim = dim3(2 * ((a.num_sms > 0 ? a.num_sms : 152) / 2), 1, 1);
-  e = cudaOccupancyMaxActiveClusters(&max_clusters, v1_fwd_kernel, &cfg);
+  e = cudaOccupancyMaxActiveClusters(&max_clusters, v1_fwd_kernel<DQK, DV>, &cfg);
   if (e != cudaSuccess || max_clusters <= 0) max_clusters = (a.num_sms > 0 ? a.num_sms : 152) / 2;
   int clusters = max_clusters;
   if (clusters > n_items) clusters = n_items;
@@ -663,7 +675,15 @@ cudaError_t launch_v1_fwd(const V1FwdArgs& a, cudaStream_t s) {
   cfg.gridDim = dim3(2 * clusters, 1, 1);
   e = cudaMemsetAsync(a.workspace, 0, sizeof(int), s);
   if (e != cudaSuccess) return e;
-  return cudaLaunchKernelEx(&cfg, v1_fwd_kernel, tq1, tq2, tk1, tk2, tv, tout, to2, a);
+  return cudaLaunchKernelEx(&cfg, v1_fwd_kernel<DQK, DV>, tq1, tq2, tk1, tk2, tv, tout, to2, a);
+}
+
+}  // namespace
+
+cudaError_t launch_v1_fwd(const V1FwdArgs& a, cudaStream_t s) {
+  if (a.d_qk == 128 && a.d_v == 256) return launch_dims<128, 256>(a, s);
+  if (a.d_qk == 64 && a.d_v == 128) return launch_dims<64, 128>(a, s);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace da

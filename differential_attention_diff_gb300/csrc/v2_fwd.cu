@@ -15,8 +15,10 @@
 //     [  0,128) S_even (fp32 scores) / P_even (bf16, first 64 columns)
 //     [128,256) S_odd / P_odd
 //     [256,384) O_even accumulator     [384,512) O_odd accumulator
-//   Shared memory: Q_even, Q_odd (2 x 32 KB), K and V rings of 2 stages
-//   (2 x 2 x 32 KB), all in 128-byte-swizzled 64-column boxes.
+//     (head dim D = 64 or 128: the first D columns of each O region)
+//   Shared memory: Q_even, Q_odd (2 x D/64 boxes), K and V rings of 2 stages
+//   (2 x 2 x D/64 boxes), all in 128-byte-swizzled 64-column boxes of 128
+//   rows (16 KB each).
 //
 //   warp 8 (one lane): TMA producer — Q of the item, then K_j, V_j per tile.
 //   warp 9 (one lane): MMA issuer — S = Q K^T (SS form) and O += P V (P read
@@ -44,12 +46,11 @@ namespace {
 
 constexpr int kBM = 128;   // query rows per item
 constexpr int kBN = 128;   // keys per tile
-constexpr int kD = 128;    // head dim
 constexpr int kThreads = 320;
 constexpr int kBox = 128 * 128;            // bytes of one 64-column box of 128 rows
-constexpr int kOffQ = 0;                   // [head][box]
-constexpr int kOffK = 4 * kBox;            // [stage][box]
-constexpr int kOffV = 8 * kBox;            // [stage][box]
+// Tiles for head dim D (64 or 128) take D / 64 boxes per 128-row tile:
+//   Q [head][box] at 0, K [stage][box] at 2 D/64 boxes, V [stage][box] at
+//   4 D/64 boxes.  The barrier block sits after the largest (D = 128) layout.
 constexpr int kOffBar = 12 * kBox;         // 196608
 constexpr int kSmemBytes = kOffBar + 4096 + 1024;  // + barriers/exchange + alignment slack
 
@@ -60,7 +61,6 @@ enum {
 };
 
 constexpr uint32_t kIdescS = idesc_bf16(128, 128, 0);   // Q (K-major) x K (K-major)
-constexpr uint32_t kIdescPV = idesc_bf16(128, 128, 1);  // P (TMEM) x V (MN-major)
 
 struct Shared {
   uint32_t base;  // 1024-aligned shared address of the tile region
@@ -122,6 +122,7 @@ __device__ __forceinline__ int sched(int k) {
          ((k & 1) ? static_cast<int>(gridDim.x) - 1 - static_cast<int>(blockIdx.x) : static_cast<int>(blockIdx.x));
 }
 
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 v2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
               const __grid_constant__ CUtensorMap tm_v, V2FwdArgs a) {
@@ -133,6 +134,9 @@ v2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     sh.base = aligned;
     sh.gen = smem_raw + (aligned - raw);
   }
+  constexpr int kNB = D / 64;                 // 64-column boxes per tile row
+  constexpr int kOffQ = 0, kOffK = 2 * kNB * kBox, kOffV = 4 * kNB * kBox;
+  constexpr uint32_t kIdescPV = idesc_bf16(128, D, 1);  // P (TMEM) x V (MN-major)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = (2 * a.h) / a.h_kv;
   const int n_mtiles = (a.N + kBM - 1) / kBM;
@@ -181,10 +185,10 @@ v2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           ok = false;
           break;
         }
-        mbar_arrive_expect_tx(sh.bar(B_QFULL), 4 * kBox);
+        mbar_arrive_expect_tx(sh.bar(B_QFULL), 2 * kNB * kBox);
         for (int hh = 0; hh < 2; ++hh)
-          for (int box = 0; box < 2; ++box)
-            tma_load_4d(sh.base + kOffQ + (hh * 2 + box) * kBox, &tm_q, sh.bar(B_QFULL), box * 64,
+          for (int box = 0; box < kNB; ++box)
+            tma_load_4d(sh.base + kOffQ + (hh * kNB + box) * kBox, &tm_q, sh.bar(B_QFULL), box * 64,
                         2 * w.p + hh, w.mt * kBM, w.b);
         for (int j = 0; j < w.n_kv; ++j, ++kv_it) {
           const int st = kv_it & 1, use = kv_it >> 1;
@@ -195,14 +199,14 @@ v2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           // (test hook: the first CTA leaves its first K tile unloaded, so
           // the MMA issuer's bounded wait for it expires)
           if (!(a.fault && blockIdx.x == 0 && kv_it == 0)) {
-            mbar_arrive_expect_tx(sh.bar(B_KFULL + st), 2 * kBox);
-            for (int box = 0; box < 2; ++box)
-              tma_load_4d(sh.base + kOffK + (st * 2 + box) * kBox, &tm_k, sh.bar(B_KFULL + st),
+            mbar_arrive_expect_tx(sh.bar(B_KFULL + st), kNB * kBox);
+            for (int box = 0; box < kNB; ++box)
+              tma_load_4d(sh.base + kOffK + (st * kNB + box) * kBox, &tm_k, sh.bar(B_KFULL + st),
                           box * 64, g, j * kBN, w.b);
           }
-          mbar_arrive_expect_tx(sh.bar(B_VFULL + st), 2 * kBox);
-          for (int box = 0; box < 2; ++box)
-            tma_load_4d(sh.base + kOffV + (st * 2 + box) * kBox, &tm_v, sh.bar(B_VFULL + st),
+          mbar_arrive_expect_tx(sh.bar(B_VFULL + st), kNB * kBox);
+          for (int box = 0; box < kNB; ++box)
+            tma_load_4d(sh.base + kOffV + (st * kNB + box) * kBox, &tm_v, sh.bar(B_VFULL + st),
                         box * 64, g, j * kBN, w.b);
           last_kv = kv_it;
         }
@@ -225,19 +229,19 @@ v2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       int kv_it = 0, it = 0, pc = 0;
       bool ok = true;
       const uint32_t t_s[2] = {tmem + 0, tmem + 128};
-      const uint32_t t_o[2] = {tmem + 256, tmem + 384};
+      const uint32_t t_o[2] = {tmem + 256, tmem + 384};  // D <= 128 columns each
       auto issue_s = [&](int hh, int st) {
-        const uint32_t qa = sh.base + kOffQ + hh * 2 * kBox;
-        const uint32_t kb = sh.base + kOffK + st * 2 * kBox;
+        const uint32_t qa = sh.base + kOffQ + hh * kNB * kBox;
+        const uint32_t kb = sh.base + kOffK + st * kNB * kBox;
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
+        for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
           tc_mma_ss(t_s[hh], sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
                     kIdescS, kk > 0);
         }
       };
       auto issue_pv = [&](int hh, int st, bool acc) {
-        const uint32_t vb = sh.base + kOffV + st * 2 * kBox;
+        const uint32_t vb = sh.base + kOffV + st * kNB * kBox;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
           tc_mma_ts(t_o[hh], t_s[hh] + kk * 8, sdesc_sw128(vb + kk * 2048, kBox, 1024), kIdescPV,
@@ -316,7 +320,7 @@ v2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
           // O is stable here: the commit that signalled S(j) covers PV(j-1).
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < D / 32; ++c) {
             uint32_t o[32];
             tmem_ld32(t_o + c * 32, o);
             tmem_ld_wait();
@@ -338,11 +342,13 @@ v2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       if (!epi_sync(0x2204)) { ok = false; break; }
       const int n = w.mt * kBM + row;
       const float le = sh.lx()[row], lo = sh.lx()[128 + row];
-      uint32_t oe[2][32], oo[2][32];
+      // each warpgroup writes half of the D features of the row
+      constexpr int kHalf = D / 2, kNC = kHalf / 32;
+      uint32_t oe[kNC][32], oo[kNC][32];
 #pragma unroll
-      for (int c = 0; c < 2; ++c) {
-        tmem_ld32(tmem + lane_off + 256 + wg * 64 + c * 32, oe[c]);
-        tmem_ld32(tmem + lane_off + 384 + wg * 64 + c * 32, oo[c]);
+      for (int c = 0; c < kNC; ++c) {
+        tmem_ld32(tmem + lane_off + 256 + wg * kHalf + c * 32, oe[c]);
+        tmem_ld32(tmem + lane_off + 384 + wg * kHalf + c * 32, oo[c]);
       }
       tmem_ld_wait();
       if (n < a.N) {
@@ -351,14 +357,14 @@ v2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           const float gte = a.gate[(static_cast<int64_t>(w.b) * a.N + n) * a.h + w.p];
           const float io = gte / lo;
           __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out.ptr) + w.b * a.out.sb +
-                               static_cast<int64_t>(n) * a.out.sn + w.p * a.out.sh + wg * 64;
+                               static_cast<int64_t>(n) * a.out.sn + w.p * a.out.sh + wg * kHalf;
           // both products rounded separately (no FMA contraction), so equal
           // even and odd outputs with gate 1 cancel exactly
           auto diff = [&](uint32_t xe, uint32_t xo) {
             return __fsub_rn(__fmul_rn(__uint_as_float(xe), ie), __fmul_rn(__uint_as_float(xo), io));
           };
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
+          for (int c = 0; c < kNC; ++c) {
 #pragma unroll
             for (int e = 0; e < 32; e += 8) {
               uint4 v;
@@ -374,10 +380,10 @@ v2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
           // the saves for the backward: each head's normalised output
           const float inv_o = 1.f / lo;
           __nv_bfloat16* he = static_cast<__nv_bfloat16*>(a.o_heads.ptr) + w.b * a.o_heads.sb +
-                              static_cast<int64_t>(n) * a.o_heads.sn + 2 * w.p * a.o_heads.sh + wg * 64;
+                              static_cast<int64_t>(n) * a.o_heads.sn + 2 * w.p * a.o_heads.sh + wg * kHalf;
           __nv_bfloat16* ho = he + a.o_heads.sh;
 #pragma unroll
-          for (int c = 0; c < 2; ++c) {
+          for (int c = 0; c < kNC; ++c) {
 #pragma unroll
             for (int e = 0; e < 32; e += 8) {
               uint4 ve, vo;
@@ -411,22 +417,29 @@ v2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   if (warp == 9) tmem_dealloc(tmem, 512);
 }
 
-}  // namespace
-
-cudaError_t launch_v2_fwd(const V2FwdArgs& a, cudaStream_t s) {
+template <int D>
+cudaError_t launch_d(const V2FwdArgs& a, cudaStream_t s) {
   CUtensorMap tq, tk, tv;
-  if (!encode_tmap_bf16_4d(&tq, a.q, a.B, a.N, 2 * a.h, kD, kBM)) return cudaErrorInvalidValue;
-  if (!encode_tmap_bf16_4d(&tk, a.k, a.B, a.N, a.h_kv, kD, kBN)) return cudaErrorInvalidValue;
-  if (!encode_tmap_bf16_4d(&tv, a.v, a.B, a.N, a.h_kv, kD, kBN)) return cudaErrorInvalidValue;
-  cudaError_t e = cudaFuncSetAttribute(v2_fwd_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  if (!encode_tmap_bf16_4d(&tq, a.q, a.B, a.N, 2 * a.h, D, kBM)) return cudaErrorInvalidValue;
+  if (!encode_tmap_bf16_4d(&tk, a.k, a.B, a.N, a.h_kv, D, kBN)) return cudaErrorInvalidValue;
+  if (!encode_tmap_bf16_4d(&tv, a.v, a.B, a.N, a.h_kv, D, kBN)) return cudaErrorInvalidValue;
+  cudaError_t e = cudaFuncSetAttribute(v2_fwd_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemBytes);
   if (e != cudaSuccess) return e;
   const int n_items = ((a.N + kBM - 1) / kBM) * a.B * a.h;
   int grid = a.num_sms > 0 ? a.num_sms : 148;
   if (grid > n_items) grid = n_items;
   if (grid <= 0) return cudaSuccess;
-  v2_fwd_kernel<<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, a);
+  v2_fwd_kernel<D><<<grid, kThreads, kSmemBytes, s>>>(tq, tk, tv, a);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+cudaError_t launch_v2_fwd(const V2FwdArgs& a, cudaStream_t s) {
+  if (a.d == 128) return launch_d<128>(a, s);
+  if (a.d == 64) return launch_d<64>(a, s);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace da

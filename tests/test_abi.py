@@ -95,6 +95,8 @@ def test_decode_argument_checks(lib):
     bad = bd.da_v2_decode_params.from_buffer_copy(p)
     bad.d = 96
     assert f(C.byref(bad), None) == bd.DA_ERR_UNSUPPORTED
+    bad.d = 64  # supported: the next check is the workspace
+    assert f(C.byref(bad), None) == bd.DA_ERR_WORKSPACE
     # workspace missing
     assert f(C.byref(p), None) == bd.DA_ERR_WORKSPACE
     ws = lib.diffattn_v2_decode_workspace_size(2, 32, 8, 128, 1024, 4, 1)
@@ -113,7 +115,9 @@ def test_v2_fwd_argument_checks(lib):
     assert f(C.byref(p), None) == bd.DA_ERR_INVALID_ARG
     p.x, p.w_lambda, p.d_model = fake, fake, 4096
     assert f(C.byref(p), None) == bd.DA_ERR_WORKSPACE
-    p.d = 64
+    p.d = 64   # head dim 64 is supported: the next check is the workspace
+    assert f(C.byref(p), None) == bd.DA_ERR_WORKSPACE
+    p.d = 96
     assert f(C.byref(p), None) == bd.DA_ERR_UNSUPPORTED
     assert lib.diffattn_v2_fwd_workspace_size(2, 8192, 32, 0) == 2 * 8192 * 32 * 4
     assert lib.diffattn_v2_fwd_workspace_size(2, 8192, 32, 1) == 0
@@ -177,7 +181,9 @@ def test_v1_decode_argument_checks(lib):
         for k, v in kw.items():
             setattr(q, k, v)
         return C.byref(q)
-    assert f(with_(d_qk=64), None) == bd.DA_ERR_UNSUPPORTED
+    assert f(with_(d_qk=64), None) == bd.DA_ERR_UNSUPPORTED              # d_v must be 2 d_qk
+    assert f(with_(d_qk=64, d_v=128), None) == bd.DA_ERR_WORKSPACE        # supported head dims
+    assert f(with_(d_qk=96, d_v=192), None) == bd.DA_ERR_UNSUPPORTED
     assert f(with_(q1=fake + 2), None) == bd.DA_ERR_INVALID_ARG          # misaligned query
     assert f(with_(lk2=None), None) == bd.DA_ERR_INVALID_ARG
     assert f(with_(rms_eps=-1.0), None) == bd.DA_ERR_INVALID_ARG

@@ -56,6 +56,14 @@ def test_grouped_parity_small(B, N, h, ratio, hkv):
     _check(t, ratio, out)
 
 
+@pytest.mark.parametrize("B,N,h,ratio,hkv", [(1, 200, 6, 3, 2), (2, 129, 8, 4, 1)])
+def test_grouped_parity_head_dim_64(B, N, h, ratio, hkv):
+    t = synth.grouped_inputs(B, N, h, ratio, hkv, 64, 128, seed=8100 + N + h, device="cuda")
+    out = bd.diffattn_grouped_fwd(t["q"], t["k"], t["v"], ratio, x=t["x"], w_lambda=t["w_lambda"])
+    torch.cuda.synchronize()
+    _check(t, ratio, out)
+
+
 def test_grouped_ratio_one_matches_v2():
     """ratio 1 is the V2 forward (which combines in fp32 rather than from
     bf16 head outputs: equal up to that rounding, well inside the bar)."""

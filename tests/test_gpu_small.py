@@ -117,6 +117,20 @@ def test_decode_parity(B, L, h, hkv, seqlens, splits):
     _decode_check(t, out)
 
 
+@pytest.mark.parametrize("B,L,h,hkv,seqlens,splits", [
+    (3, 1000, 32, 8, [1000, 1, 517], 0),
+    (2, 300, 16, 2, [300, 65], 3),
+    (2, 129, 8, 8, [129, 128], 1),
+])
+def test_decode_parity_head_dim_64(B, L, h, hkv, seqlens, splits):
+    """Head dim 64: key rows of 8 16-byte chunks, 4 feature tiles per warp MMA."""
+    t = synth.decode_inputs(B, L, h, hkv, 64, 256, seed=2100 + L, device="cuda", seqlens=seqlens)
+    out = bd.diffattn_v2_decode(t["q"], t["k_cache"], t["v_cache"], seqlens=t["seqlens"],
+                                x=t["x"], w_lambda=t["w_lambda"], num_splits=splits)
+    torch.cuda.synchronize()
+    _decode_check(t, out)
+
+
 def test_decode_gate_given_matches_x_path():
     t = synth.decode_inputs(2, 777, 32, 8, 128, 256, seed=5, device="cuda")
     gate = bd.diffattn_v2_gate(t["x"], t["w_lambda"])

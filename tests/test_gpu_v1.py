@@ -68,6 +68,29 @@ def test_v1_fwd_parity_small(B, N, H, layer):
     _check(t, li, y, sv)
 
 
+@pytest.mark.parametrize("B,N,H,layer", [(1, 200, 2, 1), (2, 300, 3, 14), (1, 1, 1, 28), (1, 700, 2, 5)])
+def test_v1_fwd_parity_head_dims_64_128(B, N, H, layer):
+    """Head dims (64, 128): one 64-column box per Q/K tile row, 32 KB of
+    exchanged O per CTA pair, one box of Y per CTA; saves checked."""
+    t = synth.v1_inputs(B, N, H, 64, 128, "bf16", seed=4100 + N + H, device="cuda")
+    li = bd.diffattn_lambda_init(layer)
+    y, sv = bd.diffattn_v1_fwd(*(t[n] for n in NAMES), li, save=True)
+    torch.cuda.synchronize()
+    _check(t, li, y, sv)
+
+
+def test_v1_fwd_exact_cancellation_head_dims_64_128():
+    t = synth.v1_inputs(1, 333, 2, 64, 128, "bf16", seed=53, device="cuda")
+    lq1 = torch.zeros(64, device="cuda")
+    lq1[0] = 1.0
+    lk1 = torch.zeros(64, device="cuda")
+    lk1[0] = math.log(2.0)
+    z = torch.zeros(64, device="cuda")
+    y = bd.diffattn_v1_fwd(t["q1"], t["q1"], t["k1"], t["k1"], t["v"], lq1, lk1, z, z, 0.0)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(y).item() == 0
+
+
 def test_v1_fwd_without_saves_matches():
     t = synth.v1_inputs(1, 300, 2, 128, 256, "bf16", seed=51, device="cuda")
     li = bd.diffattn_lambda_init(3)

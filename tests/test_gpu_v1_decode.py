@@ -67,6 +67,16 @@ def test_v1_decode_parity(B, L, H, seqlens, splits, layer):
     _check(t, li, _run(t, li, num_splits=splits))
 
 
+@pytest.mark.parametrize("B,L,H,seqlens,splits,layer", [
+    (2, 200, 2, [200, 77], 0, 1),
+    (3, 1000, 4, [1000, 513, 1], 3, 5),
+])
+def test_v1_decode_parity_head_dims_64_128(B, L, H, seqlens, splits, layer):
+    t = synth.v1_decode_inputs(B, L, H, 64, 128, seed=6100 + L + H, device="cuda", seqlens=seqlens)
+    li = bd.diffattn_lambda_init(layer)
+    _check(t, li, _run(t, li, num_splits=splits))
+
+
 def test_v1_decode_split_count_invariance():
     """The split-KV partition changes only rounding: 1 split vs many agree."""
     t = synth.v1_decode_inputs(2, 3000, 2, 128, 256, seed=61, device="cuda")

@@ -62,6 +62,37 @@ def test_v2_fwd_parity_small(B, N, h, hkv):
     _check_pairs(t, out, gate, lse=lse)
 
 
+@pytest.mark.parametrize("B,N,h,hkv", [(1, 200, 4, 2), (2, 300, 2, 1), (1, 1, 2, 1), (1, 700, 8, 2)])
+def test_v2_fwd_parity_head_dim_64(B, N, h, hkv):
+    """Head dim 64 (one 64-column box per tile row, PV with N = 64): ragged
+    tails, one token, several query tiles; LSE and per-head saves checked."""
+    t = synth.v2_inputs(B, N, h, hkv, 64, 128, seed=3100 + N + h, device="cuda")
+    out, sv = bd.diffattn_v2_fwd(t["q"], t["k"], t["v"], x=t["x"], w_lambda=t["w_lambda"], save=True)
+    torch.cuda.synchronize()
+    lse, heads = sv["lse"], sv["o_heads"]
+    gate = orc.v2_gate(f64(t["x"]), f64(t["w_lambda"]))
+    _check_pairs(t, out, gate, lse=lse)
+    # each head's normalised output: the pair with gate 0 is that head alone
+    G = 2 * h // hkv
+    for j in (0, 2 * h - 1):
+        g = j // G
+        ref = orc.v2_forward(f64(t["q"][:1, :, [j, j]]), f64(t["k"][:1, :, g:g + 1]), f64(t["v"][:1, :, g:g + 1]),
+                             np.zeros((1, N, 1)))
+        tol = TOL * rms(f64(t["v"][0, :, g]))
+        assert np.max(np.abs(f64(heads[0, :, j]) - ref["out"][0, :, 0])) <= tol
+
+
+def test_v2_fwd_exact_cancellation_head_dim_64():
+    """Head dim 64: equal even and odd queries with gate 1 give exactly zero."""
+    t = synth.v2_inputs(1, 333, 4, 2, 64, 128, seed=34, device="cuda")
+    q = t["q"].clone()
+    q[:, :, 1::2] = q[:, :, 0::2]
+    gate = torch.ones((1, 333, 4), dtype=torch.float32, device="cuda")
+    out = bd.diffattn_v2_fwd(q, t["k"], t["v"], gate=gate)
+    torch.cuda.synchronize()
+    assert torch.count_nonzero(out).item() == 0
+
+
 def test_v2_fwd_gate_given_equals_x_path():
     t = synth.v2_inputs(1, 300, 4, 2, 128, 256, seed=31, device="cuda")
     gate = bd.diffattn_v2_gate(t["x"], t["w_lambda"])
