@@ -265,7 +265,8 @@ da_status diffattn_v1_bwd(const da_v1_bwd_params* p, void* stream) {
   if (!p->lq1 || !p->lk1 || !p->lq2 || !p->lk2) return DA_ERR_INVALID_ARG;
   if (!p->dlq1 || !p->dlk1 || !p->dlq2 || !p->dlk2) return DA_ERR_INVALID_ARG;
   if (p->B == 0 || p->N == 0 || p->H == 0) return DA_OK;
-  if (p->dtype != DA_BF16 || p->d_qk != 128 || p->d_v != 256 || !p->causal)
+  if (p->dtype != DA_BF16 || !((p->d_qk == 128 && p->d_v == 256) || (p->d_qk == 64 && p->d_v == 128)) ||
+      !p->causal)
     return DA_ERR_UNSUPPORTED;
   for (const da_t4* t : {&p->q1, &p->q2, &p->k1, &p->k2, &p->v, &p->out, &p->dout, &p->o2,
                          &p->dq1, &p->dq2, &p->dk1, &p->dk2, &p->dv})
@@ -343,7 +344,7 @@ da_status diffattn_v2_bwd(const da_v2_bwd_params* p, void* stream) {
   if ((2 * p->h) % p->h_kv) return DA_ERR_INVALID_ARG;
   if ((2 * p->h / p->h_kv) % 2) return DA_ERR_INVALID_ARG;
   if (p->B == 0 || p->N == 0) return DA_OK;
-  if (p->d != 128 || !p->causal) return DA_ERR_UNSUPPORTED;
+  if ((p->d != 64 && p->d != 128) || !p->causal) return DA_ERR_UNSUPPORTED;
   for (const da_t4* t : {&p->q, &p->k, &p->v, &p->o_heads, &p->dout, &p->dq, &p->dk, &p->dv})
     if (check_t4(*t, DA_BF16) != DA_OK) return DA_ERR_INVALID_ARG;
   if (p->lse == nullptr || !aligned(p->lse, 4)) return DA_ERR_INVALID_ARG;

@@ -62,8 +62,10 @@ namespace {
 
 constexpr int kKT = 128;   // keys per item
 constexpr int kQT = 64;    // queries per iteration
-constexpr int kDqk = 128, kDv = 256;
 constexpr int kThreads = 320;
+// Head dims (DQK, DV = 2 DQK) = (128, 256) or (64, 128).  The shared-memory
+// layout below is the (128, 256) one; (64, 128) fills the first half of each
+// K, V, Q and dO region.
 
 constexpr int kBoxK = 128 * 128;   // 64 columns x 128 rows of bf16
 constexpr int kBoxQ = 64 * 128;    // 64 columns x 64 rows
@@ -91,9 +93,9 @@ __host__ __device__ constexpr uint32_t idesc2(int M, int N, int a_mn, int b_mn) 
 }
 constexpr uint32_t kIdS = idesc2(128, 64, 0, 0);    // K (K-major) x Q (K-major)
 constexpr uint32_t kIdDP = idesc2(128, 64, 0, 0);   // V (K-major) x dO (K-major)
-constexpr uint32_t kIdDV = idesc2(128, 256, 0, 1);  // Psig^T (TMEM) x dO (MN-major)
-constexpr uint32_t kIdDK = idesc2(128, 128, 0, 1);  // dS^T (TMEM) x Q (MN-major)
 constexpr uint32_t kIdDQ = idesc2(128, 64, 1, 1);   // K^T (MN-major) x dS^T (MN-major)
+// per head dims: Psig^T (TMEM) x dO (MN-major) is idesc2(128, DV, 0, 1),
+// dS^T (TMEM) x Q (MN-major) is idesc2(128, DQK, 0, 1)
 
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
@@ -176,11 +178,11 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 // --------------------------------------------------------------------------
 // Workspace carve-up (all offsets 256-byte aligned).
 struct BwdWs {
-  __nv_bfloat16* dO;   // [B, N, H, 256]
+  __nv_bfloat16* dO;   // [B, N, H, d_v]
   float* lse2[2];      // [B, H, Npad]  (LSE * log2 e; +inf in padding rows)
   float* D[2];         // [B, H, Npad]
-  float* dq[2];        // [B, N, H, 128] fp32 accumulators, or (deterministic)
-                       // [B*H, n_slots, 64, 128] per-tile slots
+  float* dq[2];        // [B, N, H, d_qk] fp32 accumulators, or (deterministic)
+                       // [B*H, n_slots, 64, d_qk] per-tile slots
   float* dlam_part;    // [preprocess blocks]
   int npad, pre_blocks;
   int det, n_kt, n_qt, n_slots;
@@ -196,7 +198,7 @@ size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
 
 constexpr int kPreWarps = 8;
 
-BwdWs carve(void* base, int B, int N, int H, bool det, size_t* total) {
+BwdWs carve(void* base, int B, int N, int H, int dqk, int dv, bool det, size_t* total) {
   BwdWs w;
   w.npad = (N + kQT - 1) / kQT * kQT;
   w.det = det ? 1 : 0;
@@ -213,10 +215,10 @@ BwdWs carve(void* base, int B, int N, int H, bool det, size_t* total) {
   };
   const size_t rows = static_cast<size_t>(B) * N * H;
   const size_t srow = static_cast<size_t>(B) * H * w.npad;
-  w.dO = reinterpret_cast<__nv_bfloat16*>(take(rows * kDv * 2));
+  w.dO = reinterpret_cast<__nv_bfloat16*>(take(rows * dv * 2));
   for (int t = 0; t < 2; ++t) w.lse2[t] = reinterpret_cast<float*>(take(srow * 4));
   for (int t = 0; t < 2; ++t) w.D[t] = reinterpret_cast<float*>(take(srow * 4));
-  const size_t dq_elems = det ? static_cast<size_t>(B) * H * w.n_slots * kQT * kDqk : rows * kDqk;
+  const size_t dq_elems = det ? static_cast<size_t>(B) * H * w.n_slots * kQT * dqk : rows * dqk;
   for (int t = 0; t < 2; ++t) w.dq[t] = reinterpret_cast<float*>(take(dq_elems * 4));
   w.dlam_part = reinterpret_cast<float*>(take(static_cast<size_t>(w.pre_blocks) * 4));
   if (total) *total = off;
@@ -241,8 +243,29 @@ __device__ __forceinline__ float lambda_dev(const V1BwdArgs& a, int lane, float*
 }
 
 // ------------------------------------------------------------ preprocess --
+// kF consecutive bf16 values (kF = 8 or 4) / zeroed fp32 values (4 or 2)
+template <int kF>
+__device__ __forceinline__ void ld_bf16(const __nv_bfloat16* p, __nv_bfloat16 (&v)[kF]) {
+  if constexpr (kF == 8) {
+    *reinterpret_cast<uint4*>(v) = *reinterpret_cast<const uint4*>(p);
+  } else {
+    *reinterpret_cast<uint2*>(v) = *reinterpret_cast<const uint2*>(p);
+  }
+}
+template <int kF>
+__device__ __forceinline__ void st_zero_f32(float* p) {
+  if constexpr (kF == 4) {
+    *reinterpret_cast<float4*>(p) = make_float4(0.f, 0.f, 0.f, 0.f);
+  } else {
+    *reinterpret_cast<float2*>(p) = make_float2(0.f, 0.f);
+  }
+}
+
+// one warp per row; lane = DV / 32 consecutive V features
+template <int DQK, int DV>
 __global__ void __launch_bounds__(kPreWarps * 32)
 v1_bwd_pre_kernel(V1BwdArgs a, BwdWs w) {
+  constexpr int kF = DV / 32, kFq = DQK / 32;
   __shared__ float s_lam;
   __shared__ float s_part[kPreWarps];
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
@@ -262,23 +285,21 @@ v1_bwd_pre_kernel(V1BwdArgs a, BwdWs w) {
     const int b = bh / a.H, h = bh % a.H;
     if (n < a.N) {
       const __nv_bfloat16* yp = static_cast<const __nv_bfloat16*>(a.out.ptr) + b * a.out.sb +
-                                static_cast<int64_t>(n) * a.out.sn + h * a.out.sh + lane * 8;
+                                static_cast<int64_t>(n) * a.out.sn + h * a.out.sh + lane * kF;
       const __nv_bfloat16* gp = static_cast<const __nv_bfloat16*>(a.dout.ptr) + b * a.dout.sb +
-                                static_cast<int64_t>(n) * a.dout.sn + h * a.dout.sh + lane * 8;
+                                static_cast<int64_t>(n) * a.dout.sn + h * a.dout.sh + lane * kF;
       const __nv_bfloat16* op = static_cast<const __nv_bfloat16*>(a.o2.ptr) + b * a.o2.sb +
-                                static_cast<int64_t>(n) * a.o2.sn + h * a.o2.sh + lane * 8;
-      const uint4 yv = *reinterpret_cast<const uint4*>(yp);
-      const uint4 gv = *reinterpret_cast<const uint4*>(gp);
-      const uint4 ov = *reinterpret_cast<const uint4*>(op);
-      const __nv_bfloat16* ye = reinterpret_cast<const __nv_bfloat16*>(&yv);
-      const __nv_bfloat16* ge = reinterpret_cast<const __nv_bfloat16*>(&gv);
-      const __nv_bfloat16* oe = reinterpret_cast<const __nv_bfloat16*>(&ov);
+                                static_cast<int64_t>(n) * a.o2.sn + h * a.o2.sh + lane * kF;
+      __nv_bfloat16 ye[kF], ge[kF], oe[kF];
+      ld_bf16<kF>(yp, ye);
+      ld_bf16<kF>(gp, ge);
+      ld_bf16<kF>(op, oe);
       const int64_t sidx = (static_cast<int64_t>(b) * a.H + h) * a.N + n;
       const float rstd = a.rstd[sidx];
       const float inv_c = c != 0.f ? 1.f / c : 0.f;
-      float yh[8], g[8], o2[8], gy = 0.f;
+      float yh[kF], g[kF], o2[kF], gy = 0.f;
 #pragma unroll
-      for (int e = 0; e < 8; ++e) {
+      for (int e = 0; e < kF; ++e) {
         yh[e] = __bfloat162float(ye[e]) * inv_c;
         g[e] = __bfloat162float(ge[e]);
         o2[e] = __bfloat162float(oe[e]);
@@ -286,13 +307,13 @@ v1_bwd_pre_kernel(V1BwdArgs a, BwdWs w) {
       }
 #pragma unroll
       for (int o = 16; o > 0; o >>= 1) gy += __shfl_xor_sync(0xffffffffu, gy, o);
-      const float mean_gy = gy * (1.f / kDv);
+      const float mean_gy = gy * (1.f / DV);
       const float k = c * rstd;
       const float inv_rstd = 1.f / rstd;
       float d1 = 0.f, d2 = 0.f;
-      uint32_t pk[4];
+      uint32_t pk[kF / 2];
 #pragma unroll
-      for (int e = 0; e < 8; e += 2) {
+      for (int e = 0; e < kF; e += 2) {
         const float do0 = k * (g[e] - yh[e] * mean_gy);
         const float do1 = k * (g[e + 1] - yh[e + 1] * mean_gy);
         // round dO to bf16 once; D1 / D2 use the rounded values the MMAs see
@@ -311,10 +332,14 @@ v1_bwd_pre_kernel(V1BwdArgs a, BwdWs w) {
         d2 += __shfl_xor_sync(0xffffffffu, d2, o);
       }
       const int64_t rrow = (static_cast<int64_t>(b) * a.N + n) * a.H + h;
-      *reinterpret_cast<uint4*>(w.dO + rrow * kDv + lane * 8) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      if constexpr (kF == 8) {
+        *reinterpret_cast<uint4*>(w.dO + rrow * DV + lane * kF) = make_uint4(pk[0], pk[1], pk[2], pk[3]);
+      } else {
+        *reinterpret_cast<uint2*>(w.dO + rrow * DV + lane * kF) = make_uint2(pk[0], pk[1]);
+      }
       if (!w.det) {
-        *reinterpret_cast<float4*>(w.dq[0] + rrow * kDqk + lane * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
-        *reinterpret_cast<float4*>(w.dq[1] + rrow * kDqk + lane * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+        st_zero_f32<kFq>(w.dq[0] + rrow * DQK + lane * kFq);
+        st_zero_f32<kFq>(w.dq[1] + rrow * DQK + lane * kFq);
       }
       if (lane == 0) {
         const int64_t pidx = static_cast<int64_t>(bh) * w.npad + n;
@@ -346,6 +371,7 @@ struct Item {
   int b, h, kt, i0, n_it;
 };
 
+template <int DQK, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
 v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__ CUtensorMap tm_q2,
                    const __grid_constant__ CUtensorMap tm_k1, const __grid_constant__ CUtensorMap tm_k2,
@@ -360,6 +386,10 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
     sh.base = al;
     sh.gen = smem_raw + (al - raw);
   }
+  constexpr int kDqk = DQK, kDv = DV;
+  constexpr int kNQ = DQK / 64, kNV = DV / 64;  // 64-column boxes per tile row
+  constexpr uint32_t kIdDV = idesc2(128, DV, 0, 1);   // Psig^T (TMEM) x dO (MN-major)
+  constexpr uint32_t kIdDK = idesc2(128, DQK, 0, 1);  // dS^T (TMEM) x Q (MN-major)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();  // stream index
   const uint32_t partner = rank ^ 1u;
@@ -418,6 +448,14 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
     prefetch_tmap(&tm_do);
     prefetch_tmap(tdq);
   }
+  if (DQK < 128 && warp < 4) {
+    // dQ^T = K^T dS^T runs with M = 128 feature rows: with d_qk = 64 the
+    // second 64-column box of the K tile is never loaded, so zero it once
+    // (feature rows 64-127 of dQ^T come out zero and are not staged)
+    uint4* zk = reinterpret_cast<uint4*>(sh.gen + kOffK + kBoxK);
+    for (int i = threadIdx.x; i < kBoxK / 16; i += 128) zk[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+  }
   tc_fence_before();
   __syncthreads();
   cluster_sync();
@@ -428,10 +466,10 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
   if (warp == 8) {
     // ---------------------------------------------------- TMA producer ----
     if (lane == 0) {
-      mbar_arrive_expect_tx(sh.bar(B_KV), 6 * kBoxK);
-      for (int box = 0; box < 2; ++box)
+      mbar_arrive_expect_tx(sh.bar(B_KV), (kNQ + kNV) * kBoxK);
+      for (int box = 0; box < kNQ; ++box)
         tma_load_4d(sh.base + kOffK + box * kBoxK, tk, sh.bar(B_KV), box * 64, it.h, it.kt * kKT, it.b);
-      for (int box = 0; box < 4; ++box)
+      for (int box = 0; box < kNV; ++box)
         tma_load_4d(sh.base + kOffV + box * kBoxK, &tm_v, sh.bar(B_KV), box * 64, it.h, it.kt * kKT, it.b);
       const size_t srow = (static_cast<size_t>(it.b) * a.H + it.h) * w.npad;
       int last = -1;
@@ -444,10 +482,10 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
         }
         const int q0 = (it.i0 + k) * kQT;
         const uint32_t sb = sh.base + kOffStage + st * kStageBytes;
-        mbar_arrive_expect_tx(sh.bar(B_QFULL + st), 6 * kBoxQ + 512);
-        for (int box = 0; box < 2; ++box)
+        mbar_arrive_expect_tx(sh.bar(B_QFULL + st), (kNQ + kNV) * kBoxQ + 512);
+        for (int box = 0; box < kNQ; ++box)
           tma_load_4d(sb + kStageQ + box * kBoxQ, tq, sh.bar(B_QFULL + st), box * 64, it.h, q0, it.b);
-        for (int box = 0; box < 4; ++box)
+        for (int box = 0; box < kNV; ++box)
           tma_load_4d(sb + kStageDO + box * kBoxQ, &tm_do, sh.bar(B_QFULL + st), box * 64, it.h, q0, it.b);
         const uint32_t lb = sh.base + kOffLse + st * 512;
         bulk_load(lb, lse2 + srow + q0, 256, sh.bar(B_QFULL + st));
@@ -555,6 +593,7 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
       tmem_ld_wait();
       tc_fence_before();
       mbar_arrive(sh.bar(B_DQFREE));
+      if (DQK < 128 && half == 1) continue;  // feature rows 64-127: zero padding
       // the staging buffer alternates between the halves: half 0 of tile k
       // waits until half 1 of tile k-1 has been read (FREE0), half 1 until
       // half 0 of tile k has (FREE1).  One barrier per direction completes
@@ -563,8 +602,11 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
       // does (a single barrier shared by both halves would let such a warp
       // match an older phase of the same parity and overwrite the buffer
       // while it is still being read).
-      if (half == 0 ? (k > 0 && !wait_bar(sh, sh.bar(B_FREE0), (k - 1) & 1, a.status, 0x4302))
-                    : !wait_bar(sh, sh.bar(B_FREE1), k & 1, a.status, 0x4302)) {
+      // With d_qk = 64 there is one half: it waits for its own copy of the
+      // tile before (FREE1, arrived by its issuer), again once per tile.
+      if (DQK < 128 ? (k > 0 && !wait_bar(sh, sh.bar(B_FREE1), (k - 1) & 1, a.status, 0x4302))
+          : half == 0 ? (k > 0 && !wait_bar(sh, sh.bar(B_FREE0), (k - 1) & 1, a.status, 0x4302))
+                      : !wait_bar(sh, sh.bar(B_FREE1), k & 1, a.status, 0x4302)) {
         ok = false;
         break;
       }
@@ -688,7 +730,7 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
       __nv_bfloat16* dkp = static_cast<__nv_bfloat16*>(rank == 0 ? a.dk1.ptr : a.dk2.ptr);
       const da_t4& dkt = rank == 0 ? a.dk1 : a.dk2;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < kDqk / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(T_DK + loff + c * 32, v);
         tmem_ld_wait();
@@ -705,13 +747,15 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
         }
       }
       // dV: swap halves with the partner (the other stream) through DSMEM.
-      // Receive buffer = this CTA's V tile region (idle now): 128 rows x 512 B.
+      // Receive buffer = this CTA's V tile region (idle now): 128 rows of
+      // d_v / 2 fp32.
+      constexpr int kHalf = kDv / 2;
       remote_arrive(map_to_rank(sh.bar(B_RTR), partner));
       if (wait_bar<true>(sh, sh.bar(B_RTR), 0, a.status, 0x4206)) {
-        const int give = (1 - static_cast<int>(rank)) * 128, keep = static_cast<int>(rank) * 128;
-        const uint32_t rx = map_to_rank(sh.base + kOffV + r * 512, partner);
+        const int give = (1 - static_cast<int>(rank)) * kHalf, keep = static_cast<int>(rank) * kHalf;
+        const uint32_t rx = map_to_rank(sh.base + kOffV + r * (kHalf * 4), partner);
 #pragma unroll 1
-        for (int c = 0; c < 4; ++c) {
+        for (int c = 0; c < kHalf / 32; ++c) {
           uint32_t v[32];
           tmem_ld32(T_DV + loff + give + c * 32, v);
           tmem_ld_wait();
@@ -723,11 +767,11 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
         }
         remote_arrive(map_to_rank(sh.bar(B_DATA), partner));
         if (wait_bar<true>(sh, sh.bar(B_DATA), 0, a.status, 0x4207)) {
-          const float* mine = reinterpret_cast<const float*>(sh.gen + kOffV + r * 512);
+          const float* mine = reinterpret_cast<const float*>(sh.gen + kOffV + r * (kHalf * 4));
           __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dv.ptr) + it.b * a.dv.sb +
                                static_cast<int64_t>(key) * a.dv.sn + it.h * a.dv.sh + keep;
 #pragma unroll 1
-          for (int c = 0; c < 4; ++c) {
+          for (int c = 0; c < kHalf / 32; ++c) {
             uint32_t v[32];
             tmem_ld32(T_DV + loff + keep + c * 32, v);
             tmem_ld_wait();
@@ -760,8 +804,10 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
 }
 
 // -------------------------------------------------------------- finalize --
+template <int DQK>
 __global__ void __launch_bounds__(256)
 v1_bwd_finalize_kernel(V1BwdArgs a, BwdWs w) {
+  constexpr int kDqk = DQK;
   const long long rows = static_cast<long long>(a.B) * a.N * a.H;
   const long long total = rows * (kDqk / 8);
   for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
@@ -830,22 +876,14 @@ v1_bwd_finalize_kernel(V1BwdArgs a, BwdWs w) {
   }
 }
 
-}  // namespace
-
-size_t v1_bwd_workspace_bytes(int B, int N, int H, int d_qk, int d_v, int deterministic) {
-  (void)d_qk;
-  (void)d_v;
+template <int DQK, int DV>
+cudaError_t launch_dims(const V1BwdArgs& a, cudaStream_t s) {
+  constexpr int kDqk = DQK, kDv = DV;
   size_t total = 0;
-  carve(nullptr, B, N, H, deterministic != 0, &total);
-  return total;
-}
-
-cudaError_t launch_v1_bwd(const V1BwdArgs& a, cudaStream_t s) {
-  size_t total = 0;
-  BwdWs w = carve(a.workspace, a.B, a.N, a.H, a.deterministic != 0, &total);
+  BwdWs w = carve(a.workspace, a.B, a.N, a.H, DQK, DV, a.deterministic != 0, &total);
   if (total > a.workspace_bytes) return cudaErrorInvalidValue;
 
-  v1_bwd_pre_kernel<<<w.pre_blocks, kPreWarps * 32, 0, s>>>(a, w);
+  v1_bwd_pre_kernel<DQK, DV><<<w.pre_blocks, kPreWarps * 32, 0, s>>>(a, w);
   cudaError_t e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
@@ -858,7 +896,7 @@ cudaError_t launch_v1_bwd(const V1BwdArgs& a, cudaStream_t s) {
       !encode_tmap_bf16_4d(&tv, a.v, a.B, a.N, a.H, kDv, kKT) ||
       !encode_tmap_bf16_4d(&tdo, dot, a.B, a.N, a.H, kDv, kQT))
     return cudaErrorInvalidValue;
-  e = cudaFuncSetAttribute(v1_bwd_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  e = cudaFuncSetAttribute(v1_bwd_main_kernel<DQK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
   if (e != cudaSuccess) return e;
   const int n_kt = (a.N + kKT - 1) / kKT;
   const int items = n_kt * a.B * a.H;
@@ -884,15 +922,29 @@ cudaError_t launch_v1_bwd(const V1BwdArgs& a, cudaStream_t s) {
              !encode_tmap_f32_4d(&tdq2, w.dq[1], a.B, a.N, a.H, kDqk, kQT, 64)) {
     return cudaErrorInvalidValue;
   }
-  e = cudaLaunchKernelEx(&cfg, v1_bwd_main_kernel, tq1, tq2, tk1, tk2, tv, tdo, tdq1, tdq2, a, w);
+  e = cudaLaunchKernelEx(&cfg, v1_bwd_main_kernel<DQK, DV>, tq1, tq2, tk1, tk2, tv, tdo, tdq1, tdq2, a, w);
   if (e != cudaSuccess) return e;
 
   const long long work = static_cast<long long>(a.B) * a.N * a.H * (kDqk / 8);
   int grid = static_cast<int>((work + 255) / 256);
   if (grid > 4 * 152) grid = 4 * 152;
   if (grid < 1) grid = 1;
-  v1_bwd_finalize_kernel<<<grid, 256, 0, s>>>(a, w);
+  v1_bwd_finalize_kernel<DQK><<<grid, 256, 0, s>>>(a, w);
   return cudaGetLastError();
+}
+
+}  // namespace
+
+size_t v1_bwd_workspace_bytes(int B, int N, int H, int d_qk, int d_v, int deterministic) {
+  size_t total = 0;
+  carve(nullptr, B, N, H, d_qk, d_v, deterministic != 0, &total);
+  return total;
+}
+
+cudaError_t launch_v1_bwd(const V1BwdArgs& a, cudaStream_t s) {
+  if (a.d_qk == 128 && a.d_v == 256) return launch_dims<128, 256>(a, s);
+  if (a.d_qk == 64 && a.d_v == 128) return launch_dims<64, 128>(a, s);
+  return cudaErrorInvalidValue;
 }
 
 }  // namespace da

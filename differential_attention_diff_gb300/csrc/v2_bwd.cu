@@ -39,6 +39,8 @@
 // Warp roles (320 threads): 0-3 softmax / dK epilogue, 4-7 dQ readback and
 // reduce / dV epilogue, 8 TMA producer, 9 MMA issuer.
 // TMEM: [0,128) dV, [128,256) dK, [256,384) S^T x 2, [384,512) dP^T / dQ^T x 2.
+// Head dim d = 128 or 64 (d = 64: half of each K, V, Q, dO tile, dV and dK
+// in the first 64 columns of their regions, dQ^T with 64 zero feature rows).
 // SMEM: K 32 KB, V 32 KB, 3 stages of (Q 16 KB, dO 16 KB), dS^T x 2
 //       (16 KB each), dQ staging 32 KB, per-stage lse2 / D (1.5 KB); every
 //       bf16 operand in 128-byte-swizzled 64-column boxes.  The MMAs are
@@ -57,7 +59,7 @@ namespace {
 
 constexpr int kKT = 128;  // keys per item
 constexpr int kQT = 64;   // queries per iteration
-constexpr int kD = 128;
+constexpr int kD = 128;   // the largest head dim: shared-memory layout and workspace sizing
 constexpr int kThreads = 320;
 constexpr int kStages = 3;
 
@@ -88,8 +90,8 @@ __host__ __device__ constexpr uint32_t idesc2(int M, int N, int a_mn, int b_mn) 
          (static_cast<uint32_t>(M >> 4) << 24);
 }
 constexpr uint32_t kIdS = idesc2(128, 64, 0, 0);    // K (K-major) x Q (K-major); V x dO
-constexpr uint32_t kIdAcc = idesc2(128, 128, 0, 1); // P^T / dS^T (TMEM) x dO / Q (MN-major)
 constexpr uint32_t kIdDQ = idesc2(128, 64, 1, 1);   // K^T (MN-major) x dS^T (MN-major)
+// (P^T / dS^T (TMEM) x dO / Q (MN-major) is idesc2(128, D, 0, 1) per head dim)
 
 __device__ __forceinline__ uint64_t globaltimer() {
   uint64_t t;
@@ -138,10 +140,10 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 constexpr int kDwChunk = 1024;  // tokens per dW partial sum
 
 struct BwdWs {
-  __nv_bfloat16* dodd;  // [B, N, h, 128]  dO of the odd heads = -g G
+  __nv_bfloat16* dodd;  // [B, N, h, d]  dO of the odd heads = -g G (room for d = 128)
   float* lse2;          // [B, 2h, Npad]   LSE * log2 e; +inf in padding rows
   float* D;             // [B, 2h, Npad]
-  float* dq;            // [B, N, 2h, 128] fp32 accumulators
+  float* dq;            // [B, N, 2h, d] fp32 accumulators (room for d = 128)
   float* gate;          // [B, N, h]  when computed here
   float* dz;            // [B, N, h]  when the caller keeps none
   float* dw_part;       // [chunks, d_model, h]
@@ -179,8 +181,29 @@ BwdWs carve(void* base, int B, int N, int h, int d_model, size_t* total) {
 // ------------------------------------------------------------ preprocess --
 constexpr int kPreWarps = 8;
 
+// kF consecutive bf16 / fp32 values of one lane (kF = 4 or 2)
+template <int kF>
+__device__ __forceinline__ void ld_bf16(const __nv_bfloat16* p, __nv_bfloat16 (&v)[kF]) {
+  if constexpr (kF == 4) {
+    *reinterpret_cast<uint2*>(v) = *reinterpret_cast<const uint2*>(p);
+  } else {
+    *reinterpret_cast<uint32_t*>(v) = *reinterpret_cast<const uint32_t*>(p);
+  }
+}
+template <int kF>
+__device__ __forceinline__ void st_zero_f32(float* p) {
+  if constexpr (kF == 4) {
+    *reinterpret_cast<float4*>(p) = make_float4(0.f, 0.f, 0.f, 0.f);
+  } else {
+    *reinterpret_cast<float2*>(p) = make_float2(0.f, 0.f);
+  }
+}
+
+// one warp per (token, pair); lane = D / 32 consecutive features
+template <int D>
 __global__ void __launch_bounds__(kPreWarps * 32)
 v2_bwd_pre_kernel(V2BwdArgs a, BwdWs w, const float* __restrict__ gate, float* __restrict__ dz) {
+  constexpr int kF = D / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const long long row = static_cast<long long>(blockIdx.x) * kPreWarps + warp;  // (b, p, n < npad)
   const long long total = static_cast<long long>(a.B) * a.h * w.npad;
@@ -201,21 +224,19 @@ v2_bwd_pre_kernel(V2BwdArgs a, BwdWs w, const float* __restrict__ gate, float* _
     return;
   }
   const __nv_bfloat16* gp = static_cast<const __nv_bfloat16*>(a.dout.ptr) + b * a.dout.sb +
-                            static_cast<int64_t>(n) * a.dout.sn + p * a.dout.sh + lane * 4;
+                            static_cast<int64_t>(n) * a.dout.sn + p * a.dout.sh + lane * kF;
   const __nv_bfloat16* op = static_cast<const __nv_bfloat16*>(a.o_heads.ptr) + b * a.o_heads.sb +
-                            static_cast<int64_t>(n) * a.o_heads.sn + he * a.o_heads.sh + lane * 4;
-  const uint2 gv = *reinterpret_cast<const uint2*>(gp);
-  const uint2 ev = *reinterpret_cast<const uint2*>(op);
-  const uint2 ov = *reinterpret_cast<const uint2*>(op + a.o_heads.sh);
-  const __nv_bfloat16* ge = reinterpret_cast<const __nv_bfloat16*>(&gv);
-  const __nv_bfloat16* ee = reinterpret_cast<const __nv_bfloat16*>(&ev);
-  const __nv_bfloat16* oe = reinterpret_cast<const __nv_bfloat16*>(&ov);
+                            static_cast<int64_t>(n) * a.o_heads.sn + he * a.o_heads.sh + lane * kF;
+  __nv_bfloat16 ge[kF], ee[kF], oe[kF];
+  ld_bf16<kF>(gp, ge);
+  ld_bf16<kF>(op, ee);
+  ld_bf16<kF>(op + a.o_heads.sh, oe);
   const int64_t tp = (static_cast<int64_t>(b) * a.N + n) * a.h + p;
   const float g = gate[tp];
   float de = 0.f, dd = 0.f, go = 0.f;
-  uint32_t pk[2];
+  uint32_t pk[kF / 2];
 #pragma unroll
-  for (int e = 0; e < 4; e += 2) {
+  for (int e = 0; e < kF; e += 2) {
     const float g0 = __bfloat162float(ge[e]), g1 = __bfloat162float(ge[e + 1]);
     // the odd head's dO is an MMA operand: round it once, and take D from
     // the rounded values the MMAs see
@@ -235,10 +256,14 @@ v2_bwd_pre_kernel(V2BwdArgs a, BwdWs w, const float* __restrict__ gate, float* _
     dd += __shfl_xor_sync(0xffffffffu, dd, o);
     go += __shfl_xor_sync(0xffffffffu, go, o);
   }
-  *reinterpret_cast<uint2*>(w.dodd + tp * kD + lane * 4) = make_uint2(pk[0], pk[1]);
+  if constexpr (kF == 4) {
+    *reinterpret_cast<uint2*>(w.dodd + tp * D + lane * kF) = make_uint2(pk[0], pk[1]);
+  } else {
+    *reinterpret_cast<uint32_t*>(w.dodd + tp * D + lane * kF) = pk[0];
+  }
   const int64_t qrow = (static_cast<int64_t>(b) * a.N + n) * 2 * a.h + he;
-  *reinterpret_cast<float4*>(w.dq + qrow * kD + lane * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
-  *reinterpret_cast<float4*>(w.dq + (qrow + 1) * kD + lane * 4) = make_float4(0.f, 0.f, 0.f, 0.f);
+  st_zero_f32<kF>(w.dq + qrow * D + lane * kF);
+  st_zero_f32<kF>(w.dq + (qrow + 1) * D + lane * kF);
   if (lane == 0) {
     const int64_t le = (static_cast<int64_t>(b) * 2 * a.h + he) * a.N + n;
     w.lse2[se] = a.lse[le] * 1.4426950408889634f;
@@ -274,6 +299,7 @@ __device__ __forceinline__ Item item_of(int i, int n_kt, int n_qt, int units, in
   return it;
 }
 
+template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
 v2_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
@@ -287,6 +313,8 @@ v2_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     sh.base = al;
     sh.gen = smem_raw + (al - raw);
   }
+  constexpr int kNB = D / 64;  // 64-column boxes per tile row
+  constexpr uint32_t kIdAcc = idesc2(128, D, 0, 1);  // P^T / dS^T (TMEM) x dO / Q (MN-major)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = (2 * a.h) / a.h_kv;
   const int n_kt = (a.N + kKT - 1) / kKT;
@@ -324,6 +352,14 @@ v2_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
     prefetch_tmap(&tm_do);
     prefetch_tmap(&tm_dq);
   }
+  if (D < 128 && warp < 4) {
+    // dQ^T = K^T dS^T runs with M = 128 feature rows: with head dim 64 the
+    // second 64-column box of the K tile is never loaded, so zero it once
+    // (feature rows 64-127 of dQ^T come out zero and are not stored)
+    uint4* zk = reinterpret_cast<uint4*>(sh.gen + kOffK + kBoxK);
+    for (int i = threadIdx.x; i < kBoxK / 16; i += 128) zk[i] = make_uint4(0u, 0u, 0u, 0u);
+    fence_proxy_async_smem();
+  }
   tc_fence_before();
   __syncthreads();
   tc_fence_after();
@@ -338,10 +374,10 @@ v2_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   if (warp == 8) {
     // ---------------------------------------------------- TMA producer ----
     if (lane == 0) {
-      mbar_arrive_expect_tx(sh.bar(B_KV), 4 * kBoxK);
-      for (int box = 0; box < 2; ++box)
+      mbar_arrive_expect_tx(sh.bar(B_KV), 2 * kNB * kBoxK);
+      for (int box = 0; box < kNB; ++box)
         tma_load_4d(sh.base + kOffK + box * kBoxK, &tm_k, sh.bar(B_KV), box * 64, it.g, it.kt * kKT, it.b);
-      for (int box = 0; box < 2; ++box)
+      for (int box = 0; box < kNB; ++box)
         tma_load_4d(sh.base + kOffV + box * kBoxK, &tm_v, sh.bar(B_KV), box * 64, it.g, it.kt * kKT, it.b);
       int last = -1;
       bool ok = true;
@@ -355,12 +391,12 @@ v2_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         const int q0 = q0_of(k);
         const uint32_t sb = sh.base + kOffStage + st * kStageBytes;
         const uint32_t bar = sh.bar(B_QFULL + st);
-        mbar_arrive_expect_tx(bar, 4 * kBoxQ + 512);
-        for (int box = 0; box < 2; ++box)
+        mbar_arrive_expect_tx(bar, 2 * kNB * kBoxQ + 512);
+        for (int box = 0; box < kNB; ++box)
           tma_load_4d(sb + kStageQ + box * kBoxQ, &tm_q, bar, box * 64, qh, q0, it.b);
         // dO of an even head is dOut itself; of an odd head, -g dOut (workspace)
         const CUtensorMap* tdo = (qh & 1) ? &tm_do : &tm_g;
-        for (int box = 0; box < 2; ++box)
+        for (int box = 0; box < kNB; ++box)
           tma_load_4d(sb + kStageDO + box * kBoxQ, tdo, bar, box * 64, qh >> 1, q0, it.b);
         const size_t srow = (static_cast<size_t>(it.b) * 2 * a.h + qh) * w.npad + q0;
         const uint32_t lb = sh.base + kOffLse + st * 512;
@@ -393,14 +429,14 @@ v2_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       auto issue_sdp = [&](int k) {  // S^T = K Q^T and dP^T = V dO^T into buffers k & 1
         const uint32_t qb = stage(k) + kStageQ, db = stage(k) + kStageDO;
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
+        for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t offa = (kk >> 2) * kBoxK + (kk & 3) * 32;
           const uint32_t offb = (kk >> 2) * kBoxQ + (kk & 3) * 32;
           tc_mma_ss(t_s(k & 1), sdesc_sw128(kA + offa, 16, 1024), sdesc_sw128(qb + offb, 16, 1024), kIdS,
                     kk > 0);
         }
 #pragma unroll
-        for (int kk = 0; kk < kD / 16; ++kk) {
+        for (int kk = 0; kk < D / 16; ++kk) {
           const uint32_t offa = (kk >> 2) * kBoxK + (kk & 3) * 32;
           const uint32_t offb = (kk >> 2) * kBoxQ + (kk & 3) * 32;
           tc_mma_ss(t_d(k & 1), sdesc_sw128(vA + offa, 16, 1024), sdesc_sw128(db + offb, 16, 1024), kIdS,
@@ -557,7 +593,7 @@ v2_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dk.ptr) + it.b * a.dk.sb +
                            static_cast<int64_t>(key) * a.dk.sn + it.g * a.dk.sh;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(T_DK + loff + c * 32, v);
         tmem_ld_wait();
@@ -597,15 +633,18 @@ v2_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         ok = false;
         break;
       }
+      // [64 queries][D] fp32; feature rows past D (zero) are not staged
+      if (r < D) {
 #pragma unroll
-      for (int c = 0; c < kQT; ++c) stage_dq[c * kD + r] = __uint_as_float(qv[c]);
+        for (int c = 0; c < kQT; ++c) stage_dq[c * D + r] = __uint_as_float(qv[c]);
+      }
       fence_proxy_async_smem();
       mbar_arrive(sh.bar(B_STG));
       bool stg_ok = true;
       if (r == 0) {
         stg_ok = wait_bar(sh, sh.bar(B_STG), k & 1, a.status, 0x6303);
         if (stg_ok) {
-          // add the [64 queries][128] tile to the fp32 accumulator (rows
+          // add the [64 queries][D] tile to the fp32 accumulator (rows
           // past N are dropped by the unit)
           tma_reduce_add_4d(&tm_dq, sh.base + kOffDQ, 0, it.g * G + head_of(k), q0_of(k), it.b);
           bulk_commit();
@@ -626,7 +665,7 @@ v2_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dv.ptr) + it.b * a.dv.sb +
                            static_cast<int64_t>(key) * a.dv.sn + it.g * a.dv.sh;
 #pragma unroll 1
-      for (int c = 0; c < 4; ++c) {
+      for (int c = 0; c < D / 32; ++c) {
         uint32_t v[32];
         tmem_ld32(T_DV + loff + c * 32, v);
         tmem_ld_wait();
@@ -650,19 +689,20 @@ v2_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
 }
 
 // -------------------------------------------------------------- finalize --
+template <int D>
 __global__ void __launch_bounds__(256)
 v2_bwd_finalize_kernel(V2BwdArgs a, BwdWs w) {
   const int H2 = 2 * a.h;
   const long long rows = static_cast<long long>(a.B) * a.N * H2;
-  const long long total = rows * (kD / 8);
+  const long long total = rows * (D / 8);
   for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
        idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const long long row = idx / (kD / 8);
-    const int c8 = static_cast<int>(idx % (kD / 8)) * 8;
+    const long long row = idx / (D / 8);
+    const int c8 = static_cast<int>(idx % (D / 8)) * 8;
     const int hq = static_cast<int>(row % H2);
     const long long bn = row / H2;
     const int n = static_cast<int>(bn % a.N), b = static_cast<int>(bn / a.N);
-    const float* src = w.dq + row * kD + c8;
+    const float* src = w.dq + row * D + c8;
     const float4 x0 = *reinterpret_cast<const float4*>(src);
     const float4 x1 = *reinterpret_cast<const float4*>(src + 4);
     __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dq.ptr) + b * a.dq.sb +
@@ -808,6 +848,50 @@ cudaError_t launch_dx(int T, int d_model, int h, const float* dz, const void* W,
   return cudaGetLastError();
 }
 
+// the attention part: preprocess, main, finalize for head dim D
+template <int D>
+cudaError_t launch_attn(const V2BwdArgs& a, const BwdWs& w, float* dz, cudaStream_t s) {
+  const long long T = static_cast<long long>(a.B) * a.N;
+  cudaError_t e;
+  const long long pre_rows = static_cast<long long>(a.B) * a.h * w.npad;
+  v2_bwd_pre_kernel<D><<<static_cast<unsigned>((pre_rows + kPreWarps - 1) / kPreWarps), kPreWarps * 32, 0, s>>>(
+      a, w, a.gate, dz);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  CUtensorMap tq, tk, tv, tg, tdo, tdq;
+  const da_t4 dot{w.dodd, static_cast<int64_t>(a.N) * a.h * D, static_cast<int64_t>(a.h) * D, D};
+  if (!encode_tmap_bf16_4d(&tq, a.q, a.B, a.N, 2 * a.h, D, kQT) ||
+      !encode_tmap_bf16_4d(&tk, a.k, a.B, a.N, a.h_kv, D, kKT) ||
+      !encode_tmap_bf16_4d(&tv, a.v, a.B, a.N, a.h_kv, D, kKT) ||
+      !encode_tmap_bf16_4d(&tg, a.dout, a.B, a.N, a.h, D, kQT) ||
+      !encode_tmap_bf16_4d(&tdo, dot, a.B, a.N, a.h, D, kQT) ||
+      !encode_tmap_f32_4d(&tdq, w.dq, a.B, a.N, 2 * a.h, D, kQT))
+    return cudaErrorInvalidValue;
+  e = cudaFuncSetAttribute(v2_bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
+  if (e != cudaSuccess) return e;
+  const int n_kt = (a.N + kKT - 1) / kKT;
+  const int units = a.B * a.h_kv;
+  const int sms = a.num_sms > 0 ? a.num_sms : 148;
+  // (batch, group) units per scheduling block: about two waves of items
+  int per = (2 * sms + n_kt - 1) / n_kt;
+  if (per < 1) per = 1;
+  if (per > units) per = units;
+  v2_bwd_main_kernel<D><<<n_kt * units, kThreads, kSmemBytes, s>>>(tq, tk, tv, tg, tdo, tdq, a, w, per);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  const long long work = T * 2 * a.h * (D / 8);
+  int grid = static_cast<int>((work + 255) / 256);
+  if (grid > 8 * sms) grid = 8 * sms;
+  if (grid < 1) grid = 1;
+  v2_bwd_finalize_kernel<D><<<grid, 256, 0, s>>>(a, w);
+  e = cudaGetLastError();
+  if (e != cudaSuccess) return e;
+
+  return cudaSuccess;
+}
+
 }  // namespace
 
 size_t v2_bwd_workspace_bytes(int B, int N, int h, int d_model) {
@@ -831,41 +915,10 @@ cudaError_t launch_v2_bwd(const V2BwdArgs& a_in, cudaStream_t s) {
   }
   float* dz = a.dz ? a.dz : w.dz;
 
-  const long long pre_rows = static_cast<long long>(a.B) * a.h * w.npad;
-  v2_bwd_pre_kernel<<<static_cast<unsigned>((pre_rows + kPreWarps - 1) / kPreWarps), kPreWarps * 32, 0, s>>>(
-      a, w, a.gate, dz);
-  e = cudaGetLastError();
+  e = a.d == 128 ? launch_attn<128>(a, w, dz, s) : a.d == 64 ? launch_attn<64>(a, w, dz, s)
+                                                              : cudaErrorInvalidValue;
   if (e != cudaSuccess) return e;
-
-  CUtensorMap tq, tk, tv, tg, tdo, tdq;
-  const da_t4 dot{w.dodd, static_cast<int64_t>(a.N) * a.h * kD, static_cast<int64_t>(a.h) * kD, kD};
-  if (!encode_tmap_bf16_4d(&tq, a.q, a.B, a.N, 2 * a.h, kD, kQT) ||
-      !encode_tmap_bf16_4d(&tk, a.k, a.B, a.N, a.h_kv, kD, kKT) ||
-      !encode_tmap_bf16_4d(&tv, a.v, a.B, a.N, a.h_kv, kD, kKT) ||
-      !encode_tmap_bf16_4d(&tg, a.dout, a.B, a.N, a.h, kD, kQT) ||
-      !encode_tmap_bf16_4d(&tdo, dot, a.B, a.N, a.h, kD, kQT) ||
-      !encode_tmap_f32_4d(&tdq, w.dq, a.B, a.N, 2 * a.h, kD, kQT))
-    return cudaErrorInvalidValue;
-  e = cudaFuncSetAttribute(v2_bwd_main_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
-  if (e != cudaSuccess) return e;
-  const int n_kt = (a.N + kKT - 1) / kKT;
-  const int units = a.B * a.h_kv;
   const int sms = a.num_sms > 0 ? a.num_sms : 148;
-  // (batch, group) units per scheduling block: about two waves of items
-  int per = (2 * sms + n_kt - 1) / n_kt;
-  if (per < 1) per = 1;
-  if (per > units) per = units;
-  v2_bwd_main_kernel<<<n_kt * units, kThreads, kSmemBytes, s>>>(tq, tk, tv, tg, tdo, tdq, a, w, per);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
-
-  const long long work = T * 2 * a.h * (kD / 8);
-  int grid = static_cast<int>((work + 255) / 256);
-  if (grid > 8 * sms) grid = 8 * sms;
-  if (grid < 1) grid = 1;
-  v2_bwd_finalize_kernel<<<grid, 256, 0, s>>>(a, w);
-  e = cudaGetLastError();
-  if (e != cudaSuccess) return e;
 
   if (a.dx) {
     e = launch_dx(static_cast<int>(T), a.d_model, a.h, dz, a.w, a.dx, s);

@@ -136,6 +136,10 @@ def test_bwd_workspace_size(lib):
     base = lib.diffattn_v1_bwd_workspace_size(1, 8192, 16, 128, 256, 0)
     det = lib.diffattn_v1_bwd_workspace_size(1, 8192, 16, 128, 256, 1)
     assert base > 0 and lib.diffattn_v1_bwd_workspace_size(0, 8192, 16, 128, 256, 0) == 0
+    # head dims (64, 128): dO and the dQ accumulators shrink by half (per row:
+    # d_v bf16 of dO + 2 streams x d_qk fp32 = 512 -> 256 bytes)
+    small = lib.diffattn_v1_bwd_workspace_size(1, 8192, 16, 64, 128, 0)
+    assert base - small >= 8192 * 16 * 256
     # deterministic mode: one fp32 [64, 128] slot per causal (key tile, query
     # tile) pair and stream replaces the [N, 128] accumulators
     n_kt, n_qt = 8192 // 128, 8192 // 64
@@ -217,7 +221,7 @@ def test_v2_bwd_argument_checks(lib):
         return C.byref(q)
     assert f(with_(h_kv=3), None) == bd.DA_ERR_INVALID_ARG       # 2h not divisible into groups
     assert f(with_(h=1, h_kv=2), None) == bd.DA_ERR_INVALID_ARG  # a pair would straddle groups
-    assert f(with_(d=64), None) == bd.DA_ERR_UNSUPPORTED
+    assert f(with_(d=96), None) == bd.DA_ERR_UNSUPPORTED
     assert f(with_(lse=None), None) == bd.DA_ERR_INVALID_ARG     # the forward's saves are needed
     assert f(with_(gate=None), None) == bd.DA_ERR_INVALID_ARG    # no gate and no x / w_lambda
     assert f(with_(dx=fake), None) == bd.DA_ERR_INVALID_ARG      # dX needs x and w_lambda

@@ -111,6 +111,41 @@ def test_v1_bwd_parity_small(B, N, H, layer):
     _compare(_run(t, li), ref, model, bar="step")
 
 
+@pytest.mark.parametrize("B,N,H,layer", [(1, 200, 2, 1), (2, 129, 1, 14), (1, 1, 1, 1), (1, 500, 2, 5)])
+def test_v1_bwd_parity_head_dims_64_128(B, N, H, layer):
+    """Head dims (64, 128): half-width K, Q tiles, one dQ^T half (feature rows
+    64-127 are zero padding), dV halves of 64 columns exchanged."""
+    t = synth.v1_inputs(B, N, H, 64, 128, "bf16", seed=5100 + N + H, device="cuda", with_dy=True)
+    li = float(np.float32(bd.diffattn_lambda_init(layer)))
+    ref = orc.v1_backward(*(f64(t[n]) for n in NAMES), li, f64(t["dy"]))
+    model = _model(t, li)
+    _compare(_run_exact_saves(t, li), ref, model, bar="bwd")
+    _compare(_run(t, li), ref, model, bar="step")
+
+
+def test_v1_bwd_deterministic_head_dims_64_128():
+    """Deterministic dQ slots at head dims (64, 128): a bitwise repeat; dK, dV
+    and the lambda-vector gradients bitwise equal to the default mode's (the
+    mode changes only how dQ leaves the main kernel); dQ, dK, dV against the
+    oracle.  (The lambda-vector gradients' oracle bar is checked by the
+    backward-alone parity tests: in a training step dlambda sums <dO, O2> over
+    every row of the bf16 forward outputs, whose own error the rounding model
+    does not count.)"""
+    t = synth.v1_inputs(1, 400, 2, 64, 128, "bf16", seed=5150, device="cuda", with_dy=True)
+    li = float(np.float32(bd.diffattn_lambda_init(3)))
+    y, sv = bd.diffattn_v1_fwd(*(t[n] for n in NAMES), li, save=True)
+    g0 = bd.diffattn_v1_bwd(*(t[n] for n in NAMES), li, y, t["dy"], sv)
+    g1 = bd.diffattn_v1_bwd(*(t[n] for n in NAMES), li, y, t["dy"], sv, deterministic=True)
+    g2 = bd.diffattn_v1_bwd(*(t[n] for n in NAMES), li, y, t["dy"], sv, deterministic=True)
+    torch.cuda.synchronize()
+    for n in g1:
+        assert torch.equal(g1[n], g2[n]), n
+    for n in ("dk1", "dk2", "dv", "dlq1", "dlk1", "dlq2", "dlk2"):
+        assert torch.equal(g0[n], g1[n]), n
+    ref = orc.v1_backward(*(f64(t[n]) for n in NAMES), li, f64(t["dy"]))
+    _compare(g1, ref, _model(t, li), lam_vectors=False, bar="step")
+
+
 def test_v1_bwd_deterministic_parts_repeat():
     """dK and dV come from one CTA each (no atomics): bitwise equal on a rerun."""
     t = synth.v1_inputs(1, 300, 2, 128, 256, "bf16", seed=61, device="cuda", with_dy=True)

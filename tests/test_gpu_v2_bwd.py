@@ -101,6 +101,16 @@ def test_v2_bwd_parity_small(B, N, h, hkv):
     _compare(_run(t), ref, model, bar="step")
 
 
+@pytest.mark.parametrize("B,N,h,hkv", [(1, 200, 2, 1), (2, 129, 2, 2), (1, 1, 1, 1), (1, 300, 4, 1)])
+def test_v2_bwd_parity_head_dim_64(B, N, h, hkv):
+    """Head dim 64: half-width K, V, Q and dO tiles, dV and dK in 64 TMEM
+    columns, dQ^T with 64 zero feature rows that are never stored."""
+    t = synth.v2_inputs(B, N, h, hkv, 64, 128, seed=7200 + N + h, device="cuda", with_dout=True)
+    ref, fwd, model = _reference(t)
+    _compare(_run_exact_saves(t, fwd), ref, model, bar="bwd")
+    _compare(_run(t), ref, model, bar="step")
+
+
 def test_v2_bwd_gate_given_matches_gate_from_x():
     """A caller-supplied gate (the same values) gives the same dQ, dK, dV as
     the gate computed from x and W inside the call."""
