@@ -238,8 +238,7 @@ da_status diffattn_v1_fwd(const da_v1_fwd_params* p, void* stream) {
                     p->lq1, p->lk1, p->lq2, p->lk2, p->lse1, p->lse2, p->rstd, p->lambda_out};
     return cuda_status(da::launch_v1_fwd_f32(a, s));
   }
-  if (!((p->d_qk == 128 && p->d_v == 256) || (p->d_qk == 64 && p->d_v == 128)) || !p->causal)
-    return DA_ERR_UNSUPPORTED;
+  if (!((p->d_qk == 128 && p->d_v == 256) || (p->d_qk == 64 && p->d_v == 128))) return DA_ERR_UNSUPPORTED;
   const size_t need = da::v1_fwd_workspace_bytes(d.num_sms);
   if (need && (p->workspace == nullptr || p->workspace_bytes < need || !aligned(p->workspace, 256)))
     return DA_ERR_WORKSPACE;
@@ -265,8 +264,9 @@ da_status diffattn_v1_bwd(const da_v1_bwd_params* p, void* stream) {
   if (!p->lq1 || !p->lk1 || !p->lq2 || !p->lk2) return DA_ERR_INVALID_ARG;
   if (!p->dlq1 || !p->dlk1 || !p->dlq2 || !p->dlk2) return DA_ERR_INVALID_ARG;
   if (p->B == 0 || p->N == 0 || p->H == 0) return DA_OK;
+  // deterministic slots are laid out for the causal (key tile, query tile) pairs
   if (p->dtype != DA_BF16 || !((p->d_qk == 128 && p->d_v == 256) || (p->d_qk == 64 && p->d_v == 128)) ||
-      !p->causal)
+      (p->deterministic && !p->causal))
     return DA_ERR_UNSUPPORTED;
   for (const da_t4* t : {&p->q1, &p->q2, &p->k1, &p->k2, &p->v, &p->out, &p->dout, &p->o2,
                          &p->dq1, &p->dq2, &p->dk1, &p->dk2, &p->dv})
@@ -299,7 +299,7 @@ da_status diffattn_v2_fwd(const da_v2_fwd_params* p, void* stream) {
   if ((2 * p->h) % p->h_kv) return DA_ERR_INVALID_ARG;
   if ((2 * p->h / p->h_kv) % 2) return DA_ERR_INVALID_ARG;
   if (p->B == 0 || p->N == 0) return DA_OK;
-  if ((p->d != 64 && p->d != 128) || !p->causal) return DA_ERR_UNSUPPORTED;
+  if (p->d != 64 && p->d != 128) return DA_ERR_UNSUPPORTED;
   for (const da_t4* t : {&p->q, &p->k, &p->v, &p->out})
     if (check_t4(*t, DA_BF16) != DA_OK) return DA_ERR_INVALID_ARG;
   if (p->o_heads.ptr && check_t4(p->o_heads, DA_BF16) != DA_OK) return DA_ERR_INVALID_ARG;
@@ -344,7 +344,7 @@ da_status diffattn_v2_bwd(const da_v2_bwd_params* p, void* stream) {
   if ((2 * p->h) % p->h_kv) return DA_ERR_INVALID_ARG;
   if ((2 * p->h / p->h_kv) % 2) return DA_ERR_INVALID_ARG;
   if (p->B == 0 || p->N == 0) return DA_OK;
-  if ((p->d != 64 && p->d != 128) || !p->causal) return DA_ERR_UNSUPPORTED;
+  if (p->d != 64 && p->d != 128) return DA_ERR_UNSUPPORTED;
   for (const da_t4* t : {&p->q, &p->k, &p->v, &p->o_heads, &p->dout, &p->dq, &p->dk, &p->dv})
     if (check_t4(*t, DA_BF16) != DA_OK) return DA_ERR_INVALID_ARG;
   if (p->lse == nullptr || !aligned(p->lse, 4)) return DA_ERR_INVALID_ARG;
@@ -444,7 +444,7 @@ da_status diffattn_grouped_fwd(const da_grouped_fwd_params* p, void* stream) {
   const int G = Hq / p->h_kv;
   if (G % (p->ratio + 1)) return DA_ERR_INVALID_ARG;  // a group must sit in one K/V group
   if (p->B == 0 || p->N == 0) return DA_OK;
-  if ((p->d != 64 && p->d != 128) || !p->causal || (G % 2)) return DA_ERR_UNSUPPORTED;
+  if ((p->d != 64 && p->d != 128) || (G % 2)) return DA_ERR_UNSUPPORTED;
   for (const da_t4* t : {&p->q, &p->k, &p->v, &p->out})
     if (check_t4(*t, DA_BF16) != DA_OK) return DA_ERR_INVALID_ARG;
   if (p->o_heads.ptr && check_t4(p->o_heads, DA_BF16) != DA_OK) return DA_ERR_INVALID_ARG;

@@ -13,7 +13,8 @@
 //    the 127 max operations per tile;  when the guard trips (scores far
 //    above every earlier one) the warp recomputes the tile against the new
 //    max and reports the rescale factor for O and l;
-//  * masking (key > query) only on the diagonal tile;
+//  * masking (key > query) only on the diagonal tile, or (not causal) only
+//    on a ragged last key tile (key >= N);
 //  * scale-and-subtract and the row sum use packed f32x2 FMA / add;
 //  * the score chunks are loaded from TMEM in two halves so that the second
 //    half's load overlaps the first half's exponentials.
@@ -50,10 +51,10 @@ __device__ __forceinline__ uint64_t add_f32x2(uint64_t a, uint64_t b) {
 }
 
 // exp2 of 32 scores (one TMEM chunk starting at key col0) against max m
-// (negm2 = {-m, -m}); writes 16 bf16x2 words to TMEM at t_p; returns the
-// pairwise partial sums.
+// (negm2 = {-m, -m}), columns past lim zeroed when kMask; writes 16 bf16x2
+// words to TMEM at t_p; returns the pairwise partial sums.
 template <bool kMask>
-__device__ __forceinline__ uint64_t exp_chunk(const uint32_t* s, int col0, int row, uint64_t sl2x2,
+__device__ __forceinline__ uint64_t exp_chunk(const uint32_t* s, int col0, int lim, uint64_t sl2x2,
                                               uint64_t negm2, uint32_t t_p) {
   uint32_t pk[16];
   uint64_t acc = 0;
@@ -65,8 +66,8 @@ __device__ __forceinline__ uint64_t exp_chunk(const uint32_t* s, int col0, int r
     float p0 = fast_exp2(f2_lo(x));
     float p1 = fast_exp2(f2_hi(x));
     if (kMask) {
-      if (col0 + 2 * e > row) p0 = 0.f;
-      if (col0 + 2 * e + 1 > row) p1 = 0.f;
+      if (col0 + 2 * e > lim) p0 = 0.f;
+      if (col0 + 2 * e + 1 > lim) p1 = 0.f;
     }
     acc = add_f32x2(acc, f2(p0, p1));
     pk[e] = pack_bf16x2(p0, p1);
@@ -76,34 +77,37 @@ __device__ __forceinline__ uint64_t exp_chunk(const uint32_t* s, int col0, int r
 }
 
 template <bool kMask>
-__device__ __forceinline__ float exp_row(const uint32_t (&s)[128], int row, uint64_t sl2x2,
+__device__ __forceinline__ float exp_row(const uint32_t (&s)[128], int lim, uint64_t sl2x2,
                                          float m, uint32_t t_s) {
   const uint64_t negm2 = f2(-m, -m);
-  uint64_t a0 = exp_chunk<kMask>(s, 0, row, sl2x2, negm2, t_s);
-  uint64_t a1 = exp_chunk<kMask>(s + 32, 32, row, sl2x2, negm2, t_s + 16);
-  uint64_t a2 = exp_chunk<kMask>(s + 64, 64, row, sl2x2, negm2, t_s + 32);
-  uint64_t a3 = exp_chunk<kMask>(s + 96, 96, row, sl2x2, negm2, t_s + 48);
+  uint64_t a0 = exp_chunk<kMask>(s, 0, lim, sl2x2, negm2, t_s);
+  uint64_t a1 = exp_chunk<kMask>(s + 32, 32, lim, sl2x2, negm2, t_s + 16);
+  uint64_t a2 = exp_chunk<kMask>(s + 64, 64, lim, sl2x2, negm2, t_s + 32);
+  uint64_t a3 = exp_chunk<kMask>(s + 96, 96, lim, sl2x2, negm2, t_s + 48);
   const uint64_t t = add_f32x2(add_f32x2(a0, a1), add_f32x2(a2, a3));
   return f2_lo(t) + f2_hi(t);
 }
 
 template <bool kMask>
-__device__ __forceinline__ float row_max(const uint32_t (&s)[128], int row) {
+__device__ __forceinline__ float row_max(const uint32_t (&s)[128], int lim) {
   float mx = -INFINITY;
 #pragma unroll
   for (int e = 0; e < 128; ++e) {
     const float v = __uint_as_float(s[e]);
-    if (!kMask || e <= row) mx = fmaxf(mx, v);
+    if (!kMask || e <= lim) mx = fmaxf(mx, v);
   }
   return mx;
 }
 
 // One tile of one row.  t_s: TMEM address of the row's 128 scores (lane
-// offset included).  Updates (m_run, l_run); returns the factor the row's O
-// accumulator must be multiplied by before the next P.V (1 = unchanged; the
-// first tile returns 0: O has no content yet).  Warp-uniform control flow:
-// `first` and `diag` are the same for the whole warp.
-__device__ __forceinline__ float softmax_tile(uint32_t t_s, int row, bool first, bool diag,
+// offset included).  With `masked`, key columns past `lim` are excluded: lim
+// is the query row within the tile on a causal diagonal tile, or the last
+// valid key column of a ragged final tile when attention is not causal.
+// Updates (m_run, l_run); returns the factor the row's O accumulator must be
+// multiplied by before the next P.V (1 = unchanged; the first tile returns 0:
+// O has no content yet).  Warp-uniform control flow: `first` and `masked` are
+// the same for the whole warp.
+__device__ __forceinline__ float softmax_tile(uint32_t t_s, int lim, bool first, bool masked,
                                               float sl2, float& m_run, float& l_run) {
   uint32_t s[128];
   const uint64_t sl2x2 = f2(sl2, sl2);
@@ -112,9 +116,9 @@ __device__ __forceinline__ float softmax_tile(uint32_t t_s, int row, bool first,
     for (int c = 0; c < 4; ++c)
       tmem_ld32(t_s + c * 32, *reinterpret_cast<uint32_t(*)[32]>(&s[c * 32]));
     tmem_ld_wait();
-    const float mx = diag ? row_max<true>(s, row) : row_max<false>(s, row);
+    const float mx = masked ? row_max<true>(s, lim) : row_max<false>(s, lim);
     m_run = mx * sl2;
-    l_run = diag ? exp_row<true>(s, row, sl2x2, m_run, t_s) : exp_row<false>(s, row, sl2x2, m_run, t_s);
+    l_run = masked ? exp_row<true>(s, lim, sl2x2, m_run, t_s) : exp_row<false>(s, lim, sl2x2, m_run, t_s);
     return 0.f;
   }
   // two-phase load: chunks 0-1, then 2-3 in flight while 0-1 are processed
@@ -125,18 +129,18 @@ __device__ __forceinline__ float softmax_tile(uint32_t t_s, int row, bool first,
   tmem_ld32(t_s + 96, *reinterpret_cast<uint32_t(*)[32]>(&s[96]));
   const uint64_t negm2 = f2(-m_run, -m_run);
   uint64_t a0, a1, a2, a3;
-  if (diag) {
-    a0 = exp_chunk<true>(s, 0, row, sl2x2, negm2, t_s);
-    a1 = exp_chunk<true>(s + 32, 32, row, sl2x2, negm2, t_s + 16);
+  if (masked) {
+    a0 = exp_chunk<true>(s, 0, lim, sl2x2, negm2, t_s);
+    a1 = exp_chunk<true>(s + 32, 32, lim, sl2x2, negm2, t_s + 16);
     tmem_ld_wait();
-    a2 = exp_chunk<true>(s + 64, 64, row, sl2x2, negm2, t_s + 32);
-    a3 = exp_chunk<true>(s + 96, 96, row, sl2x2, negm2, t_s + 48);
+    a2 = exp_chunk<true>(s + 64, 64, lim, sl2x2, negm2, t_s + 32);
+    a3 = exp_chunk<true>(s + 96, 96, lim, sl2x2, negm2, t_s + 48);
   } else {
-    a0 = exp_chunk<false>(s, 0, row, sl2x2, negm2, t_s);
-    a1 = exp_chunk<false>(s + 32, 32, row, sl2x2, negm2, t_s + 16);
+    a0 = exp_chunk<false>(s, 0, lim, sl2x2, negm2, t_s);
+    a1 = exp_chunk<false>(s + 32, 32, lim, sl2x2, negm2, t_s + 16);
     tmem_ld_wait();
-    a2 = exp_chunk<false>(s + 64, 64, row, sl2x2, negm2, t_s + 32);
-    a3 = exp_chunk<false>(s + 96, 96, row, sl2x2, negm2, t_s + 48);
+    a2 = exp_chunk<false>(s + 64, 64, lim, sl2x2, negm2, t_s + 32);
+    a3 = exp_chunk<false>(s + 96, 96, lim, sl2x2, negm2, t_s + 48);
   }
   const uint64_t t = add_f32x2(add_f32x2(a0, a1), add_f32x2(a2, a3));
   float lsum = f2_lo(t) + f2_hi(t);
@@ -145,10 +149,10 @@ __device__ __forceinline__ float softmax_tile(uint32_t t_s, int row, bool first,
     // rare: recompute the tile against a raised max (whole warp, since the
     // TMEM stores are warp-collective; rows that did not trip keep theirs)
     float m_new = m_run;
-    if (over) m_new = fmaxf(m_run, (diag ? row_max<true>(s, row) : row_max<false>(s, row)) * sl2);
+    if (over) m_new = fmaxf(m_run, (masked ? row_max<true>(s, lim) : row_max<false>(s, lim)) * sl2);
     const float alpha = fast_exp2(m_run - m_new);
     m_run = m_new;
-    lsum = diag ? exp_row<true>(s, row, sl2x2, m_run, t_s) : exp_row<false>(s, row, sl2x2, m_run, t_s);
+    lsum = masked ? exp_row<true>(s, lim, sl2x2, m_run, t_s) : exp_row<false>(s, lim, sl2x2, m_run, t_s);
     l_run = l_run * alpha + lsum;
     return alpha;
   }

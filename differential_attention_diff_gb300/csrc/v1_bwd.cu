@@ -21,7 +21,8 @@
 //  2. main (tcgen05): a work item is (batch, head, 128-key tile); a cluster
 //     of two CTAs runs it, rank 0 for stream 1 and rank 1 for stream 2.  Each
 //     CTA keeps its K tile and the V tile in shared memory and walks the
-//     64-row query tiles at and after the diagonal:
+//     64-row query tiles at and after the diagonal (all of them when not
+//     causal):
 //        S^T  = K Q^T          (TMEM, 64 columns)
 //        dP^T = V dO^T         (TMEM, 64 columns)
 //        softmax warps (thread = key row): P = exp2(S^T s log2e - lse2),
@@ -403,7 +404,7 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
     const int u = ci % units;
     it.b = u / a.H;
     it.h = u % a.H;
-    it.i0 = it.kt * (kKT / kQT);
+    it.i0 = a.causal ? it.kt * (kKT / kQT) : 0;  // causal: query tiles from the diagonal on
     it.n_it = n_qt - it.i0;
   }
   const CUtensorMap* tq = rank == 0 ? &tm_q1 : &tm_q2;
@@ -655,7 +656,10 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
       tc_fence_after();
       const float4* l2v = reinterpret_cast<const float4*>(sh.gen + kOffLse + (k & 1) * 512);
       const float4* ddv = l2v + 16;
-      const bool diag = q0 < it.kt * kKT + kKT;  // a query of this tile may precede a key
+      // causal: a query of this tile may precede a key.  (Not causal: keys
+      // past N are zero rows of K and V, which give dQ no contribution, and
+      // their dK / dV rows are never stored.)
+      const bool diag = a.causal && q0 < it.kt * kKT + kKT;
       uint32_t dkeep[16];  // dS^T of the first half, stored once the second half's S^T is read
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {

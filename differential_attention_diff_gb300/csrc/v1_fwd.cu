@@ -146,7 +146,7 @@ struct Item {
 };
 // Items are taken in blocks of `ub` (batch, head) units whose K1, K2 and V
 // fit in L2 together; inside a block, heaviest causal rows first.
-__device__ __forceinline__ Item item_of(int i, int units, int H, int n_mtiles, int ub) {
+__device__ __forceinline__ Item item_of(int i, int units, int H, int n_mtiles, int ub, bool causal) {
   const int per_blk = n_mtiles * ub;
   const int blk = i / per_blk, r = i - blk * per_blk;
   const int bsize = min(ub, units - blk * ub);
@@ -155,7 +155,7 @@ __device__ __forceinline__ Item item_of(int i, int units, int H, int n_mtiles, i
   const int u = blk * ub + r % bsize;
   it.b = u / H;
   it.h = u % H;
-  it.n_kv = it.mt + 1;
+  it.n_kv = causal ? it.mt + 1 : n_mtiles;  // causal: key tiles 0 .. mt; else all
   return it;
 }
 
@@ -185,6 +185,7 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
   const int n_mtiles = (a.N + kBM - 1) / kBM;
   const int units = a.B * a.H;
   const int n_items = n_mtiles * units;
+  const bool causal = a.causal != 0;
   // units per L2 block: K1 + K2 + V of one (batch, head) is N (2 DQK + DV) * 2 bytes
   const int ub = max(1, min(units, static_cast<int>((48ll << 20) /
                                                     (static_cast<long long>(a.N) * (2 * DQK + DV) * 2))));
@@ -300,7 +301,7 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
         const int i = rank == 0 ? publish(it) : consume(it, true);
         if (i < 0) { ok = false; break; }
         if (i >= n_items) break;
-        const Item w = item_of(i, units, a.H, n_mtiles, ub);
+        const Item w = item_of(i, units, a.H, n_mtiles, ub, causal);
         if (it > 0 && !wait_bar(sh, sh.bar(B_QEMPTY), (it - 1) & 1, a.status, 0x3001)) { ok = false; break; }
         mbar_arrive_expect_tx(sh.bar(B_QFULL), kNQ * kBox);
         for (int box = 0; box < kNQ; ++box)
@@ -375,7 +376,7 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
         const int i = consume(it, true);
         if (i < 0) { ok = false; break; }
         if (i >= n_items) break;
-        const Item w = item_of(i, units, a.H, n_mtiles, ub);
+        const Item w = item_of(i, units, a.H, n_mtiles, ub, causal);
         const int n = w.n_kv;
         if (!wait_bar(sh, sh.bar(B_QFULL), it & 1, a.status, 0x3101)) { ok = false; break; }
         tc_fence_after();
@@ -437,14 +438,18 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
       if (lane == 0 && i >= 0) release(it);  // the whole warp has read the slot
       if (i < 0) { ok = false; break; }
       if (i >= n_items) break;
-      const Item w = item_of(i, units, a.H, n_mtiles, ub);
+      const Item w = item_of(i, units, a.H, n_mtiles, ub, causal);
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < w.n_kv; ++j) {
         const int g = kv + j;
         const uint32_t t_s = tmem + lane_off + (g & 1) * 128;
         if (!wait_bar(sh, sh.bar(B_SFULL + (g & 1)), (g >> 1) & 1, a.status, 0x3201)) { ok = false; break; }
         tc_fence_after();
-        const float alpha = softmax_tile(t_s, row, j == 0, j == w.mt, sl2, m_run, l_run);
+        // masked columns: keys after the query (causal diagonal tile), or
+        // keys >= N (ragged last tile without the causal mask)
+        const bool masked = causal ? j == w.mt : (j == w.n_kv - 1 && (a.N % kBN) != 0);
+        const int lim = causal ? row : a.N - 1 - j * kBN;
+        const float alpha = softmax_tile(t_s, lim, j == 0, masked, sl2, m_run, l_run);
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
           // PV(g - 1) may still run: wait for it before rescaling O
           if (!wait_bar(sh, sh.bar(B_ODONE), (g - 1) & 1, a.status, 0x3202)) { ok = false; break; }

@@ -18,7 +18,8 @@
 //     dz, and zeroed fp32 dQ accumulators;
 //  3. main (tcgen05): a work item is (batch, K/V group, 128-key tile); one
 //     CTA keeps the K and V tiles in shared memory and walks every query head
-//     of the group and its 64-row query tiles at and after the diagonal,
+//     of the group and its 64-row query tiles at and after the diagonal (all
+//     of them when not causal),
 //     accumulating dK and dV of the group in TMEM across the heads:
 //        S^T  = K Q^T,  dP^T = V dO^T  (TMEM, double-buffered, issued while
 //                                       the softmax warps work on the tile
@@ -283,7 +284,7 @@ struct Item {
 // units are taken one block at a time (their dQ accumulators stay in L2),
 // the heaviest key tiles (most query tiles) first within each block.
 __device__ __forceinline__ Item item_of(int i, int n_kt, int n_qt, int units, int h_kv, int per,
-                                        int G) {
+                                        int G, bool causal) {
   const int blk = i / (per * n_kt);
   const int base = blk * per;
   const int pb = min(per, units - base);
@@ -293,7 +294,7 @@ __device__ __forceinline__ Item item_of(int i, int n_kt, int n_qt, int units, in
   const int u = base + wi % pb;
   it.b = u / h_kv;
   it.g = u % h_kv;
-  it.i0 = it.kt * (kKT / kQT);
+  it.i0 = causal ? it.kt * (kKT / kQT) : 0;  // causal: query tiles from the diagonal on
   it.n_ith = n_qt - it.i0;
   it.n_it = it.n_ith * G;
   return it;
@@ -319,7 +320,8 @@ v2_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   const int G = (2 * a.h) / a.h_kv;
   const int n_kt = (a.N + kKT - 1) / kKT;
   const int n_qt = w.npad / kQT;
-  const Item it = item_of(blockIdx.x, n_kt, n_qt, a.B * a.h_kv, a.h_kv, per, G);
+  const bool causal = a.causal != 0;
+  const Item it = item_of(blockIdx.x, n_kt, n_qt, a.B * a.h_kv, a.h_kv, per, G, causal);
 
   if (threadIdx.x == 0) {
     mbar_init(sh.bar(B_KV), 1);
@@ -514,7 +516,10 @@ v2_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
       tc_fence_after();
       const float4* l2v = reinterpret_cast<const float4*>(sh.gen + kOffLse + (k % kStages) * 512);
       const float4* ddv = l2v + 16;
-      const bool diag = q0 < it.kt * kKT + kKT;  // a query of this tile may precede a key
+      // causal: a query of this tile may precede a key.  (Not causal: keys
+      // past N are zero rows of K and V, which give dQ no contribution, and
+      // their dK / dV rows are never stored.)
+      const bool diag = causal && q0 < it.kt * kKT + kKT;
       uint8_t* dsbuf = sh.gen + kOffDS + b * kBoxK;
       uint32_t dkeep[16];  // dS^T of the first half, stored to TMEM once the second half's S^T is read
 #pragma unroll

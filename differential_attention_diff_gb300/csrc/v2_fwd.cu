@@ -102,13 +102,13 @@ struct Item {
   int b, p, mt, n_kv;
 };
 
-__device__ __forceinline__ Item item_of(int i, int units, int h, int n_mtiles) {
+__device__ __forceinline__ Item item_of(int i, int units, int h, int n_mtiles, bool causal) {
   Item it;
   it.mt = n_mtiles - 1 - i / units;
   const int u = i % units;
   it.b = u / h;
   it.p = u % h;
-  it.n_kv = it.mt + 1;  // causal: tiles 0 .. mt
+  it.n_kv = causal ? it.mt + 1 : n_mtiles;  // causal: key tiles 0 .. mt; else all
   return it;
 }
 
@@ -142,6 +142,7 @@ v2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
   const int n_mtiles = (a.N + kBM - 1) / kBM;
   const int units = a.B * a.h;
   const int n_items = n_mtiles * units;
+  const bool causal = a.causal != 0;
 
   if (threadIdx.x == 0) {
     mbar_init(sh.bar(B_QFULL), 1);
@@ -179,7 +180,7 @@ v2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       int last_kv = -1;  // last K/V tile issued (for the drain on error)
       bool ok = true;
       for (int i = sched(0); i < n_items && ok; ++it, i = sched(it)) {
-        const Item w = item_of(i, units, a.h, n_mtiles);
+        const Item w = item_of(i, units, a.h, n_mtiles, causal);
         const int g = (2 * w.p) / G;
         if (it > 0 && !wait_bar(sh, sh.bar(B_QEMPTY), (it - 1) & 1, a.status, 0x2001)) {
           ok = false;
@@ -249,7 +250,7 @@ v2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         }
       };
       for (int i = sched(0); i < n_items && ok; ++it, i = sched(it)) {
-        const Item w = item_of(i, units, a.h, n_mtiles);
+        const Item w = item_of(i, units, a.h, n_mtiles, causal);
         if (!wait_bar(sh, sh.bar(B_QFULL), it & 1, a.status, 0x2101)) { ok = false; break; }
         tc_fence_after();
         {
@@ -311,12 +312,16 @@ v2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       return r;
     };
     for (int i = sched(0); i < n_items && ok; ++it, i = sched(it)) {
-      const Item w = item_of(i, units, a.h, n_mtiles);
+      const Item w = item_of(i, units, a.h, n_mtiles, causal);
       float m_run = -INFINITY, l_run = 0.f;
       for (int j = 0; j < w.n_kv; ++j, ++sc) {
         if (!wait_bar(sh, sh.bar(B_SFULL + wg), sc & 1, a.status, 0x2201 + wg)) { ok = false; break; }
         tc_fence_after();
-        const float alpha = softmax_tile(t_s, row, j == 0, j == w.mt, sl2, m_run, l_run);
+        // masked columns: keys after the query (causal diagonal tile), or
+        // keys >= N (ragged last tile without the causal mask)
+        const bool masked = causal ? j == w.mt : (j == w.n_kv - 1 && (a.N % kBN) != 0);
+        const int lim = causal ? row : a.N - 1 - j * kBN;
+        const float alpha = softmax_tile(t_s, lim, j == 0, masked, sl2, m_run, l_run);
         if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
           // O is stable here: the commit that signalled S(j) covers PV(j-1).
 #pragma unroll 1

@@ -18,10 +18,11 @@ def bf16(x):
     return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
 
 
-def rounded_backward(f, fwd, li, heads=None):
+def rounded_backward(f, fwd, li, heads=None, causal=True):
     """f: fp64 inputs (q1..v, dy) as [B, N, H, D]; fwd: the oracle forward on
     them.  Returns the gradients dq1, dq2, dk1, dk2, dv (and dlam) computed
-    with the bf16 storage points; `heads` restricts to a list of heads."""
+    with the bf16 storage points; `heads` restricts to a list of heads;
+    causal=False drops the key <= query mask."""
     lam, c = fwd["lam"], 1.0 - li
     B, N, H, dqk = f["q1"].shape
     heads = range(H) if heads is None else heads
@@ -42,7 +43,9 @@ def rounded_backward(f, fwd, li, heads=None):
             dP = dO @ f["v"][b, :, h].T
             for t, (sig, D, lse) in enumerate(((1.0, D1, fwd["lse1"]), (-lam, D2, fwd["lse2"])), 1):
                 Q, K = f[f"q{t}"][b, :, h], f[f"k{t}"][b, :, h]
-                P = np.tril(np.exp(s * Q @ K.T - lse[b, h][:, None]))
+                P = np.exp(s * Q @ K.T - lse[b, h][:, None])
+                if causal:
+                    P = np.tril(P)
                 dS = bf16(sig * s * P * (dP - D[:, None]))
                 out[f"dq{t}"][b, :, h] = dS @ K
                 out[f"dk{t}"][b, :, h] = dS.T @ Q
@@ -51,7 +54,7 @@ def rounded_backward(f, fwd, li, heads=None):
     return out
 
 
-def rounded_backward_v2(f, fwd, gate, scale=None, rnd=bf16):
+def rounded_backward_v2(f, fwd, gate, scale=None, rnd=bf16, causal=True):
     """f: fp64 V2 inputs (q, k, v, x, w_lambda, dout); fwd: the oracle's V2
     forward on them; gate: fp64 [B, N, h].  Returns dq, dk, dv, dz, dx, dw
     with the V2 backward's bf16 storage points (``rnd`` = the rounding; the
@@ -68,7 +71,9 @@ def rounded_backward_v2(f, fwd, gate, scale=None, rnd=bf16):
             c = j // group
             dO = dout[b, :, j // 2] if j % 2 == 0 else dodd[b, :, j // 2]
             D = (dO * o[b, :, j]).sum(1)
-            P = np.tril(np.exp(s * q[b, :, j] @ k[b, :, c].T - fwd["lse"][b, j][:, None]))
+            P = np.exp(s * q[b, :, j] @ k[b, :, c].T - fwd["lse"][b, j][:, None])
+            if causal:
+                P = np.tril(P)
             dS = rnd(s * P * (dO @ v[b, :, c].T - D[:, None]))
             out["dq"][b, :, j] = dS @ k[b, :, c]
             out["dk"][b, :, c] += dS.T @ q[b, :, j]

@@ -78,6 +78,26 @@ def test_v1_fwd_argument_checks(lib):
     assert f(C.byref(_v1p(N=0)), None) == bd.DA_OK
 
 
+def test_v1_bwd_causal_and_deterministic_checks(lib):
+    """Not causal is supported; deterministic dQ slots exist only for the
+    causal (key tile, query tile) pairs, so that pair is refused up front."""
+    p = bd.da_v1_bwd_params()
+    p.B, p.N, p.H, p.d_qk, p.d_v, p.dtype = 1, 256, 2, 128, 256, bd.DA_BF16
+    p.lambda_init, p.rms_eps = 0.2, 1e-5
+    fake = 1 << 20
+    for n in ("q1", "q2", "k1", "k2", "dq1", "dq2", "dk1", "dk2"):
+        setattr(p, n, bd.da_t4(fake, 1 << 16, 1 << 8, 128))
+    for n in ("v", "out", "dout", "o2", "dv"):
+        setattr(p, n, bd.da_t4(fake, 1 << 17, 1 << 9, 256))
+    for n in ("lq1", "lk1", "lq2", "lk2", "dlq1", "dlk1", "dlq2", "dlk2", "lse1", "lse2", "rstd"):
+        setattr(p, n, fake)
+    f = lib.diffattn_v1_bwd
+    for causal, det, want in ((1, 0, bd.DA_ERR_WORKSPACE), (0, 0, bd.DA_ERR_WORKSPACE),
+                              (1, 1, bd.DA_ERR_WORKSPACE), (0, 1, bd.DA_ERR_UNSUPPORTED)):
+        p.causal, p.deterministic = causal, det
+        assert f(C.byref(p), None) == want, (causal, det)
+
+
 def test_decode_argument_checks(lib):
     p = bd.da_v2_decode_params()
     p.B, p.h, p.h_kv, p.d, p.L_max = 2, 32, 8, 128, 1024

@@ -26,7 +26,7 @@ def _status_clean():
     assert bd.diffattn_get_device_status() == bd.DA_OK
 
 
-def _check(t, ratio, out, rows=None, batches=None, groups=None):
+def _check(t, ratio, out, rows=None, batches=None, groups=None, causal=True):
     B, N, Hq, d = t["q"].shape
     hkv = t["k"].shape[2]
     G = Hq // hkv
@@ -41,7 +41,8 @@ def _check(t, ratio, out, rows=None, batches=None, groups=None):
             qs = slice(g * (ratio + 1), (g + 1) * (ratio + 1))
             ps = slice(g * ratio, (g + 1) * ratio)
             ref = orc.grouped_forward(f64(t["q"][b:b + 1, :, qs]), f64(t["k"][b:b + 1, :, c:c + 1]),
-                                      f64(t["v"][b:b + 1, :, c:c + 1]), gate[b:b + 1, :, ps], ratio, rows=rows)
+                                      f64(t["v"][b:b + 1, :, c:c + 1]), gate[b:b + 1, :, ps], ratio, rows=rows,
+                                      causal=causal)
             tol = TOL * float(np.sqrt(np.mean(f64(t["v"][b, :, c]) ** 2)))
             worst = max(worst, float(np.max(np.abs(o[b, ref["rows"], ps] - ref["out"][0]))) / tol)
     assert worst <= 1.0, worst
@@ -62,6 +63,14 @@ def test_grouped_parity_head_dim_64(B, N, h, ratio, hkv):
     out = bd.diffattn_grouped_fwd(t["q"], t["k"], t["v"], ratio, x=t["x"], w_lambda=t["w_lambda"])
     torch.cuda.synchronize()
     _check(t, ratio, out)
+
+
+@pytest.mark.parametrize("B,N,h,ratio,hkv,d", [(1, 200, 6, 3, 2, 128), (2, 129, 8, 4, 1, 64)])
+def test_grouped_parity_not_causal(B, N, h, ratio, hkv, d):
+    t = synth.grouped_inputs(B, N, h, ratio, hkv, d, 128, seed=8200 + N + h, device="cuda")
+    out = bd.diffattn_grouped_fwd(t["q"], t["k"], t["v"], ratio, x=t["x"], w_lambda=t["w_lambda"], causal=False)
+    torch.cuda.synchronize()
+    _check(t, ratio, out, causal=False)
 
 
 def test_grouped_ratio_one_matches_v2():

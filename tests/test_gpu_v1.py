@@ -34,7 +34,7 @@ def _status_clean():
     assert bd.diffattn_get_device_status() == bd.DA_OK
 
 
-def _check(t, li, y, sv, rows=None, heads=None, batches=None):
+def _check(t, li, y, sv, rows=None, heads=None, batches=None, causal=True):
     B, N, H, _ = t["q1"].shape
     heads = range(H) if heads is None else heads
     batches = range(B) if batches is None else batches
@@ -44,7 +44,8 @@ def _check(t, li, y, sv, rows=None, heads=None, batches=None):
         for h in heads:
             sl = lambda n: f64(t[n][b:b + 1, :, h:h + 1])  # noqa: E731
             ref = orc.v1_forward(sl("q1"), sl("q2"), sl("k1"), sl("k2"), sl("v"),
-                                 *(f64(t[n]) for n in NAMES[5:]), float(np.float32(li)), rows=rows)
+                                 *(f64(t[n]) for n in NAMES[5:]), float(np.float32(li)), rows=rows,
+                                 causal=causal)
             r = ref["rows"]
             tol = TOL * rms(f64(t["v"][b, :, h]))
             worst = max(worst, float(np.max(np.abs(yv[b, r, h] - ref["y"][0, :, 0]))) / tol)
@@ -89,6 +90,18 @@ def test_v1_fwd_exact_cancellation_head_dims_64_128():
     y = bd.diffattn_v1_fwd(t["q1"], t["q1"], t["k1"], t["k1"], t["v"], lq1, lk1, z, z, 0.0)
     torch.cuda.synchronize()
     assert torch.count_nonzero(y).item() == 0
+
+
+@pytest.mark.parametrize("B,N,H,dqk,layer", [(1, 200, 2, 128, 1), (2, 129, 3, 64, 14), (1, 1, 1, 128, 28),
+                                              (1, 640, 2, 128, 5)])
+def test_v1_fwd_parity_not_causal(B, N, H, dqk, layer):
+    """Every query attends every key: all key tiles per item, the ragged last
+    key tile masked at N; saves checked."""
+    t = synth.v1_inputs(B, N, H, dqk, 2 * dqk, "bf16", seed=4200 + N + H, device="cuda")
+    li = bd.diffattn_lambda_init(layer)
+    y, sv = bd.diffattn_v1_fwd(*(t[n] for n in NAMES), li, save=True, causal=False)
+    torch.cuda.synchronize()
+    _check(t, li, y, sv, causal=False)
 
 
 def test_v1_fwd_without_saves_matches():

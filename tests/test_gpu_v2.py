@@ -30,7 +30,7 @@ def _status_clean():
     assert bd.diffattn_get_device_status() == bd.DA_OK
 
 
-def _check_pairs(t, out, gate, pairs=None, rows=None, lse=None):
+def _check_pairs(t, out, gate, pairs=None, rows=None, lse=None, causal=True):
     B, N, H2, d = t["q"].shape
     hkv = t["k"].shape[2]
     G = H2 // hkv
@@ -41,7 +41,8 @@ def _check_pairs(t, out, gate, pairs=None, rows=None, lse=None):
         for p in pairs:
             g = (2 * p) // G
             ref = orc.v2_forward(f64(t["q"][b:b + 1, :, 2 * p:2 * p + 2]), f64(t["k"][b:b + 1, :, g:g + 1]),
-                                 f64(t["v"][b:b + 1, :, g:g + 1]), gate[b:b + 1, :, p:p + 1], rows=rows)
+                                 f64(t["v"][b:b + 1, :, g:g + 1]), gate[b:b + 1, :, p:p + 1], rows=rows,
+                                 causal=causal)
             got = o[b, ref["rows"], p]
             tol = TOL * rms(f64(t["v"][b, :, g]))
             worst = max(worst, float(np.max(np.abs(got - ref["out"][0, :, 0]))) / tol)
@@ -91,6 +92,19 @@ def test_v2_fwd_exact_cancellation_head_dim_64():
     out = bd.diffattn_v2_fwd(q, t["k"], t["v"], gate=gate)
     torch.cuda.synchronize()
     assert torch.count_nonzero(out).item() == 0
+
+
+@pytest.mark.parametrize("B,N,h,hkv,d", [(1, 200, 4, 2, 128), (2, 129, 2, 1, 64), (1, 1, 2, 1, 128),
+                                          (1, 384, 4, 4, 128), (1, 700, 8, 2, 64)])
+def test_v2_fwd_parity_not_causal(B, N, h, hkv, d):
+    """Every query attends every key: all key tiles per item, the ragged last
+    key tile masked at N."""
+    t = synth.v2_inputs(B, N, h, hkv, d, 128, seed=3200 + N + h, device="cuda")
+    out, sv = bd.diffattn_v2_fwd(t["q"], t["k"], t["v"], x=t["x"], w_lambda=t["w_lambda"], save=True,
+                                 causal=False)
+    torch.cuda.synchronize()
+    gate = orc.v2_gate(f64(t["x"]), f64(t["w_lambda"]))
+    _check_pairs(t, out, gate, lse=sv["lse"], causal=False)
 
 
 def test_v2_fwd_gate_given_equals_x_path():

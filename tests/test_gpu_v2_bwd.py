@@ -41,31 +41,32 @@ def _status_clean():
     assert bd.diffattn_get_device_status() == bd.DA_OK
 
 
-def _run(t):
+def _run(t, causal=True):
     """The training step: GPU forward with saves, then the GPU backward."""
-    _, sv = bd.diffattn_v2_fwd(t["q"], t["k"], t["v"], x=t["x"], w_lambda=t["w_lambda"], save=True)
+    _, sv = bd.diffattn_v2_fwd(t["q"], t["k"], t["v"], x=t["x"], w_lambda=t["w_lambda"], save=True,
+                               causal=causal)
     g = bd.diffattn_v2_bwd(t["q"], t["k"], t["v"], t["dout"], sv, x=t["x"], w_lambda=t["w_lambda"],
-                           want_dz=True)
+                           want_dz=True, causal=causal)
     torch.cuda.synchronize()
     return g
 
 
-def _run_exact_saves(t, fwd):
+def _run_exact_saves(t, fwd, causal=True):
     """The GPU backward alone, given the oracle's forward saves."""
     dev = t["q"].device
     sv = dict(o_heads=torch.from_numpy(fwd["o"]).to(dev, torch.bfloat16),
               lse=torch.from_numpy(fwd["lse"]).to(dev, torch.float32))
     g = bd.diffattn_v2_bwd(t["q"], t["k"], t["v"], t["dout"], sv, x=t["x"], w_lambda=t["w_lambda"],
-                           want_dz=True)
+                           want_dz=True, causal=causal)
     torch.cuda.synchronize()
     return g
 
 
-def _reference(t):
+def _reference(t, causal=True):
     f = {n: f64(v) for n, v in t.items()}
-    ref = orc.v2_backward(f["q"], f["k"], f["v"], f["x"], f["w_lambda"], f["dout"])
+    ref = orc.v2_backward(f["q"], f["k"], f["v"], f["x"], f["w_lambda"], f["dout"], causal=causal)
     fwd = dict(o=ref["o"], lse=ref["lse"])  # the forward the oracle's chain rule ran on
-    model = rounded_backward_v2(f, fwd, ref["gate"])
+    model = rounded_backward_v2(f, fwd, ref["gate"], causal=causal)
     return ref, fwd, model
 
 
@@ -109,6 +110,17 @@ def test_v2_bwd_parity_head_dim_64(B, N, h, hkv):
     ref, fwd, model = _reference(t)
     _compare(_run_exact_saves(t, fwd), ref, model, bar="bwd")
     _compare(_run(t), ref, model, bar="step")
+
+
+@pytest.mark.parametrize("B,N,h,hkv,d", [(1, 200, 2, 1, 128), (2, 129, 2, 2, 64), (1, 1, 1, 1, 128),
+                                          (1, 300, 4, 1, 128)])
+def test_v2_bwd_parity_not_causal(B, N, h, hkv, d):
+    """Every key attends every query: each key tile walks all query tiles of
+    every head, no diagonal mask; ragged key tails."""
+    t = synth.v2_inputs(B, N, h, hkv, d, 128, seed=7300 + N + h, device="cuda", with_dout=True)
+    ref, fwd, model = _reference(t, causal=False)
+    _compare(_run_exact_saves(t, fwd, causal=False), ref, model, bar="bwd")
+    _compare(_run(t, causal=False), ref, model, bar="step")
 
 
 def test_v2_bwd_gate_given_matches_gate_from_x():

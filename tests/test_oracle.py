@@ -114,6 +114,18 @@ def test_v1_lambda_zero_is_library_attention():
             np.testing.assert_allclose(out["o2"][b, :, h], ref2, atol=1e-12)
 
 
+def test_v1_lambda_zero_not_causal_is_library_attention():
+    """As above without the causal mask: every query sees every key."""
+    t = _v1_rand(seed=5)
+    for n in ("lq1", "lk1", "lq2", "lk2"):
+        t[n] = np.zeros_like(t[n])
+    out = _v1(t, 0.0, causal=False)
+    for b in range(2):
+        for h in range(3):
+            ref = _sdpa(t["q1"][b, :, h], t["k1"][b, :, h], t["v"][b, :, h], causal=False)
+            np.testing.assert_allclose(out["o"][b, :, h], ref, atol=1e-12)
+
+
 def test_v1_identical_streams_scale_by_one_minus_lambda():
     """Q2 = Q1, K2 = K1: both maps are equal, so O = (1 - lambda) * attention."""
     t = _v1_rand(seed=3)
@@ -438,18 +450,20 @@ def test_grouped_gate_zero_and_shared_noise():
 
 # -------------------------------------------------------------- backward ----
 
-def test_v1_backward_finite_differences():
+@pytest.mark.parametrize("causal", [True, False])
+def test_v1_backward_finite_differences(causal):
     """Every gradient (Q1, Q2, K1, K2, V and the four lambda vectors) against
-    central differences of the forward (fp64, step 1e-6)."""
+    central differences of the forward (fp64, step 1e-6), with and without
+    the causal mask."""
     t = _v1_rand(B=1, N=5, H=2, dqk=3, dv=6, seed=30, lam_std=0.4)
     li = 0.35
     r = _rng(31)
     dy = r.standard_normal((1, 5, 2, 6))
     grads = orc.v1_backward(t["q1"], t["q2"], t["k1"], t["k2"], t["v"], t["lq1"],
-                            t["lk1"], t["lq2"], t["lk2"], li, dy)
+                            t["lk1"], t["lq2"], t["lk2"], li, dy, causal=causal)
 
     def loss(tt):
-        return float(np.sum(_v1(tt, li)["y"] * dy))
+        return float(np.sum(_v1(tt, li, causal=causal)["y"] * dy))
 
     eps = 1e-6
     for name in ("q1", "q2", "k1", "k2", "v", "lq1", "lk1", "lq2", "lk2"):
@@ -467,20 +481,22 @@ def test_v1_backward_finite_differences():
         assert err < 1e-6, (name, err)
 
 
-def test_v2_backward_finite_differences():
+@pytest.mark.parametrize("causal", [True, False])
+def test_v2_backward_finite_differences(causal):
     """Every V2 gradient (q, k, v, x, w_lambda) against central differences of
-    gate + forward (fp64), on a GQA case with two pairs per K/V group."""
+    gate + forward (fp64), on a GQA case with two pairs per K/V group, with
+    and without the causal mask."""
     r = _rng(40)
     B, N, h, hkv, d, dm = 1, 5, 2, 1, 3, 4
     t = dict(q=r.standard_normal((B, N, 2 * h, d)), k=r.standard_normal((B, N, hkv, d)),
              v=r.standard_normal((B, N, hkv, d)), x=r.standard_normal((B, N, dm)),
              w=0.5 * r.standard_normal((dm, h)))
     dout = r.standard_normal((B, N, h, d))
-    grads = orc.v2_backward(t["q"], t["k"], t["v"], t["x"], t["w"], dout)
+    grads = orc.v2_backward(t["q"], t["k"], t["v"], t["x"], t["w"], dout, causal=causal)
 
     def loss(tt):
         gate = orc.v2_gate(tt["x"], tt["w"])
-        return float(np.sum(orc.v2_forward(tt["q"], tt["k"], tt["v"], gate)["out"] * dout))
+        return float(np.sum(orc.v2_forward(tt["q"], tt["k"], tt["v"], gate, causal=causal)["out"] * dout))
 
     eps = 1e-6
     for name in ("q", "k", "v", "x", "w"):
