@@ -29,8 +29,9 @@ Sources (two web pages on the method; titles and sections as printed):
 
 Readings where the pages are silent (each also listed in the design notes):
 the exact lambda form exp(lq1.lk1) - exp(lq2.lk2) + lambda_init, the
-(1 - lambda_init) post-norm scale, RMSNorm eps 1e-5 inside the root with unit
-weight over the V head dim, 1/sqrt(d) with d the Q/K head dim, causal j <= i,
+(1 - lambda_init) post-norm scale, RMSNorm eps 1e-5 inside the root over the
+V head dim with a fixed per-feature weight (unit unless given; it takes no
+gradient), 1/sqrt(d) with d the Q/K head dim, causal j <= i (or no mask),
 even head 2p minus gate times odd head 2p+1, contiguous GQA groups
 (q head j -> kv head j // (2h/h_kv)), no gate bias, no clamp on lambda.
 
@@ -113,15 +114,16 @@ def attention_maps(q, k, scale: float, causal: bool, rows=None):
 
 def v1_forward(q1, q2, k1, k2, v, lq1, lk1, lq2, lk2, lam_init: float, *,
                scale: float | None = None, causal: bool = True,
-               eps: float = 1e-5, rows=None):
+               eps: float = 1e-5, rows=None, rms_weight=None):
     """V1 differential attention forward, then per-head RMSNorm and scale.
 
     [P1] "Differential Attention: 빼기의 힘":
         O = (softmax(s Q1 K1^T) - lambda softmax(s Q2 K2^T)) V,  s = 1/sqrt(d_qk)
     [P2] §1: per-head RMS normalisation after the subtraction, then the scale
     given by the per-layer init, read as
-        Y = (1 - lambda_init) * O / sqrt(mean_k O_k^2 + eps)
-    over the V head dim (2 d_qk) of each (b, n, h); unit weight.
+        Y = (1 - lambda_init) * w * O / sqrt(mean_k O_k^2 + eps)
+    over the V head dim (2 d_qk) of each (b, n, h); w is the RMSNorm weight
+    ([d_v], shared by heads; None = unit, as the pages' configuration).
 
     q1, q2, k1, k2: [B, N, H, d_qk]; v: [B, N, H, d_v]; lq1..lk2: [d_qk].
     ``rows`` restricts the query rows computed (every key is still used).
@@ -143,6 +145,7 @@ def v1_forward(q1, q2, k1, k2, v, lq1, lk1, lq2, lk2, lam_init: float, *,
     lse2 = np.zeros((B, H, R))
     rstd = np.zeros((B, H, R))
     c = 1.0 - lam_init
+    w = np.ones(dv) if rms_weight is None else _f64(rms_weight)
     for b in range(B):
         for h in range(H):
             a1, l1 = attention_maps(q1[b, :, h], k1[b, :, h], scale, causal, rows)
@@ -150,7 +153,7 @@ def v1_forward(q1, q2, k1, k2, v, lq1, lk1, lq2, lk2, lam_init: float, *,
             o_bh = (a1 - lam * a2) @ v[b, :, h]
             o2_bh = a2 @ v[b, :, h]
             r = np.sqrt(np.mean(o_bh * o_bh, axis=1) + eps)
-            y[b, :, h] = c * o_bh / r[:, None]
+            y[b, :, h] = c * w * o_bh / r[:, None]
             o[b, :, h] = o_bh
             o2[b, :, h] = o2_bh
             lse1[b, h] = l1
@@ -162,13 +165,14 @@ def v1_forward(q1, q2, k1, k2, v, lq1, lk1, lq2, lk2, lam_init: float, *,
 
 def v1_backward(q1, q2, k1, k2, v, lq1, lk1, lq2, lk2, lam_init: float, dy, *,
                 scale: float | None = None, causal: bool = True,
-                eps: float = 1e-5):
+                eps: float = 1e-5, rms_weight=None):
     """Gradients of the V1 forward above (all rows), by the chain rule.
 
     The pages give no backward formulas; this is the derivative of
-    ``v1_forward`` written step by step.  With c = 1 - lambda_init,
-    r = sqrt(mean O^2 + eps), Ohat = O / r, G = dY:
-      dOhat = c G;  dO = (dOhat - Ohat * mean(dOhat * Ohat)) / r
+    ``v1_forward`` written step by step.  With c = 1 - lambda_init, w the
+    RMSNorm weight (a constant: no gradient), r = sqrt(mean O^2 + eps),
+    Ohat = O / r, G = dY:
+      dOhat = c w G;  dO = (dOhat - Ohat * mean(dOhat * Ohat)) / r
       dlambda = -sum <dO, A2 V>
       dP = dO V^T
       dS1 = A1 * (dP - <dO, A1 V>),  dS2 = -lambda A2 * (dP - <dO, A2 V>)
@@ -185,6 +189,7 @@ def v1_backward(q1, q2, k1, k2, v, lq1, lk1, lq2, lk2, lam_init: float, dy, *,
         scale = 1.0 / np.sqrt(dqk)
     lam = lambda_full(lq1, lk1, lq2, lk2, lam_init)
     c = 1.0 - lam_init
+    w = np.ones(v.shape[-1]) if rms_weight is None else _f64(rms_weight)
     grads = {name: np.zeros_like(t) for name, t in
              (("dq1", q1), ("dq2", q2), ("dk1", k1), ("dk2", k2), ("dv", v))}
     dlam = 0.0
@@ -198,7 +203,7 @@ def v1_backward(q1, q2, k1, k2, v, lq1, lk1, lq2, lk2, lam_init: float, dy, *,
             O1 = a1 @ V
             r = np.sqrt(np.mean(O * O, axis=1) + eps)
             Ohat = O / r[:, None]
-            dOhat = c * dy[b, :, h]
+            dOhat = c * w * dy[b, :, h]
             dO = (dOhat - Ohat * np.mean(dOhat * Ohat, axis=1, keepdims=True)) / r[:, None]
             dlam += -float(np.sum(dO * O2))
             dP = dO @ V.T
@@ -342,7 +347,8 @@ def v2_decode(q, k_cache, v_cache, seqlens, gate, *, scale: float | None = None)
 
 
 def v1_decode(q1, q2, k1_cache, k2_cache, v_cache, seqlens, lq1, lk1, lq2, lk2,
-              lam_init: float, *, scale: float | None = None, eps: float = 1e-5):
+              lam_init: float, *, scale: float | None = None, eps: float = 1e-5,
+              rms_weight=None):
     """V1 decode: one new token per sequence, the V1 operator of [P1]
     "Differential Attention: 빼기의 힘" (two maps over two K caches, one shared
     V cache) followed by the per-head RMSNorm and (1 - lambda_init) scale of
@@ -351,7 +357,8 @@ def v1_decode(q1, q2, k1_cache, k2_cache, v_cache, seqlens, lq1, lk1, lq2, lk2,
     decoding as the memory-bound case.
 
     q1, q2: [B, H, d_qk]; k1_cache, k2_cache: [B, L_max, H, d_qk];
-    v_cache: [B, L_max, H, d_v]; seqlens: [B] ints.
+    v_cache: [B, L_max, H, d_v]; seqlens: [B] ints; rms_weight: [d_v] or
+    None (unit), as in ``v1_forward``.
     Returns dict: y [B, H, d_v], o (pre-norm) [B, H, d_v], lse1, lse2 [B, H],
     lam.
     """
@@ -362,6 +369,7 @@ def v1_decode(q1, q2, k1_cache, k2_cache, v_cache, seqlens, lq1, lk1, lq2, lk2,
         scale = 1.0 / np.sqrt(dqk)
     lam = lambda_full(lq1, lk1, lq2, lk2, lam_init)
     c = 1.0 - lam_init
+    w = np.ones(dv) if rms_weight is None else _f64(rms_weight)
     y = np.zeros((B, H, dv))
     o = np.zeros((B, H, dv))
     lse1 = np.zeros((B, H))
@@ -373,7 +381,7 @@ def v1_decode(q1, q2, k1_cache, k2_cache, v_cache, seqlens, lq1, lk1, lq2, lk2,
             a2, l2 = attention_maps(q2[b, h][None, :], k2_cache[b, :L, h], scale, causal=False)
             o_bh = ((a1 - lam * a2) @ v_cache[b, :L, h])[0]
             r = np.sqrt(np.mean(o_bh * o_bh) + eps)
-            y[b, h] = c * o_bh / r
+            y[b, h] = c * w * o_bh / r
             o[b, h] = o_bh
             lse1[b, h] = l1[0]
             lse2[b, h] = l2[0]

@@ -180,6 +180,22 @@ def test_v1_per_head_rms_and_scale():
     np.testing.assert_allclose(out["rstd"], 1 / np.sqrt(ms_o.transpose(0, 2, 1) + 1e-5), rtol=1e-12)
 
 
+def test_v1_rms_weight_scales_features():
+    """The RMSNorm weight multiplies each feature of the normalised output:
+    Y_w = w * Y_unit exactly (its definition), the pre-norm O and the saves
+    unchanged; the decode applies it the same way."""
+    t = _v1_rand(seed=9)
+    w = _rng(10).uniform(0.5, 1.5, t["v"].shape[-1])
+    base, wtd = _v1(t, 0.3), _v1(t, 0.3, rms_weight=w)
+    np.testing.assert_allclose(wtd["y"], base["y"] * w, rtol=1e-15, atol=0)
+    for n in ("o", "o2", "rstd", "lse1", "lse2"):
+        assert np.array_equal(wtd[n], base[n]), n
+    B, N, H, dqk = t["q1"].shape
+    dec = orc.v1_decode(t["q1"][:, -1], t["q2"][:, -1], t["k1"], t["k2"], t["v"], [N] * B,
+                        t["lq1"], t["lk1"], t["lq2"], t["lk2"], 0.3, rms_weight=w)
+    np.testing.assert_allclose(dec["y"], wtd["y"][:, -1], rtol=1e-12, atol=1e-14)
+
+
 def test_v1_first_row_closed_form():
     """Causal row 0 sees only key 0: both maps are [1], O[0] = (1 - lambda) V[0]."""
     t = _v1_rand(seed=7, N=5)
@@ -459,11 +475,13 @@ def test_v1_backward_finite_differences(causal):
     li = 0.35
     r = _rng(31)
     dy = r.standard_normal((1, 5, 2, 6))
+    # a non-unit RMSNorm weight on the causal case (it enters as dOhat = c w G)
+    w = _rng(32).uniform(0.5, 1.5, 6) if causal else None
     grads = orc.v1_backward(t["q1"], t["q2"], t["k1"], t["k2"], t["v"], t["lq1"],
-                            t["lk1"], t["lq2"], t["lk2"], li, dy, causal=causal)
+                            t["lk1"], t["lq2"], t["lk2"], li, dy, causal=causal, rms_weight=w)
 
     def loss(tt):
-        return float(np.sum(_v1(tt, li, causal=causal)["y"] * dy))
+        return float(np.sum(_v1(tt, li, causal=causal, rms_weight=w)["y"] * dy))
 
     eps = 1e-6
     for name in ("q1", "q2", "k1", "k2", "v", "lq1", "lk1", "lq2", "lk2"):
