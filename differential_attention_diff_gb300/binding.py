@@ -74,7 +74,7 @@ class da_v1_fwd_params(C.Structure):
                 ("lq1", C.c_void_p), ("lk1", C.c_void_p), ("lq2", C.c_void_p), ("lk2", C.c_void_p),
                 ("out", da_t4), ("lse1", C.c_void_p), ("lse2", C.c_void_p), ("rstd", C.c_void_p),
                 ("o2", da_t4), ("lambda_out", C.c_void_p),
-                ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t)]
+                ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t), ("rms_weight", C.c_void_p)]
 
 
 class da_v1_bwd_params(C.Structure):
@@ -87,7 +87,8 @@ class da_v1_bwd_params(C.Structure):
                 ("lse1", C.c_void_p), ("lse2", C.c_void_p), ("rstd", C.c_void_p), ("o2", da_t4),
                 ("dq1", da_t4), ("dq2", da_t4), ("dk1", da_t4), ("dk2", da_t4), ("dv", da_t4),
                 ("dlq1", C.c_void_p), ("dlk1", C.c_void_p), ("dlq2", C.c_void_p), ("dlk2", C.c_void_p),
-                ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t), ("deterministic", C.c_int)]
+                ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t), ("deterministic", C.c_int),
+                ("rms_weight", C.c_void_p)]
 
 
 class da_v1_decode_params(C.Structure):
@@ -96,7 +97,7 @@ class da_v1_decode_params(C.Structure):
                 ("q1", C.c_void_p), ("q2", C.c_void_p), ("k1_cache", da_t4), ("k2_cache", da_t4),
                 ("v_cache", da_t4), ("seqlens", C.c_void_p), ("lq1", C.c_void_p), ("lk1", C.c_void_p),
                 ("lq2", C.c_void_p), ("lk2", C.c_void_p), ("out", C.c_void_p), ("num_splits", C.c_int),
-                ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t)]
+                ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t), ("rms_weight", C.c_void_p)]
 
 
 class da_v2_gate_params(C.Structure):
@@ -239,10 +240,11 @@ def diffattn_lambda_init(layer: int) -> float:
 
 
 def diffattn_v1_fwd(q1, q2, k1, k2, v, lq1, lk1, lq2, lk2, lambda_init, *, out=None,
-                    causal=True, softmax_scale=0.0, rms_eps=1e-5, save=False, saves=None,
-                    workspace=None, stream=None):
+                    causal=True, softmax_scale=0.0, rms_eps=1e-5, rms_weight=None, save=False,
+                    saves=None, workspace=None, stream=None):
     """V1 forward.  Returns ``out`` or, with save=True, ``(out, saves)`` where
-    saves = dict(lse1, lse2, rstd, o2, lam) are the tensors the backward reads."""
+    saves = dict(lse1, lse2, rstd, o2, lam) are the tensors the backward reads.
+    rms_weight: fp32 [d_v] RMSNorm weight (None = unit)."""
     lib = load()
     B, N, H, dqk = q1.shape
     dv = v.shape[-1]
@@ -266,16 +268,17 @@ def diffattn_v1_fwd(q1, q2, k1, k2, v, lq1, lk1, lq2, lk2, lambda_init, *, out=N
         _ptr(saves["lse1"]) if saves else None, _ptr(saves["lse2"]) if saves else None,
         _ptr(saves["rstd"]) if saves else None, _t4(saves["o2"] if saves else None),
         _ptr(saves["lam"]) if saves else None, _ptr(workspace),
-        0 if workspace is None else workspace.numel() * workspace.element_size())
+        0 if workspace is None else workspace.numel() * workspace.element_size(), _ptr(rms_weight))
     _check(lib.diffattn_v1_fwd(C.byref(p), _stream(stream)), "diffattn_v1_fwd")
     return (out, saves) if save else out
 
 
 def diffattn_v1_bwd(q1, q2, k1, k2, v, lq1, lk1, lq2, lk2, lambda_init, out, dout, saves, *,
-                    causal=True, softmax_scale=0.0, rms_eps=1e-5, grads=None, workspace=None,
-                    deterministic=False, stream=None):
+                    causal=True, softmax_scale=0.0, rms_eps=1e-5, rms_weight=None, grads=None,
+                    workspace=None, deterministic=False, stream=None):
     """V1 backward.  Returns dict(dq1, dq2, dk1, dk2, dv, dlq1, dlk1, dlq2, dlk2).
-    deterministic=True makes dQ (and so every output) bitwise reproducible."""
+    deterministic=True makes dQ (and so every output) bitwise reproducible.
+    rms_weight: the forward's RMSNorm weight (None = unit; entries nonzero)."""
     lib = load()
     B, N, H, dqk = q1.shape
     dv = v.shape[-1]
@@ -293,7 +296,7 @@ def diffattn_v1_bwd(q1, q2, k1, k2, v, lq1, lk1, lq2, lk2, lambda_init, out, dou
         _ptr(saves["rstd"]), _t4(saves["o2"]), _t4(grads["dq1"]), _t4(grads["dq2"]),
         _t4(grads["dk1"]), _t4(grads["dk2"]), _t4(grads["dv"]), _ptr(grads["dlq1"]),
         _ptr(grads["dlk1"]), _ptr(grads["dlq2"]), _ptr(grads["dlk2"]), workspace.data_ptr(),
-        workspace.numel() * workspace.element_size(), int(bool(deterministic)))
+        workspace.numel() * workspace.element_size(), int(bool(deterministic)), _ptr(rms_weight))
     _check(lib.diffattn_v1_bwd(C.byref(p), _stream(stream)), "diffattn_v1_bwd")
     return grads
 
@@ -308,8 +311,9 @@ def diffattn_v1_decode_workspace_size(B, H, d_v, L_max, num_splits=0) -> int:
 
 def diffattn_v1_decode(q1, q2, k1_cache, k2_cache, v_cache, lq1, lk1, lq2, lk2, lambda_init, *,
                        seqlens=None, out=None, num_splits=0, softmax_scale=0.0, rms_eps=1e-5,
-                       workspace=None, stream=None):
-    """V1 decode: out [B, H, d_v] for one new token per sequence."""
+                       rms_weight=None, workspace=None, stream=None):
+    """V1 decode: out [B, H, d_v] for one new token per sequence.
+    rms_weight: fp32 [d_v] RMSNorm weight (None = unit)."""
     lib = load()
     B, H, dqk = q1.shape
     L_max, dv = v_cache.shape[1], v_cache.shape[3]
@@ -322,7 +326,7 @@ def diffattn_v1_decode(q1, q2, k1_cache, k2_cache, v_cache, lq1, lk1, lq2, lk2, 
         B, H, dqk, dv, L_max, float(softmax_scale), float(lambda_init), float(rms_eps), q1.data_ptr(),
         q2.data_ptr(), _t4(k1_cache), _t4(k2_cache), _t4(v_cache), _ptr(seqlens), _ptr(lq1), _ptr(lk1),
         _ptr(lq2), _ptr(lk2), out.data_ptr(), int(num_splits), workspace.data_ptr(),
-        workspace.numel() * workspace.element_size())
+        workspace.numel() * workspace.element_size(), _ptr(rms_weight))
     _check(lib.diffattn_v1_decode(C.byref(p), _stream(stream)), "diffattn_v1_decode")
     return out
 

@@ -222,6 +222,7 @@ da_status diffattn_v1_fwd(const da_v1_fwd_params* p, void* stream) {
   if (p->dtype != DA_F32 && p->dtype != DA_BF16) return DA_ERR_INVALID_ARG;
   if (!(p->rms_eps >= 0.f)) return DA_ERR_INVALID_ARG;
   if (!p->lq1 || !p->lk1 || !p->lq2 || !p->lk2) return DA_ERR_INVALID_ARG;
+  if (p->rms_weight && !aligned(p->rms_weight, 4)) return DA_ERR_INVALID_ARG;
   if (p->B == 0 || p->N == 0 || p->H == 0) return DA_OK;
   for (const da_t4* t : {&p->q1, &p->q2, &p->k1, &p->k2, &p->v, &p->out})
     if (check_t4(*t, p->dtype) != DA_OK) return DA_ERR_INVALID_ARG;
@@ -235,7 +236,8 @@ da_status diffattn_v1_fwd(const da_v1_fwd_params* p, void* stream) {
     if (p->d_qk > 128 || p->d_v > 256 || (p->d_v % 32)) return DA_ERR_UNSUPPORTED;
     da::V1F32Args a{p->B, p->N, p->H, p->d_qk, p->d_v, p->causal, scale, p->lambda_init,
                     p->rms_eps, p->q1, p->q2, p->k1, p->k2, p->v, p->out, p->o2,
-                    p->lq1, p->lk1, p->lq2, p->lk2, p->lse1, p->lse2, p->rstd, p->lambda_out};
+                    p->lq1, p->lk1, p->lq2, p->lk2, p->lse1, p->lse2, p->rstd, p->lambda_out,
+                    p->rms_weight};
     return cuda_status(da::launch_v1_fwd_f32(a, s));
   }
   if (!((p->d_qk == 128 && p->d_v == 256) || (p->d_qk == 64 && p->d_v == 128))) return DA_ERR_UNSUPPORTED;
@@ -247,7 +249,7 @@ da_status diffattn_v1_fwd(const da_v1_fwd_params* p, void* stream) {
                   p->lambda_init, p->rms_eps, p->q1, p->q2, p->k1, p->k2, p->v,
                   p->out, p->o2, p->lq1, p->lk1, p->lq2, p->lk2, p->lse1, p->lse2,
                   p->rstd, p->lambda_out, p->workspace, p->workspace_bytes, d.status,
-                  d.num_sms};
+                  d.num_sms, p->rms_weight};
   return cuda_status(da::launch_v1_fwd(a, s));
 }
 
@@ -263,6 +265,7 @@ da_status diffattn_v1_bwd(const da_v1_bwd_params* p, void* stream) {
   if (p->dtype != DA_BF16 && p->dtype != DA_F32) return DA_ERR_INVALID_ARG;
   if (!p->lq1 || !p->lk1 || !p->lq2 || !p->lk2) return DA_ERR_INVALID_ARG;
   if (!p->dlq1 || !p->dlk1 || !p->dlq2 || !p->dlk2) return DA_ERR_INVALID_ARG;
+  if (p->rms_weight && !aligned(p->rms_weight, 4)) return DA_ERR_INVALID_ARG;
   if (p->B == 0 || p->N == 0 || p->H == 0) return DA_OK;
   // deterministic slots are laid out for the causal (key tile, query tile) pairs
   if (p->dtype != DA_BF16 || !((p->d_qk == 128 && p->d_v == 256) || (p->d_qk == 64 && p->d_v == 128)) ||
@@ -283,7 +286,8 @@ da_status diffattn_v1_bwd(const da_v1_bwd_params* p, void* stream) {
                   p->rms_eps, p->q1, p->q2, p->k1, p->k2, p->v, p->out, p->dout, p->o2,
                   p->lq1, p->lk1, p->lq2, p->lk2, p->lse1, p->lse2, p->rstd,
                   p->dq1, p->dq2, p->dk1, p->dk2, p->dv, p->dlq1, p->dlk1, p->dlq2, p->dlk2,
-                  p->workspace, p->workspace_bytes, d.status, d.num_sms, p->deterministic != 0};
+                  p->workspace, p->workspace_bytes, d.status, d.num_sms, p->deterministic != 0,
+                  p->rms_weight};
   return cuda_status(da::launch_v1_bwd(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -404,6 +408,7 @@ da_status diffattn_v1_decode(const da_v1_decode_params* p, void* stream) {
   if (!p->q1 || !p->q2 || !p->out || !aligned(p->q1, 16) || !aligned(p->q2, 16) || !aligned(p->out, 16))
     return DA_ERR_INVALID_ARG;
   if (!p->lq1 || !p->lk1 || !p->lq2 || !p->lk2) return DA_ERR_INVALID_ARG;
+  if (p->rms_weight && !aligned(p->rms_weight, 4)) return DA_ERR_INVALID_ARG;
   for (const da_t4* t : {&p->k1_cache, &p->k2_cache, &p->v_cache})
     if (check_t4(*t, DA_BF16) != DA_OK) return DA_ERR_INVALID_ARG;
   const int splits = p->num_splits > 0 ? p->num_splits : diffattn_v1_decode_num_splits(p->B, p->H, p->L_max);
@@ -420,7 +425,8 @@ da_status diffattn_v1_decode(const da_v1_decode_params* p, void* stream) {
   da::V1DecodeArgs a{p->B, p->H, p->d_qk, p->d_v, p->L_max, splits, scale * kLog2e, p->lambda_init, p->rms_eps,
                      p->q1, p->q2, p->k1_cache, p->k2_cache, p->v_cache, p->seqlens,
                      p->lq1, p->lk1, p->lq2, p->lk2, p->out,
-                     reinterpret_cast<float*>(ws), reinterpret_cast<float*>(ws + align256(po)), d.status};
+                     reinterpret_cast<float*>(ws), reinterpret_cast<float*>(ws + align256(po)), d.status,
+                     p->rms_weight};
   return cuda_status(da::launch_v1_decode(a, static_cast<cudaStream_t>(stream)));
 }
 

@@ -48,6 +48,7 @@ struct V1DecodeArgs {
   float* part_o;   // [splits, B, H, 2, d_v]
   float* part_ml;  // [splits, B, H, 2, 2]  (running max in log2 units, sum)
   uint32_t* status;
+  const float* rms_weight;  // [d_v] or nullptr (unit)
 };
 cudaError_t launch_v1_decode(const V1DecodeArgs& a, cudaStream_t s);
 
@@ -58,6 +59,7 @@ struct V1F32Args {
   da_t4 q1, q2, k1, k2, v, out, o2;
   const float *lq1, *lk1, *lq2, *lk2;
   float *lse1, *lse2, *rstd, *lambda_out;
+  const float* rms_weight;  // [d_v] or nullptr (unit)
 };
 cudaError_t launch_v1_fwd_f32(const V1F32Args& a, cudaStream_t s);
 
@@ -116,6 +118,7 @@ struct V1FwdArgs {
   size_t workspace_bytes;
   uint32_t* status;
   int num_sms;
+  const float* rms_weight;  // [d_v] or nullptr (unit)
 };
 size_t v1_fwd_workspace_bytes(int num_sms);
 cudaError_t launch_v1_fwd(const V1FwdArgs& a, cudaStream_t s);
@@ -134,6 +137,7 @@ struct V1BwdArgs {
   uint32_t* status;
   int num_sms;
   int deterministic;  // dQ through per-key-tile slots summed in a fixed order
+  const float* rms_weight;  // [d_v] or nullptr (unit); entries nonzero
 };
 size_t v1_bwd_workspace_bytes(int B, int N, int H, int d_qk, int d_v, int deterministic);
 cudaError_t launch_v1_bwd(const V1BwdArgs& a, cudaStream_t s);

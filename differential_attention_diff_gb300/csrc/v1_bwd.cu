@@ -4,8 +4,9 @@
 // The method pages ("Differential Transformer | ICLR 2025 Oral", dainus.ai,
 // "Differential Attention: 빼기의 힘"; "Differential Transformer V2",
 // pogovet.com, §1) define the forward; this is its chain rule.  With
-// c = 1 - lambda_init, Yhat = Y / c = O * rstd, G = dY, s = softmax scale:
-//   dO  = c * rstd * (G - Yhat * mean(G * Yhat))        (RMSNorm backward)
+// c = 1 - lambda_init, w the RMSNorm weight (fixed; unit by default),
+// Yhat = Y / (c w) = O * rstd, G = dY, s = softmax scale:
+//   dO  = c * rstd * (w G - Yhat * mean(w G * Yhat))    (RMSNorm backward)
 //   D1  = <dO, A1 V> = <dO, O + lambda O2>,   D2 = <dO, A2 V>
 //   dP  = dO V^T  (shared by both streams)
 //   dS1 = A1 (dP - D1),   dS2 = -lambda A2 (dP - D2)
@@ -298,11 +299,17 @@ v1_bwd_pre_kernel(V1BwdArgs a, BwdWs w) {
       const int64_t sidx = (static_cast<int64_t>(b) * a.H + h) * a.N + n;
       const float rstd = a.rstd[sidx];
       const float inv_c = c != 0.f ? 1.f / c : 0.f;
+      // yh = Y / (c w) is the normalised O, g = w G; then dOhat = c g
       float yh[kF], g[kF], o2[kF], gy = 0.f;
 #pragma unroll
       for (int e = 0; e < kF; ++e) {
         yh[e] = __bfloat162float(ye[e]) * inv_c;
         g[e] = __bfloat162float(ge[e]);
+        if (a.rms_weight) {
+          const float wv = a.rms_weight[lane * kF + e];
+          yh[e] = yh[e] / wv;
+          g[e] = g[e] * wv;
+        }
         o2[e] = __bfloat162float(oe[e]);
         gy = fmaf(g[e], yh[e], gy);
       }

@@ -330,8 +330,9 @@ v1_decode_merge_kernel(V1DecodeArgs a) {
   for (int w = 0; w < 8; ++w)
     if (w < dv / 32) tot += s_red[w];
   const float rstd = 1.f / sqrtf(tot * (1.f / dv) + a.rms_eps);
+  const float w = a.rms_weight ? a.rms_weight[f] : 1.f;
   static_cast<__nv_bfloat16*>(a.out)[(static_cast<int64_t>(b) * a.H + h) * dv + f] =
-      __float2bfloat16_rn((1.f - a.lambda_init) * o * rstd);
+      __float2bfloat16_rn((1.f - a.lambda_init) * o * rstd * w);
 }
 
 template <int DQK, int DV>

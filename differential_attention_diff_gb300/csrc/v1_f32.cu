@@ -137,7 +137,7 @@ v1_fwd_f32_kernel(V1F32Args a) {
 #pragma unroll
   for (int c = 0; c < kMaxDv / 32; ++c) {
     if (c < nv) {
-      out[lane + 32 * c] = o[c] * cs;
+      out[lane + 32 * c] = a.rms_weight ? (o[c] * cs) * a.rms_weight[lane + 32 * c] : o[c] * cs;
       if (o2p) o2p[lane + 32 * c] = o2[c];
     }
   }

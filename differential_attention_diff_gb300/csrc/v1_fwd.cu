@@ -591,13 +591,22 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
       const float tot = rank == 0 ? ssq + other_ssq : other_ssq + ssq;
       const float rstd = 1.f / sqrtf(tot * (1.f / kDv) + a.rms_eps);
       const float cs = cscale * rstd;
+      if (a.rms_weight) {
+        // Y = (1 - lambda_init) w O / rms: the per-feature weight of my half
+        const float* wk = a.rms_weight + keep;
+#pragma unroll
+        for (int e = 0; e < kHalf; ++e) dvals[e] = __fmul_rn(__fmul_rn(dvals[e], cs), __ldg(wk + e));
+      } else {
+#pragma unroll
+        for (int e = 0; e < kHalf; ++e) dvals[e] = __fmul_rn(dvals[e], cs);
+      }
 #pragma unroll
       for (int e = 0; e < kHalf; e += 8) {
         uint4 pk;
-        pk.x = pack_bf16x2(__fmul_rn(dvals[e], cs), __fmul_rn(dvals[e + 1], cs));
-        pk.y = pack_bf16x2(__fmul_rn(dvals[e + 2], cs), __fmul_rn(dvals[e + 3], cs));
-        pk.z = pack_bf16x2(__fmul_rn(dvals[e + 4], cs), __fmul_rn(dvals[e + 5], cs));
-        pk.w = pack_bf16x2(__fmul_rn(dvals[e + 6], cs), __fmul_rn(dvals[e + 7], cs));
+        pk.x = pack_bf16x2(dvals[e], dvals[e + 1]);
+        pk.y = pack_bf16x2(dvals[e + 2], dvals[e + 3]);
+        pk.z = pack_bf16x2(dvals[e + 4], dvals[e + 5]);
+        pk.w = pack_bf16x2(dvals[e + 6], dvals[e + 7]);
         *reinterpret_cast<uint4*>(stg + (e >> 6) * kBox + row * 128 + ((((e & 63) >> 3) ^ (row & 7)) << 4)) = pk;
       }
       if (live) {

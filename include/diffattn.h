@@ -72,12 +72,14 @@ float diffattn_lambda_init(int layer);
  *   lambda = exp(lq1 . lk1) - exp(lq2 . lk2) + lambda_init   (one scalar,
  *            computed on the device from the four vectors; never clamped)
  *   O      = (softmax(s Q1 K1^T) - lambda softmax(s Q2 K2^T)) V
- *   Y      = (1 - lambda_init) * O / sqrt(mean_k O_k^2 + rms_eps)
- * per (b, n, h), the mean over the V head dim d_v (unit RMSNorm weight).
+ *   Y      = (1 - lambda_init) * w * O / sqrt(mean_k O_k^2 + rms_eps)
+ * per (b, n, h), the mean over the V head dim d_v; w = rms_weight, the fixed
+ * per-feature RMSNorm weight (fp32 [d_v], shared by heads; NULL = unit).
  * q1, q2, k1, k2: [B, N, H, d_qk]; v, out: [B, N, H, d_v]; all of `dtype`.
  * lq1, lk1, lq2, lk2: fp32 [d_qk].
- * Supported: dtype DA_BF16 with d_qk = 128, d_v = 256, causal;
- *            dtype DA_F32 with d_qk <= 128, d_v <= 256 (d_v % 32 == 0).
+ * Supported: dtype DA_BF16 with (d_qk, d_v) = (128, 256) or (64, 128);
+ *            dtype DA_F32 with d_qk <= 128, d_v <= 256 (d_v % 32 == 0);
+ *            causal (key j <= query i) or not.
  * Optional saves for the backward (NULL pointer = not written):
  *   lse1, lse2 (log-sum-exp of the scaled scores per row), rstd
  *   (1/sqrt(mean O^2 + eps)): fp32 [B, H, N] contiguous;
@@ -101,6 +103,7 @@ typedef struct {
   float* lambda_out;
   void* workspace;
   size_t workspace_bytes;
+  const float* rms_weight;  /* fp32 [d_v]: the RMSNorm weight w (NULL = unit) */
 } da_v1_fwd_params;
 
 /* Workspace bytes diffattn_v1_fwd needs on the current device. */
@@ -119,7 +122,13 @@ da_status diffattn_v1_fwd(const da_v1_fwd_params* p, void* cuda_stream);
  * Inputs: the forward's inputs, its output `out` (Y), `dout` (dY), and the
  * saves lse1, lse2, rstd, o2 written by diffattn_v1_fwd.  Outputs: dq1, dq2,
  * dk1, dk2 [B,N,H,d_qk], dv [B,N,H,d_v] (dtype), dlq1, dlk1, dlq2, dlk2 fp32
- * [d_qk] (overwritten).  Supported: DA_BF16, d_qk = 128, d_v = 256, causal.
+ * [d_qk] (overwritten).  rms_weight: the forward's RMSNorm weight (NULL =
+ * unit); its entries must be nonzero, since the backward recovers the
+ * normalised output as Y / ((1 - lambda_init) w).  Supported: DA_BF16,
+ * (d_qk, d_v) = (128, 256) or
+ * (64, 128), causal or not; deterministic = 1 needs causal = 1
+ * (DA_ERR_UNSUPPORTED otherwise: its dQ slots are laid out for the causal
+ * tile pairs).
  * workspace: at least diffattn_v1_bwd_workspace_size(..., deterministic)
  * bytes, 256-byte aligned; its contents on entry do not matter.
  * deterministic = 0: each key tile adds its dQ tile into an fp32 accumulator
@@ -146,6 +155,7 @@ typedef struct {
   void* workspace;
   size_t workspace_bytes;
   int deterministic;
+  const float* rms_weight;  /* fp32 [d_v], as given to the forward (NULL = unit) */
 } da_v1_bwd_params;
 
 size_t diffattn_v1_bwd_workspace_size(int B, int N, int H, int d_qk, int d_v, int deterministic);
@@ -159,7 +169,7 @@ da_status diffattn_v1_bwd(const da_v1_bwd_params* p, void* cuda_stream);
  * seqlens[b] - 1, and its queries q1, q2 attend to positions
  * 0 .. seqlens[b] - 1 of the two K caches and the shared V cache:
  *   O = (softmax(s q1 K1^T) - lambda softmax(s q2 K2^T)) V
- *   Y = (1 - lambda_init) O / sqrt(mean_k O_k^2 + rms_eps)
+ *   Y = (1 - lambda_init) w O / sqrt(mean_k O_k^2 + rms_eps)  (w: rms_weight)
  * with lambda from the four vectors as in diffattn_v1_fwd.
  * q1, q2: bf16 [B, H, d_qk] contiguous; k1_cache, k2_cache: bf16
  * [B, L_max, H, d_qk], v_cache: bf16 [B, L_max, H, d_v] (da_t4 strides);
@@ -168,9 +178,9 @@ da_status diffattn_v1_bwd(const da_v1_bwd_params* p, void* cuda_stream);
  * num_splits: key-range splits per (b, head); 0 = chosen by the library
  * (diffattn_v1_decode_num_splits).  Workspace: split partials,
  * diffattn_v1_decode_workspace_size bytes, 256-byte aligned.
- * Supported: d_qk = 128, d_v = 256.  A sequence length outside [1, L_max] is
- * recorded as DA_ERR_BOUNDS in the device status word and that row of out is
- * written as zeros. */
+ * Supported: (d_qk, d_v) = (128, 256) or (64, 128).  A sequence length
+ * outside [1, L_max] is recorded as DA_ERR_BOUNDS in the device status word
+ * and that row of out is written as zeros. */
 typedef struct {
   int B, H, d_qk, d_v, L_max;
   float softmax_scale;   /* <= 0 selects 1/sqrt(d_qk) */
@@ -185,6 +195,7 @@ typedef struct {
   int num_splits;
   void* workspace;
   size_t workspace_bytes;
+  const float* rms_weight;  /* fp32 [d_v]: the RMSNorm weight w (NULL = unit) */
 } da_v1_decode_params;
 
 int diffattn_v1_decode_num_splits(int B, int H, int L_max);
@@ -224,7 +235,7 @@ da_status diffattn_v2_gate(const da_v2_gate_params* p, void* cuda_stream);
  * [B, 2h, N] contiguous (natural-log log-sum-exp of each head's scaled scores
  * per query); o_heads, bf16 [B, N, 2h, d] (each head's normalised output
  * O[t, j] before the even/odd combination).
- * Supported: d = 128, causal, (2h / h_kv) even. */
+ * Supported: d = 64 or 128, causal or not, (2h / h_kv) even. */
 typedef struct {
   int B, N, h, h_kv, d, d_model;
   int causal;
@@ -257,8 +268,8 @@ da_status diffattn_v2_fwd(const da_v2_fwd_params* p, void* cuda_stream);
  * Gate source as in diffattn_v2_fwd (fp32 [B, N, h], or x + w_lambda with
  * w_lambda [d_model, h]).  Optional saves: lse fp32 [B, Hq, N]; o_heads bf16
  * [B, N, Hq, d] (each head's normalised output; when NULL the per-head
- * outputs go to the workspace).  Supported: d = 128, causal, h divisible by
- * ratio, Hq / h_kv a multiple of ratio + 1 and even.
+ * outputs go to the workspace).  Supported: d = 64 or 128, causal or not,
+ * h divisible by ratio, Hq / h_kv a multiple of ratio + 1 and even.
  * workspace: diffattn_grouped_fwd_workspace_size bytes, 256-byte aligned. */
 typedef struct {
   int B, N, h, ratio, h_kv, d, d_model;
@@ -297,8 +308,8 @@ da_status diffattn_grouped_fwd(const da_grouped_fwd_params* p, void* cuda_stream
  * Optional outputs (NULL = not computed): dgate_logit fp32 [B, N, h]
  * contiguous (dz); dx bf16 [B, N, d_model] contiguous and dw_lambda fp32
  * [d_model, h] row-major, both of which need x and w_lambda.
- * Supported: d = 128, causal, (2h / h_kv) even; d_model % 64 == 0 and
- * h <= 64 where x / w_lambda are used.
+ * Supported: d = 64 or 128, causal or not, (2h / h_kv) even;
+ * d_model % 64 == 0 and h <= 64 where x / w_lambda are used.
  * workspace: diffattn_v2_bwd_workspace_size(B, N, h, d_model) bytes (with
  * d_model = 0 it covers calls that do not request dw_lambda), 256-byte
  * aligned, contents on entry irrelevant. */
@@ -337,7 +348,7 @@ da_status diffattn_v2_bwd(const da_v2_bwd_params* p, void* cuda_stream);
  * w_lambda as in diffattn_v2_fwd; out: bf16 [B, h, d] contiguous.
  * num_splits: key-range splits per (b, kv head); 0 = chosen by the library
  * (diffattn_v2_decode_num_splits).  Workspace: split partials,
- * diffattn_v2_decode_workspace_size bytes.  Supported: d = 128,
+ * diffattn_v2_decode_workspace_size bytes.  Supported: d = 64 or 128,
  * 2 <= 2h / h_kv <= 16 and even.  A sequence length outside [1, L_max] is
  * recorded as DA_ERR_BOUNDS in the device status word and its output row is
  * written as zeros. */

@@ -18,11 +18,12 @@ def bf16(x):
     return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
 
 
-def rounded_backward(f, fwd, li, heads=None, causal=True):
+def rounded_backward(f, fwd, li, heads=None, causal=True, rms_weight=None):
     """f: fp64 inputs (q1..v, dy) as [B, N, H, D]; fwd: the oracle forward on
     them.  Returns the gradients dq1, dq2, dk1, dk2, dv (and dlam) computed
     with the bf16 storage points; `heads` restricts to a list of heads;
-    causal=False drops the key <= query mask."""
+    causal=False drops the key <= query mask; rms_weight is the forward's
+    RMSNorm weight (None = unit)."""
     lam, c = fwd["lam"], 1.0 - li
     B, N, H, dqk = f["q1"].shape
     heads = range(H) if heads is None else heads
@@ -34,9 +35,11 @@ def rounded_backward(f, fwd, li, heads=None, causal=True):
         for h in heads:
             Y, O2, rstd = bf16(fwd["y"][b, :, h]), bf16(fwd["o2"][b, :, h]), fwd["rstd"][b, h]
             G = f["dy"][b, :, h]
-            yh = Y / c
-            gy = (G * yh).sum(1, keepdims=True)
-            dO = bf16(c * rstd[:, None] * (G - yh * gy / Y.shape[1]))
+            w = np.ones(Y.shape[1]) if rms_weight is None else rms_weight
+            yh = Y / (c * w)
+            gw = G * w
+            gy = (gw * yh).sum(1, keepdims=True)
+            dO = bf16(c * rstd[:, None] * (gw - yh * gy / Y.shape[1]))
             D2 = (dO * O2).sum(1)
             D1 = (dO * (yh / rstd[:, None] + lam * O2)).sum(1)
             dlam -= float(D2.sum())

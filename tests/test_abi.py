@@ -74,6 +74,7 @@ def test_v1_fwd_argument_checks(lib):
     assert f(C.byref(_v1p(k1=bd.da_t4((1 << 20) + 2, 64, 64, 64))), None) == bd.DA_ERR_INVALID_ARG
     assert f(C.byref(_v1p(v=bd.da_t4(1 << 20, 64, 60, 64))), None) == bd.DA_ERR_INVALID_ARG
     assert f(C.byref(_v1p(rms_eps=-1.0)), None) == bd.DA_ERR_INVALID_ARG
+    assert f(C.byref(_v1p(rms_weight=(1 << 20) + 2)), None) == bd.DA_ERR_INVALID_ARG  # fp32 alignment
     # empty problems are a no-op
     assert f(C.byref(_v1p(N=0)), None) == bd.DA_OK
 

@@ -73,6 +73,18 @@ def test_v1_fwd_f32_parity(B, N, H, dqk, dv, layer):
     assert abs(float(sv["lam"][0]) - ref["lam"]) <= 1e-6
 
 
+def test_v1_fwd_f32_rms_weight():
+    t = synth.v1_inputs(2, 77, 3, 20, 64, dtype="f32", seed=1077, device="cuda")
+    w = 0.5 + torch.rand(64, generator=torch.Generator().manual_seed(1078), dtype=torch.float32).cuda()
+    li = bd.diffattn_lambda_init(3)
+    out = bd.diffattn_v1_fwd(t["q1"], t["q2"], t["k1"], t["k2"], t["v"], t["lq1"], t["lk1"],
+                             t["lq2"], t["lk2"], li, rms_weight=w)
+    torch.cuda.synchronize()
+    ref = orc.v1_forward(*(f64(t[n]) for n in ("q1", "q2", "k1", "k2", "v", "lq1", "lk1", "lq2",
+                                                "lk2")), float(np.float32(li)), rms_weight=f64(w))
+    assert maxdiff(f64(out), ref["y"]) <= F32_TOL * rms(f64(t["v"]))
+
+
 def test_v1_fwd_f32_exact_cancellation():
     """Q1 = Q2, K1 = K2 and lambda = 1: both streams run the same arithmetic,
     so the difference and the output are exactly zero."""

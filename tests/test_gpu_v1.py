@@ -34,7 +34,7 @@ def _status_clean():
     assert bd.diffattn_get_device_status() == bd.DA_OK
 
 
-def _check(t, li, y, sv, rows=None, heads=None, batches=None, causal=True):
+def _check(t, li, y, sv, rows=None, heads=None, batches=None, causal=True, w=None):
     B, N, H, _ = t["q1"].shape
     heads = range(H) if heads is None else heads
     batches = range(B) if batches is None else batches
@@ -45,7 +45,7 @@ def _check(t, li, y, sv, rows=None, heads=None, batches=None, causal=True):
             sl = lambda n: f64(t[n][b:b + 1, :, h:h + 1])  # noqa: E731
             ref = orc.v1_forward(sl("q1"), sl("q2"), sl("k1"), sl("k2"), sl("v"),
                                  *(f64(t[n]) for n in NAMES[5:]), float(np.float32(li)), rows=rows,
-                                 causal=causal)
+                                 causal=causal, rms_weight=None if w is None else f64(w))
             r = ref["rows"]
             tol = TOL * rms(f64(t["v"][b, :, h]))
             worst = max(worst, float(np.max(np.abs(yv[b, r, h] - ref["y"][0, :, 0]))) / tol)
@@ -102,6 +102,17 @@ def test_v1_fwd_parity_not_causal(B, N, H, dqk, layer):
     y, sv = bd.diffattn_v1_fwd(*(t[n] for n in NAMES), li, save=True, causal=False)
     torch.cuda.synchronize()
     _check(t, li, y, sv, causal=False)
+
+
+@pytest.mark.parametrize("B,N,H,dqk", [(1, 200, 2, 128), (2, 129, 3, 64)])
+def test_v1_fwd_parity_rms_weight(B, N, H, dqk):
+    """A non-unit RMSNorm weight multiplies each normalised feature."""
+    t = synth.v1_inputs(B, N, H, dqk, 2 * dqk, "bf16", seed=4300 + N + H, device="cuda")
+    w = 0.5 + torch.rand(2 * dqk, generator=torch.Generator().manual_seed(4301), dtype=torch.float32).cuda()
+    li = bd.diffattn_lambda_init(2)
+    y, sv = bd.diffattn_v1_fwd(*(t[n] for n in NAMES), li, save=True, rms_weight=w)
+    torch.cuda.synchronize()
+    _check(t, li, y, sv, w=w)
 
 
 def test_v1_fwd_without_saves_matches():

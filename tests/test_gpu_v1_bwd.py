@@ -49,12 +49,12 @@ def _status_clean():
     assert bd.diffattn_get_device_status() == bd.DA_OK
 
 
-def _run(t, li, causal=True):
+def _run(t, li, causal=True, w=None):
     """The training step: GPU forward with saves, then the GPU backward."""
-    y, sv = bd.diffattn_v1_fwd(*(t[n] for n in NAMES), li, save=True, causal=causal)
-    g = bd.diffattn_v1_bwd(*(t[n] for n in NAMES), li, y, t["dy"], sv, causal=causal)
+    y, sv = bd.diffattn_v1_fwd(*(t[n] for n in NAMES), li, save=True, causal=causal, rms_weight=w)
+    g = bd.diffattn_v1_bwd(*(t[n] for n in NAMES), li, y, t["dy"], sv, causal=causal, rms_weight=w)
     torch.cuda.synchronize()
-    g["saves"] = dict(t=t, li=li, y=y, sv=sv)  # what this backward received
+    g["saves"] = dict(t=t, li=li, y=y, sv=sv, w=w)  # what this backward received
     return g
 
 
@@ -64,9 +64,11 @@ def _dlam_from_saves(sv):
     the same with dO rounded to bf16 (the value the kernels hold)."""
     c = 1.0 - sv["li"]
     Y, O2, G = f64(sv["y"]), f64(sv["sv"]["o2"]), f64(sv["t"]["dy"])
+    w = 1.0 if sv.get("w") is None else f64(sv["w"])
     rstd = np.transpose(f64(sv["sv"]["rstd"]), (0, 2, 1))[..., None]  # [B, N, H, 1]
-    yh = Y / c
-    dO = c * rstd * (G - yh * (G * yh).mean(-1, keepdims=True))
+    yh = Y / (c * w)
+    gw = G * w
+    dO = c * rstd * (gw - yh * (gw * yh).mean(-1, keepdims=True))
     return -float(np.sum(dO * O2)), -float(np.sum(bf16(dO) * O2))
 
 
@@ -78,16 +80,17 @@ def _lam_vectors(t, dlam):
     return dict(dlq1=dlam * ea * lk1, dlk1=dlam * ea * lq1, dlq2=-dlam * eb * lk2, dlk2=-dlam * eb * lq2)
 
 
-def _run_exact_saves(t, li, causal=True):
+def _run_exact_saves(t, li, causal=True, w=None):
     """The GPU backward alone, given the oracle's forward outputs."""
-    fwd = orc.v1_forward(*(f64(t[n]) for n in NAMES), li, causal=causal)
+    fwd = orc.v1_forward(*(f64(t[n]) for n in NAMES), li, causal=causal,
+                         rms_weight=None if w is None else f64(w))
     dev = t["q1"].device
     y = torch.from_numpy(fwd["y"]).to(dev, torch.bfloat16)
     sv = dict(o2=torch.from_numpy(fwd["o2"]).to(dev, torch.bfloat16),
               lse1=torch.from_numpy(fwd["lse1"]).to(dev, torch.float32),
               lse2=torch.from_numpy(fwd["lse2"]).to(dev, torch.float32),
               rstd=torch.from_numpy(fwd["rstd"]).to(dev, torch.float32))
-    g = bd.diffattn_v1_bwd(*(t[n] for n in NAMES), li, y, t["dy"], sv, causal=causal)
+    g = bd.diffattn_v1_bwd(*(t[n] for n in NAMES), li, y, t["dy"], sv, causal=causal, rms_weight=w)
     torch.cuda.synchronize()
     return g
 
@@ -131,10 +134,11 @@ def _compare(g, ref, model, heads=None, lam_vectors=True, bar="bwd"):
     assert max(worst.values()) <= 1.0, worst
 
 
-def _model(t, li, heads=None, causal=True):
+def _model(t, li, heads=None, causal=True, w=None):
     f = {n: f64(t[n]) for n in NAMES + ("dy",)}
-    fwd = orc.v1_forward(*(f[n] for n in NAMES), li, causal=causal)
-    return rounded_backward(f, fwd, li, heads=heads, causal=causal)
+    wf = None if w is None else f64(w)
+    fwd = orc.v1_forward(*(f[n] for n in NAMES), li, causal=causal, rms_weight=wf)
+    return rounded_backward(f, fwd, li, heads=heads, causal=causal, rms_weight=wf)
 
 
 @pytest.mark.parametrize("B,N,H,layer", [(1, 200, 2, 1), (2, 384, 1, 3), (1, 129, 2, 14),
@@ -194,6 +198,19 @@ def test_v1_bwd_parity_not_causal(B, N, H, dqk, layer):
     model = _model(t, li, causal=False)
     _compare(_run_exact_saves(t, li, causal=False), ref, model, bar="bwd")
     _compare(_run(t, li, causal=False), ref, model, bar="step")
+
+
+@pytest.mark.parametrize("B,N,H,dqk,layer", [(1, 200, 2, 128, 1), (2, 129, 1, 64, 14)])
+def test_v1_bwd_parity_rms_weight(B, N, H, dqk, layer):
+    """A non-unit RMSNorm weight w (fixed: no gradient): the preprocess takes
+    the normalised output as Y / ((1 - lambda_init) w) and dOhat = c w G."""
+    t = synth.v1_inputs(B, N, H, dqk, 2 * dqk, "bf16", seed=5300 + N + H, device="cuda", with_dy=True)
+    w = 0.5 + torch.rand(2 * dqk, generator=torch.Generator().manual_seed(5301), dtype=torch.float32).cuda()
+    li = float(np.float32(bd.diffattn_lambda_init(layer)))
+    ref = orc.v1_backward(*(f64(t[n]) for n in NAMES), li, f64(t["dy"]), rms_weight=f64(w))
+    model = _model(t, li, w=w)
+    _compare(_run_exact_saves(t, li, w=w), ref, model, bar="bwd")
+    _compare(_run(t, li, w=w), ref, model, bar="step")
 
 
 def test_v1_bwd_deterministic_parts_repeat():

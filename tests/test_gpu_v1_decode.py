@@ -36,7 +36,7 @@ def _run(t, li, **kw):
     return out
 
 
-def _check(t, li, out, batches=None):
+def _check(t, li, out, batches=None, w=None):
     B = t["q1"].shape[0]
     batches = range(B) if batches is None else batches
     sl = [int(x) for x in t["seqlens"].cpu()]
@@ -46,7 +46,8 @@ def _check(t, li, out, batches=None):
         L = sl[b]
         ref = orc.v1_decode(f64(t["q1"][b:b + 1]), f64(t["q2"][b:b + 1]), f64(t["k1_cache"][b:b + 1, :L]),
                             f64(t["k2_cache"][b:b + 1, :L]), f64(t["v_cache"][b:b + 1, :L]), [L],
-                            *(f64(t[n]) for n in LAMS), float(np.float32(li)))
+                            *(f64(t[n]) for n in LAMS), float(np.float32(li)),
+                            rms_weight=None if w is None else f64(w))
         for h in range(t["q1"].shape[1]):
             v = f64(t["v_cache"][b, :L, h])
             tol = TOL * float(np.sqrt(np.mean(v * v)))
@@ -75,6 +76,13 @@ def test_v1_decode_parity_head_dims_64_128(B, L, H, seqlens, splits, layer):
     t = synth.v1_decode_inputs(B, L, H, 64, 128, seed=6100 + L + H, device="cuda", seqlens=seqlens)
     li = bd.diffattn_lambda_init(layer)
     _check(t, li, _run(t, li, num_splits=splits))
+
+
+def test_v1_decode_parity_rms_weight():
+    t = synth.v1_decode_inputs(2, 700, 3, 128, 256, seed=6200, device="cuda", seqlens=[700, 333])
+    w = 0.5 + torch.rand(256, generator=torch.Generator().manual_seed(6201), dtype=torch.float32).cuda()
+    li = bd.diffattn_lambda_init(4)
+    _check(t, li, _run(t, li, num_splits=3, rms_weight=w), w=w)
 
 
 def test_v1_decode_split_count_invariance():
