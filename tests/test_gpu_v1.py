@@ -115,6 +115,18 @@ def test_v1_fwd_parity_rms_weight(B, N, H, dqk):
     _check(t, li, y, sv, w=w)
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_v1_fwd_late_large_scores_rescale(causal):
+    """K1 rows from 256 on scaled by 30 (stream 1 only): stream 1's rows
+    re-normalise mid-sequence while stream 2's do not."""
+    t = synth.v1_inputs(1, 500, 2, 128, 256, "bf16", seed=4400, device="cuda")
+    t["k1"][:, 256:] *= 30.0
+    li = bd.diffattn_lambda_init(1)
+    y, sv = bd.diffattn_v1_fwd(*(t[n] for n in NAMES), li, save=True, causal=causal)
+    torch.cuda.synchronize()
+    _check(t, li, y, sv, causal=causal)
+
+
 def test_v1_fwd_without_saves_matches():
     t = synth.v1_inputs(1, 300, 2, 128, 256, "bf16", seed=51, device="cuda")
     li = bd.diffattn_lambda_init(3)

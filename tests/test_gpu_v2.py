@@ -107,6 +107,20 @@ def test_v2_fwd_parity_not_causal(B, N, h, hkv, d):
     _check_pairs(t, out, gate, lse=sv["lse"], causal=False)
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_v2_fwd_late_large_scores_rescale(causal):
+    """Keys from 256 on scaled by 30: their scores exceed the first tile's
+    running max by far more than the softmax's stale-max guard allows, so the
+    rows re-normalise mid-sequence (new max, O and l rescaled)."""
+    t = synth.v2_inputs(1, 500, 2, 1, 128, 128, seed=3300, device="cuda")
+    t["k"][:, 256:] *= 30.0
+    out, sv = bd.diffattn_v2_fwd(t["q"], t["k"], t["v"], x=t["x"], w_lambda=t["w_lambda"], save=True,
+                                 causal=causal)
+    torch.cuda.synchronize()
+    gate = orc.v2_gate(f64(t["x"]), f64(t["w_lambda"]))
+    _check_pairs(t, out, gate, lse=sv["lse"], causal=causal)
+
+
 def test_v2_fwd_gate_given_equals_x_path():
     t = synth.v2_inputs(1, 300, 4, 2, 128, 256, seed=31, device="cuda")
     gate = bd.diffattn_v2_gate(t["x"], t["w_lambda"])
