@@ -44,13 +44,14 @@ constexpr int kBox = 128 * 128;  // one 64-column box of 128 rows (bf16)
 //   Q at 0 (DQK/64), K ring [stage][DQK/64] after it, V ring [stage][DV/64]
 //   after that.  The barrier block sits after the largest layout.
 constexpr int kOffBar = 14 * kBox;            // 229376
-constexpr int kSmemBytes = kOffBar + 1024 + 1024;
+constexpr int kSmemBytes = kOffBar + 2048 + 1024;  // 232448: the per-block limit
 
 enum {
   B_QFULL = 0, B_QEMPTY, B_KFULL, B_KFULL1, B_KEMPTY, B_KEMPTY1, B_VFULL, B_VFULL1,
-  B_VEMPTY, B_VEMPTY1, B_SFULL, B_SFULL1, B_PFULL, B_PFULL1, B_ORDY, B_ODONE, B_DATA, B_SSQ,
+  B_VEMPTY, B_VEMPTY1, B_SFULL, B_SFULL1, B_PFULL, B_PFULL1, B_ORDY, B_ODONE, B_DATA, B_SSQ, B_SSQ1,
   B_RXRDY, B_RXFREE, B_STG, B_STGFREE, B_GIVE, B_SCHF, B_SCHE = B_SCHF + 4, B_COUNT = B_SCHE + 4
 };
+static_assert(B_COUNT * 8 <= 256, "barriers end where the TMEM slot begins");
 
 constexpr uint32_t kIdescS = idesc_bf16(128, 128, 0);
 
@@ -66,8 +67,9 @@ struct Shared {
   // ring of the next work items (4 slots), written by rank 0's producer
   __device__ volatile int* ring() const { return reinterpret_cast<volatile int*>(gen + kOffBar + 272); }
   __device__ uint32_t ring_s(int slot) const { return base + kOffBar + 272 + 4 * slot; }
-  __device__ uint32_t ssq_rx() const { return base + kOffBar + 512; }  // float[128]
-  __device__ float* ssq_rx_ptr() const { return reinterpret_cast<float*>(gen + kOffBar + 512); }
+  // the partner's per-row partial sums of squares, by item parity: float[2][128]
+  __device__ uint32_t ssq_rx(int p) const { return base + kOffBar + 512 + 512 * p; }
+  __device__ float* ssq_rx_ptr(int p) const { return reinterpret_cast<float*>(gen + kOffBar + 512 + 512 * p); }
 };
 
 __device__ __forceinline__ uint64_t globaltimer() {
@@ -128,8 +130,12 @@ __device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t
 __device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v) {
   asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
 }
-__device__ __forceinline__ void st_cluster_f32(uint32_t addr, float v) {
-  asm volatile("st.shared::cluster.f32 [%0], %1;" ::"r"(addr), "f"(v) : "memory");
+// 4 bytes into a cluster peer's shared memory, completion counted in bytes on
+// the peer's mbarrier
+__device__ __forceinline__ void st_async_f32(uint32_t dst_cluster, float v, uint32_t bar_cluster) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(dst_cluster),
+               "r"(__float_as_uint(v)), "r"(bar_cluster)
+               : "memory");
 }
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -206,7 +212,8 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
     mbar_init(sh.bar(B_ORDY), 1);
     mbar_init(sh.bar(B_ODONE), 1);
     mbar_init(sh.bar(B_DATA), 1);  // + 64 KB of bulk-copy bytes from the partner
-    mbar_init(sh.bar(B_SSQ), 128);
+    mbar_init(sh.bar(B_SSQ), 1);   // + 512 bytes of the partner's partial sums
+    mbar_init(sh.bar(B_SSQ1), 1);
     mbar_init(sh.bar(B_RXRDY), 1);
     mbar_init(sh.bar(B_GIVE), 128);
     mbar_init(sh.bar(B_RXFREE), 128);
@@ -428,8 +435,9 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
     const uint32_t partner_rx0 = map_to_rank(sh.base + kOffK, partner);
     const uint32_t partner_rxrdy = map_to_rank(sh.bar(B_RXRDY), partner);
     const uint32_t partner_data = map_to_rank(sh.bar(B_DATA), partner);
-    const uint32_t partner_ssq_bar = map_to_rank(sh.bar(B_SSQ), partner);
-    const uint32_t partner_ssq_slot = map_to_rank(sh.ssq_rx() + row * 4, partner);
+    const uint32_t partner_ssq_bar[2] = {map_to_rank(sh.bar(B_SSQ), partner), map_to_rank(sh.bar(B_SSQ1), partner)};
+    const uint32_t partner_ssq_slot[2] = {map_to_rank(sh.ssq_rx(0) + row * 4, partner),
+                                          map_to_rank(sh.ssq_rx(1) + row * 4, partner)};
     int kv = 0, it = 0;
     bool ok = true;
     for (;; ++it) {
@@ -475,10 +483,7 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
       tc_fence_after();
       const float inv_l = 1.f / l_run;
       const int give = (1 - static_cast<int>(rank)) * kHalf, keep = static_cast<int>(rank) * kHalf;
-      // (1) my MMAs are done, so my K ring may receive; wait until the
-      //     partner's is free too, then write the partner's half of my O/l
-      //     into it (row r: 512 bytes, 16-byte chunks XOR-swizzled by r & 7)
-      // stage the partner's half of my O/l in this item's last V stage (idle
+      // (1) stage the partner's half of my O/l in this item's last V stage (idle
       // now; row r at r * 512 bytes, 16-byte chunks XOR-swizzled by r & 7),
       // then one thread moves the 64 KB into the partner's K ring with a bulk
       // copy whose bytes complete on the partner's DATA barrier
@@ -511,9 +516,18 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
         }
         bulk_copy_to_peer(partner_rx0, sh.base + kOffV + give_stage * kNV * kBox, 128 * kRowX, partner_data);
       }
-      if (!wait_bar<true>(sh, sh.bar(B_DATA), it & 1, a.status, 0x3204)) { ok = false; break; }
-      // (2) O = O1/l1 - lambda O2/l2 on my half; partial sum of squares
+      // (2) my own half of O/l into registers while the copies are in flight
       float dvals[kHalf];
+#pragma unroll
+      for (int c = 0; c < kHalf / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(t_o + keep + c * 32, o);
+        tmem_ld_wait();
+#pragma unroll
+        for (int e = 0; e < 32; ++e) dvals[c * 32 + e] = __uint_as_float(o[e]) * inv_l;
+      }
+      if (!wait_bar<true>(sh, sh.bar(B_DATA), it & 1, a.status, 0x3204)) { ok = false; break; }
+      // (3) O = O1/l1 - lambda O2/l2 on my half; partial sum of squares
       float ssq = 0.f;
       const int n = w.mt * kBM + row;
       const bool live = n < a.N;
@@ -528,29 +542,27 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
       const uint32_t stg_s = sh.base + kOffV + stg_stage * kNV * kBox;
       const bool want_o2 = a.o2.ptr != nullptr;
 #pragma unroll
-      for (int c = 0; c < kHalf / 32; ++c) {
-        uint32_t o[32];
-        tmem_ld32(t_o + keep + c * 32, o);
-        tmem_ld_wait();
+      for (int u = 0; u < kHalf / 4; ++u) {
+        const float4 oth = *reinterpret_cast<const float4*>(my_rx + ((u ^ (row & 7)) << 4));
+        const float othv[4] = {oth.x, oth.y, oth.z, oth.w};
 #pragma unroll
-        for (int e = 0; e < 32; e += 4) {
-          const int u = (c * 32 + e) >> 2;
-          const float4 oth = *reinterpret_cast<const float4*>(my_rx + ((u ^ (row & 7)) << 4));
-          const float othv[4] = {oth.x, oth.y, oth.z, oth.w};
-#pragma unroll
-          for (int q = 0; q < 4; ++q) {
-            const float own = __uint_as_float(o[e + q]) * inv_l;
-            const float a1 = rank == 0 ? own : othv[q];
-            const float a2 = rank == 0 ? othv[q] : own;
-            const float dd = __fsub_rn(a1, __fmul_rn(lam, a2));
-            dvals[c * 32 + e + q] = dd;
-            ssq = fmaf(dd, dd, ssq);
-          }
+        for (int q = 0; q < 4; ++q) {
+          const float own = dvals[4 * u + q];
+          const float a1 = rank == 0 ? own : othv[q];
+          const float a2 = rank == 0 ? othv[q] : own;
+          const float dd = __fsub_rn(a1, __fmul_rn(lam, a2));
+          dvals[4 * u + q] = dd;
+          ssq = fmaf(dd, dd, ssq);
         }
       }
-      st_cluster_f32(partner_ssq_slot, ssq);
-      remote_arrive(partner_ssq_bar);
-      if (!wait_bar<true>(sh, sh.bar(B_SSQ), it & 1, a.status, 0x3205)) { ok = false; break; }
+      // (4) swap the per-row partial sums: one asynchronous 4-byte store per
+      //     row into the partner's slot of this item's parity, its bytes
+      //     counted on the partner's barrier of that parity (one local
+      //     arrive with the expected 512 bytes per phase)
+      const int sp = it & 1;
+      if (row == 0) mbar_arrive_expect_tx(sh.bar(B_SSQ + sp), 128 * 4);
+      st_async_f32(partner_ssq_slot[sp], ssq, partner_ssq_bar[sp]);
+      if (!wait_bar<true>(sh, sh.bar(B_SSQ + sp), (it >> 1) & 1, a.status, 0x3205)) { ok = false; break; }
       if (want_o2) {
         // O2 / l2 of my columns: received (rank 0) or my own (rank 1)
 #pragma unroll 1
@@ -587,7 +599,7 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
         }
       }
       mbar_arrive(sh.bar(B_RXFREE));  // this row's part of the K ring has been read
-      const float other_ssq = sh.ssq_rx_ptr()[row];
+      const float other_ssq = sh.ssq_rx_ptr(sp)[row];
       const float tot = rank == 0 ? ssq + other_ssq : other_ssq + ssq;
       const float rstd = 1.f / sqrtf(tot * (1.f / kDv) + a.rms_eps);
       const float cs = cscale * rstd;
