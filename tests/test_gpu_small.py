@@ -85,6 +85,21 @@ def test_v1_fwd_f32_rms_weight():
     assert maxdiff(f64(out), ref["y"]) <= F32_TOL * rms(f64(t["v"]))
 
 
+def test_v1_fwd_f32_not_causal():
+    """The fp32 SIMT path without the causal mask: every query sees every key."""
+    t = synth.v1_inputs(2, 77, 3, 20, 64, dtype="f32", seed=1177, device="cuda")
+    li = bd.diffattn_lambda_init(5)
+    out, sv = bd.diffattn_v1_fwd(t["q1"], t["q2"], t["k1"], t["k2"], t["v"], t["lq1"], t["lk1"],
+                                 t["lq2"], t["lk2"], li, save=True, causal=False)
+    torch.cuda.synchronize()
+    ref = orc.v1_forward(*(f64(t[n]) for n in ("q1", "q2", "k1", "k2", "v", "lq1", "lk1", "lq2",
+                                                "lk2")), float(np.float32(li)), causal=False)
+    tol = F32_TOL * rms(f64(t["v"]))
+    assert maxdiff(f64(out), ref["y"]) <= tol
+    assert maxdiff(f64(sv["o2"]), ref["o2"]) <= tol
+    assert maxdiff(f64(sv["lse1"]), ref["lse1"]) <= 1e-4
+
+
 def test_v1_fwd_f32_exact_cancellation():
     """Q1 = Q2, K1 = K2 and lambda = 1: both streams run the same arithmetic,
     so the difference and the output are exactly zero."""
