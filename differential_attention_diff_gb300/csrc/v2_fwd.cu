@@ -24,15 +24,20 @@
 //   warp 9 (one lane): MMA issuer — S = Q K^T (SS form) and O += P V (P read
 //     from TMEM, V from shared memory), interleaving the two heads so that
 //     one head's softmax overlaps the other head's MMAs.
-//   warps 0-3 / 4-7: softmax of the even / odd head, one thread per query row
-//     (TMEM lane): online softmax per tile (softmax.cuh: the row max of the
-//     first tile, a guarded stale max afterwards), P written back to TMEM as
-//     bf16, O rescaled in TMEM on the rare tiles that raise the max.
-//     The same threads run the epilogue: O_even / l_even - gate * O_odd /
-//     l_odd, bf16 store, optional log-sum-exp and per-head outputs (the
-//     backward's saves).  With no output tensor the kernel writes only the
-//     per-head outputs (the attention part of grouped differential
-//     attention, whose groups span more than a pair).
+//   warps 0-7: softmax of every tile of both heads, split by key columns:
+//     warpgroup 0 takes keys 0-63 of the tile, warpgroup 1 keys 64-127 (one
+//     thread per query row and half), so a head's tile is done by eight warps
+//     and its next P.V and S MMAs start sooner (the per-head chain softmax ->
+//     P.V -> next S bounds the loop).  Online softmax per tile (the row max
+//     of the first tile, shared by the two halves; a guarded stale max
+//     afterwards), P written back to TMEM as bf16 over the columns each half
+//     read, O rescaled in TMEM on the rare tiles that raise the max.  The
+//     same threads run the epilogue (each warpgroup half of the D features):
+//     O_even / l_even - gate * O_odd / l_odd, bf16 store, optional
+//     log-sum-exp and per-head outputs (the backward's saves).  With no
+//     output tensor the kernel writes only the per-head outputs (the
+//     attention part of grouped differential attention, whose groups span
+//     more than a pair).
 //
 // Every mbarrier wait is bounded (about 2 s); on expiry the kernel records
 // DA_ERR_TIMEOUT in the status word, raises a shared abort flag so the other
@@ -52,7 +57,7 @@ constexpr int kBox = 128 * 128;            // bytes of one 64-column box of 128 
 //   Q [head][box] at 0, K [stage][box] at 2 D/64 boxes, V [stage][box] at
 //   4 D/64 boxes.  The barrier block sits after the largest (D = 128) layout.
 constexpr int kOffBar = 12 * kBox;         // 196608
-constexpr int kSmemBytes = kOffBar + 4096 + 1024;  // + barriers/exchange + alignment slack
+constexpr int kSmemBytes = kOffBar + 8192 + 1024;  // + barriers/exchange + alignment slack
 
 // barrier indices (8 bytes each)
 enum {
@@ -70,8 +75,9 @@ struct Shared {
   __device__ volatile int* abort_flag() const {
     return reinterpret_cast<volatile int*>(gen + kOffBar + 192);
   }
-  __device__ float* lx() const { return reinterpret_cast<float*>(gen + kOffBar + 256); }  // [2][128]
-  __device__ float* mx() const { return reinterpret_cast<float*>(gen + kOffBar + 1280); } // [2][128]
+  // per-row partial sums [head][half][128] and half maxima [head][half][128]
+  __device__ float* lx() const { return reinterpret_cast<float*>(gen + kOffBar + 256); }
+  __device__ float* xm() const { return reinterpret_cast<float*>(gen + kOffBar + 256 + 2048); }
 };
 
 __device__ __forceinline__ uint64_t globaltimer() {
@@ -96,6 +102,43 @@ __device__ __forceinline__ bool wait_bar(const Shared& sh, uint32_t bar, uint32_
       return false;
     }
   }
+}
+
+// ---- the softmax of one half row (64 key columns) --------------------------
+// Max over the valid columns of this half (key column c0 + e <= lim when
+// masked; -inf when none is valid).
+template <bool kMask>
+__device__ __forceinline__ float half_max(const uint32_t (&s)[64], int c0, int lim) {
+  float mx = -INFINITY;
+#pragma unroll
+  for (int e = 0; e < 64; ++e)
+    if (!kMask || c0 + e <= lim) mx = fmaxf(mx, __uint_as_float(s[e]));
+  return mx;
+}
+// exp2(S scale log2e - m) of the 64 scores, written as bf16 pairs over the
+// first 32 of those columns (t_p); returns their sum.
+template <bool kMask>
+__device__ __forceinline__ float exp_half(const uint32_t (&s)[64], int c0, int lim, uint64_t sl2x2,
+                                          float m, uint32_t t_p) {
+  const uint64_t negm2 = f2(-m, -m);
+  const uint64_t a0 = exp_chunk<kMask>(s, c0, lim, sl2x2, negm2, t_p);
+  const uint64_t a1 = exp_chunk<kMask>(s + 32, c0 + 32, lim, sl2x2, negm2, t_p + 16);
+  const uint64_t t = add_f32x2(a0, a1);
+  return f2_lo(t) + f2_hi(t);
+}
+// Named barrier 1 over the 256 softmax threads (warps 0-7): a plain sync,
+// and a sync that returns whether any of them passed `pred`.
+__device__ __forceinline__ void named_sync_256() {
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+}
+__device__ __forceinline__ bool named_red_or_256(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, 256, p;\n selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred))
+      : "memory");
+  return r != 0;
 }
 
 struct Item {
@@ -152,7 +195,7 @@ v2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       mbar_init(sh.bar(B_VFULL + s), 1);
       mbar_init(sh.bar(B_KVEMPTY + s), 1);
       mbar_init(sh.bar(B_SFULL + s), 1);
-      mbar_init(sh.bar(B_PFULL + s), 128);
+      mbar_init(sh.bar(B_PFULL + s), 256);  // both warpgroups write P of every tile
     }
     mbar_init(sh.bar(B_ORDY), 1);
     mbar_init(sh.bar(B_EPI), 256);
@@ -245,7 +288,8 @@ v2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
         const uint32_t vb = sh.base + kOffV + st * kNB * kBox;
 #pragma unroll
         for (int kk = 0; kk < kBN / 16; ++kk) {
-          tc_mma_ts(t_o[hh], t_s[hh] + kk * 8, sdesc_sw128(vb + kk * 2048, kBox, 1024), kIdescPV,
+          // P of keys 0-63 in columns 0-31 of the S buffer, keys 64-127 in 64-95
+          tc_mma_ts(t_o[hh], t_s[hh] + kk * 8 + (kk >= 4 ? 32 : 0), sdesc_sw128(vb + kk * 2048, kBox, 1024), kIdescPV,
                     (acc || kk > 0) ? 1u : 0u);
         }
       };
@@ -295,13 +339,23 @@ v2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
     }
   } else {
     // --------------------------------------------- softmax + epilogue -----
-    const int wg = warp >> 2;             // 0 = even head, 1 = odd head
+    // Both warpgroups work on every tile of both heads: warpgroup wg takes
+    // key columns [64 wg, 64 wg + 64) of the tile (thread = query row = TMEM
+    // lane), so a tile's exponentials run on eight warps and the head's next
+    // P.V / S MMAs start sooner.  The two halves of a row share one running
+    // max: exchanged on a row's first tile, and re-exchanged on the rare tile
+    // whose sum overflows the stale-max guard in either half (a CTA-wide
+    // barrier reduction decides).  Named barrier 1 (these 256 threads) is
+    // reached by both warpgroups in the same sequence (it depends only on
+    // the item, the tile and that reduction); every stop is decided by a
+    // barrier reduction, so neither leaves while the other waits.
+    const int wg = warp >> 2;             // key-column half of the tile
     const int q4 = warp & 3;
     const int row = q4 * 32 + lane;       // query row within the item = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
-    const uint32_t t_s = tmem + lane_off + wg * 128;
-    const uint32_t t_o = tmem + lane_off + 256 + wg * 128;
     const float sl2 = a.scale_log2;
+    const uint64_t sl2x2 = f2(sl2, sl2);
+    const int c0 = wg * 64;               // first key column of this half
     int it = 0, sc = 0, ec = 0;
     bool ok = true;
     // bounded 256-thread sync of the two softmax warpgroups
@@ -311,108 +365,159 @@ v2_fwd_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ 
       ++ec;
       return r;
     };
-    for (int i = sched(0); i < n_items && ok; ++it, i = sched(it)) {
+    float* xm = sh.xm();  // [head][half][row] half maxima
+    for (int i = sched(0); i < n_items; ++it, i = sched(it)) {
       const Item w = item_of(i, units, a.h, n_mtiles, causal);
-      float m_run = -INFINITY, l_run = 0.f;
-      for (int j = 0; j < w.n_kv; ++j, ++sc) {
-        if (!wait_bar(sh, sh.bar(B_SFULL + wg), sc & 1, a.status, 0x2201 + wg)) { ok = false; break; }
-        tc_fence_after();
+      float m_run[2] = {-INFINITY, -INFINITY}, l_half[2] = {0.f, 0.f};
+      bool stop = false;
+      for (int j = 0; j < w.n_kv && !stop; ++j, ++sc) {
         // masked columns: keys after the query (causal diagonal tile), or
         // keys >= N (ragged last tile without the causal mask)
         const bool masked = causal ? j == w.mt : (j == w.n_kv - 1 && (a.N % kBN) != 0);
         const int lim = causal ? row : a.N - 1 - j * kBN;
-        const float alpha = softmax_tile(t_s, lim, j == 0, masked, sl2, m_run, l_run);
-        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          // O is stable here: the commit that signalled S(j) covers PV(j-1).
 #pragma unroll 1
-          for (int c = 0; c < D / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(t_o + c * 32, o);
-            tmem_ld_wait();
+        for (int hh = 0; hh < 2; ++hh) {
+          // a failed wait does not leave here: the named-barrier sequence
+          // below is the same for both warpgroups, and the stop is decided
+          // together after the tile
+          if (!wait_bar(sh, sh.bar(B_SFULL + hh), sc & 1, a.status, 0x2201 + hh)) ok = false;
+          tc_fence_after();
+          const uint32_t t_s = tmem + lane_off + hh * 128 + c0;
+          uint32_t sv[64];
+          tmem_ld32(t_s, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+          tmem_ld32(t_s + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+          tmem_ld_wait();
+          if (j == 0) {
+            const float hm = masked ? half_max<true>(sv, c0, lim) : half_max<false>(sv, c0, lim);
+            xm[(hh * 2 + wg) * 128 + row] = hm;
+            named_sync_256();
+            m_run[hh] = fmaxf(hm, xm[(hh * 2 + (wg ^ 1)) * 128 + row]) * sl2;
+            l_half[hh] = masked ? exp_half<true>(sv, c0, lim, sl2x2, m_run[hh], t_s)
+                                : exp_half<false>(sv, c0, lim, sl2x2, m_run[hh], t_s);
+          } else {
+            float lsum = masked ? exp_half<true>(sv, c0, lim, sl2x2, m_run[hh], t_s)
+                                : exp_half<false>(sv, c0, lim, sl2x2, m_run[hh], t_s);
+            if (named_red_or_256(!(lsum <= kSumGuard))) {
+              // rare: some row's half left the guard; both halves of every
+              // row recompute against a max raised over this tile, and O is
+              // rescaled (O is stable here: the commit that signalled S(j)
+              // covers PV(j - 1))
+              const float hm = masked ? half_max<true>(sv, c0, lim) : half_max<false>(sv, c0, lim);
+              xm[(hh * 2 + wg) * 128 + row] = hm;
+              named_sync_256();
+              const float m_new = fmaxf(m_run[hh], fmaxf(hm, xm[(hh * 2 + (wg ^ 1)) * 128 + row]) * sl2);
+              const float alpha = fast_exp2(m_run[hh] - m_new);
+              m_run[hh] = m_new;
+              lsum = masked ? exp_half<true>(sv, c0, lim, sl2x2, m_new, t_s)
+                            : exp_half<false>(sv, c0, lim, sl2x2, m_new, t_s);
+              l_half[hh] = l_half[hh] * alpha + lsum;
+              if (__any_sync(0xffffffffu, alpha != 1.f)) {
+                // this half's D / 2 columns of the head's O
+                const uint32_t t_o = tmem + lane_off + 256 + hh * 128 + wg * (D / 2);
+#pragma unroll 1
+                for (int c = 0; c < D / 64; ++c) {
+                  uint32_t o[32];
+                  tmem_ld32(t_o + c * 32, o);
+                  tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(t_o + c * 32, o);
+                  for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                  tmem_st32(t_o + c * 32, o);
+                }
+              }
+            } else {
+              l_half[hh] += lsum;
+            }
           }
+          tmem_st_wait();
+          tc_fence_before();
+          mbar_arrive(sh.bar(B_PFULL + hh));
         }
-        tmem_st_wait();
-        tc_fence_before();
-        mbar_arrive(sh.bar(B_PFULL + wg));
+        stop = named_red_or_256(!ok || *sh.abort_flag());
       }
-      if (!ok) break;
+      if (stop) break;
       // ----------------------------------------------------- epilogue ----
-      if (!wait_bar(sh, sh.bar(B_ORDY), it & 1, a.status, 0x2203)) { ok = false; break; }
-      tc_fence_after();
-      sh.lx()[wg * 128 + row] = l_run;
-      sh.mx()[wg * 128 + row] = m_run;
-      if (!epi_sync(0x2204)) { ok = false; break; }
-      const int n = w.mt * kBM + row;
-      const float le = sh.lx()[row], lo = sh.lx()[128 + row];
-      // each warpgroup writes half of the D features of the row
-      constexpr int kHalf = D / 2, kNC = kHalf / 32;
-      uint32_t oe[kNC][32], oo[kNC][32];
-#pragma unroll
-      for (int c = 0; c < kNC; ++c) {
-        tmem_ld32(tmem + lane_off + 256 + wg * kHalf + c * 32, oe[c]);
-        tmem_ld32(tmem + lane_off + 384 + wg * kHalf + c * 32, oo[c]);
+      bool eok = wait_bar(sh, sh.bar(B_ORDY), it & 1, a.status, 0x2203);
+      if (eok) {
+        tc_fence_after();
+        sh.lx()[(0 * 2 + wg) * 128 + row] = l_half[0];
+        sh.lx()[(1 * 2 + wg) * 128 + row] = l_half[1];
+        eok = epi_sync(0x2204);
       }
-      tmem_ld_wait();
-      if (n < a.N) {
-        const float ie = 1.f / le;
-        if (a.out.ptr) {
-          const float gte = a.gate[(static_cast<int64_t>(w.b) * a.N + n) * a.h + w.p];
-          const float io = gte / lo;
-          __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out.ptr) + w.b * a.out.sb +
-                               static_cast<int64_t>(n) * a.out.sn + w.p * a.out.sh + wg * kHalf;
-          // both products rounded separately (no FMA contraction), so equal
-          // even and odd outputs with gate 1 cancel exactly
-          auto diff = [&](uint32_t xe, uint32_t xo) {
-            return __fsub_rn(__fmul_rn(__uint_as_float(xe), ie), __fmul_rn(__uint_as_float(xo), io));
-          };
+      if (eok) {
+        const int n = w.mt * kBM + row;
+        // l of each head: the two column halves' partial sums, in a fixed order
+        const float le = sh.lx()[0 * 128 + row] + sh.lx()[1 * 128 + row];
+        const float lo = sh.lx()[2 * 128 + row] + sh.lx()[3 * 128 + row];
+        // each warpgroup writes half of the D features of the row
+        constexpr int kHalf = D / 2, kNC = kHalf / 32;
+        uint32_t oe[kNC][32], oo[kNC][32];
 #pragma unroll
-          for (int c = 0; c < kNC; ++c) {
+        for (int c = 0; c < kNC; ++c) {
+          tmem_ld32(tmem + lane_off + 256 + wg * kHalf + c * 32, oe[c]);
+          tmem_ld32(tmem + lane_off + 384 + wg * kHalf + c * 32, oo[c]);
+        }
+        tmem_ld_wait();
+        if (n < a.N) {
+          const float ie = 1.f / le;
+          if (a.out.ptr) {
+            const float gte = a.gate[(static_cast<int64_t>(w.b) * a.N + n) * a.h + w.p];
+            const float io = gte / lo;
+            __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out.ptr) + w.b * a.out.sb +
+                                 static_cast<int64_t>(n) * a.out.sn + w.p * a.out.sh + wg * kHalf;
+            // both products rounded separately (no FMA contraction), so equal
+            // even and odd outputs with gate 1 cancel exactly
+            auto diff = [&](uint32_t xe, uint32_t xo) {
+              return __fsub_rn(__fmul_rn(__uint_as_float(xe), ie), __fmul_rn(__uint_as_float(xo), io));
+            };
 #pragma unroll
-            for (int e = 0; e < 32; e += 8) {
-              uint4 v;
-              v.x = pack_bf16x2(diff(oe[c][e], oo[c][e]), diff(oe[c][e + 1], oo[c][e + 1]));
-              v.y = pack_bf16x2(diff(oe[c][e + 2], oo[c][e + 2]), diff(oe[c][e + 3], oo[c][e + 3]));
-              v.z = pack_bf16x2(diff(oe[c][e + 4], oo[c][e + 4]), diff(oe[c][e + 5], oo[c][e + 5]));
-              v.w = pack_bf16x2(diff(oe[c][e + 6], oo[c][e + 6]), diff(oe[c][e + 7], oo[c][e + 7]));
-              *reinterpret_cast<uint4*>(dst + c * 32 + e) = v;
+            for (int c = 0; c < kNC; ++c) {
+#pragma unroll
+              for (int e = 0; e < 32; e += 8) {
+                uint4 v;
+                v.x = pack_bf16x2(diff(oe[c][e], oo[c][e]), diff(oe[c][e + 1], oo[c][e + 1]));
+                v.y = pack_bf16x2(diff(oe[c][e + 2], oo[c][e + 2]), diff(oe[c][e + 3], oo[c][e + 3]));
+                v.z = pack_bf16x2(diff(oe[c][e + 4], oo[c][e + 4]), diff(oe[c][e + 5], oo[c][e + 5]));
+                v.w = pack_bf16x2(diff(oe[c][e + 6], oo[c][e + 6]), diff(oe[c][e + 7], oo[c][e + 7]));
+                *reinterpret_cast<uint4*>(dst + c * 32 + e) = v;
+              }
             }
           }
-        }
-        if (a.o_heads.ptr) {
-          // the saves for the backward: each head's normalised output
-          const float inv_o = 1.f / lo;
-          __nv_bfloat16* he = static_cast<__nv_bfloat16*>(a.o_heads.ptr) + w.b * a.o_heads.sb +
-                              static_cast<int64_t>(n) * a.o_heads.sn + 2 * w.p * a.o_heads.sh + wg * kHalf;
-          __nv_bfloat16* ho = he + a.o_heads.sh;
+          if (a.o_heads.ptr) {
+            // the saves for the backward: each head's normalised output
+            const float inv_o = 1.f / lo;
+            __nv_bfloat16* he = static_cast<__nv_bfloat16*>(a.o_heads.ptr) + w.b * a.o_heads.sb +
+                                static_cast<int64_t>(n) * a.o_heads.sn + 2 * w.p * a.o_heads.sh + wg * kHalf;
+            __nv_bfloat16* ho = he + a.o_heads.sh;
 #pragma unroll
-          for (int c = 0; c < kNC; ++c) {
+            for (int c = 0; c < kNC; ++c) {
 #pragma unroll
-            for (int e = 0; e < 32; e += 8) {
-              uint4 ve, vo;
-              ve.x = pack_bf16x2(__uint_as_float(oe[c][e]) * ie, __uint_as_float(oe[c][e + 1]) * ie);
-              ve.y = pack_bf16x2(__uint_as_float(oe[c][e + 2]) * ie, __uint_as_float(oe[c][e + 3]) * ie);
-              ve.z = pack_bf16x2(__uint_as_float(oe[c][e + 4]) * ie, __uint_as_float(oe[c][e + 5]) * ie);
-              ve.w = pack_bf16x2(__uint_as_float(oe[c][e + 6]) * ie, __uint_as_float(oe[c][e + 7]) * ie);
-              vo.x = pack_bf16x2(__uint_as_float(oo[c][e]) * inv_o, __uint_as_float(oo[c][e + 1]) * inv_o);
-              vo.y = pack_bf16x2(__uint_as_float(oo[c][e + 2]) * inv_o, __uint_as_float(oo[c][e + 3]) * inv_o);
-              vo.z = pack_bf16x2(__uint_as_float(oo[c][e + 4]) * inv_o, __uint_as_float(oo[c][e + 5]) * inv_o);
-              vo.w = pack_bf16x2(__uint_as_float(oo[c][e + 6]) * inv_o, __uint_as_float(oo[c][e + 7]) * inv_o);
-              *reinterpret_cast<uint4*>(he + c * 32 + e) = ve;
-              *reinterpret_cast<uint4*>(ho + c * 32 + e) = vo;
+              for (int e = 0; e < 32; e += 8) {
+                uint4 ve, vo;
+                ve.x = pack_bf16x2(__uint_as_float(oe[c][e]) * ie, __uint_as_float(oe[c][e + 1]) * ie);
+                ve.y = pack_bf16x2(__uint_as_float(oe[c][e + 2]) * ie, __uint_as_float(oe[c][e + 3]) * ie);
+                ve.z = pack_bf16x2(__uint_as_float(oe[c][e + 4]) * ie, __uint_as_float(oe[c][e + 5]) * ie);
+                ve.w = pack_bf16x2(__uint_as_float(oe[c][e + 6]) * ie, __uint_as_float(oe[c][e + 7]) * ie);
+                vo.x = pack_bf16x2(__uint_as_float(oo[c][e]) * inv_o, __uint_as_float(oo[c][e + 1]) * inv_o);
+                vo.y = pack_bf16x2(__uint_as_float(oo[c][e + 2]) * inv_o, __uint_as_float(oo[c][e + 3]) * inv_o);
+                vo.z = pack_bf16x2(__uint_as_float(oo[c][e + 4]) * inv_o, __uint_as_float(oo[c][e + 5]) * inv_o);
+                vo.w = pack_bf16x2(__uint_as_float(oo[c][e + 6]) * inv_o, __uint_as_float(oo[c][e + 7]) * inv_o);
+                *reinterpret_cast<uint4*>(he + c * 32 + e) = ve;
+                *reinterpret_cast<uint4*>(ho + c * 32 + e) = vo;
+              }
             }
           }
+          if (a.lse) {
+            // natural-log LSE of head 2p + wg: (m + log2 l) * ln 2
+            a.lse[(static_cast<int64_t>(w.b) * 2 * a.h + 2 * w.p + wg) * a.N + n] =
+                (m_run[wg] + __log2f(wg == 0 ? le : lo)) * 0.69314718055994531f;
+          }
         }
-        if (a.lse) {
-          // natural-log LSE of head 2p + wg: (m + log2 l) * ln 2
-          a.lse[(static_cast<int64_t>(w.b) * 2 * a.h + 2 * w.p + wg) * a.N + n] =
-              (m_run + __log2f(l_run)) * 0.69314718055994531f;
-        }
+
+        tc_fence_before();
+        eok = epi_sync(0x2205);
       }
-      tc_fence_before();
-      if (!epi_sync(0x2205)) { ok = false; break; }
+      if (!eok) ok = false;
+      if (named_red_or_256(!ok || *sh.abort_flag())) break;
     }
   }
 
