@@ -7,9 +7,10 @@
 // the group from the same shared-memory tile (the even/odd pair of a
 // difference always sits in one group).
 //
-// Stage 1 (split-KV): grid (splits, h_kv, B), 4 warps.  K/V tiles of 64 keys
-// are staged through a 3-deep cp.async ring (16-byte chunks, XOR-swizzled
-// rows); each warp owns 16 keys of a tile and runs the scores and P.V on the
+// Stage 1 (split-KV): grid (splits, h_kv, B), 8 warps, one CTA per SM.  K/V
+// tiles of 128 keys are staged through a 3-deep cp.async ring (16-byte
+// chunks, XOR-swizzled rows; up to 128 KB in flight per SM, which the HBM
+// latency needs); each warp owns 16 keys of a tile and runs the scores and P.V on the
 // warp MMA with the group's query heads as the M rows (16 rows, the unused
 // ones zero).  Per split it writes an unnormalised partial O plus the running
 // max (log2 units) and sum.
@@ -21,9 +22,9 @@
 namespace da {
 namespace {
 
-constexpr int kTileKeys = 64;    // keys per pipeline stage
+constexpr int kTileKeys = 128;   // keys per pipeline stage (16 per warp)
 constexpr int kStages = 3;
-constexpr int kWarps = 4;
+constexpr int kWarps = 8;
 // Per head dim D (64 or 128): key rows of D * 2 bytes (D / 8 16-byte chunks),
 // K + V tiles of 64 keys per stage.
 template <int D>
@@ -33,7 +34,7 @@ struct Cfg {
   static constexpr int kTileBytes = kTileKeys * kRowBytes;
   static constexpr int kStageBytes = 2 * kTileBytes;  // K + V
 };
-constexpr int kSmemBytes = kStages * Cfg<128>::kStageBytes;  // 96 KB (the D = 128 ring)
+constexpr int kSmemBytes = kStages * Cfg<128>::kStageBytes;  // 192 KB (the D = 128 ring)
 
 // Byte offset of 16-byte chunk c of key row r inside a tile (rows of D / 8
 // chunks; the low 3 chunk bits are XORed with the row so that 8 consecutive
@@ -44,7 +45,7 @@ __device__ __forceinline__ uint32_t tile_off(int r, int c) {
 }
 
 template <int D>
-__global__ void __launch_bounds__(kWarps * 32, 2)
+__global__ void __launch_bounds__(kWarps * 32, 1)
 decode_split_kernel(DecodeArgs a) {
   constexpr int kD = D;
   constexpr int kChunks = Cfg<D>::kChunks;
