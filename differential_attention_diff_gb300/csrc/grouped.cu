@@ -16,48 +16,51 @@
 namespace da {
 namespace {
 
-// One thread per 8 features of one (b, n, output head).
+// One CTA per token (b, n): its threads walk the token's h * d / 8 groups of
+// 8 features (output head p, features c8 .. c8 + 7), so the token's per-head
+// row block is read with coalesced 16-byte loads (each noise row serves its
+// `ratio` signal rows from L1) and the index arithmetic is per token.
 __global__ void __launch_bounds__(256)
 grouped_combine_kernel(GroupedArgs a) {
   const int nc = a.d / 8;
-  const long long total = static_cast<long long>(a.B) * a.N * a.h * nc;
-  for (long long idx = static_cast<long long>(blockIdx.x) * blockDim.x + threadIdx.x; idx < total;
-       idx += static_cast<long long>(gridDim.x) * blockDim.x) {
-    const int c8 = static_cast<int>(idx % nc) * 8;
-    const long long row = idx / nc;  // (b, n, p)
-    const int p = static_cast<int>(row % a.h);
-    const long long bn = row / a.h;
-    const int n = static_cast<int>(bn % a.N), b = static_cast<int>(bn / a.N);
-    const int g = p / a.ratio, i = p % a.ratio;
+  const int work = a.h * nc;
+  for (long long tok = blockIdx.x; tok < static_cast<long long>(a.B) * a.N; tok += gridDim.x) {
+    const int n = static_cast<int>(tok % a.N), b = static_cast<int>(tok / a.N);
     const __nv_bfloat16* base = static_cast<const __nv_bfloat16*>(a.o_heads.ptr) + b * a.o_heads.sb +
-                                static_cast<int64_t>(n) * a.o_heads.sn + c8;
-    const uint4 sv = *reinterpret_cast<const uint4*>(base + static_cast<int64_t>(g * (a.ratio + 1) + i) * a.o_heads.sh);
-    const uint4 nv =
-        *reinterpret_cast<const uint4*>(base + static_cast<int64_t>(g * (a.ratio + 1) + a.ratio) * a.o_heads.sh);
-    const float gt = a.gate[row];
-    const __nv_bfloat162* s2 = reinterpret_cast<const __nv_bfloat162*>(&sv);
-    const __nv_bfloat162* n2 = reinterpret_cast<const __nv_bfloat162*>(&nv);
-    uint32_t r[4];
+                                static_cast<int64_t>(n) * a.o_heads.sn;
+    const float* gt_row = a.gate + tok * a.h;
+    __nv_bfloat16* dst_row = static_cast<__nv_bfloat16*>(a.out.ptr) + b * a.out.sb +
+                             static_cast<int64_t>(n) * a.out.sn;
+    for (int idx = threadIdx.x; idx < work; idx += blockDim.x) {
+      const int p = idx / nc, c8 = (idx - p * nc) * 8;
+      const int g = p / a.ratio, i = p - g * a.ratio;
+      const uint4 sv =
+          *reinterpret_cast<const uint4*>(base + static_cast<int64_t>(g * (a.ratio + 1) + i) * a.o_heads.sh + c8);
+      const uint4 nv = *reinterpret_cast<const uint4*>(
+          base + static_cast<int64_t>(g * (a.ratio + 1) + a.ratio) * a.o_heads.sh + c8);
+      const float gt = gt_row[p];
+      const __nv_bfloat162* s2 = reinterpret_cast<const __nv_bfloat162*>(&sv);
+      const __nv_bfloat162* n2 = reinterpret_cast<const __nv_bfloat162*>(&nv);
+      uint32_t r[4];
 #pragma unroll
-    for (int e = 0; e < 4; ++e) {
-      // both terms rounded on their own: equal signal and noise rows with
-      // gate 1 give exactly zero
-      const float lo = __fsub_rn(__low2float(s2[e]), __fmul_rn(gt, __low2float(n2[e])));
-      const float hi = __fsub_rn(__high2float(s2[e]), __fmul_rn(gt, __high2float(n2[e])));
-      r[e] = pack_bf16x2(lo, hi);
+      for (int e = 0; e < 4; ++e) {
+        // both terms rounded on their own: equal signal and noise rows with
+        // gate 1 give exactly zero
+        const float lo = __fsub_rn(__low2float(s2[e]), __fmul_rn(gt, __low2float(n2[e])));
+        const float hi = __fsub_rn(__high2float(s2[e]), __fmul_rn(gt, __high2float(n2[e])));
+        r[e] = pack_bf16x2(lo, hi);
+      }
+      *reinterpret_cast<uint4*>(dst_row + static_cast<int64_t>(p) * a.out.sh + c8) = make_uint4(r[0], r[1], r[2], r[3]);
     }
-    __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.out.ptr) + b * a.out.sb + static_cast<int64_t>(n) * a.out.sn +
-                         p * a.out.sh + c8;
-    *reinterpret_cast<uint4*>(dst) = make_uint4(r[0], r[1], r[2], r[3]);
   }
 }
 
 }  // namespace
 
 cudaError_t launch_grouped_combine(const GroupedArgs& a, cudaStream_t s) {
-  const long long total = static_cast<long long>(a.B) * a.N * a.h * (a.d / 8);
-  long long grid = (total + 255) / 256;
-  if (grid > 16 * 152) grid = 16 * 152;
+  const long long tokens = static_cast<long long>(a.B) * a.N;
+  long long grid = tokens;
+  if (grid > 64 * 152) grid = 64 * 152;
   if (grid < 1) grid = 1;
   grouped_combine_kernel<<<static_cast<unsigned>(grid), 256, 0, s>>>(a);
   return cudaGetLastError();
