@@ -49,7 +49,8 @@ def _check(t, ratio, out, rows=None, batches=None, groups=None, causal=True):
 
 
 @pytest.mark.parametrize("B,N,h,ratio,hkv", [(1, 200, 6, 3, 2), (1, 300, 8, 4, 1), (2, 64, 6, 3, 1),
-                                              (1, 1, 3, 3, 1), (1, 500, 12, 3, 2), (2, 129, 16, 4, 2)])
+                                              (1, 1, 3, 3, 1), (1, 500, 12, 3, 2), (2, 129, 16, 4, 2),
+                                              (2, 7, 6, 3, 2)])
 def test_grouped_parity_small(B, N, h, ratio, hkv):
     t = synth.grouped_inputs(B, N, h, ratio, hkv, 128, 128, seed=8000 + N + h, device="cuda")
     out = bd.diffattn_grouped_fwd(t["q"], t["k"], t["v"], ratio, x=t["x"], w_lambda=t["w_lambda"])

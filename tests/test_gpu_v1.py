@@ -58,7 +58,8 @@ def _check(t, li, y, sv, rows=None, heads=None, batches=None, causal=True, w=Non
 
 
 @pytest.mark.parametrize("B,N,H,layer", [(1, 200, 2, 1), (2, 384, 3, 2), (1, 129, 2, 14),
-                                          (1, 1, 1, 28), (1, 1000, 4, 5), (3, 256, 1, 1)])
+                                          (1, 1, 1, 28), (1, 1000, 4, 5), (3, 256, 1, 1),
+                                          (2, 7, 2, 3), (1, 64, 3, 2)])
 def test_v1_fwd_parity_small(B, N, H, layer):
     t = synth.v1_inputs(B, N, H, 128, 256, "bf16", seed=4000 + N + H, device="cuda")
     li = bd.diffattn_lambda_init(layer)

@@ -142,7 +142,7 @@ def _model(t, li, heads=None, causal=True, w=None):
 
 
 @pytest.mark.parametrize("B,N,H,layer", [(1, 200, 2, 1), (2, 384, 1, 3), (1, 129, 2, 14),
-                                          (1, 1, 1, 1), (1, 700, 3, 28)])
+                                          (1, 1, 1, 1), (1, 700, 3, 28), (2, 7, 2, 2), (1, 64, 2, 5)])
 def test_v1_bwd_parity_small(B, N, H, layer):
     t = synth.v1_inputs(B, N, H, 128, 256, "bf16", seed=5000 + N + H, device="cuda", with_dy=True)
     li = float(np.float32(bd.diffattn_lambda_init(layer)))

@@ -53,7 +53,7 @@ def _check_pairs(t, out, gate, pairs=None, rows=None, lse=None, causal=True):
 
 
 @pytest.mark.parametrize("B,N,h,hkv", [(1, 200, 4, 2), (2, 384, 2, 1), (1, 129, 4, 4), (1, 1, 2, 1),
-                                        (2, 1000, 8, 2), (1, 640, 16, 2)])
+                                        (2, 1000, 8, 2), (1, 640, 16, 2), (2, 7, 2, 1), (1, 64, 4, 2)])
 def test_v2_fwd_parity_small(B, N, h, hkv):
     t = synth.v2_inputs(B, N, h, hkv, 128, 128, seed=3000 + N + h, device="cuda")
     lse = torch.empty((B, 2 * h, N), dtype=torch.float32, device="cuda")

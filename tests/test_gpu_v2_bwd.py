@@ -92,7 +92,7 @@ def _compare(g, ref, model, names=ATTN + GATE, bar="bwd", sl=None):
 
 
 @pytest.mark.parametrize("B,N,h,hkv", [(1, 200, 2, 1), (2, 129, 2, 2), (1, 1, 1, 1), (1, 300, 4, 1),
-                                        (1, 700, 4, 2), (2, 64, 8, 2)])
+                                        (1, 700, 4, 2), (2, 64, 8, 2), (2, 7, 2, 1)])
 def test_v2_bwd_parity_small(B, N, h, hkv):
     """Query-head groups of 2, 4 and 8, one token, ragged tails across several
     128-key tiles, two batches."""
