@@ -213,6 +213,31 @@ def test_v1_bwd_parity_rms_weight(B, N, H, dqk, layer):
     _compare(_run(t, li, w=w), ref, model, bar="step")
 
 
+def test_v1_bwd_strided_packed_views():
+    """q1/q2 and k1/k2 as views into packed [B, N, H, 2, d_qk] buffers, and the
+    gradients written into views of packed buffers of the same layout: the
+    backward equals the one on contiguous copies bit for bit."""
+    B, N, H = 1, 260, 2
+    t = synth.v1_inputs(B, N, H, 128, 256, "bf16", seed=5400, device="cuda", with_dy=True)
+    qp = torch.stack([t["q1"], t["q2"]], dim=3).contiguous()
+    kp = torch.stack([t["k1"], t["k2"]], dim=3).contiguous()
+    tv = dict(t, q1=qp[:, :, :, 0], q2=qp[:, :, :, 1], k1=kp[:, :, :, 0], k2=kp[:, :, :, 1])
+    li = float(np.float32(bd.diffattn_lambda_init(2)))
+    y, sv = bd.diffattn_v1_fwd(*(t[n] for n in NAMES), li, save=True)
+    ref = bd.diffattn_v1_bwd(*(t[n] for n in NAMES), li, y, t["dy"], sv)
+    dqp = torch.empty_like(qp)
+    dkp = torch.empty_like(kp)
+    grads = dict(dq1=dqp[:, :, :, 0], dq2=dqp[:, :, :, 1], dk1=dkp[:, :, :, 0], dk2=dkp[:, :, :, 1],
+                 dv=torch.empty_like(t["v"]), dlq1=torch.empty_like(t["lq1"]), dlk1=torch.empty_like(t["lk1"]),
+                 dlq2=torch.empty_like(t["lq2"]), dlk2=torch.empty_like(t["lk2"]))
+    got = bd.diffattn_v1_bwd(*(tv[n] for n in NAMES), li, y, t["dy"], sv, grads=grads)
+    torch.cuda.synchronize()
+    for n in ("dk1", "dk2", "dv", "dlq1", "dlk1", "dlq2", "dlk2"):
+        assert torch.equal(got[n], ref[n]), n
+    for n in ("dq1", "dq2"):  # fp32 reduce-adds: order may differ run to run
+        assert torch.allclose(got[n].float(), ref[n].float(), rtol=1e-2, atol=1e-3 * float(ref[n].float().abs().max()))
+
+
 def test_v1_bwd_deterministic_parts_repeat():
     """dK and dV come from one CTA each (no atomics): bitwise equal on a rerun."""
     t = synth.v1_inputs(1, 300, 2, 128, 256, "bf16", seed=61, device="cuda", with_dy=True)

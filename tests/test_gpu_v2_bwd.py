@@ -123,6 +123,23 @@ def test_v2_bwd_parity_not_causal(B, N, h, hkv, d):
     _compare(_run(t, causal=False), ref, model, bar="step")
 
 
+def test_v2_bwd_strided_views():
+    """q, k, v as views into one packed [B, N, 2h + 2 h_kv, d] buffer: the
+    backward equals the one on contiguous copies (dK, dV bit for bit)."""
+    B, N, h, hkv = 1, 300, 4, 2
+    t = synth.v2_inputs(B, N, h, hkv, 128, 128, seed=7400, device="cuda", with_dout=True)
+    buf = torch.cat([t["q"], t["k"], t["v"]], dim=2).contiguous()
+    tv = dict(t, q=buf[:, :, :2 * h], k=buf[:, :, 2 * h:2 * h + hkv], v=buf[:, :, 2 * h + hkv:])
+    _, sv = bd.diffattn_v2_fwd(t["q"], t["k"], t["v"], x=t["x"], w_lambda=t["w_lambda"], save=True)
+    ref = bd.diffattn_v2_bwd(t["q"], t["k"], t["v"], t["dout"], sv, x=t["x"], w_lambda=t["w_lambda"])
+    got = bd.diffattn_v2_bwd(tv["q"], tv["k"], tv["v"], t["dout"], sv, x=t["x"], w_lambda=t["w_lambda"])
+    torch.cuda.synchronize()
+    for n in ("dk", "dv"):
+        assert torch.equal(got[n], ref[n]), n
+    assert torch.allclose(got["dq"].float(), ref["dq"].float(), rtol=1e-2,
+                          atol=1e-3 * float(ref["dq"].float().abs().max()))
+
+
 def test_v2_bwd_gate_given_matches_gate_from_x():
     """A caller-supplied gate (the same values) gives the same dQ, dK, dV as
     the gate computed from x and W inside the call."""
