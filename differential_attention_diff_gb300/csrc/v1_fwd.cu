@@ -14,22 +14,28 @@
 // columns for its O accumulator (d_v = 256): the whole 512-column TMEM of an
 // SM.  So a work item (batch, head, 128 query rows) runs on a cluster of two
 // CTAs: rank 0 computes stream 1, rank 1 stream 2, each from its own TMA
-// loads (V is read by both; the second read mostly hits L2).  In the
-// epilogue each CTA keeps half of the 256 output columns: it stages the other
-// half of its O/l in an idle V stage and one bulk copy moves it into the
-// partner's shared memory (distributed shared memory, into the partner's K
-// ring, which is idle then: each CTA's producer loads the next item's K tiles
-// only after its own epilogue has read the ring), forms
-// O = O1/l1 - lambda O2/l2 on its half, swaps the per-row partial sums of
-// squares the same way, and writes Y = (1 - lambda_init) O / sqrt(mean O^2 +
-// eps).  Every hand-off is an mbarrier with a bounded wait (remote arrives at
-// cluster scope).
+// loads (V is read by both; the second read mostly hits L2).
+//
+// The epilogue runs in warps of its own, under the next item's main loop.
+// Shared memory is full with the Q tile and the K and V rings, so the
+// epilogue keeps nothing there: each CTA keeps half of the 256 output
+// columns; it writes the other half of its O/l to its exchange slot in the
+// workspace (64 KB, which stays in L2) and tells the partner with a release
+// arrive at cluster scope; it reads the partner's slot for its own half,
+// forms O = O1/l1 - lambda O2/l2, swaps the per-row partial sums of squares
+// through distributed shared memory (asynchronous 4-byte stores counted on
+// an mbarrier), and writes Y = (1 - lambda_init) O / sqrt(mean O^2 + eps)
+// straight from registers.  The O accumulator is released to the next
+// item's first P.V as soon as the epilogue has read it out of TMEM.  Every
+// hand-off is an mbarrier with a bounded wait.
 //
 //   TMEM: [0,128) S / P buffer 0, [128,256) S / P buffer 1, [256,256+DV) O.
 //   SMEM: Q (32 KB), K ring 2 x 32 KB, V ring 2 x 64 KB (128-byte swizzle),
 //   for head dims (128, 256); half of each for (64, 128).
-//   warps 0-3: softmax (softmax.cuh) + epilogue (thread = query row = TMEM lane);
-//   warp 4: TMA producer; warp 5: MMA issuer (one lane).
+//   warps 0-3: softmax (softmax.cuh; thread = query row = TMEM lane);
+//   warps 4-7: epilogue (thread = query row); warp 8: TMA producer;
+//   warp 9: MMA issuer (one lane); warps 10-11 idle (they complete the third
+//   warpgroup, whose registers go to the first two).
 #include "kernels.h"
 #include "softmax.cuh"
 #include "tma.cuh"
@@ -38,18 +44,26 @@ namespace da {
 namespace {
 
 constexpr int kBM = 128, kBN = 128;
-constexpr int kThreads = 192;
+constexpr int kThreads = 384;
+// registers per thread after the split: the softmax and epilogue warpgroups
+// take what the producer warpgroup gives up (launch: 384 x 168; after:
+// 128 x 56 + 256 x 224, the same total)
+constexpr int kRegsLow = 56, kRegsHigh = 224;
 constexpr int kBox = 128 * 128;  // one 64-column box of 128 rows (bf16)
 // Tiles for head dims (DQK, DV = 2 DQK) = (128, 256) or (64, 128), in boxes:
 //   Q at 0 (DQK/64), K ring [stage][DQK/64] after it, V ring [stage][DV/64]
 //   after that.  The barrier block sits after the largest layout.
 constexpr int kOffBar = 14 * kBox;            // 229376
 constexpr int kSmemBytes = kOffBar + 2048 + 1024;  // 232448: the per-block limit
+// workspace: the work counter, then one exchange slot per CTA of
+// 128 rows x 128 fp32 (the half of O/l its partner finishes)
+constexpr size_t kXchgOff = 256;
+constexpr size_t kXchgBytes = 128 * 128 * 4;
 
 enum {
   B_QFULL = 0, B_QEMPTY, B_KFULL, B_KFULL1, B_KEMPTY, B_KEMPTY1, B_VFULL, B_VFULL1,
-  B_VEMPTY, B_VEMPTY1, B_SFULL, B_SFULL1, B_PFULL, B_PFULL1, B_ORDY, B_ODONE, B_DATA, B_SSQ, B_SSQ1,
-  B_RXRDY, B_RXFREE, B_STG, B_STGFREE, B_GIVE, B_SCHF, B_SCHE = B_SCHF + 4, B_COUNT = B_SCHE + 4
+  B_VEMPTY, B_VEMPTY1, B_SFULL, B_SFULL1, B_PFULL, B_PFULL1, B_ORDY, B_ODONE, B_EPI, B_OFREE, B_XRDY,
+  B_SSQ, B_SSQ1, B_SCHF, B_SCHE = B_SCHF + 4, B_COUNT = B_SCHE + 4
 };
 static_assert(B_COUNT * 8 <= 256, "barriers end where the TMEM slot begins");
 
@@ -67,6 +81,9 @@ struct Shared {
   // ring of the next work items (4 slots), written by rank 0's producer
   __device__ volatile int* ring() const { return reinterpret_cast<volatile int*>(gen + kOffBar + 272); }
   __device__ uint32_t ring_s(int slot) const { return base + kOffBar + 272 + 4 * slot; }
+  // softmax -> epilogue hand-off of one item: its index and each row's sum l
+  __device__ volatile int* epi_item() const { return reinterpret_cast<volatile int*>(gen + kOffBar + 288); }
+  __device__ volatile float* epi_l() const { return reinterpret_cast<volatile float*>(gen + kOffBar + 1536); }
   // the partner's per-row partial sums of squares, by item parity: float[2][128]
   __device__ uint32_t ssq_rx(int p) const { return base + kOffBar + 512 + 512 * p; }
   __device__ float* ssq_rx_ptr(int p) const { return reinterpret_cast<float*>(gen + kOffBar + 512 + 512 * p); }
@@ -117,15 +134,12 @@ __device__ __forceinline__ void remote_arrive(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
                : "memory");
 }
-// shared::cta -> a cluster peer's shared memory, completion counted in bytes
-// on the peer's mbarrier
-__device__ __forceinline__ void bulk_copy_to_peer(uint32_t dst_cluster, uint32_t src, uint32_t bytes,
-                                                  uint32_t bar_cluster) {
-  asm volatile(
-      "cp.async.bulk.shared::cluster.shared::cta.mbarrier::complete_tx::bytes [%0], [%1], %2, [%3];" ::"r"(
-          dst_cluster),
-      "r"(src), "r"(bytes), "r"(bar_cluster)
-      : "memory");
+// a value of another SM's exchange slot, read at L2 (never a stale L1 line
+// of an earlier item)
+__device__ __forceinline__ float ld_cg_f32(const float* p) {
+  float v;
+  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+  return v;
 }
 __device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v) {
   asm volatile("st.shared::cluster.s32 [%0], %1;" ::"r"(addr), "r"(v) : "memory");
@@ -136,6 +150,14 @@ __device__ __forceinline__ void st_async_f32(uint32_t dst_cluster, float v, uint
   asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.b32 [%0], %1, [%2];" ::"r"(dst_cluster),
                "r"(__float_as_uint(v)), "r"(bar_cluster)
                : "memory");
+}
+template <int kRegs>
+__device__ __forceinline__ void regs_inc() {
+  asm volatile("setmaxnreg.inc.sync.aligned.u32 %0;" ::"n"(kRegs));
+}
+template <int kRegs>
+__device__ __forceinline__ void regs_dec() {
+  asm volatile("setmaxnreg.dec.sync.aligned.u32 %0;" ::"n"(kRegs));
 }
 __device__ __forceinline__ uint32_t cluster_rank() {
   uint32_t r;
@@ -169,8 +191,7 @@ template <int DQK, int DV>
 __global__ void __launch_bounds__(kThreads, 1)
 v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__ CUtensorMap tm_q2,
               const __grid_constant__ CUtensorMap tm_k1, const __grid_constant__ CUtensorMap tm_k2,
-              const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_out,
-              const __grid_constant__ CUtensorMap tm_o2, V1FwdArgs a) {
+              const __grid_constant__ CUtensorMap tm_v, V1FwdArgs a) {
   extern __shared__ uint8_t smem_raw[];
   Shared sh;
   {
@@ -183,7 +204,6 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
   constexpr int kNQ = DQK / 64, kNV = DV / 64;  // 64-column boxes per tile row
   constexpr int kOffQ = 0, kOffK = kNQ * kBox, kOffV = 3 * kNQ * kBox;
   constexpr int kHalf = DV / 2;                 // output columns each CTA finishes
-  constexpr int kRowX = kHalf * 4;              // bytes per row of exchanged fp32 O/l
   constexpr uint32_t kIdescPV = idesc_bf16(128, DV, 1);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();         // 0: stream 1, 1: stream 2
@@ -211,14 +231,11 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
     }
     mbar_init(sh.bar(B_ORDY), 1);
     mbar_init(sh.bar(B_ODONE), 1);
-    mbar_init(sh.bar(B_DATA), 1);  // + 64 KB of bulk-copy bytes from the partner
-    mbar_init(sh.bar(B_SSQ), 1);   // + 512 bytes of the partner's partial sums
+    mbar_init(sh.bar(B_EPI), 128);    // softmax rows: item handed to the epilogue
+    mbar_init(sh.bar(B_OFREE), 128);  // epilogue rows: O read out of TMEM
+    mbar_init(sh.bar(B_XRDY), 128);   // the partner's epilogue rows: its slot is written
+    mbar_init(sh.bar(B_SSQ), 1);      // + 512 bytes of the partner's partial sums
     mbar_init(sh.bar(B_SSQ1), 1);
-    mbar_init(sh.bar(B_RXRDY), 1);
-    mbar_init(sh.bar(B_GIVE), 128);
-    mbar_init(sh.bar(B_RXFREE), 128);
-    mbar_init(sh.bar(B_STGFREE), 1);
-    mbar_init(sh.bar(B_STG), 128);
     for (int q = 0; q < 4; ++q) {
       mbar_init(sh.bar(B_SCHF + q), 1);
       mbar_init(sh.bar(B_SCHE + q), 11);  // rank 0: MMA + 4 softmax warps; rank 1: + its producer
@@ -244,11 +261,11 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
       if (a.lambda_out && blockIdx.x == 0) *a.lambda_out = lam;
     }
   }
-  if (warp == 5) {
+  if (warp == 9) {
     tmem_alloc(smem_u32(sh.tmem_slot()), 512);
     tmem_relinquish();
   }
-  if (warp == 4 && lane == 0) {
+  if (warp == 8 && lane == 0) {
     prefetch_tmap(tq);
     prefetch_tmap(tk);
     prefetch_tmap(&tm_v);
@@ -262,8 +279,9 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
   // ---- dynamic work distribution ------------------------------------------
   // Rank 0's producer takes item indices from a global counter (zeroed by the
   // host before the launch; heaviest items come first in index order) and
-  // publishes them to a 4-slot ring in both CTAs; every role of both CTAs
-  // reads the same sequence.  Index >= n_items ends the sequence.
+  // publishes them to a 4-slot ring in both CTAs; the producer, MMA and
+  // softmax roles of both CTAs read the same sequence (the epilogue warps get
+  // each item from the softmax warps).  Index >= n_items ends the sequence.
   int* counter = static_cast<int*>(a.workspace);
   auto publish = [&](int k) -> int {  // rank 0 producer only
     const int slot = k & 3;
@@ -290,164 +308,138 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
     return idx;
   };
 
-  if (warp == 4) {
-    // ------------------------------------------------------ TMA producer --
-    if (lane == 0) {
-      int kv = 0;
-      bool ok = true;
-      // epilogues whose Y / O2 staging still occupies a V stage: the last tile
-      // of item `seq` used stage tile & 1; a V load into that stage for a
-      // later tile waits until the item's TMA stores have read the staging
-      int pend_tile[4], pend_seq[4], npend = 0;
-      for (int it = 0; ok; ++it) {
-        if (it > 0 && npend < 4) {
-          pend_tile[npend] = kv - 1;
-          pend_seq[npend] = it - 1;
-          ++npend;
-        }
-        const int i = rank == 0 ? publish(it) : consume(it, true);
-        if (i < 0) { ok = false; break; }
-        if (i >= n_items) break;
-        const Item w = item_of(i, units, a.H, n_mtiles, ub, causal);
-        if (it > 0 && !wait_bar(sh, sh.bar(B_QEMPTY), (it - 1) & 1, a.status, 0x3001)) { ok = false; break; }
-        mbar_arrive_expect_tx(sh.bar(B_QFULL), kNQ * kBox);
-        for (int box = 0; box < kNQ; ++box)
-          tma_load_4d(sh.base + kOffQ + box * kBox, tq, sh.bar(B_QFULL), box * 64, w.h, w.mt * kBM, w.b);
-        for (int j = 0; j < w.n_kv; ++j, ++kv) {
-          const int st = kv & 1, use = kv >> 1;
-          auto load_k = [&]() -> bool {
-            if (use > 0 && !wait_bar(sh, sh.bar(B_KEMPTY + st), (use - 1) & 1, a.status, 0x3002)) return false;
+  if (warp >= 8) {
+    regs_dec<kRegsLow>();
+    if (warp == 8) {
+      // ------------------------------------------------------ TMA producer --
+      if (lane == 0) {
+        int kv = 0;
+        bool ok = true;
+        for (int it = 0; ok; ++it) {
+          const int i = rank == 0 ? publish(it) : consume(it, true);
+          if (i < 0) { ok = false; break; }
+          if (i >= n_items) break;
+          const Item w = item_of(i, units, a.H, n_mtiles, ub, causal);
+          if (it > 0 && !wait_bar(sh, sh.bar(B_QEMPTY), (it - 1) & 1, a.status, 0x3001)) { ok = false; break; }
+          mbar_arrive_expect_tx(sh.bar(B_QFULL), kNQ * kBox);
+          for (int box = 0; box < kNQ; ++box)
+            tma_load_4d(sh.base + kOffQ + box * kBox, tq, sh.bar(B_QFULL), box * 64, w.h, w.mt * kBM, w.b);
+          for (int j = 0; j < w.n_kv; ++j, ++kv) {
+            const int st = kv & 1, use = kv >> 1;
+            if (use > 0 && !wait_bar(sh, sh.bar(B_KEMPTY + st), (use - 1) & 1, a.status, 0x3002)) { ok = false; break; }
             mbar_arrive_expect_tx(sh.bar(B_KFULL + st), kNQ * kBox);
             for (int box = 0; box < kNQ; ++box)
-              tma_load_4d(sh.base + kOffK + (st * kNQ + box) * kBox, tk, sh.bar(B_KFULL + st), box * 64,
-                          w.h, j * kBN, w.b);
-            return true;
-          };
-          auto load_v = [&]() -> bool {
-            // release staging entries in order: the head when this load
-            // reuses its stage, or once the load is two tiles past it
-            while (npend > 0 && kv > pend_tile[0] + ((pend_tile[0] & 1) == st ? 0 : 1)) {
-              if (!wait_bar(sh, sh.bar(B_STGFREE), pend_seq[0] & 1, a.status, 0x3005)) return false;
-              for (int q = 1; q < npend; ++q) {
-                pend_tile[q - 1] = pend_tile[q];
-                pend_seq[q - 1] = pend_seq[q];
-              }
-              --npend;
-            }
-            if (use > 0 && !wait_bar(sh, sh.bar(B_VEMPTY + st), (use - 1) & 1, a.status, 0x3003)) return false;
+              tma_load_4d(sh.base + kOffK + (st * kNQ + box) * kBox, tk, sh.bar(B_KFULL + st), box * 64, w.h,
+                          j * kBN, w.b);
+            if (use > 0 && !wait_bar(sh, sh.bar(B_VEMPTY + st), (use - 1) & 1, a.status, 0x3003)) { ok = false; break; }
             mbar_arrive_expect_tx(sh.bar(B_VFULL + st), kNV * kBox);
             for (int box = 0; box < kNV; ++box)
-              tma_load_4d(sh.base + kOffV + (st * kNV + box) * kBox, &tm_v, sh.bar(B_VFULL + st),
-                          box * 64, w.h, j * kBN, w.b);
-            return true;
-          };
-          if (j == 0) {
-            // the K ring receives the partner's half of O during the previous
-            // item's epilogue: load K once every row has read it
-            if (!load_v()) { ok = false; break; }
-            if (it > 0 && !wait_bar(sh, sh.bar(B_RXFREE), (it - 1) & 1, a.status, 0x3004)) { ok = false; break; }
-            if (!load_k()) { ok = false; break; }
-          } else {
-            if (!load_k() || !load_v()) { ok = false; break; }
+              tma_load_4d(sh.base + kOffV + (st * kNV + box) * kBox, &tm_v, sh.bar(B_VFULL + st), box * 64, w.h,
+                          j * kBN, w.b);
+          }
+        }
+        if (!ok) {
+          // bounded drain of the loads that may still be in flight
+          const uint64_t t0 = globaltimer();
+          while (globaltimer() - t0 < 200000000ull) {
           }
         }
       }
-      if (!ok) {
-        // bounded drain of the loads that may still be in flight
-        const uint64_t t0 = globaltimer();
-        while (globaltimer() - t0 < 200000000ull) {
-        }
-      }
-    }
-  } else if (warp == 5) {
-    // ------------------------------------------------------- MMA issuer ---
-    if (lane == 0) {
-      int kv = 0, it = 0;
-      bool ok = true;
-      const uint32_t t_o = tmem + 256;
-      auto issue_s = [&](int g) {  // S of global tile g into buffer g & 1
-        const int st = g & 1;
-        const uint32_t kb = sh.base + kOffK + st * kNQ * kBox;
-        const uint32_t qa = sh.base + kOffQ;
-#pragma unroll
-        for (int kk = 0; kk < kDqk / 16; ++kk) {
-          const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-          tc_mma_ss(tmem + (g & 1) * 128, sdesc_sw128(qa + off, 16, 1024),
-                    sdesc_sw128(kb + off, 16, 1024), kIdescS, kk > 0);
-        }
-      };
-      auto wait_k = [&](int g) {
-        return wait_bar(sh, sh.bar(B_KFULL + (g & 1)), (g >> 1) & 1, a.status, 0x3102);
-      };
-      for (;; ++it) {
-        const int i = consume(it, true);
-        if (i < 0) { ok = false; break; }
-        if (i >= n_items) break;
-        const Item w = item_of(i, units, a.H, n_mtiles, ub, causal);
-        const int n = w.n_kv;
-        if (!wait_bar(sh, sh.bar(B_QFULL), it & 1, a.status, 0x3101)) { ok = false; break; }
-        tc_fence_after();
-        for (int j = 0; j < 2 && j < n; ++j) {
-          if (!wait_k(kv + j)) { ok = false; break; }
+    } else if (warp == 9) {
+      // ------------------------------------------------------- MMA issuer ---
+      if (lane == 0) {
+        int kv = 0, it = 0;
+        bool ok = true;
+        const uint32_t t_o = tmem + 256;
+        auto issue_s = [&](int g) {  // S of global tile g into buffer g & 1
+          const int st = g & 1;
+          const uint32_t kb = sh.base + kOffK + st * kNQ * kBox;
+          const uint32_t qa = sh.base + kOffQ;
+  #pragma unroll
+          for (int kk = 0; kk < kDqk / 16; ++kk) {
+            const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
+            tc_mma_ss(tmem + (g & 1) * 128, sdesc_sw128(qa + off, 16, 1024),
+                      sdesc_sw128(kb + off, 16, 1024), kIdescS, kk > 0);
+          }
+        };
+        auto wait_k = [&](int g) {
+          return wait_bar(sh, sh.bar(B_KFULL + (g & 1)), (g >> 1) & 1, a.status, 0x3102);
+        };
+        for (;; ++it) {
+          const int i = consume(it, true);
+          if (i < 0) { ok = false; break; }
+          if (i >= n_items) break;
+          const Item w = item_of(i, units, a.H, n_mtiles, ub, causal);
+          const int n = w.n_kv;
+          if (!wait_bar(sh, sh.bar(B_QFULL), it & 1, a.status, 0x3101)) { ok = false; break; }
           tc_fence_after();
-          issue_s(kv + j);
-          tc_commit(sh.bar(B_KEMPTY + ((kv + j) & 1)));
-          tc_commit(sh.bar(B_SFULL + ((kv + j) & 1)));
-          if (j == n - 1) tc_commit(sh.bar(B_QEMPTY));
-        }
-        if (!ok) break;
-        for (int j = 0; j < n; ++j) {
-          const int g = kv + j, st = g & 1;
-          if (!wait_bar(sh, sh.bar(B_PFULL + st), (g >> 1) & 1, a.status, 0x3103)) { ok = false; break; }
-          if (!wait_bar(sh, sh.bar(B_VFULL + st), (g >> 1) & 1, a.status, 0x3104)) { ok = false; break; }
-          tc_fence_after();
-          const uint32_t vb = sh.base + kOffV + st * kNV * kBox;
-#pragma unroll
-          for (int kk = 0; kk < kBN / 16; ++kk)
-            tc_mma_ts(t_o, tmem + st * 128 + kk * 8, sdesc_sw128(vb + kk * 2048, kBox, 1024),
-                      kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-          tc_commit(sh.bar(B_VEMPTY + st));
-          tc_commit(sh.bar(B_ODONE));
-          if (j + 2 < n) {
-            if (!wait_k(g + 2)) { ok = false; break; }
+          for (int j = 0; j < 2 && j < n; ++j) {
+            if (!wait_k(kv + j)) { ok = false; break; }
             tc_fence_after();
-            issue_s(g + 2);
-            tc_commit(sh.bar(B_KEMPTY + st));
-            tc_commit(sh.bar(B_SFULL + st));
-            if (j + 2 == n - 1) tc_commit(sh.bar(B_QEMPTY));
+            issue_s(kv + j);
+            tc_commit(sh.bar(B_KEMPTY + ((kv + j) & 1)));
+            tc_commit(sh.bar(B_SFULL + ((kv + j) & 1)));
+            if (j == n - 1) tc_commit(sh.bar(B_QEMPTY));
           }
+          if (!ok) break;
+          for (int j = 0; j < n; ++j) {
+            const int g = kv + j, st = g & 1;
+            // the first P.V overwrites O: the previous item's epilogue has read it
+            if (j == 0 && it > 0 && !wait_bar(sh, sh.bar(B_OFREE), (it - 1) & 1, a.status, 0x3105)) {
+              ok = false;
+              break;
+            }
+            if (!wait_bar(sh, sh.bar(B_PFULL + st), (g >> 1) & 1, a.status, 0x3103)) { ok = false; break; }
+            if (!wait_bar(sh, sh.bar(B_VFULL + st), (g >> 1) & 1, a.status, 0x3104)) { ok = false; break; }
+            tc_fence_after();
+            const uint32_t vb = sh.base + kOffV + st * kNV * kBox;
+  #pragma unroll
+            for (int kk = 0; kk < kBN / 16; ++kk)
+              tc_mma_ts(t_o, tmem + st * 128 + kk * 8, sdesc_sw128(vb + kk * 2048, kBox, 1024),
+                        kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+            tc_commit(sh.bar(B_VEMPTY + st));
+            tc_commit(sh.bar(B_ODONE));
+            if (j + 2 < n) {
+              if (!wait_k(g + 2)) { ok = false; break; }
+              tc_fence_after();
+              issue_s(g + 2);
+              tc_commit(sh.bar(B_KEMPTY + st));
+              tc_commit(sh.bar(B_SFULL + st));
+              if (j + 2 == n - 1) tc_commit(sh.bar(B_QEMPTY));
+            }
+          }
+          if (!ok) break;
+          tc_commit(sh.bar(B_ORDY));
+          kv += n;
         }
-        if (!ok) break;
-        tc_commit(sh.bar(B_ORDY));
-        kv += n;
       }
     }
-  } else {
-    // --------------------------------------------- softmax + epilogue -----
+    // warps 10-11: idle (they complete the producer warpgroup)
+  } else if (warp < 4) {
+    // ------------------------------------------------------- softmax ------
+    regs_inc<kRegsHigh>();
     const int row = warp * 32 + lane;  // query row within the item = TMEM lane
     const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
     const uint32_t t_o = tmem + lane_off + 256;
     const float sl2 = a.scale_log2;
-    const float lam = *sh.lam();
-    const float cscale = 1.f - a.lambda_init;
-    // receive buffer: this CTA's K ring, row r at r * 512 bytes
-    const uint8_t* my_rx = sh.gen + kOffK + row * kRowX;
-    const uint32_t partner_rx0 = map_to_rank(sh.base + kOffK, partner);
-    const uint32_t partner_rxrdy = map_to_rank(sh.bar(B_RXRDY), partner);
-    const uint32_t partner_data = map_to_rank(sh.bar(B_DATA), partner);
-    const uint32_t partner_ssq_bar[2] = {map_to_rank(sh.bar(B_SSQ), partner), map_to_rank(sh.bar(B_SSQ1), partner)};
-    const uint32_t partner_ssq_slot[2] = {map_to_rank(sh.ssq_rx(0) + row * 4, partner),
-                                          map_to_rank(sh.ssq_rx(1) + row * 4, partner)};
+    float* lse = rank == 0 ? a.lse1 : a.lse2;
     int kv = 0, it = 0;
-    bool ok = true;
     for (;; ++it) {
       const int i = consume(it, false);
       __syncwarp();
       if (lane == 0 && i >= 0) release(it);  // the whole warp has read the slot
-      if (i < 0) { ok = false; break; }
-      if (i >= n_items) break;
+      if (i < 0) break;
+      // (the hand-off slot is free once the epilogue warps have taken the
+      // previous item: they read it before they release O)
+      if (i >= n_items) {
+        if (it > 0 && !wait_bar(sh, sh.bar(B_OFREE), (it - 1) & 1, a.status, 0x3209)) break;
+        if (row == 0) *sh.epi_item() = n_items;  // end of the sequence
+        mbar_arrive(sh.bar(B_EPI));
+        break;
+      }
       const Item w = item_of(i, units, a.H, n_mtiles, ub, causal);
       float m_run = -INFINITY, l_run = 0.f;
+      bool ok = true;
       for (int j = 0; j < w.n_kv; ++j) {
         const int g = kv + j;
         const uint32_t t_s = tmem + lane_off + (g & 1) * 128;
@@ -478,45 +470,67 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
       }
       if (!ok) break;
       kv += w.n_kv;
-      // ----------------------------------------------------- epilogue ----
-      if (!wait_bar(sh, sh.bar(B_ORDY), it & 1, a.status, 0x3203)) { ok = false; break; }
+      const int n = w.mt * kBM + row;
+      if (lse && n < a.N)
+        lse[(static_cast<int64_t>(w.b) * a.H + w.h) * a.N + n] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
+      // hand the item and this row's sum to the epilogue warps
+      if (it > 0 && !wait_bar(sh, sh.bar(B_OFREE), (it - 1) & 1, a.status, 0x320a)) break;
+      sh.epi_l()[row] = l_run;
+      if (row == 0) *sh.epi_item() = i;
+      mbar_arrive(sh.bar(B_EPI));
+    }
+  } else {
+    // ------------------------------------------------------ epilogue ------
+    regs_inc<kRegsHigh>();
+    const int q = warp - 4;
+    const int row = q * 32 + lane;  // query row = TMEM lane of this warp's quadrant
+    const uint32_t t_o = tmem + (static_cast<uint32_t>(q * 32) << 16) + 256;
+    const float lam = *sh.lam();
+    const float cscale = 1.f - a.lambda_init;
+    const int give = (1 - static_cast<int>(rank)) * kHalf, keep = static_cast<int>(rank) * kHalf;
+    // exchange slots: kHalf columns of 128 fp32 (O/l of the columns the
+    // partner finishes, column-major so that a warp's 32 rows of one column
+    // are one 128-byte line)
+    float* xchg = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + kXchgOff);
+    const size_t cl = blockIdx.x >> 1;
+    float* my_x = xchg + (cl * 2 + rank) * 128 * kHalf + row;              // column c at [c * 128]
+    const float* partner_x = xchg + (cl * 2 + partner) * 128 * kHalf + row;
+    const uint32_t partner_xrdy = map_to_rank(sh.bar(B_XRDY), partner);
+    const uint32_t partner_ssq_bar0 = map_to_rank(sh.bar(B_SSQ), partner);
+    const uint32_t partner_ssq_bar1 = map_to_rank(sh.bar(B_SSQ1), partner);
+    const uint32_t partner_ssq_slot0 = map_to_rank(sh.ssq_rx(0) + row * 4, partner);
+    const uint32_t partner_ssq_slot1 = map_to_rank(sh.ssq_rx(1) + row * 4, partner);
+    const bool want_o2 = a.o2.ptr != nullptr;
+    __nv_bfloat16* const yb = static_cast<__nv_bfloat16*>(a.out.ptr);
+    __nv_bfloat16* const o2b = static_cast<__nv_bfloat16*>(a.o2.ptr);
+    // bf16 of 8 values, 16 bytes
+    auto pack8 = [](const float* v) {
+      uint4 pk;
+      pk.x = pack_bf16x2(v[0], v[1]);
+      pk.y = pack_bf16x2(v[2], v[3]);
+      pk.z = pack_bf16x2(v[4], v[5]);
+      pk.w = pack_bf16x2(v[6], v[7]);
+      return pk;
+    };
+    for (int it = 0;; ++it) {
+      if (!wait_bar(sh, sh.bar(B_EPI), it & 1, a.status, 0x3203)) break;
+      const int i = *sh.epi_item();
+      const float l_run = sh.epi_l()[row];
+      if (i >= n_items) break;
+      const Item w = item_of(i, units, a.H, n_mtiles, ub, causal);
+      if (!wait_bar(sh, sh.bar(B_ORDY), it & 1, a.status, 0x3204)) break;
       tc_fence_after();
       const float inv_l = 1.f / l_run;
-      const int give = (1 - static_cast<int>(rank)) * kHalf, keep = static_cast<int>(rank) * kHalf;
-      // (1) stage the partner's half of my O/l in this item's last V stage (idle
-      // now; row r at r * 512 bytes, 16-byte chunks XOR-swizzled by r & 7),
-      // then one thread moves the 64 KB into the partner's K ring with a bulk
-      // copy whose bytes complete on the partner's DATA barrier
-      const int give_stage = (kv - 1) & 1;
-      uint8_t* gstg = sh.gen + kOffV + give_stage * kNV * kBox + row * kRowX;
+      // (1) the partner's half of my O/l into my exchange slot
 #pragma unroll 1
-      for (int c2 = 0; c2 < kHalf / 64; ++c2) {
-        uint32_t o[64];
-        tmem_ld32(t_o + give + c2 * 64, *reinterpret_cast<uint32_t(*)[32]>(&o[0]));
-        tmem_ld32(t_o + give + c2 * 64 + 32, *reinterpret_cast<uint32_t(*)[32]>(&o[32]));
+      for (int c = 0; c < kHalf / 32; ++c) {
+        uint32_t o[32];
+        tmem_ld32(t_o + give + c * 32, o);
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 64; e += 4) {
-          const int u = (c2 * 64 + e) >> 2;
-          *reinterpret_cast<float4*>(gstg + ((u ^ (row & 7)) << 4)) =
-              make_float4(__uint_as_float(o[e]) * inv_l, __uint_as_float(o[e + 1]) * inv_l,
-                          __uint_as_float(o[e + 2]) * inv_l, __uint_as_float(o[e + 3]) * inv_l);
-        }
+        for (int e = 0; e < 32; ++e) my_x[(c * 32 + e) * 128] = __uint_as_float(o[e]) * inv_l;
       }
-      fence_proxy_async_smem();
-      mbar_arrive(sh.bar(B_GIVE));
-      if (row == 0) {
-        // my MMAs are done (ORDY), so my K ring may receive
-        remote_arrive(partner_rxrdy);
-        mbar_arrive_expect_tx(sh.bar(B_DATA), 128 * kRowX);
-        if (!wait_bar(sh, sh.bar(B_GIVE), it & 1, a.status, 0x3208) ||
-            !wait_bar<true>(sh, sh.bar(B_RXRDY), it & 1, a.status, 0x3206)) {
-          ok = false;
-          break;
-        }
-        bulk_copy_to_peer(partner_rx0, sh.base + kOffV + give_stage * kNV * kBox, 128 * kRowX, partner_data);
-      }
-      // (2) my own half of O/l into registers while the copies are in flight
+      // (2) my own half of O/l into registers
       float dvals[kHalf];
 #pragma unroll
       for (int c = 0; c < kHalf / 32; ++c) {
@@ -526,124 +540,79 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
 #pragma unroll
         for (int e = 0; e < 32; ++e) dvals[c * 32 + e] = __uint_as_float(o[e]) * inv_l;
       }
-      if (!wait_bar<true>(sh, sh.bar(B_DATA), it & 1, a.status, 0x3204)) { ok = false; break; }
-      // (3) O = O1/l1 - lambda O2/l2 on my half; partial sum of squares
-      float ssq = 0.f;
+      // O has been read: the next item's first P.V may overwrite it; my slot
+      // row is written: release it to the partner (cluster scope orders the
+      // slot stores before the arrive)
+      tc_fence_before();
+      mbar_arrive(sh.bar(B_OFREE));
+      remote_arrive(partner_xrdy);
       const int n = w.mt * kBM + row;
       const bool live = n < a.N;
-      // staging for the TMA stores: the V stage of this item's last tile,
-      // which the producer refills only after these stores have read it (Y in
-      // the first DV/128 boxes, O2 in the next DV/128, 128-byte swizzle).  It held the outgoing
-      // half of O until the bulk copy read it: the partner sends its partial
-      // sums only after all those bytes arrived, so after the SSQ wait below
-      // it is free again.
-      const int stg_stage = (kv - 1) & 1;
-      uint8_t* stg = sh.gen + kOffV + stg_stage * kNV * kBox;
-      const uint32_t stg_s = sh.base + kOffV + stg_stage * kNV * kBox;
-      const bool want_o2 = a.o2.ptr != nullptr;
+      const int64_t yrow = static_cast<int64_t>(w.b) * a.out.sb + static_cast<int64_t>(n) * a.out.sn +
+                           static_cast<int64_t>(w.h) * a.out.sh + keep;
+      const int64_t o2row = static_cast<int64_t>(w.b) * a.o2.sb + static_cast<int64_t>(n) * a.o2.sn +
+                            static_cast<int64_t>(w.h) * a.o2.sh + keep;
+      if (want_o2 && rank == 1 && live) {
+        // O2 / l2 of my columns: my own stream
 #pragma unroll
-      for (int u = 0; u < kHalf / 4; ++u) {
-        const float4 oth = *reinterpret_cast<const float4*>(my_rx + ((u ^ (row & 7)) << 4));
-        const float othv[4] = {oth.x, oth.y, oth.z, oth.w};
+        for (int e = 0; e < kHalf; e += 8) *reinterpret_cast<uint4*>(o2b + o2row + e) = pack8(&dvals[e]);
+      }
+      // (3) the partner's half of its O/l for my columns
+      if (!wait_bar<true>(sh, sh.bar(B_XRDY), it & 1, a.status, 0x3205)) break;
+      float ssq = 0.f;
 #pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float own = dvals[4 * u + q];
-          const float a1 = rank == 0 ? own : othv[q];
-          const float a2 = rank == 0 ? othv[q] : own;
+      for (int c = 0; c < kHalf / 32; ++c) {
+        float oth[32];
+#pragma unroll
+        for (int e = 0; e < 32; ++e) oth[e] = ld_cg_f32(partner_x + (c * 32 + e) * 128);
+#pragma unroll
+        for (int e = 0; e < 32; ++e) {
+          const float own = dvals[c * 32 + e];
+          const float a1 = rank == 0 ? own : oth[e];
+          const float a2 = rank == 0 ? oth[e] : own;
           const float dd = __fsub_rn(a1, __fmul_rn(lam, a2));
-          dvals[4 * u + q] = dd;
+          dvals[c * 32 + e] = dd;
           ssq = fmaf(dd, dd, ssq);
+        }
+      }
+      if (want_o2 && rank == 0 && live) {
+        // O2 / l2 of my columns: received
+#pragma unroll 1
+        for (int e = 0; e < kHalf; e += 8) {
+          float v[8];
+#pragma unroll
+          for (int k = 0; k < 8; ++k) v[k] = ld_cg_f32(partner_x + (e + k) * 128);
+          *reinterpret_cast<uint4*>(o2b + o2row + e) = pack8(v);
         }
       }
       // (4) swap the per-row partial sums: one asynchronous 4-byte store per
       //     row into the partner's slot of this item's parity, its bytes
-      //     counted on the partner's barrier of that parity (one local
-      //     arrive with the expected 512 bytes per phase)
+      //     counted on the partner's barrier of that parity (one local arrive
+      //     with the expected 512 bytes per phase).  The partner sends its
+      //     sums only after it has read my slot, so once they are here my
+      //     slot may take the next item.
       const int sp = it & 1;
       if (row == 0) mbar_arrive_expect_tx(sh.bar(B_SSQ + sp), 128 * 4);
-      st_async_f32(partner_ssq_slot[sp], ssq, partner_ssq_bar[sp]);
-      if (!wait_bar<true>(sh, sh.bar(B_SSQ + sp), (it >> 1) & 1, a.status, 0x3205)) { ok = false; break; }
-      if (want_o2) {
-        // O2 / l2 of my columns: received (rank 0) or my own (rank 1)
-#pragma unroll 1
-        for (int c = 0; c < kHalf / 32; ++c) {
-          float o2v[32];
-          if (rank == 0) {
-#pragma unroll
-            for (int e = 0; e < 32; e += 4) {
-              const int u = (c * 32 + e) >> 2;
-              const float4 v4 = *reinterpret_cast<const float4*>(my_rx + ((u ^ (row & 7)) << 4));
-              o2v[e] = v4.x;
-              o2v[e + 1] = v4.y;
-              o2v[e + 2] = v4.z;
-              o2v[e + 3] = v4.w;
-            }
-          } else {
-            uint32_t o[32];
-            tmem_ld32(t_o + keep + c * 32, o);
-            tmem_ld_wait();
-#pragma unroll
-            for (int e = 0; e < 32; ++e) o2v[e] = __uint_as_float(o[e]) * inv_l;
-          }
-#pragma unroll
-          for (int e = 0; e < 32; e += 8) {
-            const int col = c * 32 + e;  // column within this CTA's half
-            uint4 pk;
-            pk.x = pack_bf16x2(o2v[e], o2v[e + 1]);
-            pk.y = pack_bf16x2(o2v[e + 2], o2v[e + 3]);
-            pk.z = pack_bf16x2(o2v[e + 4], o2v[e + 5]);
-            pk.w = pack_bf16x2(o2v[e + 6], o2v[e + 7]);
-            *reinterpret_cast<uint4*>(stg + (kHalf / 64 + (col >> 6)) * kBox + row * 128 +
-                                      ((((col & 63) >> 3) ^ (row & 7)) << 4)) = pk;
-          }
-        }
-      }
-      mbar_arrive(sh.bar(B_RXFREE));  // this row's part of the K ring has been read
+      st_async_f32(sp ? partner_ssq_slot1 : partner_ssq_slot0, ssq, sp ? partner_ssq_bar1 : partner_ssq_bar0);
+      if (!wait_bar<true>(sh, sh.bar(B_SSQ + sp), (it >> 1) & 1, a.status, 0x3206)) break;
       const float other_ssq = sh.ssq_rx_ptr(sp)[row];
       const float tot = rank == 0 ? ssq + other_ssq : other_ssq + ssq;
       const float rstd = 1.f / sqrtf(tot * (1.f / kDv) + a.rms_eps);
       const float cs = cscale * rstd;
-      if (a.rms_weight) {
-        // Y = (1 - lambda_init) w O / rms: the per-feature weight of my half
-        const float* wk = a.rms_weight + keep;
-#pragma unroll
-        for (int e = 0; e < kHalf; ++e) dvals[e] = __fmul_rn(__fmul_rn(dvals[e], cs), __ldg(wk + e));
-      } else {
-#pragma unroll
-        for (int e = 0; e < kHalf; ++e) dvals[e] = __fmul_rn(dvals[e], cs);
-      }
-#pragma unroll
-      for (int e = 0; e < kHalf; e += 8) {
-        uint4 pk;
-        pk.x = pack_bf16x2(dvals[e], dvals[e + 1]);
-        pk.y = pack_bf16x2(dvals[e + 2], dvals[e + 3]);
-        pk.z = pack_bf16x2(dvals[e + 4], dvals[e + 5]);
-        pk.w = pack_bf16x2(dvals[e + 6], dvals[e + 7]);
-        *reinterpret_cast<uint4*>(stg + (e >> 6) * kBox + row * 128 + ((((e & 63) >> 3) ^ (row & 7)) << 4)) = pk;
-      }
+      // (5) Y = (1 - lambda_init) w O / rms on my columns, straight to HBM
       if (live) {
-        const int64_t sidx = (static_cast<int64_t>(w.b) * a.H + w.h) * a.N + n;
-        float* lse = rank == 0 ? a.lse1 : a.lse2;
-        if (lse) lse[sidx] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
-        if (rank == 0 && a.rstd) a.rstd[sidx] = rstd;
+        if (a.rms_weight) {
+          const float* wk = a.rms_weight + keep;
+#pragma unroll
+          for (int e = 0; e < kHalf; ++e) dvals[e] = __fmul_rn(__fmul_rn(dvals[e], cs), __ldg(wk + e));
+        } else {
+#pragma unroll
+          for (int e = 0; e < kHalf; ++e) dvals[e] = __fmul_rn(dvals[e], cs);
+        }
+#pragma unroll
+        for (int e = 0; e < kHalf; e += 8) *reinterpret_cast<uint4*>(yb + yrow + e) = pack8(&dvals[e]);
+        if (rank == 0 && a.rstd) a.rstd[(static_cast<int64_t>(w.b) * a.H + w.h) * a.N + n] = rstd;
       }
-      // all rows staged -> one thread stores the tiles with TMA (rows past N
-      // are dropped) and, once the staging has been read, releases this V
-      // stage to the producer
-      fence_proxy_async_smem();
-      mbar_arrive(sh.bar(B_STG));
-      if (!wait_bar(sh, sh.bar(B_STG), it & 1, a.status, 0x3207)) { ok = false; break; }
-      if (row == 0) {
-        for (int bx = 0; bx < kHalf / 64; ++bx)
-          tma_store_4d(&tm_out, stg_s + bx * kBox, keep + bx * 64, w.h, w.mt * kBM, w.b);
-        if (want_o2)
-          for (int bx = 0; bx < kHalf / 64; ++bx)
-            tma_store_4d(&tm_o2, stg_s + (kHalf / 64 + bx) * kBox, keep + bx * 64, w.h, w.mt * kBM, w.b);
-        bulk_commit();
-        bulk_wait_read();
-        mbar_arrive(sh.bar(B_STGFREE));
-      }
-      tc_fence_before();
     }
   }
 
@@ -651,13 +620,16 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
   __syncthreads();
   cluster_sync();  // no CTA leaves while its partner may still address its shared memory
   tc_fence_after();
-  if (warp == 5) tmem_dealloc(tmem, 512);
+  if (warp == 9) tmem_dealloc(tmem, 512);
 }
 
 }  // namespace
 
-// the work counter of the dynamic schedule
-size_t v1_fwd_workspace_bytes(int) { return 256; }
+// the work counter of the dynamic schedule and one exchange slot per CTA
+size_t v1_fwd_workspace_bytes(int num_sms) {
+  const int sms = num_sms > 0 ? num_sms : 152;
+  return kXchgOff + static_cast<size_t>(sms / 2) * 2 * kXchgBytes;
+}
 
 namespace {
 
@@ -671,15 +643,13 @@ cudaError_t launch_dims(const V1FwdArgs& a, cudaStream_t s) {
       !encode_tmap_bf16_4d(&tk2, a.k2, a.B, a.N, a.H, kDqk, kBN) ||
       !encode_tmap_bf16_4d(&tv, a.v, a.B, a.N, a.H, kDv, kBN))
     return cudaErrorInvalidValue;
-  CUtensorMap tout, to2;
-  if (!encode_tmap_bf16_4d(&tout, a.out, a.B, a.N, a.H, kDv, kBM) ||
-      !encode_tmap_bf16_4d(&to2, a.o2.ptr ? a.o2 : a.out, a.B, a.N, a.H, kDv, kBM))
-    return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(v1_fwd_kernel<DQK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemBytes);
   if (e != cudaSuccess) return e;
   const int n_items = ((a.N + kBM - 1) / kBM) * a.B * a.H;
-  // clusters of two CTAs; as many as fit at once (one CTA per SM)
+  const int sms = a.num_sms > 0 ? a.num_sms : 152;
+  // clusters of two CTAs; as many as fit at once (one CTA per SM), and no
+  // more than the workspace has exchange slots for
   cudaLaunchConfig_t cfg = {};
   cudaLaunchAttribute attr[1];
   attr[0].id = cudaLaunchAttributeClusterDimension;
@@ -692,16 +662,18 @@ cudaError_t launch_dims(const V1FwdArgs& a, cudaStream_t s) {
   cfg.attrs = attr;
   cfg.numAttrs = 1;
   int max_clusters = 0;
-  cfg.gridDim = dim3(2 * ((a.num_sms > 0 ? a.num_sms : 152) / 2), 1, 1);
+  cfg.gridDim = dim3(2 * (sms / 2), 1, 1);
   e = cudaOccupancyMaxActiveClusters(&max_clusters, v1_fwd_kernel<DQK, DV>, &cfg);
-  if (e != cudaSuccess || max_clusters <= 0) max_clusters = (a.num_sms > 0 ? a.num_sms : 152) / 2;
+  if (e != cudaSuccess || max_clusters <= 0) max_clusters = sms / 2;
   int clusters = max_clusters;
+  if (clusters > sms / 2) clusters = sms / 2;
   if (clusters > n_items) clusters = n_items;
   if (clusters <= 0) return cudaErrorInvalidValue;
+  if (a.workspace_bytes < kXchgOff + static_cast<size_t>(clusters) * 2 * kXchgBytes) return cudaErrorInvalidValue;
   cfg.gridDim = dim3(2 * clusters, 1, 1);
   e = cudaMemsetAsync(a.workspace, 0, sizeof(int), s);
   if (e != cudaSuccess) return e;
-  return cudaLaunchKernelEx(&cfg, v1_fwd_kernel<DQK, DV>, tq1, tq2, tk1, tk2, tv, tout, to2, a);
+  return cudaLaunchKernelEx(&cfg, v1_fwd_kernel<DQK, DV>, tq1, tq2, tk1, tk2, tv, a);
 }
 
 }  // namespace

@@ -85,9 +85,12 @@ float diffattn_lambda_init(int layer);
  *   (1/sqrt(mean O^2 + eps)): fp32 [B, H, N] contiguous;
  *   o2 = softmax(s Q2 K2^T) V: [B, N, H, d_v] of `dtype`;
  *   lambda_out: fp32 [1].
- * workspace: diffattn_v1_fwd_workspace_size(...) bytes (a work counter of
- * the bf16 path's dynamic schedule; 0 for DA_F32), 256-byte aligned,
- * contents on entry irrelevant (the call clears it on the stream). */
+ * workspace: diffattn_v1_fwd_workspace_size(...) bytes (for the bf16 path:
+ * the work counter of its dynamic schedule, cleared by the call on the
+ * stream, and one 64 KB slot per SM through which the two CTAs of a pair
+ * exchange half of their outputs, about 10 MB on a 152-SM GPU; 0 for
+ * DA_F32), 256-byte aligned, contents on entry irrelevant.  Calls that run
+ * at the same time need workspaces of their own. */
 typedef struct {
   int B, N, H, d_qk, d_v;
   da_dtype dtype;
