@@ -169,6 +169,19 @@ def test_bwd_workspace_size(lib):
     assert lib.diffattn_v2_bwd_workspace_size(2, 8192, 32, 4096) > lib.diffattn_v2_bwd_workspace_size(2, 8192, 32, 0)
 
 
+def test_v1_fwd_workspace_size(lib):
+    # bf16 path: a 256-byte work counter, then one 64 KB exchange slot
+    # (128 rows x 128 fp32) per CTA of every 2-CTA cluster that can run at once
+    ws = lib.diffattn_v1_fwd_workspace_size(4, 4096, 12, 128, 256, bd.DA_BF16)
+    slot = 128 * 128 * 4
+    assert ws > 256 and (ws - 256) % (2 * slot) == 0
+    # the same for the (64, 128) head dims (the slot is sized for the larger)
+    assert lib.diffattn_v1_fwd_workspace_size(4, 4096, 12, 64, 128, bd.DA_BF16) == ws
+    # the fp32 path needs none; empty shapes need none
+    assert lib.diffattn_v1_fwd_workspace_size(1, 64, 2, 16, 32, bd.DA_F32) == 0
+    assert lib.diffattn_v1_fwd_workspace_size(0, 4096, 12, 128, 256, bd.DA_BF16) == 0
+
+
 def test_grouped_shape_checks(lib):
     """Grouped differential attention rejects, before any launch, groups that
     do not divide the heads or straddle K/V groups, and an odd number of query
