@@ -60,6 +60,7 @@ __all__ = [
     "v2_backward",
     "v1_decode",
     "grouped_forward",
+    "grouped_backward",
 ]
 
 
@@ -433,3 +434,61 @@ def grouped_forward(q, k, v, gate, ratio: int, *, scale: float | None = None,
             out[:, :, p] = o[:, :, g * (ratio + 1) + i] - gate[:, rows, p, None] * noise
     return dict(out=out, o=o, lse=lse, rows=rows)
 
+
+def grouped_backward(q, k, v, x, w, dout, ratio: int, *, scale: float | None = None,
+                     causal: bool = True):
+    """Gradients of grouped differential attention (``v2_gate`` then
+    ``grouped_forward``) with respect to q, k, v, x and w, given dOut.  The
+    pages state no backward ([P1] "같은 문제, 다른 접근" names the 3:1 / 4:1
+    signal:noise follow-up only); this is the chain rule of the forward above,
+    step by step.  With r = ratio, group gi holding signal heads
+    gi (r+1) + i (i < r) and noise head gi (r+1) + r, output head
+    p = gi r + i, g = sigmoid(z), z = X W, G = dOut:
+      Out_p = O_signal(p) - g_p O_noise(gi)
+      dO_signal(p) = G_p,   dO_noise(gi) = -sum_i g_p G_p
+      dg_p = -<G_p, O_noise(gi)>,   dz = dg g (1 - g)
+      dW = X^T dz,  dX = dz W^T
+      per query head j (kv head c = j // group):  A = softmax(s Q_j K_c^T),
+      dP = dO_j V_c^T,  dS = A * (dP - <dO_j, O_j>),
+      dQ_j = s dS K_c,  dK_c += s dS^T Q_j,  dV_c += A^T dO_j.
+    Pinned against central finite differences of the forward, and against
+    ``v2_backward`` at ratio 1."""
+    q, k, v, x, w, dout = (_f64(t) for t in (q, k, v, x, w, dout))
+    B, N, Hq, d = q.shape
+    hkv = k.shape[2]
+    group = Hq // hkv
+    n_groups = Hq // (ratio + 1)
+    if scale is None:
+        scale = 1.0 / np.sqrt(d)
+    z = x @ w
+    g = _sigmoid(z)
+    fwd = grouped_forward(q, k, v, g, ratio, scale=scale, causal=causal)
+    o = fwd["o"]
+    do = np.zeros_like(o)
+    dg = np.zeros_like(g)
+    for gi in range(n_groups):
+        noise = gi * (ratio + 1) + ratio
+        for i in range(ratio):
+            p = gi * ratio + i
+            do[:, :, gi * (ratio + 1) + i] = dout[:, :, p]
+            do[:, :, noise] -= g[:, :, p, None] * dout[:, :, p]
+            dg[:, :, p] = -np.sum(dout[:, :, p] * o[:, :, noise], axis=-1)
+    dz = dg * g * (1.0 - g)
+    dw = np.einsum("btk,btp->kp", x, dz)
+    dx = dz @ w.T
+    dq = np.zeros_like(q)
+    dk = np.zeros_like(k)
+    dv = np.zeros_like(v)
+    for b in range(B):
+        for j in range(Hq):
+            c = j // group
+            Q, K, V = q[b, :, j], k[b, :, c], v[b, :, c]
+            a, _ = attention_maps(Q, K, scale, causal)
+            dO = do[b, :, j]
+            dP = dO @ V.T
+            D = np.sum(dO * o[b, :, j], axis=1, keepdims=True)
+            dS = a * (dP - D)
+            dq[b, :, j] = scale * dS @ K
+            dk[b, :, c] += scale * dS.T @ Q
+            dv[b, :, c] += a.T @ dO
+    return dict(dq=dq, dk=dk, dv=dv, dx=dx, dw=dw, dz=dz, gate=g, o=o, lse=fwd["lse"])

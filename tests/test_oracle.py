@@ -551,3 +551,75 @@ def test_v2_backward_gate_zero_reduces_to_even_heads():
     dv_odd = -0.5 * np.cumsum((dout[0, :, 0] / n)[::-1], axis=0)[::-1]
     np.testing.assert_allclose(full["dv"][0, :, 0], dv_even + dv_odd, atol=1e-12)
     np.testing.assert_allclose(full["gate"], 0.5, atol=0)
+
+
+@pytest.mark.parametrize("ratio,causal", [(3, True), (4, False), (2, True)])
+def test_grouped_backward_finite_differences(ratio, causal):
+    """Every grouped-attention gradient (q, k, v, x, w_lambda) against central
+    differences of gate + grouped forward (fp64): two groups sharing one K/V
+    head, with and without the causal mask."""
+    r = _rng(50 + ratio)
+    B, N, hkv, d, dm = 1, 4, 1, 3, 3
+    Hq = 2 * (ratio + 1)
+    h = 2 * ratio
+    t = dict(q=r.standard_normal((B, N, Hq, d)), k=r.standard_normal((B, N, hkv, d)),
+             v=r.standard_normal((B, N, hkv, d)), x=r.standard_normal((B, N, dm)),
+             w=0.5 * r.standard_normal((dm, h)))
+    dout = r.standard_normal((B, N, h, d))
+    grads = orc.grouped_backward(t["q"], t["k"], t["v"], t["x"], t["w"], dout, ratio, causal=causal)
+
+    def loss(tt):
+        gate = orc.v2_gate(tt["x"], tt["w"])
+        out = orc.grouped_forward(tt["q"], tt["k"], tt["v"], gate, ratio, causal=causal)["out"]
+        return float(np.sum(out * dout))
+
+    eps = 1e-6
+    for name in ("q", "k", "v", "x", "w"):
+        g = grads["d" + name]
+        num = np.zeros_like(t[name])
+        it = np.nditer(t[name], flags=["multi_index"])
+        for _ in it:
+            idx = it.multi_index
+            tp = {kk: vv.copy() for kk, vv in t.items()}
+            tm = {kk: vv.copy() for kk, vv in t.items()}
+            tp[name][idx] += eps
+            tm[name][idx] -= eps
+            num[idx] = (loss(tp) - loss(tm)) / (2 * eps)
+        err = np.max(np.abs(num - g)) / max(np.max(np.abs(num)), 1e-12)
+        assert err < 1e-6, (name, err)
+
+
+def test_grouped_backward_ratio_one_is_v2_backward():
+    """Ratio 1 (one signal head per noise head) is V2: the grouped backward
+    equals the V2 backward, itself pinned by finite differences."""
+    r = _rng(55)
+    B, N, h, hkv, d, dm = 2, 9, 4, 2, 4, 5
+    q, k, v = (r.standard_normal(s) for s in ((B, N, 2 * h, d), (B, N, hkv, d), (B, N, hkv, d)))
+    x, w, dout = r.standard_normal((B, N, dm)), 0.3 * r.standard_normal((dm, h)), r.standard_normal((B, N, h, d))
+    a = orc.grouped_backward(q, k, v, x, w, dout, 1)
+    b = orc.v2_backward(q, k, v, x, w, dout)
+    for n in ("dq", "dk", "dv", "dx", "dw", "dz"):
+        np.testing.assert_allclose(a[n], b[n], rtol=1e-12, atol=1e-12 * np.max(np.abs(b[n])))
+
+
+def test_grouped_backward_noise_gradient_collects_every_signal_head():
+    """With the signal queries zero and the gate weight zero (every gate 1/2),
+    the K/V group's dV is the closed form: the signal heads are uniform causal
+    maps of dOut, the noise head a softmax map of -1/2 sum_i dOut_i, so
+    dV = sum_i U^T dOut_i + A_noise^T (-1/2 sum_i dOut_i), U the uniform causal
+    map (pins that every signal head of the group feeds the noise head's dO)."""
+    r = _rng(56)
+    ratio, B, N, d, dm = 3, 1, 6, 4, 3
+    q = r.standard_normal((B, N, ratio + 1, d))
+    q[:, :, :ratio] = 0.0
+    k, v = r.standard_normal((B, N, 1, d)), r.standard_normal((B, N, 1, d))
+    x, w = r.standard_normal((B, N, dm)), np.zeros((dm, ratio))
+    dout = r.standard_normal((B, N, ratio, d))
+    full = orc.grouped_backward(q, k, v, x, w, dout, ratio)
+    s = 1 / np.sqrt(d)
+    a_noise, _ = orc.attention_maps(q[0, :, ratio], k[0, :, 0], s, True)
+    n = np.arange(1, N + 1)[:, None]
+    dsum = dout[0].sum(axis=1)  # sum over the signal heads
+    dv_signal = np.cumsum((dsum / n)[::-1], axis=0)[::-1]  # U^T applied to each, summed
+    dv_noise = a_noise.T @ (-0.5 * dsum)
+    np.testing.assert_allclose(full["dv"][0, :, 0], dv_signal + dv_noise, atol=1e-12)
