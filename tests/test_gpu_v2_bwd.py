@@ -9,11 +9,13 @@ precision alone causes on the same inputs.  Per gradient tensor:
 * max|GPU - oracle| <= k * max|model - oracle| + 1e-3 * RMS(oracle) + floor,
   k = 2 for the backward alone (fed the oracle's forward saves), 3 for the
   training step (GPU forward with saves, then the GPU backward);
-* ||GPU - oracle|| <= max(1.5e-2 ||oracle||, k ||model - oracle||) (2e-2 for
-  the step): the second term only matters where a gradient vanishes
-  analytically and rounding noise is all that is left;
+* ||GPU - oracle|| <= 1.5e-2 ||oracle|| (2e-2 for the step), a fixed bar that
+  does not involve the model; only where a gradient vanishes analytically
+  (N = 1: dQ and dK are exactly zero, the oracle's norm is rounding residue)
+  is it k times the model's own Frobenius error;
 floor = 1e-3 * RMS(oracle dV) for dQ / dK / dV and 1e-3 * RMS of the tensor
-itself for the gate gradients (dQ and dK vanish analytically at N = 1).
+itself for the gate gradients.  Every expected value is the oracle's.  Each
+test records error / allowed per tensor (tests/ratio_log.py).
 """
 
 import numpy as np
@@ -24,6 +26,7 @@ from differential_attention_diff_gb300 import binding as bd
 from differential_attention_diff_gb300 import synth
 from bf16_model import rounded_backward_v2
 from oracle import diffattn_oracle as orc
+from ratio_log import record
 
 pytestmark = pytest.mark.gpu
 BARS = {"bwd": (2.0, 1.5e-2), "step": (3.0, 2e-2)}
@@ -73,6 +76,7 @@ def _reference(t, causal=True):
 def _compare(g, ref, model, names=ATTN + GATE, bar="bwd", sl=None):
     k, fro = BARS[bar]
     floor_attn = 1e-3 * float(np.sqrt(np.mean(ref["dv"] ** 2)))
+    dv_norm = float(np.linalg.norm(ref["dv"]))
     worst = {}
     for n in names:
         got, exp, mod = f64(g[n]), ref[n], model[n]
@@ -82,12 +86,13 @@ def _compare(g, ref, model, names=ATTN + GATE, bar="bwd", sl=None):
         floor = floor_attn if n in ATTN else 1e-3 * rms
         allowed = k * float(np.max(np.abs(mod - exp))) + 1e-3 * rms + floor
         worst[n] = float(np.max(np.abs(got - exp))) / allowed
-        # relative Frobenius bar, or k times the rounding model's own error
-        # where the gradient vanishes analytically (N = 1) and only rounding
-        # noise is left
-        worst[n + "_fro"] = float(np.linalg.norm(got - exp)) / (
-            max(fro * float(np.linalg.norm(exp)), k * float(np.linalg.norm(mod - exp)))
-            + floor * np.sqrt(exp.size))
+        exp_norm = float(np.linalg.norm(exp))
+        if exp_norm > 1e-9 * dv_norm:
+            fro_allowed = fro * exp_norm
+        else:  # analytically zero (N = 1): rounding noise against rounding noise
+            fro_allowed = k * float(np.linalg.norm(mod - exp))
+        worst[n + "_fro"] = float(np.linalg.norm(got - exp)) / (fro_allowed + floor * np.sqrt(exp.size))
+    record(worst, bar)
     assert max(worst.values()) <= 1.0, worst
 
 
