@@ -161,7 +161,11 @@ size_t diffattn_v2_decode_workspace_size(int B, int h, int h_kv, int d, int L_ma
   return align256(po) + align256(pml) + align256(g);
 }
 
-da_status diffattn_v2_decode(const da_v2_decode_params* p, void* stream) {
+}  // extern "C"
+
+// Every check of a V2 decode call except those of the split count and the
+// workspace (shared with the entry point that brings its own scratch).
+da_status da::check_v2_decode_args(const da_v2_decode_params* p) {
   if (p == nullptr) return DA_ERR_INVALID_ARG;
   if (p->B <= 0 || p->h <= 0 || p->h_kv <= 0 || p->d <= 0 || p->L_max <= 0)
     return DA_ERR_INVALID_ARG;
@@ -178,9 +182,18 @@ da_status diffattn_v2_decode(const da_v2_decode_params* p, void* stream) {
   } else if (!aligned(p->gate, 4)) {
     return DA_ERR_INVALID_ARG;
   }
+  if (p->num_splits > da::kMaxDecodeSplits) return DA_ERR_INVALID_ARG;
+  return DA_OK;
+}
+
+extern "C" {
+
+da_status diffattn_v2_decode(const da_v2_decode_params* p, void* stream) {
+  const da_status chk = da::check_v2_decode_args(p);
+  if (chk != DA_OK) return chk;
   const int splits = p->num_splits > 0 ? p->num_splits
                                        : diffattn_v2_decode_num_splits(p->B, p->h_kv, p->L_max);
-  if (splits > 65535) return DA_ERR_INVALID_ARG;
+  if (splits > da::kMaxDecodeSplits) return DA_ERR_INVALID_ARG;
   const size_t need = diffattn_v2_decode_workspace_size(p->B, p->h, p->h_kv, p->d, p->L_max,
                                                         splits, p->gate != nullptr);
   if (p->workspace == nullptr || p->workspace_bytes < need || !aligned(p->workspace, 256))

@@ -15,15 +15,21 @@
 // Every GPU that loads the library reserves those 16 MiB until the process
 // exits.  The first call on a device looks up the array's device address
 // (cudaGetSymbolAddress, with that device current) and caches it; later calls
-// reuse it.  All calls share the one array: calls that overlap on the GPU
-// (different streams, or several host threads) race on it and must be
-// serialised by the caller.  Nothing in the array needs to start at zero:
-// every call overwrites every partial it later reads.
+// reuse it.  The cached address belongs to the device's primary context as it
+// was at that first call: after a cudaDeviceReset the array lives at a new
+// address in a new context, so the library (this entry point, and the device
+// status word every entry point uses, which is cached the same way) must not
+// be used again in a process that has reset the device.  All calls share the
+// one array: calls that overlap on the GPU (different streams, or several
+// host threads) race on it and must be serialised by the caller.  Nothing in
+// the array needs to start at zero: every call overwrites every partial it
+// later reads.
 #include <cuda_runtime.h>
 
 #include <mutex>
 
 #include "diffattn.h"
+#include "kernels.h"
 
 namespace {
 
@@ -53,9 +59,10 @@ da_status scratch_address(void** out) {
 }  // namespace
 
 extern "C" da_status diffattn_v2_decode_noalloc(const da_v2_decode_params* p, void* stream) {
-  if (p == nullptr) return DA_ERR_INVALID_ARG;
-  if (p->B <= 0 || p->h <= 0 || p->h_kv <= 0 || p->d <= 0 || p->L_max <= 0)
-    return DA_ERR_INVALID_ARG;
+  // the shape checks of diffattn_v2_decode first, so that a malformed problem
+  // is reported as such and not as one that does not fit the scratch
+  const da_status chk = da::check_v2_decode_args(p);
+  if (chk != DA_OK) return chk;
   const int gate_given = p->gate != nullptr;
   auto need = [&](int splits) {
     return diffattn_v2_decode_workspace_size(p->B, p->h, p->h_kv, p->d, p->L_max, splits,

@@ -34,6 +34,11 @@ struct DecodeArgs {
   uint32_t* status;
 };
 cudaError_t launch_decode(const DecodeArgs& a, cudaStream_t s);
+// The split count is a grid dimension (at most 65535).
+constexpr int kMaxDecodeSplits = 65535;
+// Every argument check of diffattn_v2_decode except the split count chosen
+// by the library and the workspace; DA_OK or the status the call returns.
+da_status check_v2_decode_args(const da_v2_decode_params* p);
 
 // ---- V1 decode: split-KV partials of both streams, then merge + RMSNorm ----
 struct V1DecodeArgs {

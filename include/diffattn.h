@@ -396,7 +396,11 @@ da_status diffattn_v2_decode(const da_v2_decode_params* p, void* cuda_stream);
  *
  * The first call on a device looks up the array's device address once (a
  * CUDA runtime query with that device current); make that first call before
- * any stream capture begins.  All calls share the array and each call
+ * any stream capture begins.  The address stays cached for the life of the
+ * process, so do not call the library again after a cudaDeviceReset (the
+ * same holds for every entry point: the device status word's address is
+ * cached the same way).  Shape errors are reported as by
+ * diffattn_v2_decode, before the size check.  All calls share the array and each call
  * overwrites what the previous one left there (nothing needs to start at
  * zero), so calls that may overlap on the GPU — other streams, other host
  * threads — race and must be serialised by the caller. */
@@ -409,7 +413,10 @@ da_status diffattn_v2_decode_noalloc(const da_v2_decode_params* p, void* cuda_st
  * trapping.  diffattn_get_device_status synchronises `cuda_stream`, returns
  * the recorded status (DA_OK if none) and clears the word.
  * diffattn_get_device_status_detail additionally returns the raw word
- * (status in the low byte, a kernel-specific site code above it). */
+ * (status in the low byte, a kernel-specific site code above it).
+ * The word's device address is looked up once per device and cached for the
+ * life of the process: after a cudaDeviceReset the library must not be used
+ * again in that process. */
 da_status diffattn_get_device_status(void* cuda_stream);
 da_status diffattn_get_device_status_detail(void* cuda_stream, uint32_t* raw);
 

@@ -125,6 +125,26 @@ def test_decode_argument_checks(lib):
     assert lib.diffattn_v2_decode_workspace_size(2, 32, 8, 128, 1024, 4, 0) > ws
 
 
+def test_noalloc_decode_reports_shape_errors_before_size(lib):
+    """The entry point without a workspace checks shapes as diffattn_v2_decode
+    does before it sizes the partials: a malformed problem that would also be
+    too large for its fixed scratch is reported as malformed, not as one that
+    does not fit."""
+    p = bd.da_v2_decode_params()
+    p.B, p.h, p.h_kv, p.d, p.L_max = 4096, 64, 8, 128, 1024  # too large for the scratch
+    fake = 1 << 20
+    p.q, p.out, p.gate = fake, fake, fake
+    p.k_cache = bd.da_t4(fake, 1024 * 8 * 128, 8 * 128, 128)
+    p.v_cache = bd.da_t4(fake, 1024 * 8 * 128, 8 * 128, 128)
+    f = lib.diffattn_v2_decode_noalloc
+    for field, value, expect in (("d", 96, bd.DA_ERR_UNSUPPORTED), ("h_kv", 3, bd.DA_ERR_INVALID_ARG),
+                                 ("h_kv", 128, bd.DA_ERR_INVALID_ARG), ("num_splits", 70000, bd.DA_ERR_INVALID_ARG)):
+        bad = bd.da_v2_decode_params.from_buffer_copy(p)
+        setattr(bad, field, value)
+        assert f(C.byref(bad), None) == expect, (field, value)
+        assert lib.diffattn_v2_decode(C.byref(bad), None) == expect, (field, value)
+
+
 def test_v2_fwd_argument_checks(lib):
     p = bd.da_v2_fwd_params()
     p.B, p.N, p.h, p.h_kv, p.d, p.causal = 1, 128, 32, 8, 128, 1
