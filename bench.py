@@ -127,6 +127,18 @@ class V1Fwd(Workload):
     def args(self, t):
         return [t[n] for n in ("q1", "q2", "k1", "k2", "v", "lq1", "lk1", "lq2", "lk2")]
 
+    def setup_host(self):
+        """Inputs for the oracle legs alone: drawn on the host with the same
+        shapes and distributions (the host generator's values differ from the
+        device's; the oracle's time does not depend on them), lambda_init from
+        the oracle; nothing of the library is loaded."""
+        from differential_attention_diff_gb300 import synth
+        from oracle import diffattn_oracle as orc
+        self.t = synth.v1_inputs(self.B, self.N, self.H, self.dqk, self.dv,
+                                 "f32" if self.dtype == "f32" else "bf16", seed=1002, device="cpu",
+                                 with_dy=True)
+        self.li = float(np.float32(orc.lambda_init(self.layer)))
+
     def run(self):
         self.bd.diffattn_v1_fwd(*self.args(self.t), self.li, out=self.out, workspace=self.fws)
 
@@ -221,6 +233,23 @@ class V1FwdBwd(V1Fwd):
                                 deterministic=self.deterministic)
 
 
+    def oracle_sample(self, big=True):
+        """fp64 oracle forward + backward on a bounded sample: one head of the
+        workload cut to its first n tokens (causal, so a prefix is a
+        self-contained problem)."""
+        from oracle import diffattn_oracle as orc
+        n = 2048 if big else 512
+        names = ("q1", "q2", "k1", "k2", "v", "lq1", "lk1", "lq2", "lk2")
+        ts = {k: (v[0:1, :n, 0:1] if v.dim() == 4 else v).to("cpu", torch.float64).numpy()
+              for k, v in self.t.items()}
+        t0 = time.perf_counter()
+        orc.v1_forward(*(ts[k] for k in names), self.li)
+        orc.v1_backward(*(ts[k] for k in names), self.li, ts["dy"])
+        dt = time.perf_counter() - t0
+        flops = v1_fwd_flops(1, n, 1, self.dqk, self.dv) + v1_bwd_flops(1, n, 1, self.dqk, self.dv)
+        return dt, flops, f"batch 0, head 0, first {n} tokens (fp64 oracle fwd+bwd)"
+
+
 class V1FwdBwdDet(V1FwdBwd):
     name = "v1_fwd_bwd_det"
     desc = ("V1 DiffAttn fwd+bwd bf16 B1 H16 N8192 d_qk128 d_v256 causal, layer 1, "
@@ -268,6 +297,12 @@ class V2Fwd(Workload):
         t = self.t
         self.bd.diffattn_v2_fwd(t["q"], t["k"], t["v"], x=t["x"], w_lambda=t["w_lambda"],
                                 out=self.out, workspace=self.ws)
+
+    def setup_host(self):
+        """Inputs for the oracle legs alone, drawn on the host (see V1Fwd)."""
+        from differential_attention_diff_gb300 import synth
+        self.t = synth.v2_inputs(self.B, self.N, self.h, self.hkv, self.d, self.dm, seed=1003,
+                                 device="cpu", with_dout=True)
 
     def run_dominant(self):
         t = self.t
@@ -398,6 +433,12 @@ class GroupedFwd(Workload):
         self.bd.diffattn_grouped_fwd(t["q"], t["k"], t["v"], self.ratio, x=t["x"], w_lambda=t["w_lambda"],
                                      out=self.out, workspace=self.ws)
 
+    def setup_host(self):
+        """Inputs for the oracle legs alone, drawn on the host (see V1Fwd)."""
+        from differential_attention_diff_gb300 import synth
+        self.t = synth.grouped_inputs(self.B, self.N, self.h, self.ratio, self.hkv, self.d, self.dm, seed=1007,
+                                      device="cpu")
+
     def e2e_inputs(self):
         return dict(self.t)
 
@@ -446,6 +487,13 @@ class V2Decode(Workload):
         t = self.t
         self.bd.diffattn_v2_decode(t["q"], t["k_cache"], t["v_cache"], x=t["x"],
                                    w_lambda=t["w_lambda"], out=self.out, workspace=self.ws)
+
+    def setup_host(self):
+        """Inputs for the oracle legs alone, drawn on the host (see V1Fwd):
+        only the sequence the oracle sample reads (a full 32768-position
+        cache), not all 64."""
+        from differential_attention_diff_gb300 import synth
+        self.t = synth.decode_inputs(1, self.L, self.h, self.hkv, self.d, self.dm, seed=1004, device="cpu")
 
     # end to end: the KV cache is the model's resident state; each step
     # uploads the new tokens' queries and gate inputs and reads the output
@@ -500,6 +548,14 @@ class V1Decode(Workload):
         self.bd.diffattn_v1_decode(t["q1"], t["q2"], t["k1_cache"], t["k2_cache"], t["v_cache"],
                                    t["lq1"], t["lk1"], t["lq2"], t["lk2"], self.li, out=self.out,
                                    workspace=self.ws)
+
+    def setup_host(self):
+        """Inputs for the oracle legs alone, drawn on the host (see V1Fwd):
+        only the sequence the oracle sample reads."""
+        from differential_attention_diff_gb300 import synth
+        from oracle import diffattn_oracle as orc
+        self.t = synth.v1_decode_inputs(1, self.L, self.H, self.dqk, self.dv, seed=1006, device="cpu")
+        self.li = float(np.float32(orc.lambda_init(self.layer)))
 
     RESIDENT = ("k1_cache", "k2_cache", "v_cache", "seqlens")
 
@@ -894,21 +950,23 @@ def run_ours(args, ws, rank, local):
 
 
 def run_reference(args, ws, rank):
-    """Reference arm: the fp64 CPU oracle on a bounded sample of the same
-    workload, on the host cores (rank 0 only)."""
+    """Reference arm: the fp64 CPU oracle, timed as it stands on the host
+    cores, on the same bounded sample of the same workload as `cpu_baseline`
+    (rank 0 only; other ranks exit without work).  It loads nothing of the
+    library: inputs are drawn on the host by `synth` and lambda_init comes
+    from the oracle."""
     if rank != 0:
         return
     main = {**WORKLOADS, **PROFILE_ONLY}[args.workload]()
-    dev = "cuda" if torch.cuda.is_available() else "cpu"
-    main.setup(dev) if dev == "cuda" else None
-    if dev != "cuda":
-        print(json.dumps({"impl": "reference", "unavailable": "needs the GPU to draw inputs"}))
+    if not hasattr(main, "oracle_sample"):
+        print(json.dumps({"impl": "reference", "unavailable": f"no oracle sample for {main.name}"}))
         return
+    main.setup_host()
     for _ in range(args.warmup):
-        main.oracle_sample(big=False)
+        main.oracle_sample()
     secs, work, sample = 0.0, 0.0, ""
     for _ in range(args.steps):
-        dt, w, sample = main.oracle_sample(big=False)
+        dt, w, sample = main.oracle_sample()
         secs += dt
         work += w
     ms = secs * 1e3 / args.steps

@@ -49,3 +49,27 @@ def test_two_rank_gloo_max_time_and_summed_work():
     t, value = out[0]
     assert t == pytest.approx(20.0)          # the slowest rank: 80 ms / 4 steps
     assert value == pytest.approx(100.0)     # 2 ranks x 1 TFLOP per 20 ms step
+
+
+def test_reference_arm_loads_no_library():
+    """The reference arm (the fp64 oracle on the host cores) draws its inputs
+    with `synth` on the host and takes lambda_init from the oracle: it runs
+    without a GPU and never loads the CUDA library (checked in a fresh
+    process, whose mapped files must not include it)."""
+    import json
+    import subprocess
+    import sys
+
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    code = ("import json, types, bench\n"
+            "args = types.SimpleNamespace(workload='v1_fwd_f32', steps=2, warmup=1)\n"
+            "bench.run_reference(args, 1, 0)\n"
+            "from differential_attention_diff_gb300 import binding\n"
+            "maps = open('/proc/self/maps').read()\n"
+            "print(json.dumps({'lib': binding._lib is not None, 'mapped': 'libdiffattn' in maps}))\n")
+    out = subprocess.run([sys.executable, "-c", code], cwd=root, capture_output=True, text=True,
+                         timeout=300, check=True).stdout.strip().splitlines()
+    line, probe = json.loads(out[-2]), json.loads(out[-1])
+    assert line["impl"] == "reference" and line["value"] > 0
+    assert line["cpu_baseline"]["sample"]
+    assert probe == {"lib": False, "mapped": False}
