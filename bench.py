@@ -463,6 +463,84 @@ class GroupedFwd(Workload):
         return dt, flops, f"batch 0, group 0 ({self.ratio + 1} query heads), {len(rows)} seeded rows (gate included)"
 
 
+class GroupedFwdBwd(GroupedFwd):
+    name = "grouped_fwd_bwd"
+    desc = ("Grouped DiffAttn 3:1 fwd+bwd bf16 B2 N8192, 64 query heads = 16 x (3 signal + 1 noise), 8 kv heads, "
+            "d128 causal, gate from X[2,8192,4096]; grads of q, k, v, X, W_lambda")
+    launches = None
+
+    def work(self):
+        Hq = self.h // self.ratio * (self.ratio + 1)
+        return v2_fwd_flops(self.B, self.N, Hq // 2, self.d) + v2_bwd_flops(self.B, self.N, Hq // 2, self.d)
+
+    def dominant_work(self):
+        Hq = self.h // self.ratio * (self.ratio + 1)
+        return v2_bwd_flops(self.B, self.N, Hq // 2, self.d)
+
+    def setup(self, dev):
+        super().setup(dev)
+        t = self.t
+        g = torch.Generator(device=dev).manual_seed(1008)
+        t["dout"] = torch.randn((self.B, self.N, self.h, self.d), generator=g, device=dev).to(torch.bfloat16)
+        Hq = self.h // self.ratio * (self.ratio + 1)
+        self.saves = dict(o_heads=torch.empty((self.B, self.N, Hq, self.d), dtype=torch.bfloat16, device=dev),
+                          lse=torch.empty((self.B, Hq, self.N), dtype=torch.float32, device=dev))
+        need = self.bd.load().diffattn_grouped_fwd_workspace_size(self.B, self.N, self.h, self.ratio, self.d, 0, 1)
+        self.ws = torch.empty((need,), dtype=torch.uint8, device=dev)
+        self._fwd(t)
+        need = self.bd.diffattn_grouped_bwd_workspace_size(self.B, self.N, self.h, self.ratio, self.dm)
+        self.bws = torch.empty((need,), dtype=torch.uint8, device=dev)
+        self.grads = self.bd.diffattn_grouped_bwd(t["q"], t["k"], t["v"], t["dout"], self.saves, self.ratio,
+                                                  x=t["x"], w_lambda=t["w_lambda"], workspace=self.bws)
+
+    def _fwd(self, t):
+        self.bd.diffattn_grouped_fwd(t["q"], t["k"], t["v"], self.ratio, x=t["x"], w_lambda=t["w_lambda"],
+                                     out=self.out, o_heads=self.saves["o_heads"], lse=self.saves["lse"],
+                                     workspace=self.ws)
+
+    def _bwd(self, t, grads):
+        self.bd.diffattn_grouped_bwd(t["q"], t["k"], t["v"], t["dout"], self.saves, self.ratio, x=t["x"],
+                                     w_lambda=t["w_lambda"], grads=grads, workspace=self.bws)
+
+    def run(self):
+        self._fwd(self.t)
+        self._bwd(self.t, self.grads)
+
+    def run_dominant(self):
+        self._bwd(self.t, self.grads)
+
+    def e2e_outputs(self):
+        return [self.grads[n] for n in sorted(self.grads)]
+
+    def e2e_compute(self, d, outs):
+        self._fwd(d)
+        self._bwd(d, dict(zip(sorted(self.grads), outs)))
+
+    def setup_host(self):
+        super().setup_host()
+        g = torch.Generator().manual_seed(1008)
+        self.t["dout"] = torch.randn((self.B, self.N, self.h, self.d), generator=g).to(torch.bfloat16)
+
+    def oracle_sample(self, big=True):
+        """fp64 oracle forward + backward on a bounded sample: one (batch, K/V
+        group) of the workload cut to its first n tokens (causal, so a prefix
+        is a self-contained problem)."""
+        from oracle import diffattn_oracle as orc
+        n = 1024 if big else 256
+        Hq = self.h // self.ratio * (self.ratio + 1)
+        G = Hq // self.hkv
+        hg = G // (self.ratio + 1) * self.ratio  # output heads of the group
+        sl = lambda x: x.to("cpu", torch.float64).numpy()  # noqa: E731
+        t = self.t
+        t0 = time.perf_counter()
+        orc.grouped_backward(sl(t["q"][0:1, :n, 0:G]), sl(t["k"][0:1, :n, 0:1]), sl(t["v"][0:1, :n, 0:1]),
+                             sl(t["x"][0:1, :n]), sl(t["w_lambda"][:, 0:hg]), sl(t["dout"][0:1, :n, 0:hg]),
+                             self.ratio)
+        dt = time.perf_counter() - t0
+        flops = v2_fwd_flops(1, n, G // 2, self.d) + v2_bwd_flops(1, n, G // 2, self.d)
+        return dt, flops, f"batch 0, K/V group 0 ({G} query heads), first {n} tokens (fp64 oracle fwd+bwd)"
+
+
 class V2Decode(Workload):
     name = "v2_decode"
     desc = "V2 decode bf16 B64 cache 32768 8 KV heads 64 query heads d128, gate from X[64,4096]"
@@ -607,7 +685,7 @@ class V1DecodeSmall(V1Decode):
 
 
 WORKLOADS = {w.name: w for w in (V1Fwd, V1FwdF32, V2Fwd, V2Decode, V1FwdBwd, V1FwdBwdDet, V2FwdBwd,
-                                 V1Decode, GroupedFwd)}
+                                 V1Decode, GroupedFwd, GroupedFwdBwd)}
 PROFILE_ONLY = {V2DecodeSmall.name: V2DecodeSmall, V2FwdBwdSmall.name: V2FwdBwdSmall,
                 V1DecodeSmall.name: V1DecodeSmall}
 
@@ -623,6 +701,7 @@ KERNEL_SOURCES = {
     "v2_fwd_bwd": ("v2_bwd.cu", "softmax.cuh", "tma.cuh", "common.cuh"),
     "v1_decode": ("v1_decode.cu", "common.cuh"),
     "grouped_fwd": ("v2_fwd.cu", "grouped.cu", "softmax.cuh", "tma.cuh", "common.cuh"),
+    "grouped_fwd_bwd": ("v2_bwd.cu", "softmax.cuh", "tma.cuh", "common.cuh"),
 }
 
 

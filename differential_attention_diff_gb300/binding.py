@@ -39,6 +39,8 @@ EXPORTS = (
     "diffattn_v2_bwd_workspace_size",
     "diffattn_grouped_fwd",
     "diffattn_grouped_fwd_workspace_size",
+    "diffattn_grouped_bwd",
+    "diffattn_grouped_bwd_workspace_size",
     "diffattn_v2_gate",
     "diffattn_v2_fwd",
     "diffattn_v2_fwd_workspace_size",
@@ -131,6 +133,16 @@ class da_v2_bwd_params(C.Structure):
                 ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t)]
 
 
+class da_grouped_bwd_params(C.Structure):
+    _fields_ = [("B", C.c_int), ("N", C.c_int), ("h", C.c_int), ("ratio", C.c_int), ("h_kv", C.c_int),
+                ("d", C.c_int), ("d_model", C.c_int), ("causal", C.c_int), ("softmax_scale", C.c_float),
+                ("q", da_t4), ("k", da_t4), ("v", da_t4), ("gate", C.c_void_p), ("x", C.c_void_p),
+                ("w_lambda", C.c_void_p), ("o_heads", da_t4), ("lse", C.c_void_p), ("dout", da_t4),
+                ("dq", da_t4), ("dk", da_t4), ("dv", da_t4), ("dgate_logit", C.c_void_p),
+                ("dx", C.c_void_p), ("dw_lambda", C.c_void_p),
+                ("workspace", C.c_void_p), ("workspace_bytes", C.c_size_t)]
+
+
 class da_v2_decode_params(C.Structure):
     _fields_ = [("B", C.c_int), ("h", C.c_int), ("h_kv", C.c_int), ("d", C.c_int),
                 ("L_max", C.c_int), ("d_model", C.c_int), ("softmax_scale", C.c_float),
@@ -164,6 +176,7 @@ def load(path: str = LIB_PATH):
                          ("diffattn_v2_gate", da_v2_gate_params), ("diffattn_v2_fwd", da_v2_fwd_params),
                          ("diffattn_v2_bwd", da_v2_bwd_params), ("diffattn_v1_decode", da_v1_decode_params),
                          ("diffattn_grouped_fwd", da_grouped_fwd_params),
+                         ("diffattn_grouped_bwd", da_grouped_bwd_params),
                          ("diffattn_v2_decode", da_v2_decode_params),
                          ("diffattn_v2_decode_noalloc", da_v2_decode_params)):
             f = getattr(lib, name)
@@ -181,6 +194,8 @@ def load(path: str = LIB_PATH):
         lib.diffattn_v1_decode_workspace_size.argtypes = [C.c_int] * 5
         lib.diffattn_grouped_fwd_workspace_size.restype = C.c_size_t
         lib.diffattn_grouped_fwd_workspace_size.argtypes = [C.c_int] * 7
+        lib.diffattn_grouped_bwd_workspace_size.restype = C.c_size_t
+        lib.diffattn_grouped_bwd_workspace_size.argtypes = [C.c_int] * 5
         lib.diffattn_v2_bwd_workspace_size.restype = C.c_size_t
         lib.diffattn_v2_bwd_workspace_size.argtypes = [C.c_int] * 4
         lib.diffattn_v2_decode_num_splits.restype = C.c_int
@@ -433,6 +448,47 @@ def diffattn_v2_bwd(q, k, v, dout, saves, *, gate=None, x=None, w_lambda=None, g
         _ptr(grads.get("dx")), _ptr(grads.get("dw")), workspace.data_ptr(),
         workspace.numel() * workspace.element_size())
     _check(lib.diffattn_v2_bwd(C.byref(p), _stream(stream)), "diffattn_v2_bwd")
+    return grads
+
+
+def diffattn_grouped_bwd_workspace_size(B, N, h, ratio, d_model=0) -> int:
+    return int(load().diffattn_grouped_bwd_workspace_size(B, N, h, ratio, d_model))
+
+
+def diffattn_grouped_bwd(q, k, v, dout, saves, ratio, *, gate=None, x=None, w_lambda=None, grads=None,
+                         want_dx=None, want_dw=None, want_dz=False, causal=True, softmax_scale=0.0,
+                         workspace=None, stream=None):
+    """Grouped differential attention backward.  saves: dict(o_heads [B, N, Hq,
+    d] bf16, lse [B, Hq, N] fp32) written by diffattn_grouped_fwd.  Returns
+    dict(dq, dk, dv) plus dx, dw (when x and w_lambda are given, unless
+    want_dx / want_dw say otherwise) and dz (want_dz)."""
+    lib = load()
+    B, N, Hq, d = q.shape
+    h = Hq // (ratio + 1) * ratio
+    hkv = k.shape[2]
+    d_model = 0 if x is None else x.shape[-1]
+    have_xw = x is not None and w_lambda is not None
+    want_dx = have_xw if want_dx is None else want_dx
+    want_dw = have_xw if want_dw is None else want_dw
+    if grads is None:
+        grads = dict(dq=torch.empty_like(q), dk=torch.empty_like(k), dv=torch.empty_like(v))
+        if want_dx:
+            grads["dx"] = torch.empty((B, N, d_model), dtype=q.dtype, device=q.device)
+        if want_dw:
+            grads["dw"] = torch.empty((d_model, h), dtype=torch.float32, device=q.device)
+        if want_dz:
+            grads["dz"] = torch.empty((B, N, h), dtype=torch.float32, device=q.device)
+    need = lib.diffattn_grouped_bwd_workspace_size(B, N, h, ratio,
+                                                   d_model if grads.get("dw") is not None else 0)
+    if workspace is None:
+        workspace = torch.empty((max(need, 1),), dtype=torch.uint8, device=q.device)
+    p = da_grouped_bwd_params(
+        B, N, h, int(ratio), hkv, d, d_model, int(causal), float(softmax_scale), _t4(q), _t4(k), _t4(v),
+        _ptr(gate), _ptr(x), _ptr(w_lambda), _t4(saves["o_heads"]), _ptr(saves["lse"]), _t4(dout),
+        _t4(grads["dq"]), _t4(grads["dk"]), _t4(grads["dv"]), _ptr(grads.get("dz")),
+        _ptr(grads.get("dx")), _ptr(grads.get("dw")), workspace.data_ptr(),
+        workspace.numel() * workspace.element_size())
+    _check(lib.diffattn_grouped_bwd(C.byref(p), _stream(stream)), "diffattn_grouped_bwd")
     return grads
 
 

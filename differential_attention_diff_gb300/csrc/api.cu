@@ -387,7 +387,7 @@ da_status diffattn_v2_bwd(const da_v2_bwd_params* p, void* stream) {
   da::V2BwdArgs a{p->B, p->N, p->h, p->h_kv, p->d, p->d_model, p->causal, scale,
                   p->q, p->k, p->v, p->o_heads, p->dout, p->dq, p->dk, p->dv,
                   p->gate, p->lse, p->x, p->w_lambda, p->dgate_logit, p->dx, p->dw_lambda,
-                  p->workspace, p->workspace_bytes, d.status, d.num_sms};
+                  p->workspace, p->workspace_bytes, d.status, d.num_sms, 1, p->h};
   return cuda_status(da::launch_v2_bwd(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -508,6 +508,53 @@ da_status diffattn_grouped_fwd(const da_grouped_fwd_params* p, void* stream) {
   if (da::launch_v2_fwd(fa, s) != cudaSuccess) return DA_ERR_CUDA;
   da::GroupedArgs ca{p->B, p->N, p->h, p->ratio, p->d, heads, gate, p->out};
   return cuda_status(da::launch_grouped_combine(ca, s));
+}
+
+// ------------------------------------------------------------ grouped bwd ----
+size_t diffattn_grouped_bwd_workspace_size(int B, int N, int h, int ratio, int d_model) {
+  if (B <= 0 || N <= 0 || h <= 0 || ratio <= 0 || h % ratio) return 0;
+  const int Hq = h / ratio * (ratio + 1);
+  if (Hq % 2) return 0;
+  return da::grouped_bwd_workspace_bytes(B, N, Hq / 2, h, d_model > 0 ? d_model : 0);
+}
+
+da_status diffattn_grouped_bwd(const da_grouped_bwd_params* p, void* stream) {
+  if (p == nullptr) return DA_ERR_INVALID_ARG;
+  if (p->B < 0 || p->N < 0 || p->h <= 0 || p->ratio <= 0 || p->h_kv <= 0 || p->d <= 0)
+    return DA_ERR_INVALID_ARG;
+  if (p->h % p->ratio) return DA_ERR_INVALID_ARG;
+  const int Hq = p->h / p->ratio * (p->ratio + 1);
+  if (Hq % p->h_kv) return DA_ERR_INVALID_ARG;
+  const int G = Hq / p->h_kv;
+  if (G % (p->ratio + 1)) return DA_ERR_INVALID_ARG;  // a group must sit in one K/V group
+  if (p->B == 0 || p->N == 0) return DA_OK;
+  if ((p->d != 64 && p->d != 128) || (G % 2)) return DA_ERR_UNSUPPORTED;
+  for (const da_t4* t : {&p->q, &p->k, &p->v, &p->o_heads, &p->dout, &p->dq, &p->dk, &p->dv})
+    if (check_t4(*t, DA_BF16) != DA_OK) return DA_ERR_INVALID_ARG;
+  if (p->lse == nullptr || !aligned(p->lse, 4)) return DA_ERR_INVALID_ARG;
+  const bool need_xw = p->gate == nullptr || p->dx != nullptr || p->dw_lambda != nullptr;
+  if (need_xw) {
+    if (!p->x || !p->w_lambda || p->d_model <= 0) return DA_ERR_INVALID_ARG;
+    if (!aligned(p->x, 16) || !aligned(p->w_lambda, 16)) return DA_ERR_INVALID_ARG;
+    if ((p->d_model % 64) || p->h > 64) return DA_ERR_UNSUPPORTED;
+  }
+  if (p->gate && !aligned(p->gate, 4)) return DA_ERR_INVALID_ARG;
+  if (p->dgate_logit && !aligned(p->dgate_logit, 4)) return DA_ERR_INVALID_ARG;
+  if (p->dx && !aligned(p->dx, 16)) return DA_ERR_INVALID_ARG;
+  if (p->dw_lambda && !aligned(p->dw_lambda, 4)) return DA_ERR_INVALID_ARG;
+  const size_t need = da::grouped_bwd_workspace_bytes(p->B, p->N, Hq / 2, p->h, p->dw_lambda ? p->d_model : 0);
+  if (p->workspace == nullptr || p->workspace_bytes < need || !aligned(p->workspace, 256))
+    return DA_ERR_WORKSPACE;
+  if (!da::tma_available()) return DA_ERR_CUDA;
+  DevInfo d = device_info();
+  if (!d.ok) return DA_ERR_CUDA;
+  const float scale = p->softmax_scale > 0.f ? p->softmax_scale
+                                             : 1.f / std::sqrt(static_cast<float>(p->d));
+  da::V2BwdArgs a{p->B, p->N, Hq / 2, p->h_kv, p->d, p->d_model, p->causal, scale,
+                  p->q, p->k, p->v, p->o_heads, p->dout, p->dq, p->dk, p->dv,
+                  p->gate, p->lse, p->x, p->w_lambda, p->dgate_logit, p->dx, p->dw_lambda,
+                  p->workspace, p->workspace_bytes, d.status, d.num_sms, p->ratio, p->h};
+  return cuda_status(da::launch_v2_bwd(a, static_cast<cudaStream_t>(stream)));
 }
 
 }  // extern "C"

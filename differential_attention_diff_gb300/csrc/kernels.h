@@ -108,8 +108,16 @@ struct V2BwdArgs {
   size_t workspace_bytes;
   uint32_t* status;
   int num_sms;
+  // Grouped differential attention (ratio >= 2): the 2h query heads come in
+  // groups of `ratio` signal heads and one noise head; dout, gate, dz, w and
+  // dw have h_out = 2h ratio / (ratio + 1) output heads.  ratio <= 1 is V2
+  // (h_out = h, even/odd pairs).
+  int ratio;
+  int h_out;
 };
 size_t v2_bwd_workspace_bytes(int B, int N, int h, int d_model);
+// grouped: h_attn = Hq / 2 (half the query heads), h_out = the output heads
+size_t grouped_bwd_workspace_bytes(int B, int N, int h_attn, int h_out, int d_model);
 cudaError_t launch_v2_bwd(const V2BwdArgs& a, cudaStream_t s);
 
 // ---- V1 forward, bf16, tcgen05 ---------------------------------------------

@@ -49,6 +49,15 @@
 //       dK through TMEM.
 // Every mbarrier wait is bounded (about 2 s); on expiry the kernel records
 // DA_ERR_TIMEOUT, raises an abort flag that the other roles see, and leaves.
+//
+// Grouped differential attention (the 3:1 / 4:1 signal:noise follow-up named
+// in "Differential Transformer | ICLR 2025 Oral", "같은 문제, 다른 접근", read
+// in the V2 form): the query heads come in groups of r signal heads and one
+// noise head, out[t, p] = O[t, signal(p)] - g[t, p] O[t, noise(p)].  Its
+// chain rule differs from V2's only in the preprocess: dO of signal head p is
+// dOut_p itself, dO of a group's noise head is -sum_p g_p dOut_p (rounded to
+// bf16 once), dz_p = -<dOut_p, O_noise> g_p (1 - g_p); the main kernel, the
+// finalize and the gate-projection gradients are shared (r = 1 is V2).
 #include <type_traits>
 
 #include "kernels.h"
@@ -141,19 +150,21 @@ __device__ __forceinline__ void bulk_load(uint32_t dst, const void* src, uint32_
 constexpr int kDwChunk = 1024;  // tokens per dW partial sum
 
 struct BwdWs {
-  __nv_bfloat16* dodd;  // [B, N, h, d]  dO of the odd heads = -g G (room for d = 128)
+  __nv_bfloat16* dodd;  // [B, N, h, d]  dO of the odd heads = -g G (room for d = 128);
+                        // grouped: dO of the noise heads [B, N, 2h / (r + 1), d]
   float* lse2;          // [B, 2h, Npad]   LSE * log2 e; +inf in padding rows
   float* D;             // [B, 2h, Npad]
   float* dq;            // [B, N, 2h, d] fp32 accumulators (room for d = 128)
-  float* gate;          // [B, N, h]  when computed here
-  float* dz;            // [B, N, h]  when the caller keeps none
-  float* dw_part;       // [chunks, d_model, h]
+  float* gate;          // [B, N, h_out]  when computed here
+  float* dz;            // [B, N, h_out]  when the caller keeps none
+  float* dw_part;       // [chunks, d_model, h_out]
   int npad, chunks;
 };
 
 size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
 
-BwdWs carve(void* base, int B, int N, int h, int d_model, size_t* total) {
+// h: half the query heads (V2: the pairs); h_out: the output heads (V2: h)
+BwdWs carve(void* base, int B, int N, int h, int h_out, int d_model, size_t* total) {
   BwdWs w;
   w.npad = (N + kQT - 1) / kQT * kQT;
   const long long T = static_cast<long long>(B) * N;
@@ -171,10 +182,10 @@ BwdWs carve(void* base, int B, int N, int h, int d_model, size_t* total) {
   w.lse2 = reinterpret_cast<float*>(take(srow * 4));
   w.D = reinterpret_cast<float*>(take(srow * 4));
   w.dq = reinterpret_cast<float*>(take(tok * 2 * h * kD * 4));
-  w.gate = reinterpret_cast<float*>(take(tok * h * 4));
-  w.dz = reinterpret_cast<float*>(take(tok * h * 4));
+  w.gate = reinterpret_cast<float*>(take(tok * h_out * 4));
+  w.dz = reinterpret_cast<float*>(take(tok * h_out * 4));
   w.dw_part = reinterpret_cast<float*>(
-      take(d_model > 0 ? static_cast<size_t>(w.chunks) * d_model * h * 4 : 0));
+      take(d_model > 0 ? static_cast<size_t>(w.chunks) * d_model * h_out * 4 : 0));
   if (total) *total = off;
   return w;
 }
@@ -275,6 +286,101 @@ v2_bwd_pre_kernel(V2BwdArgs a, BwdWs w, const float* __restrict__ gate, float* _
   }
 }
 
+// Grouped: one warp per (token, group of r signal heads + 1 noise head);
+// lane = D / 32 consecutive features.  Signal head i of group gi is query head
+// gi (r+1) + i and output head p = gi r + i; its dO is dOut_p (read by the main
+// kernel directly), D = <dOut_p, O_i>, dz_p = -<dOut_p, O_noise> g_p (1 - g_p).
+// The noise head's dO = -sum_i g_p dOut_p is accumulated in fp32, rounded to
+// bf16 once (an MMA operand), and its D taken from the rounded values.
+template <int D>
+__global__ void __launch_bounds__(kPreWarps * 32)
+grouped_bwd_pre_kernel(V2BwdArgs a, BwdWs w, const float* __restrict__ gate, float* __restrict__ dz) {
+  constexpr int kF = D / 32;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int r = a.ratio;
+  const int n_groups = 2 * a.h / (r + 1);
+  const long long row = static_cast<long long>(blockIdx.x) * kPreWarps + warp;  // (b, group, n < npad)
+  const long long total = static_cast<long long>(a.B) * n_groups * w.npad;
+  if (row >= total) return;
+  const int n = static_cast<int>(row % w.npad);
+  const int bg = static_cast<int>(row / w.npad);
+  const int b = bg / n_groups, gi = bg % n_groups;
+  const int hq0 = gi * (r + 1), noise = hq0 + r;
+  auto srow = [&](int j) { return (static_cast<int64_t>(b) * 2 * a.h + j) * w.npad + n; };
+  if (n >= a.N) {
+    if (lane == 0)
+      for (int j = hq0; j <= noise; ++j) {
+        w.lse2[srow(j)] = INFINITY;
+        w.D[srow(j)] = 0.f;
+      }
+    return;
+  }
+  const __nv_bfloat16* ob = static_cast<const __nv_bfloat16*>(a.o_heads.ptr) + b * a.o_heads.sb +
+                            static_cast<int64_t>(n) * a.o_heads.sn + lane * kF;
+  __nv_bfloat16 ne[kF];
+  ld_bf16<kF>(ob + noise * a.o_heads.sh, ne);
+  float on[kF], dn[kF];
+#pragma unroll
+  for (int e = 0; e < kF; ++e) {
+    on[e] = __bfloat162float(ne[e]);
+    dn[e] = 0.f;
+  }
+  const int64_t tok = static_cast<int64_t>(b) * a.N + n;
+  const int64_t qrow0 = tok * 2 * a.h;
+  for (int i = 0; i < r; ++i) {
+    const int p = gi * r + i;
+    const __nv_bfloat16* gp = static_cast<const __nv_bfloat16*>(a.dout.ptr) + b * a.dout.sb +
+                              static_cast<int64_t>(n) * a.dout.sn + p * a.dout.sh + lane * kF;
+    __nv_bfloat16 ge[kF], se[kF];
+    ld_bf16<kF>(gp, ge);
+    ld_bf16<kF>(ob + (hq0 + i) * a.o_heads.sh, se);
+    const float g = gate[tok * a.h_out + p];
+    float ds = 0.f, gn = 0.f;
+#pragma unroll
+    for (int e = 0; e < kF; ++e) {
+      const float gv = __bfloat162float(ge[e]);
+      ds = fmaf(gv, __bfloat162float(se[e]), ds);
+      gn = fmaf(gv, on[e], gn);
+      dn[e] = fmaf(-g, gv, dn[e]);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) {
+      ds += __shfl_xor_sync(0xffffffffu, ds, o);
+      gn += __shfl_xor_sync(0xffffffffu, gn, o);
+    }
+    st_zero_f32<kF>(w.dq + (qrow0 + hq0 + i) * D + lane * kF);
+    if (lane == 0) {
+      const int64_t le = (static_cast<int64_t>(b) * 2 * a.h + hq0 + i) * a.N + n;
+      w.lse2[srow(hq0 + i)] = a.lse[le] * 1.4426950408889634f;
+      w.D[srow(hq0 + i)] = ds;
+      dz[tok * a.h_out + p] = -gn * g * (1.f - g);
+    }
+  }
+  uint32_t pk[kF / 2];
+  float dd = 0.f;
+#pragma unroll
+  for (int e = 0; e < kF; e += 2) {
+    pk[e / 2] = pack_bf16x2(dn[e], dn[e + 1]);
+    const __nv_bfloat162 rr = *reinterpret_cast<const __nv_bfloat162*>(&pk[e / 2]);
+    dd = fmaf(__low2float(rr), on[e], dd);
+    dd = fmaf(__high2float(rr), on[e + 1], dd);
+  }
+#pragma unroll
+  for (int o = 16; o > 0; o >>= 1) dd += __shfl_xor_sync(0xffffffffu, dd, o);
+  __nv_bfloat16* dst = w.dodd + (tok * n_groups + gi) * D + lane * kF;
+  if constexpr (kF == 4) {
+    *reinterpret_cast<uint2*>(dst) = make_uint2(pk[0], pk[1]);
+  } else {
+    *reinterpret_cast<uint32_t*>(dst) = pk[0];
+  }
+  st_zero_f32<kF>(w.dq + (qrow0 + noise) * D + lane * kF);
+  if (lane == 0) {
+    const int64_t le = (static_cast<int64_t>(b) * 2 * a.h + noise) * a.N + n;
+    w.lse2[srow(noise)] = a.lse[le] * 1.4426950408889634f;
+    w.D[srow(noise)] = dd;
+  }
+}
+
 // -------------------------------------------------------------- main -------
 struct Item {
   int b, g, kt, i0, n_ith, n_it;
@@ -321,6 +427,7 @@ v2_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   const int n_kt = (a.N + kKT - 1) / kKT;
   const int n_qt = w.npad / kQT;
   const bool causal = a.causal != 0;
+  const int ratio = a.ratio > 1 ? a.ratio : 1;
   const Item it = item_of(blockIdx.x, n_kt, n_qt, a.B * a.h_kv, a.h_kv, per, G, causal);
 
   if (threadIdx.x == 0) {
@@ -396,10 +503,15 @@ v2_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
         mbar_arrive_expect_tx(bar, 2 * kNB * kBoxQ + 512);
         for (int box = 0; box < kNB; ++box)
           tma_load_4d(sb + kStageQ + box * kBoxQ, &tm_q, bar, box * 64, qh, q0, it.b);
-        // dO of an even head is dOut itself; of an odd head, -g dOut (workspace)
-        const CUtensorMap* tdo = (qh & 1) ? &tm_do : &tm_g;
+        // dO of a signal head (V2: an even head) is dOut itself, at output
+        // head grp r + i; of a noise head (V2: odd), the workspace's
+        // -sum g dOut, at index grp
+        const int grp = qh / (ratio + 1), gsub = qh - grp * (ratio + 1);
+        const bool signal = gsub < ratio;
+        const CUtensorMap* tdo = signal ? &tm_g : &tm_do;
+        const int dsel = signal ? grp * ratio + gsub : grp;
         for (int box = 0; box < kNB; ++box)
-          tma_load_4d(sb + kStageDO + box * kBoxQ, tdo, bar, box * 64, qh >> 1, q0, it.b);
+          tma_load_4d(sb + kStageDO + box * kBoxQ, tdo, bar, box * 64, dsel, q0, it.b);
         const size_t srow = (static_cast<size_t>(it.b) * 2 * a.h + qh) * w.npad + q0;
         const uint32_t lb = sh.base + kOffLse + st * 512;
         bulk_load(lb, w.lse2 + srow, 256, bar);
@@ -858,19 +970,27 @@ template <int D>
 cudaError_t launch_attn(const V2BwdArgs& a, const BwdWs& w, float* dz, cudaStream_t s) {
   const long long T = static_cast<long long>(a.B) * a.N;
   cudaError_t e;
-  const long long pre_rows = static_cast<long long>(a.B) * a.h * w.npad;
-  v2_bwd_pre_kernel<D><<<static_cast<unsigned>((pre_rows + kPreWarps - 1) / kPreWarps), kPreWarps * 32, 0, s>>>(
-      a, w, a.gate, dz);
+  const int ratio = a.ratio > 1 ? a.ratio : 1;
+  const int n_noise = 2 * a.h / (ratio + 1);  // V2: h odd heads
+  if (ratio == 1) {
+    const long long pre_rows = static_cast<long long>(a.B) * a.h * w.npad;
+    v2_bwd_pre_kernel<D><<<static_cast<unsigned>((pre_rows + kPreWarps - 1) / kPreWarps), kPreWarps * 32, 0, s>>>(
+        a, w, a.gate, dz);
+  } else {
+    const long long pre_rows = static_cast<long long>(a.B) * n_noise * w.npad;
+    grouped_bwd_pre_kernel<D><<<static_cast<unsigned>((pre_rows + kPreWarps - 1) / kPreWarps), kPreWarps * 32, 0,
+                                s>>>(a, w, a.gate, dz);
+  }
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
   CUtensorMap tq, tk, tv, tg, tdo, tdq;
-  const da_t4 dot{w.dodd, static_cast<int64_t>(a.N) * a.h * D, static_cast<int64_t>(a.h) * D, D};
+  const da_t4 dot{w.dodd, static_cast<int64_t>(a.N) * n_noise * D, static_cast<int64_t>(n_noise) * D, D};
   if (!encode_tmap_bf16_4d(&tq, a.q, a.B, a.N, 2 * a.h, D, kQT) ||
       !encode_tmap_bf16_4d(&tk, a.k, a.B, a.N, a.h_kv, D, kKT) ||
       !encode_tmap_bf16_4d(&tv, a.v, a.B, a.N, a.h_kv, D, kKT) ||
-      !encode_tmap_bf16_4d(&tg, a.dout, a.B, a.N, a.h, D, kQT) ||
-      !encode_tmap_bf16_4d(&tdo, dot, a.B, a.N, a.h, D, kQT) ||
+      !encode_tmap_bf16_4d(&tg, a.dout, a.B, a.N, a.h_out, D, kQT) ||
+      !encode_tmap_bf16_4d(&tdo, dot, a.B, a.N, n_noise, D, kQT) ||
       !encode_tmap_f32_4d(&tdq, w.dq, a.B, a.N, 2 * a.h, D, kQT))
     return cudaErrorInvalidValue;
   e = cudaFuncSetAttribute(v2_bwd_main_kernel<D>, cudaFuncAttributeMaxDynamicSharedMemorySize, kSmemBytes);
@@ -901,19 +1021,27 @@ cudaError_t launch_attn(const V2BwdArgs& a, const BwdWs& w, float* dz, cudaStrea
 
 size_t v2_bwd_workspace_bytes(int B, int N, int h, int d_model) {
   size_t total = 0;
-  carve(nullptr, B, N, h, d_model, &total);
+  carve(nullptr, B, N, h, h, d_model, &total);
+  return total;
+}
+
+size_t grouped_bwd_workspace_bytes(int B, int N, int h_attn, int h_out, int d_model) {
+  size_t total = 0;
+  carve(nullptr, B, N, h_attn, h_out, d_model, &total);
   return total;
 }
 
 cudaError_t launch_v2_bwd(const V2BwdArgs& a_in, cudaStream_t s) {
   V2BwdArgs a = a_in;
+  if (a.ratio < 1) a.ratio = 1;
+  if (a.ratio == 1) a.h_out = a.h;
   size_t total = 0;
-  const BwdWs w = carve(a.workspace, a.B, a.N, a.h, a.dw ? a.d_model : 0, &total);
+  const BwdWs w = carve(a.workspace, a.B, a.N, a.h, a.h_out, a.dw ? a.d_model : 0, &total);
   if (total > a.workspace_bytes) return cudaErrorInvalidValue;
   const long long T = static_cast<long long>(a.B) * a.N;
   cudaError_t e;
   if (a.gate == nullptr) {
-    GateArgs ga{static_cast<int>(T), a.d_model, a.h, a.x, a.d_model, a.w, w.gate};
+    GateArgs ga{static_cast<int>(T), a.d_model, a.h_out, a.x, a.d_model, a.w, w.gate};
     e = launch_gate(ga, s);
     if (e != cudaSuccess) return e;
     a.gate = w.gate;
@@ -926,18 +1054,19 @@ cudaError_t launch_v2_bwd(const V2BwdArgs& a_in, cudaStream_t s) {
   const int sms = a.num_sms > 0 ? a.num_sms : 148;
 
   if (a.dx) {
-    e = launch_dx(static_cast<int>(T), a.d_model, a.h, dz, a.w, a.dx, s);
+    e = launch_dx(static_cast<int>(T), a.d_model, a.h_out, dz, a.w, a.dx, s);
     if (e != cudaSuccess) return e;
   }
   if (a.dw) {
-    v2_bwd_dw_partial_kernel<<<dim3((a.d_model + kGC - 1) / kGC, w.chunks, (a.h + kGP - 1) / kGP), 256, 0, s>>>(
-        static_cast<int>(T), a.d_model, a.h, dz, static_cast<const __nv_bfloat16*>(a.x), w.dw_part);
+    v2_bwd_dw_partial_kernel<<<dim3((a.d_model + kGC - 1) / kGC, w.chunks, (a.h_out + kGP - 1) / kGP), 256, 0,
+                               s>>>(static_cast<int>(T), a.d_model, a.h_out, dz,
+                                    static_cast<const __nv_bfloat16*>(a.x), w.dw_part);
     e = cudaGetLastError();
     if (e != cudaSuccess) return e;
-    const long long n = static_cast<long long>(a.d_model) * a.h;
+    const long long n = static_cast<long long>(a.d_model) * a.h_out;
     int g2 = static_cast<int>((n + 255) / 256);
     if (g2 > 4 * sms) g2 = 4 * sms;
-    v2_bwd_dw_reduce_kernel<<<g2, 256, 0, s>>>(a.d_model, a.h, w.chunks, w.dw_part, a.dw);
+    v2_bwd_dw_reduce_kernel<<<g2, 256, 0, s>>>(a.d_model, a.h_out, w.chunks, w.dw_part, a.dw);
     e = cudaGetLastError();
   }
   return e;

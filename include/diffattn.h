@@ -339,6 +339,50 @@ size_t diffattn_v2_bwd_workspace_size(int B, int N, int h, int d_model);
 da_status diffattn_v2_bwd(const da_v2_bwd_params* p, void* cuda_stream);
 
 /* ------------------------------------------------------------------------ */
+/* Grouped differential attention, backward: gradients of diffattn_grouped_fwd
+ * (and of the gate projection) given dOut.  The pages state no backward; it
+ * is the chain rule of the grouped forward above.  With r = ratio, output
+ * head p = g r + i reading signal query head g (r+1) + i and noise query head
+ * g (r+1) + r, gate[t, p] = sigmoid(z), G = dOut[t, p]:
+ *   dO_signal(p) = G_p,  dO_noise(g) = -sum_i gate[t, g r + i] G_{g r + i}
+ *   dz_p = -<G_p, O_noise(g)> gate (1 - gate),  dW_lambda = X^T dz,  dX = dz W_lambda^T
+ *   per query head j reading K/V head c: as in diffattn_v2_bwd.
+ * With ratio 1 this is diffattn_v2_bwd's result.
+ * Inputs: the forward's q, k, v, the gate source (gate fp32 [B, N, h], or x
+ * and w_lambda [d_model, h] when gate == NULL), the forward's saves o_heads
+ * (bf16 [B, N, Hq, d], required here) and lse (fp32 [B, Hq, N]), and dout
+ * (bf16 [B, N, h, d]).  Outputs (overwritten): dq [B, N, Hq, d], dk, dv
+ * [B, N, h_kv, d], bf16.  Optional outputs (NULL = not computed):
+ * dgate_logit fp32 [B, N, h] (dz); dx bf16 [B, N, d_model] and dw_lambda fp32
+ * [d_model, h] (these need x and w_lambda).  Supported: the shapes of
+ * diffattn_grouped_fwd; d_model % 64 == 0 and h <= 64 where x / w_lambda are
+ * used.  workspace: diffattn_grouped_bwd_workspace_size(B, N, h, ratio,
+ * d_model) bytes (d_model = 0 covers calls without dw_lambda), 256-byte
+ * aligned, contents on entry irrelevant.  dQ is accumulated with fp32
+ * reduce-adds (not bitwise reproducible); every other output is. */
+typedef struct {
+  int B, N, h, ratio, h_kv, d, d_model;
+  int causal;
+  float softmax_scale;   /* <= 0 selects 1/sqrt(d) */
+  da_t4 q, k, v;
+  const float* gate;
+  const void* x;
+  const void* w_lambda;
+  da_t4 o_heads;
+  const float* lse;
+  da_t4 dout;
+  da_t4 dq, dk, dv;
+  float* dgate_logit;
+  void* dx;
+  float* dw_lambda;
+  void* workspace;
+  size_t workspace_bytes;
+} da_grouped_bwd_params;
+
+size_t diffattn_grouped_bwd_workspace_size(int B, int N, int h, int ratio, int d_model);
+da_status diffattn_grouped_bwd(const da_grouped_bwd_params* p, void* cuda_stream);
+
+/* ------------------------------------------------------------------------ */
 /* V2 decode.  [P1] "V2로의 진화" and [P2] §2: one new token per sequence
  * attends over its KV cache; the KV heads and cache are those of a standard
  * GQA model (only the query heads double), so the step is bound by reading

@@ -88,3 +88,47 @@ def rounded_backward_v2(f, fwd, gate, scale=None, rnd=bf16, causal=True):
     for n in ("dq", "dk", "dv"):
         out[n] = rnd(out[n])
     return out
+
+
+def rounded_backward_grouped(f, fwd, gate, ratio, scale=None, rnd=bf16, causal=True):
+    """The grouped backward with its bf16 storage points: the saved per-head
+    outputs O_j, each noise head's dO = -sum_i g_i dOut_i (summed exactly,
+    rounded once), the P and dS tiles, and the bf16 gradient outputs.  f: fp64
+    inputs (q, k, v, x, w_lambda, dout); fwd: the oracle's grouped forward on
+    them; gate: fp64 [B, N, h].  ratio 1 gives ``rounded_backward_v2``."""
+    q, k, v, dout = f["q"], f["k"], f["v"], f["dout"]
+    B, N, Hq, d = q.shape
+    group = Hq // k.shape[2]
+    n_groups = Hq // (ratio + 1)
+    s = 1.0 / np.sqrt(d) if scale is None else scale
+    o = rnd(fwd["o"])
+    do = np.zeros_like(o)
+    dz = np.zeros_like(gate)
+    for gi in range(n_groups):
+        noise = gi * (ratio + 1) + ratio
+        acc = np.zeros_like(dout[:, :, 0])
+        for i in range(ratio):
+            p = gi * ratio + i
+            do[:, :, gi * (ratio + 1) + i] = dout[:, :, p]
+            acc -= gate[:, :, p, None] * dout[:, :, p]
+            dz[:, :, p] = -(dout[:, :, p] * o[:, :, noise]).sum(-1) * gate[:, :, p] * (1.0 - gate[:, :, p])
+        do[:, :, noise] = rnd(acc)
+    out = dict(dq=np.zeros_like(q), dk=np.zeros_like(k), dv=np.zeros_like(v))
+    for b in range(B):
+        for j in range(Hq):
+            c = j // group
+            dO = do[b, :, j]
+            D = (dO * o[b, :, j]).sum(1)
+            P = np.exp(s * q[b, :, j] @ k[b, :, c].T - fwd["lse"][b, j][:, None])
+            if causal:
+                P = np.tril(P)
+            dS = rnd(s * P * (dO @ v[b, :, c].T - D[:, None]))
+            out["dq"][b, :, j] = dS @ k[b, :, c]
+            out["dk"][b, :, c] += dS.T @ q[b, :, j]
+            out["dv"][b, :, c] += rnd(P).T @ dO
+    out["dz"] = dz
+    out["dx"] = rnd(dz @ f["w_lambda"].T)
+    out["dw"] = np.einsum("btk,btp->kp", f["x"], dz)
+    for n in ("dq", "dk", "dv"):
+        out[n] = rnd(out[n])
+    return out

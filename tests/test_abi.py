@@ -46,7 +46,7 @@ def test_status_strings(lib):
 def test_null_params_rejected(lib):
     for name in ("diffattn_v1_fwd", "diffattn_v1_bwd", "diffattn_v2_gate", "diffattn_v2_fwd",
                  "diffattn_v2_decode", "diffattn_v2_decode_noalloc", "diffattn_v2_bwd", "diffattn_v1_decode",
-                 "diffattn_grouped_fwd"):
+                 "diffattn_grouped_fwd", "diffattn_grouped_bwd"):
         assert getattr(lib, name)(None, None) == bd.DA_ERR_INVALID_ARG, name
 
 
@@ -281,3 +281,36 @@ def test_v2_bwd_argument_checks(lib):
     assert f(with_(dx=fake), None) == bd.DA_ERR_INVALID_ARG      # dX needs x and w_lambda
     assert f(with_(), None) == bd.DA_ERR_WORKSPACE
     assert f(with_(N=0), None) == bd.DA_OK                       # empty problem
+
+
+def test_grouped_bwd_checks_and_workspace(lib):
+    """Grouped backward: the forward's shape rules, its saves required, and at
+    ratio 1 the same workspace as the V2 backward."""
+    p = bd.da_grouped_bwd_params()
+    p.B, p.N, p.h, p.ratio, p.h_kv, p.d, p.d_model, p.causal = 1, 256, 6, 3, 2, 128, 0, 1
+    fake = 1 << 20
+    for n in ("q", "k", "v", "o_heads", "dout", "dq", "dk", "dv"):
+        setattr(p, n, bd.da_t4(fake, 256 * 8 * 128, 8 * 128, 128))
+    p.gate = p.lse = fake
+    f = lib.diffattn_grouped_bwd
+    assert f(C.byref(p), None) == bd.DA_ERR_WORKSPACE  # valid shapes; no workspace
+    bad = bd.da_grouped_bwd_params.from_buffer_copy(p)
+    bad.h = 5  # not a multiple of the ratio
+    assert f(C.byref(bad), None) == bd.DA_ERR_INVALID_ARG
+    bad = bd.da_grouped_bwd_params.from_buffer_copy(p)
+    bad.h_kv = 3  # 8 query heads do not split into 3 K/V groups
+    assert f(C.byref(bad), None) == bd.DA_ERR_INVALID_ARG
+    bad = bd.da_grouped_bwd_params.from_buffer_copy(p)
+    bad.d = 96
+    assert f(C.byref(bad), None) == bd.DA_ERR_UNSUPPORTED
+    bad = bd.da_grouped_bwd_params.from_buffer_copy(p)
+    bad.lse = None  # the forward's saves are required
+    assert f(C.byref(bad), None) == bd.DA_ERR_INVALID_ARG
+    bad = bd.da_grouped_bwd_params.from_buffer_copy(p)
+    bad.gate = None  # the gate source: neither gate nor x and w_lambda
+    assert f(C.byref(bad), None) == bd.DA_ERR_INVALID_ARG
+    for B, N, h, dm in ((2, 8192, 32, 4096), (1, 300, 4, 0)):
+        assert (lib.diffattn_grouped_bwd_workspace_size(B, N, h, 1, dm) ==
+                lib.diffattn_v2_bwd_workspace_size(B, N, h, dm))
+    assert lib.diffattn_grouped_bwd_workspace_size(2, 8192, 48, 3, 4096) > 0
+    assert lib.diffattn_grouped_bwd_workspace_size(2, 8192, 47, 3, 4096) == 0

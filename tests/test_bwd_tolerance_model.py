@@ -19,7 +19,7 @@ import numpy as np
 import torch
 
 from differential_attention_diff_gb300 import synth
-from bf16_model import rounded_backward, rounded_backward_v2
+from bf16_model import rounded_backward, rounded_backward_grouped, rounded_backward_v2
 from oracle import diffattn_oracle as orc
 
 
@@ -55,3 +55,30 @@ def test_v2_rounding_model_is_the_chain_rule_and_sets_the_tolerance():
     for n in ("dq", "dk", "dv", "dz", "dx", "dw"):
         fro = float(np.linalg.norm(got[n] - ref[n]) / np.linalg.norm(ref[n]))
         assert fro < 0.5 * 1.5e-2, (n, fro)
+
+
+def test_grouped_rounding_model_is_the_chain_rule_and_sets_the_tolerance():
+    """The grouped model without rounding reproduces the oracle's grouped
+    backward (it rounds the right quantities of the right formula), equals the
+    V2 model at ratio 1, and with bf16 rounding keeps its Frobenius error well
+    under the GPU bars."""
+    t = synth.grouped_inputs(1, 150, 6, 3, 1, 64, 64, seed=5204, device="cpu")
+    t["dout"] = torch.randn((1, 150, 6, 64), generator=torch.Generator().manual_seed(5205)).to(torch.bfloat16)
+    f = {k: v.to(torch.float64).numpy() for k, v in t.items()}
+    ref = orc.grouped_backward(f["q"], f["k"], f["v"], f["x"], f["w_lambda"], f["dout"], 3)
+    fwd = orc.grouped_forward(f["q"], f["k"], f["v"], ref["gate"], 3)
+    exact = rounded_backward_grouped(f, fwd, ref["gate"], 3, rnd=lambda a: a)
+    for n in ("dq", "dk", "dv", "dz", "dx", "dw"):
+        np.testing.assert_allclose(exact[n], ref[n], rtol=1e-10, atol=1e-12 * np.abs(ref[n]).max())
+    got = rounded_backward_grouped(f, fwd, ref["gate"], 3)
+    for n in ("dq", "dk", "dv", "dz", "dx", "dw"):
+        fro = float(np.linalg.norm(got[n] - ref[n]) / np.linalg.norm(ref[n]))
+        assert fro < 0.5 * 1.5e-2, (n, fro)
+    t2 = synth.v2_inputs(1, 70, 2, 1, 64, 64, seed=5206, device="cpu", with_dout=True)
+    f2 = {k: v.to(torch.float64).numpy() for k, v in t2.items()}
+    ref2 = orc.v2_backward(f2["q"], f2["k"], f2["v"], f2["x"], f2["w_lambda"], f2["dout"])
+    fwd2 = orc.v2_forward(f2["q"], f2["k"], f2["v"], ref2["gate"])
+    a = rounded_backward_grouped(f2, fwd2, ref2["gate"], 1)
+    b = rounded_backward_v2(f2, fwd2, ref2["gate"])
+    for n in ("dq", "dk", "dv", "dz", "dx", "dw"):
+        np.testing.assert_allclose(a[n], b[n], rtol=1e-12, atol=1e-12 * np.abs(b[n]).max())
