@@ -130,7 +130,9 @@ da_status diffattn_v2_gate(const da_v2_gate_params* p, void* stream) {
     return DA_ERR_INVALID_ARG;
   if (p->x_stride < p->d_model || (p->x_stride % 8)) return DA_ERR_INVALID_ARG;
   if ((p->d_model % 64) || p->h > 64) return DA_ERR_UNSUPPORTED;
-  da::GateArgs a{p->T, p->d_model, p->h, p->x, p->x_stride, p->w_lambda, p->gate};
+  DevInfo d = device_info();
+  if (!d.ok) return DA_ERR_CUDA;
+  da::GateArgs a{p->T, p->d_model, p->h, p->x, p->x_stride, p->w_lambda, p->gate, d.status};
   return cuda_status(da::launch_gate(a, static_cast<cudaStream_t>(stream)));
 }
 
@@ -210,7 +212,7 @@ da_status diffattn_v2_decode(const da_v2_decode_params* p, void* stream) {
   const float* gate = p->gate;
   if (gate == nullptr) {
     float* g = reinterpret_cast<float*>(ws + align256(po) + align256(pml));
-    da::GateArgs ga{p->B, p->d_model, p->h, p->x, p->d_model, p->w_lambda, g};
+    da::GateArgs ga{p->B, p->d_model, p->h, p->x, p->d_model, p->w_lambda, g, d.status};
     cudaError_t e = da::launch_gate(ga, s);
     if (e != cudaSuccess) return DA_ERR_CUDA;
     gate = g;
@@ -338,7 +340,7 @@ da_status diffattn_v2_fwd(const da_v2_fwd_params* p, void* stream) {
   const float* gate = p->gate;
   if (gate == nullptr) {
     float* g = static_cast<float*>(p->workspace);
-    da::GateArgs ga{p->B * p->N, p->d_model, p->h, p->x, p->d_model, p->w_lambda, g};
+    da::GateArgs ga{p->B * p->N, p->d_model, p->h, p->x, p->d_model, p->w_lambda, g, d.status};
     if (da::launch_gate(ga, s) != cudaSuccess) return DA_ERR_CUDA;
     gate = g;
   }
@@ -490,7 +492,7 @@ da_status diffattn_grouped_fwd(const da_grouped_fwd_params* p, void* stream) {
   size_t off = 0;
   if (gate == nullptr) {
     float* g = reinterpret_cast<float*>(ws);
-    da::GateArgs ga{p->B * p->N, p->d_model, p->h, p->x, p->d_model, p->w_lambda, g};
+    da::GateArgs ga{p->B * p->N, p->d_model, p->h, p->x, p->d_model, p->w_lambda, g, d.status};
     if (da::launch_gate(ga, s) != cudaSuccess) return DA_ERR_CUDA;
     gate = g;
     off = align256(static_cast<size_t>(p->B) * p->N * p->h * sizeof(float));

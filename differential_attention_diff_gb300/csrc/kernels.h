@@ -17,6 +17,7 @@ struct GateArgs {
   int64_t x_stride;
   const void* w;
   float* gate;
+  uint32_t* status;  // device status word for bounded waits (may be null)
 };
 cudaError_t launch_gate(const GateArgs& a, cudaStream_t s);
 

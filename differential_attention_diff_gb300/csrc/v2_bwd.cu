@@ -1041,7 +1041,7 @@ cudaError_t launch_v2_bwd(const V2BwdArgs& a_in, cudaStream_t s) {
   const long long T = static_cast<long long>(a.B) * a.N;
   cudaError_t e;
   if (a.gate == nullptr) {
-    GateArgs ga{static_cast<int>(T), a.d_model, a.h_out, a.x, a.d_model, a.w, w.gate};
+    GateArgs ga{static_cast<int>(T), a.d_model, a.h_out, a.x, a.d_model, a.w, w.gate, a.status};
     e = launch_gate(ga, s);
     if (e != cudaSuccess) return e;
     a.gate = w.gate;

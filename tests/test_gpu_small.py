@@ -42,8 +42,12 @@ def _status_clean():
 
 # ------------------------------------------------------------------ gate ----
 
-@pytest.mark.parametrize("T,dm,h", [(300, 256, 32), (64, 4096, 32), (1, 64, 8), (129, 128, 64)])
+@pytest.mark.parametrize("T,dm,h", [(300, 256, 32), (64, 4096, 32), (1, 64, 8), (129, 128, 64),
+                                    (2433, 256, 8), (5000, 512, 48), (16384, 4096, 32), (7001, 128, 64)])
 def test_gate_parity(T, dm, h):
+    """Few tokens run the cluster-split kernel; 16 or more per SM (with h a
+    multiple of 8) the row-range TMA kernel: ragged per-CTA ranges, h = 8 to
+    64, d_model from 128 to 4096 (the prefill workload's X [16384, 4096])."""
     g = torch.Generator(device="cuda").manual_seed(100 + T)
     x = torch.randn((T, dm), generator=g, device="cuda").to(torch.bfloat16)
     w = (0.02 * torch.randn((dm, h), generator=g, device="cuda")).to(torch.bfloat16)
@@ -51,6 +55,20 @@ def test_gate_parity(T, dm, h):
     torch.cuda.synchronize()
     ref = orc.v2_gate(f64(x), f64(w))
     assert maxdiff(f64(gate), ref) <= 1e-4
+
+
+def test_gate_strided_rows_many_tokens():
+    """X as a strided view (row stride 4096 + 64 elements) on the row-range
+    kernel: the gate of the view equals the gate of a contiguous copy."""
+    g = torch.Generator(device="cuda").manual_seed(7)
+    buf = torch.randn((4000, 4160), generator=g, device="cuda").to(torch.bfloat16)
+    x = buf[:, :4096]
+    w = (0.02 * torch.randn((4096, 32), generator=g, device="cuda")).to(torch.bfloat16)
+    a = bd.diffattn_v2_gate(x, w)
+    b = bd.diffattn_v2_gate(x.contiguous(), w)
+    torch.cuda.synchronize()
+    assert torch.equal(a, b)
+    assert maxdiff(f64(a), orc.v2_gate(f64(x), f64(w))) <= 1e-4
 
 
 # --------------------------------------------------------------- V1 fp32 ----
