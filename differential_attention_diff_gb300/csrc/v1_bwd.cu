@@ -26,15 +26,18 @@
 //     causal):
 //        S^T  = K Q^T          (TMEM, 64 columns)
 //        dP^T = V dO^T         (TMEM, 64 columns)
-//        softmax warps (thread = key row): P = exp2(S^T s log2e - lse2),
-//          dS^T = sigma s P (dP^T - D), Psig^T = sigma P  (sigma = 1 or
-//          -lambda), both as bf16 over the S^T columns just read (TMEM),
-//          dS^T also into shared memory
+//        softmax warps (thread = key row), in two steps so that each overlaps
+//        an MMA: (1) once S^T is in, P = exp2(S^T s log2e - lse2) and
+//          Psig^T = sigma P (sigma = 1 or -lambda) as bf16 over the S^T
+//          columns just read, while dP^T is still being computed;
+//          (2) once dP^T is in, dS^T = sigma s P (dP^T - D) as bf16 over the
+//          rest of the S^T columns and into shared memory, while dV runs
+//        dV  += Psig^T dO      (TMEM, 256 columns; A operand from TMEM),
+//                               issued after step (1)
 //        dQ^T = K^T dS^T       (TMEM, reusing the dP^T columns) -> read by the
 //                               dQ warps, staged in shared memory in two
 //                               halves and added to the fp32 accumulator
 //                               with TMA reduce-adds
-//        dV  += Psig^T dO      (TMEM, 256 columns; A operand from TMEM)
 //        dK  += dS^T Q         (TMEM, 128 columns; A operand from TMEM)
 //     At the end each CTA writes its dK; the dV halves of the two streams are
 //     summed through distributed shared memory and written as bf16;
@@ -84,7 +87,7 @@ constexpr int kOffBar = kOffLse + 1024;
 constexpr int kSmemBytes = kOffBar + 512 + 1024;   // 231936 <= 232448
 
 enum {
-  B_KV = 0, B_QFULL, B_QFULL1, B_QEMPTY, B_QEMPTY1, B_SFULL, B_DPFULL, B_PFULL, B_DQFULL,
+  B_KV = 0, B_QFULL, B_QFULL1, B_QEMPTY, B_QEMPTY1, B_SFULL, B_DPFULL, B_PREADY, B_PFULL, B_DQFULL,
   B_DQFREE, B_ACC, B_RTR, B_DATA, B_STG0, B_STG1, B_FREE0, B_FREE1, B_COUNT
 };
 
@@ -428,6 +431,7 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
     }
     mbar_init(sh.bar(B_SFULL), 1);
     mbar_init(sh.bar(B_DPFULL), 1);
+    mbar_init(sh.bar(B_PREADY), 128);
     mbar_init(sh.bar(B_PFULL), 128);
     mbar_init(sh.bar(B_DQFULL), 1);
     mbar_init(sh.bar(B_DQFREE), 128);
@@ -549,6 +553,14 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
       }
       for (int k = 0; k < it.n_it && ok; ++k) {
         const int ph = k & 1;
+        const uint32_t db = stage(k) + kStageDO, qb = stage(k) + kStageQ;
+        // dV += Psig^T dO as soon as Psig^T is in TMEM (S^T columns 0-31):
+        // it runs while the softmax warps form dS^T
+        if (!wait_bar(sh, sh.bar(B_PREADY), ph, a.status, 0x4106)) { ok = false; break; }
+        tc_fence_after();
+#pragma unroll
+        for (int kk = 0; kk < kQT / 16; ++kk)
+          tc_mma_ts(T_DV, T_S + kk * 8, sdesc_sw128(db + kk * 2048, kBoxQ, 1024), kIdDV, (k > 0 || kk > 0) ? 1u : 0u);
         if (!wait_bar(sh, sh.bar(B_PFULL), ph, a.status, 0x4103)) { ok = false; break; }
         tc_fence_after();
         // dQ^T = K^T dS^T  (into the dP^T columns, already read)
@@ -557,12 +569,7 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
           tc_mma_ss(T_DP, sdesc_sw128(kA + kk * 2048, kBoxK, 1024), sdesc_sw128(dsA + kk * 2048, kBoxQ, 1024),
                     kIdDQ, kk > 0);
         tc_commit(sh.bar(B_DQFULL));
-        // dV += Psig^T dO ; dK += dS^T Q  (Psig^T in S^T columns 0-31, dS^T
-        // in 32-63)
-        const uint32_t db = stage(k) + kStageDO, qb = stage(k) + kStageQ;
-#pragma unroll
-        for (int kk = 0; kk < kQT / 16; ++kk)
-          tc_mma_ts(T_DV, T_S + kk * 8, sdesc_sw128(db + kk * 2048, kBoxQ, 1024), kIdDV, (k > 0 || kk > 0) ? 1u : 0u);
+        // dK += dS^T Q  (dS^T in S^T columns 32-63)
 #pragma unroll
         for (int kk = 0; kk < kQT / 16; ++kk)
           tc_mma_ts(T_DK, T_S + 32 + kk * 8, sdesc_sw128(qb + kk * 2048, kBoxQ, 1024), kIdDK,
@@ -659,7 +666,6 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
       const int ph = k & 1;
       const int q0 = (it.i0 + k) * kQT;
       if (!wait_bar(sh, sh.bar(B_SFULL), ph, a.status, 0x4201)) { ok = false; break; }
-      if (!wait_bar(sh, sh.bar(B_DPFULL), ph, a.status, 0x4202)) { ok = false; break; }
       tc_fence_after();
       const float4* l2v = reinterpret_cast<const float4*>(sh.gen + kOffLse + (k & 1) * 512);
       const float4* ddv = l2v + 16;
@@ -667,20 +673,20 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
       // past N are zero rows of K and V, which give dQ no contribution, and
       // their dK / dV rows are never stored.)
       const bool diag = a.causal && q0 < it.kt * kKT + kKT;
-      uint32_t dkeep[16];  // dS^T of the first half, stored once the second half's S^T is read
+      // (1) P = exp2(S s log2e - lse2), Psig^T = sigma P (bf16) over the
+      //     S^T columns just read; P stays in registers for dS
+      float p[64];
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
-        uint32_t sv[32], dp[32];
+        uint32_t sv[32];
         tmem_ld32(T_S + loff + hf * 32, sv);
-        tmem_ld32(T_DP + loff + hf * 32, dp);
         tmem_ld_wait();
-        uint32_t pw[16], dw[16];
-        auto tile = [&](auto masked) {
+        uint32_t pw[16];
+        auto ptile = [&](auto masked) {
           constexpr bool kMask = decltype(masked)::value;
 #pragma unroll
           for (int q4 = 0; q4 < 8; ++q4) {  // 4 queries at a time
             const float4 lq = l2v[hf * 8 + q4];
-            const float4 dq4 = ddv[hf * 8 + q4];
             const int c = q4 * 4;
             const int qa = q0 + hf * 32 + c;
             const uint64_t x01 = fma_f32x2(f2(__uint_as_float(sv[c]), __uint_as_float(sv[c + 1])), sl2x2,
@@ -695,37 +701,52 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
               if (key > qa + 2) p2 = 0.f;
               if (key > qa + 3) p3 = 0.f;
             }
-            const uint64_t t01 = add_f32x2(f2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), f2(-dq4.x, -dq4.y));
-            const uint64_t t23 =
-                add_f32x2(f2(__uint_as_float(dp[c + 2]), __uint_as_float(dp[c + 3])), f2(-dq4.z, -dq4.w));
-            const uint64_t p01 = f2(p0, p1), p23 = f2(p2, p3);
-            const uint64_t d01 = mul_f32x2(mul_f32x2(t01, p01), sds2);
-            const uint64_t d23 = mul_f32x2(mul_f32x2(t23, p23), sds2);
-            const uint64_t s01 = mul_f32x2(p01, sig2), s23 = mul_f32x2(p23, sig2);
+            p[hf * 32 + c] = p0;
+            p[hf * 32 + c + 1] = p1;
+            p[hf * 32 + c + 2] = p2;
+            p[hf * 32 + c + 3] = p3;
+            const uint64_t s01 = mul_f32x2(f2(p0, p1), sig2), s23 = mul_f32x2(f2(p2, p3), sig2);
             pw[q4 * 2] = pack_bf16x2(f2_lo(s01), f2_hi(s01));
             pw[q4 * 2 + 1] = pack_bf16x2(f2_lo(s23), f2_hi(s23));
-            dw[q4 * 2] = pack_bf16x2(f2_lo(d01), f2_hi(d01));
-            dw[q4 * 2 + 1] = pack_bf16x2(f2_lo(d23), f2_hi(d23));
           }
         };
-        if (diag) tile(std::true_type{});
-        else tile(std::false_type{});
-        // Psig^T over S^T columns this thread has already read
+        if (diag) ptile(std::true_type{});
+        else ptile(std::false_type{});
         tmem_st16(T_S + loff + hf * 16, pw);
-        // dS^T for the dQ^T MMA (its previous reader, dQ^T of the tile
-        // before, completed before S^T of this tile was signalled)
+      }
+      tmem_st_wait();
+      tc_fence_before();
+      mbar_arrive(sh.bar(B_PREADY));  // the dV MMA may read Psig^T
+      // (2) dS^T = sigma s P (dP^T - D) (bf16) over S^T columns 32-63 (read in
+      //     (1)) for the dK MMA, and into shared memory for the dQ^T MMA (its
+      //     previous reader, dQ^T of the tile before, completed before S^T of
+      //     this tile was signalled)
+      if (!wait_bar(sh, sh.bar(B_DPFULL), ph, a.status, 0x4202)) { ok = false; break; }
+      tc_fence_after();
+#pragma unroll
+      for (int hf = 0; hf < 2; ++hf) {
+        uint32_t dp[32];
+        tmem_ld32(T_DP + loff + hf * 32, dp);
+        tmem_ld_wait();
+        uint32_t dw[16];
+#pragma unroll
+        for (int q4 = 0; q4 < 8; ++q4) {
+          const float4 dq4 = ddv[hf * 8 + q4];
+          const int c = q4 * 4;
+          const uint64_t t01 = add_f32x2(f2(__uint_as_float(dp[c]), __uint_as_float(dp[c + 1])), f2(-dq4.x, -dq4.y));
+          const uint64_t t23 =
+              add_f32x2(f2(__uint_as_float(dp[c + 2]), __uint_as_float(dp[c + 3])), f2(-dq4.z, -dq4.w));
+          const uint64_t d01 = mul_f32x2(mul_f32x2(t01, f2(p[hf * 32 + c], p[hf * 32 + c + 1])), sds2);
+          const uint64_t d23 = mul_f32x2(mul_f32x2(t23, f2(p[hf * 32 + c + 2], p[hf * 32 + c + 3])), sds2);
+          dw[q4 * 2] = pack_bf16x2(f2_lo(d01), f2_hi(d01));
+          dw[q4 * 2 + 1] = pack_bf16x2(f2_lo(d23), f2_hi(d23));
+        }
+        tmem_st16(T_S + loff + 32 + hf * 16, dw);
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           const int ch = hf * 4 + cc;
           const int off = r * 128 + ((ch ^ (r & 7)) << 4);
           *reinterpret_cast<uint4*>(dsbuf + off) = make_uint4(dw[cc * 4], dw[cc * 4 + 1], dw[cc * 4 + 2], dw[cc * 4 + 3]);
-        }
-        if (hf == 0) {
-#pragma unroll
-          for (int e = 0; e < 16; ++e) dkeep[e] = dw[e];
-        } else {
-          tmem_st16(T_S + loff + 32, dkeep);
-          tmem_st16(T_S + loff + 48, dw);
         }
       }
       tmem_st_wait();
