@@ -30,15 +30,18 @@
 //        an MMA: (1) once S^T is in, P = exp2(S^T s log2e - lse2) and
 //          Psig^T = sigma P (sigma = 1 or -lambda) as bf16 over the S^T
 //          columns just read, while dP^T is still being computed;
-//          (2) once dP^T is in, dS^T = sigma s P (dP^T - D) as bf16 over the
-//          rest of the S^T columns and into shared memory, while dV runs
+//          (2) once dP^T is in, dS^T = sigma s P (dP^T - D) as bf16 into
+//          shared memory, while dV runs
 //        dV  += Psig^T dO      (TMEM, 256 columns; A operand from TMEM),
 //                               issued after step (1)
 //        dQ^T = K^T dS^T       (TMEM, reusing the dP^T columns) -> read by the
 //                               dQ warps, staged in shared memory in two
 //                               halves and added to the fp32 accumulator
 //                               with TMA reduce-adds
-//        dK  += dS^T Q         (TMEM, 128 columns; A operand from TMEM)
+//        dK  += dS^T Q         (TMEM, 128 columns; A operand dS^T from shared
+//                               memory, so that S^T of the next tile can be
+//                               issued right after dV when its Q tile has
+//                               landed, ahead of dQ^T and dK)
 //     At the end each CTA writes its dK; the dV halves of the two streams are
 //     summed through distributed shared memory and written as bf16;
 //  3. finalize: dQ accumulators -> bf16, and the lambda-vector gradients.
@@ -50,7 +53,7 @@
 //
 // Warp roles (320 threads): 0-3 softmax / dS and the epilogue, 4-7 dQ readback
 // and reduce, 8 TMA producer, 9 MMA issuer.  TMEM: [0,256) dV, [256,384) dK,
-// [384,448) S^T (then Psig^T and dS^T), [448,512) dP^T / dQ^T.  TMEM is full,
+// [384,448) S^T (then Psig^T), [448,512) dP^T / dQ^T.  TMEM is full,
 // so S^T and dP^T are single-buffered; taking the dQ readback off the softmax
 // warps keeps it out of the per-tile chain.
 // SMEM: K 32 KB, V 64 KB, 2 stages of (Q 16 KB, dO 32 KB), dQ staging of one
@@ -147,6 +150,19 @@ __device__ __forceinline__ bool wait_bar(const Shared& sh, uint32_t bar, uint32_
       return false;
     }
   }
+}
+
+// Non-blocking test of a phase (try_wait may suspend the thread for a
+// while before it reports an incomplete phase; test_wait returns at once).
+__device__ __forceinline__ bool mbar_test_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n .reg .pred p;\n mbarrier.test_wait.parity.shared::cta.b64 p, [%1], %2;\n"
+      " selp.u32 %0, 1, 0, p;\n}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
 }
 
 __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
@@ -561,6 +577,17 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
 #pragma unroll
         for (int kk = 0; kk < kQT / 16; ++kk)
           tc_mma_ts(T_DV, T_S + kk * 8, sdesc_sw128(db + kk * 2048, kBoxQ, 1024), kIdDV, (k > 0 || kk > 0) ? 1u : 0u);
+        // S^T(k+1) may overwrite Psig^T(k) as soon as dV(k) is issued (in
+        // order on the tensor pipe; dK takes dS^T from shared memory): issue
+        // it now when its Q tile has landed, so the softmax warps can start
+        // on it while dQ^T(k) and dK(k) run; else after them
+        const int k1 = k + 1;
+        bool s_next = false;
+        if (k1 < it.n_it && mbar_test_wait(sh.bar(B_QFULL + (k1 & 1)), (k1 >> 1) & 1)) {
+          tc_fence_after();
+          issue_s(k1);
+          s_next = true;
+        }
         if (!wait_bar(sh, sh.bar(B_PFULL), ph, a.status, 0x4103)) { ok = false; break; }
         tc_fence_after();
         // dQ^T = K^T dS^T  (into the dP^T columns, already read)
@@ -569,18 +596,18 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
           tc_mma_ss(T_DP, sdesc_sw128(kA + kk * 2048, kBoxK, 1024), sdesc_sw128(dsA + kk * 2048, kBoxQ, 1024),
                     kIdDQ, kk > 0);
         tc_commit(sh.bar(B_DQFULL));
-        // dK += dS^T Q  (dS^T in S^T columns 32-63)
+        // dK += dS^T Q  (dS^T K-major in shared memory)
 #pragma unroll
         for (int kk = 0; kk < kQT / 16; ++kk)
-          tc_mma_ts(T_DK, T_S + 32 + kk * 8, sdesc_sw128(qb + kk * 2048, kBoxQ, 1024), kIdDK,
+          tc_mma_ss(T_DK, sdesc_sw128(dsA + kk * 32, 16, 1024), sdesc_sw128(qb + kk * 2048, kBoxQ, 1024), kIdDK,
                     (k > 0 || kk > 0) ? 1u : 0u);
         tc_commit(sh.bar(B_QEMPTY + (k & 1)));
-        if (k + 1 < it.n_it) {
-          if (!wait_bar(sh, sh.bar(B_QFULL + ((k + 1) & 1)), ((k + 1) >> 1) & 1, a.status, 0x4104)) { ok = false; break; }
-          tc_fence_after();
-          // S^T(k+1) overwrites Psig^T / dS^T only after dV(k) / dK(k) have
-          // read them (MMAs of one thread run in order)
-          issue_s(k + 1);
+        if (k1 < it.n_it) {
+          if (!s_next) {
+            if (!wait_bar(sh, sh.bar(B_QFULL + (k1 & 1)), (k1 >> 1) & 1, a.status, 0x4104)) { ok = false; break; }
+            tc_fence_after();
+            issue_s(k1);
+          }
           // dP^T(k+1) overwrites dQ^T(k) once the dQ warps have read it
           if (!wait_bar(sh, sh.bar(B_DQFREE), ph, a.status, 0x4105)) { ok = false; break; }
           tc_fence_after();
@@ -717,10 +744,10 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
       tmem_st_wait();
       tc_fence_before();
       mbar_arrive(sh.bar(B_PREADY));  // the dV MMA may read Psig^T
-      // (2) dS^T = sigma s P (dP^T - D) (bf16) over S^T columns 32-63 (read in
-      //     (1)) for the dK MMA, and into shared memory for the dQ^T MMA (its
-      //     previous reader, dQ^T of the tile before, completed before S^T of
-      //     this tile was signalled)
+      // (2) dS^T = sigma s P (dP^T - D) (bf16) into shared memory, the
+      //     operand of the dQ^T and dK MMAs (its previous readers, those MMAs
+      //     of the tile before, completed before dP^T of this tile was
+      //     signalled: dP^T is issued after them)
       if (!wait_bar(sh, sh.bar(B_DPFULL), ph, a.status, 0x4202)) { ok = false; break; }
       tc_fence_after();
 #pragma unroll
@@ -741,7 +768,6 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
           dw[q4 * 2] = pack_bf16x2(f2_lo(d01), f2_hi(d01));
           dw[q4 * 2 + 1] = pack_bf16x2(f2_lo(d23), f2_hi(d23));
         }
-        tmem_st16(T_S + loff + 32 + hf * 16, dw);
 #pragma unroll
         for (int cc = 0; cc < 4; ++cc) {
           const int ch = hf * 4 + cc;

@@ -594,7 +594,16 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
       const int sp = it & 1;
       if (row == 0) mbar_arrive_expect_tx(sh.bar(B_SSQ + sp), 128 * 4);
       st_async_f32(sp ? partner_ssq_slot1 : partner_ssq_slot0, ssq, sp ? partner_ssq_bar1 : partner_ssq_bar0);
-      if (!wait_bar<true>(sh, sh.bar(B_SSQ + sp), (it >> 1) & 1, a.status, 0x3206)) break;
+      if (!wait_bar<true>(sh, sh.bar(B_SSQ + sp), (it >> 1) & 1, a.status, 0x3206)) {
+        // abort path: the partner's asynchronous stores into this CTA's
+        // shared memory may still be in flight; give them a short, bounded
+        // time to land before this CTA can leave (barrier.cluster does not
+        // wait for them)
+        const uint64_t t0 = globaltimer();
+        while (globaltimer() - t0 < 100000000ull && !try_wait_cluster(sh.bar(B_SSQ + sp), (it >> 1) & 1)) {
+        }
+        break;
+      }
       const float other_ssq = sh.ssq_rx_ptr(sp)[row];
       const float tot = rank == 0 ? ssq + other_ssq : other_ssq + ssq;
       const float rstd = 1.f / sqrtf(tot * (1.f / kDv) + a.rms_eps);
