@@ -238,7 +238,7 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
     mbar_init(sh.bar(B_SSQ1), 1);
     for (int q = 0; q < 4; ++q) {
       mbar_init(sh.bar(B_SCHF + q), 1);
-      mbar_init(sh.bar(B_SCHE + q), 11);  // rank 0: MMA + 4 softmax warps; rank 1: + its producer
+      mbar_init(sh.bar(B_SCHE + q), 2);  // one epilogue thread of each CTA
     }
     *sh.abort_flag() = 0;
     fence_mbar_init();
@@ -279,9 +279,16 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
   // ---- dynamic work distribution ------------------------------------------
   // Rank 0's producer takes item indices from a global counter (zeroed by the
   // host before the launch; heaviest items come first in index order) and
-  // publishes them to a 4-slot ring in both CTAs; the producer, MMA and
-  // softmax roles of both CTAs read the same sequence (the epilogue warps get
-  // each item from the softmax warps).  Index >= n_items ends the sequence.
+  // publishes them to a 4-slot ring in both CTAs, item k + 1 while it loads
+  // item k's first key tiles (so that neither the atomic nor the arrives sit
+  // between two items); the producer, MMA and softmax roles of both CTAs
+  // read the same sequence (the epilogue warps get each item from the
+  // softmax warps).  Index >= n_items ends the sequence.  A slot is released
+  // in each CTA by one epilogue thread once it has the item, by which time
+  // every reader in that CTA has read it: an arrive on the other CTA's
+  // barrier with a cluster-scope release costs the arriving thread about
+  // 0.8 us, which the producer, MMA and softmax roles would otherwise pay at
+  // every item start.
   int* counter = static_cast<int*>(a.workspace);
   auto publish = [&](int k) -> int {  // rank 0 producer only
     const int slot = k & 3;
@@ -293,19 +300,16 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
     remote_arrive(map_to_rank(sh.bar(B_SCHF + slot), partner));
     return idx;
   };
-  // consumers: returns the k-th item index (-1 on timeout); `releaser` arrives
-  // on rank 0's slot-free barrier once the index has been read
+  // consumers: the k-th item index (-1 on timeout)
   auto release = [&](int k) {
     const int slot = k & 3;
     if (rank == 0) mbar_arrive(sh.bar(B_SCHE + slot));
     else remote_arrive(map_to_rank(sh.bar(B_SCHE + slot), 0));
   };
-  auto consume = [&](int k, bool releaser) -> int {
+  auto consume = [&](int k) -> int {
     const int slot = k & 3;
     if (!wait_bar<true>(sh, sh.bar(B_SCHF + slot), (k >> 2) & 1, a.status, 0x3009)) return -1;
-    const int idx = sh.ring()[slot];
-    if (releaser) release(k);
-    return idx;
+    return sh.ring()[slot];
   };
 
   if (warp >= 8) {
@@ -315,8 +319,9 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
       if (lane == 0) {
         int kv = 0;
         bool ok = true;
+        int next = rank == 0 ? publish(0) : 0;
         for (int it = 0; ok; ++it) {
-          const int i = rank == 0 ? publish(it) : consume(it, true);
+          const int i = rank == 0 ? next : consume(it);
           if (i < 0) { ok = false; break; }
           if (i >= n_items) break;
           const Item w = item_of(i, units, a.H, n_mtiles, ub, causal);
@@ -331,6 +336,7 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
             for (int box = 0; box < kNQ; ++box)
               tma_load_4d(sh.base + kOffK + (st * kNQ + box) * kBox, tk, sh.bar(B_KFULL + st), box * 64, w.h,
                           j * kBN, w.b);
+            if (rank == 0 && j == min(1, w.n_kv - 1)) next = publish(it + 1);
             if (use > 0 && !wait_bar(sh, sh.bar(B_VEMPTY + st), (use - 1) & 1, a.status, 0x3003)) { ok = false; break; }
             mbar_arrive_expect_tx(sh.bar(B_VFULL + st), kNV * kBox);
             for (int box = 0; box < kNV; ++box)
@@ -366,7 +372,7 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
           return wait_bar(sh, sh.bar(B_KFULL + (g & 1)), (g >> 1) & 1, a.status, 0x3102);
         };
         for (;; ++it) {
-          const int i = consume(it, true);
+          const int i = consume(it);
           if (i < 0) { ok = false; break; }
           if (i >= n_items) break;
           const Item w = item_of(i, units, a.H, n_mtiles, ub, causal);
@@ -425,9 +431,7 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
     float* lse = rank == 0 ? a.lse1 : a.lse2;
     int kv = 0, it = 0;
     for (;; ++it) {
-      const int i = consume(it, false);
-      __syncwarp();
-      if (lane == 0 && i >= 0) release(it);  // the whole warp has read the slot
+      const int i = consume(it);
       if (i < 0) break;
       // (the hand-off slot is free once the epilogue warps have taken the
       // previous item: they read it before they release O)
@@ -546,6 +550,7 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
       tc_fence_before();
       mbar_arrive(sh.bar(B_OFREE));
       remote_arrive(partner_xrdy);
+      if (q == 0 && lane == 0) release(it);  // the item's ring slot: every reader in this CTA has read it
       const int n = w.mt * kBM + row;
       const bool live = n < a.N;
       const int64_t yrow = static_cast<int64_t>(w.b) * a.out.sb + static_cast<int64_t>(n) * a.out.sn +
