@@ -928,7 +928,10 @@ def run_ours(args, ws, rank, local):
 
     main = {**WORKLOADS, **PROFILE_ONLY}[args.workload]()
     main.setup(dev)
+    # warm-up steps are the timed steps' twins, L2 flush included (the first
+    # use of the flush buffer otherwise lands in the first timed step)
     for _ in range(args.warmup):
+        flush.add_(1)
         main.run()
     torch.cuda.synchronize()
 
