@@ -131,6 +131,20 @@ def test_v1_fwd_late_large_scores_rescale(causal):
     _check(t, li, y, sv, causal=causal)
 
 
+@pytest.mark.parametrize("causal", [True, False])
+def test_v1_fwd_first_tile_late_large_scores(causal):
+    """K1 rows 64-127 scaled by 30 (stream 1 only): inside the first key
+    tile, the scores past its first 64 keys dwarf the first 64, so the first
+    tile's stand-in max (taken over its first 64 scores) sends the tile's sum
+    past the guard, and those rows recompute it against their full max."""
+    t = synth.v1_inputs(1, 300, 2, 128, 256, "bf16", seed=4410, device="cuda")
+    t["k1"][:, 64:128] *= 30.0
+    li = bd.diffattn_lambda_init(1)
+    y, sv = bd.diffattn_v1_fwd(*(t[n] for n in NAMES), li, save=True, causal=causal)
+    torch.cuda.synchronize()
+    _check(t, li, y, sv, causal=causal)
+
+
 def test_v1_fwd_without_saves_matches():
     t = synth.v1_inputs(1, 300, 2, 128, 256, "bf16", seed=51, device="cuda")
     li = bd.diffattn_lambda_init(3)
