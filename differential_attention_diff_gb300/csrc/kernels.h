@@ -20,6 +20,11 @@ struct GateArgs {
   uint32_t* status;  // device status word for bounded waits (may be null)
 };
 cudaError_t launch_gate(const GateArgs& a, cudaStream_t s);
+// dX = dz W^T of the gate projection on tensor cores (gate_grads.cu), for
+// T >= 128, h <= 64 with h % 8 == 0, d_model % 64 == 0
+bool gate_dx_tc_ok(int T, int d_model, int h);
+cudaError_t launch_gate_dx_tc(int T, int d_model, int h, const float* dz, const void* W, void* dx, uint32_t* status,
+                              cudaStream_t s);
 
 // ---- V2 decode: split-KV partials, then merge + even/odd gate ------------
 struct DecodeArgs {

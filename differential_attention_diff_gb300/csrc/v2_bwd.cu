@@ -957,8 +957,10 @@ v2_bwd_dw_reduce_kernel(int d_model, int h, int chunks, const float* __restrict_
   }
 }
 
-cudaError_t launch_dx(int T, int d_model, int h, const float* dz, const void* W, void* dx,
+cudaError_t launch_dx(int T, int d_model, int h, const float* dz, const void* W, void* dx, uint32_t* status,
                       cudaStream_t s) {
+  // tensor cores (gate_grads.cu) where the shape allows; CUDA cores otherwise
+  if (gate_dx_tc_ok(T, d_model, h)) return launch_gate_dx_tc(T, d_model, h, dz, W, dx, status, s);
   const dim3 grid((T + kGT - 1) / kGT, (d_model + kGC - 1) / kGC);
   v2_bwd_dx_kernel<<<grid, 256, 0, s>>>(T, d_model, h, dz, static_cast<const __nv_bfloat16*>(W),
                                         static_cast<__nv_bfloat16*>(dx));
@@ -1054,7 +1056,7 @@ cudaError_t launch_v2_bwd(const V2BwdArgs& a_in, cudaStream_t s) {
   const int sms = a.num_sms > 0 ? a.num_sms : 148;
 
   if (a.dx) {
-    e = launch_dx(static_cast<int>(T), a.d_model, a.h_out, dz, a.w, a.dx, s);
+    e = launch_dx(static_cast<int>(T), a.d_model, a.h_out, dz, a.w, a.dx, a.status, s);
     if (e != cudaSuccess) return e;
   }
   if (a.dw) {
