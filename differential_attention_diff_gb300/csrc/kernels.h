@@ -23,6 +23,12 @@ cudaError_t launch_gate(const GateArgs& a, cudaStream_t s);
 // dX = dz W^T of the gate projection on tensor cores (gate_grads.cu), for
 // T >= 128, h <= 64 with h % 8 == 0, d_model % 64 == 0
 bool gate_dx_tc_ok(int T, int d_model, int h);
+// partial sums of dW = X^T dz per chunk of chunk_tokens tokens (a multiple of
+// 64) on tensor cores, part = fp32 [chunks][d_model][h]; for T >= 64, h <= 64
+// with h % 8 == 0, d_model % 128 == 0
+bool gate_dw_tc_ok(int T, int d_model, int h);
+cudaError_t launch_gate_dw_tc(int T, int d_model, int h, int chunk_tokens, int chunks, const float* dz, const void* X,
+                              float* part, uint32_t* status, cudaStream_t s);
 cudaError_t launch_gate_dx_tc(int T, int d_model, int h, const float* dz, const void* W, void* dx, uint32_t* status,
                               cudaStream_t s);
 

@@ -1060,10 +1060,17 @@ cudaError_t launch_v2_bwd(const V2BwdArgs& a_in, cudaStream_t s) {
     if (e != cudaSuccess) return e;
   }
   if (a.dw) {
-    v2_bwd_dw_partial_kernel<<<dim3((a.d_model + kGC - 1) / kGC, w.chunks, (a.h_out + kGP - 1) / kGP), 256, 0,
-                               s>>>(static_cast<int>(T), a.d_model, a.h_out, dz,
-                                    static_cast<const __nv_bfloat16*>(a.x), w.dw_part);
-    e = cudaGetLastError();
+    // partial sums per chunk of kDwChunk tokens: on tensor cores
+    // (gate_grads.cu) where the shape allows, CUDA cores otherwise
+    if (gate_dw_tc_ok(static_cast<int>(T), a.d_model, a.h_out)) {
+      e = launch_gate_dw_tc(static_cast<int>(T), a.d_model, a.h_out, kDwChunk, w.chunks, dz, a.x, w.dw_part,
+                            a.status, s);
+    } else {
+      v2_bwd_dw_partial_kernel<<<dim3((a.d_model + kGC - 1) / kGC, w.chunks, (a.h_out + kGP - 1) / kGP), 256, 0,
+                                 s>>>(static_cast<int>(T), a.d_model, a.h_out, dz,
+                                      static_cast<const __nv_bfloat16*>(a.x), w.dw_part);
+      e = cudaGetLastError();
+    }
     if (e != cudaSuccess) return e;
     const long long n = static_cast<long long>(a.d_model) * a.h_out;
     int g2 = static_cast<int>((n + 255) / 256);

@@ -199,24 +199,29 @@ def test_v2_bwd_full_size_b2_n8192_64q_8kv_one_group():
     _compare(g, ref, model, names=ATTN + ("dz",), bar="step", sl=sl)
 
 
-@pytest.mark.parametrize("B,N,h,dm", [(2, 200, 8, 320), (1, 300, 16, 128), (1, 129, 24, 192),
-                                      (2, 160, 32, 256), (1, 257, 64, 384)])
-def test_v2_bwd_dx_is_dz_times_w(B, N, h, dm):
-    """dX = dz W^T, checked against the product of the call's own dz (fp64)
-    and W, rounded to bf16 once: a bar independent of the attention's error.
-    Shapes reach the tensor-core kernel (T >= 128, h % 8 == 0) with a ragged
-    last token block and, at d_model 320 / 192 / 384, a partial last
-    256-feature tile; h from 8 to 64 gate heads."""
+@pytest.mark.parametrize("B,N,h,dm", [(2, 200, 8, 320), (1, 300, 16, 128), (1, 129, 24, 256),
+                                      (2, 160, 32, 384), (1, 257, 64, 512), (1, 1100, 32, 256)])
+def test_v2_bwd_gate_grads_are_products(B, N, h, dm):
+    """dX = dz W^T and dW = X^T dz, checked against the products of the
+    call's own dz (fp64) with W and X: bars independent of the attention's
+    error.  The shapes reach the tensor-core kernels (T >= 128, h % 8 == 0;
+    dW also d_model % 128 == 0, else its CUDA-core kernel) with a ragged last
+    token block, a partial last 256-feature tile of dX (d_model 320 / 384),
+    h from 8 to 64 gate heads and, at T = 1100, two 1024-token dW chunks."""
     t = synth.v2_inputs(B, N, h, 1, 128, dm, seed=7500 + h + dm, device="cuda", with_dout=True)
     _, sv = bd.diffattn_v2_fwd(t["q"], t["k"], t["v"], x=t["x"], w_lambda=t["w_lambda"], save=True)
     g = bd.diffattn_v2_bwd(t["q"], t["k"], t["v"], t["dout"], sv, x=t["x"], w_lambda=t["w_lambda"], want_dz=True)
     torch.cuda.synchronize()
     dz = f64(g["dz"]).reshape(B * N, h)
+    # dX in bf16: one rounding of a product carried to about 16 bits, so
+    # within one bf16 ulp of the exact value
     ref = dz @ f64(t["w_lambda"]).T
     got = f64(g["dx"]).reshape(B * N, dm)
     ref_bf16 = torch.from_numpy(ref).to(torch.bfloat16).double().numpy()
-    err = np.abs(got - ref_bf16)
-    # one bf16 rounding of a product carried to about 16 bits: within one
-    # bf16 ulp of the exact value
     tol = np.abs(ref) * 2.0 ** -7 + 1e-6 * float(np.abs(ref).max())
-    assert np.all(err <= tol), float((err / tol).max())
+    assert np.all(np.abs(got - ref_bf16) <= tol), float((np.abs(got - ref_bf16) / tol).max())
+    # dW in fp32, summed over the tokens
+    ref_w = f64(t["x"]).reshape(B * N, dm).T @ dz
+    got_w = f64(g["dw"])
+    tol_w = 1e-3 * np.abs(ref_w) + 1e-4 * float(np.abs(ref_w).max())
+    assert np.all(np.abs(got_w - ref_w) <= tol_w), float((np.abs(got_w - ref_w) / tol_w).max())
