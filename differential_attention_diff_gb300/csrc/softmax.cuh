@@ -160,4 +160,50 @@ __device__ __forceinline__ float softmax_tile(uint32_t t_s, int lim, bool first,
   return 1.f;
 }
 
+// ---- the softmax of one half row (64 key columns) --------------------------
+// Max over the valid columns of this half (key column c0 + e <= lim when
+// masked; -inf when none is valid).
+template <bool kMask>
+__device__ __forceinline__ float half_max(const uint32_t (&s)[64], int c0, int lim) {
+  float mx = -INFINITY;
+#pragma unroll
+  for (int e = 0; e < 64; ++e)
+    if (!kMask || c0 + e <= lim) mx = fmaxf(mx, __uint_as_float(s[e]));
+  return mx;
+}
+// The same over 32 scores starting at key column c0, folded into mx.
+template <bool kMask>
+__device__ __forceinline__ float chunk_max(const uint32_t (&s)[32], int c0, int lim, float mx) {
+#pragma unroll
+  for (int e = 0; e < 32; ++e)
+    if (!kMask || c0 + e <= lim) mx = fmaxf(mx, __uint_as_float(s[e]));
+  return mx;
+}
+// exp2(S scale log2e - m) of the 64 scores, written as bf16 pairs over the
+// first 32 of those columns (t_p); returns their sum.
+template <bool kMask>
+__device__ __forceinline__ float exp_half(const uint32_t (&s)[64], int c0, int lim, uint64_t sl2x2,
+                                          float m, uint32_t t_p) {
+  const uint64_t negm2 = f2(-m, -m);
+  const uint64_t a0 = exp_chunk<kMask>(s, c0, lim, sl2x2, negm2, t_p);
+  const uint64_t a1 = exp_chunk<kMask>(s + 32, c0 + 32, lim, sl2x2, negm2, t_p + 16);
+  const uint64_t t = add_f32x2(a0, a1);
+  return f2_lo(t) + f2_hi(t);
+}
+// Named barrier 1 over 256 softmax threads (warps 0-7, two warpgroups that
+// split each tile's key columns): a plain sync, and a sync that returns
+// whether any of them passed `pred`.
+__device__ __forceinline__ void named_sync_256() {
+  asm volatile("bar.sync 1, 256;" ::: "memory");
+}
+__device__ __forceinline__ bool named_red_or_256(bool pred) {
+  uint32_t r;
+  asm volatile(
+      "{\n .reg .pred p, q;\n setp.ne.u32 p, %1, 0;\n bar.red.or.pred q, 1, 256, p;\n selp.u32 %0, 1, 0, q;\n}"
+      : "=r"(r)
+      : "r"(static_cast<uint32_t>(pred))
+      : "memory");
+  return r != 0;
+}
+
 }  // namespace da

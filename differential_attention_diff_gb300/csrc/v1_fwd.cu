@@ -13,8 +13,11 @@
 // buffered, so the next tile's Q K^T runs while the softmax works) plus 256
 // columns for its O accumulator (d_v = 256): the whole 512-column TMEM of an
 // SM.  So a work item (batch, head, 128 query rows) runs on a cluster of two
-// CTAs: rank 0 computes stream 1, rank 1 stream 2, each from its own TMA
-// loads (V is read by both; the second read mostly hits L2).
+// CTAs: rank 0 computes stream 1, rank 1 stream 2, each from its own Q and K
+// loads; V, which both streams multiply, is read once per pair: each CTA
+// loads half of every V tile's column boxes with cluster multicast, into
+// both CTAs' shared memory, and a V stage is refilled only once both CTAs'
+// P.V MMAs are done with it (their commits arrive on both CTAs' barriers).
 //
 // The epilogue runs in warps of its own, under the next item's main loop.
 // Shared memory is full with the Q tile and the K and V rings, so the
@@ -32,10 +35,11 @@
 //   TMEM: [0,128) S / P buffer 0, [128,256) S / P buffer 1, [256,256+DV) O.
 //   SMEM: Q (32 KB), K ring 2 x 32 KB, V ring 2 x 64 KB (128-byte swizzle),
 //   for head dims (128, 256); half of each for (64, 128).
-//   warps 0-3: softmax (softmax.cuh; thread = query row = TMEM lane);
-//   warps 4-7: epilogue (thread = query row); warp 8: TMA producer;
-//   warp 9: MMA issuer (one lane); warps 10-11 idle (they complete the third
-//   warpgroup, whose registers go to the first two).
+//   warps 0-7: softmax, two warpgroups, each taking 64 key columns of every
+//   tile (softmax.cuh; thread = query row = TMEM lane); warps 8-11:
+//   epilogue (thread = query row); warps 12 and 14: TMA producers (Q and K;
+//   V); warp 13: MMA issuer (one lane); warp 15 idle (it completes the
+//   fourth warpgroup, whose registers go to the epilogue).
 #include "kernels.h"
 #include "softmax.cuh"
 #include "tma.cuh"
@@ -44,11 +48,11 @@ namespace da {
 namespace {
 
 constexpr int kBM = 128, kBN = 128;
-constexpr int kThreads = 384;
-// registers per thread after the split: the softmax and epilogue warpgroups
-// take what the producer warpgroup gives up (launch: 384 x 168; after:
-// 128 x 56 + 256 x 224, the same total)
-constexpr int kRegsLow = 56, kRegsHigh = 224;
+constexpr int kThreads = 512;
+// registers per thread after the split: the epilogue warpgroup takes what
+// the producer warpgroup gives up (launch: 512 x 128; after: 128 x 48 +
+// 256 x 128 + 128 x 208, the same total)
+constexpr int kRegsLow = 48, kRegsEpi = 208;
 constexpr int kBox = 128 * 128;  // one 64-column box of 128 rows (bf16)
 // Tiles for head dims (DQK, DV = 2 DQK) = (128, 256) or (64, 128), in boxes:
 //   Q at 0 (DQK/64), K ring [stage][DQK/64] after it, V ring [stage][DV/64]
@@ -81,12 +85,16 @@ struct Shared {
   // ring of the next work items (4 slots), written by rank 0's producer
   __device__ volatile int* ring() const { return reinterpret_cast<volatile int*>(gen + kOffBar + 272); }
   __device__ uint32_t ring_s(int slot) const { return base + kOffBar + 272 + 4 * slot; }
-  // softmax -> epilogue hand-off of one item: its index and each row's sum l
+  // softmax -> epilogue hand-off of one item: its index, and each row's two
+  // half sums of l, float[2][128] (on the rare tile that raises a row's max,
+  // the softmax warpgroups swap their half maxima through the same slots)
   __device__ volatile int* epi_item() const { return reinterpret_cast<volatile int*>(gen + kOffBar + 288); }
-  __device__ volatile float* epi_l() const { return reinterpret_cast<volatile float*>(gen + kOffBar + 1536); }
-  // the partner's per-row partial sums of squares, by item parity: float[2][128]
-  __device__ uint32_t ssq_rx(int p) const { return base + kOffBar + 512 + 512 * p; }
-  __device__ float* ssq_rx_ptr(int p) const { return reinterpret_cast<float*>(gen + kOffBar + 512 + 512 * p); }
+  __device__ volatile float* epi_l() const { return reinterpret_cast<volatile float*>(gen + kOffBar + 1024); }
+  // the partner's per-row partial sums of squares, float[128]: one slot
+  // serves every item, since the partner sends an item's sums only after it
+  // has my slot row of that item, which I write after reading its last sums
+  __device__ uint32_t ssq_rx() const { return base + kOffBar + 512; }
+  __device__ float* ssq_rx_ptr() const { return reinterpret_cast<float*>(gen + kOffBar + 512); }
 };
 
 __device__ __forceinline__ uint64_t globaltimer() {
@@ -134,11 +142,14 @@ __device__ __forceinline__ void remote_arrive(uint32_t cluster_bar) {
   asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
                : "memory");
 }
-// a value of another SM's exchange slot, read at L2 (never a stale L1 line
-// of an earlier item)
-__device__ __forceinline__ float ld_cg_f32(const float* p) {
-  float v;
-  asm volatile("ld.global.cg.f32 %0, [%1];" : "=f"(v) : "l"(p) : "memory");
+// four values of another SM's exchange slot, read at L2 (never a stale L1
+// line of an earlier item)
+__device__ __forceinline__ float4 ld_cg_f32x4(const float4* p) {
+  float4 v;
+  asm volatile("ld.global.cg.v4.f32 {%0, %1, %2, %3}, [%4];"
+               : "=f"(v.x), "=f"(v.y), "=f"(v.z), "=f"(v.w)
+               : "l"(p)
+               : "memory");
   return v;
 }
 __device__ __forceinline__ void st_cluster_s32(uint32_t addr, int v) {
@@ -225,13 +236,13 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
       mbar_init(sh.bar(B_KFULL + s), 1);
       mbar_init(sh.bar(B_KEMPTY + s), 1);
       mbar_init(sh.bar(B_VFULL + s), 1);
-      mbar_init(sh.bar(B_VEMPTY + s), 1);
+      mbar_init(sh.bar(B_VEMPTY + s), 2);  // both CTAs' P.V commits
       mbar_init(sh.bar(B_SFULL + s), 1);
-      mbar_init(sh.bar(B_PFULL + s), 128);
+      mbar_init(sh.bar(B_PFULL + s), 256);
     }
     mbar_init(sh.bar(B_ORDY), 1);
     mbar_init(sh.bar(B_ODONE), 1);
-    mbar_init(sh.bar(B_EPI), 128);    // softmax rows: item handed to the epilogue
+    mbar_init(sh.bar(B_EPI), 256);    // softmax threads: item handed to the epilogue
     mbar_init(sh.bar(B_OFREE), 128);  // epilogue rows: O read out of TMEM
     mbar_init(sh.bar(B_XRDY), 128);   // the partner's epilogue rows: its slot is written
     mbar_init(sh.bar(B_SSQ), 1);      // + 512 bytes of the partner's partial sums
@@ -261,11 +272,11 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
       if (a.lambda_out && blockIdx.x == 0) *a.lambda_out = lam;
     }
   }
-  if (warp == 9) {
+  if (warp == 13) {
     tmem_alloc(smem_u32(sh.tmem_slot()), 512);
     tmem_relinquish();
   }
-  if (warp == 8 && lane == 0) {
+  if (warp == 12 && lane == 0) {
     prefetch_tmap(tq);
     prefetch_tmap(tk);
     prefetch_tmap(&tm_v);
@@ -312,36 +323,46 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
     return sh.ring()[slot];
   };
 
-  if (warp >= 8) {
+  if (warp >= 12) {
     regs_dec<kRegsLow>();
-    if (warp == 8) {
-      // ------------------------------------------------------ TMA producer --
+    if (warp == 12 || warp == 14) {
+      // ----------------------------------------------------- TMA producers --
+      // warp 12: the Q and K tiles (and, in rank 0, the work ring); warp 14:
+      // the V tiles.  Two threads, so that a K load waits only for its own
+      // ring stage, never behind a V stage that a P.V still reads.
       if (lane == 0) {
+        const bool qk = warp == 12;
         int kv = 0;
         bool ok = true;
-        int next = rank == 0 ? publish(0) : 0;
+        int next = (qk && rank == 0) ? publish(0) : 0;
         for (int it = 0; ok; ++it) {
-          const int i = rank == 0 ? next : consume(it);
+          const int i = (qk && rank == 0) ? next : consume(it);
           if (i < 0) { ok = false; break; }
           if (i >= n_items) break;
           const Item w = item_of(i, units, a.H, n_mtiles, ub, causal);
-          if (it > 0 && !wait_bar(sh, sh.bar(B_QEMPTY), (it - 1) & 1, a.status, 0x3001)) { ok = false; break; }
-          mbar_arrive_expect_tx(sh.bar(B_QFULL), kNQ * kBox);
-          for (int box = 0; box < kNQ; ++box)
-            tma_load_4d(sh.base + kOffQ + box * kBox, tq, sh.bar(B_QFULL), box * 64, w.h, w.mt * kBM, w.b);
+          if (qk) {
+            if (it > 0 && !wait_bar(sh, sh.bar(B_QEMPTY), (it - 1) & 1, a.status, 0x3001)) { ok = false; break; }
+            mbar_arrive_expect_tx(sh.bar(B_QFULL), kNQ * kBox);
+            for (int box = 0; box < kNQ; ++box)
+              tma_load_4d(sh.base + kOffQ + box * kBox, tq, sh.bar(B_QFULL), box * 64, w.h, w.mt * kBM, w.b);
+          }
           for (int j = 0; j < w.n_kv; ++j, ++kv) {
             const int st = kv & 1, use = kv >> 1;
-            if (use > 0 && !wait_bar(sh, sh.bar(B_KEMPTY + st), (use - 1) & 1, a.status, 0x3002)) { ok = false; break; }
-            mbar_arrive_expect_tx(sh.bar(B_KFULL + st), kNQ * kBox);
-            for (int box = 0; box < kNQ; ++box)
-              tma_load_4d(sh.base + kOffK + (st * kNQ + box) * kBox, tk, sh.bar(B_KFULL + st), box * 64, w.h,
-                          j * kBN, w.b);
-            if (rank == 0 && j == min(1, w.n_kv - 1)) next = publish(it + 1);
-            if (use > 0 && !wait_bar(sh, sh.bar(B_VEMPTY + st), (use - 1) & 1, a.status, 0x3003)) { ok = false; break; }
-            mbar_arrive_expect_tx(sh.bar(B_VFULL + st), kNV * kBox);
-            for (int box = 0; box < kNV; ++box)
-              tma_load_4d(sh.base + kOffV + (st * kNV + box) * kBox, &tm_v, sh.bar(B_VFULL + st), box * 64, w.h,
-                          j * kBN, w.b);
+            if (qk) {
+              if (use > 0 && !wait_bar(sh, sh.bar(B_KEMPTY + st), (use - 1) & 1, a.status, 0x3002)) { ok = false; break; }
+              mbar_arrive_expect_tx(sh.bar(B_KFULL + st), kNQ * kBox);
+              for (int box = 0; box < kNQ; ++box)
+                tma_load_4d(sh.base + kOffK + (st * kNQ + box) * kBox, tk, sh.bar(B_KFULL + st), box * 64, w.h,
+                            j * kBN, w.b);
+              if (rank == 0 && j == min(1, w.n_kv - 1)) next = publish(it + 1);
+            } else {
+              if (use > 0 && !wait_bar(sh, sh.bar(B_VEMPTY + st), (use - 1) & 1, a.status, 0x3003)) { ok = false; break; }
+              // the whole tile lands here: this CTA's half and the partner's
+              mbar_arrive_expect_tx(sh.bar(B_VFULL + st), kNV * kBox);
+              for (int box = static_cast<int>(rank) * (kNV / 2); box < (static_cast<int>(rank) + 1) * (kNV / 2); ++box)
+                tma_load_4d_mc(sh.base + kOffV + (st * kNV + box) * kBox, &tm_v, sh.bar(B_VFULL + st), box * 64, w.h,
+                               j * kBN, w.b, 3);
+            }
           }
         }
         if (!ok) {
@@ -351,7 +372,7 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
           }
         }
       }
-    } else if (warp == 9) {
+    } else if (warp == 13) {
       // ------------------------------------------------------- MMA issuer ---
       if (lane == 0) {
         int kv = 0, it = 0;
@@ -400,10 +421,10 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
             tc_fence_after();
             const uint32_t vb = sh.base + kOffV + st * kNV * kBox;
   #pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk)
-              tc_mma_ts(t_o, tmem + st * 128 + kk * 8, sdesc_sw128(vb + kk * 2048, kBox, 1024),
-                        kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
-            tc_commit(sh.bar(B_VEMPTY + st));
+            for (int kk = 0; kk < kBN / 16; ++kk)  // P of keys 64 h.. at columns 64 h.. of the buffer
+              tc_mma_ts(t_o, tmem + st * 128 + (kk >> 2) * 64 + (kk & 3) * 8,
+                        sdesc_sw128(vb + kk * 2048, kBox, 1024), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+            tc_commit_mc(sh.bar(B_VEMPTY + st), 3);  // the stage is free in both CTAs
             tc_commit(sh.bar(B_ODONE));
             if (j + 2 < n) {
               if (!wait_k(g + 2)) { ok = false; break; }
@@ -420,90 +441,150 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
         }
       }
     }
-    // warps 10-11: idle (they complete the producer warpgroup)
-  } else if (warp < 4) {
+    // warp 15: idle (it completes the producer warpgroup)
+  } else if (warp < 8) {
     // ------------------------------------------------------- softmax ------
-    regs_inc<kRegsHigh>();
-    const int row = warp * 32 + lane;  // query row within the item = TMEM lane
-    const uint32_t lane_off = static_cast<uint32_t>(warp * 32) << 16;
-    const uint32_t t_o = tmem + lane_off + 256;
+    // Both warpgroups work on every tile: warpgroup wg takes key columns
+    // [64 wg, 64 wg + 64) (thread = query row = TMEM lane) and writes its P
+    // as bf16 pairs over the first 32 of those columns, so a tile's
+    // exponentials run on eight warps.  The halves of a row share one running
+    // max: on a row's first tile both read the whole row and take the same
+    // max (a barrier keeps either from writing P over scores the other still
+    // reads); later tiles keep that stale max, and on the rare tile whose sum
+    // leaves the guard in some half (a barrier reduction over both
+    // warpgroups decides) both halves recompute against a max raised over the
+    // tile, swapped through shared memory.  Named barrier 1 (these 256
+    // threads) is reached by both warpgroups in the same sequence: a failed
+    // wait only clears `ok`, and every stop is decided by a barrier reduction.
+    const int wg = warp >> 2, q4 = warp & 3;
+    const int row = q4 * 32 + lane;  // query row within the item = TMEM lane
+    const uint32_t lane_off = static_cast<uint32_t>(q4 * 32) << 16;
+    const int c0 = wg * 64;          // first key column of this half
+    const uint32_t t_oh = tmem + lane_off + 256 + wg * kHalf;  // this half's O columns (rescale)
     const float sl2 = a.scale_log2;
+    const uint64_t sl2x2 = f2(sl2, sl2);
     float* lse = rank == 0 ? a.lse1 : a.lse2;
-    int kv = 0, it = 0;
-    for (;; ++it) {
+    volatile float* xl = sh.epi_l();  // [half][row]
+    int kv = 0;
+    bool ok = true;
+    for (int it = 0;; ++it) {
       const int i = consume(it);
-      if (i < 0) break;
-      // (the hand-off slot is free once the epilogue warps have taken the
-      // previous item: they read it before they release O)
+      if (named_red_or_256(i < 0 || !ok)) break;
+      // (the hand-off slots are free once the epilogue warps have taken the
+      // previous item: they read them before they release O)
       if (i >= n_items) {
         if (it > 0 && !wait_bar(sh, sh.bar(B_OFREE), (it - 1) & 1, a.status, 0x3209)) break;
-        if (row == 0) *sh.epi_item() = n_items;  // end of the sequence
+        if (threadIdx.x == 0) *sh.epi_item() = n_items;  // end of the sequence
         mbar_arrive(sh.bar(B_EPI));
         break;
       }
       const Item w = item_of(i, units, a.H, n_mtiles, ub, causal);
-      float m_run = -INFINITY, l_run = 0.f;
-      bool ok = true;
+      float m_run = -INFINITY, l_half = 0.f;
       for (int j = 0; j < w.n_kv; ++j) {
         const int g = kv + j;
         const uint32_t t_s = tmem + lane_off + (g & 1) * 128;
-        if (!wait_bar(sh, sh.bar(B_SFULL + (g & 1)), (g >> 1) & 1, a.status, 0x3201)) { ok = false; break; }
+        if (!wait_bar(sh, sh.bar(B_SFULL + (g & 1)), (g >> 1) & 1, a.status, 0x3201)) ok = false;
         tc_fence_after();
         // masked columns: keys after the query (causal diagonal tile), or
         // keys >= N (ragged last tile without the causal mask)
         const bool masked = causal ? j == w.mt : (j == w.n_kv - 1 && (a.N % kBN) != 0);
         const int lim = causal ? row : a.N - 1 - j * kBN;
-        const float alpha = softmax_tile(t_s, lim, j == 0, masked, sl2, m_run, l_run);
-        if (j > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          // PV(g - 1) may still run: wait for it before rescaling O
-          if (!wait_bar(sh, sh.bar(B_ODONE), (g - 1) & 1, a.status, 0x3202)) { ok = false; break; }
-          tc_fence_after();
+        uint32_t sv[64];
+        tmem_ld32(t_s + c0, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
+        tmem_ld32(t_s + c0 + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+        if (j == 0) {
+          // the row max over both halves (the same value in both warpgroups)
+          const int o0 = c0 ^ 64;
+          uint32_t ov[32];
+          tmem_ld32(t_s + o0, ov);
+          tmem_ld_wait();
+          float mx = masked ? half_max<true>(sv, c0, lim) : half_max<false>(sv, c0, lim);
+          mx = masked ? chunk_max<true>(ov, o0, lim, mx) : chunk_max<false>(ov, o0, lim, mx);
+          tmem_ld32(t_s + o0 + 32, ov);
+          tmem_ld_wait();
+          mx = masked ? chunk_max<true>(ov, o0 + 32, lim, mx) : chunk_max<false>(ov, o0 + 32, lim, mx);
+          m_run = mx * sl2;
+          named_sync_256();  // both halves have read the row
+          l_half = masked ? exp_half<true>(sv, c0, lim, sl2x2, m_run, t_s + c0)
+                          : exp_half<false>(sv, c0, lim, sl2x2, m_run, t_s + c0);
+        } else {
+          tmem_ld_wait();
+          float lsum = masked ? exp_half<true>(sv, c0, lim, sl2x2, m_run, t_s + c0)
+                              : exp_half<false>(sv, c0, lim, sl2x2, m_run, t_s + c0);
+          if (named_red_or_256(!(lsum <= kSumGuard))) {
+            // rare: some row's half left the guard.  Both halves of every row
+            // recompute against a max raised over this tile; the half maxima
+            // go through the hand-off slots, which the epilogue has left once
+            // it released the previous item's O
+            if (it > 0 && !wait_bar(sh, sh.bar(B_OFREE), (it - 1) & 1, a.status, 0x320b)) ok = false;
+            const float hm = masked ? half_max<true>(sv, c0, lim) : half_max<false>(sv, c0, lim);
+            xl[wg * 128 + row] = hm;
+            named_sync_256();
+            const float m_new = fmaxf(m_run, fmaxf(hm, xl[(wg ^ 1) * 128 + row]) * sl2);
+            const float alpha = fast_exp2(m_run - m_new);
+            m_run = m_new;
+            lsum = masked ? exp_half<true>(sv, c0, lim, sl2x2, m_new, t_s + c0)
+                          : exp_half<false>(sv, c0, lim, sl2x2, m_new, t_s + c0);
+            l_half = l_half * alpha + lsum;
+            if (__any_sync(0xffffffffu, alpha != 1.f)) {
+              // PV(g - 1) may still run: wait for it before rescaling this
+              // half's columns of O
+              if (!wait_bar(sh, sh.bar(B_ODONE), (g - 1) & 1, a.status, 0x3202)) ok = false;
+              tc_fence_after();
 #pragma unroll 1
-          for (int c = 0; c < kDv / 32; ++c) {
-            uint32_t o[32];
-            tmem_ld32(t_o + c * 32, o);
-            tmem_ld_wait();
+              for (int c = 0; c < kHalf / 32; ++c) {
+                uint32_t o[32];
+                tmem_ld32(t_oh + c * 32, o);
+                tmem_ld_wait();
 #pragma unroll
-            for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
-            tmem_st32(t_o + c * 32, o);
+                for (int e = 0; e < 32; ++e) o[e] = __float_as_uint(__uint_as_float(o[e]) * alpha);
+                tmem_st32(t_oh + c * 32, o);
+              }
+            }
+            named_sync_256();  // both halves have read the swapped maxima
+          } else {
+            l_half += lsum;
           }
         }
         tmem_st_wait();
         tc_fence_before();
         mbar_arrive(sh.bar(B_PFULL + (g & 1)));
       }
-      if (!ok) break;
       kv += w.n_kv;
-      const int n = w.mt * kBM + row;
-      if (lse && n < a.N)
-        lse[(static_cast<int64_t>(w.b) * a.H + w.h) * a.N + n] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
-      // hand the item and this row's sum to the epilogue warps
-      if (it > 0 && !wait_bar(sh, sh.bar(B_OFREE), (it - 1) & 1, a.status, 0x320a)) break;
-      sh.epi_l()[row] = l_run;
-      if (row == 0) *sh.epi_item() = i;
+      // hand the item and the row's half sums to the epilogue warps
+      if (it > 0 && !wait_bar(sh, sh.bar(B_OFREE), (it - 1) & 1, a.status, 0x320a)) ok = false;
+      xl[wg * 128 + row] = l_half;
+      named_sync_256();
+      if (wg == 0) {
+        const int n = w.mt * kBM + row;
+        const float l_run = xl[row] + xl[128 + row];
+        if (lse && n < a.N)
+          lse[(static_cast<int64_t>(w.b) * a.H + w.h) * a.N + n] = (m_run + __log2f(l_run)) * 0.69314718055994531f;
+      }
+      if (threadIdx.x == 0) *sh.epi_item() = i;
       mbar_arrive(sh.bar(B_EPI));
     }
   } else {
     // ------------------------------------------------------ epilogue ------
-    regs_inc<kRegsHigh>();
-    const int q = warp - 4;
+    regs_inc<kRegsEpi>();
+    const int q = warp - 8;
     const int row = q * 32 + lane;  // query row = TMEM lane of this warp's quadrant
     const uint32_t t_o = tmem + (static_cast<uint32_t>(q * 32) << 16) + 256;
     const float lam = *sh.lam();
     const float cscale = 1.f - a.lambda_init;
     const int give = (1 - static_cast<int>(rank)) * kHalf, keep = static_cast<int>(rank) * kHalf;
-    // exchange slots: kHalf columns of 128 fp32 (O/l of the columns the
-    // partner finishes, column-major so that a warp's 32 rows of one column
-    // are one 128-byte line)
+    // exchange slots: 128 rows x kHalf fp32 (O/l of the columns the partner
+    // finishes), stored as float4 groups of four columns, group-major, so
+    // that one 16-byte store per lane writes 512 contiguous bytes per warp
     float* xchg = reinterpret_cast<float*>(static_cast<uint8_t*>(a.workspace) + kXchgOff);
     const size_t cl = blockIdx.x >> 1;
-    float* my_x = xchg + (cl * 2 + rank) * 128 * kHalf + row;              // column c at [c * 128]
-    const float* partner_x = xchg + (cl * 2 + partner) * 128 * kHalf + row;
+    // (columns 4k .. 4k + 3 of a row at float4 [k * 128 + row])
+    float4* my_x = reinterpret_cast<float4*>(xchg + (cl * 2 + rank) * 128 * kHalf) + row;
+    const float4* partner_x = reinterpret_cast<const float4*>(xchg + (cl * 2 + partner) * 128 * kHalf) + row;
     const uint32_t partner_xrdy = map_to_rank(sh.bar(B_XRDY), partner);
     const uint32_t partner_ssq_bar0 = map_to_rank(sh.bar(B_SSQ), partner);
     const uint32_t partner_ssq_bar1 = map_to_rank(sh.bar(B_SSQ1), partner);
-    const uint32_t partner_ssq_slot0 = map_to_rank(sh.ssq_rx(0) + row * 4, partner);
-    const uint32_t partner_ssq_slot1 = map_to_rank(sh.ssq_rx(1) + row * 4, partner);
+    const uint32_t partner_ssq_slot = map_to_rank(sh.ssq_rx() + row * 4, partner);
     const bool want_o2 = a.o2.ptr != nullptr;
     __nv_bfloat16* const yb = static_cast<__nv_bfloat16*>(a.out.ptr);
     __nv_bfloat16* const o2b = static_cast<__nv_bfloat16*>(a.o2.ptr);
@@ -519,7 +600,7 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
     for (int it = 0;; ++it) {
       if (!wait_bar(sh, sh.bar(B_EPI), it & 1, a.status, 0x3203)) break;
       const int i = *sh.epi_item();
-      const float l_run = sh.epi_l()[row];
+      const float l_run = sh.epi_l()[row] + sh.epi_l()[128 + row];
       if (i >= n_items) break;
       const Item w = item_of(i, units, a.H, n_mtiles, ub, causal);
       if (!wait_bar(sh, sh.bar(B_ORDY), it & 1, a.status, 0x3204)) break;
@@ -532,7 +613,9 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
         tmem_ld32(t_o + give + c * 32, o);
         tmem_ld_wait();
 #pragma unroll
-        for (int e = 0; e < 32; ++e) my_x[(c * 32 + e) * 128] = __uint_as_float(o[e]) * inv_l;
+        for (int e = 0; e < 8; ++e)
+          my_x[(c * 8 + e) * 128] = make_float4(__uint_as_float(o[4 * e]) * inv_l, __uint_as_float(o[4 * e + 1]) * inv_l,
+                                                __uint_as_float(o[4 * e + 2]) * inv_l, __uint_as_float(o[4 * e + 3]) * inv_l);
       }
       // (2) my own half of O/l into registers
       float dvals[kHalf];
@@ -569,7 +652,7 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
       for (int c = 0; c < kHalf / 32; ++c) {
         float oth[32];
 #pragma unroll
-        for (int e = 0; e < 32; ++e) oth[e] = ld_cg_f32(partner_x + (c * 32 + e) * 128);
+        for (int e = 0; e < 8; ++e) *reinterpret_cast<float4*>(&oth[4 * e]) = ld_cg_f32x4(partner_x + (c * 8 + e) * 128);
 #pragma unroll
         for (int e = 0; e < 32; ++e) {
           const float own = dvals[c * 32 + e];
@@ -586,7 +669,8 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
         for (int e = 0; e < kHalf; e += 8) {
           float v[8];
 #pragma unroll
-          for (int k = 0; k < 8; ++k) v[k] = ld_cg_f32(partner_x + (e + k) * 128);
+          *reinterpret_cast<float4*>(&v[0]) = ld_cg_f32x4(partner_x + (e / 4) * 128);
+          *reinterpret_cast<float4*>(&v[4]) = ld_cg_f32x4(partner_x + (e / 4 + 1) * 128);
           *reinterpret_cast<uint4*>(o2b + o2row + e) = pack8(v);
         }
       }
@@ -598,7 +682,7 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
       //     slot may take the next item.
       const int sp = it & 1;
       if (row == 0) mbar_arrive_expect_tx(sh.bar(B_SSQ + sp), 128 * 4);
-      st_async_f32(sp ? partner_ssq_slot1 : partner_ssq_slot0, ssq, sp ? partner_ssq_bar1 : partner_ssq_bar0);
+      st_async_f32(partner_ssq_slot, ssq, sp ? partner_ssq_bar1 : partner_ssq_bar0);
       if (!wait_bar<true>(sh, sh.bar(B_SSQ + sp), (it >> 1) & 1, a.status, 0x3206)) {
         // abort path: the partner's asynchronous stores into this CTA's
         // shared memory may still be in flight; give them a short, bounded
@@ -609,7 +693,7 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
         }
         break;
       }
-      const float other_ssq = sh.ssq_rx_ptr(sp)[row];
+      const float other_ssq = sh.ssq_rx_ptr()[row];
       const float tot = rank == 0 ? ssq + other_ssq : other_ssq + ssq;
       const float rstd = 1.f / sqrtf(tot * (1.f / kDv) + a.rms_eps);
       const float cs = cscale * rstd;
@@ -634,7 +718,7 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
   __syncthreads();
   cluster_sync();  // no CTA leaves while its partner may still address its shared memory
   tc_fence_after();
-  if (warp == 9) tmem_dealloc(tmem, 512);
+  if (warp == 13) tmem_dealloc(tmem, 512);
 }
 
 }  // namespace

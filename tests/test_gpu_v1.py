@@ -132,11 +132,25 @@ def test_v1_fwd_late_large_scores_rescale(causal):
 
 
 @pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("off", [32, 96])
+def test_v1_fwd_late_large_scores_second_chunk(causal, off):
+    """K1 rows 256+off .. 256+off+31 scaled by 30 (stream 1 only): in key
+    tile 2 only one 32-key chunk of one softmax warpgroup's half (keys 32-63
+    or 96-127 of the tile) is large, so one warpgroup trips the sum guard and
+    both recompute the tile against the raised max."""
+    t = synth.v1_inputs(1, 500, 2, 128, 256, "bf16", seed=4420 + off, device="cuda")
+    t["k1"][:, 256 + off:256 + off + 32] *= 30.0
+    li = bd.diffattn_lambda_init(2)
+    y, sv = bd.diffattn_v1_fwd(*(t[n] for n in NAMES), li, save=True, causal=causal)
+    torch.cuda.synchronize()
+    _check(t, li, y, sv, causal=causal)
+
+
+@pytest.mark.parametrize("causal", [True, False])
 def test_v1_fwd_first_tile_late_large_scores(causal):
     """K1 rows 64-127 scaled by 30 (stream 1 only): inside the first key
-    tile, the scores past its first 64 keys dwarf the first 64, so the first
-    tile's stand-in max (taken over its first 64 scores) sends the tile's sum
-    past the guard, and those rows recompute it against their full max."""
+    tile the second softmax warpgroup's scores dwarf the first's; both
+    warpgroups take the row max over the whole first tile."""
     t = synth.v1_inputs(1, 300, 2, 128, 256, "bf16", seed=4410, device="cuda")
     t["k1"][:, 64:128] *= 30.0
     li = bd.diffattn_lambda_init(1)
