@@ -170,13 +170,18 @@ __device__ __forceinline__ uint32_t map_to_rank(uint32_t saddr, uint32_t rank) {
   asm volatile("mapa.shared::cluster.u32 %0, %1, %2;" : "=r"(r) : "r"(saddr), "r"(rank));
   return r;
 }
-__device__ __forceinline__ void remote_arrive(uint32_t cluster_bar) {
-  asm volatile("mbarrier.arrive.release.cluster.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar)
-               : "memory");
+// an arrive on a cluster peer's barrier with a CTA-scope release: enough where
+// the hand-off orders only tensor-core and asynchronous-proxy accesses (a
+// cluster-scope release costs the arriving thread about a microsecond)
+__device__ __forceinline__ void remote_arrive_cta(uint32_t cluster_bar) {
+  asm volatile("mbarrier.arrive.shared::cluster.b64 _, [%0];" ::"r"(cluster_bar) : "memory");
 }
-__device__ __forceinline__ void st_cluster_v4(uint32_t addr, float4 v) {
-  asm volatile("st.shared::cluster.v4.f32 [%0], {%1, %2, %3, %4};" ::"r"(addr), "f"(v.x),
-               "f"(v.y), "f"(v.z), "f"(v.w)
+// 16 bytes into a cluster peer's shared memory, completion counted in bytes
+// on the peer's mbarrier
+__device__ __forceinline__ void st_async_v4(uint32_t addr, float4 v, uint32_t bar_cluster) {
+  asm volatile("st.async.shared::cluster.mbarrier::complete_tx::bytes.v4.f32 [%0], {%1, %2, %3, %4}, [%5];" ::"r"(
+                   addr),
+               "f"(v.x), "f"(v.y), "f"(v.z), "f"(v.w), "r"(bar_cluster)
                : "memory");
 }
 __device__ __forceinline__ uint32_t cluster_rank() {
@@ -439,6 +444,29 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
   const CUtensorMap* tdq = rank == 0 ? &tm_dq1 : &tm_dq2;
   const float* Dv = w.D[rank];
 
+  // the item's K and V tiles, and query tile k's Q, dO, lse2 and D into
+  // stage k & 1 (issued by one thread)
+  const size_t srow = (static_cast<size_t>(it.b) * a.H + it.h) * w.npad;
+  auto load_kv = [&]() {
+    mbar_arrive_expect_tx(sh.bar(B_KV), (kNQ + kNV) * kBoxK);
+    for (int box = 0; box < kNQ; ++box)
+      tma_load_4d(sh.base + kOffK + box * kBoxK, tk, sh.bar(B_KV), box * 64, it.h, it.kt * kKT, it.b);
+    for (int box = 0; box < kNV; ++box)
+      tma_load_4d(sh.base + kOffV + box * kBoxK, &tm_v, sh.bar(B_KV), box * 64, it.h, it.kt * kKT, it.b);
+  };
+  auto load_q = [&](int k) {
+    const int st = k & 1;
+    const int q0 = (it.i0 + k) * kQT;
+    const uint32_t sb = sh.base + kOffStage + st * kStageBytes;
+    mbar_arrive_expect_tx(sh.bar(B_QFULL + st), (kNQ + kNV) * kBoxQ + 512);
+    for (int box = 0; box < kNQ; ++box)
+      tma_load_4d(sb + kStageQ + box * kBoxQ, tq, sh.bar(B_QFULL + st), box * 64, it.h, q0, it.b);
+    for (int box = 0; box < kNV; ++box)
+      tma_load_4d(sb + kStageDO + box * kBoxQ, &tm_do, sh.bar(B_QFULL + st), box * 64, it.h, q0, it.b);
+    const uint32_t lb = sh.base + kOffLse + st * 512;
+    bulk_load(lb, lse2 + srow + q0, 256, sh.bar(B_QFULL + st));
+    bulk_load(lb + 256, Dv + srow + q0, 256, sh.bar(B_QFULL + st));
+  };
   if (threadIdx.x == 0) {
     mbar_init(sh.bar(B_KV), 1);
     for (int s = 0; s < 2; ++s) {
@@ -452,14 +480,19 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
     mbar_init(sh.bar(B_DQFULL), 1);
     mbar_init(sh.bar(B_DQFREE), 128);
     mbar_init(sh.bar(B_ACC), 1);
-    mbar_init(sh.bar(B_RTR), 128);
-    mbar_init(sh.bar(B_DATA), 128);
+    mbar_init(sh.bar(B_RTR), 1);   // the partner's MMAs are done: its V region may take my half of dV
+    mbar_init(sh.bar(B_DATA), 1);  // + the bytes of the partner's half
     for (int h = 0; h < 2; ++h) {
       mbar_init(sh.bar(B_STG0 + h), 64);
       mbar_init(sh.bar(B_FREE0 + h), 1);
     }
     *sh.abort_flag() = 0;
     fence_mbar_init();
+    // the loads that need no stage released go out now, under the rest of
+    // the set-up (TMEM allocation, lambda, the cluster barrier): they touch
+    // only this CTA's shared memory and barriers
+    load_kv();
+    for (int k = 0; k < 2 && k < it.n_it; ++k) load_q(k);
   }
   if (warp == 0) {
     const float lam = lambda_dev(a, lane, nullptr, nullptr);
@@ -494,30 +527,16 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
   if (warp == 8) {
     // ---------------------------------------------------- TMA producer ----
     if (lane == 0) {
-      mbar_arrive_expect_tx(sh.bar(B_KV), (kNQ + kNV) * kBoxK);
-      for (int box = 0; box < kNQ; ++box)
-        tma_load_4d(sh.base + kOffK + box * kBoxK, tk, sh.bar(B_KV), box * 64, it.h, it.kt * kKT, it.b);
-      for (int box = 0; box < kNV; ++box)
-        tma_load_4d(sh.base + kOffV + box * kBoxK, &tm_v, sh.bar(B_KV), box * 64, it.h, it.kt * kKT, it.b);
-      const size_t srow = (static_cast<size_t>(it.b) * a.H + it.h) * w.npad;
-      int last = -1;
+      // K, V and the first two query tiles were issued at set-up
+      int last = min(2, it.n_it) - 1;
       bool ok = true;
-      for (int k = 0; k < it.n_it; ++k) {
+      for (int k = 2; k < it.n_it; ++k) {
         const int st = k & 1, use = k >> 1;
-        if (use > 0 && !wait_bar(sh, sh.bar(B_QEMPTY + st), (use - 1) & 1, a.status, 0x4001)) {
+        if (!wait_bar(sh, sh.bar(B_QEMPTY + st), (use - 1) & 1, a.status, 0x4001)) {
           ok = false;
           break;
         }
-        const int q0 = (it.i0 + k) * kQT;
-        const uint32_t sb = sh.base + kOffStage + st * kStageBytes;
-        mbar_arrive_expect_tx(sh.bar(B_QFULL + st), (kNQ + kNV) * kBoxQ + 512);
-        for (int box = 0; box < kNQ; ++box)
-          tma_load_4d(sb + kStageQ + box * kBoxQ, tq, sh.bar(B_QFULL + st), box * 64, it.h, q0, it.b);
-        for (int box = 0; box < kNV; ++box)
-          tma_load_4d(sb + kStageDO + box * kBoxQ, &tm_do, sh.bar(B_QFULL + st), box * 64, it.h, q0, it.b);
-        const uint32_t lb = sh.base + kOffLse + st * 512;
-        bulk_load(lb, lse2 + srow + q0, 256, sh.bar(B_QFULL + st));
-        bulk_load(lb + 256, Dv + srow + q0, 256, sh.bar(B_QFULL + st));
+        load_q(k);
         last = k;
       }
       if (!ok) {
@@ -784,7 +803,37 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
     if (ok && wait_bar(sh, sh.bar(B_ACC), 0, a.status, 0x4205)) {
       tc_fence_after();
       const bool live = key < a.N;
-      // dK of this stream
+      // (1) dV: swap halves with the partner (the other stream) through
+      //     DSMEM.  Receive buffer = this CTA's V tile region, idle now that
+      //     its MMAs are done (which one arrive on the partner's RTR says):
+      //     128 rows of d_v / 2 fp32, float4 j of row r at [j * 128 + r] so
+      //     that a warp's 16-byte accesses are consecutive.  The partner's
+      //     rows arrive as asynchronous stores counted in bytes on DATA, while
+      //     this CTA writes its dK.
+      constexpr int kHalf = kDv / 2;
+      const int give = (1 - static_cast<int>(rank)) * kHalf, keep = static_cast<int>(rank) * kHalf;
+      if (r == 0) {
+        mbar_arrive_expect_tx(sh.bar(B_DATA), 128 * kHalf * 4);
+        remote_arrive_cta(map_to_rank(sh.bar(B_RTR), partner));
+      }
+      const bool rtr = wait_bar<true>(sh, sh.bar(B_RTR), 0, a.status, 0x4206);
+      if (rtr) {
+        const uint32_t rx = map_to_rank(sh.base + kOffV + r * 16, partner);
+        const uint32_t rx_bar = map_to_rank(sh.bar(B_DATA), partner);
+#pragma unroll 1
+        for (int c = 0; c < kHalf / 32; ++c) {
+          uint32_t v[32];
+          tmem_ld32(T_DV + loff + give + c * 32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int e = 0; e < 32; e += 4)
+            st_async_v4(rx + ((c * 32 + e) / 4) * 128 * 16,
+                        make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
+                                    __uint_as_float(v[e + 3])),
+                        rx_bar);
+        }
+      }
+      // (2) dK of this stream
       __nv_bfloat16* dkp = static_cast<__nv_bfloat16*>(rank == 0 ? a.dk1.ptr : a.dk2.ptr);
       const da_t4& dkt = rank == 0 ? a.dk1 : a.dk2;
 #pragma unroll 1
@@ -804,28 +853,18 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
           }
         }
       }
-      // dV: swap halves with the partner (the other stream) through DSMEM.
-      // Receive buffer = this CTA's V tile region (idle now): 128 rows of
-      // d_v / 2 fp32.
-      constexpr int kHalf = kDv / 2;
-      remote_arrive(map_to_rank(sh.bar(B_RTR), partner));
-      if (wait_bar<true>(sh, sh.bar(B_RTR), 0, a.status, 0x4206)) {
-        const int give = (1 - static_cast<int>(rank)) * kHalf, keep = static_cast<int>(rank) * kHalf;
-        const uint32_t rx = map_to_rank(sh.base + kOffV + r * (kHalf * 4), partner);
-#pragma unroll 1
-        for (int c = 0; c < kHalf / 32; ++c) {
-          uint32_t v[32];
-          tmem_ld32(T_DV + loff + give + c * 32, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int e = 0; e < 32; e += 4)
-            st_cluster_v4(rx + (c * 32 + e) * 4,
-                          make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]),
-                                      __uint_as_float(v[e + 2]), __uint_as_float(v[e + 3])));
-        }
-        remote_arrive(map_to_rank(sh.bar(B_DATA), partner));
-        if (wait_bar<true>(sh, sh.bar(B_DATA), 0, a.status, 0x4207)) {
-          const float* mine = reinterpret_cast<const float*>(sh.gen + kOffV + r * (kHalf * 4));
+      // (3) dV of my columns: my stream's half plus the partner's
+      if (rtr) {
+        if (!wait_bar<true>(sh, sh.bar(B_DATA), 0, a.status, 0x4207)) {
+          // abort path: the partner's asynchronous stores into this CTA's
+          // shared memory may still be in flight; give them a short, bounded
+          // time to land before this CTA can leave (barrier.cluster does not
+          // wait for them)
+          const uint64_t t0 = globaltimer();
+          while (globaltimer() - t0 < 100000000ull && !try_wait_cluster(sh.bar(B_DATA), 0)) {
+          }
+        } else {
+          const float4* mine = reinterpret_cast<const float4*>(sh.gen + kOffV) + r;
           __nv_bfloat16* dst = static_cast<__nv_bfloat16*>(a.dv.ptr) + it.b * a.dv.sb +
                                static_cast<int64_t>(key) * a.dv.sn + it.h * a.dv.sh + keep;
 #pragma unroll 1
@@ -837,11 +876,13 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
 #pragma unroll
               for (int e = 0; e < 32; e += 8) {
                 float s8[8];
+                float o8[8];
+                *reinterpret_cast<float4*>(&o8[0]) = mine[((c * 32 + e) / 4) * 128];
+                *reinterpret_cast<float4*>(&o8[4]) = mine[((c * 32 + e) / 4 + 1) * 128];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                  const float other = mine[c * 32 + e + u];
                   // stream 1 + stream 2 in a fixed order on both CTAs
-                  s8[u] = rank == 0 ? __uint_as_float(v[e + u]) + other : other + __uint_as_float(v[e + u]);
+                  s8[u] = rank == 0 ? __uint_as_float(v[e + u]) + o8[u] : o8[u] + __uint_as_float(v[e + u]);
                 }
                 *reinterpret_cast<uint4*>(dst + c * 32 + e) =
                     make_uint4(pack_bf16x2(s8[0], s8[1]), pack_bf16x2(s8[2], s8[3]),

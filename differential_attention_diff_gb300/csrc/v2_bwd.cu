@@ -386,18 +386,16 @@ struct Item {
   int b, g, kt, i0, n_ith, n_it;
 };
 
-// Items: (batch, K/V group, key tile).  Groups of `per` (batch, K/V group)
-// units are taken one block at a time (their dQ accumulators stay in L2),
-// the heaviest key tiles (most query tiles) first within each block.
-__device__ __forceinline__ Item item_of(int i, int n_kt, int n_qt, int units, int h_kv, int per,
-                                        int G, bool causal) {
-  const int blk = i / (per * n_kt);
-  const int base = blk * per;
-  const int pb = min(per, units - base);
-  const int wi = i - blk * per * n_kt;
+// Items: (batch, K/V group, key tile), one per CTA, in launch order the
+// heaviest key tiles (most query tiles) of every (batch, K/V group) unit
+// first.  (Taking the units a block at a time, so that fewer dQ accumulators
+// are live in L2, left the last block's heavy items to start late: at B2
+// N8192 with 16 units in blocks of 5, 5, 5 and 1 the SMs were 82 % busy and
+// the kernel 18 % slower.)
+__device__ __forceinline__ Item item_of(int i, int n_qt, int units, int h_kv, int G, bool causal) {
   Item it;
-  it.kt = wi / pb;
-  const int u = base + wi % pb;
+  it.kt = i / units;
+  const int u = i % units;
   it.b = u / h_kv;
   it.g = u % h_kv;
   it.i0 = causal ? it.kt * (kKT / kQT) : 0;  // causal: query tiles from the diagonal on
@@ -411,7 +409,7 @@ __global__ void __launch_bounds__(kThreads, 1)
 v2_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_constant__ CUtensorMap tm_k,
                    const __grid_constant__ CUtensorMap tm_v, const __grid_constant__ CUtensorMap tm_g,
                    const __grid_constant__ CUtensorMap tm_do, const __grid_constant__ CUtensorMap tm_dq,
-                   V2BwdArgs a, BwdWs w, int per) {
+                   V2BwdArgs a, BwdWs w) {
   extern __shared__ uint8_t smem_raw[];
   Shared sh;
   {
@@ -424,11 +422,10 @@ v2_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q, const __grid_consta
   constexpr uint32_t kIdAcc = idesc2(128, D, 0, 1);  // P^T / dS^T (TMEM) x dO / Q (MN-major)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int G = (2 * a.h) / a.h_kv;
-  const int n_kt = (a.N + kKT - 1) / kKT;
   const int n_qt = w.npad / kQT;
   const bool causal = a.causal != 0;
   const int ratio = a.ratio > 1 ? a.ratio : 1;
-  const Item it = item_of(blockIdx.x, n_kt, n_qt, a.B * a.h_kv, a.h_kv, per, G, causal);
+  const Item it = item_of(blockIdx.x, n_qt, a.B * a.h_kv, a.h_kv, G, causal);
 
   if (threadIdx.x == 0) {
     mbar_init(sh.bar(B_KV), 1);
@@ -999,15 +996,11 @@ cudaError_t launch_attn(const V2BwdArgs& a, const BwdWs& w, float* dz, cudaStrea
   if (e != cudaSuccess) return e;
   const int n_kt = (a.N + kKT - 1) / kKT;
   const int units = a.B * a.h_kv;
-  const int sms = a.num_sms > 0 ? a.num_sms : 148;
-  // (batch, group) units per scheduling block: about two waves of items
-  int per = (2 * sms + n_kt - 1) / n_kt;
-  if (per < 1) per = 1;
-  if (per > units) per = units;
-  v2_bwd_main_kernel<D><<<n_kt * units, kThreads, kSmemBytes, s>>>(tq, tk, tv, tg, tdo, tdq, a, w, per);
+  v2_bwd_main_kernel<D><<<n_kt * units, kThreads, kSmemBytes, s>>>(tq, tk, tv, tg, tdo, tdq, a, w);
   e = cudaGetLastError();
   if (e != cudaSuccess) return e;
 
+  const int sms = a.num_sms > 0 ? a.num_sms : 148;
   const long long work = T * 2 * a.h * (D / 8);
   int grid = static_cast<int>((work + 255) / 256);
   if (grid > 8 * sms) grid = 8 * sms;
