@@ -210,6 +210,30 @@ __device__ __forceinline__ void st_zero_f32(float* p) {
     *reinterpret_cast<float2*>(p) = make_float2(0.f, 0.f);
   }
 }
+// The grouped preprocess zeroes the dQ accumulators of a (token, group) -
+// (r + 1) contiguous rows - with bulk copies (the TMA unit writes them, not
+// the load/store path the kernel's reads use): each block keeps a zeroed
+// buffer of kZeroBytes in shared memory, and each warp copies it over its
+// rows.  (For the two rows of a V2 pair the per-lane stores measured faster:
+// 205 against 228 us at B2 N8192 with 64 query heads.)
+constexpr int kZeroBytes = 4096;
+__device__ __forceinline__ void zero_init(float* zbuf) {
+  for (int i = threadIdx.x; i < kZeroBytes / 16; i += blockDim.x)
+    reinterpret_cast<float4*>(zbuf)[i] = make_float4(0.f, 0.f, 0.f, 0.f);
+  fence_proxy_async_smem();
+  __syncthreads();
+}
+// `bytes` (a multiple of 16) of zeros at dst (16-byte aligned), one lane
+__device__ __forceinline__ void bulk_zero(float* dst, const float* zbuf, uint32_t bytes) {
+  for (uint32_t off = 0; off < bytes; off += kZeroBytes) {
+    const uint32_t n = min(bytes - off, static_cast<uint32_t>(kZeroBytes));
+    asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(
+                     reinterpret_cast<uint8_t*>(dst) + off),
+                 "r"(smem_u32(zbuf)), "r"(n)
+                 : "memory");
+  }
+  bulk_commit();
+}
 
 // one warp per (token, pair); lane = D / 32 consecutive features
 template <int D>
@@ -296,6 +320,8 @@ template <int D>
 __global__ void __launch_bounds__(kPreWarps * 32)
 grouped_bwd_pre_kernel(V2BwdArgs a, BwdWs w, const float* __restrict__ gate, float* __restrict__ dz) {
   constexpr int kF = D / 32;
+  __shared__ __align__(128) float zbuf[kZeroBytes / 4];
+  zero_init(zbuf);
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int r = a.ratio;
   const int n_groups = 2 * a.h / (r + 1);
@@ -327,6 +353,7 @@ grouped_bwd_pre_kernel(V2BwdArgs a, BwdWs w, const float* __restrict__ gate, flo
   }
   const int64_t tok = static_cast<int64_t>(b) * a.N + n;
   const int64_t qrow0 = tok * 2 * a.h;
+  if (lane == 0) bulk_zero(w.dq + (qrow0 + hq0) * D, zbuf, (r + 1) * D * 4);  // the group's dQ rows
   for (int i = 0; i < r; ++i) {
     const int p = gi * r + i;
     const __nv_bfloat16* gp = static_cast<const __nv_bfloat16*>(a.dout.ptr) + b * a.dout.sb +
@@ -348,7 +375,6 @@ grouped_bwd_pre_kernel(V2BwdArgs a, BwdWs w, const float* __restrict__ gate, flo
       ds += __shfl_xor_sync(0xffffffffu, ds, o);
       gn += __shfl_xor_sync(0xffffffffu, gn, o);
     }
-    st_zero_f32<kF>(w.dq + (qrow0 + hq0 + i) * D + lane * kF);
     if (lane == 0) {
       const int64_t le = (static_cast<int64_t>(b) * 2 * a.h + hq0 + i) * a.N + n;
       w.lse2[srow(hq0 + i)] = a.lse[le] * 1.4426950408889634f;
@@ -373,8 +399,8 @@ grouped_bwd_pre_kernel(V2BwdArgs a, BwdWs w, const float* __restrict__ gate, flo
   } else {
     *reinterpret_cast<uint32_t*>(dst) = pk[0];
   }
-  st_zero_f32<kF>(w.dq + (qrow0 + noise) * D + lane * kF);
   if (lane == 0) {
+    bulk_wait_read();
     const int64_t le = (static_cast<int64_t>(b) * 2 * a.h + noise) * a.N + n;
     w.lse2[srow(noise)] = a.lse[le] * 1.4426950408889634f;
     w.D[srow(noise)] = dd;
