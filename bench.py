@@ -764,15 +764,21 @@ class ClockSampler:
         self.lines = []
 
     def start(self):
+        """Start sampling every 50 ms and return once the first sample is in
+        (at most 3 s), so that a short timed region is bracketed by samples."""
         try:
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--query-gpu={self.Q}", "--format=csv,noheader,nounits",
-                 "-lms", "200", "-i", str(self.index)],
+                 "-lms", "50", "-i", str(self.index)],
                 stdout=subprocess.PIPE, stderr=subprocess.DEVNULL, text=True)
             self.thread = threading.Thread(target=self._read, daemon=True)
             self.thread.start()
         except Exception:  # noqa: BLE001
             self.proc = None
+            return
+        t0 = time.time()
+        while not self.lines and self.proc.poll() is None and time.time() - t0 < 3.0:
+            time.sleep(0.005)
 
     def _read(self):
         for line in self.proc.stdout:
@@ -781,6 +787,11 @@ class ClockSampler:
     def stop(self):
         if self.proc is None:
             return None
+        # one more sample after the region ends (at most 1 s): the timed
+        # region can be shorter than the sampling interval
+        n0, t0 = len(self.lines), time.time()
+        while len(self.lines) <= n0 and self.proc.poll() is None and time.time() - t0 < 1.0:
+            time.sleep(0.005)
         self.proc.terminate()
         try:
             self.proc.wait(timeout=5)
@@ -803,7 +814,8 @@ class ClockSampler:
         if not sm:
             return None
         return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(smax),
-                "reasons": sorted(reasons), "samples": len(sm)}
+                "reasons": sorted(reasons), "samples": len(sm),
+                "window": "every 50 ms from just before the timed region to just after it"}
 
 
 def dist_env():
