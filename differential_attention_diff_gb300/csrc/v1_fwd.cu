@@ -668,7 +668,6 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
 #pragma unroll 1
         for (int e = 0; e < kHalf; e += 8) {
           float v[8];
-#pragma unroll
           *reinterpret_cast<float4*>(&v[0]) = ld_cg_f32x4(partner_x + (e / 4) * 128);
           *reinterpret_cast<float4*>(&v[4]) = ld_cg_f32x4(partner_x + (e / 4 + 1) * 128);
           *reinterpret_cast<uint4*>(o2b + o2row + e) = pack8(v);
