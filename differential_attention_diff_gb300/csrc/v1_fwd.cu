@@ -64,12 +64,15 @@ constexpr int kSmemBytes = kOffBar + 2048 + 1024;  // 232448: the per-block limi
 constexpr size_t kXchgOff = 256;
 constexpr size_t kXchgBytes = 128 * 128 * 4;
 
+// K stages land per 64-column box ([stage][box]) and V stages per 64-key half
+// ([stage][half]), so that a tile's first MMAs start before the rest of it
+// has arrived
 enum {
-  B_QFULL = 0, B_QEMPTY, B_KFULL, B_KFULL1, B_KEMPTY, B_KEMPTY1, B_VFULL, B_VFULL1,
-  B_VEMPTY, B_VEMPTY1, B_SFULL, B_SFULL1, B_PFULL, B_PFULL1, B_ORDY, B_ODONE, B_EPI, B_OFREE, B_XRDY,
+  B_QFULL = 0, B_QEMPTY, B_KFULL, B_KEMPTY = B_KFULL + 4, B_VFULL = B_KEMPTY + 2, B_VEMPTY = B_VFULL + 4,
+  B_SFULL = B_VEMPTY + 2, B_PFULL = B_SFULL + 2, B_ORDY = B_PFULL + 2, B_ODONE, B_EPI, B_OFREE, B_XRDY,
   B_SSQ, B_SSQ1, B_SCHF, B_SCHE = B_SCHF + 4, B_COUNT = B_SCHE + 4
 };
-static_assert(B_COUNT * 8 <= 256, "barriers end where the TMEM slot begins");
+static_assert(B_COUNT * 8 <= 320, "barriers end where the TMEM slot begins");
 
 constexpr uint32_t kIdescS = idesc_bf16(128, 128, 0);
 
@@ -77,18 +80,18 @@ struct Shared {
   uint32_t base;
   uint8_t* gen;
   __device__ uint32_t bar(int i) const { return base + kOffBar + 8 * i; }
-  __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(gen + kOffBar + 256); }
+  __device__ uint32_t* tmem_slot() const { return reinterpret_cast<uint32_t*>(gen + kOffBar + 320); }
   __device__ volatile int* abort_flag() const {
-    return reinterpret_cast<volatile int*>(gen + kOffBar + 264);
+    return reinterpret_cast<volatile int*>(gen + kOffBar + 328);
   }
-  __device__ float* lam() const { return reinterpret_cast<float*>(gen + kOffBar + 268); }
+  __device__ float* lam() const { return reinterpret_cast<float*>(gen + kOffBar + 332); }
   // ring of the next work items (4 slots), written by rank 0's producer
-  __device__ volatile int* ring() const { return reinterpret_cast<volatile int*>(gen + kOffBar + 272); }
-  __device__ uint32_t ring_s(int slot) const { return base + kOffBar + 272 + 4 * slot; }
+  __device__ volatile int* ring() const { return reinterpret_cast<volatile int*>(gen + kOffBar + 336); }
+  __device__ uint32_t ring_s(int slot) const { return base + kOffBar + 336 + 4 * slot; }
   // softmax -> epilogue hand-off of one item: its index, and each row's two
   // half sums of l, float[2][128] (on the rare tile that raises a row's max,
   // the softmax warpgroups swap their half maxima through the same slots)
-  __device__ volatile int* epi_item() const { return reinterpret_cast<volatile int*>(gen + kOffBar + 288); }
+  __device__ volatile int* epi_item() const { return reinterpret_cast<volatile int*>(gen + kOffBar + 352); }
   __device__ volatile float* epi_l() const { return reinterpret_cast<volatile float*>(gen + kOffBar + 1024); }
   // the partner's per-row partial sums of squares, float[128]: one slot
   // serves every item, since the partner sends an item's sums only after it
@@ -211,7 +214,7 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
     sh.base = al;
     sh.gen = smem_raw + (al - raw);
   }
-  constexpr int kDqk = DQK, kDv = DV;
+  constexpr int kDv = DV;
   constexpr int kNQ = DQK / 64, kNV = DV / 64;  // 64-column boxes per tile row
   constexpr int kOffQ = 0, kOffK = kNQ * kBox, kOffV = 3 * kNQ * kBox;
   constexpr int kHalf = DV / 2;                 // output columns each CTA finishes
@@ -233,9 +236,11 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
     mbar_init(sh.bar(B_QFULL), 1);
     mbar_init(sh.bar(B_QEMPTY), 1);
     for (int s = 0; s < 2; ++s) {
-      mbar_init(sh.bar(B_KFULL + s), 1);
+      mbar_init(sh.bar(B_KFULL + 2 * s), 1);
+      mbar_init(sh.bar(B_KFULL + 2 * s + 1), 1);
       mbar_init(sh.bar(B_KEMPTY + s), 1);
-      mbar_init(sh.bar(B_VFULL + s), 1);
+      mbar_init(sh.bar(B_VFULL + 2 * s), 1);
+      mbar_init(sh.bar(B_VFULL + 2 * s + 1), 1);
       mbar_init(sh.bar(B_VEMPTY + s), 2);  // both CTAs' P.V commits
       mbar_init(sh.bar(B_SFULL + s), 1);
       mbar_init(sh.bar(B_PFULL + s), 256);
@@ -350,18 +355,24 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
             const int st = kv & 1, use = kv >> 1;
             if (qk) {
               if (use > 0 && !wait_bar(sh, sh.bar(B_KEMPTY + st), (use - 1) & 1, a.status, 0x3002)) { ok = false; break; }
-              mbar_arrive_expect_tx(sh.bar(B_KFULL + st), kNQ * kBox);
-              for (int box = 0; box < kNQ; ++box)
-                tma_load_4d(sh.base + kOffK + (st * kNQ + box) * kBox, tk, sh.bar(B_KFULL + st), box * 64, w.h,
-                            j * kBN, w.b);
+              for (int box = 0; box < kNQ; ++box) {
+                mbar_arrive_expect_tx(sh.bar(B_KFULL + 2 * st + box), kBox);
+                tma_load_4d(sh.base + kOffK + (st * kNQ + box) * kBox, tk, sh.bar(B_KFULL + 2 * st + box), box * 64,
+                            w.h, j * kBN, w.b);
+              }
               if (rank == 0 && j == min(1, w.n_kv - 1)) next = publish(it + 1);
             } else {
               if (use > 0 && !wait_bar(sh, sh.bar(B_VEMPTY + st), (use - 1) & 1, a.status, 0x3003)) { ok = false; break; }
-              // the whole tile lands here: this CTA's half and the partner's
-              mbar_arrive_expect_tx(sh.bar(B_VFULL + st), kNV * kBox);
-              for (int box = static_cast<int>(rank) * (kNV / 2); box < (static_cast<int>(rank) + 1) * (kNV / 2); ++box)
-                tma_load_4d_mc(sh.base + kOffV + (st * kNV + box) * kBox, &tm_v, sh.bar(B_VFULL + st), box * 64, w.h,
-                               j * kBN, w.b, 3);
+              // each 64-key half of the tile lands whole here: this CTA's
+              // column boxes and the partner's (64-row boxes: the second
+              // half sits 8 KB into each 128-row box, the swizzle unchanged)
+              for (int half = 0; half < 2; ++half) {
+                mbar_arrive_expect_tx(sh.bar(B_VFULL + 2 * st + half), kNV * (kBox / 2));
+                for (int box = static_cast<int>(rank) * (kNV / 2); box < (static_cast<int>(rank) + 1) * (kNV / 2);
+                     ++box)
+                  tma_load_4d_mc(sh.base + kOffV + (st * kNV + box) * kBox + half * (kBox / 2), &tm_v,
+                                 sh.bar(B_VFULL + 2 * st + half), box * 64, w.h, j * kBN + half * 64, w.b, 3);
+              }
             }
           }
         }
@@ -378,19 +389,24 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
         int kv = 0, it = 0;
         bool ok = true;
         const uint32_t t_o = tmem + 256;
-        auto issue_s = [&](int g) {  // S of global tile g into buffer g & 1
+        // S of global tile g into buffer g & 1, each 64-column box of K as
+        // soon as it has landed (false on a failed wait)
+        auto issue_s = [&](int g) -> bool {
           const int st = g & 1;
           const uint32_t kb = sh.base + kOffK + st * kNQ * kBox;
           const uint32_t qa = sh.base + kOffQ;
   #pragma unroll
-          for (int kk = 0; kk < kDqk / 16; ++kk) {
-            const uint32_t off = (kk >> 2) * kBox + (kk & 3) * 32;
-            tc_mma_ss(tmem + (g & 1) * 128, sdesc_sw128(qa + off, 16, 1024),
-                      sdesc_sw128(kb + off, 16, 1024), kIdescS, kk > 0);
+          for (int box = 0; box < kNQ; ++box) {
+            if (!wait_bar(sh, sh.bar(B_KFULL + 2 * st + box), (g >> 1) & 1, a.status, 0x3102)) return false;
+            tc_fence_after();
+  #pragma unroll
+            for (int kq = 0; kq < 4; ++kq) {
+              const uint32_t off = box * kBox + kq * 32;
+              tc_mma_ss(tmem + st * 128, sdesc_sw128(qa + off, 16, 1024), sdesc_sw128(kb + off, 16, 1024),
+                        kIdescS, (box | kq) != 0 ? 1u : 0u);
+            }
           }
-        };
-        auto wait_k = [&](int g) {
-          return wait_bar(sh, sh.bar(B_KFULL + (g & 1)), (g >> 1) & 1, a.status, 0x3102);
+          return true;
         };
         for (;; ++it) {
           const int i = consume(it);
@@ -401,9 +417,7 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
           if (!wait_bar(sh, sh.bar(B_QFULL), it & 1, a.status, 0x3101)) { ok = false; break; }
           tc_fence_after();
           for (int j = 0; j < 2 && j < n; ++j) {
-            if (!wait_k(kv + j)) { ok = false; break; }
-            tc_fence_after();
-            issue_s(kv + j);
+            if (!issue_s(kv + j)) { ok = false; break; }
             tc_commit(sh.bar(B_KEMPTY + ((kv + j) & 1)));
             tc_commit(sh.bar(B_SFULL + ((kv + j) & 1)));
             if (j == n - 1) tc_commit(sh.bar(B_QEMPTY));
@@ -417,19 +431,28 @@ v1_fwd_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_constant__
               break;
             }
             if (!wait_bar(sh, sh.bar(B_PFULL + st), (g >> 1) & 1, a.status, 0x3103)) { ok = false; break; }
-            if (!wait_bar(sh, sh.bar(B_VFULL + st), (g >> 1) & 1, a.status, 0x3104)) { ok = false; break; }
-            tc_fence_after();
             const uint32_t vb = sh.base + kOffV + st * kNV * kBox;
+            // each 64-key half of V as soon as it has landed; P of keys
+            // 64 h .. 64 h + 63 sits at columns 64 h .. of the buffer
   #pragma unroll
-            for (int kk = 0; kk < kBN / 16; ++kk)  // P of keys 64 h.. at columns 64 h.. of the buffer
-              tc_mma_ts(t_o, tmem + st * 128 + (kk >> 2) * 64 + (kk & 3) * 8,
-                        sdesc_sw128(vb + kk * 2048, kBox, 1024), kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+            for (int half = 0; half < 2 && ok; ++half) {
+              if (!wait_bar(sh, sh.bar(B_VFULL + 2 * st + half), (g >> 1) & 1, a.status, 0x3104)) {
+                ok = false;
+                break;
+              }
+              tc_fence_after();
+  #pragma unroll
+              for (int kq = 0; kq < 4; ++kq) {
+                const int kk = half * 4 + kq;
+                tc_mma_ts(t_o, tmem + st * 128 + half * 64 + kq * 8, sdesc_sw128(vb + kk * 2048, kBox, 1024),
+                          kIdescPV, (j > 0 || kk > 0) ? 1u : 0u);
+              }
+            }
+            if (!ok) break;
             tc_commit_mc(sh.bar(B_VEMPTY + st), 3);  // the stage is free in both CTAs
             tc_commit(sh.bar(B_ODONE));
             if (j + 2 < n) {
-              if (!wait_k(g + 2)) { ok = false; break; }
-              tc_fence_after();
-              issue_s(g + 2);
+              if (!issue_s(g + 2)) { ok = false; break; }
               tc_commit(sh.bar(B_KEMPTY + st));
               tc_commit(sh.bar(B_SFULL + st));
               if (j + 2 == n - 1) tc_commit(sh.bar(B_QEMPTY));
@@ -738,7 +761,7 @@ cudaError_t launch_dims(const V1FwdArgs& a, cudaStream_t s) {
       !encode_tmap_bf16_4d(&tq2, a.q2, a.B, a.N, a.H, kDqk, kBM) ||
       !encode_tmap_bf16_4d(&tk1, a.k1, a.B, a.N, a.H, kDqk, kBN) ||
       !encode_tmap_bf16_4d(&tk2, a.k2, a.B, a.N, a.H, kDqk, kBN) ||
-      !encode_tmap_bf16_4d(&tv, a.v, a.B, a.N, a.H, kDv, kBN))
+      !encode_tmap_bf16_4d(&tv, a.v, a.B, a.N, a.H, kDv, kBN / 2))
     return cudaErrorInvalidValue;
   cudaError_t e = cudaFuncSetAttribute(v1_fwd_kernel<DQK, DV>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                        kSmemBytes);
