@@ -73,6 +73,20 @@ def test_v1_fwd_parity_small(B, N, H, layer):
     _check(t, li, y, sv)
 
 
+@pytest.mark.parametrize("causal", [True, False])
+@pytest.mark.parametrize("N", [128, 250])
+def test_v1_fwd_many_short_items(N, causal):
+    """B8 H16: 128 or 256 items of one or two key tiles, more than the CTA
+    pairs, so every pair runs item after item with short main loops: the
+    work ring, the producers' stages and the O hand-off to the epilogue turn
+    over at every tile or two."""
+    t = synth.v1_inputs(8, N, 16, 128, 256, "bf16", seed=4500 + N, device="cuda")
+    li = bd.diffattn_lambda_init(3)
+    y, sv = bd.diffattn_v1_fwd(*(t[n] for n in NAMES), li, save=True, causal=causal)
+    torch.cuda.synchronize()
+    _check(t, li, y, sv, causal=causal)
+
+
 @pytest.mark.parametrize("B,N,H,layer", [(1, 200, 2, 1), (2, 300, 3, 14), (1, 1, 1, 28), (1, 700, 2, 5)])
 def test_v1_fwd_parity_head_dims_64_128(B, N, H, layer):
     """Head dims (64, 128): one 64-column box per Q/K tile row, 32 KB of
