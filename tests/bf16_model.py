@@ -3,7 +3,8 @@
 Each runs the chain rule in exact fp64 EXCEPT at the points where the
 library's backward must hold bf16 values.  V1: the forward outputs Y and O2,
 the upstream gradient after the RMSNorm backward (dO, an MMA operand), and the
-P and dS tiles fed to the tensor cores.  V2: the saved per-head outputs O_j,
+P and dS tiles fed to the tensor cores; for the training step the forward's
+own P.V operand as well (``rounded_forward``).  V2: the saved per-head outputs O_j,
 the odd heads' dO = -g dOut (an MMA operand), the P and dS tiles, and the
 bf16 gradient outputs.  A model's error against the fp64 oracle is the error
 any bf16 implementation with these storage points has; the GPU parity tests
@@ -16,6 +17,45 @@ import torch
 
 def bf16(x):
     return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
+
+
+def rounded_forward(f, fwd, li, causal=True, rms_weight=None, eps=1e-5, rnd=bf16):
+    """The V1 forward with its own bf16 storage points, for the bars of the
+    training step (the library's forward, then its backward on the forward's
+    saves).  fp64 everywhere EXCEPT: P = exp(S - m) (m the row max) is rounded
+    before the product with V, as the P.V operand of a bf16 tensor-core
+    forward must be, while the row sum l takes the unrounded P (an fp32
+    accumulation); Y = c w (O1 - lambda O2) rstd and O2 are stored rounded.
+    f: fp64 inputs as in ``rounded_backward``; fwd: the oracle forward on
+    them (lambda and the LSEs are taken from it).  Returns fwd with y, o2 and
+    rstd replaced; with rnd the identity it reproduces the oracle forward's.
+    Under strong cancellation between the streams (lambda near 1, long rows)
+    the rounded P dominates the step's gradient error, which the backward
+    model fed exact forward outputs does not contain."""
+    lam, c = fwd["lam"], 1.0 - li
+    B, N, H, dqk = f["q1"].shape
+    dv = f["v"].shape[3]
+    s = 1.0 / np.sqrt(dqk)
+    w = np.ones(dv) if rms_weight is None else rms_weight
+    y = np.zeros((B, N, H, dv))
+    o2 = np.zeros((B, N, H, dv))
+    rstd = np.zeros((B, H, N))
+    keep = np.tril(np.ones((N, N), bool)) if causal else np.ones((N, N), bool)
+    for b in range(B):
+        for h in range(H):
+            O = []
+            for t in (1, 2):
+                S = np.where(keep, s * f[f"q{t}"][b, :, h] @ f[f"k{t}"][b, :, h].T, -np.inf)
+                P = np.exp(S - S.max(1, keepdims=True))
+                O.append((rnd(P) @ f["v"][b, :, h]) / P.sum(1, keepdims=True))
+            d = O[0] - lam * O[1]
+            r = 1.0 / np.sqrt(np.mean(d * d, 1) + eps)
+            rstd[b, h] = r
+            y[b, :, h] = rnd(c * w * d * r[:, None])
+            o2[b, :, h] = rnd(O[1])
+    out = dict(fwd)
+    out.update(y=y, o2=o2, rstd=rstd)
+    return out
 
 
 def rounded_backward(f, fwd, li, heads=None, causal=True, rms_weight=None):

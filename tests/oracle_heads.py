@@ -26,27 +26,31 @@ LAM_GRADS = ("dlq1", "dlk1", "dlq2", "dlk2")
 
 
 def _one_head(task):
-    from bf16_model import rounded_backward
+    from bf16_model import rounded_backward, rounded_forward
     from oracle import diffattn_oracle as orc
 
-    f, li, causal = task
+    f, li, causal, step = task
     ref = orc.v1_backward(*(f[n] for n in NAMES), li, f["dy"], causal=causal)
     fwd = orc.v1_forward(*(f[n] for n in NAMES), li, causal=causal)
+    if step:
+        fwd = rounded_forward(f, fwd, li, causal=causal)
     model = rounded_backward(f, fwd, li, causal=causal)
     keep = HEAD_GRADS + LAM_GRADS + ("dlam",)
     return {n: ref[n] for n in keep}, {n: model[n] for n in HEAD_GRADS + ("dlam",)}
 
 
-def v1_backward_by_head(f, li, causal=True, workers=None):
+def v1_backward_by_head(f, li, causal=True, workers=None, step=False):
     """f: fp64 arrays of the V1 inputs and dy ([B, N, H, D]; lambda vectors
     [d_qk]).  Returns (ref, model) for every head, in the layout of
-    ``orc.v1_backward`` / ``rounded_backward`` on the whole problem."""
+    ``orc.v1_backward`` / ``rounded_backward`` on the whole problem; with
+    step=True the model also rounds the forward's storage points
+    (``rounded_forward``), as for the training step."""
     B, N, H, _ = f["q1"].shape
     tasks = []
     for b in range(B):
         for h in range(H):
             fh = {n: (f[n][b:b + 1, :, h:h + 1] if f[n].ndim == 4 else f[n]) for n in NAMES + ("dy",)}
-            tasks.append((fh, li, causal))
+            tasks.append((fh, li, causal, step))
     if workers is None:
         workers = max(1, min(len(tasks), (os.cpu_count() or 4) // 4))
     if workers == 1:

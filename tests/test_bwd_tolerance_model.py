@@ -19,7 +19,7 @@ import numpy as np
 import torch
 
 from differential_attention_diff_gb300 import synth
-from bf16_model import rounded_backward, rounded_backward_grouped, rounded_backward_v2
+from bf16_model import rounded_backward, rounded_backward_grouped, rounded_backward_v2, rounded_forward
 from oracle import diffattn_oracle as orc
 
 
@@ -82,3 +82,42 @@ def test_grouped_rounding_model_is_the_chain_rule_and_sets_the_tolerance():
     b = rounded_backward_v2(f2, fwd2, ref2["gate"])
     for n in ("dq", "dk", "dv", "dz", "dx", "dw"):
         np.testing.assert_allclose(a[n], b[n], rtol=1e-12, atol=1e-12 * np.abs(b[n]).max())
+
+
+def test_v1_forward_rounding_model_and_the_step_bar():
+    """The V1 forward model behind the training step's bar.  Without rounding
+    it reproduces the oracle forward (Y, O2, rstd), so it rounds the right
+    quantities of the right formula.  With its bf16 points, the forward's Y
+    error stays inside the forward tests' 2e-2 * RMS(V).  Under strong
+    cancellation between the streams (lambda vectors chosen so that
+    lambda = 1 at layer 13: O1 - O2 is small in long rows, and rstd large),
+    the backward fed the rounded forward has several times the dQ/dK error
+    of the backward fed exact forward outputs.  That is why the step's
+    max-abs bar takes the forward-aware model.  Its Frobenius error stays
+    well under the step's fixed 2e-2 bar."""
+    names = ("q1", "q2", "k1", "k2", "v", "lq1", "lk1", "lq2", "lk2")
+    t = synth.v1_inputs(1, 256, 2, 64, 128, "bf16", seed=5221, device="cpu", with_dy=True)
+    f = {k: v.to(torch.float64).numpy() for k, v in t.items()}
+    li = float(np.float32(orc.lambda_init(13)))
+    # lambda = exp(lq1.lk1) - exp(lq2.lk2) + lambda_init = 1
+    e0 = np.zeros(64)
+    e0[0] = np.sqrt(np.log(2.0 - li))
+    f["lq1"] = f["lk1"] = e0
+    f["lq2"] = f["lk2"] = np.zeros(64)
+    fwd = orc.v1_forward(*(f[n] for n in names), li)
+    assert abs(fwd["lam"] - 1.0) < 1e-12
+    exact = rounded_forward(f, fwd, li, rnd=lambda a: a)
+    np.testing.assert_allclose(exact["y"], fwd["y"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(exact["o2"], fwd["o2"], rtol=0, atol=1e-12)
+    np.testing.assert_allclose(exact["rstd"], fwd["rstd"], rtol=1e-12)
+    rf = rounded_forward(f, fwd, li)
+    rms_v = float(np.sqrt(np.mean(f["v"] ** 2)))
+    assert np.max(np.abs(rf["y"] - fwd["y"])) <= 2e-2 * rms_v
+    ref = orc.v1_backward(*(f[n] for n in names), li, f["dy"])
+    bwd_only = rounded_backward(f, fwd, li)
+    step = rounded_backward(f, rf, li)
+    grow = max(np.max(np.abs(step[n] - ref[n])) / np.max(np.abs(bwd_only[n] - ref[n]))
+               for n in ("dq1", "dq2", "dk1", "dk2"))
+    assert grow > 2.0, grow
+    for n in ("dq1", "dq2", "dk1", "dk2", "dv"):
+        assert np.linalg.norm(step[n] - ref[n]) / np.linalg.norm(ref[n]) < 0.5 * 2e-2, n

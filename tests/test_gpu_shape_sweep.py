@@ -1,0 +1,244 @@
+"""A seeded sweep of drawn shapes through every entry point against the fp64
+oracle, with the bars of the fixed-shape parity tests (their checks are
+reused as they are): batch, length (one token, under a tile, whole tiles,
+ragged tails over several tiles), head counts and group sizes, head dims,
+causal or not, the layer index, an RMSNorm weight, decode lengths and split
+counts are drawn together, so that combinations the hand-picked cases leave
+out are run as well.  The draws are fixed by the seed; the CPU test checks
+that every drawn shape is one the entry points accept and that the sweep
+spans the categories it claims."""
+
+import random
+
+import numpy as np
+import pytest
+import torch
+
+SEED = 7309
+CASES = 6
+
+# length categories, cycled over a sweep's cases: under one 128-row tile,
+# whole tiles, ragged over several tiles
+def _length(rng, i, cap):
+    kind = i % 3
+    if kind == 0:
+        return rng.choice([1, rng.randint(2, 127)])
+    if kind == 1:
+        return 128 * rng.randint(1, cap // 128)
+    return 128 * rng.randint(1, cap // 128 - 1) + rng.randint(1, 127)
+
+
+def sweep_cases(op, n=CASES, seed=SEED):
+    rng = random.Random(f"{op}/{seed}")
+    cases = []
+    for i in range(n):
+        causal = i % 2 == 0 or rng.random() < 0.5
+        if op in ("v1_fwd", "v1_bwd"):
+            dqk, dv = rng.choice([(128, 256), (64, 128)])
+            cap = 700 if op == "v1_fwd" else 400
+            cases.append(dict(B=rng.randint(1, 3), N=_length(rng, i, cap), H=rng.randint(1, 3 if op == "v1_bwd" else 4),
+                              dqk=dqk, dv=dv, causal=causal, layer=rng.randint(1, 28),
+                              weighted=rng.random() < 0.3))
+        elif op in ("v2_fwd", "v2_bwd"):
+            hkv = rng.choice([1, 2, 4])
+            per = rng.choice([1, 2] if op == "v2_bwd" else [1, 2, 4])  # head pairs per K/V head
+            cap = 700 if op == "v2_fwd" else 400
+            cases.append(dict(B=rng.randint(1, 3), N=_length(rng, i, cap), h=hkv * per, hkv=hkv,
+                              d=rng.choice([64, 128]), dm=rng.choice([64, 128, 192, 256]), causal=causal))
+        elif op in ("grouped_fwd", "grouped_bwd"):
+            ratio = rng.choice([2, 3, 4])
+            hkv = rng.choice([1, 2])
+            # query heads per K/V head, (ratio + 1) * groups per K/V head,
+            # must be even
+            groups = hkv * (rng.choice([1, 2]) if ratio % 2 else 2)
+            cap = 600 if op == "grouped_fwd" else 300
+            cases.append(dict(B=rng.randint(1, 2), N=_length(rng, i, cap), h=groups * ratio, ratio=ratio, hkv=hkv,
+                              d=rng.choice([64, 128]), dm=rng.choice([128, 256]), causal=causal))
+        elif op == "v2_decode":
+            hkv = rng.choice([1, 2, 8])
+            B = rng.randint(1, 4)
+            L = rng.randint(1, 3000)
+            seqlens = [L] + [rng.randint(1, L) for _ in range(B - 1)]
+            cases.append(dict(B=B, L=L, h=hkv * rng.choice([1, 2, 4]), hkv=hkv, d=rng.choice([64, 128]),
+                              dm=rng.choice([64, 256]), seqlens=seqlens, splits=rng.choice([0, 1, 2, 3, 5])))
+        elif op == "v1_decode":
+            B = rng.randint(1, 4)
+            L = rng.randint(1, 3000)
+            seqlens = [L] + [rng.randint(1, L) for _ in range(B - 1)]
+            dqk, dv = rng.choice([(128, 256), (64, 128)])
+            cases.append(dict(B=B, L=L, H=rng.randint(1, 4), dqk=dqk, dv=dv, seqlens=seqlens,
+                              splits=rng.choice([0, 1, 2, 3, 5]), layer=rng.randint(1, 28),
+                              weighted=rng.random() < 0.3))
+        else:
+            raise ValueError(op)
+    return cases
+
+
+OPS = ("v1_fwd", "v1_bwd", "v2_fwd", "v2_bwd", "grouped_fwd", "grouped_bwd", "v2_decode", "v1_decode")
+
+
+def _ids(op):
+    return [f"{op}-{i}" for i in range(CASES)]
+
+
+def test_sweep_shapes_are_valid():
+    """Every drawn shape satisfies the entry points' documented constraints,
+    and each sweep spans short, whole-tile and ragged lengths (decode:
+    several lengths and split counts)."""
+    for op in OPS:
+        cases = sweep_cases(op)
+        assert len(cases) == CASES
+        assert sweep_cases(op) == cases  # fixed by the seed
+        for c in cases:
+            if op.startswith("v2") and op != "v2_decode":
+                assert c["h"] % c["hkv"] == 0 and c["dm"] % 64 == 0 and c["d"] in (64, 128)
+            if op.startswith("grouped"):
+                groups = c["h"] // c["ratio"]
+                assert c["h"] % c["ratio"] == 0 and groups % c["hkv"] == 0
+                G = groups * (c["ratio"] + 1) // c["hkv"]  # query heads per K/V head
+                assert G % (c["ratio"] + 1) == 0 and G % 2 == 0
+            if op.endswith("decode"):
+                assert len(c["seqlens"]) == c["B"] and max(c["seqlens"]) == c["L"]
+                assert all(1 <= s <= c["L"] for s in c["seqlens"])
+            if op == "v2_decode":
+                assert c["h"] % c["hkv"] == 0
+            if op.startswith("v1") and op != "v1_decode":
+                assert (c["dqk"], c["dv"]) in ((128, 256), (64, 128))
+        if not op.endswith("decode"):
+            ns = [c["N"] for c in cases]
+            assert any(n < 128 for n in ns) and any(n % 128 == 0 for n in ns)
+            assert any(n > 128 and n % 128 for n in ns)
+            assert any(c["causal"] for c in cases)
+
+
+# ------------------------------------------------------------------- GPU ----
+
+@pytest.fixture
+def gpu_ops():
+    """The binding and the fixed-shape tests' checks; afterwards the device
+    status word must be clean."""
+    import test_gpu_grouped as tg
+    import test_gpu_grouped_bwd as tgb
+    import test_gpu_small as tsm
+    import test_gpu_v1 as tv1
+    import test_gpu_v1_bwd as tv1b
+    import test_gpu_v1_decode as tv1d
+    import test_gpu_v2 as tv2
+    import test_gpu_v2_bwd as tv2b
+    from differential_attention_diff_gb300 import binding as bd
+    ns = dict(bd=bd, tg=tg, tgb=tgb, tsm=tsm, tv1=tv1, tv1b=tv1b, tv1d=tv1d, tv2=tv2, tv2b=tv2b)
+    yield ns
+    assert bd.diffattn_get_device_status() == bd.DA_OK
+
+
+def _f64(t):
+    return t.detach().to("cpu", torch.float64).numpy()
+
+
+def _rms_weight(n, seed):
+    return 0.5 + torch.rand(n, generator=torch.Generator().manual_seed(seed), dtype=torch.float32).cuda()
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("c", sweep_cases("v1_fwd"), ids=_ids("v1_fwd"))
+def test_sweep_v1_fwd(c, gpu_ops):
+    from differential_attention_diff_gb300 import synth
+    bd, tv1 = gpu_ops["bd"], gpu_ops["tv1"]
+    t = synth.v1_inputs(c["B"], c["N"], c["H"], c["dqk"], c["dv"], "bf16", seed=11000 + c["N"], device="cuda")
+    li = bd.diffattn_lambda_init(c["layer"])
+    w = _rms_weight(c["dv"], 11001) if c["weighted"] else None
+    y, sv = bd.diffattn_v1_fwd(*(t[n] for n in tv1.NAMES), li, save=True, causal=c["causal"], rms_weight=w)
+    torch.cuda.synchronize()
+    tv1._check(t, li, y, sv, causal=c["causal"], w=w)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("c", sweep_cases("v1_bwd"), ids=_ids("v1_bwd"))
+def test_sweep_v1_bwd(c, gpu_ops):
+    from differential_attention_diff_gb300 import synth
+    from oracle import diffattn_oracle as orc
+    bd, tv1b = gpu_ops["bd"], gpu_ops["tv1b"]
+    t = synth.v1_inputs(c["B"], c["N"], c["H"], c["dqk"], c["dv"], "bf16", seed=12000 + c["N"], device="cuda",
+                        with_dy=True)
+    li = float(np.float32(bd.diffattn_lambda_init(c["layer"])))
+    w = _rms_weight(c["dv"], 12001) if c["weighted"] else None
+    wf = None if w is None else _f64(w)
+    ref = orc.v1_backward(*(_f64(t[n]) for n in tv1b.NAMES), li, _f64(t["dy"]), causal=c["causal"], rms_weight=wf)
+    tv1b._compare(tv1b._run_exact_saves(t, li, causal=c["causal"], w=w), ref,
+                  tv1b._model(t, li, causal=c["causal"], w=w), bar="bwd")
+    tv1b._compare(tv1b._run(t, li, causal=c["causal"], w=w), ref,
+                  tv1b._model(t, li, causal=c["causal"], w=w, step=True), bar="step")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("c", sweep_cases("v2_fwd"), ids=_ids("v2_fwd"))
+def test_sweep_v2_fwd(c, gpu_ops):
+    from differential_attention_diff_gb300 import synth
+    from oracle import diffattn_oracle as orc
+    bd, tv2 = gpu_ops["bd"], gpu_ops["tv2"]
+    t = synth.v2_inputs(c["B"], c["N"], c["h"], c["hkv"], c["d"], c["dm"], seed=13000 + c["N"], device="cuda")
+    lse = torch.empty((c["B"], 2 * c["h"], c["N"]), dtype=torch.float32, device="cuda")
+    out = bd.diffattn_v2_fwd(t["q"], t["k"], t["v"], x=t["x"], w_lambda=t["w_lambda"], lse=lse, causal=c["causal"])
+    torch.cuda.synchronize()
+    gate = orc.v2_gate(_f64(t["x"]), _f64(t["w_lambda"]))
+    tv2._check_pairs(t, out, gate, lse=lse, causal=c["causal"])
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("c", sweep_cases("v2_bwd"), ids=_ids("v2_bwd"))
+def test_sweep_v2_bwd(c, gpu_ops):
+    from differential_attention_diff_gb300 import synth
+    tv2b = gpu_ops["tv2b"]
+    t = synth.v2_inputs(c["B"], c["N"], c["h"], c["hkv"], c["d"], c["dm"], seed=14000 + c["N"], device="cuda",
+                        with_dout=True)
+    ref, fwd, model = tv2b._reference(t, causal=c["causal"])
+    tv2b._compare(tv2b._run_exact_saves(t, fwd, causal=c["causal"]), ref, model, bar="bwd")
+    tv2b._compare(tv2b._run(t, causal=c["causal"]), ref, model, bar="step")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("c", sweep_cases("grouped_fwd"), ids=_ids("grouped_fwd"))
+def test_sweep_grouped_fwd(c, gpu_ops):
+    from differential_attention_diff_gb300 import synth
+    bd, tg = gpu_ops["bd"], gpu_ops["tg"]
+    t = synth.grouped_inputs(c["B"], c["N"], c["h"], c["ratio"], c["hkv"], c["d"], c["dm"], seed=15000 + c["N"],
+                             device="cuda")
+    out = bd.diffattn_grouped_fwd(t["q"], t["k"], t["v"], c["ratio"], x=t["x"], w_lambda=t["w_lambda"],
+                                  causal=c["causal"])
+    torch.cuda.synchronize()
+    tg._check(t, c["ratio"], out, causal=c["causal"])
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("c", sweep_cases("grouped_bwd"), ids=_ids("grouped_bwd"))
+def test_sweep_grouped_bwd(c, gpu_ops):
+    tgb = gpu_ops["tgb"]
+    t = tgb._inputs(c["B"], c["N"], c["h"], c["ratio"], c["hkv"], c["d"], c["dm"], seed=16000 + c["N"])
+    ref, model = tgb._reference(t, c["ratio"], causal=c["causal"])
+    tgb._compare(tgb._run_exact_saves(t, c["ratio"], ref, causal=c["causal"]), ref, model, bar="bwd")
+    tgb._compare(tgb._run(t, c["ratio"], causal=c["causal"]), ref, model, bar="step")
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("c", sweep_cases("v2_decode"), ids=_ids("v2_decode"))
+def test_sweep_v2_decode(c, gpu_ops):
+    from differential_attention_diff_gb300 import synth
+    bd, tsm = gpu_ops["bd"], gpu_ops["tsm"]
+    t = synth.decode_inputs(c["B"], c["L"], c["h"], c["hkv"], c["d"], c["dm"], seed=17000 + c["L"], device="cuda",
+                            seqlens=c["seqlens"])
+    out = bd.diffattn_v2_decode(t["q"], t["k_cache"], t["v_cache"], seqlens=t["seqlens"], x=t["x"],
+                                w_lambda=t["w_lambda"], num_splits=c["splits"])
+    torch.cuda.synchronize()
+    tsm._decode_check(t, out)
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("c", sweep_cases("v1_decode"), ids=_ids("v1_decode"))
+def test_sweep_v1_decode(c, gpu_ops):
+    from differential_attention_diff_gb300 import synth
+    bd, tv1d = gpu_ops["bd"], gpu_ops["tv1d"]
+    t = synth.v1_decode_inputs(c["B"], c["L"], c["H"], c["dqk"], c["dv"], seed=18000 + c["L"], device="cuda",
+                               seqlens=c["seqlens"])
+    li = bd.diffattn_lambda_init(c["layer"])
+    w = _rms_weight(c["dv"], 18001) if c["weighted"] else None
+    tv1d._check(t, li, tv1d._run(t, li, num_splits=c["splits"], rms_weight=w), w=w)
