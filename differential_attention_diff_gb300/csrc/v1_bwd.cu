@@ -27,13 +27,15 @@
 //        S^T  = K Q^T          (TMEM, 64 columns)
 //        dP^T = V dO^T         (TMEM, 64 columns)
 //        softmax warps (thread = key row), in two steps so that each overlaps
-//        an MMA: (1) once S^T is in, P = exp2(S^T s log2e - lse2) and
-//          Psig^T = sigma P (sigma = 1 or -lambda) as bf16 over the S^T
-//          columns just read, while dP^T is still being computed;
+//        an MMA: (1) once S^T is in, P = exp2(S^T s log2e - lse2) and P^T
+//          as bf16 over the S^T columns just read, while dP^T is still
+//          being computed;
 //          (2) once dP^T is in, dS^T = sigma s P (dP^T - D) as bf16 into
 //          shared memory, while dV runs
-//        dV  += Psig^T dO      (TMEM, 256 columns; A operand from TMEM),
-//                               issued after step (1)
+//        dV  += P^T dO         (TMEM, 256 columns; A operand from TMEM),
+//                               issued after step (1); the stream's sign
+//                               and lambda (sigma = 1 or -lambda) multiply
+//                               the fp32 accumulator at the end
 //        dQ^T = K^T dS^T       (TMEM, reusing the dP^T columns) -> read by the
 //                               dQ warps, staged in shared memory in two
 //                               halves and added to the fp32 accumulator
@@ -42,8 +44,9 @@
 //                               memory, so that S^T of the next tile can be
 //                               issued right after dV when its Q tile has
 //                               landed, ahead of dQ^T and dK)
-//     At the end each CTA writes its dK; the dV halves of the two streams are
-//     summed through distributed shared memory and written as bf16;
+//     At the end each CTA writes its dK; the dV halves of the two streams,
+//     each times its sigma, are summed through distributed shared memory and
+//     written as bf16;
 //  3. finalize: dQ accumulators -> bf16, and the lambda-vector gradients.
 // Deterministic mode: the main kernel stores each dQ tile (TMA store) into a
 // slot of its own, (key tile, query tile) compacted to the causal tiles, and
@@ -53,7 +56,7 @@
 //
 // Warp roles (320 threads): 0-3 softmax / dS and the epilogue, 4-7 dQ readback
 // and reduce, 8 TMA producer, 9 MMA issuer.  TMEM: [0,256) dV, [256,384) dK,
-// [384,448) S^T (then Psig^T), [448,512) dP^T / dQ^T.  TMEM is full,
+// [384,448) S^T (then P^T), [448,512) dP^T / dQ^T.  TMEM is full,
 // so S^T and dP^T are single-buffered; taking the dQ readback off the softmax
 // warps keeps it out of the per-tile chain.
 // SMEM: K 32 KB, V 64 KB, 2 stages of (Q 16 KB, dO 32 KB), dQ staging of one
@@ -102,7 +105,7 @@ __host__ __device__ constexpr uint32_t idesc2(int M, int N, int a_mn, int b_mn) 
 constexpr uint32_t kIdS = idesc2(128, 64, 0, 0);    // K (K-major) x Q (K-major)
 constexpr uint32_t kIdDP = idesc2(128, 64, 0, 0);   // V (K-major) x dO (K-major)
 constexpr uint32_t kIdDQ = idesc2(128, 64, 1, 1);   // K^T (MN-major) x dS^T (MN-major)
-// per head dims: Psig^T (TMEM) x dO (MN-major) is idesc2(128, DV, 0, 1),
+// per head dims: P^T (TMEM) x dO (MN-major) is idesc2(128, DV, 0, 1),
 // dS^T (TMEM) x Q (MN-major) is idesc2(128, DQK, 0, 1)
 
 __device__ __forceinline__ uint64_t globaltimer() {
@@ -420,7 +423,7 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
   }
   constexpr int kDqk = DQK, kDv = DV;
   constexpr int kNQ = DQK / 64, kNV = DV / 64;  // 64-column boxes per tile row
-  constexpr uint32_t kIdDV = idesc2(128, DV, 0, 1);   // Psig^T (TMEM) x dO (MN-major)
+  constexpr uint32_t kIdDV = idesc2(128, DV, 0, 1);   // P^T (TMEM) x dO (MN-major)
   constexpr uint32_t kIdDK = idesc2(128, DQK, 0, 1);  // dS^T (TMEM) x Q (MN-major)
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t rank = cluster_rank();  // stream index
@@ -589,14 +592,14 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
       for (int k = 0; k < it.n_it && ok; ++k) {
         const int ph = k & 1;
         const uint32_t db = stage(k) + kStageDO, qb = stage(k) + kStageQ;
-        // dV += Psig^T dO as soon as Psig^T is in TMEM (S^T columns 0-31):
+        // dV += P^T dO as soon as P^T is in TMEM (S^T columns 0-31):
         // it runs while the softmax warps form dS^T
         if (!wait_bar(sh, sh.bar(B_PREADY), ph, a.status, 0x4106)) { ok = false; break; }
         tc_fence_after();
 #pragma unroll
         for (int kk = 0; kk < kQT / 16; ++kk)
           tc_mma_ts(T_DV, T_S + kk * 8, sdesc_sw128(db + kk * 2048, kBoxQ, 1024), kIdDV, (k > 0 || kk > 0) ? 1u : 0u);
-        // S^T(k+1) may overwrite Psig^T(k) as soon as dV(k) is issued (in
+        // S^T(k+1) may overwrite P^T(k) as soon as dV(k) is issued (in
         // order on the tensor pipe; dK takes dS^T from shared memory): issue
         // it now when its Q tile has landed, so the softmax warps can start
         // on it while dQ^T(k) and dK(k) run; else after them
@@ -704,7 +707,7 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
     const float sigma = rank == 0 ? 1.f : -lam;
     const float sds = sigma * a.scale;
     const float sl2 = a.scale * 1.4426950408889634f;
-    const uint64_t sl2x2 = f2(sl2, sl2), sds2 = f2(sds, sds), sig2 = f2(sigma, sigma);
+    const uint64_t sl2x2 = f2(sl2, sl2), sds2 = f2(sds, sds);
     const int key = it.kt * kKT + r;
     bool ok = true;
     uint8_t* dsbuf = sh.gen + kOffDS;
@@ -719,8 +722,11 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
       // past N are zero rows of K and V, which give dQ no contribution, and
       // their dK / dV rows are never stored.)
       const bool diag = a.causal && q0 < it.kt * kKT + kKT;
-      // (1) P = exp2(S s log2e - lse2), Psig^T = sigma P (bf16) over the
-      //     S^T columns just read; P stays in registers for dS
+      // (1) P = exp2(S s log2e - lse2), P^T (bf16) over the S^T columns
+      //     just read, the dV MMA's operand; P stays in registers for dS.
+      //     sigma is applied to the fp32 dV accumulator at the end, not to
+      //     this operand: bf16(-lambda P) would make even an exact P = 1
+      //     inexact, and dV = P1^T dO - lambda P2^T dO can cancel strongly
       float p[64];
 #pragma unroll
       for (int hf = 0; hf < 2; ++hf) {
@@ -751,9 +757,8 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
             p[hf * 32 + c + 1] = p1;
             p[hf * 32 + c + 2] = p2;
             p[hf * 32 + c + 3] = p3;
-            const uint64_t s01 = mul_f32x2(f2(p0, p1), sig2), s23 = mul_f32x2(f2(p2, p3), sig2);
-            pw[q4 * 2] = pack_bf16x2(f2_lo(s01), f2_hi(s01));
-            pw[q4 * 2 + 1] = pack_bf16x2(f2_lo(s23), f2_hi(s23));
+            pw[q4 * 2] = pack_bf16x2(p0, p1);
+            pw[q4 * 2 + 1] = pack_bf16x2(p2, p3);
           }
         };
         if (diag) ptile(std::true_type{});
@@ -762,7 +767,7 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
       }
       tmem_st_wait();
       tc_fence_before();
-      mbar_arrive(sh.bar(B_PREADY));  // the dV MMA may read Psig^T
+      mbar_arrive(sh.bar(B_PREADY));  // the dV MMA may read P^T
       // (2) dS^T = sigma s P (dP^T - D) (bf16) into shared memory, the
       //     operand of the dQ^T and dK MMAs (its previous readers, those MMAs
       //     of the tile before, completed before dP^T of this tile was
@@ -828,8 +833,8 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
 #pragma unroll
           for (int e = 0; e < 32; e += 4)
             st_async_v4(rx + ((c * 32 + e) / 4) * 128 * 16,
-                        make_float4(__uint_as_float(v[e]), __uint_as_float(v[e + 1]), __uint_as_float(v[e + 2]),
-                                    __uint_as_float(v[e + 3])),
+                        make_float4(__uint_as_float(v[e]) * sigma, __uint_as_float(v[e + 1]) * sigma,
+                                    __uint_as_float(v[e + 2]) * sigma, __uint_as_float(v[e + 3]) * sigma),
                         rx_bar);
         }
       }
@@ -881,8 +886,9 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
                 *reinterpret_cast<float4*>(&o8[4]) = mine[((c * 32 + e) / 4 + 1) * 128];
 #pragma unroll
                 for (int u = 0; u < 8; ++u) {
-                  // stream 1 + stream 2 in a fixed order on both CTAs
-                  s8[u] = rank == 0 ? __uint_as_float(v[e + u]) + o8[u] : o8[u] + __uint_as_float(v[e + u]);
+                  // stream 1 + sigma stream 2 in a fixed order on both CTAs
+                  const float own = __uint_as_float(v[e + u]) * sigma;
+                  s8[u] = rank == 0 ? own + o8[u] : o8[u] + own;
                 }
                 *reinterpret_cast<uint4*>(dst + c * 32 + e) =
                     make_uint4(pack_bf16x2(s8[0], s8[1]), pack_bf16x2(s8[2], s8[3]),

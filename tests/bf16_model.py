@@ -92,7 +92,9 @@ def rounded_backward(f, fwd, li, heads=None, causal=True, rms_weight=None):
                 dS = bf16(sig * s * P * (dP - D[:, None]))
                 out[f"dq{t}"][b, :, h] = dS @ K
                 out[f"dk{t}"][b, :, h] = dS.T @ Q
-                out["dv"][b, :, h] += bf16(sig * P).T @ dO
+                # the dV operand is P itself; sigma multiplies the stream's
+                # fp32 accumulator when the streams are summed
+                out["dv"][b, :, h] += sig * (bf16(P).T @ dO)
     out["dlam"] = dlam
     return out
 
