@@ -2,9 +2,9 @@
 
 Each runs the chain rule in exact fp64 EXCEPT at the points where the
 library's backward must hold bf16 values.  V1: the forward outputs Y and O2,
-the upstream gradient after the RMSNorm backward (dO, an MMA operand), and the
-P and dS tiles fed to the tensor cores; for the training step the forward's
-own P.V operand as well (``rounded_forward``).  V2: the saved per-head outputs O_j,
+the upstream gradient after the RMSNorm backward (dO, an MMA operand), the
+P and dS tiles fed to the tensor cores, and the bf16 gradient outputs; for the
+training step the forward's own P.V operand as well (``rounded_forward``).  V2: the saved per-head outputs O_j,
 the odd heads' dO = -g dOut (an MMA operand), the P and dS tiles, and the
 bf16 gradient outputs.  A model's error against the fp64 oracle is the error
 any bf16 implementation with these storage points has; the GPU parity tests
@@ -58,44 +58,66 @@ def rounded_forward(f, fwd, li, causal=True, rms_weight=None, eps=1e-5, rnd=bf16
     return out
 
 
-def rounded_backward(f, fwd, li, heads=None, causal=True, rms_weight=None):
-    """f: fp64 inputs (q1..v, dy) as [B, N, H, D]; fwd: the oracle forward on
-    them.  Returns the gradients dq1, dq2, dk1, dk2, dv (and dlam) computed
-    with the bf16 storage points; `heads` restricts to a list of heads;
+def _upstream(f, fw, li, b, h, rms_weight, rnd):
+    """Per (batch, head): the saved Y and O2 as stored, the normalised output
+    yh = Y / (c w), the RMSNorm backward's dO (an MMA operand, so stored) and
+    the per-row terms <dO, O2> whose sum is -dlambda."""
+    c = 1.0 - li
+    Y, O2, rstd = rnd(fw["y"][b, :, h]), rnd(fw["o2"][b, :, h]), fw["rstd"][b, h]
+    G = f["dy"][b, :, h]
+    w = np.ones(Y.shape[1]) if rms_weight is None else rms_weight
+    yh = Y / (c * w)
+    gw = G * w
+    gy = (gw * yh).sum(1, keepdims=True)
+    dO = rnd(c * rstd[:, None] * (gw - yh * gy / Y.shape[1]))
+    return dO, O2, yh, rstd, (dO * O2).sum(1)
+
+
+def rounded_backward(f, fwd, li, heads=None, causal=True, rms_weight=None, rnd=bf16, exact_fwd=None):
+    """f: fp64 inputs (q1..v, dy) as [B, N, H, D]; fwd: the forward on them
+    (the oracle's, or ``rounded_forward``'s for the training step).  Returns
+    the gradients dq1, dq2, dk1, dk2, dv and dlam computed with the bf16
+    storage points (rnd; the identity gives the oracle's chain rule): the
+    saved Y and O2, dO, the MMA operands dS and P, and the gradient outputs
+    themselves (bf16 by the interface).  `heads` restricts to a list of heads;
     causal=False drops the key <= query mask; rms_weight is the forward's
-    RMSNorm weight (None = unit)."""
-    lam, c = fwd["lam"], 1.0 - li
+    RMSNorm weight (None = unit).  With exact_fwd (the oracle forward) it also
+    returns dlam_ss, the sum over rows of the squared differences between this
+    model's per-row terms of dlam = -sum_rows <dO, O2> and the exact ones: the
+    scale of dlam's error when the rows' errors have independent signs."""
+    lam = fwd["lam"]
     B, N, H, dqk = f["q1"].shape
     heads = range(H) if heads is None else heads
     s = 1.0 / np.sqrt(dqk)
     out = {n: np.zeros_like(f["q1"]) for n in ("dq1", "dq2", "dk1", "dk2")}
     out["dv"] = np.zeros_like(f["v"])
     dlam = 0.0
+    dlam_ss = 0.0
     for b in range(B):
         for h in heads:
-            Y, O2, rstd = bf16(fwd["y"][b, :, h]), bf16(fwd["o2"][b, :, h]), fwd["rstd"][b, h]
-            G = f["dy"][b, :, h]
-            w = np.ones(Y.shape[1]) if rms_weight is None else rms_weight
-            yh = Y / (c * w)
-            gw = G * w
-            gy = (gw * yh).sum(1, keepdims=True)
-            dO = bf16(c * rstd[:, None] * (gw - yh * gy / Y.shape[1]))
-            D2 = (dO * O2).sum(1)
+            dO, O2, yh, rstd, D2 = _upstream(f, fwd, li, b, h, rms_weight, rnd)
             D1 = (dO * (yh / rstd[:, None] + lam * O2)).sum(1)
             dlam -= float(D2.sum())
+            if exact_fwd is not None:
+                D2x = _upstream(f, exact_fwd, li, b, h, rms_weight, lambda a: a)[4]
+                dlam_ss += float(((D2 - D2x) ** 2).sum())
             dP = dO @ f["v"][b, :, h].T
             for t, (sig, D, lse) in enumerate(((1.0, D1, fwd["lse1"]), (-lam, D2, fwd["lse2"])), 1):
                 Q, K = f[f"q{t}"][b, :, h], f[f"k{t}"][b, :, h]
                 P = np.exp(s * Q @ K.T - lse[b, h][:, None])
                 if causal:
                     P = np.tril(P)
-                dS = bf16(sig * s * P * (dP - D[:, None]))
+                dS = rnd(sig * s * P * (dP - D[:, None]))
                 out[f"dq{t}"][b, :, h] = dS @ K
                 out[f"dk{t}"][b, :, h] = dS.T @ Q
                 # the dV operand is P itself; sigma multiplies the stream's
                 # fp32 accumulator when the streams are summed
-                out["dv"][b, :, h] += sig * (bf16(P).T @ dO)
+                out["dv"][b, :, h] += sig * (rnd(P).T @ dO)
+    for n in ("dq1", "dq2", "dk1", "dk2", "dv"):
+        out[n] = rnd(out[n])
     out["dlam"] = dlam
+    if exact_fwd is not None:
+        out["dlam_ss"] = dlam_ss
     return out
 
 

@@ -33,10 +33,11 @@ def _one_head(task):
     ref = orc.v1_backward(*(f[n] for n in NAMES), li, f["dy"], causal=causal)
     fwd = orc.v1_forward(*(f[n] for n in NAMES), li, causal=causal)
     if step:
-        fwd = rounded_forward(f, fwd, li, causal=causal)
-    model = rounded_backward(f, fwd, li, causal=causal)
+        model = rounded_backward(f, rounded_forward(f, fwd, li, causal=causal), li, causal=causal, exact_fwd=fwd)
+    else:
+        model = rounded_backward(f, fwd, li, causal=causal)
     keep = HEAD_GRADS + LAM_GRADS + ("dlam",)
-    return {n: ref[n] for n in keep}, {n: model[n] for n in HEAD_GRADS + ("dlam",)}
+    return {n: ref[n] for n in keep}, {n: model[n] for n in HEAD_GRADS + ("dlam", "dlam_ss") if n in model}
 
 
 def v1_backward_by_head(f, li, causal=True, workers=None, step=False):
@@ -72,4 +73,6 @@ def v1_backward_by_head(f, li, causal=True, workers=None, step=False):
             ref[n] += r[n]
         ref["dlam"] += r["dlam"]
         model["dlam"] += m["dlam"]
+        if "dlam_ss" in m:  # heads' rows add their squared errors
+            model["dlam_ss"] = model.get("dlam_ss", 0.0) + m["dlam_ss"]
     return ref, model

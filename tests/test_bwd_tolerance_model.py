@@ -121,3 +121,23 @@ def test_v1_forward_rounding_model_and_the_step_bar():
     assert grow > 2.0, grow
     for n in ("dq1", "dq2", "dk1", "dk2", "dv"):
         assert np.linalg.norm(step[n] - ref[n]) / np.linalg.norm(ref[n]) < 0.5 * 2e-2, n
+
+
+def test_v1_rounding_model_is_the_chain_rule():
+    """The V1 backward model with its rounding switched off reproduces the
+    oracle's gradients and dlambda (causal or not, with an RMSNorm weight), so
+    it rounds the right quantities of the right formula; the per-row dlambda
+    error it reports is then zero."""
+    names = ("q1", "q2", "k1", "k2", "v", "lq1", "lk1", "lq2", "lk2")
+    t = synth.v1_inputs(2, 70, 2, 64, 128, "bf16", seed=5240, device="cpu", with_dy=True)
+    f = {k: v.to(torch.float64).numpy() for k, v in t.items()}
+    li = float(np.float32(orc.lambda_init(5)))
+    w = 0.5 + np.arange(128) / 256.0
+    for causal in (True, False):
+        ref = orc.v1_backward(*(f[n] for n in names), li, f["dy"], causal=causal, rms_weight=w)
+        fwd = orc.v1_forward(*(f[n] for n in names), li, causal=causal, rms_weight=w)
+        exact = rounded_backward(f, fwd, li, causal=causal, rms_weight=w, rnd=lambda a: a, exact_fwd=fwd)
+        for n in ("dq1", "dq2", "dk1", "dk2", "dv"):
+            np.testing.assert_allclose(exact[n], ref[n], rtol=0, atol=1e-12 * np.abs(ref[n]).max())
+        assert abs(exact["dlam"] - ref["dlam"]) <= 1e-12 * abs(ref["dlam"])
+        assert exact["dlam_ss"] == 0.0
