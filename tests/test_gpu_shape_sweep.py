@@ -15,7 +15,7 @@ import pytest
 import torch
 
 SEED = 7309
-CASES = 6
+CASES = 12
 
 # length categories, cycled over a sweep's cases: under one 128-row tile,
 # whole tiles, ragged over several tiles
