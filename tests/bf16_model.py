@@ -19,7 +19,7 @@ def bf16(x):
     return torch.from_numpy(np.asarray(x, np.float32)).to(torch.bfloat16).to(torch.float64).numpy()
 
 
-def rounded_forward(f, fwd, li, causal=True, rms_weight=None, eps=1e-5, rnd=bf16):
+def rounded_forward(f, fwd, li, causal=True, rms_weight=None, eps=1e-5, rnd=bf16, scale=None):
     """The V1 forward with its own bf16 storage points, for the bars of the
     training step (the library's forward, then its backward on the forward's
     saves).  fp64 everywhere EXCEPT: P = exp(S - m) (m the row max) is rounded
@@ -29,13 +29,13 @@ def rounded_forward(f, fwd, li, causal=True, rms_weight=None, eps=1e-5, rnd=bf16
     f: fp64 inputs as in ``rounded_backward``; fwd: the oracle forward on
     them (lambda and the LSEs are taken from it).  Returns fwd with y, o2 and
     rstd replaced; with rnd the identity it reproduces the oracle forward's.
-    Under strong cancellation between the streams (lambda near 1, long rows)
+    scale: the softmax scale (None = 1/sqrt(d_qk)).  Under strong cancellation between the streams (lambda near 1, long rows)
     the rounded P dominates the step's gradient error, which the backward
     model fed exact forward outputs does not contain."""
     lam, c = fwd["lam"], 1.0 - li
     B, N, H, dqk = f["q1"].shape
     dv = f["v"].shape[3]
-    s = 1.0 / np.sqrt(dqk)
+    s = 1.0 / np.sqrt(dqk) if scale is None else scale
     w = np.ones(dv) if rms_weight is None else rms_weight
     y = np.zeros((B, N, H, dv))
     o2 = np.zeros((B, N, H, dv))
@@ -73,7 +73,8 @@ def _upstream(f, fw, li, b, h, rms_weight, rnd):
     return dO, O2, yh, rstd, (dO * O2).sum(1)
 
 
-def rounded_backward(f, fwd, li, heads=None, causal=True, rms_weight=None, rnd=bf16, exact_fwd=None):
+def rounded_backward(f, fwd, li, heads=None, causal=True, rms_weight=None, rnd=bf16, exact_fwd=None,
+                     scale=None):
     """f: fp64 inputs (q1..v, dy) as [B, N, H, D]; fwd: the forward on them
     (the oracle's, or ``rounded_forward``'s for the training step).  Returns
     the gradients dq1, dq2, dk1, dk2, dv and dlam computed with the bf16
@@ -81,14 +82,15 @@ def rounded_backward(f, fwd, li, heads=None, causal=True, rms_weight=None, rnd=b
     saved Y and O2, dO, the MMA operands dS and P, and the gradient outputs
     themselves (bf16 by the interface).  `heads` restricts to a list of heads;
     causal=False drops the key <= query mask; rms_weight is the forward's
-    RMSNorm weight (None = unit).  With exact_fwd (the oracle forward) it also
+    RMSNorm weight (None = unit); scale the softmax scale (None =
+    1/sqrt(d_qk)).  With exact_fwd (the oracle forward) it also
     returns dlam_ss, the sum over rows of the squared differences between this
     model's per-row terms of dlam = -sum_rows <dO, O2> and the exact ones: the
     scale of dlam's error when the rows' errors have independent signs."""
     lam = fwd["lam"]
     B, N, H, dqk = f["q1"].shape
     heads = range(H) if heads is None else heads
-    s = 1.0 / np.sqrt(dqk)
+    s = 1.0 / np.sqrt(dqk) if scale is None else scale
     out = {n: np.zeros_like(f["q1"]) for n in ("dq1", "dq2", "dk1", "dk2")}
     out["dv"] = np.zeros_like(f["v"])
     dlam = 0.0

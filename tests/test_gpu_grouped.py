@@ -28,7 +28,7 @@ def _status_clean():
     assert bd.diffattn_get_device_status() == bd.DA_OK
 
 
-def _check(t, ratio, out, rows=None, batches=None, groups=None, causal=True):
+def _check(t, ratio, out, rows=None, batches=None, groups=None, causal=True, scale=None):
     B, N, Hq, d = t["q"].shape
     hkv = t["k"].shape[2]
     G = Hq // hkv
@@ -44,7 +44,7 @@ def _check(t, ratio, out, rows=None, batches=None, groups=None, causal=True):
             ps = slice(g * ratio, (g + 1) * ratio)
             ref = orc.grouped_forward(f64(t["q"][b:b + 1, :, qs]), f64(t["k"][b:b + 1, :, c:c + 1]),
                                       f64(t["v"][b:b + 1, :, c:c + 1]), gate[b:b + 1, :, ps], ratio, rows=rows,
-                                      causal=causal)
+                                      causal=causal, scale=scale)
             tol = TOL * float(np.sqrt(np.mean(f64(t["v"][b, :, c]) ** 2)))
             worst = max(worst, float(np.max(np.abs(o[b, ref["rows"], ps] - ref["out"][0]))) / tol)
     record({"out": worst})

@@ -51,39 +51,40 @@ def _inputs(B, N, h, ratio, hkv, d, dm, seed):
     return t
 
 
-def _forward_saves(t, ratio, causal=True):
+def _forward_saves(t, ratio, causal=True, scale=None):
     B, N, Hq, d = t["q"].shape
     heads = torch.empty((B, N, Hq, d), dtype=torch.bfloat16, device="cuda")
     lse = torch.empty((B, Hq, N), dtype=torch.float32, device="cuda")
     bd.diffattn_grouped_fwd(t["q"], t["k"], t["v"], ratio, x=t["x"], w_lambda=t["w_lambda"], o_heads=heads,
-                            lse=lse, causal=causal)
+                            lse=lse, causal=causal, softmax_scale=0.0 if scale is None else scale)
     return dict(o_heads=heads, lse=lse)
 
 
-def _run(t, ratio, causal=True):
+def _run(t, ratio, causal=True, scale=None):
     """The training step: GPU grouped forward with saves, then the backward."""
-    sv = _forward_saves(t, ratio, causal)
+    sv = _forward_saves(t, ratio, causal, scale)
     g = bd.diffattn_grouped_bwd(t["q"], t["k"], t["v"], t["dout"], sv, ratio, x=t["x"], w_lambda=t["w_lambda"],
-                                want_dz=True, causal=causal)
+                                want_dz=True, causal=causal, softmax_scale=0.0 if scale is None else scale)
     torch.cuda.synchronize()
     return g
 
 
-def _run_exact_saves(t, ratio, ref, causal=True):
+def _run_exact_saves(t, ratio, ref, causal=True, scale=None):
     """The GPU backward alone, given the oracle's forward saves."""
     sv = dict(o_heads=torch.from_numpy(ref["o"]).to("cuda", torch.bfloat16),
               lse=torch.from_numpy(ref["lse"]).to("cuda", torch.float32))
     g = bd.diffattn_grouped_bwd(t["q"], t["k"], t["v"], t["dout"], sv, ratio, x=t["x"], w_lambda=t["w_lambda"],
-                                want_dz=True, causal=causal)
+                                want_dz=True, causal=causal, softmax_scale=0.0 if scale is None else scale)
     torch.cuda.synchronize()
     return g
 
 
-def _reference(t, ratio, causal=True):
+def _reference(t, ratio, causal=True, scale=None):
     f = {n: f64(v) for n, v in t.items()}
-    ref = orc.grouped_backward(f["q"], f["k"], f["v"], f["x"], f["w_lambda"], f["dout"], ratio, causal=causal)
+    ref = orc.grouped_backward(f["q"], f["k"], f["v"], f["x"], f["w_lambda"], f["dout"], ratio, causal=causal,
+                               scale=scale)
     fwd = dict(o=ref["o"], lse=ref["lse"])  # the forward the oracle's chain rule ran on
-    model = rounded_backward_grouped(f, fwd, ref["gate"], ratio, causal=causal)
+    model = rounded_backward_grouped(f, fwd, ref["gate"], ratio, causal=causal, scale=scale)
     return ref, model
 
 

@@ -3,7 +3,7 @@ oracle, with the bars of the fixed-shape parity tests (their checks are
 reused as they are): batch, length (one token, under a tile, whole tiles,
 ragged tails over several tiles), head counts and group sizes, head dims,
 causal or not, the layer index, an RMSNorm weight, decode lengths and split
-counts are drawn together, so that combinations the hand-picked cases leave
+counts and the softmax scale are drawn together, so that combinations the hand-picked cases leave
 out are run as well.  The draws are fixed by the seed; the CPU test checks
 that every drawn shape is one the entry points accept and that the sweep
 spans the categories it claims."""
@@ -33,6 +33,9 @@ def sweep_cases(op, n=CASES, seed=SEED):
     cases = []
     for i in range(n):
         causal = i % 2 == 0 or rng.random() < 0.5
+        # every third case a softmax scale other than the default 1/sqrt(d),
+        # exactly representable in fp32 as the interface takes it
+        scale = float(np.float32(rng.uniform(0.03, 0.2))) if i % 3 == 2 else None
         if op in ("v1_fwd", "v1_bwd"):
             dqk, dv = rng.choice([(128, 256), (64, 128)])
             cap = 700 if op == "v1_fwd" else 400
@@ -71,6 +74,7 @@ def sweep_cases(op, n=CASES, seed=SEED):
                               weighted=rng.random() < 0.3))
         else:
             raise ValueError(op)
+        cases[-1]["scale"] = scale
     return cases
 
 
@@ -104,6 +108,8 @@ def test_sweep_shapes_are_valid():
                 assert c["h"] % c["hkv"] == 0
             if op.startswith("v1") and op != "v1_decode":
                 assert (c["dqk"], c["dv"]) in ((128, 256), (64, 128))
+            assert c["scale"] is None or (0 < c["scale"] < 1 and float(np.float32(c["scale"])) == c["scale"])
+        assert any(c["scale"] is not None for c in cases) and any(c["scale"] is None for c in cases)
         if not op.endswith("decode"):
             ns = [c["N"] for c in cases]
             assert any(n < 128 for n in ns) and any(n % 128 == 0 for n in ns)
@@ -135,6 +141,10 @@ def _f64(t):
     return t.detach().to("cpu", torch.float64).numpy()
 
 
+def _ss(c):
+    return 0.0 if c["scale"] is None else c["scale"]
+
+
 def _rms_weight(n, seed):
     return 0.5 + torch.rand(n, generator=torch.Generator().manual_seed(seed), dtype=torch.float32).cuda()
 
@@ -147,9 +157,10 @@ def test_sweep_v1_fwd(c, gpu_ops):
     t = synth.v1_inputs(c["B"], c["N"], c["H"], c["dqk"], c["dv"], "bf16", seed=11000 + c["N"], device="cuda")
     li = bd.diffattn_lambda_init(c["layer"])
     w = _rms_weight(c["dv"], 11001) if c["weighted"] else None
-    y, sv = bd.diffattn_v1_fwd(*(t[n] for n in tv1.NAMES), li, save=True, causal=c["causal"], rms_weight=w)
+    y, sv = bd.diffattn_v1_fwd(*(t[n] for n in tv1.NAMES), li, save=True, causal=c["causal"], rms_weight=w,
+                               softmax_scale=_ss(c))
     torch.cuda.synchronize()
-    tv1._check(t, li, y, sv, causal=c["causal"], w=w)
+    tv1._check(t, li, y, sv, causal=c["causal"], w=w, scale=c["scale"])
 
 
 @pytest.mark.gpu
@@ -163,11 +174,13 @@ def test_sweep_v1_bwd(c, gpu_ops):
     li = float(np.float32(bd.diffattn_lambda_init(c["layer"])))
     w = _rms_weight(c["dv"], 12001) if c["weighted"] else None
     wf = None if w is None else _f64(w)
-    ref = orc.v1_backward(*(_f64(t[n]) for n in tv1b.NAMES), li, _f64(t["dy"]), causal=c["causal"], rms_weight=wf)
-    tv1b._compare(tv1b._run_exact_saves(t, li, causal=c["causal"], w=w), ref,
-                  tv1b._model(t, li, causal=c["causal"], w=w), bar="bwd")
-    tv1b._compare(tv1b._run(t, li, causal=c["causal"], w=w), ref,
-                  tv1b._model(t, li, causal=c["causal"], w=w, step=True), bar="step")
+    sc = c["scale"]
+    ref = orc.v1_backward(*(_f64(t[n]) for n in tv1b.NAMES), li, _f64(t["dy"]), causal=c["causal"], rms_weight=wf,
+                          scale=sc)
+    tv1b._compare(tv1b._run_exact_saves(t, li, causal=c["causal"], w=w, scale=sc), ref,
+                  tv1b._model(t, li, causal=c["causal"], w=w, scale=sc), bar="bwd")
+    tv1b._compare(tv1b._run(t, li, causal=c["causal"], w=w, scale=sc), ref,
+                  tv1b._model(t, li, causal=c["causal"], w=w, step=True, scale=sc), bar="step")
 
 
 @pytest.mark.gpu
@@ -178,10 +191,11 @@ def test_sweep_v2_fwd(c, gpu_ops):
     bd, tv2 = gpu_ops["bd"], gpu_ops["tv2"]
     t = synth.v2_inputs(c["B"], c["N"], c["h"], c["hkv"], c["d"], c["dm"], seed=13000 + c["N"], device="cuda")
     lse = torch.empty((c["B"], 2 * c["h"], c["N"]), dtype=torch.float32, device="cuda")
-    out = bd.diffattn_v2_fwd(t["q"], t["k"], t["v"], x=t["x"], w_lambda=t["w_lambda"], lse=lse, causal=c["causal"])
+    out = bd.diffattn_v2_fwd(t["q"], t["k"], t["v"], x=t["x"], w_lambda=t["w_lambda"], lse=lse, causal=c["causal"],
+                             softmax_scale=_ss(c))
     torch.cuda.synchronize()
     gate = orc.v2_gate(_f64(t["x"]), _f64(t["w_lambda"]))
-    tv2._check_pairs(t, out, gate, lse=lse, causal=c["causal"])
+    tv2._check_pairs(t, out, gate, lse=lse, causal=c["causal"], scale=c["scale"])
 
 
 @pytest.mark.gpu
@@ -191,9 +205,10 @@ def test_sweep_v2_bwd(c, gpu_ops):
     tv2b = gpu_ops["tv2b"]
     t = synth.v2_inputs(c["B"], c["N"], c["h"], c["hkv"], c["d"], c["dm"], seed=14000 + c["N"], device="cuda",
                         with_dout=True)
-    ref, fwd, model = tv2b._reference(t, causal=c["causal"])
-    tv2b._compare(tv2b._run_exact_saves(t, fwd, causal=c["causal"]), ref, model, bar="bwd")
-    tv2b._compare(tv2b._run(t, causal=c["causal"]), ref, model, bar="step")
+    sc = c["scale"]
+    ref, fwd, model = tv2b._reference(t, causal=c["causal"], scale=sc)
+    tv2b._compare(tv2b._run_exact_saves(t, fwd, causal=c["causal"], scale=sc), ref, model, bar="bwd")
+    tv2b._compare(tv2b._run(t, causal=c["causal"], scale=sc), ref, model, bar="step")
 
 
 @pytest.mark.gpu
@@ -204,9 +219,9 @@ def test_sweep_grouped_fwd(c, gpu_ops):
     t = synth.grouped_inputs(c["B"], c["N"], c["h"], c["ratio"], c["hkv"], c["d"], c["dm"], seed=15000 + c["N"],
                              device="cuda")
     out = bd.diffattn_grouped_fwd(t["q"], t["k"], t["v"], c["ratio"], x=t["x"], w_lambda=t["w_lambda"],
-                                  causal=c["causal"])
+                                  causal=c["causal"], softmax_scale=_ss(c))
     torch.cuda.synchronize()
-    tg._check(t, c["ratio"], out, causal=c["causal"])
+    tg._check(t, c["ratio"], out, causal=c["causal"], scale=c["scale"])
 
 
 @pytest.mark.gpu
@@ -214,9 +229,10 @@ def test_sweep_grouped_fwd(c, gpu_ops):
 def test_sweep_grouped_bwd(c, gpu_ops):
     tgb = gpu_ops["tgb"]
     t = tgb._inputs(c["B"], c["N"], c["h"], c["ratio"], c["hkv"], c["d"], c["dm"], seed=16000 + c["N"])
-    ref, model = tgb._reference(t, c["ratio"], causal=c["causal"])
-    tgb._compare(tgb._run_exact_saves(t, c["ratio"], ref, causal=c["causal"]), ref, model, bar="bwd")
-    tgb._compare(tgb._run(t, c["ratio"], causal=c["causal"]), ref, model, bar="step")
+    sc = c["scale"]
+    ref, model = tgb._reference(t, c["ratio"], causal=c["causal"], scale=sc)
+    tgb._compare(tgb._run_exact_saves(t, c["ratio"], ref, causal=c["causal"], scale=sc), ref, model, bar="bwd")
+    tgb._compare(tgb._run(t, c["ratio"], causal=c["causal"], scale=sc), ref, model, bar="step")
 
 
 @pytest.mark.gpu
@@ -227,9 +243,9 @@ def test_sweep_v2_decode(c, gpu_ops):
     t = synth.decode_inputs(c["B"], c["L"], c["h"], c["hkv"], c["d"], c["dm"], seed=17000 + c["L"], device="cuda",
                             seqlens=c["seqlens"])
     out = bd.diffattn_v2_decode(t["q"], t["k_cache"], t["v_cache"], seqlens=t["seqlens"], x=t["x"],
-                                w_lambda=t["w_lambda"], num_splits=c["splits"])
+                                w_lambda=t["w_lambda"], num_splits=c["splits"], softmax_scale=_ss(c))
     torch.cuda.synchronize()
-    tsm._decode_check(t, out)
+    tsm._decode_check(t, out, scale=c["scale"])
 
 
 @pytest.mark.gpu
@@ -241,4 +257,5 @@ def test_sweep_v1_decode(c, gpu_ops):
                                seqlens=c["seqlens"])
     li = bd.diffattn_lambda_init(c["layer"])
     w = _rms_weight(c["dv"], 18001) if c["weighted"] else None
-    tv1d._check(t, li, tv1d._run(t, li, num_splits=c["splits"], rms_weight=w), w=w)
+    tv1d._check(t, li, tv1d._run(t, li, num_splits=c["splits"], rms_weight=w, softmax_scale=_ss(c)), w=w,
+                scale=c["scale"])

@@ -131,7 +131,7 @@ def test_v1_fwd_f32_exact_cancellation():
 
 # ---------------------------------------------------------------- decode ----
 
-def _decode_check(t, out, gate=None, batches=None):
+def _decode_check(t, out, gate=None, batches=None, scale=None):
     q, kc, vc = f64(t["q"]), t["k_cache"], t["v_cache"]
     sl = t["seqlens"].cpu().numpy()
     if gate is None:
@@ -142,7 +142,7 @@ def _decode_check(t, out, gate=None, batches=None):
     for b in batches:
         L = int(sl[b])
         ref = orc.v2_decode(q[b:b + 1], f64(kc[b:b + 1, :L]), f64(vc[b:b + 1, :L]), [L],
-                            gate[b:b + 1])
+                            gate[b:b + 1], scale=scale)
         tol = BF16_TOL * rms(f64(vc[b, :L]))
         d = maxdiff(o[b], ref["out"][0])
         worst = max(worst, d / tol)

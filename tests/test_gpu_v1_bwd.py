@@ -67,25 +67,30 @@ def _status_clean():
     assert bd.diffattn_get_device_status() == bd.DA_OK
 
 
-def _run(t, li, causal=True, w=None):
-    """The training step: GPU forward with saves, then the GPU backward."""
-    y, sv = bd.diffattn_v1_fwd(*(t[n] for n in NAMES), li, save=True, causal=causal, rms_weight=w)
-    g = bd.diffattn_v1_bwd(*(t[n] for n in NAMES), li, y, t["dy"], sv, causal=causal, rms_weight=w)
+def _run(t, li, causal=True, w=None, scale=None):
+    """The training step: GPU forward with saves, then the GPU backward
+    (scale: the softmax scale, None = the default 1/sqrt(d_qk))."""
+    ss = 0.0 if scale is None else scale
+    y, sv = bd.diffattn_v1_fwd(*(t[n] for n in NAMES), li, save=True, causal=causal, rms_weight=w,
+                               softmax_scale=ss)
+    g = bd.diffattn_v1_bwd(*(t[n] for n in NAMES), li, y, t["dy"], sv, causal=causal, rms_weight=w,
+                           softmax_scale=ss)
     torch.cuda.synchronize()
     return g
 
 
-def _run_exact_saves(t, li, causal=True, w=None):
+def _run_exact_saves(t, li, causal=True, w=None, scale=None):
     """The GPU backward alone, given the oracle's forward outputs."""
     fwd = orc.v1_forward(*(f64(t[n]) for n in NAMES), li, causal=causal,
-                         rms_weight=None if w is None else f64(w))
+                         rms_weight=None if w is None else f64(w), scale=scale)
     dev = t["q1"].device
     y = torch.from_numpy(fwd["y"]).to(dev, torch.bfloat16)
     sv = dict(o2=torch.from_numpy(fwd["o2"]).to(dev, torch.bfloat16),
               lse1=torch.from_numpy(fwd["lse1"]).to(dev, torch.float32),
               lse2=torch.from_numpy(fwd["lse2"]).to(dev, torch.float32),
               rstd=torch.from_numpy(fwd["rstd"]).to(dev, torch.float32))
-    g = bd.diffattn_v1_bwd(*(t[n] for n in NAMES), li, y, t["dy"], sv, causal=causal, rms_weight=w)
+    g = bd.diffattn_v1_bwd(*(t[n] for n in NAMES), li, y, t["dy"], sv, causal=causal, rms_weight=w,
+                           softmax_scale=0.0 if scale is None else scale)
     torch.cuda.synchronize()
     return g
 
@@ -126,19 +131,20 @@ def _compare(g, ref, model, heads=None, lam_vectors=True, bar="bwd"):
     assert max(worst.values()) <= 1.0, worst
 
 
-def _model(t, li, heads=None, causal=True, w=None, step=False):
+def _model(t, li, heads=None, causal=True, w=None, step=False, scale=None):
     """The rounding model on these inputs: the backward's storage points fed
     the exact forward outputs, or with step=True the forward's own storage
     points as well (the training step's backward runs on its forward's
     bf16 saves)."""
     f = {n: f64(t[n]) for n in NAMES + ("dy",)}
     wf = None if w is None else f64(w)
-    fwd = orc.v1_forward(*(f[n] for n in NAMES), li, causal=causal, rms_weight=wf)
+    fwd = orc.v1_forward(*(f[n] for n in NAMES), li, causal=causal, rms_weight=wf, scale=scale)
     if step:
         exact = fwd
-        fwd = rounded_forward(f, exact, li, causal=causal, rms_weight=wf)
-        return rounded_backward(f, fwd, li, heads=heads, causal=causal, rms_weight=wf, exact_fwd=exact)
-    return rounded_backward(f, fwd, li, heads=heads, causal=causal, rms_weight=wf)
+        fwd = rounded_forward(f, exact, li, causal=causal, rms_weight=wf, scale=scale)
+        return rounded_backward(f, fwd, li, heads=heads, causal=causal, rms_weight=wf, exact_fwd=exact,
+                                scale=scale)
+    return rounded_backward(f, fwd, li, heads=heads, causal=causal, rms_weight=wf, scale=scale)
 
 
 @pytest.mark.parametrize("B,N,H,layer", [(1, 200, 2, 1), (2, 384, 1, 3), (1, 129, 2, 14),

@@ -32,7 +32,7 @@ def _status_clean():
     assert bd.diffattn_get_device_status() == bd.DA_OK
 
 
-def _check_pairs(t, out, gate, pairs=None, rows=None, lse=None, causal=True):
+def _check_pairs(t, out, gate, pairs=None, rows=None, lse=None, causal=True, scale=None):
     B, N, H2, d = t["q"].shape
     hkv = t["k"].shape[2]
     G = H2 // hkv
@@ -44,7 +44,7 @@ def _check_pairs(t, out, gate, pairs=None, rows=None, lse=None, causal=True):
             g = (2 * p) // G
             ref = orc.v2_forward(f64(t["q"][b:b + 1, :, 2 * p:2 * p + 2]), f64(t["k"][b:b + 1, :, g:g + 1]),
                                  f64(t["v"][b:b + 1, :, g:g + 1]), gate[b:b + 1, :, p:p + 1], rows=rows,
-                                 causal=causal)
+                                 causal=causal, scale=scale)
             got = o[b, ref["rows"], p]
             tol = TOL * rms(f64(t["v"][b, :, g]))
             worst = max(worst, float(np.max(np.abs(got - ref["out"][0, :, 0]))) / tol)

@@ -44,32 +44,34 @@ def _status_clean():
     assert bd.diffattn_get_device_status() == bd.DA_OK
 
 
-def _run(t, causal=True):
-    """The training step: GPU forward with saves, then the GPU backward."""
+def _run(t, causal=True, scale=None):
+    """The training step: GPU forward with saves, then the GPU backward
+    (scale: the softmax scale, None = the default 1/sqrt(d))."""
+    ss = 0.0 if scale is None else scale
     _, sv = bd.diffattn_v2_fwd(t["q"], t["k"], t["v"], x=t["x"], w_lambda=t["w_lambda"], save=True,
-                               causal=causal)
+                               causal=causal, softmax_scale=ss)
     g = bd.diffattn_v2_bwd(t["q"], t["k"], t["v"], t["dout"], sv, x=t["x"], w_lambda=t["w_lambda"],
-                           want_dz=True, causal=causal)
+                           want_dz=True, causal=causal, softmax_scale=ss)
     torch.cuda.synchronize()
     return g
 
 
-def _run_exact_saves(t, fwd, causal=True):
+def _run_exact_saves(t, fwd, causal=True, scale=None):
     """The GPU backward alone, given the oracle's forward saves."""
     dev = t["q"].device
     sv = dict(o_heads=torch.from_numpy(fwd["o"]).to(dev, torch.bfloat16),
               lse=torch.from_numpy(fwd["lse"]).to(dev, torch.float32))
     g = bd.diffattn_v2_bwd(t["q"], t["k"], t["v"], t["dout"], sv, x=t["x"], w_lambda=t["w_lambda"],
-                           want_dz=True, causal=causal)
+                           want_dz=True, causal=causal, softmax_scale=0.0 if scale is None else scale)
     torch.cuda.synchronize()
     return g
 
 
-def _reference(t, causal=True):
+def _reference(t, causal=True, scale=None):
     f = {n: f64(v) for n, v in t.items()}
-    ref = orc.v2_backward(f["q"], f["k"], f["v"], f["x"], f["w_lambda"], f["dout"], causal=causal)
+    ref = orc.v2_backward(f["q"], f["k"], f["v"], f["x"], f["w_lambda"], f["dout"], causal=causal, scale=scale)
     fwd = dict(o=ref["o"], lse=ref["lse"])  # the forward the oracle's chain rule ran on
-    model = rounded_backward_v2(f, fwd, ref["gate"], causal=causal)
+    model = rounded_backward_v2(f, fwd, ref["gate"], causal=causal, scale=scale)
     return ref, fwd, model
 
 
