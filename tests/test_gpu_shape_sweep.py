@@ -3,7 +3,7 @@ oracle, with the bars of the fixed-shape parity tests (their checks are
 reused as they are): batch, length (one token, under a tile, whole tiles,
 ragged tails over several tiles), head counts and group sizes, head dims,
 causal or not, the layer index, an RMSNorm weight, decode lengths and split
-counts and the softmax scale are drawn together, so that combinations the hand-picked cases leave
+counts, the softmax scale and the V1 RMSNorm epsilon are drawn together, so that combinations the hand-picked cases leave
 out are run as well.  The draws are fixed by the seed; the CPU test checks
 that every drawn shape is one the entry points accept and that the sweep
 spans the categories it claims."""
@@ -28,6 +28,12 @@ def _length(rng, i, cap):
     return 128 * rng.randint(1, cap // 128 - 1) + rng.randint(1, 127)
 
 
+def _eps(rng):
+    """The V1 RMSNorm epsilon: mostly the default, sometimes large enough
+    (against mean O^2 of about 0.05) to change the result visibly."""
+    return float(np.float32(rng.choice([1e-5, 1e-5, 1e-3, 3e-2])))
+
+
 def sweep_cases(op, n=CASES, seed=SEED):
     rng = random.Random(f"{op}/{seed}")
     cases = []
@@ -41,7 +47,7 @@ def sweep_cases(op, n=CASES, seed=SEED):
             cap = 700 if op == "v1_fwd" else 400
             cases.append(dict(B=rng.randint(1, 3), N=_length(rng, i, cap), H=rng.randint(1, 3 if op == "v1_bwd" else 4),
                               dqk=dqk, dv=dv, causal=causal, layer=rng.randint(1, 28),
-                              weighted=rng.random() < 0.3))
+                              weighted=rng.random() < 0.3, eps=_eps(rng)))
         elif op in ("v2_fwd", "v2_bwd"):
             hkv = rng.choice([1, 2, 4])
             per = rng.choice([1, 2] if op == "v2_bwd" else [1, 2, 4])  # head pairs per K/V head
@@ -71,7 +77,7 @@ def sweep_cases(op, n=CASES, seed=SEED):
             dqk, dv = rng.choice([(128, 256), (64, 128)])
             cases.append(dict(B=B, L=L, H=rng.randint(1, 4), dqk=dqk, dv=dv, seqlens=seqlens,
                               splits=rng.choice([0, 1, 2, 3, 5]), layer=rng.randint(1, 28),
-                              weighted=rng.random() < 0.3))
+                              weighted=rng.random() < 0.3, eps=_eps(rng)))
         else:
             raise ValueError(op)
         cases[-1]["scale"] = scale
@@ -110,6 +116,8 @@ def test_sweep_shapes_are_valid():
                 assert (c["dqk"], c["dv"]) in ((128, 256), (64, 128))
             assert c["scale"] is None or (0 < c["scale"] < 1 and float(np.float32(c["scale"])) == c["scale"])
         assert any(c["scale"] is not None for c in cases) and any(c["scale"] is None for c in cases)
+        if op.startswith("v1"):
+            assert any(c["eps"] > 1e-4 for c in cases) and all(c["eps"] > 0 for c in cases)
         if not op.endswith("decode"):
             ns = [c["N"] for c in cases]
             assert any(n < 128 for n in ns) and any(n % 128 == 0 for n in ns)
@@ -158,9 +166,9 @@ def test_sweep_v1_fwd(c, gpu_ops):
     li = bd.diffattn_lambda_init(c["layer"])
     w = _rms_weight(c["dv"], 11001) if c["weighted"] else None
     y, sv = bd.diffattn_v1_fwd(*(t[n] for n in tv1.NAMES), li, save=True, causal=c["causal"], rms_weight=w,
-                               softmax_scale=_ss(c))
+                               softmax_scale=_ss(c), rms_eps=c["eps"])
     torch.cuda.synchronize()
-    tv1._check(t, li, y, sv, causal=c["causal"], w=w, scale=c["scale"])
+    tv1._check(t, li, y, sv, causal=c["causal"], w=w, scale=c["scale"], eps=c["eps"])
 
 
 @pytest.mark.gpu
@@ -174,13 +182,13 @@ def test_sweep_v1_bwd(c, gpu_ops):
     li = float(np.float32(bd.diffattn_lambda_init(c["layer"])))
     w = _rms_weight(c["dv"], 12001) if c["weighted"] else None
     wf = None if w is None else _f64(w)
-    sc = c["scale"]
+    sc, eps = c["scale"], c["eps"]
     ref = orc.v1_backward(*(_f64(t[n]) for n in tv1b.NAMES), li, _f64(t["dy"]), causal=c["causal"], rms_weight=wf,
-                          scale=sc)
-    tv1b._compare(tv1b._run_exact_saves(t, li, causal=c["causal"], w=w, scale=sc), ref,
-                  tv1b._model(t, li, causal=c["causal"], w=w, scale=sc), bar="bwd")
-    tv1b._compare(tv1b._run(t, li, causal=c["causal"], w=w, scale=sc), ref,
-                  tv1b._model(t, li, causal=c["causal"], w=w, step=True, scale=sc), bar="step")
+                          scale=sc, eps=eps)
+    tv1b._compare(tv1b._run_exact_saves(t, li, causal=c["causal"], w=w, scale=sc, eps=eps), ref,
+                  tv1b._model(t, li, causal=c["causal"], w=w, scale=sc, eps=eps), bar="bwd")
+    tv1b._compare(tv1b._run(t, li, causal=c["causal"], w=w, scale=sc, eps=eps), ref,
+                  tv1b._model(t, li, causal=c["causal"], w=w, step=True, scale=sc, eps=eps), bar="step")
 
 
 @pytest.mark.gpu
@@ -257,5 +265,5 @@ def test_sweep_v1_decode(c, gpu_ops):
                                seqlens=c["seqlens"])
     li = bd.diffattn_lambda_init(c["layer"])
     w = _rms_weight(c["dv"], 18001) if c["weighted"] else None
-    tv1d._check(t, li, tv1d._run(t, li, num_splits=c["splits"], rms_weight=w, softmax_scale=_ss(c)), w=w,
-                scale=c["scale"])
+    tv1d._check(t, li, tv1d._run(t, li, num_splits=c["splits"], rms_weight=w, softmax_scale=_ss(c),
+                                 rms_eps=c["eps"]), w=w, scale=c["scale"], eps=c["eps"])

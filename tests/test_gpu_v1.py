@@ -36,7 +36,7 @@ def _status_clean():
     assert bd.diffattn_get_device_status() == bd.DA_OK
 
 
-def _check(t, li, y, sv, rows=None, heads=None, batches=None, causal=True, w=None, scale=None):
+def _check(t, li, y, sv, rows=None, heads=None, batches=None, causal=True, w=None, scale=None, eps=1e-5):
     B, N, H, _ = t["q1"].shape
     heads = range(H) if heads is None else heads
     batches = range(B) if batches is None else batches
@@ -47,7 +47,8 @@ def _check(t, li, y, sv, rows=None, heads=None, batches=None, causal=True, w=Non
             sl = lambda n: f64(t[n][b:b + 1, :, h:h + 1])  # noqa: E731
             ref = orc.v1_forward(sl("q1"), sl("q2"), sl("k1"), sl("k2"), sl("v"),
                                  *(f64(t[n]) for n in NAMES[5:]), float(np.float32(li)), rows=rows,
-                                 causal=causal, rms_weight=None if w is None else f64(w), scale=scale)
+                                 causal=causal, rms_weight=None if w is None else f64(w), scale=scale,
+                                 eps=eps)
             r = ref["rows"]
             tol = TOL * rms(f64(t["v"][b, :, h]))
             worst = max(worst, float(np.max(np.abs(yv[b, r, h] - ref["y"][0, :, 0]))) / tol)

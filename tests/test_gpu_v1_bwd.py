@@ -67,22 +67,23 @@ def _status_clean():
     assert bd.diffattn_get_device_status() == bd.DA_OK
 
 
-def _run(t, li, causal=True, w=None, scale=None):
+def _run(t, li, causal=True, w=None, scale=None, eps=1e-5):
     """The training step: GPU forward with saves, then the GPU backward
-    (scale: the softmax scale, None = the default 1/sqrt(d_qk))."""
+    (scale: the softmax scale, None = the default 1/sqrt(d_qk); eps: the
+    RMSNorm epsilon)."""
     ss = 0.0 if scale is None else scale
     y, sv = bd.diffattn_v1_fwd(*(t[n] for n in NAMES), li, save=True, causal=causal, rms_weight=w,
-                               softmax_scale=ss)
+                               softmax_scale=ss, rms_eps=eps)
     g = bd.diffattn_v1_bwd(*(t[n] for n in NAMES), li, y, t["dy"], sv, causal=causal, rms_weight=w,
-                           softmax_scale=ss)
+                           softmax_scale=ss, rms_eps=eps)
     torch.cuda.synchronize()
     return g
 
 
-def _run_exact_saves(t, li, causal=True, w=None, scale=None):
+def _run_exact_saves(t, li, causal=True, w=None, scale=None, eps=1e-5):
     """The GPU backward alone, given the oracle's forward outputs."""
     fwd = orc.v1_forward(*(f64(t[n]) for n in NAMES), li, causal=causal,
-                         rms_weight=None if w is None else f64(w), scale=scale)
+                         rms_weight=None if w is None else f64(w), scale=scale, eps=eps)
     dev = t["q1"].device
     y = torch.from_numpy(fwd["y"]).to(dev, torch.bfloat16)
     sv = dict(o2=torch.from_numpy(fwd["o2"]).to(dev, torch.bfloat16),
@@ -90,7 +91,7 @@ def _run_exact_saves(t, li, causal=True, w=None, scale=None):
               lse2=torch.from_numpy(fwd["lse2"]).to(dev, torch.float32),
               rstd=torch.from_numpy(fwd["rstd"]).to(dev, torch.float32))
     g = bd.diffattn_v1_bwd(*(t[n] for n in NAMES), li, y, t["dy"], sv, causal=causal, rms_weight=w,
-                           softmax_scale=0.0 if scale is None else scale)
+                           softmax_scale=0.0 if scale is None else scale, rms_eps=eps)
     torch.cuda.synchronize()
     return g
 
@@ -131,17 +132,17 @@ def _compare(g, ref, model, heads=None, lam_vectors=True, bar="bwd"):
     assert max(worst.values()) <= 1.0, worst
 
 
-def _model(t, li, heads=None, causal=True, w=None, step=False, scale=None):
+def _model(t, li, heads=None, causal=True, w=None, step=False, scale=None, eps=1e-5):
     """The rounding model on these inputs: the backward's storage points fed
     the exact forward outputs, or with step=True the forward's own storage
     points as well (the training step's backward runs on its forward's
     bf16 saves)."""
     f = {n: f64(t[n]) for n in NAMES + ("dy",)}
     wf = None if w is None else f64(w)
-    fwd = orc.v1_forward(*(f[n] for n in NAMES), li, causal=causal, rms_weight=wf, scale=scale)
+    fwd = orc.v1_forward(*(f[n] for n in NAMES), li, causal=causal, rms_weight=wf, scale=scale, eps=eps)
     if step:
         exact = fwd
-        fwd = rounded_forward(f, exact, li, causal=causal, rms_weight=wf, scale=scale)
+        fwd = rounded_forward(f, exact, li, causal=causal, rms_weight=wf, scale=scale, eps=eps)
         return rounded_backward(f, fwd, li, heads=heads, causal=causal, rms_weight=wf, exact_fwd=exact,
                                 scale=scale)
     return rounded_backward(f, fwd, li, heads=heads, causal=causal, rms_weight=wf, scale=scale)

@@ -36,7 +36,7 @@ def _run(t, li, **kw):
     return out
 
 
-def _check(t, li, out, batches=None, w=None, scale=None):
+def _check(t, li, out, batches=None, w=None, scale=None, eps=1e-5):
     B = t["q1"].shape[0]
     batches = range(B) if batches is None else batches
     sl = [int(x) for x in t["seqlens"].cpu()]
@@ -47,7 +47,7 @@ def _check(t, li, out, batches=None, w=None, scale=None):
         ref = orc.v1_decode(f64(t["q1"][b:b + 1]), f64(t["q2"][b:b + 1]), f64(t["k1_cache"][b:b + 1, :L]),
                             f64(t["k2_cache"][b:b + 1, :L]), f64(t["v_cache"][b:b + 1, :L]), [L],
                             *(f64(t[n]) for n in LAMS), float(np.float32(li)),
-                            rms_weight=None if w is None else f64(w), scale=scale)
+                            rms_weight=None if w is None else f64(w), scale=scale, eps=eps)
         for h in range(t["q1"].shape[1]):
             v = f64(t["v_cache"][b, :L, h])
             tol = TOL * float(np.sqrt(np.mean(v * v)))
