@@ -272,7 +272,9 @@ da_status diffattn_v1_fwd(const da_v1_fwd_params* p, void* stream) {
 // ----------------------------------------------------------- V1 bwd --------
 size_t diffattn_v1_bwd_workspace_size(int B, int N, int H, int d_qk, int d_v, int deterministic) {
   if (B <= 0 || N <= 0 || H <= 0) return 0;
-  return da::v1_bwd_workspace_bytes(B, N, H, d_qk, d_v, deterministic != 0);
+  // without the mask flag, size for every (key tile, query tile) pair: enough
+  // for a causal call too
+  return da::v1_bwd_workspace_bytes(B, N, H, d_qk, d_v, deterministic != 0, 0);
 }
 
 da_status diffattn_v1_bwd(const da_v1_bwd_params* p, void* stream) {
@@ -283,15 +285,14 @@ da_status diffattn_v1_bwd(const da_v1_bwd_params* p, void* stream) {
   if (!p->dlq1 || !p->dlk1 || !p->dlq2 || !p->dlk2) return DA_ERR_INVALID_ARG;
   if (p->rms_weight && !aligned(p->rms_weight, 4)) return DA_ERR_INVALID_ARG;
   if (p->B == 0 || p->N == 0 || p->H == 0) return DA_OK;
-  // deterministic slots are laid out for the causal (key tile, query tile) pairs
-  if (p->dtype != DA_BF16 || !((p->d_qk == 128 && p->d_v == 256) || (p->d_qk == 64 && p->d_v == 128)) ||
-      (p->deterministic && !p->causal))
+  if (p->dtype != DA_BF16 || !((p->d_qk == 128 && p->d_v == 256) || (p->d_qk == 64 && p->d_v == 128)))
     return DA_ERR_UNSUPPORTED;
   for (const da_t4* t : {&p->q1, &p->q2, &p->k1, &p->k2, &p->v, &p->out, &p->dout, &p->o2,
                          &p->dq1, &p->dq2, &p->dk1, &p->dk2, &p->dv})
     if (check_t4(*t, p->dtype) != DA_OK) return DA_ERR_INVALID_ARG;
   if (!p->lse1 || !p->lse2 || !p->rstd) return DA_ERR_INVALID_ARG;
-  const size_t need = da::v1_bwd_workspace_bytes(p->B, p->N, p->H, p->d_qk, p->d_v, p->deterministic != 0);
+  const size_t need =
+      da::v1_bwd_workspace_bytes(p->B, p->N, p->H, p->d_qk, p->d_v, p->deterministic != 0, p->causal != 0);
   if (p->workspace == nullptr || p->workspace_bytes < need || !aligned(p->workspace, 256))
     return DA_ERR_WORKSPACE;
   DevInfo d = device_info();

@@ -164,7 +164,8 @@ struct V1BwdArgs {
   int deterministic;  // dQ through per-key-tile slots summed in a fixed order
   const float* rms_weight;  // [d_v] or nullptr (unit); entries nonzero
 };
-size_t v1_bwd_workspace_bytes(int B, int N, int H, int d_qk, int d_v, int deterministic);
+// deterministic dQ slots: the causal tile pairs when causal, all pairs otherwise
+size_t v1_bwd_workspace_bytes(int B, int N, int H, int d_qk, int d_v, int deterministic, int causal);
 cudaError_t launch_v1_bwd(const V1BwdArgs& a, cudaStream_t s);
 
 // TMA descriptor encoding (driver entry point fetched through the runtime).

@@ -49,8 +49,9 @@
 //     written as bf16;
 //  3. finalize: dQ accumulators -> bf16, and the lambda-vector gradients.
 // Deterministic mode: the main kernel stores each dQ tile (TMA store) into a
-// slot of its own, (key tile, query tile) compacted to the causal tiles, and
-// the finalize sums a row's slots in ascending key-tile order instead of
+// slot of its own, (key tile, query tile) compacted to the causal tiles (all
+// pairs when not causal), and the finalize sums a row's slots in ascending
+// key-tile order instead of
 // reading an accumulator, so no result depends on the order in which CTAs
 // finish.
 //
@@ -214,26 +215,28 @@ struct BwdWs {
                        // [B*H, n_slots, 64, d_qk] per-tile slots
   float* dlam_part;    // [preprocess blocks]
   int npad, pre_blocks;
-  int det, n_kt, n_qt, n_slots;
+  int det, causal, n_kt, n_qt, n_slots;
 };
 
-// Slot of the dQ tile of (key tile kt, query tile qt), qt >= 2 kt: the causal
-// tiles of key tiles 0 .. kt-1 come first.
-__host__ __device__ __forceinline__ int dq_slot(int kt, int qt, int n_qt) {
-  return kt * n_qt - kt * (kt - 1) + (qt - 2 * kt);
+// Slot of the dQ tile of (key tile kt, query tile qt).  Causal: qt >= 2 kt,
+// and the causal tiles of key tiles 0 .. kt-1 come first.  Not causal: every
+// pair, key-tile major.
+__host__ __device__ __forceinline__ int dq_slot(int kt, int qt, int n_qt, int causal) {
+  return causal ? kt * n_qt - kt * (kt - 1) + (qt - 2 * kt) : kt * n_qt + qt;
 }
 
 size_t a256(size_t x) { return (x + 255) & ~size_t(255); }
 
 constexpr int kPreWarps = 8;
 
-BwdWs carve(void* base, int B, int N, int H, int dqk, int dv, bool det, size_t* total) {
+BwdWs carve(void* base, int B, int N, int H, int dqk, int dv, bool det, bool causal, size_t* total) {
   BwdWs w;
   w.npad = (N + kQT - 1) / kQT * kQT;
   w.det = det ? 1 : 0;
+  w.causal = causal ? 1 : 0;
   w.n_kt = (N + kKT - 1) / kKT;
   w.n_qt = w.npad / kQT;
-  w.n_slots = w.n_kt * w.n_qt - w.n_kt * (w.n_kt - 1);
+  w.n_slots = causal ? w.n_kt * w.n_qt - w.n_kt * (w.n_kt - 1) : w.n_kt * w.n_qt;
   w.pre_blocks = static_cast<int>((static_cast<long long>(B) * H * w.npad + kPreWarps - 1) / kPreWarps);
   uint8_t* p = static_cast<uint8_t*>(base);
   size_t off = 0;
@@ -685,7 +688,7 @@ v1_bwd_main_kernel(const __grid_constant__ CUtensorMap tm_q1, const __grid_const
           // add the [64 queries][64 features] tile into the fp32 accumulator
           // (rows past N are dropped by the unit), or store it into its slot
           if (w.det)
-            tma_store_4d(tdq, sh.base + kOffStg, half * 64, 0, dq_slot(it.kt, it.i0 + k, w.n_qt),
+            tma_store_4d(tdq, sh.base + kOffStg, half * 64, 0, dq_slot(it.kt, it.i0 + k, w.n_qt, w.causal),
                          it.b * a.H + it.h);
           else
             tma_reduce_add_4d(tdq, sh.base + kOffStg, half * 64, it.h, (it.i0 + k) * kQT, it.b);
@@ -926,14 +929,16 @@ v1_bwd_finalize_kernel(V1BwdArgs a, BwdWs w) {
     for (int t = 0; t < 2; ++t) {
       float4 x0, x1;
       if (w.det) {
-        // the key tiles 0 .. qt / 2 that reach this query row, in that order
+        // the key tiles that reach this query row (0 .. qt / 2 when causal,
+        // all of them otherwise), in that order
         const int qt = n / kQT;
+        const int kt_end = w.causal ? qt / 2 : w.n_kt - 1;
         const float* base = w.dq[t] + (static_cast<int64_t>(b) * a.H + h) * w.n_slots * (kQT * kDqk) +
                             (n % kQT) * kDqk + c8;
         x0 = make_float4(0.f, 0.f, 0.f, 0.f);
         x1 = x0;
-        for (int kt = 0; kt <= qt / 2; ++kt) {
-          const float* src = base + static_cast<int64_t>(dq_slot(kt, qt, w.n_qt)) * (kQT * kDqk);
+        for (int kt = 0; kt <= kt_end; ++kt) {
+          const float* src = base + static_cast<int64_t>(dq_slot(kt, qt, w.n_qt, w.causal)) * (kQT * kDqk);
           const float4 y0 = *reinterpret_cast<const float4*>(src);
           const float4 y1 = *reinterpret_cast<const float4*>(src + 4);
           x0.x += y0.x; x0.y += y0.y; x0.z += y0.z; x0.w += y0.w;
@@ -985,7 +990,7 @@ template <int DQK, int DV>
 cudaError_t launch_dims(const V1BwdArgs& a, cudaStream_t s) {
   constexpr int kDqk = DQK, kDv = DV;
   size_t total = 0;
-  BwdWs w = carve(a.workspace, a.B, a.N, a.H, DQK, DV, a.deterministic != 0, &total);
+  BwdWs w = carve(a.workspace, a.B, a.N, a.H, DQK, DV, a.deterministic != 0, a.causal != 0, &total);
   if (total > a.workspace_bytes) return cudaErrorInvalidValue;
 
   v1_bwd_pre_kernel<DQK, DV><<<w.pre_blocks, kPreWarps * 32, 0, s>>>(a, w);
@@ -1040,9 +1045,9 @@ cudaError_t launch_dims(const V1BwdArgs& a, cudaStream_t s) {
 
 }  // namespace
 
-size_t v1_bwd_workspace_bytes(int B, int N, int H, int d_qk, int d_v, int deterministic) {
+size_t v1_bwd_workspace_bytes(int B, int N, int H, int d_qk, int d_v, int deterministic, int causal) {
   size_t total = 0;
-  carve(nullptr, B, N, H, d_qk, d_v, deterministic != 0, &total);
+  carve(nullptr, B, N, H, d_qk, d_v, deterministic != 0, causal != 0, &total);
   return total;
 }
 

@@ -129,18 +129,19 @@ da_status diffattn_v1_fwd(const da_v1_fwd_params* p, void* cuda_stream);
  * unit); its entries must be nonzero, since the backward recovers the
  * normalised output as Y / ((1 - lambda_init) w).  Supported: DA_BF16,
  * (d_qk, d_v) = (128, 256) or
- * (64, 128), causal or not; deterministic = 1 needs causal = 1
- * (DA_ERR_UNSUPPORTED otherwise: its dQ slots are laid out for the causal
- * tile pairs).
+ * (64, 128), causal or not, either mode.
  * workspace: at least diffattn_v1_bwd_workspace_size(..., deterministic)
- * bytes, 256-byte aligned; its contents on entry do not matter.
+ * bytes, 256-byte aligned; its contents on entry do not matter.  (With
+ * deterministic set, that size covers the slots of every tile pair, as a call
+ * without the causal mask needs; a causal call uses about half of them.)
  * deterministic = 0: each key tile adds its dQ tile into an fp32 accumulator
  * (TMA reduce-add), so dQ1 / dQ2 may differ in the last bits between runs;
  * every other output is reproducible.  deterministic != 0: each key tile
  * stores its dQ tile into its own slot of the workspace and the finalize sums
  * the slots in ascending key-tile order, so every output is bitwise
  * reproducible; the workspace grows by about B*H*N^2/64 * 4 bytes per stream
- * (causal tiles only) and the call takes longer. */
+ * (B*H*N^2/128 * 4 of them written by a causal call) and the call takes
+ * longer. */
 typedef struct {
   int B, N, H, d_qk, d_v;
   da_dtype dtype;

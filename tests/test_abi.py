@@ -80,8 +80,8 @@ def test_v1_fwd_argument_checks(lib):
 
 
 def test_v1_bwd_causal_and_deterministic_checks(lib):
-    """Not causal is supported; deterministic dQ slots exist only for the
-    causal (key tile, query tile) pairs, so that pair is refused up front."""
+    """Causal or not, either dQ mode, is accepted (each combination reaches
+    the workspace check, with none given)."""
     p = bd.da_v1_bwd_params()
     p.B, p.N, p.H, p.d_qk, p.d_v, p.dtype = 1, 256, 2, 128, 256, bd.DA_BF16
     p.lambda_init, p.rms_eps = 0.2, 1e-5
@@ -94,7 +94,7 @@ def test_v1_bwd_causal_and_deterministic_checks(lib):
         setattr(p, n, fake)
     f = lib.diffattn_v1_bwd
     for causal, det, want in ((1, 0, bd.DA_ERR_WORKSPACE), (0, 0, bd.DA_ERR_WORKSPACE),
-                              (1, 1, bd.DA_ERR_WORKSPACE), (0, 1, bd.DA_ERR_UNSUPPORTED)):
+                              (1, 1, bd.DA_ERR_WORKSPACE), (0, 1, bd.DA_ERR_WORKSPACE)):
         p.causal, p.deterministic = causal, det
         assert f(C.byref(p), None) == want, (causal, det)
 
@@ -181,10 +181,12 @@ def test_bwd_workspace_size(lib):
     # d_v bf16 of dO + 2 streams x d_qk fp32 = 512 -> 256 bytes)
     small = lib.diffattn_v1_bwd_workspace_size(1, 8192, 16, 64, 128, 0)
     assert base - small >= 8192 * 16 * 256
-    # deterministic mode: one fp32 [64, 128] slot per causal (key tile, query
-    # tile) pair and stream replaces the [N, 128] accumulators
+    # deterministic mode: one fp32 [64, 128] slot per (key tile, query tile)
+    # pair and stream replaces the [N, 128] accumulators; the size query has no
+    # mask flag, so it covers every pair (a causal call uses only the pairs
+    # with query tile >= 2 key tile)
     n_kt, n_qt = 8192 // 128, 8192 // 64
-    slots = n_kt * n_qt - n_kt * (n_kt - 1)
+    slots = n_kt * n_qt
     assert det - base == 2 * 16 * (slots * 64 - 8192) * 128 * 4
     assert lib.diffattn_v2_bwd_workspace_size(2, 8192, 32, 4096) > lib.diffattn_v2_bwd_workspace_size(2, 8192, 32, 0)
 

@@ -3,7 +3,8 @@ oracle, with the bars of the fixed-shape parity tests (their checks are
 reused as they are): batch, length (one token, under a tile, whole tiles,
 ragged tails over several tiles), head counts and group sizes, head dims,
 causal or not, the layer index, an RMSNorm weight, decode lengths and split
-counts, the softmax scale and the V1 RMSNorm epsilon are drawn together, so that combinations the hand-picked cases leave
+counts, the softmax scale, the V1 RMSNorm epsilon and the V1 backward's
+deterministic mode are drawn together, so that combinations the hand-picked cases leave
 out are run as well.  The draws are fixed by the seed; the CPU test checks
 that every drawn shape is one the entry points accept and that the sweep
 spans the categories it claims."""
@@ -48,6 +49,8 @@ def sweep_cases(op, n=CASES, seed=SEED):
             cases.append(dict(B=rng.randint(1, 3), N=_length(rng, i, cap), H=rng.randint(1, 3 if op == "v1_bwd" else 4),
                               dqk=dqk, dv=dv, causal=causal, layer=rng.randint(1, 28),
                               weighted=rng.random() < 0.3, eps=_eps(rng)))
+            if op == "v1_bwd":  # every fourth step with dQ through the ordered slots
+                cases[-1]["det"] = i % 4 == 1
         elif op in ("v2_fwd", "v2_bwd"):
             hkv = rng.choice([1, 2, 4])
             per = rng.choice([1, 2] if op == "v2_bwd" else [1, 2, 4])  # head pairs per K/V head
@@ -118,6 +121,8 @@ def test_sweep_shapes_are_valid():
         assert any(c["scale"] is not None for c in cases) and any(c["scale"] is None for c in cases)
         if op.startswith("v1"):
             assert any(c["eps"] > 1e-4 for c in cases) and all(c["eps"] > 0 for c in cases)
+        if op == "v1_bwd":
+            assert any(c["det"] for c in cases) and not all(c["det"] for c in cases)
         if not op.endswith("decode"):
             ns = [c["N"] for c in cases]
             assert any(n < 128 for n in ns) and any(n % 128 == 0 for n in ns)
@@ -186,9 +191,10 @@ def test_sweep_v1_bwd(c, gpu_ops):
     ref = orc.v1_backward(*(_f64(t[n]) for n in tv1b.NAMES), li, _f64(t["dy"]), causal=c["causal"], rms_weight=wf,
                           scale=sc, eps=eps)
     tv1b._compare(tv1b._run_exact_saves(t, li, causal=c["causal"], w=w, scale=sc, eps=eps), ref,
-                  tv1b._model(t, li, causal=c["causal"], w=w, scale=sc, eps=eps), bar="bwd")
-    tv1b._compare(tv1b._run(t, li, causal=c["causal"], w=w, scale=sc, eps=eps), ref,
-                  tv1b._model(t, li, causal=c["causal"], w=w, step=True, scale=sc, eps=eps), bar="step")
+                  tv1b._model(t, li, causal=c["causal"], w=w, scale=sc, eps=eps), bar="bwd", layer=c["layer"])
+    tv1b._compare(tv1b._run(t, li, causal=c["causal"], w=w, scale=sc, eps=eps, deterministic=c["det"]), ref,
+                  tv1b._model(t, li, causal=c["causal"], w=w, step=True, scale=sc, eps=eps), bar="step",
+                  layer=c["layer"])
 
 
 @pytest.mark.gpu

@@ -21,10 +21,15 @@ reaches 11 % of RMS on dV).  So, per gradient tensor:
   dK error, about ten times the backward-only model's, and the GPU step
   follows the forward-aware model to within the backward's own rounding;
 * ||GPU - oracle|| <= 1.5e-2 ||oracle|| (2e-2 for the step), a fixed bar that
-  does not involve the model; only where a gradient vanishes analytically
-  (N = 1: dQ and dK are exactly zero, the oracle's norm is rounding residue)
-  is it k times the model's own Frobenius error, since then nothing but
-  rounding noise is left to compare;
+  does not involve the model, or k times the model's own Frobenius error
+  where that is larger: under strong cancellation the storage points alone
+  exceed the fixed bar (lambda 0.98, N 72: the first rows see one or two
+  keys, O1 and lambda O2 nearly cancel, rstd reaches 48, and the step's
+  forward-aware model has 3.7 % on dQ, exactly the GPU's).  At layer 1,
+  every bench workload, the fixed term must be the one that applies (the
+  test asserts it).  Where a gradient vanishes analytically (N = 1: dQ and
+  dK are exactly zero, the oracle's norm is rounding residue) only the
+  model term is used, since nothing but rounding noise is left to compare;
 * the four lambda-vector gradients (dlambda times fixed vectors) against the
   oracle's, max-abs within rel * max|oracle|: rel = k * (the model's relative
   dlambda error) + 2e-3 for the backward alone.  In the training step
@@ -67,15 +72,15 @@ def _status_clean():
     assert bd.diffattn_get_device_status() == bd.DA_OK
 
 
-def _run(t, li, causal=True, w=None, scale=None, eps=1e-5):
+def _run(t, li, causal=True, w=None, scale=None, eps=1e-5, deterministic=False):
     """The training step: GPU forward with saves, then the GPU backward
     (scale: the softmax scale, None = the default 1/sqrt(d_qk); eps: the
-    RMSNorm epsilon)."""
+    RMSNorm epsilon; deterministic: dQ through the ordered slots)."""
     ss = 0.0 if scale is None else scale
     y, sv = bd.diffattn_v1_fwd(*(t[n] for n in NAMES), li, save=True, causal=causal, rms_weight=w,
                                softmax_scale=ss, rms_eps=eps)
     g = bd.diffattn_v1_bwd(*(t[n] for n in NAMES), li, y, t["dy"], sv, causal=causal, rms_weight=w,
-                           softmax_scale=ss, rms_eps=eps)
+                           softmax_scale=ss, rms_eps=eps, deterministic=deterministic)
     torch.cuda.synchronize()
     return g
 
@@ -96,7 +101,11 @@ def _run_exact_saves(t, li, causal=True, w=None, scale=None, eps=1e-5):
     return g
 
 
-def _compare(g, ref, model, heads=None, lam_vectors=True, bar="bwd"):
+def _compare(g, ref, model, heads=None, lam_vectors=True, bar="bwd", layer=None):
+    """Every gradient against the oracle (bars in the module docstring).
+    layer: the model layer of the case; at layer 1 (every bench workload,
+    little cancellation between the streams) the fixed Frobenius bar must be
+    the one that applies."""
     k, fro = BARS[bar]
     floor = 1e-3 * float(np.sqrt(np.mean(ref["dv"] ** 2)))
     dv_norm = float(np.linalg.norm(ref["dv"]))
@@ -109,10 +118,16 @@ def _compare(g, ref, model, heads=None, lam_vectors=True, bar="bwd"):
         allowed = k * float(np.max(np.abs(mod - exp))) + 1e-3 * rms + floor
         worst[n] = float(np.max(np.abs(got - exp))) / allowed
         exp_norm = float(np.linalg.norm(exp))
+        model_fro = k * float(np.linalg.norm(mod - exp))
         if exp_norm > 1e-9 * dv_norm:
-            fro_allowed = fro * exp_norm
+            # fixed, unless the storage points alone exceed it (strong
+            # cancellation: the first rows of a causal map see one or two
+            # keys, so O1 and lambda O2 nearly cancel there at lambda near 1)
+            fro_allowed = max(fro * exp_norm, model_fro)
+            if layer == 1:
+                assert model_fro <= fro * exp_norm, (n, model_fro / (fro * exp_norm))
         else:  # analytically zero (N = 1): rounding noise against rounding noise
-            fro_allowed = k * float(np.linalg.norm(mod - exp))
+            fro_allowed = model_fro
         worst[n + "_fro"] = float(np.linalg.norm(got - exp)) / (fro_allowed + floor * np.sqrt(exp.size))
     if lam_vectors:
         if bar == "step":
@@ -154,8 +169,8 @@ def test_v1_bwd_parity_small(B, N, H, layer):
     t = synth.v1_inputs(B, N, H, 128, 256, "bf16", seed=5000 + N + H, device="cuda", with_dy=True)
     li = float(np.float32(bd.diffattn_lambda_init(layer)))
     ref = orc.v1_backward(*(f64(t[n]) for n in NAMES), li, f64(t["dy"]))
-    _compare(_run_exact_saves(t, li), ref, _model(t, li), bar="bwd")
-    _compare(_run(t, li), ref, _model(t, li, step=True), bar="step")
+    _compare(_run_exact_saves(t, li), ref, _model(t, li), bar="bwd", layer=layer)
+    _compare(_run(t, li), ref, _model(t, li, step=True), bar="step", layer=layer)
 
 
 @pytest.mark.parametrize("B,N,H,layer", [(1, 200, 2, 1), (2, 129, 1, 14), (1, 1, 1, 1), (1, 500, 2, 5)])
@@ -165,8 +180,8 @@ def test_v1_bwd_parity_head_dims_64_128(B, N, H, layer):
     t = synth.v1_inputs(B, N, H, 64, 128, "bf16", seed=5100 + N + H, device="cuda", with_dy=True)
     li = float(np.float32(bd.diffattn_lambda_init(layer)))
     ref = orc.v1_backward(*(f64(t[n]) for n in NAMES), li, f64(t["dy"]))
-    _compare(_run_exact_saves(t, li), ref, _model(t, li), bar="bwd")
-    _compare(_run(t, li), ref, _model(t, li, step=True), bar="step")
+    _compare(_run_exact_saves(t, li), ref, _model(t, li), bar="bwd", layer=layer)
+    _compare(_run(t, li), ref, _model(t, li, step=True), bar="step", layer=layer)
 
 
 def test_v1_bwd_deterministic_head_dims_64_128():
@@ -174,8 +189,9 @@ def test_v1_bwd_deterministic_head_dims_64_128():
     and the lambda-vector gradients bitwise equal to the default mode's (the
     mode changes only how dQ leaves the main kernel); every gradient against
     the oracle, the lambda vectors included."""
+    layer = 3
     t = synth.v1_inputs(1, 400, 2, 64, 128, "bf16", seed=5150, device="cuda", with_dy=True)
-    li = float(np.float32(bd.diffattn_lambda_init(3)))
+    li = float(np.float32(bd.diffattn_lambda_init(layer)))
     y, sv = bd.diffattn_v1_fwd(*(t[n] for n in NAMES), li, save=True)
     g0 = bd.diffattn_v1_bwd(*(t[n] for n in NAMES), li, y, t["dy"], sv)
     g1 = bd.diffattn_v1_bwd(*(t[n] for n in NAMES), li, y, t["dy"], sv, deterministic=True)
@@ -186,7 +202,7 @@ def test_v1_bwd_deterministic_head_dims_64_128():
     for n in ("dk1", "dk2", "dv", "dlq1", "dlk1", "dlq2", "dlk2"):
         assert torch.equal(g0[n], g1[n]), n
     ref = orc.v1_backward(*(f64(t[n]) for n in NAMES), li, f64(t["dy"]))
-    _compare(g1, ref, _model(t, li, step=True), bar="step")
+    _compare(g1, ref, _model(t, li, step=True), bar="step", layer=layer)
 
 
 @pytest.mark.parametrize("B,N,H,dqk,layer", [(1, 200, 2, 128, 1), (2, 129, 1, 64, 14), (1, 1, 1, 128, 1),
@@ -197,8 +213,8 @@ def test_v1_bwd_parity_not_causal(B, N, H, dqk, layer):
     t = synth.v1_inputs(B, N, H, dqk, 2 * dqk, "bf16", seed=5200 + N + H, device="cuda", with_dy=True)
     li = float(np.float32(bd.diffattn_lambda_init(layer)))
     ref = orc.v1_backward(*(f64(t[n]) for n in NAMES), li, f64(t["dy"]), causal=False)
-    _compare(_run_exact_saves(t, li, causal=False), ref, _model(t, li, causal=False), bar="bwd")
-    _compare(_run(t, li, causal=False), ref, _model(t, li, causal=False, step=True), bar="step")
+    _compare(_run_exact_saves(t, li, causal=False), ref, _model(t, li, causal=False), bar="bwd", layer=layer)
+    _compare(_run(t, li, causal=False), ref, _model(t, li, causal=False, step=True), bar="step", layer=layer)
 
 
 @pytest.mark.parametrize("B,N,H,dqk,layer", [(1, 200, 2, 128, 1), (2, 129, 1, 64, 14)])
@@ -209,8 +225,8 @@ def test_v1_bwd_parity_rms_weight(B, N, H, dqk, layer):
     w = 0.5 + torch.rand(2 * dqk, generator=torch.Generator().manual_seed(5301), dtype=torch.float32).cuda()
     li = float(np.float32(bd.diffattn_lambda_init(layer)))
     ref = orc.v1_backward(*(f64(t[n]) for n in NAMES), li, f64(t["dy"]), rms_weight=f64(w))
-    _compare(_run_exact_saves(t, li, w=w), ref, _model(t, li, w=w), bar="bwd")
-    _compare(_run(t, li, w=w), ref, _model(t, li, w=w, step=True), bar="step")
+    _compare(_run_exact_saves(t, li, w=w), ref, _model(t, li, w=w), bar="bwd", layer=layer)
+    _compare(_run(t, li, w=w), ref, _model(t, li, w=w, step=True), bar="step", layer=layer)
 
 
 def test_v1_bwd_strided_packed_views():
@@ -251,11 +267,12 @@ def test_v1_bwd_deterministic_parts_repeat():
 def test_v1_bwd_h16_n1024_all_heads():
     """16 heads at N 1024: every gradient incl. the lambda vectors (dlambda
     sums over all heads and rows)."""
+    layer = 1
     t = synth.v1_inputs(1, 1024, 16, 128, 256, "bf16", seed=62, device="cuda", with_dy=True)
-    li = float(np.float32(bd.diffattn_lambda_init(1)))
+    li = float(np.float32(bd.diffattn_lambda_init(layer)))
     ref = orc.v1_backward(*(f64(t[n]) for n in NAMES), li, f64(t["dy"]))
-    _compare(_run_exact_saves(t, li), ref, _model(t, li), bar="bwd")
-    _compare(_run(t, li), ref, _model(t, li, step=True), bar="step")
+    _compare(_run_exact_saves(t, li), ref, _model(t, li), bar="bwd", layer=layer)
+    _compare(_run(t, li), ref, _model(t, li, step=True), bar="step", layer=layer)
 
 
 def test_v1_bwd_full_size_b1_h16_n8192():
@@ -264,14 +281,15 @@ def test_v1_bwd_full_size_b1_h16_n8192():
     backward, all 16 heads, and every gradient is compared element by element:
     dQ1, dQ2, dK1, dK2, dV and the four lambda-vector gradients, whose dlambda
     sums over every head and all 8192 rows."""
+    layer = 1
     t = synth.v1_inputs(1, 8192, 16, 128, 256, "bf16", seed=1005, device="cuda", with_dy=True)
-    li = float(np.float32(bd.diffattn_lambda_init(1)))
+    li = float(np.float32(bd.diffattn_lambda_init(layer)))
     g = _run(t, li)
     f = {n: f64(t[n]) for n in NAMES + ("dy",)}
     del t
     torch.cuda.empty_cache()
     ref, model = v1_backward_by_head(f, li, step=True)
-    _compare(g, ref, model, bar="step")
+    _compare(g, ref, model, bar="step", layer=layer)
 
 
 @pytest.mark.parametrize("B,N,H,layer", [(1, 300, 2, 2), (2, 129, 1, 14), (1, 1, 1, 1)])
@@ -288,7 +306,30 @@ def test_v1_bwd_deterministic_mode(B, N, H, layer):
     torch.cuda.synchronize()
     for n in g1:
         assert torch.equal(g1[n], g2[n]), n
-    _compare(g1, ref, model, bar="step")
+    _compare(g1, ref, model, bar="step", layer=layer)
+
+
+@pytest.mark.parametrize("B,N,H,dqk", [(1, 300, 2, 128), (2, 129, 1, 64), (1, 1, 1, 128), (1, 640, 1, 128)])
+def test_v1_bwd_deterministic_not_causal(B, N, H, dqk):
+    """deterministic=True without the causal mask: a dQ slot for every (key
+    tile, query tile) pair, a row's slots summed over all key tiles in
+    ascending order.  A bitwise repeat; dK, dV and the lambda-vector
+    gradients bitwise equal to the default mode's; every gradient against
+    the oracle."""
+    layer = 4
+    t = synth.v1_inputs(B, N, H, dqk, 2 * dqk, "bf16", seed=5500 + N + H, device="cuda", with_dy=True)
+    li = float(np.float32(bd.diffattn_lambda_init(layer)))
+    ref = orc.v1_backward(*(f64(t[n]) for n in NAMES), li, f64(t["dy"]), causal=False)
+    y, sv = bd.diffattn_v1_fwd(*(t[n] for n in NAMES), li, save=True, causal=False)
+    g0 = bd.diffattn_v1_bwd(*(t[n] for n in NAMES), li, y, t["dy"], sv, causal=False)
+    g1 = bd.diffattn_v1_bwd(*(t[n] for n in NAMES), li, y, t["dy"], sv, causal=False, deterministic=True)
+    g2 = bd.diffattn_v1_bwd(*(t[n] for n in NAMES), li, y, t["dy"], sv, causal=False, deterministic=True)
+    torch.cuda.synchronize()
+    for n in g1:
+        assert torch.equal(g1[n], g2[n]), n
+    for n in ("dk1", "dk2", "dv", "dlq1", "dlk1", "dlq2", "dlk2"):
+        assert torch.equal(g0[n], g1[n]), n
+    _compare(g1, ref, _model(t, li, causal=False, step=True), bar="step", layer=layer)
 
 
 def test_v1_bwd_deterministic_full_size_repeat():
