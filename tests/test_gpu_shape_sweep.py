@@ -51,6 +51,11 @@ def sweep_cases(op, n=CASES, seed=SEED):
                               weighted=rng.random() < 0.3, eps=_eps(rng)))
             if op == "v1_bwd":  # every fourth step with dQ through the ordered slots
                 cases[-1]["det"] = i % 4 == 1
+        elif op == "v1_fwd_f32":
+            # the fp32 path: any d_qk <= 128, d_v <= 256 with d_v % 32 == 0
+            cases.append(dict(B=rng.randint(1, 3), N=_length(rng, i, 384), H=rng.randint(1, 4),
+                              dqk=rng.randint(1, 128), dv=32 * rng.randint(1, 8), causal=causal,
+                              layer=rng.randint(1, 28), weighted=rng.random() < 0.3, eps=_eps(rng)))
         elif op in ("v2_fwd", "v2_bwd"):
             hkv = rng.choice([1, 2, 4])
             per = rng.choice([1, 2] if op == "v2_bwd" else [1, 2, 4])  # head pairs per K/V head
@@ -87,7 +92,8 @@ def sweep_cases(op, n=CASES, seed=SEED):
     return cases
 
 
-OPS = ("v1_fwd", "v1_bwd", "v2_fwd", "v2_bwd", "grouped_fwd", "grouped_bwd", "v2_decode", "v1_decode")
+OPS = ("v1_fwd", "v1_bwd", "v1_fwd_f32", "v2_fwd", "v2_bwd", "grouped_fwd", "grouped_bwd", "v2_decode",
+       "v1_decode")
 
 
 def _ids(op):
@@ -115,8 +121,10 @@ def test_sweep_shapes_are_valid():
                 assert all(1 <= s <= c["L"] for s in c["seqlens"])
             if op == "v2_decode":
                 assert c["h"] % c["hkv"] == 0
-            if op.startswith("v1") and op != "v1_decode":
+            if op in ("v1_fwd", "v1_bwd"):
                 assert (c["dqk"], c["dv"]) in ((128, 256), (64, 128))
+            if op == "v1_fwd_f32":
+                assert 1 <= c["dqk"] <= 128 and c["dv"] <= 256 and c["dv"] % 32 == 0
             assert c["scale"] is None or (0 < c["scale"] < 1 and float(np.float32(c["scale"])) == c["scale"])
         assert any(c["scale"] is not None for c in cases) and any(c["scale"] is None for c in cases)
         if op.startswith("v1"):
@@ -273,3 +281,29 @@ def test_sweep_v1_decode(c, gpu_ops):
     w = _rms_weight(c["dv"], 18001) if c["weighted"] else None
     tv1d._check(t, li, tv1d._run(t, li, num_splits=c["splits"], rms_weight=w, softmax_scale=_ss(c),
                                  rms_eps=c["eps"]), w=w, scale=c["scale"], eps=c["eps"])
+
+
+@pytest.mark.gpu
+@pytest.mark.parametrize("c", sweep_cases("v1_fwd_f32"), ids=_ids("v1_fwd_f32"))
+def test_sweep_v1_fwd_f32(c, gpu_ops):
+    """The fp32 V1 path (its own SIMT kernel) at drawn head dims: Y and O2
+    within 1e-4 * RMS(V), the LSEs within 1e-4, rstd within 1e-4 relative."""
+    from differential_attention_diff_gb300 import synth
+    from oracle import diffattn_oracle as orc
+    bd, tsm = gpu_ops["bd"], gpu_ops["tsm"]
+    names = ("q1", "q2", "k1", "k2", "v", "lq1", "lk1", "lq2", "lk2")
+    t = synth.v1_inputs(c["B"], c["N"], c["H"], c["dqk"], c["dv"], dtype="f32", seed=19000 + c["N"], device="cuda")
+    li = bd.diffattn_lambda_init(c["layer"])
+    w = _rms_weight(c["dv"], 19001) if c["weighted"] else None
+    out, sv = bd.diffattn_v1_fwd(*(t[n] for n in names), li, save=True, causal=c["causal"], rms_weight=w,
+                                 softmax_scale=_ss(c), rms_eps=c["eps"])
+    torch.cuda.synchronize()
+    ref = orc.v1_forward(*(_f64(t[n]) for n in names), float(np.float32(li)), causal=c["causal"],
+                         rms_weight=None if w is None else _f64(w), scale=c["scale"], eps=c["eps"])
+    tol = tsm.F32_TOL * float(np.sqrt(np.mean(_f64(t["v"]) ** 2)))
+    worst = max(tsm.maxdiff(_f64(out), ref["y"]), tsm.maxdiff(_f64(sv["o2"]), ref["o2"])) / tol
+    tsm.record({"y_o2": worst})
+    assert worst <= 1.0, worst
+    assert tsm.maxdiff(_f64(sv["lse1"]), ref["lse1"]) <= 1e-4
+    assert tsm.maxdiff(_f64(sv["lse2"]), ref["lse2"]) <= 1e-4
+    assert np.max(np.abs(_f64(sv["rstd"]) / ref["rstd"] - 1)) <= 1e-4
