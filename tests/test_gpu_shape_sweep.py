@@ -3,8 +3,8 @@ oracle, with the bars of the fixed-shape parity tests (their checks are
 reused as they are): batch, length (one token, under a tile, whole tiles,
 ragged tails over several tiles), head counts and group sizes, head dims,
 causal or not, the layer index, an RMSNorm weight, decode lengths and split
-counts, the softmax scale, the V1 RMSNorm epsilon and the V1 backward's
-deterministic mode are drawn together, so that combinations the hand-picked cases leave
+counts, the softmax scale, the V1 RMSNorm epsilon, the V1 backward's
+deterministic mode and strided input views are drawn together, so that combinations the hand-picked cases leave
 out are run as well.  The draws are fixed by the seed; the CPU test checks
 that every drawn shape is one the entry points accept and that the sweep
 spans the categories it claims."""
@@ -89,6 +89,8 @@ def sweep_cases(op, n=CASES, seed=SEED):
         else:
             raise ValueError(op)
         cases[-1]["scale"] = scale
+        # every fourth case reads its 4-D inputs through strided views
+        cases[-1]["strided"] = i % 4 == 3
     return cases
 
 
@@ -166,6 +168,26 @@ def _ss(c):
     return 0.0 if c["scale"] is None else c["scale"]
 
 
+def _strided(t, names, seed):
+    """The 4-D tensors `names` of t as views into larger NaN-filled buffers:
+    one or two extra heads and a few extra rows per batch, the view starting
+    at a drawn head and row offset, so that every batch, row and head stride
+    differs from the contiguous one.  A kernel that read outside its view
+    would pick up NaN and fail parity."""
+    rng = random.Random(seed)
+    out = dict(t)
+    for n in names:
+        x = t[n]
+        B, N, H, D = x.shape
+        ph, pn = rng.randint(1, 2), rng.randint(1, 5)
+        oh, on = rng.randint(0, ph), rng.randint(0, pn)
+        buf = torch.full((B, N + pn, H + ph, D), float("nan"), dtype=x.dtype, device=x.device)
+        v = buf[:, on:on + N, oh:oh + H]
+        v.copy_(x)
+        out[n] = v
+    return out
+
+
 def _rms_weight(n, seed):
     return 0.5 + torch.rand(n, generator=torch.Generator().manual_seed(seed), dtype=torch.float32).cuda()
 
@@ -176,6 +198,8 @@ def test_sweep_v1_fwd(c, gpu_ops):
     from differential_attention_diff_gb300 import synth
     bd, tv1 = gpu_ops["bd"], gpu_ops["tv1"]
     t = synth.v1_inputs(c["B"], c["N"], c["H"], c["dqk"], c["dv"], "bf16", seed=11000 + c["N"], device="cuda")
+    if c["strided"]:
+        t = _strided(t, ("q1", "q2", "k1", "k2", "v"), 11002 + c["N"])
     li = bd.diffattn_lambda_init(c["layer"])
     w = _rms_weight(c["dv"], 11001) if c["weighted"] else None
     y, sv = bd.diffattn_v1_fwd(*(t[n] for n in tv1.NAMES), li, save=True, causal=c["causal"], rms_weight=w,
@@ -192,6 +216,8 @@ def test_sweep_v1_bwd(c, gpu_ops):
     bd, tv1b = gpu_ops["bd"], gpu_ops["tv1b"]
     t = synth.v1_inputs(c["B"], c["N"], c["H"], c["dqk"], c["dv"], "bf16", seed=12000 + c["N"], device="cuda",
                         with_dy=True)
+    if c["strided"]:
+        t = _strided(t, ("q1", "q2", "k1", "k2", "v", "dy"), 12002 + c["N"])
     li = float(np.float32(bd.diffattn_lambda_init(c["layer"])))
     w = _rms_weight(c["dv"], 12001) if c["weighted"] else None
     wf = None if w is None else _f64(w)
@@ -212,6 +238,8 @@ def test_sweep_v2_fwd(c, gpu_ops):
     from oracle import diffattn_oracle as orc
     bd, tv2 = gpu_ops["bd"], gpu_ops["tv2"]
     t = synth.v2_inputs(c["B"], c["N"], c["h"], c["hkv"], c["d"], c["dm"], seed=13000 + c["N"], device="cuda")
+    if c["strided"]:
+        t = _strided(t, ("q", "k", "v"), 13002 + c["N"])
     lse = torch.empty((c["B"], 2 * c["h"], c["N"]), dtype=torch.float32, device="cuda")
     out = bd.diffattn_v2_fwd(t["q"], t["k"], t["v"], x=t["x"], w_lambda=t["w_lambda"], lse=lse, causal=c["causal"],
                              softmax_scale=_ss(c))
@@ -227,6 +255,8 @@ def test_sweep_v2_bwd(c, gpu_ops):
     tv2b = gpu_ops["tv2b"]
     t = synth.v2_inputs(c["B"], c["N"], c["h"], c["hkv"], c["d"], c["dm"], seed=14000 + c["N"], device="cuda",
                         with_dout=True)
+    if c["strided"]:
+        t = _strided(t, ("q", "k", "v", "dout"), 14002 + c["N"])
     sc = c["scale"]
     ref, fwd, model = tv2b._reference(t, causal=c["causal"], scale=sc)
     tv2b._compare(tv2b._run_exact_saves(t, fwd, causal=c["causal"], scale=sc), ref, model, bar="bwd")
@@ -240,6 +270,8 @@ def test_sweep_grouped_fwd(c, gpu_ops):
     bd, tg = gpu_ops["bd"], gpu_ops["tg"]
     t = synth.grouped_inputs(c["B"], c["N"], c["h"], c["ratio"], c["hkv"], c["d"], c["dm"], seed=15000 + c["N"],
                              device="cuda")
+    if c["strided"]:
+        t = _strided(t, ("q", "k", "v"), 15002 + c["N"])
     out = bd.diffattn_grouped_fwd(t["q"], t["k"], t["v"], c["ratio"], x=t["x"], w_lambda=t["w_lambda"],
                                   causal=c["causal"], softmax_scale=_ss(c))
     torch.cuda.synchronize()
@@ -251,6 +283,8 @@ def test_sweep_grouped_fwd(c, gpu_ops):
 def test_sweep_grouped_bwd(c, gpu_ops):
     tgb = gpu_ops["tgb"]
     t = tgb._inputs(c["B"], c["N"], c["h"], c["ratio"], c["hkv"], c["d"], c["dm"], seed=16000 + c["N"])
+    if c["strided"]:
+        t = _strided(t, ("q", "k", "v", "dout"), 16002 + c["N"])
     sc = c["scale"]
     ref, model = tgb._reference(t, c["ratio"], causal=c["causal"], scale=sc)
     tgb._compare(tgb._run_exact_saves(t, c["ratio"], ref, causal=c["causal"], scale=sc), ref, model, bar="bwd")
@@ -264,6 +298,8 @@ def test_sweep_v2_decode(c, gpu_ops):
     bd, tsm = gpu_ops["bd"], gpu_ops["tsm"]
     t = synth.decode_inputs(c["B"], c["L"], c["h"], c["hkv"], c["d"], c["dm"], seed=17000 + c["L"], device="cuda",
                             seqlens=c["seqlens"])
+    if c["strided"]:
+        t = _strided(t, ("k_cache", "v_cache"), 17002 + c["L"])
     out = bd.diffattn_v2_decode(t["q"], t["k_cache"], t["v_cache"], seqlens=t["seqlens"], x=t["x"],
                                 w_lambda=t["w_lambda"], num_splits=c["splits"], softmax_scale=_ss(c))
     torch.cuda.synchronize()
@@ -277,6 +313,8 @@ def test_sweep_v1_decode(c, gpu_ops):
     bd, tv1d = gpu_ops["bd"], gpu_ops["tv1d"]
     t = synth.v1_decode_inputs(c["B"], c["L"], c["H"], c["dqk"], c["dv"], seed=18000 + c["L"], device="cuda",
                                seqlens=c["seqlens"])
+    if c["strided"]:
+        t = _strided(t, ("k1_cache", "k2_cache", "v_cache"), 18002 + c["L"])
     li = bd.diffattn_lambda_init(c["layer"])
     w = _rms_weight(c["dv"], 18001) if c["weighted"] else None
     tv1d._check(t, li, tv1d._run(t, li, num_splits=c["splits"], rms_weight=w, softmax_scale=_ss(c),

@@ -14,11 +14,13 @@ import torch
 from differential_attention_diff_gb300 import binding as bd
 from differential_attention_diff_gb300 import synth
 from oracle import diffattn_oracle as orc
+from bf16_model import rounded_forward
 from ratio_log import record
 from sampling import tile_rows
 
 pytestmark = pytest.mark.gpu
 TOL = 2e-2
+RSTD_TOL = 2e-2
 NAMES = ("q1", "q2", "k1", "k2", "v", "lq1", "lk1", "lq2", "lk2")
 
 
@@ -36,28 +38,60 @@ def _status_clean():
     assert bd.diffattn_get_device_status() == bd.DA_OK
 
 
+def _forward_model(sl, lam_vectors, li, causal, w, scale, eps):
+    """The oracle forward and the forward rounding model (bf16 P as the P.V
+    operand, Y and O2 stored in bf16) on every row of one head."""
+    f = {n: sl(n) for n in NAMES[:5]}
+    wf = None if w is None else f64(w)
+    li = float(np.float32(li))
+    exact = orc.v1_forward(*(f[n] for n in NAMES[:5]), *lam_vectors, li, causal=causal, rms_weight=wf,
+                           scale=scale, eps=eps)
+    return exact, rounded_forward(f, exact, li, causal=causal, rms_weight=wf, eps=eps, scale=scale)
+
+
 def _check(t, li, y, sv, rows=None, heads=None, batches=None, causal=True, w=None, scale=None, eps=1e-5):
+    """Y and O2 within 2e-2 * RMS(V) per element, the LSEs within 1e-2, rstd
+    within 2e-2 relative.  A row of Y or rstd beyond its bar is held to 3
+    times the forward rounding model's own error on that row instead: where
+    O1 and lambda O2 nearly cancel (the first rows of a causal map see one or
+    two keys, and at lambda near 1 rstd reaches 30-300) the bf16 P.V operand
+    alone moves the normalised output past the bar.  The model runs only for
+    the heads that need it, and such rows are counted in the ratio log."""
     B, N, H, _ = t["q1"].shape
     heads = range(H) if heads is None else heads
     batches = range(B) if batches is None else batches
     yv = f64(y)
+    lam_vectors = [f64(t[n]) for n in NAMES[5:]]
     worst = 0.0
+    model_rows = 0
     for b in batches:
         for h in heads:
             sl = lambda n: f64(t[n][b:b + 1, :, h:h + 1])  # noqa: E731
             ref = orc.v1_forward(sl("q1"), sl("q2"), sl("k1"), sl("k2"), sl("v"),
-                                 *(f64(t[n]) for n in NAMES[5:]), float(np.float32(li)), rows=rows,
+                                 *lam_vectors, float(np.float32(li)), rows=rows,
                                  causal=causal, rms_weight=None if w is None else f64(w), scale=scale,
                                  eps=eps)
             r = ref["rows"]
             tol = TOL * rms(f64(t["v"][b, :, h]))
-            worst = max(worst, float(np.max(np.abs(yv[b, r, h] - ref["y"][0, :, 0]))) / tol)
+            ey = np.max(np.abs(yv[b, r, h] - ref["y"][0, :, 0]), axis=1)
+            rstd_rel = None
             if sv is not None:
                 worst = max(worst, float(np.max(np.abs(f64(sv["o2"][b, r, h]) - ref["o2"][0, :, 0]))) / tol)
                 assert np.max(np.abs(f64(sv["lse1"][b, h, r]) - ref["lse1"][0, 0])) <= 1e-2
                 assert np.max(np.abs(f64(sv["lse2"][b, h, r]) - ref["lse2"][0, 0])) <= 1e-2
-                assert np.max(np.abs(f64(sv["rstd"][b, h, r]) / ref["rstd"][0, 0] - 1)) <= 2e-2
-    record({"y_o2": worst})
+                rstd_rel = np.abs(f64(sv["rstd"][b, h, r]) / ref["rstd"][0, 0] - 1)
+            y_allowed = np.full_like(ey, tol)
+            rstd_allowed = np.full(len(r), RSTD_TOL)
+            if np.max(ey) > tol or (rstd_rel is not None and np.max(rstd_rel) > RSTD_TOL):
+                exact, model = _forward_model(sl, lam_vectors, li, causal, w, scale, eps)
+                my = np.max(np.abs(model["y"][0, r, 0] - exact["y"][0, r, 0]), axis=1)
+                y_allowed = np.maximum(tol, 3 * my)
+                rstd_allowed = np.maximum(RSTD_TOL, 3 * np.abs(model["rstd"][0, 0][r] / exact["rstd"][0, 0][r] - 1))
+                model_rows += int(np.sum(y_allowed > tol))
+            worst = max(worst, float(np.max(ey / y_allowed)))
+            if rstd_rel is not None:
+                assert np.all(rstd_rel <= rstd_allowed), float(np.max(rstd_rel / rstd_allowed))
+    record({"y_o2": worst, "rows_on_model_bar": model_rows})
     assert worst <= 1.0, worst
 
 
