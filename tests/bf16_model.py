@@ -198,3 +198,22 @@ def rounded_backward_grouped(f, fwd, gate, ratio, scale=None, rnd=bf16, causal=T
     for n in ("dq", "dk", "dv"):
         out[n] = rnd(out[n])
     return out
+
+
+def rounded_grouped_forward(q, k, v, gate, ratio, scale=None, causal=True, rnd=bf16):
+    """The grouped forward of one group with its bf16 storage points: each
+    head's P = exp(S - m) rounded as the P.V operand (the row sum from the
+    unrounded P), each head's normalised output stored rounded (the o_heads
+    save the combine reads), and out = O_signal - gate O_noise rounded.
+    q: [N, ratio + 1, d] (signal heads, then the noise head); k, v: [N, d];
+    gate: [N, ratio].  Returns out [N, ratio, d]; with rnd the identity it is
+    the oracle's grouped forward of the group."""
+    N, _, d = q.shape
+    s = 1.0 / np.sqrt(d) if scale is None else scale
+    keep = np.tril(np.ones((N, N), bool)) if causal else np.ones((N, N), bool)
+    heads = []
+    for j in range(ratio + 1):
+        S = np.where(keep, s * q[:, j] @ k.T, -np.inf)
+        P = np.exp(S - S.max(1, keepdims=True))
+        heads.append(rnd((rnd(P) @ v) / P.sum(1, keepdims=True)))
+    return rnd(np.stack([heads[i] - gate[:, i:i + 1] * heads[ratio] for i in range(ratio)], 1))

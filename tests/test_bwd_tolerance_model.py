@@ -19,7 +19,8 @@ import numpy as np
 import torch
 
 from differential_attention_diff_gb300 import synth
-from bf16_model import rounded_backward, rounded_backward_grouped, rounded_backward_v2, rounded_forward
+from bf16_model import (rounded_backward, rounded_backward_grouped, rounded_backward_v2, rounded_forward,
+                        rounded_grouped_forward)
 from oracle import diffattn_oracle as orc
 
 
@@ -141,3 +142,22 @@ def test_v1_rounding_model_is_the_chain_rule():
             np.testing.assert_allclose(exact[n], ref[n], rtol=0, atol=1e-12 * np.abs(ref[n]).max())
         assert abs(exact["dlam"] - ref["dlam"]) <= 1e-12 * abs(ref["dlam"])
         assert exact["dlam_ss"] == 0.0
+
+
+def test_grouped_forward_rounding_model_is_the_forward():
+    """The grouped forward model with its rounding switched off is the
+    oracle's grouped forward (causal or not, a non-default scale); with bf16
+    rounding it stays inside the 2e-2 * RMS(V) output bar on ordinary inputs."""
+    rng = np.random.default_rng(5250)
+    N, r, d = 60, 3, 64
+    q = rng.standard_normal((N, r + 1, d))
+    k = rng.standard_normal((N, d))
+    v = rng.standard_normal((N, d))
+    g = rng.uniform(0.0, 1.0, (N, r))
+    for causal in (True, False):
+        ref = orc.grouped_forward(q[None], k[None, :, None], v[None, :, None], g[None], r, causal=causal,
+                                  scale=0.1)["out"][0]
+        exact = rounded_grouped_forward(q, k, v, g, r, scale=0.1, causal=causal, rnd=lambda a: a)
+        np.testing.assert_allclose(exact, ref, rtol=0, atol=1e-12)
+        rounded = rounded_grouped_forward(q, k, v, g, r, scale=0.1, causal=causal)
+        assert np.max(np.abs(rounded - ref)) <= 2e-2 * np.sqrt(np.mean(v ** 2))

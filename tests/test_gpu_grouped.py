@@ -11,6 +11,7 @@ import torch
 from differential_attention_diff_gb300 import binding as bd
 from differential_attention_diff_gb300 import synth
 from oracle import diffattn_oracle as orc
+from bf16_model import rounded_grouped_forward
 from ratio_log import record
 from sampling import tile_rows
 
@@ -29,6 +30,13 @@ def _status_clean():
 
 
 def _check(t, ratio, out, rows=None, batches=None, groups=None, causal=True, scale=None):
+    """out within 2e-2 * RMS(V) per element.  A row beyond that is held to 3
+    times the grouped rounding model's own error on that row instead
+    (bf16_model.rounded_grouped_forward: bf16 P, the per-head outputs stored
+    in bf16 for the combine, the output rounded).  Those three storage points
+    in series can reach the bar at elements of 2-3 RMS(V) under a sharp
+    softmax.  The model runs only for groups that need it, and the ratio log
+    counts such rows."""
     B, N, Hq, d = t["q"].shape
     hkv = t["k"].shape[2]
     G = Hq // hkv
@@ -37,6 +45,7 @@ def _check(t, ratio, out, rows=None, batches=None, groups=None, causal=True, sca
     gate = orc.v2_gate(f64(t["x"]), f64(t["w_lambda"]))
     o = f64(out)
     worst = 0.0
+    model_rows = 0
     for b in batches:
         for g in groups:
             c = g * (ratio + 1) // G
@@ -45,9 +54,21 @@ def _check(t, ratio, out, rows=None, batches=None, groups=None, causal=True, sca
             ref = orc.grouped_forward(f64(t["q"][b:b + 1, :, qs]), f64(t["k"][b:b + 1, :, c:c + 1]),
                                       f64(t["v"][b:b + 1, :, c:c + 1]), gate[b:b + 1, :, ps], ratio, rows=rows,
                                       causal=causal, scale=scale)
+            r = ref["rows"]
             tol = TOL * float(np.sqrt(np.mean(f64(t["v"][b, :, c]) ** 2)))
-            worst = max(worst, float(np.max(np.abs(o[b, ref["rows"], ps] - ref["out"][0]))) / tol)
-    record({"out": worst})
+            err = np.max(np.abs(o[b, r, ps] - ref["out"][0]), axis=(1, 2))
+            allowed = np.full_like(err, tol)
+            if np.max(err) > tol:
+                exact = orc.grouped_forward(f64(t["q"][b:b + 1, :, qs]), f64(t["k"][b:b + 1, :, c:c + 1]),
+                                            f64(t["v"][b:b + 1, :, c:c + 1]), gate[b:b + 1, :, ps], ratio,
+                                            causal=causal, scale=scale)["out"][0]
+                model = rounded_grouped_forward(f64(t["q"][b, :, qs]), f64(t["k"][b, :, c]), f64(t["v"][b, :, c]),
+                                                gate[b, :, ps], ratio, scale=scale, causal=causal)
+                merr = np.max(np.abs(model[r] - exact[r]), axis=(1, 2))
+                allowed = np.maximum(tol, 3 * merr)
+                model_rows += int(np.sum(allowed > tol))
+            worst = max(worst, float(np.max(err / allowed)))
+    record({"out": worst, "rows_on_model_bar": model_rows})
     assert worst <= 1.0, worst
 
 
