@@ -140,6 +140,32 @@ def test_sweep_shapes_are_valid():
             assert any(c["causal"] for c in cases)
 
 
+def test_strided_views_hold_the_values_and_nan_around_them():
+    """The strided-view helper (CPU tensors here): each view equals its source,
+    its batch, row and head strides differ from a contiguous tensor's, it
+    starts 16-byte aligned with strides in whole 16-byte steps (what the
+    interface requires of bf16 tensors), and everything of its buffer outside
+    the view is NaN."""
+    g = torch.Generator().manual_seed(3)
+    t = {"a": torch.randn((2, 37, 3, 64), generator=g).to(torch.bfloat16),
+         "b": torch.randn((1, 5, 2, 128), generator=g).to(torch.bfloat16)}
+    for seed in range(20):
+        out = _strided(t, ("a", "b"), seed)
+        for n, x in t.items():
+            v = out[n]
+            assert torch.equal(v, x)
+            assert v.stride(3) == 1 and v.stride()[:3] != x.contiguous().stride()[:3]
+            assert v.data_ptr() % 16 == 0 and all((st * 2) % 16 == 0 for st in v.stride()[:3])
+            base = v.storage_offset()
+            buf = torch.empty(0, dtype=v.dtype).set_(v.untyped_storage())
+            mask = torch.ones(buf.numel(), dtype=torch.bool)
+            idx = torch.arange(v.numel()).view(v.shape)
+            flat = (base + sum(idx.new_tensor(list(range(sz))).view([-1 if i == d else 1 for i in range(4)]) * st
+                               for d, (sz, st) in enumerate(zip(v.shape, v.stride())))).reshape(-1)
+            mask[flat] = False
+            assert torch.isnan(buf[mask].float()).all()
+
+
 # ------------------------------------------------------------------- GPU ----
 
 @pytest.fixture
